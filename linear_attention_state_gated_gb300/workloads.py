@@ -1,0 +1,198 @@
+"""Seeded synthetic inputs for the segment scan and composition workloads.
+
+This module holds no arithmetic of the method itself: it only draws random
+numbers (numpy PCG64, seeded), shapes them, L2-normalises key/query rows where
+a workload asks for it and rounds to bf16 (round-to-nearest-even) where the
+workload's inputs are bf16.  Both the CUDA path and the fp64 oracle are fed
+from here; every bf16 input is also returned as the float32 array of the
+exact bf16 values, so the oracle sees precisely what the GPU sees.
+
+Workloads (sizes as named in the HYPIC evaluation set-up; the pages run a
+production RAG trace and public QA/summarisation sets, for which these seeded
+draws stand in):
+
+* ``tiny_dense``      -- gated delta rule, fp32, 1 layer, 2 heads, d=32,
+                         two 64-token segments, alpha~U(0.9,1), beta~U(0,1).
+* ``scalar_diag``     -- 32 heads, d=128, bf16 q/k/v, batch of equal segments;
+                         scalar gate gamma_h = 1 - 2^(-5 - 6h/32) for every
+                         token, or diagonal gate sigmoid(N(2,1))^(1/16).
+* ``dense_stack``     -- gated delta rule on a 30-layer x 32-head x 128 stack,
+                         bf16 q, v ~ N(0,1), k L2-normalised,
+                         alpha = exp(-0.1 softplus(N(0,1))), beta = sigmoid(N(0,1)).
+* ``rag_pool`` / ``rag_requests`` -- a pool of cached (lambda, S) pairs and
+                         requests drawing distinct pool entries by truncated
+                         Zipf(1.1) weights in random order.
+* ``long_mix``        -- one long prompt split into equal segments, some
+                         cached and some not, gated delta rule.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+SCALAR, DIAG, DENSE = 0, 1, 2
+
+
+def rng(seed: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(seed))
+
+
+def bf16_round(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to the nearest bf16 (ties to even); float32 result."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    u = x.view(np.uint32)
+    lsb = (u >> np.uint32(16)) & np.uint32(1)
+    r = (u + np.uint32(0x7FFF) + lsb) & np.uint32(0xFFFF0000)
+    out = r.view(np.float32)
+    nan = np.isnan(x)
+    if nan.any():
+        out = out.copy()
+        out[nan] = np.nan
+    return out
+
+
+def bf16_bits(x: np.ndarray) -> np.ndarray:
+    """uint16 bit patterns of float32 values that are already bf16-exact."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    return (x.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+def _normal(g, shape):
+    return g.standard_normal(size=shape, dtype=np.float32)
+
+
+def _l2_rows(x):
+    n = np.sqrt(np.sum(x.astype(np.float64) ** 2, axis=-1, keepdims=True))
+    n[n == 0] = 1.0
+    return (x / n).astype(np.float32)
+
+
+def _sigmoid(x):
+    return (1.0 / (1.0 + np.exp(-x.astype(np.float64)))).astype(np.float32)
+
+
+def _softplus(x):
+    x = x.astype(np.float64)
+    return np.where(x > 20, x, np.log1p(np.exp(np.minimum(x, 20))))
+
+
+def equal_offsets(n_seg: int, length: int) -> np.ndarray:
+    return np.arange(n_seg + 1, dtype=np.int64) * length
+
+
+def tiny_dense(seed: int = 0, n_seg: int = 2, seg_len: int = 64, H: int = 2, d: int = 32):
+    """Gated delta rule, fp32 inputs: k, q L2-normalised N(0,1), v N(0,1)."""
+    g = rng(seed)
+    N = n_seg * seg_len
+    k = _l2_rows(_normal(g, (1, N, H, d)))
+    q = _l2_rows(_normal(g, (1, N, H, d)))
+    v = _normal(g, (1, N, H, d))
+    alpha = g.uniform(0.9, 1.0, size=(1, N, H)).astype(np.float32)
+    beta = g.uniform(0.0, 1.0, size=(1, N, H)).astype(np.float32)
+    return dict(family=DENSE, dtype="f32", q=q, k=k, v=v, alpha=alpha, beta=beta,
+                seg_offsets=equal_offsets(n_seg, seg_len))
+
+
+def retnet_gamma(H: int) -> np.ndarray:
+    """Per-head fixed decay gamma_h = 1 - 2^(-5 - 6h/H) (RetNet-style heads)."""
+    h = np.arange(H, dtype=np.float64)
+    return (1.0 - np.exp2(-5.0 - 6.0 * h / H)).astype(np.float32)
+
+
+def scalar_diag(family: int, seg_len: int, n_seg: int = 8, H: int = 32, d: int = 128,
+                seed: int = 1, with_q: bool = False, n_layers: int = 1,
+                lengths=None):
+    """Scalar (fixed gamma_h per head) or diagonal (per-channel GLA gate) workload.
+
+    k, q: L2-normalised N(0,1) rows, v ~ N(0,1); all bf16.  No beta.
+    ``lengths`` overrides the equal segment lengths (ragged batches).
+    """
+    g = rng(seed)
+    if lengths is None:
+        lengths = [seg_len] * n_seg
+    offs = np.concatenate([[0], np.cumsum(np.asarray(lengths, dtype=np.int64))]).astype(np.int64)
+    N = int(offs[-1])
+    k = bf16_round(_l2_rows(_normal(g, (n_layers, N, H, d))))
+    v = bf16_round(_normal(g, (n_layers, N, H, d)))
+    q = bf16_round(_l2_rows(_normal(g, (n_layers, N, H, d)))) if with_q else None
+    if family == SCALAR:
+        alpha = np.broadcast_to(retnet_gamma(H)[None, None, :], (n_layers, N, H)).copy()
+    elif family == DIAG:
+        alpha = _sigmoid(g.normal(2.0, 1.0, size=(n_layers, N, H, d))) ** np.float32(1.0 / 16.0)
+        alpha = alpha.astype(np.float32)
+    else:
+        raise ValueError("scalar_diag: family must be SCALAR or DIAG")
+    return dict(family=family, dtype="bf16", q=q, k=k, v=v, alpha=alpha, beta=None,
+                seg_offsets=offs)
+
+
+def dense_stack(seg_len: int, n_layers: int = 30, H: int = 32, d: int = 128, seed: int = 2,
+                with_q: bool = False, n_seg: int = 1, lengths=None):
+    """Gated delta rule: bf16 q, v ~ N(0,1), k L2-normalised; fp32 alpha, beta."""
+    g = rng(seed)
+    if lengths is None:
+        lengths = [seg_len] * n_seg
+    offs = np.concatenate([[0], np.cumsum(np.asarray(lengths, dtype=np.int64))]).astype(np.int64)
+    N = int(offs[-1])
+    k = bf16_round(_l2_rows(_normal(g, (n_layers, N, H, d))))
+    v = bf16_round(_normal(g, (n_layers, N, H, d)))
+    q = bf16_round(_normal(g, (n_layers, N, H, d))) if with_q else None
+    alpha = np.exp(-0.1 * _softplus(_normal(g, (n_layers, N, H)))).astype(np.float32)
+    beta = _sigmoid(_normal(g, (n_layers, N, H)))
+    return dict(family=DENSE, dtype="bf16", q=q, k=k, v=v, alpha=alpha, beta=beta,
+                seg_offsets=offs)
+
+
+def rag_pool(family: int, P: int = 200, n_layers: int = 30, H: int = 32, d: int = 128,
+             seed: int = 3, len_lo: int = 1024, len_hi: int = 4096):
+    """Pool of P cached segment pairs (lambda, S) with segment lengths ~ U{len_lo..len_hi}.
+
+    Stands in for scanned pool segments: lambda is drawn per (entry, layer, head)
+    with the magnitude a segment of that length has under the scalar/diagonal
+    gates of ``scalar_diag`` (lengths x a per-head or per-channel rate), S is
+    drawn N(0, 1/d) per entry.  Dense pools also get a transition factor M
+    drawn N(0,1/d) and a scalar lambda.  All fp32.
+    """
+    g = rng(seed)
+    lengths = g.integers(len_lo, len_hi + 1, size=P).astype(np.int64)
+    if family == SCALAR:
+        rate = np.exp2(-5.0 - 6.0 * np.arange(H) / H)
+        lam = -(lengths[:, None, None] * rate[None, None, :]) * g.uniform(
+            0.95, 1.05, size=(P, n_layers, H))
+    elif family == DIAG:
+        lam = -lengths[:, None, None, None] * g.uniform(0.005, 0.02, size=(P, n_layers, H, d))
+    else:
+        lam = -lengths[:, None, None] * g.uniform(0.05, 0.1, size=(P, n_layers, H))
+    S = _normal(g, (P, n_layers, H, d, d)) * np.float32(1.0 / np.sqrt(d))
+    out = dict(family=family, lengths=lengths, lam=lam.astype(np.float32), S=S)
+    if family == DENSE:
+        out["M"] = _normal(g, (P, n_layers, H, d, d)) * np.float32(1.0 / np.sqrt(d))
+    return out
+
+
+def rag_requests(R: int = 64, n: int = 20, P: int = 200, zipf_s: float = 1.1, seed: int = 3):
+    """R requests, each n distinct pool indices drawn by truncated Zipf(s) weights.
+
+    Ranks i = 1..P carry weight i^-s over a seeded permutation of the pool;
+    the prompt order is the draw order.
+    """
+    g = rng(seed + 1000)
+    perm = g.permutation(P)
+    w = np.arange(1, P + 1, dtype=np.float64) ** (-zipf_s)
+    idx = np.zeros((R, n), dtype=np.int32)
+    for r in range(R):
+        ranks = g.choice(P, size=n, replace=False, p=w / w.sum())
+        idx[r] = perm[ranks]
+    return np.full(R, n, dtype=np.int32), idx
+
+
+def long_mix(n_seg: int = 64, seg_len: int = 2048, n_uncached: int = 16, n_layers: int = 30,
+             H: int = 32, d: int = 128, seed: int = 4):
+    """A long prompt of n_seg equal segments (dense gate law of ``dense_stack``).
+
+    Returns the full-prompt inputs plus which segments are uncached (a seeded
+    choice of n_uncached); the others are cached.
+    """
+    w = dense_stack(seg_len, n_layers=n_layers, H=H, d=d, seed=seed, with_q=True, n_seg=n_seg)
+    g = rng(seed + 1000)
+    w["uncached"] = np.sort(g.permutation(n_seg)[:n_uncached]).astype(np.int64)
+    return w
