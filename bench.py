@@ -1,0 +1,470 @@
+#!/usr/bin/env python3
+"""Benchmark of the HYPIC linear-attention hot path on GB300.
+
+Headline workload (one "step"): a batch of 8 independently prefilled segments
+of L = 8192 tokens, 32 heads, d_k = d_v = 128, bf16 k/v with fp32 state,
+scanned once with the scalar (RetNet-style fixed gamma_h) gate and once with
+the diagonal (GLA-style per-channel) gate: per segment and head the
+transition operator T_C and the zero-start state S(C|0).  Metric: segment
+tokens per second (each family's batch counts its B x L tokens).
+
+Extra rows in the same JSON line (own units and rooflines):
+  dense_scan -- gated delta rule on a 30-layer x 32-head x 128 stack, one
+                segment per layer;
+  rag_chain  -- composes/s: 64 requests x 20 cached segments (Zipf(1.1) from a
+                pool of 200) folded in order through 30 layers x 32 heads.
+
+Timing: CUDA events on the launching stream, warm-up first, inputs resident
+in HBM and larger than L2; ``e2e`` repeats the headline step from pinned host
+buffers with the copies inside the timed region.  ``--impl reference`` times
+the fp64 oracle on host cores instead (bounded sample, same metric).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+MEASURED = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
+
+
+# ------------------------------------------------------------------ helpers
+
+def peaks():
+    try:
+        with open(MEASURED) as f:
+            m = json.load(f)
+        return float(m["hbm_gbs"]), float(m["bf16_tflops"]), float(m.get("bf16_tflops_sustained", m["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = [r.split(",") for r in open(self.path).read().strip().splitlines() if r.strip()]
+        os.unlink(self.path)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def dist_setup(n_gpus):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ workloads
+
+HEAD = dict(B=8, H=32, d=128)
+
+
+def headline_inputs(L, seed=1):
+    from linear_attention_state_gated_gb300 import workloads as wl
+    return {fam: wl.scalar_diag(fam, seg_len=L, n_seg=HEAD["B"], H=HEAD["H"], d=HEAD["d"], seed=seed)
+            for fam in (wl.SCALAR, wl.DIAG)}
+
+
+def pinned(x, bf16=False):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(x))
+    if bf16:
+        t = t.to(torch.bfloat16)
+    return t.pin_memory()
+
+
+def scan_bytes(fam, n_tok_heads, n_units, d=128, in_bytes=2):
+    """Algorithmic HBM bytes of one scan launch: read k, v (and the gate) once,
+    write lambda and S(C|0) (and M for dense) once per (layer, segment, head)."""
+    gate = 4 * d if fam == 1 else 4
+    beta = 4 if fam == 2 else 0
+    per_tok = 2 * d * in_bytes + gate + beta
+    per_unit = 4 * d * d + (4 * d if fam == 1 else 4) + (4 * d * d if fam == 2 else 0)
+    return n_tok_heads * per_tok + n_units * per_unit
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_headline(args, rank, world):
+    import torch
+    import linear_attention_state_gated_gb300 as hy
+
+    L = args.L
+    B, H, d = HEAD["B"], HEAD["H"], HEAD["d"]
+    inp = headline_inputs(L, seed=1 + rank)
+    dev = torch.device("cuda")
+    host, devt, outs = {}, {}, {}
+    for fam, w in inp.items():
+        host[fam] = {"k": pinned(w["k"], True), "v": pinned(w["v"], True),
+                     "alpha": pinned(w["alpha"]), "offs": pinned(w["seg_offsets"])}
+        devt[fam] = {key: t.to(dev, non_blocking=False) for key, t in host[fam].items()}
+        n_seg = B
+        lam_shape = (1, n_seg, H, d) if fam == 1 else (1, n_seg, H)
+        outs[fam] = {"lam": torch.empty(lam_shape, dtype=torch.float32, device=dev),
+                     "S": torch.empty((1, n_seg, H, d, d), dtype=torch.float32, device=dev)}
+    torch.cuda.synchronize()
+
+    def step(events=None):
+        for fam in (0, 1):
+            t = devt[fam]
+            if events is not None:
+                events[fam][0].record()
+            hy.segment_scan(fam, t["k"], t["v"], t["alpha"], t["offs"], out=outs[fam])
+            if events is not None:
+                events[fam][1].record()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+
+    clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")) if world > 1 else 0)
+    if rank == 0:
+        clocks.start()
+    per_kernel = {0: [], 1: []}
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)] for _ in range(2)]
+    barrier(world)
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for i in range(args.steps):
+        step(events={0: ev[0][i], 1: ev[1][i]})
+    stop.record()
+    torch.cuda.synchronize()
+    elapsed = start.elapsed_time(stop) / 1e3
+    barrier(world)
+    clk = clocks.stop() if rank == 0 else None
+    for fam in (0, 1):
+        per_kernel[fam] = [a.elapsed_time(b) / 1e3 for a, b in ev[fam]]
+    t_max = max_over_ranks(elapsed, world)
+    tokens_per_step = 2 * B * L
+    value = tokens_per_step * args.steps * world / t_max
+
+    # end to end: pinned host inputs -> device -> scan -> host results, every step
+    e2e_steps = max(3, min(args.steps, 10))
+    res_host = {fam: {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+                      for k, v in outs[fam].items()} for fam in (0, 1)}
+    h2d = sum(t.numel() * t.element_size() for fam in (0, 1) for t in host[fam].values())
+    d2h = sum(t.numel() * t.element_size() for fam in (0, 1) for t in res_host[fam].values())
+
+    def e2e_step():
+        for fam in (0, 1):
+            for key in devt[fam]:
+                devt[fam][key].copy_(host[fam][key], non_blocking=True)
+            hy.segment_scan(fam, devt[fam]["k"], devt[fam]["v"], devt[fam]["alpha"],
+                            devt[fam]["offs"], out=outs[fam])
+            for key in outs[fam]:
+                res_host[fam][key].copy_(outs[fam][key], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2.record()
+    torch.cuda.synchronize()
+    e2e_t = max_over_ranks(s2.elapsed_time(e2) / 1e3, world)
+    e2e_value = tokens_per_step * e2e_steps * world / e2e_t
+
+    hbm, bf16, bf16_sus, src = peaks()
+    n_tok_heads = B * L * H
+    kern = {}
+    for fam in (0, 1):
+        avg = sum(per_kernel[fam]) / len(per_kernel[fam])
+        by = scan_bytes(fam, n_tok_heads, B * H, d)
+        kern[fam] = dict(avg_s=avg, bytes=by, gbs=by / avg / 1e9)
+    dom = max((0, 1), key=lambda f: kern[f]["avg_s"])
+    return dict(value=value, elapsed=t_max, clocks=clk, kern=kern, dom=dom,
+                e2e=dict(value=e2e_value, unit="tokens/s", h2d_bytes_per_step=h2d,
+                         d2h_bytes_per_step=d2h, steps=e2e_steps),
+                hbm=hbm, src=src)
+
+
+def run_dense(args, L):
+    import torch
+    import linear_attention_state_gated_gb300 as hy
+    from linear_attention_state_gated_gb300 import workloads as wl
+    Lyr, H, d = 30, 32, 128
+    w = wl.dense_stack(seg_len=L, n_layers=Lyr, H=H, d=d, seed=2)
+    dev = torch.device("cuda")
+    k = torch.from_numpy(w["k"]).to(torch.bfloat16).to(dev)
+    v = torch.from_numpy(w["v"]).to(torch.bfloat16).to(dev)
+    a = torch.from_numpy(w["alpha"]).to(dev)
+    b = torch.from_numpy(w["beta"]).to(dev)
+    offs = torch.from_numpy(w["seg_offsets"]).to(dev)
+    out = {"lam": torch.empty((Lyr, 1, H), dtype=torch.float32, device=dev),
+           "S": torch.empty((Lyr, 1, H, d, d), dtype=torch.float32, device=dev),
+           "M": torch.empty((Lyr, 1, H, d, d), dtype=torch.float32, device=dev)}
+    del w
+    for _ in range(2):
+        hy.segment_scan(2, k, v, a, offs, beta=b, out=out)
+    torch.cuda.synchronize()
+    reps = 3
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for s, e in evs:
+        s.record()
+        hy.segment_scan(2, k, v, a, offs, beta=b, out=out)
+        e.record()
+    torch.cuda.synchronize()
+    t = sum(s.elapsed_time(e) for s, e in evs) / reps / 1e3
+    tok_heads = Lyr * L * H
+    flops = tok_heads * 180e3       # algorithmic flops per token-head of the chunked form, C = 64
+    _, bf16, bf16_sus, src = peaks()
+    return {"workload": f"gated delta rule, {Lyr} layers x {H} heads x {d}, one segment of {L} tokens per layer",
+            "value": L / t, "unit": "tokens/s (all 30 layers)", "head_tokens_per_s": tok_heads / t,
+            "ms": t * 1e3,
+            "roofline": {"bound": "tensor", "achieved": flops / t / 1e12, "peak": bf16,
+                         "unit": "TFLOP/s", "frac": flops / t / 1e12 / bf16, "traffic": None,
+                         "peak_kind": f"bf16 burst, {src}"}}
+
+
+def run_chain(args):
+    import torch
+    import linear_attention_state_gated_gb300 as hy
+    from linear_attention_state_gated_gb300 import workloads as wl
+    res = {}
+    hbm, _, _, src = peaks()
+    clen, idx = wl.rag_requests()
+    dev = torch.device("cuda")
+    cl, ix = torch.from_numpy(clen).to(dev), torch.from_numpy(idx).to(dev)
+    for fam, name in ((0, "scalar"), (1, "diag")):
+        pool = wl.rag_pool(fam)
+        pl = torch.from_numpy(pool["lam"]).to(dev)
+        pS = torch.from_numpy(pool["S"]).to(dev)
+        del pool
+        R, Lyr, H, d = 64, 30, 32, 128
+        out = torch.empty((R, Lyr, H, d, d), dtype=torch.float32, device=dev)
+        for _ in range(3):
+            hy.compose_chain(fam, cl, ix, pl, pS, S_out=out)
+        torch.cuda.synchronize()
+        reps = 5
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(reps):
+            hy.compose_chain(fam, cl, ix, pl, pS, S_out=out)
+        e.record()
+        torch.cuda.synchronize()
+        t = s.elapsed_time(e) / reps / 1e3
+        n_steps = int(clen.sum())
+        composes = n_steps * Lyr                       # (request, segment, layer) triples
+        lam_b = 4 * d if fam == 1 else 4
+        by = n_steps * Lyr * H * (4 * d * d + lam_b) + R * Lyr * H * 4 * d * d
+        res[name] = {"value": composes / t, "unit": "composes/s (all 32 heads)", "ms": t * 1e3,
+                     "roofline": {"bound": "hbm", "achieved": by / t / 1e9, "peak": hbm,
+                                  "unit": "GB/s", "frac": by / t / 1e9 / hbm, "traffic": None,
+                                  "peak_kind": f"copy, {src}"}}
+        del pl, pS, out
+        torch.cuda.empty_cache()
+    return res
+
+
+# ------------------------------------------------------------------ oracle (CPU)
+
+_SAMPLE_CACHE = {}
+
+
+def oracle_sample_rate(L, families=(0, 1), seg_tokens=512, heads=(0, 4, 8, 12, 16, 20, 24, 28)):
+    """Time the fp64 oracle on a bounded sample of the headline workload: every
+    segment's first `seg_tokens` tokens for a subset of heads, both gates.
+    Returns (tokens/s in the headline unit, seconds, threads, description)."""
+    import oracle
+    if L not in _SAMPLE_CACHE:
+        _SAMPLE_CACHE[L] = headline_inputs(L, seed=1)
+    inp = _SAMPLE_CACHE[L]
+    hs = list(heads)
+    tok_heads = 0
+    t_total = 0.0
+    for fam in families:
+        w = inp[fam]
+        offs = w["seg_offsets"]
+        idx = np.concatenate([np.arange(offs[s], offs[s] + seg_tokens) for s in range(len(offs) - 1)])
+        k = np.ascontiguousarray(w["k"][:, idx][:, :, hs])
+        v = np.ascontiguousarray(w["v"][:, idx][:, :, hs])
+        a = np.ascontiguousarray(w["alpha"][:, idx][:, :, hs])
+        so = np.arange(len(offs), dtype=np.int64) * seg_tokens
+        t0 = time.perf_counter()
+        oracle.segment_scan(fam, k, v, a, so)
+        t_total += time.perf_counter() - t0
+        tok_heads += len(idx) * len(hs)
+    # a token counts once all 32 heads have passed
+    rate = tok_heads / HEAD["H"] / t_total
+    desc = (f"fp64 oracle, {len(families)} gates x {HEAD['B']} segments x first {seg_tokens} tokens "
+            f"x {len(hs)} of {HEAD['H']} heads; tokens/s = token-heads/s / {HEAD['H']}")
+    return rate, t_total, oracle.max_threads(), desc
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    rates, times = [], []
+    for i in range(args.warmup + args.steps):
+        rate, t, cores, desc = oracle_sample_rate(args.L, seg_tokens=256)
+        if i >= args.warmup:
+            rates.append(rate)
+            times.append(t)
+    value = statistics.median(rates)
+    line = {"impl": "reference", "metric": "segment-scan tokens/s (T_C+S_C)", "value": value,
+            "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * statistics.median(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": headline_config(args.L),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def headline_config(L):
+    return {"workload": (f"scalar (RetNet gamma_h) + diagonal (GLA) segment scan, batch "
+                         f"{HEAD['B']} x {L} tokens, {HEAD['H']} heads, d_k=d_v={HEAD['d']}, "
+                         "bf16 k/v, fp32 state"),
+            "global_batch": HEAD["B"], "seq_len": L, "parallelism": "replicas",
+            "l2": "inputs (>= 1 GB per step) exceed the 129 MB L2; no flush"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="hypic", choices=["hypic", "reference"])
+    ap.add_argument("--L", type=int, default=8192)
+    ap.add_argument("--rows", default="dense,chain", help="extra rows: dense,chain or none")
+    ap.add_argument("--dense-L", type=int, default=2048)
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    import linear_attention_state_gated_gb300 as hy
+    hy.library()   # raises if the CUDA library is missing: no fallback
+    rank, world, local = dist_setup(args.gpus)
+    h = run_headline(args, rank, world)
+    rows = {}
+    if rank == 0 and "dense" in args.rows:
+        rows["dense_scan"] = run_dense(args, args.dense_L)
+    if rank == 0 and "chain" in args.rows:
+        rows["rag_chain"] = run_chain(args)
+    if rank != 0:
+        barrier(world)
+        return
+    cpu = None
+    if not args.no_cpu:
+        rate, t, cores, desc = oracle_sample_rate(args.L)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc,
+               "seconds": round(t, 2)}
+    kd = h["kern"][h["dom"]]
+    fam_name = {0: "scalar", 1: "diag"}
+    line = {
+        "metric": "segment-scan tokens/s (T_C+S_C)", "value": h["value"], "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * h["elapsed"] / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": headline_config(args.L),
+        "roofline": {"bound": "hbm", "achieved": kd["gbs"], "peak": h["hbm"], "unit": "GB/s",
+                     "frac": kd["gbs"] / h["hbm"], "traffic": None,
+                     "kernel": f"segment scan, {fam_name[h['dom']]} gate",
+                     "algorithmic_bytes": kd["bytes"], "avg_launch_ms": kd["avg_s"] * 1e3,
+                     "peak_kind": f"HBM copy, {h['src']}"},
+        "kernels": {fam_name[f]: {"avg_launch_ms": h["kern"][f]["avg_s"] * 1e3,
+                                  "GB/s": h["kern"][f]["gbs"]} for f in (0, 1)},
+        "cpu_baseline": cpu, "e2e": h["e2e"], "clocks": h["clocks"],
+        "gpu_launches": 2 * args.steps, "rows": rows,
+    }
+    barrier(world)
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,157 @@
+/*
+ * hypic.h -- C ABI of the GB300 segment-scan and state-composition library
+ * for position-independent caching (HYPIC) of hybrid linear-attention models.
+ *
+ * What the operations are (web pages about HYPIC):
+ *   xix.ai/fr, "Xiaohongshu, l'Université de Pékin et l'Université Jiao Tong de
+ *   Shanghai dévoilent HYPIC ...", paragraph on linear layers ("opérateurs de
+ *   transition"): each segment C is prefilled once from a zero state; the cache
+ *   keeps the pair (T_C, S(C|0)), T_C being the product of every per-token
+ *   transition matrix of the segment; at reuse the running state is
+ *   left-multiplied by T_C and S(C|0) is added:  S(C1.C2) = T(C2) S(C1) + S(C2).
+ *   remio.ai/ja, "HYPIC ...", section "how HYPIC composes states": the
+ *   composition costs the same whatever the segment length; section "cold
+ *   requests become parallel": a combine step folds the pairs of many segments
+ *   into the request's running state.
+ *
+ * The pages print no per-token rule.  This library reads the three families
+ * named there as (state S in R^{dk x dv}, fp32):
+ *   S_t = T_t S_{t-1} + beta_t k_t v_t^T,  o_t = S_t^T q_t  (state after token t)
+ *     HYPIC_SCALAR : T_t = alpha_t I                       (RetNet, Mamba2)
+ *     HYPIC_DIAG   : T_t = diag(alpha_t), alpha_t in R^dk  (GLA; gates the key axis)
+ *     HYPIC_DENSE  : T_t = alpha_t (I - beta_t k_t k_t^T)  (gated delta rule)
+ *   T_C = T_L ... T_1,  S(C|0) = S_L from S_0 = 0.
+ * T_C is stored in log-scaled form T_C = exp(lambda) * M, because the plain
+ * product underflows fp32 (and fp64) at the segment lengths of long prompts:
+ *   scalar: lambda [.., H] = sum_t log alpha_t;              M is 1 (not stored)
+ *   diag  : lambda [.., H, dk] = sum_t log alpha_{t,i};      M is I (not stored)
+ *   dense : lambda [.., H], M [.., H, dk, dk] with max|M| in [1, 2)
+ *           (M == 0 exactly only for a product that is exactly zero).
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     allocates no memory and keeps no state between calls.  Every call is
+ *     asynchronous on `cuda_stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and safe to issue from several host threads.
+ *   - Layouts are dense row-major, innermost index last.
+ *   - Arguments are checked on the host before any launch; a bad argument
+ *     returns a negative hypic_status and launches nothing.  A launch failure
+ *     returns HYPIC_ECUDA.  Device-side problems (pool index out of range,
+ *     segment offsets not ascending within [0, total_tokens]) never trap: the
+ *     offending index is clamped or the segment treated as empty, and
+ *     HYPIC_EINDEX is written to `d_err` when `d_err` is non-NULL (a device
+ *     int the caller zeroes and reads after synchronising).
+ *   - Supported head sizes: dk, dv in {32, 64, 128}.
+ *   - Every gate alpha must be finite and > 0.
+ */
+#ifndef HYPIC_H
+#define HYPIC_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    HYPIC_OK = 0,
+    HYPIC_EINVAL = -1,       /* bad count, null required pointer, inconsistent options */
+    HYPIC_EUNSUPPORTED = -2, /* head size or family/dtype combination not built */
+    HYPIC_EALIGN = -3,       /* a pointer is not aligned as documented */
+    HYPIC_ECUDA = -4,        /* a CUDA runtime call or kernel launch failed */
+    HYPIC_EINDEX = -5        /* device side: index out of range (written to d_err) */
+} hypic_status;
+
+typedef enum { HYPIC_SCALAR = 0, HYPIC_DIAG = 1, HYPIC_DENSE = 2 } hypic_family;
+
+typedef enum { HYPIC_BF16 = 0, HYPIC_F32 = 1 } hypic_dtype;
+
+/*
+ * hypic_segment_scan -- per segment C and head: (T_C, S(C|0)) and optionally
+ * the per-token outputs o_t.  (xix.ai/fr, linear-layer paragraph: the pair is
+ * built at the segment's first prefill from a zero state and depends only on
+ * the segment's own tokens.)
+ *
+ * Segments are packed along the token axis and shared by all layers:
+ * segment s of every layer covers tokens [seg_offsets[s], seg_offsets[s+1]).
+ *   fam, in_dtype      family; element type of q, k, v and o_out
+ *   n_layers, n_seg, total_tokens (N), n_heads (H), d_k, d_v   sizes
+ *   seg_offsets        int64 [n_seg + 1], ascending, 0 .. N        (device)
+ *   q                  [n_layers, N, H, d_k]; required iff o_out != NULL
+ *   k                  [n_layers, N, H, d_k]
+ *   v                  [n_layers, N, H, d_v]
+ *   alpha   fp32       [n_layers, N, H] (scalar, dense) or [n_layers, N, H, d_k] (diag)
+ *   beta    fp32       [n_layers, N, H] or NULL (=> 1 for every token)
+ *   lam_out fp32       [n_layers, n_seg, H] or [n_layers, n_seg, H, d_k] (diag)
+ *   M_out   fp32       [n_layers, n_seg, H, d_k, d_k]; dense: required; else must be NULL
+ *   S_out   fp32       [n_layers, n_seg, H, d_k, d_v]
+ *   o_out   in_dtype   [n_layers, N, H, d_v] or NULL; o_t = S_t^T q_t
+ *   d_err              device int or NULL (see conventions)
+ * An empty segment yields lambda = 0, M = I, S = 0.
+ * Alignment: q, k, v, o_out, S_out, M_out and the diag alpha / lambda must be
+ * 16-byte aligned; other pointers 4-byte (seg_offsets 8-byte).
+ */
+int hypic_segment_scan(int fam, int in_dtype, int n_layers, int n_seg,
+                       int64_t total_tokens, int n_heads, int d_k, int d_v,
+                       const int64_t *seg_offsets, const void *q, const void *k,
+                       const void *v, const float *alpha, const float *beta,
+                       float *lam_out, float *M_out, float *S_out, void *o_out,
+                       int *d_err, void *cuda_stream);
+
+/*
+ * hypic_compose -- S = T_C S_prev + S_C for n items x H heads, with
+ * T_C = exp(lambda) M.  (xix.ai/fr, linear-layer paragraph:
+ * S(C1.C2) = T(C2) S(C1) + S(C2); left-multiplication by the cached T then an
+ * addition.)  Optionally also the operator of the concatenation,
+ * T(C1.C2) = T(C2) T(C1), which makes compositions chainable in any grouping.
+ *   lam     fp32  [n, H] (scalar, dense) or [n, H, d_k] (diag)   -- T(C2)
+ *   M       fp32  [n, H, d_k, d_k] (dense; must be NULL otherwise)
+ *   S_prev  fp32  [n, H, d_k, d_v] or NULL (=> 0)                 -- S(C1)
+ *   S_C     fp32  [n, H, d_k, d_v]                                -- S(C2)
+ *   S_out   fp32  [n, H, d_k, d_v]; may be the same pointer as S_prev
+ *                 (scalar, diag and dense); must not overlap S_C otherwise
+ *   lam_prev, lam_out  like lam; both NULL or both given          -- T(C1), T(C1.C2)
+ *   M_prev, M_out      like M (dense; given iff lam_out is)
+ * Dense M_out has max|M_out| in [1, 2) (exact power-of-two scaling into lam_out).
+ * All pointers 16-byte aligned except scalar/dense lambdas (4-byte).
+ */
+int hypic_compose(int fam, int n, int n_heads, int d_k, int d_v, const float *lam,
+                  const float *M, const float *S_prev, const float *S_C, float *S_out,
+                  const float *lam_prev, const float *M_prev, float *lam_out,
+                  float *M_out, void *cuda_stream);
+
+/*
+ * hypic_compose_chain -- the combine step: for every request r, layer l and
+ * head h, starting from S_init (or 0), fold the cached pairs of the pool
+ * entries seg_idx[r, 0 .. chain_len[r]-1] in that order:
+ *   S <- T_p S + S_p
+ * and write the final state once.  (xix.ai/fr: reuse under any prefix;
+ * remio.ai/ja, "cold requests become parallel": the combine worker folds each
+ * segment's transition and state into the running state.)
+ *   chain_len  int32 [n_req]            0 <= chain_len[r] <= max_chain
+ *   seg_idx    int32 [n_req, max_chain] pool indices in prompt order
+ *   pool_lam   fp32  [pool_size, n_layers, H] or [pool_size, n_layers, H, d_k] (diag)
+ *   pool_M     fp32  [pool_size, n_layers, H, d_k, d_k] (dense; NULL otherwise)
+ *   pool_S     fp32  [pool_size, n_layers, H, d_k, d_v]
+ *   S_init     fp32  [n_req, n_layers, H, d_k, d_v] or NULL (=> 0)
+ *   S_out      fp32  [n_req, n_layers, H, d_k, d_v]; may alias S_init
+ *   d_err      device int or NULL: an index outside [0, pool_size) or a
+ *              chain length outside [0, max_chain] is clamped and reported.
+ */
+int hypic_compose_chain(int fam, int n_req, int n_layers, int n_heads, int d_k, int d_v,
+                        int max_chain, const int32_t *chain_len, const int32_t *seg_idx,
+                        int pool_size, const float *pool_lam, const float *pool_M,
+                        const float *pool_S, const float *S_init, float *S_out,
+                        int *d_err, void *cuda_stream);
+
+/* Human-readable name of a hypic_status value (static string, never NULL). */
+const char *hypic_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int hypic_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HYPIC_H */

@@ -1,2 +1,220 @@
 """GB300-native segment scan and state composition for position-independent
-caching of hybrid linear-attention models (HYPIC)."""
+caching of hybrid linear-attention models (HYPIC).
+
+Thin ctypes binding over ``libhypic.so`` (built from ``csrc/`` by
+``_build.build()``).  These functions only check and marshal arguments --
+device pointers of torch tensors and the current CUDA stream -- into the
+C ABI declared in ``include/hypic.h``; every step of the computation runs in
+the library's CUDA kernels.  There is no CPU fallback: if the library is not
+built, or a tensor is not on a CUDA device, the call raises.
+
+The operations (HYPIC, xix.ai/fr article, paragraph on linear layers):
+  segment_scan  -- per segment C and head, T_C = product of the per-token
+                   transitions (as exp(lam) * M) and S(C|0), the final state
+                   from a zero start; optionally o_t = S_t^T q_t.
+  compose       -- S(C1.C2) = T(C2) S(C1) + S(C2), optionally T(C2) T(C1).
+  compose_chain -- fold many cached pairs in order into a running state
+                   (remio.ai/ja, "cold requests become parallel": the combine step).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import _build
+
+SCALAR, DIAG, DENSE = 0, 1, 2
+FAMILIES = {"scalar": SCALAR, "diag": DIAG, "dense": DENSE}
+BF16, F32 = 0, 1
+STATUS = {0: "HYPIC_OK", -1: "HYPIC_EINVAL", -2: "HYPIC_EUNSUPPORTED", -3: "HYPIC_EALIGN",
+          -4: "HYPIC_ECUDA", -5: "HYPIC_EINDEX"}
+
+__all__ = ["segment_scan", "compose", "compose_chain", "status_string", "library",
+           "HypicError", "SCALAR", "DIAG", "DENSE"]
+
+
+class HypicError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)} ({status_string(status)})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+# every symbol include/hypic.h declares, with its ctypes signature
+_P, _I32, _I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+SIGNATURES = {
+    "hypic_segment_scan": (_I32, [_I32, _I32, _I32, _I32, _I64, _I32, _I32, _I32,
+                                  _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "hypic_compose": (_I32, [_I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "hypic_compose_chain": (_I32, [_I32, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _I32,
+                                   _P, _P, _P, _P, _P, _P, _P]),
+    "hypic_status_string": (ctypes.c_char_p, [_I32]),
+    "hypic_version": (_I32, []),
+}
+
+
+def library(path: str | None = None):
+    """Load libhypic.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None or path is not None:
+            p = path or _build.LIB
+            if not os.path.exists(p):
+                raise RuntimeError(f"{p} is missing: build it with "
+                                   "`python -m linear_attention_state_gated_gb300._build`")
+            lib = ctypes.CDLL(p)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            if path is not None:
+                return lib
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return library().hypic_status_string(int(status)).decode()
+
+
+def _fam(f):
+    return FAMILIES[f] if isinstance(f, str) else int(f)
+
+
+def _dev(t, name, dtype=None, allow_none=False):
+    if t is None:
+        if allow_none:
+            return None
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _ptr(t):
+    return ctypes.c_void_p(None if t is None else t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn, status):
+    if status != 0:
+        raise HypicError(fn, status)
+
+
+def segment_scan(family, k, v, alpha, seg_offsets, beta=None, q=None, want_o=False,
+                 out=None, d_err=None, stream=None):
+    """(T_C, S(C|0)) for every (layer, segment, head); optionally o_t.
+
+    k [Lyr,N,H,dk], v [Lyr,N,H,dv] (bf16 or fp32), alpha fp32 [Lyr,N,H] or
+    [Lyr,N,H,dk] (diag), beta fp32 [Lyr,N,H] or None, q like k (for o_t),
+    seg_offsets int64 [n_seg+1] on the device.  ``out`` may hold preallocated
+    ``lam``, ``M``, ``S``, ``o`` tensors.  Returns a dict with lam, S, M (dense), o.
+    """
+    fam = _fam(family)
+    k = _dev(k, "k")
+    dt = k.dtype
+    if dt not in (torch.bfloat16, torch.float32):
+        raise ValueError("k must be bf16 or fp32")
+    v = _dev(v, "v", dt)
+    alpha = _dev(alpha, "alpha", torch.float32)
+    beta = _dev(beta, "beta", torch.float32, allow_none=True)
+    seg_offsets = _dev(seg_offsets, "seg_offsets", torch.int64)
+    if want_o:
+        q = _dev(q, "q", dt)
+    Lyr, N, H, dk = k.shape
+    dv = v.shape[-1]
+    n_seg = seg_offsets.numel() - 1
+    out = dict(out or {})
+    dev = k.device
+    lam_shape = (Lyr, n_seg, H, dk) if fam == DIAG else (Lyr, n_seg, H)
+    if "lam" not in out:
+        out["lam"] = torch.empty(lam_shape, dtype=torch.float32, device=dev)
+    if "S" not in out:
+        out["S"] = torch.empty((Lyr, n_seg, H, dk, dv), dtype=torch.float32, device=dev)
+    if fam == DENSE and "M" not in out:
+        out["M"] = torch.empty((Lyr, n_seg, H, dk, dk), dtype=torch.float32, device=dev)
+    if want_o and "o" not in out:
+        out["o"] = torch.empty((Lyr, N, H, dv), dtype=dt, device=dev)
+    st = library().hypic_segment_scan(
+        fam, BF16 if dt == torch.bfloat16 else F32, Lyr, n_seg, N, H, dk, dv,
+        _ptr(seg_offsets), _ptr(q if want_o else None), _ptr(k), _ptr(v), _ptr(alpha),
+        _ptr(beta), _ptr(out["lam"]), _ptr(out.get("M") if fam == DENSE else None),
+        _ptr(out["S"]), _ptr(out.get("o") if want_o else None), _ptr(d_err), _stream(stream))
+    _check("hypic_segment_scan", st)
+    return out
+
+
+def compose(family, lam, S_C, S_prev=None, M=None, lam_prev=None, M_prev=None, S_out=None,
+            lam_out=None, M_out=None, stream=None):
+    """S = exp(lam) M S_prev + S_C over [n, H] items (M = 1 / I for scalar / diag).
+
+    With lam_prev (and M_prev for dense) also returns the composed operator
+    T(C1.C2) = T(C2) T(C1) as lam (and M).  S_out may be S_prev (in place).
+    """
+    fam = _fam(family)
+    S_C = _dev(S_C, "S_C", torch.float32)
+    lam = _dev(lam, "lam", torch.float32)
+    S_prev = _dev(S_prev, "S_prev", torch.float32, allow_none=True)
+    M = _dev(M, "M", torch.float32, allow_none=True)
+    lam_prev = _dev(lam_prev, "lam_prev", torch.float32, allow_none=True)
+    M_prev = _dev(M_prev, "M_prev", torch.float32, allow_none=True)
+    n, H, dk, dv = S_C.shape
+    if S_out is None:
+        S_out = torch.empty_like(S_C)
+    want_T = lam_prev is not None
+    if want_T and lam_out is None:
+        lam_out = torch.empty_like(lam)
+    if want_T and fam == DENSE and M_out is None:
+        M_out = torch.empty_like(M)
+    st = library().hypic_compose(fam, n, H, dk, dv, _ptr(lam), _ptr(M), _ptr(S_prev), _ptr(S_C),
+                                 _ptr(S_out), _ptr(lam_prev), _ptr(M_prev),
+                                 _ptr(lam_out if want_T else None),
+                                 _ptr(M_out if (want_T and fam == DENSE) else None),
+                                 _stream(stream))
+    _check("hypic_compose", st)
+    res = {"S": S_out}
+    if want_T:
+        res["lam"] = lam_out
+        if fam == DENSE:
+            res["M"] = M_out
+    return res
+
+
+def compose_chain(family, chain_len, seg_idx, pool_lam, pool_S, pool_M=None, S_init=None,
+                  S_out=None, d_err=None, stream=None):
+    """Fold pool entries seg_idx[r, :chain_len[r]] in order: S <- T_p S + S_p.
+
+    pool_lam [P,Lyr,H] or [P,Lyr,H,dk], pool_M [P,Lyr,H,dk,dk] (dense),
+    pool_S [P,Lyr,H,dk,dv], S_init [R,Lyr,H,dk,dv] or None.  Returns S [R,Lyr,H,dk,dv].
+    """
+    fam = _fam(family)
+    chain_len = _dev(chain_len, "chain_len", torch.int32)
+    seg_idx = _dev(seg_idx, "seg_idx", torch.int32)
+    pool_lam = _dev(pool_lam, "pool_lam", torch.float32)
+    pool_S = _dev(pool_S, "pool_S", torch.float32)
+    pool_M = _dev(pool_M, "pool_M", torch.float32, allow_none=True)
+    S_init = _dev(S_init, "S_init", torch.float32, allow_none=True)
+    P, Lyr, H, dk, dv = pool_S.shape
+    R = chain_len.numel()
+    max_chain = seg_idx.shape[1] if seg_idx.dim() == 2 else 0
+    if S_out is None:
+        S_out = torch.empty((R, Lyr, H, dk, dv), dtype=torch.float32, device=pool_S.device)
+    st = library().hypic_compose_chain(fam, R, Lyr, H, dk, dv, max_chain, _ptr(chain_len),
+                                       _ptr(seg_idx), P, _ptr(pool_lam), _ptr(pool_M),
+                                       _ptr(pool_S), _ptr(S_init), _ptr(S_out), _ptr(d_err),
+                                       _stream(stream))
+    _check("hypic_compose_chain", st)
+    return S_out

@@ -1,0 +1,180 @@
+// api.cu -- the extern "C" entry points of libhypic: argument checks on the
+// host, then one or more launches on the caller's stream.  No allocation, no
+// global state, no synchronisation.
+#include <stdint.h>
+
+#include "internal.cuh"
+
+namespace {
+
+bool aligned(const void *p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
+
+bool head_size_ok(int d) { return d == 32 || d == 64 || d == 128; }
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? HYPIC_OK : HYPIC_ECUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int hypic_version(void) { return 100; }
+
+const char *hypic_status_string(int status) {
+    switch (status) {
+        case HYPIC_OK: return "ok";
+        case HYPIC_EINVAL: return "invalid argument";
+        case HYPIC_EUNSUPPORTED: return "unsupported size or option";
+        case HYPIC_EALIGN: return "misaligned pointer";
+        case HYPIC_ECUDA: return "CUDA error";
+        case HYPIC_EINDEX: return "index out of range (device side)";
+    }
+    return "unknown status";
+}
+
+int hypic_segment_scan(int fam, int in_dtype, int n_layers, int n_seg, int64_t total_tokens,
+                       int n_heads, int d_k, int d_v, const int64_t *seg_offsets, const void *q,
+                       const void *k, const void *v, const float *alpha, const float *beta,
+                       float *lam_out, float *M_out, float *S_out, void *o_out, int *d_err,
+                       void *cuda_stream) {
+    if (fam < HYPIC_SCALAR || fam > HYPIC_DENSE) return HYPIC_EINVAL;
+    if (in_dtype != HYPIC_BF16 && in_dtype != HYPIC_F32) return HYPIC_EINVAL;
+    if (n_layers < 0 || n_seg < 0 || total_tokens < 0 || n_heads <= 0) return HYPIC_EINVAL;
+    if (!head_size_ok(d_k) || !head_size_ok(d_v)) return HYPIC_EUNSUPPORTED;
+    if ((int64_t)n_layers * n_seg * n_heads > INT32_MAX) return HYPIC_EUNSUPPORTED;
+    if ((int64_t)n_layers * total_tokens * n_heads > (INT64_MAX / 256)) return HYPIC_EUNSUPPORTED;
+    if (n_layers == 0 || n_seg == 0) return HYPIC_OK;
+    const bool has_tokens = total_tokens > 0;
+    if (!seg_offsets || !lam_out || !S_out) return HYPIC_EINVAL;
+    if (has_tokens && (!k || !v || !alpha)) return HYPIC_EINVAL;
+    if ((fam == HYPIC_DENSE) != (M_out != nullptr)) return HYPIC_EINVAL;
+    if (o_out && !q && has_tokens) return HYPIC_EINVAL;
+    if (!aligned(seg_offsets, 8)) return HYPIC_EALIGN;
+    const void *a16[] = {q, k, v, o_out, S_out, M_out, fam == HYPIC_DIAG ? alpha : nullptr,
+                         fam == HYPIC_DIAG ? lam_out : nullptr};
+    for (const void *p : a16)
+        if (p && !aligned(p, 16)) return HYPIC_EALIGN;
+    const void *a4[] = {alpha, beta, lam_out, d_err};
+    for (const void *p : a4)
+        if (p && !aligned(p, 4)) return HYPIC_EALIGN;
+
+    hypic::ScanArgs a;
+    a.fam = fam;
+    a.in_dtype = in_dtype;
+    a.n_layers = n_layers;
+    a.n_seg = n_seg;
+    a.H = n_heads;
+    a.dk = d_k;
+    a.dv = d_v;
+    a.N = total_tokens;
+    a.seg_offsets = seg_offsets;
+    a.q = o_out ? q : nullptr;
+    a.k = k;
+    a.v = v;
+    a.alpha = alpha;
+    a.beta = beta;
+    a.lam_out = lam_out;
+    a.M_out = M_out;
+    a.S_out = S_out;
+    a.o_out = o_out;
+    a.d_err = d_err;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    return from_cuda(hypic::launch_scan_recurrent(a, s));
+}
+
+int hypic_compose(int fam, int n, int n_heads, int d_k, int d_v, const float *lam, const float *M,
+                  const float *S_prev, const float *S_C, float *S_out, const float *lam_prev,
+                  const float *M_prev, float *lam_out, float *M_out, void *cuda_stream) {
+    if (fam < HYPIC_SCALAR || fam > HYPIC_DENSE) return HYPIC_EINVAL;
+    if (n < 0 || n_heads <= 0) return HYPIC_EINVAL;
+    if (!head_size_ok(d_k) || !head_size_ok(d_v)) return HYPIC_EUNSUPPORTED;
+    if ((int64_t)n * n_heads > INT32_MAX) return HYPIC_EUNSUPPORTED;
+    if (n == 0) return HYPIC_OK;
+    if (!lam || !S_C || !S_out) return HYPIC_EINVAL;
+    if ((fam == HYPIC_DENSE) != (M != nullptr)) return HYPIC_EINVAL;
+    if ((lam_prev == nullptr) != (lam_out == nullptr)) return HYPIC_EINVAL;
+    if (fam == HYPIC_DENSE) {
+        if ((M_prev == nullptr) != (lam_out == nullptr) || (M_out == nullptr) != (lam_out == nullptr))
+            return HYPIC_EINVAL;
+    } else if (M_prev || M_out) {
+        return HYPIC_EINVAL;
+    }
+    const void *a16[] = {M, S_prev, S_C, S_out, M_prev, M_out,
+                         fam == HYPIC_DIAG ? lam : nullptr, fam == HYPIC_DIAG ? lam_prev : nullptr,
+                         fam == HYPIC_DIAG ? lam_out : nullptr};
+    for (const void *p : a16)
+        if (p && !aligned(p, 16)) return HYPIC_EALIGN;
+    const void *a4[] = {lam, lam_prev, lam_out};
+    for (const void *p : a4)
+        if (p && !aligned(p, 4)) return HYPIC_EALIGN;
+    // S_out may be S_prev; any other overlap with an input is not supported
+    const size_t sbytes = (size_t)n * n_heads * d_k * d_v * sizeof(float);
+    auto overlaps = [](const void *x, const void *y, size_t bytes) {
+        if (!x || !y) return false;
+        const char *a = static_cast<const char *>(x), *b = static_cast<const char *>(y);
+        return a < b + bytes && b < a + bytes;
+    };
+    if (overlaps(S_out, S_C, sbytes) && S_out != S_C) return HYPIC_EINVAL;
+    if (S_prev && S_out != S_prev && overlaps(S_out, S_prev, sbytes)) return HYPIC_EINVAL;
+    if (fam == HYPIC_DENSE && (overlaps(S_out, M, sbytes) || overlaps(S_out, M_prev, sbytes)))
+        return HYPIC_EINVAL;
+
+    hypic::ComposeArgs a;
+    a.fam = fam;
+    a.n = n;
+    a.H = n_heads;
+    a.dk = d_k;
+    a.dv = d_v;
+    a.lam = lam;
+    a.M = M;
+    a.S_prev = S_prev;
+    a.S_C = S_C;
+    a.S_out = S_out;
+    a.lam_prev = lam_prev;
+    a.M_prev = M_prev;
+    a.lam_out = lam_out;
+    a.M_out = M_out;
+    return from_cuda(hypic::launch_compose(a, static_cast<cudaStream_t>(cuda_stream)));
+}
+
+int hypic_compose_chain(int fam, int n_req, int n_layers, int n_heads, int d_k, int d_v,
+                        int max_chain, const int32_t *chain_len, const int32_t *seg_idx,
+                        int pool_size, const float *pool_lam, const float *pool_M,
+                        const float *pool_S, const float *S_init, float *S_out, int *d_err,
+                        void *cuda_stream) {
+    if (fam < HYPIC_SCALAR || fam > HYPIC_DENSE) return HYPIC_EINVAL;
+    if (n_req < 0 || n_layers < 0 || n_heads <= 0 || max_chain < 0 || pool_size < 0)
+        return HYPIC_EINVAL;
+    if (!head_size_ok(d_k) || !head_size_ok(d_v)) return HYPIC_EUNSUPPORTED;
+    if ((int64_t)n_req * n_layers * n_heads > INT32_MAX) return HYPIC_EUNSUPPORTED;
+    if (n_req == 0 || n_layers == 0) return HYPIC_OK;
+    if (!chain_len || !S_out) return HYPIC_EINVAL;
+    if (max_chain > 0 && (!seg_idx || pool_size == 0 || !pool_lam || !pool_S)) return HYPIC_EINVAL;
+    if (max_chain > 0 && (fam == HYPIC_DENSE) != (pool_M != nullptr)) return HYPIC_EINVAL;
+    const void *a16[] = {pool_M, pool_S, S_init, S_out, fam == HYPIC_DIAG ? pool_lam : nullptr};
+    for (const void *p : a16)
+        if (p && !aligned(p, 16)) return HYPIC_EALIGN;
+    const void *a4[] = {chain_len, seg_idx, pool_lam, d_err};
+    for (const void *p : a4)
+        if (p && !aligned(p, 4)) return HYPIC_EALIGN;
+
+    hypic::ChainArgs a;
+    a.fam = fam;
+    a.R = n_req;
+    a.n_layers = n_layers;
+    a.H = n_heads;
+    a.dk = d_k;
+    a.dv = d_v;
+    a.max_chain = max_chain;
+    a.P = pool_size;
+    a.chain_len = chain_len;
+    a.seg_idx = seg_idx;
+    a.pool_lam = pool_lam;
+    a.pool_M = pool_M;
+    a.pool_S = pool_S;
+    a.S_init = S_init;
+    a.S_out = S_out;
+    a.d_err = d_err;
+    return from_cuda(hypic::launch_compose_chain(a, static_cast<cudaStream_t>(cuda_stream)));
+}
+
+}  // extern "C"

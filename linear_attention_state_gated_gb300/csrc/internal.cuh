@@ -1,0 +1,62 @@
+// internal.cuh -- declarations shared by the translation units of libhypic.
+// Launchers return a cudaError_t; api.cu turns that into a hypic_status.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/hypic.h"
+
+namespace hypic {
+
+struct ScanArgs {
+    int fam;          // hypic_family
+    int in_dtype;     // hypic_dtype
+    int n_layers, n_seg, H, dk, dv;
+    int64_t N;        // tokens per layer
+    const int64_t *seg_offsets;
+    const void *q, *k, *v;
+    const float *alpha, *beta;
+    float *lam_out, *M_out, *S_out;
+    void *o_out;
+    int *d_err;
+};
+
+struct ComposeArgs {
+    int fam, n, H, dk, dv;
+    const float *lam, *M, *S_prev, *S_C;
+    float *S_out;
+    const float *lam_prev, *M_prev;
+    float *lam_out, *M_out;
+};
+
+struct ChainArgs {
+    int fam, R, n_layers, H, dk, dv, max_chain, P;
+    const int32_t *chain_len, *seg_idx;
+    const float *pool_lam, *pool_M, *pool_S, *S_init;
+    float *S_out;
+    int *d_err;
+};
+
+// Token-by-token fp32 recurrence on CUDA cores, every family, optional o_t.
+cudaError_t launch_scan_recurrent(const ScanArgs &a, cudaStream_t s);
+
+cudaError_t launch_compose(const ComposeArgs &a, cudaStream_t s);
+cudaError_t launch_compose_chain(const ChainArgs &a, cudaStream_t s);
+
+// Report a device-side index problem without trapping.
+__device__ __forceinline__ void flag_index_error(int *d_err) {
+    if (d_err) atomicExch(d_err, (int)HYPIC_EINDEX);
+}
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+}  // namespace hypic

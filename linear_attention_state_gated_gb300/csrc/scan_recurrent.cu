@@ -1,0 +1,258 @@
+// scan_recurrent.cu -- token-by-token segment scan on CUDA cores, fp32.
+//
+// One CTA walks one (layer, segment, head) chain token by token, exactly the
+// recurrence of the family (S_t = T_t S_{t-1} + beta_t k_t v_t^T, see hypic.h),
+// keeping the state in registers.  It serves every family and the optional
+// per-token output o_t = S_t^T q_t, and is the path for fp32 inputs and for
+// scalar/diagonal scans that ask for o_t.  The transition of the dense family
+// is carried as exp(lambda) * M with M renormalised by exact powers of two.
+//
+// Thread layout: the state (and, for the dense family, M) is split by
+// columns: thread (g, c) owns column c and rows [g*RPT, (g+1)*RPT).  A token
+// is a rank-1 update of every column, so a thread needs only the scalar
+// u_c = k^T X[:, c] (a reduction over its G row groups) and the broadcast key.
+#include "internal.cuh"
+
+namespace hypic {
+namespace {
+
+constexpr int kTB = 16;  // tokens staged in shared memory per round
+
+__device__ __forceinline__ void kahan_add(float &sum, float &comp, float v) {
+    const float y = v - comp;
+    const float t = sum + y;
+    comp = (t - sum) - y;
+    sum = t;
+}
+
+template <int FAM, int DK, typename TIn>
+__global__ void __launch_bounds__(512) scan_recurrent_kernel(const ScanArgs a) {
+    constexpr int RPT = DK < 64 ? DK : 64;   // rows per thread
+    constexpr int G = DK / RPT;              // row groups
+    constexpr bool kDense = FAM == HYPIC_DENSE;
+    constexpr bool kDiag = FAM == HYPIC_DIAG;
+    const int DV = a.dv;
+    const int NCOL = (kDense ? DK : 0) + DV;
+    const int NT = NCOL * G;
+    const int tid = threadIdx.x;
+    const int c = tid % NCOL, g = tid / NCOL;
+    const int row0 = g * RPT;
+    const bool mcol = kDense && c < DK;                  // column of M
+    const int scol = c - (kDense ? DK : 0);              // column of S (if !mcol)
+    const bool want_o = a.o_out != nullptr;
+
+    extern __shared__ float smem[];
+    float *sk = smem;                                    // [kTB][DK]
+    float *sv = sk + kTB * DK;                           // [kTB][DV]
+    float *sq = sv + kTB * DV;                           // [kTB][DK] if want_o
+    float *sa = sq + (want_o ? kTB * DK : 0);            // [kTB][DK] diag, else [kTB]
+    float *sb = sa + kTB * (kDiag ? DK : 1);             // [kTB]
+    float *red = sb + kTB;                               // [2][G][NCOL]
+    float *redo = red + 2 * G * NCOL;                    // [G][DV]
+    float *redm = redo + G * DV;                         // [32]
+
+    const int unit = blockIdx.x;
+    const int h = unit % a.H;
+    const int seg = (unit / a.H) % a.n_seg;
+    const int l = unit / (a.H * a.n_seg);
+
+    int64_t t0 = a.seg_offsets[seg], t1 = a.seg_offsets[seg + 1];
+    if (!(t0 >= 0 && t0 <= t1 && t1 <= a.N)) {
+        if (tid == 0) flag_index_error(a.d_err);
+        t0 = t1 = 0;
+    }
+
+    float x[RPT];
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) x[r] = (mcol && row0 + r == c) ? 1.f : 0.f;
+    float lam_sum = 0.f, lam_comp = 0.f;
+    int lam_exp = 0;   // power-of-two exponent moved out of M
+
+    const TIn *Kp = static_cast<const TIn *>(a.k);
+    const TIn *Vp = static_cast<const TIn *>(a.v);
+    const TIn *Qp = static_cast<const TIn *>(a.q);
+    TIn *Op = static_cast<TIn *>(a.o_out);
+    const int64_t layer_row0 = (int64_t)l * a.N;
+
+    for (int64_t tb = t0; tb < t1; tb += kTB) {
+        const int nt = (int)((t1 - tb) < kTB ? (t1 - tb) : kTB);
+        __syncthreads();
+        for (int i = tid; i < nt * DK; i += NT) {
+            const int tt = i / DK, d = i % DK;
+            const int64_t row = (layer_row0 + tb + tt) * a.H + h;
+            sk[tt * DK + d] = to_f32(Kp[row * DK + d]);
+            if (want_o) sq[tt * DK + d] = to_f32(Qp[row * DK + d]);
+            if (kDiag) sa[tt * DK + d] = a.alpha[row * DK + d];
+        }
+        for (int i = tid; i < nt * DV; i += NT) {
+            const int tt = i / DV, d = i % DV;
+            const int64_t row = (layer_row0 + tb + tt) * a.H + h;
+            sv[tt * DV + d] = to_f32(Vp[row * DV + d]);
+        }
+        for (int i = tid; i < nt; i += NT) {
+            const int64_t row = (layer_row0 + tb + i) * a.H + h;
+            if (!kDiag) sa[i] = a.alpha[row];
+            sb[i] = a.beta ? a.beta[row] : 1.f;
+        }
+        __syncthreads();
+
+        for (int tt = 0; tt < nt; ++tt) {
+            const float *kt = sk + tt * DK + row0;
+            const float b = sb[tt];
+            if (kDense) {
+                const float al = sa[tt];
+                float p = 0.f;
+#pragma unroll
+                for (int r = 0; r < RPT; ++r) p = fmaf(kt[r], x[r], p);
+                float u = p;
+                if (G > 1) {
+                    float *rb = red + (tt & 1) * G * NCOL;
+                    rb[g * NCOL + c] = p;
+                    __syncthreads();
+                    u = 0.f;
+#pragma unroll
+                    for (int gg = 0; gg < G; ++gg) u += rb[gg * NCOL + c];
+                }
+                if (mcol) {
+                    // M <- M - beta k (k^T M)
+                    const float w = -b * u;
+#pragma unroll
+                    for (int r = 0; r < RPT; ++r) x[r] = fmaf(kt[r], w, x[r]);
+                } else {
+                    // S <- alpha (S - beta k (k^T S)) + beta k v^T = alpha S + k (beta (v - alpha u))^T
+                    const float w = b * (sv[tt * DV + scol] - al * u);
+#pragma unroll
+                    for (int r = 0; r < RPT; ++r) x[r] = fmaf(kt[r], w, al * x[r]);
+                }
+                if (tid == 0) kahan_add(lam_sum, lam_comp, logf(al));
+            } else if (!kDiag) {
+                const float al = sa[tt];
+                const float w = b * sv[tt * DV + scol];
+#pragma unroll
+                for (int r = 0; r < RPT; ++r) x[r] = fmaf(kt[r], w, al * x[r]);
+                if (tid == 0) kahan_add(lam_sum, lam_comp, logf(al));
+            } else {
+                const float *at = sa + tt * DK;
+                const float w = b * sv[tt * DV + scol];
+#pragma unroll
+                for (int r = 0; r < RPT; ++r) x[r] = fmaf(kt[r], w, at[row0 + r] * x[r]);
+                if (tid < DK) kahan_add(lam_sum, lam_comp, logf(at[tid]));
+            }
+            if (want_o) {
+                float po = 0.f;
+                if (!mcol) {
+                    const float *qt = sq + tt * DK + row0;
+#pragma unroll
+                    for (int r = 0; r < RPT; ++r) po = fmaf(qt[r], x[r], po);
+                }
+                const int64_t orow = (layer_row0 + tb + tt) * a.H + h;
+                if (G > 1) {
+                    __syncthreads();
+                    if (!mcol) redo[g * DV + scol] = po;
+                    __syncthreads();
+                    if (!mcol && g == 0) {
+                        float s = 0.f;
+#pragma unroll
+                        for (int gg = 0; gg < G; ++gg) s += redo[gg * DV + scol];
+                        Op[orow * DV + scol] = from_f32<TIn>(s);
+                    }
+                } else if (!mcol) {
+                    Op[orow * DV + scol] = from_f32<TIn>(po);
+                }
+            }
+        }
+
+        if (kDense) {
+            // keep max|M| in [1, 2) with exact power-of-two scaling
+            float mx = 0.f;
+            if (mcol) {
+#pragma unroll
+                for (int r = 0; r < RPT; ++r) mx = fmaxf(mx, fabsf(x[r]));
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            __syncthreads();
+            if ((tid & 31) == 0) redm[tid >> 5] = mx;
+            __syncthreads();
+            mx = 0.f;
+            for (int w = 0; w < (NT + 31) / 32; ++w) mx = fmaxf(mx, redm[w]);
+            if (mx > 0.f && (mx < 1.f || mx >= 2.f)) {
+                int ex;
+                frexpf(mx, &ex);
+                const int e = ex - 1;
+                const float sc = ldexpf(1.f, -e);
+                if (mcol) {
+#pragma unroll
+                    for (int r = 0; r < RPT; ++r) x[r] *= sc;
+                }
+                lam_exp += e;
+            }
+        }
+    }
+
+    const int64_t u_out = ((int64_t)l * a.n_seg + seg) * a.H + h;
+    if (!mcol) {
+        float *So = a.S_out + u_out * DK * DV;
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) So[(int64_t)(row0 + r) * DV + scol] = x[r];
+    } else {
+        float *Mo = a.M_out + u_out * DK * DK;
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) Mo[(int64_t)(row0 + r) * DK + c] = x[r];
+    }
+    if (kDiag) {
+        if (tid < DK) a.lam_out[u_out * DK + tid] = lam_sum;
+    } else if (tid == 0) {
+        const double lam = (double)lam_sum + (double)lam_exp * 0.69314718055994530942;
+        a.lam_out[u_out] = (float)lam;
+    }
+}
+
+template <int FAM, int DK, typename TIn>
+cudaError_t launch_one(const ScanArgs &a, cudaStream_t s) {
+    constexpr int RPT = DK < 64 ? DK : 64;
+    constexpr int G = DK / RPT;
+    const int ncol = (FAM == HYPIC_DENSE ? DK : 0) + a.dv;
+    const int nt = ncol * G;
+    const bool want_o = a.o_out != nullptr;
+    size_t floats = (size_t)kTB * DK + (size_t)kTB * a.dv + (want_o ? (size_t)kTB * DK : 0) +
+                    (size_t)kTB * (FAM == HYPIC_DIAG ? DK : 1) + kTB + 2 * G * ncol + G * a.dv + 32;
+    const size_t smem = floats * sizeof(float);
+    auto kern = scan_recurrent_kernel<FAM, DK, TIn>;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    const int64_t units = (int64_t)a.n_layers * a.n_seg * a.H;
+    kern<<<(unsigned)units, nt, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <int FAM, typename TIn>
+cudaError_t launch_dk(const ScanArgs &a, cudaStream_t s) {
+    switch (a.dk) {
+        case 32: return launch_one<FAM, 32, TIn>(a, s);
+        case 64: return launch_one<FAM, 64, TIn>(a, s);
+        case 128: return launch_one<FAM, 128, TIn>(a, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <typename TIn>
+cudaError_t launch_fam(const ScanArgs &a, cudaStream_t s) {
+    switch (a.fam) {
+        case HYPIC_SCALAR: return launch_dk<HYPIC_SCALAR, TIn>(a, s);
+        case HYPIC_DIAG: return launch_dk<HYPIC_DIAG, TIn>(a, s);
+        case HYPIC_DENSE: return launch_dk<HYPIC_DENSE, TIn>(a, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_scan_recurrent(const ScanArgs &a, cudaStream_t s) {
+    if ((int64_t)a.n_layers * a.n_seg * a.H == 0) return cudaSuccess;
+    return a.in_dtype == HYPIC_BF16 ? launch_fam<__nv_bfloat16>(a, s) : launch_fam<float>(a, s);
+}
+
+}  // namespace hypic

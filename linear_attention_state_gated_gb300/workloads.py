@@ -27,13 +27,27 @@ draws stand in):
 """
 from __future__ import annotations
 
+import os
+
 import numpy as np
 
 SCALAR, DIAG, DENSE = 0, 1, 2
 
 
-def rng(seed: int) -> np.random.Generator:
+def rng(seed) -> np.random.Generator:
     return np.random.Generator(np.random.PCG64(seed))
+
+
+_BLOCK = 2048          # tokens per independently seeded block
+_POOL = None
+
+
+def _pool():
+    global _POOL
+    if _POOL is None:
+        import concurrent.futures as cf
+        _POOL = cf.ThreadPoolExecutor(max(1, min(16, os.cpu_count() or 1)))
+    return _POOL
 
 
 def bf16_round(x: np.ndarray) -> np.ndarray:
@@ -56,12 +70,8 @@ def bf16_bits(x: np.ndarray) -> np.ndarray:
     return (x.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
 
 
-def _normal(g, shape):
-    return g.standard_normal(size=shape, dtype=np.float32)
-
-
 def _l2_rows(x):
-    n = np.sqrt(np.sum(x.astype(np.float64) ** 2, axis=-1, keepdims=True))
+    n = np.sqrt(np.sum(np.square(x, dtype=np.float32), axis=-1, keepdims=True, dtype=np.float32))
     n[n == 0] = 1.0
     return (x / n).astype(np.float32)
 
@@ -75,17 +85,53 @@ def _softplus(x):
     return np.where(x > 20, x, np.log1p(np.exp(np.minimum(x, 20))))
 
 
+def _field(seed: int, field: int, n_layers: int, N: int, tail_shape, make, layers=None):
+    """[n_layers or len(layers), N, *tail_shape] float32, filled block by block.
+
+    Block (layer l, tokens [b*_BLOCK, ...)) draws from PCG64 seeded with
+    (seed, field, l, b), so the values do not depend on the thread count and
+    any layer can be regenerated on its own.  ``make(gen, shape)`` draws one block.
+    """
+    layers = list(range(n_layers)) if layers is None else list(layers)
+    out = np.empty((len(layers), N, *tail_shape), dtype=np.float32)
+    nblk = (N + _BLOCK - 1) // _BLOCK
+
+    def job(i, b):
+        l = layers[i]
+        t0, t1 = b * _BLOCK, min(N, (b + 1) * _BLOCK)
+        g = rng([seed, field, l, b])
+        out[i, t0:t1] = make(g, (t1 - t0, *tail_shape))
+
+    futs = [_pool().submit(job, i, b) for i in range(len(layers)) for b in range(nblk)]
+    for f in futs:
+        f.result()
+    return out
+
+
+def _unit_rows_bf16(g, shape):
+    return bf16_round(_l2_rows(g.standard_normal(size=shape, dtype=np.float32)))
+
+
+def _normal_bf16(g, shape):
+    return bf16_round(g.standard_normal(size=shape, dtype=np.float32))
+
+
 def equal_offsets(n_seg: int, length: int) -> np.ndarray:
     return np.arange(n_seg + 1, dtype=np.int64) * length
 
 
+def _offsets(lengths):
+    return np.concatenate([[0], np.cumsum(np.asarray(lengths, dtype=np.int64))]).astype(np.int64)
+
+
 def tiny_dense(seed: int = 0, n_seg: int = 2, seg_len: int = 64, H: int = 2, d: int = 32):
-    """Gated delta rule, fp32 inputs: k, q L2-normalised N(0,1), v N(0,1)."""
+    """Gated delta rule, fp32 inputs: k, q L2-normalised N(0,1), v N(0,1),
+    alpha ~ U(0.9, 1), beta ~ U(0, 1)."""
     g = rng(seed)
     N = n_seg * seg_len
-    k = _l2_rows(_normal(g, (1, N, H, d)))
-    q = _l2_rows(_normal(g, (1, N, H, d)))
-    v = _normal(g, (1, N, H, d))
+    k = _l2_rows(g.standard_normal((1, N, H, d), dtype=np.float32))
+    q = _l2_rows(g.standard_normal((1, N, H, d), dtype=np.float32))
+    v = g.standard_normal((1, N, H, d), dtype=np.float32)
     alpha = g.uniform(0.9, 1.0, size=(1, N, H)).astype(np.float32)
     beta = g.uniform(0.0, 1.0, size=(1, N, H)).astype(np.float32)
     return dict(family=DENSE, dtype="f32", q=q, k=k, v=v, alpha=alpha, beta=beta,
@@ -98,46 +144,59 @@ def retnet_gamma(H: int) -> np.ndarray:
     return (1.0 - np.exp2(-5.0 - 6.0 * h / H)).astype(np.float32)
 
 
-def scalar_diag(family: int, seg_len: int, n_seg: int = 8, H: int = 32, d: int = 128,
-                seed: int = 1, with_q: bool = False, n_layers: int = 1,
-                lengths=None):
+def _diag_gate(g, shape):
+    x = g.standard_normal(size=shape, dtype=np.float32) + np.float32(2.0)
+    return (_sigmoid(x) ** np.float32(1.0 / 16.0)).astype(np.float32)
+
+
+def scalar_diag(family: int, seg_len: int = 512, n_seg: int = 8, H: int = 32, d: int = 128,
+                seed: int = 1, with_q: bool = False, n_layers: int = 1, lengths=None,
+                layers=None):
     """Scalar (fixed gamma_h per head) or diagonal (per-channel GLA gate) workload.
 
     k, q: L2-normalised N(0,1) rows, v ~ N(0,1); all bf16.  No beta.
-    ``lengths`` overrides the equal segment lengths (ragged batches).
+    ``lengths`` overrides the equal segment lengths (ragged batches);
+    ``layers`` regenerates only those layers (same values as in the full set).
     """
-    g = rng(seed)
     if lengths is None:
         lengths = [seg_len] * n_seg
-    offs = np.concatenate([[0], np.cumsum(np.asarray(lengths, dtype=np.int64))]).astype(np.int64)
+    offs = _offsets(lengths)
     N = int(offs[-1])
-    k = bf16_round(_l2_rows(_normal(g, (n_layers, N, H, d))))
-    v = bf16_round(_normal(g, (n_layers, N, H, d)))
-    q = bf16_round(_l2_rows(_normal(g, (n_layers, N, H, d)))) if with_q else None
+    nl = n_layers if layers is None else len(layers)
+    k = _field(seed, 1, n_layers, N, (H, d), _unit_rows_bf16, layers)
+    v = _field(seed, 2, n_layers, N, (H, d), _normal_bf16, layers)
+    q = _field(seed, 3, n_layers, N, (H, d), _unit_rows_bf16, layers) if with_q else None
     if family == SCALAR:
-        alpha = np.broadcast_to(retnet_gamma(H)[None, None, :], (n_layers, N, H)).copy()
+        alpha = np.broadcast_to(retnet_gamma(H)[None, None, :], (nl, N, H)).copy()
     elif family == DIAG:
-        alpha = _sigmoid(g.normal(2.0, 1.0, size=(n_layers, N, H, d))) ** np.float32(1.0 / 16.0)
-        alpha = alpha.astype(np.float32)
+        alpha = _field(seed, 4, n_layers, N, (H, d), _diag_gate, layers)
     else:
         raise ValueError("scalar_diag: family must be SCALAR or DIAG")
     return dict(family=family, dtype="bf16", q=q, k=k, v=v, alpha=alpha, beta=None,
                 seg_offsets=offs)
 
 
-def dense_stack(seg_len: int, n_layers: int = 30, H: int = 32, d: int = 128, seed: int = 2,
-                with_q: bool = False, n_seg: int = 1, lengths=None):
-    """Gated delta rule: bf16 q, v ~ N(0,1), k L2-normalised; fp32 alpha, beta."""
-    g = rng(seed)
+def _dense_alpha(g, shape):
+    return np.exp(-0.1 * _softplus(g.standard_normal(size=shape, dtype=np.float32))).astype(np.float32)
+
+
+def _dense_beta(g, shape):
+    return _sigmoid(g.standard_normal(size=shape, dtype=np.float32))
+
+
+def dense_stack(seg_len: int = 512, n_layers: int = 30, H: int = 32, d: int = 128, seed: int = 2,
+                with_q: bool = False, n_seg: int = 1, lengths=None, layers=None):
+    """Gated delta rule: bf16 q, v ~ N(0,1), k L2-normalised; fp32
+    alpha = exp(-0.1 softplus(N(0,1))), beta = sigmoid(N(0,1))."""
     if lengths is None:
         lengths = [seg_len] * n_seg
-    offs = np.concatenate([[0], np.cumsum(np.asarray(lengths, dtype=np.int64))]).astype(np.int64)
+    offs = _offsets(lengths)
     N = int(offs[-1])
-    k = bf16_round(_l2_rows(_normal(g, (n_layers, N, H, d))))
-    v = bf16_round(_normal(g, (n_layers, N, H, d)))
-    q = bf16_round(_normal(g, (n_layers, N, H, d))) if with_q else None
-    alpha = np.exp(-0.1 * _softplus(_normal(g, (n_layers, N, H)))).astype(np.float32)
-    beta = _sigmoid(_normal(g, (n_layers, N, H)))
+    k = _field(seed, 1, n_layers, N, (H, d), _unit_rows_bf16, layers)
+    v = _field(seed, 2, n_layers, N, (H, d), _normal_bf16, layers)
+    q = _field(seed, 3, n_layers, N, (H, d), _normal_bf16, layers) if with_q else None
+    alpha = _field(seed, 4, n_layers, N, (H,), _dense_alpha, layers)
+    beta = _field(seed, 5, n_layers, N, (H,), _dense_beta, layers)
     return dict(family=DENSE, dtype="bf16", q=q, k=k, v=v, alpha=alpha, beta=beta,
                 seg_offsets=offs)
 
@@ -162,10 +221,10 @@ def rag_pool(family: int, P: int = 200, n_layers: int = 30, H: int = 32, d: int 
         lam = -lengths[:, None, None, None] * g.uniform(0.005, 0.02, size=(P, n_layers, H, d))
     else:
         lam = -lengths[:, None, None] * g.uniform(0.05, 0.1, size=(P, n_layers, H))
-    S = _normal(g, (P, n_layers, H, d, d)) * np.float32(1.0 / np.sqrt(d))
+    S = g.standard_normal((P, n_layers, H, d, d), dtype=np.float32) * np.float32(1.0 / np.sqrt(d))
     out = dict(family=family, lengths=lengths, lam=lam.astype(np.float32), S=S)
     if family == DENSE:
-        out["M"] = _normal(g, (P, n_layers, H, d, d)) * np.float32(1.0 / np.sqrt(d))
+        out["M"] = g.standard_normal((P, n_layers, H, d, d), dtype=np.float32) * np.float32(1.0 / np.sqrt(d))
     return out
 
 

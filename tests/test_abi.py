@@ -1,0 +1,130 @@
+"""The C ABI without a GPU: the library builds for sm_103a, loads, exports
+every symbol ``include/hypic.h`` declares, and rejects bad arguments on the
+host with the documented status codes before touching the device.  Fake
+(never dereferenced) device addresses stand in for tensors here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "hypic.h")
+
+OK, EINVAL, EUNSUP, EALIGN = 0, -1, -2, -3
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from linear_attention_state_gated_gb300 import _build, library
+    _build.build()
+    return library()
+
+
+def declared_symbols():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(hypic_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for s in ("hypic_segment_scan", "hypic_compose", "hypic_compose_chain", "hypic_status_string"):
+        assert s in syms
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from linear_attention_state_gated_gb300 import SIGNATURES
+    for s in declared_symbols():
+        assert hasattr(lib, s), s
+        assert s in SIGNATURES, f"binding lacks a signature for {s}"
+
+
+def test_status_strings(lib):
+    for st in (0, -1, -2, -3, -4, -5, 7):
+        assert isinstance(lib.hypic_status_string(st), bytes)
+    assert lib.hypic_version() >= 100
+
+
+A = 0x10000          # fake 16-byte aligned device address (never dereferenced)
+
+
+def P(x):
+    return ctypes.c_void_p(x)
+
+
+def scan(lib, fam=0, dtype=0, L=1, S=2, N=64, H=2, dk=128, dv=128, offs=A, q=0, k=A, v=A,
+         alpha=A, beta=0, lam=A, M=0, Sout=A, o=0, err=0):
+    return lib.hypic_segment_scan(fam, dtype, L, S, N, H, dk, dv, P(offs), P(q or None),
+                                  P(k or None), P(v or None), P(alpha or None), P(beta or None),
+                                  P(lam or None), P(M or None), P(Sout or None), P(o or None),
+                                  P(err or None), P(None))
+
+
+def test_scan_rejects_bad_arguments(lib):
+    assert scan(lib, fam=3) == EINVAL
+    assert scan(lib, dtype=2) == EINVAL
+    assert scan(lib, dk=96) == EUNSUP
+    assert scan(lib, dv=256) == EUNSUP
+    assert scan(lib, H=0) == EINVAL
+    assert scan(lib, N=-1) == EINVAL
+    assert scan(lib, k=0) == EINVAL
+    assert scan(lib, alpha=0) == EINVAL
+    assert scan(lib, Sout=0) == EINVAL
+    assert scan(lib, fam=2, M=0) == EINVAL          # dense needs M_out
+    assert scan(lib, fam=0, M=A) == EINVAL          # scalar must not get M_out
+    assert scan(lib, o=A, q=0) == EINVAL            # o_t needs q
+    assert scan(lib, k=A + 8) == EALIGN
+    assert scan(lib, Sout=A + 4) == EALIGN
+    assert scan(lib, fam=1, alpha=A + 4) == EALIGN  # diag gates are 16-byte rows
+    assert scan(lib, offs=A + 4) == EALIGN
+    assert scan(lib, L=0) == OK                     # nothing to do: no launch
+    assert scan(lib, S=0) == OK
+
+
+def compose(lib, fam=0, n=3, H=2, dk=64, dv=64, lam=A, M=0, Sp=A, Sc=A + 0x100000,
+            So=A + 0x200000, lp=0, Mp=0, lo=0, Mo=0):
+    return lib.hypic_compose(fam, n, H, dk, dv, P(lam or None), P(M or None), P(Sp or None),
+                             P(Sc or None), P(So or None), P(lp or None), P(Mp or None),
+                             P(lo or None), P(Mo or None), P(None))
+
+
+def test_compose_rejects_bad_arguments(lib):
+    assert compose(lib, fam=5) == EINVAL
+    assert compose(lib, dk=48) == EUNSUP
+    assert compose(lib, lam=0) == EINVAL
+    assert compose(lib, Sc=0) == EINVAL
+    assert compose(lib, fam=2, M=0) == EINVAL
+    assert compose(lib, fam=0, M=A) == EINVAL
+    assert compose(lib, lp=A) == EINVAL              # lam_prev without lam_out
+    assert compose(lib, fam=2, M=A + 0x300000, lp=A, lo=A, Mp=0, Mo=A) == EINVAL
+    assert compose(lib, Sc=A + 0x100008) == EALIGN
+    assert compose(lib, So=A + 0x100000 + 64) == EINVAL  # S_out overlaps S_C
+    assert compose(lib, n=0) == OK
+
+
+def chain(lib, fam=0, R=2, L=2, H=2, dk=64, dv=64, mc=3, cl=A, idx=A, P_=5, pl=A, pM=0,
+          pS=A, Si=0, So=A, err=0):
+    return lib.hypic_compose_chain(fam, R, L, H, dk, dv, mc, P(cl or None), P(idx or None), P_,
+                                   P(pl or None), P(pM or None), P(pS or None), P(Si or None),
+                                   P(So or None), P(err or None), P(None))
+
+
+def test_chain_rejects_bad_arguments(lib):
+    assert chain(lib, fam=4) == EINVAL
+    assert chain(lib, dv=16) == EUNSUP
+    assert chain(lib, cl=0) == EINVAL
+    assert chain(lib, idx=0) == EINVAL
+    assert chain(lib, P_=0) == EINVAL
+    assert chain(lib, fam=2, pM=0) == EINVAL
+    assert chain(lib, pS=A + 4) == EALIGN
+    assert chain(lib, cl=A + 2) == EALIGN
+    assert chain(lib, R=0) == OK
+
+
+def test_python_binding_refuses_host_tensors():
+    import torch
+    import linear_attention_state_gated_gb300 as hy
+    k = torch.zeros(1, 4, 1, 32)
+    with pytest.raises(ValueError):
+        hy.segment_scan("scalar", k, k, torch.ones(1, 4, 1), torch.tensor([0, 4]))

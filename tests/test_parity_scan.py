@@ -1,0 +1,145 @@
+"""GPU segment scan against the fp64 oracle on the same seeded inputs.
+
+Small ragged cases are compared element by element over every (layer,
+segment, head); the full-size workloads run in the configuration the
+benchmark times and are compared on sampled (layer, segment, head) units the
+oracle computes one by one."""
+import numpy as np
+import pytest
+
+import oracle
+from helpers import TOL_F32, TOL_O_BF16, TOL_SCAN_BF16, rel_fro, t_err, to_dev, to_host
+from linear_attention_state_gated_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+SCALAR, DIAG, DENSE = wl.SCALAR, wl.DIAG, wl.DENSE
+
+
+def gpu_scan(w, want_o=False, d_err=None):
+    import linear_attention_state_gated_gb300 as hy
+    dt = w["dtype"]
+    return hy.segment_scan(w["family"], to_dev(w["k"], dt), to_dev(w["v"], dt),
+                           to_dev(w["alpha"]), to_dev(w["seg_offsets"]), beta=to_dev(w["beta"]),
+                           q=to_dev(w["q"], dt) if want_o else None, want_o=want_o, d_err=d_err)
+
+
+def host(out):
+    return {k: to_host(v) for k, v in out.items()}
+
+
+def check(fam, got, ref, tol, o_tol=None, seg_offsets=None):
+    e_s = rel_fro(got["S"], ref["S"])
+    e_t = t_err(fam, got["lam"], ref["lam"], got.get("M"), ref.get("M"))
+    assert e_s.max() <= tol, f"S error {e_s.max():.3e} > {tol}"
+    assert e_t.max() <= tol, f"T error {e_t.max():.3e} > {tol}"
+    if o_tol is not None:
+        # per (layer, segment, head): relative Frobenius over the segment's rows of o
+        go, ro = got["o"], ref["o"]
+        for s in range(len(seg_offsets) - 1):
+            a, b = seg_offsets[s], seg_offsets[s + 1]
+            if b > a:
+                e_o = rel_fro(np.moveaxis(go[:, a:b], 1, -2), np.moveaxis(ro[:, a:b], 1, -2))
+                assert e_o.max() <= o_tol, f"o error {e_o.max():.3e} (segment {s})"
+    return float(e_s.max()), float(e_t.max())
+
+
+def oracle_scan(w, want_o=False):
+    return oracle.segment_scan(w["family"], w["k"], w["v"], w["alpha"], w["seg_offsets"],
+                               beta=w["beta"], q=w["q"], want_o=want_o)
+
+
+def test_tiny_dense_fp32_scan_compose_vs_sequential():
+    """1 layer, 2 heads, d=32, two 64-token segments, fp32: scan both segments,
+    compose, and compare with the straight recurrence over 128 tokens."""
+    import linear_attention_state_gated_gb300 as hy
+    w = wl.tiny_dense(seed=0)
+    got = gpu_scan(w, want_o=True)
+    ref = oracle_scan(w, want_o=True)
+    check(DENSE, host(got), ref, TOL_F32, o_tol=TOL_F32, seg_offsets=w["seg_offsets"])
+    comp = hy.compose("dense", got["lam"][:, 1], got["S"][:, 1], S_prev=got["S"][:, 0].contiguous(),
+                      M=got["M"][:, 1].contiguous(), lam_prev=got["lam"][:, 0].contiguous(),
+                      M_prev=got["M"][:, 0].contiguous())
+    seq = oracle.sequential(DENSE, w["k"], w["v"], w["alpha"], w["beta"])
+    assert rel_fro(to_host(comp["S"]), seq["S"]).max() <= TOL_F32
+    assert t_err(DENSE, to_host(comp["lam"]), seq["lam"], to_host(comp["M"]), seq["M"]).max() <= TOL_F32
+
+
+RAGGED = [1, 0, 63, 64, 65, 300, 129, 2]
+
+
+@pytest.mark.parametrize("fam", [SCALAR, DIAG, DENSE], ids=["scalar", "diag", "dense"])
+@pytest.mark.parametrize("d", [32, 64, 128])
+def test_scan_ragged_all_units(fam, d):
+    """Ragged segments (empty, one token, tile edges, several tiles + tail), o_t."""
+    if fam == DENSE:
+        w = wl.dense_stack(lengths=RAGGED, n_layers=2, H=3, d=d, seed=7, with_q=True)
+    else:
+        w = wl.scalar_diag(fam, lengths=RAGGED, n_layers=2, H=3, d=d, seed=7, with_q=True)
+    got = host(gpu_scan(w, want_o=True))
+    ref = oracle_scan(w, want_o=True)
+    check(fam, got, ref, TOL_SCAN_BF16, o_tol=TOL_O_BF16, seg_offsets=w["seg_offsets"])
+    # the empty segment: lambda = 0, M = I, S = 0 exactly
+    assert np.all(got["S"][:, 1] == 0) and np.all(got["lam"][:, 1] == 0)
+    if fam == DENSE:
+        assert np.array_equal(got["M"][:, 1], np.broadcast_to(np.eye(d), got["M"][:, 1].shape))
+
+
+@pytest.mark.parametrize("fam", [SCALAR, DIAG], ids=["scalar", "diag"])
+@pytest.mark.parametrize("L", [512, 8192])
+def test_scalar_diag_full_size_sampled(fam, L):
+    """32 heads, d=128, batch of 8 segments of L tokens (the benchmark's launch)."""
+    w = wl.scalar_diag(fam, seg_len=L, n_seg=8)
+    got = host(gpu_scan(w))
+    rs = np.random.default_rng(L + fam)
+    for seg, h in [(0, 0), (7, 31)] + [tuple(x) for x in rs.integers([0, 0], [8, 32], size=(2, 2))]:
+        a, b = w["seg_offsets"][seg], w["seg_offsets"][seg + 1]
+        ref = oracle.sequential(fam, w["k"][:, a:b, h:h + 1], w["v"][:, a:b, h:h + 1],
+                                w["alpha"][:, a:b, h:h + 1])
+        sub = {"S": got["S"][:, seg, h:h + 1], "lam": got["lam"][:, seg, h:h + 1]}
+        check(fam, sub, ref, TOL_SCAN_BF16)
+
+
+@pytest.mark.parametrize("L", [512, 2048])
+def test_dense_full_stack_sampled(L):
+    """30 layers x 32 heads x 128, one segment per layer (the benchmark's launch)."""
+    w = wl.dense_stack(seg_len=L)
+    got = host(gpu_scan(w))
+    for l, h in [(0, 0), (29, 31), (13, 7)]:
+        ref = oracle.sequential(DENSE, w["k"][l:l + 1, :, h:h + 1], w["v"][l:l + 1, :, h:h + 1],
+                                w["alpha"][l:l + 1, :, h:h + 1], w["beta"][l:l + 1, :, h:h + 1])
+        sub = {"S": got["S"][l:l + 1, 0, h:h + 1], "lam": got["lam"][l:l + 1, 0, h:h + 1],
+               "M": got["M"][l:l + 1, 0, h:h + 1]}
+        check(DENSE, sub, ref, TOL_SCAN_BF16)
+
+
+@pytest.mark.parametrize("fam", [SCALAR, DIAG, DENSE], ids=["scalar", "diag", "dense"])
+def test_segment_independence_bitwise(fam):
+    """T_C and S(C|0) depend only on the segment's tokens: the same segment
+    alone or inside a batch at another offset gives identical bits."""
+    import torch
+    lens = [200, 77, 130]
+    mk = wl.dense_stack if fam == DENSE else (lambda **kw: wl.scalar_diag(fam, **kw))
+    w = mk(lengths=lens, n_layers=1, H=2, d=128, seed=11)
+    got = gpu_scan(w)
+    a, b = w["seg_offsets"][1], w["seg_offsets"][2]
+    alone = dict(w)
+    for key in ("k", "v", "alpha", "beta"):
+        if w[key] is not None:
+            alone[key] = np.ascontiguousarray(w[key][:, a:b])
+    alone["seg_offsets"] = np.array([0, b - a], dtype=np.int64)
+    g1 = gpu_scan(alone)
+    for key in g1:
+        assert torch.equal(g1[key][:, 0], got[key][:, 1]), key
+
+
+def test_bad_offsets_flag_error_without_fault():
+    """Offsets out of [0, N] are reported through d_err and the segment is treated as empty."""
+    import torch
+    w = wl.scalar_diag(SCALAR, lengths=[64, 64], n_layers=1, H=2, d=64, seed=3)
+    w["seg_offsets"] = np.array([0, 64, 1000], dtype=np.int64)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = gpu_scan(w, d_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == -5
+    assert torch.all(got["S"][:, 1] == 0)
