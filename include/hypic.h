@@ -59,7 +59,9 @@ typedef enum {
     HYPIC_EUNSUPPORTED = -2, /* head size or family/dtype combination not built */
     HYPIC_EALIGN = -3,       /* a pointer is not aligned as documented */
     HYPIC_ECUDA = -4,        /* a CUDA runtime call or kernel launch failed */
-    HYPIC_EINDEX = -5        /* device side: index out of range (written to d_err) */
+    HYPIC_EINDEX = -5,       /* device side: index out of range (written to d_err) */
+    HYPIC_ETIMEOUT = -6      /* device side: a pipeline wait gave up after ~2 s (written to d_err);
+                                the kernel left its outputs incomplete and released its resources */
 } hypic_status;
 
 typedef enum { HYPIC_SCALAR = 0, HYPIC_DIAG = 1, HYPIC_DENSE = 2 } hypic_family;

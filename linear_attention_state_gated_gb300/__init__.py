@@ -30,7 +30,7 @@ SCALAR, DIAG, DENSE = 0, 1, 2
 FAMILIES = {"scalar": SCALAR, "diag": DIAG, "dense": DENSE}
 BF16, F32 = 0, 1
 STATUS = {0: "HYPIC_OK", -1: "HYPIC_EINVAL", -2: "HYPIC_EUNSUPPORTED", -3: "HYPIC_EALIGN",
-          -4: "HYPIC_ECUDA", -5: "HYPIC_EINDEX"}
+          -4: "HYPIC_ECUDA", -5: "HYPIC_EINDEX", -6: "HYPIC_ETIMEOUT"}
 
 __all__ = ["segment_scan", "compose", "compose_chain", "status_string", "library",
            "HypicError", "SCALAR", "DIAG", "DENSE"]

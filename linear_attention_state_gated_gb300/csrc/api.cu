@@ -27,6 +27,7 @@ const char *hypic_status_string(int status) {
         case HYPIC_EALIGN: return "misaligned pointer";
         case HYPIC_ECUDA: return "CUDA error";
         case HYPIC_EINDEX: return "index out of range (device side)";
+        case HYPIC_ETIMEOUT: return "a device-side wait timed out";
     }
     return "unknown status";
 }
@@ -78,6 +79,7 @@ int hypic_segment_scan(int fam, int in_dtype, int n_layers, int n_seg, int64_t t
     a.o_out = o_out;
     a.d_err = d_err;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    if (hypic::scan_sd_tc_supported(a)) return from_cuda(hypic::launch_scan_sd_tc(a, s));
     return from_cuda(hypic::launch_scan_recurrent(a, s));
 }
 
@@ -108,14 +110,17 @@ int hypic_compose(int fam, int n, int n_heads, int d_k, int d_v, const float *la
         if (p && !aligned(p, 4)) return HYPIC_EALIGN;
     // S_out may be S_prev; any other overlap with an input is not supported
     const size_t sbytes = (size_t)n * n_heads * d_k * d_v * sizeof(float);
-    auto overlaps = [](const void *x, const void *y, size_t bytes) {
+    const size_t mbytes = (size_t)n * n_heads * d_k * d_k * sizeof(float);
+    auto overlaps = [](const void *x, size_t xb, const void *y, size_t yb) {
         if (!x || !y) return false;
         const char *a = static_cast<const char *>(x), *b = static_cast<const char *>(y);
-        return a < b + bytes && b < a + bytes;
+        return a < b + yb && b < a + xb;
     };
-    if (overlaps(S_out, S_C, sbytes) && S_out != S_C) return HYPIC_EINVAL;
-    if (S_prev && S_out != S_prev && overlaps(S_out, S_prev, sbytes)) return HYPIC_EINVAL;
-    if (fam == HYPIC_DENSE && (overlaps(S_out, M, sbytes) || overlaps(S_out, M_prev, sbytes)))
+    if (S_out != S_C && overlaps(S_out, sbytes, S_C, sbytes)) return HYPIC_EINVAL;
+    if (S_prev && S_out != S_prev && overlaps(S_out, sbytes, S_prev, sbytes)) return HYPIC_EINVAL;
+    if (fam == HYPIC_DENSE &&
+        (overlaps(S_out, sbytes, M, mbytes) || overlaps(S_out, sbytes, M_prev, mbytes) ||
+         overlaps(M_out, mbytes, M, mbytes) || overlaps(M_out, mbytes, M_prev, mbytes)))
         return HYPIC_EINVAL;
 
     hypic::ComposeArgs a;

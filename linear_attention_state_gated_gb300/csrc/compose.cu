@@ -212,6 +212,7 @@ __global__ void __launch_bounds__(256) chain_sd_kernel(const ChainArgs a) {
         const int j = tid + i * 256;
         s[i] = (init && j < per4) ? init[j] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    __shared__ float row_scale[2][128];   // exp(lambda_row) of the current step, double-buffered
     const int n = clamp_len(a, r);
     for (int c = 0; c < n; ++c) {
         const int p = clamp_idx(a, r, c);
@@ -229,11 +230,13 @@ __global__ void __launch_bounds__(256) chain_sd_kernel(const ChainArgs a) {
             for (int i = 0; i < MAXV; ++i)
                 if (tid + i * 256 < per4) s[i] = axpy4(sc, s[i], x[i]);
         } else {
-            const float *lp = a.pool_lam + e * DK;
+            float *rs = row_scale[c & 1];
+            if (tid < DK) rs[tid] = expf(a.pool_lam[e * DK + tid]);
+            __syncthreads();
 #pragma unroll
             for (int i = 0; i < MAXV; ++i) {
                 const int j = tid + i * 256;
-                if (j < per4) s[i] = axpy4(expf(lp[j >> row4_shift]), s[i], x[i]);
+                if (j < per4) s[i] = axpy4(rs[j >> row4_shift], s[i], x[i]);
             }
         }
     }

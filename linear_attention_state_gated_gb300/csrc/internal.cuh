@@ -42,6 +42,10 @@ struct ChainArgs {
 // Token-by-token fp32 recurrence on CUDA cores, every family, optional o_t.
 cudaError_t launch_scan_recurrent(const ScanArgs &a, cudaStream_t s);
 
+// Scalar / diagonal scan on tcgen05 tensor cores (bf16 inputs, d_k = d_v = 128, no o_t).
+bool scan_sd_tc_supported(const ScanArgs &a);
+cudaError_t launch_scan_sd_tc(const ScanArgs &a, cudaStream_t s);
+
 cudaError_t launch_compose(const ComposeArgs &a, cudaStream_t s);
 cudaError_t launch_compose_chain(const ChainArgs &a, cudaStream_t s);
 

@@ -85,6 +85,37 @@ def test_scan_ragged_all_units(fam, d):
         assert np.array_equal(got["M"][:, 1], np.broadcast_to(np.eye(d), got["M"][:, 1].shape))
 
 
+@pytest.mark.parametrize("fam", [SCALAR, DIAG, DENSE], ids=["scalar", "diag", "dense"])
+def test_scan_ragged_state_only(fam):
+    """d = 128, no o_t (the tensor-core path for scalar/diag): ragged segments
+    including empty, one-token, chunk-edge and multi-chunk-plus-tail lengths."""
+    lens = RAGGED + [31, 32, 33, 127, 128, 129, 1000]
+    if fam == DENSE:
+        w = wl.dense_stack(lengths=lens, n_layers=2, H=3, d=128, seed=8)
+    else:
+        w = wl.scalar_diag(fam, lengths=lens, n_layers=2, H=3, d=128, seed=8)
+    got = host(gpu_scan(w))
+    ref = oracle_scan(w)
+    check(fam, got, ref, TOL_SCAN_BF16)
+    assert np.all(got["S"][:, 1] == 0) and np.all(got["lam"][:, 1] == 0)
+
+
+def test_scan_with_beta_and_mamba_like_gates():
+    """Scalar gates that vary per token and a write scale beta (Mamba2-style),
+    including strong decays; diagonal gates with beta."""
+    import linear_attention_state_gated_gb300 as hy
+    g = np.random.default_rng(12)
+    lens = [300, 77, 0, 640]
+    for fam in (SCALAR, DIAG):
+        w = wl.scalar_diag(fam, lengths=lens, n_layers=1, H=4, d=128, seed=9)
+        shape = w["alpha"].shape
+        w["alpha"] = np.exp(-g.exponential(0.5, size=shape)).astype(np.float32)
+        w["beta"] = g.uniform(0.0, 2.0, size=w["k"].shape[:3]).astype(np.float32)
+        got = host(gpu_scan(w))
+        ref = oracle_scan(w)
+        check(fam, got, ref, TOL_SCAN_BF16)
+
+
 @pytest.mark.parametrize("fam", [SCALAR, DIAG], ids=["scalar", "diag"])
 @pytest.mark.parametrize("L", [512, 8192])
 def test_scalar_diag_full_size_sampled(fam, L):
