@@ -32,7 +32,7 @@ BF16, F32 = 0, 1
 STATUS = {0: "HYPIC_OK", -1: "HYPIC_EINVAL", -2: "HYPIC_EUNSUPPORTED", -3: "HYPIC_EALIGN",
           -4: "HYPIC_ECUDA", -5: "HYPIC_EINDEX", -6: "HYPIC_ETIMEOUT"}
 
-__all__ = ["segment_scan", "compose", "compose_chain", "status_string", "library",
+__all__ = ["segment_scan", "compose", "compose_chain", "status_string", "library", "use_library",
            "HypicError", "SCALAR", "DIAG", "DENSE"]
 
 
@@ -76,6 +76,16 @@ def library(path: str | None = None):
                 return lib
             _lib = lib
     return _lib
+
+
+def use_library(path: str):
+    """Route every call of this module to the library at `path` (another build
+    of libhypic, e.g. with different tile sizes); returns the handle."""
+    global _lib
+    lib = library(path)
+    with _lock:
+        _lib = lib
+    return lib
 
 
 def status_string(status: int) -> str:

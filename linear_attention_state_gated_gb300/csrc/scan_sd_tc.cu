@@ -41,15 +41,17 @@ struct SdCfg {
     static constexpr int BOX = C * 128;                    // 64 channels x C tokens, bf16
     static constexpr int TILE = 2 * BOX;                   // 128 channels
     static constexpr int ATILE = FAM == HYPIC_DIAG ? C * 512 : 0;   // fp32 gates
-    static constexpr int STAGE = 3 * TILE + ATILE;         // K (-> K~hi), K~lo, V, gates
-    static constexpr uint32_t TX = 2 * TILE + ATILE;       // bytes TMA brings per stage
-    static constexpr int SMEM = NS * STAGE + 2048;         // + control block + alignment slack
+    static constexpr int STAGE = 2 * TILE + ATILE;         // TMA ring stage: K (-> K~hi), V, gates
+    static constexpr uint32_t TX = STAGE;                  // bytes TMA brings per stage
+    static constexpr int LO = NS * STAGE;                  // two K~lo tiles (chunk parity) after the ring
+    static constexpr int SMEM = NS * STAGE + 2 * TILE + 2048;   // + control block + alignment slack
     static_assert(C == 32 || C == 64, "chunk of 32 or 64 tokens");
+    static_assert(NS >= 2 && NS <= 8, "2 to 8 stages");
     static_assert(STAGE % 1024 == 0, "stages stay 1024-byte aligned");
 };
 
 struct SdCtrl {
-    uint64_t full[4], ready[4], empty[4], accf;
+    uint64_t full[8], ready[8], empty[8], lofree[2], accf;
     float rowf[2][64];
     uint32_t tmem;
     int abort;
@@ -94,7 +96,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
-    SdCtrl *ctl = reinterpret_cast<SdCtrl *>(smem + NS * Cfg::STAGE);
+    SdCtrl *ctl = reinterpret_cast<SdCtrl *>(smem + Cfg::LO + 2 * Cfg::TILE);
     volatile int *abortp = &ctl->abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -115,6 +117,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&ctl->ready[s], 4);
             mbar_init(&ctl->empty[s], 1);
         }
+        mbar_init(&ctl->lofree[0], 1);
+        mbar_init(&ctl->lofree[1], 1);
         mbar_init(&ctl->accf, 1);
         ctl->abort = 0;
         mbar_fence_init();
@@ -146,9 +150,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_expect_tx(&ctl->full[s], Cfg::TX);
                 tma_load_3d(st, &tm_k, &ctl->full[s], 0, h, row);
                 tma_load_3d(st + Cfg::BOX, &tm_k, &ctl->full[s], 64, h, row);
-                tma_load_3d(st + 2 * Cfg::TILE, &tm_v, &ctl->full[s], 0, h, row);
-                tma_load_3d(st + 2 * Cfg::TILE + Cfg::BOX, &tm_v, &ctl->full[s], 64, h, row);
-                if (kDiag) tma_load_3d(st + 3 * Cfg::TILE, &tm_a, &ctl->full[s], 0, h, row);
+                tma_load_3d(st + Cfg::TILE, &tm_v, &ctl->full[s], 0, h, row);
+                tma_load_3d(st + Cfg::TILE + Cfg::BOX, &tm_v, &ctl->full[s], 64, h, row);
+                if (kDiag) tma_load_3d(st + 2 * Cfg::TILE, &tm_a, &ctl->full[s], 0, h, row);
                 issued = j + 1;
             }
             if (*abortp) {   // let copies already in flight land before the CTA leaves
@@ -169,7 +173,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t kb = smem_addr(smem + s * Cfg::STAGE);
-                const uint32_t lb = kb + Cfg::TILE, vb = kb + 2 * Cfg::TILE;
+                const uint32_t vb = kb + Cfg::TILE;
+                const uint32_t lb = smem_addr(smem + Cfg::LO + (j & 1) * Cfg::TILE);
 #pragma unroll
                 for (int ks = 0; ks < C / 16; ++ks) {
                     const uint32_t off = (uint32_t)ks * 2048u;   // 16 tokens = two 8-row groups
@@ -178,6 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_f16(tmem, smem_desc_sw128(lb + off, Cfg::BOX, 1024), bd, idesc, 1u);
                 }
                 mma_commit(&ctl->empty[s]);
+                mma_commit(&ctl->lofree[j & 1]);
             }
             if (nc > 0) {
                 mma_commit(&ctl->accf);
@@ -237,13 +243,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (j + 1 < nc) prefetch(j + 1);
             }
-            const bool ok = mbar_wait(&ctl->full[s], ph) && !*abortp;
+            const bool ok = mbar_wait(&ctl->full[s], ph) &&
+                            mbar_wait(&ctl->lofree[par], ((uint32_t)(j >> 1) & 1u) ^ 1u) && !*abortp;
             if (!bar_and(1, 128, ok)) {
                 *abortp = 1;
                 break;
             }
             uint8_t *kt = smem + s * Cfg::STAGE;
-            uint8_t *lo = kt + Cfg::TILE;
+            uint8_t *lo = smem + Cfg::LO + par * Cfg::TILE;
             if (!kDiag) {
 #pragma unroll 4
                 for (int i = 0; i < 16 * C / 128; ++i) {
@@ -256,26 +263,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *reinterpret_cast<uint4 *>(lo + q * 16) = lw;
                 }
             } else {
-                const float *at = reinterpret_cast<const float *>(kt + 3 * Cfg::TILE);
+                const float *at = reinterpret_cast<const float *>(kt + 2 * Cfg::TILE);
                 const int box = ti >> 6, ci = ti & 63, c16 = ci >> 3, within = ci & 7;
-                for (int r = C - 1; r >= 0; --r) {
-                    const int off = box * Cfg::BOX + r * 128 + (((c16 ^ (r & 7)) << 4) | (within << 1));
-                    __nv_bfloat16 *kp = reinterpret_cast<__nv_bfloat16 *>(kt + off);
-                    __nv_bfloat16 *lp = reinterpret_cast<__nv_bfloat16 *>(lo + off);
-                    if (tbase + r < t0) {   // before the segment: contributes nothing
-                        *kp = __float2bfloat16_rn(0.f);
-                        *lp = __float2bfloat16_rn(0.f);
-                        continue;
+                const float *rf = ctl->rowf[par];
+                // rows in groups of 8, last row first: all loads of a group are
+                // issued before the sequential product over its rows
+#pragma unroll
+                for (int g = C / 8 - 1; g >= 0; --g) {
+                    float av[8], kv[8];
+                    int offs[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int r = 8 * g + u;
+                        offs[u] = box * Cfg::BOX + r * 128 + (((c16 ^ (r & 7)) << 4) | (within << 1));
+                        av[u] = at[r * 128 + ti];
+                        kv[u] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(kt + offs[u]));
                     }
-                    const float x = ctl->rowf[par][r] * (m * scale) * __bfloat162float(*kp);
-                    const __nv_bfloat16 xh = __float2bfloat16_rn(x);
-                    *kp = xh;
-                    *lp = __float2bfloat16_rn(x - __bfloat162float(xh));
-                    m *= at[r * 128 + ti];
-                    if (m < 0x1p-60f) {
-                        m *= 0x1p64f;
-                        E -= 64;
-                        scale = pow2f(E);
+#pragma unroll
+                    for (int u = 7; u >= 0; --u) {
+                        const int r = 8 * g + u;
+                        const bool v = tbase + r >= t0;          // rows before the segment add nothing
+                        const float x = rf[r] * (m * scale) * kv[u];   // rf = beta (0 outside)
+                        const __nv_bfloat16 xh = __float2bfloat16_rn(x);
+                        *reinterpret_cast<__nv_bfloat16 *>(kt + offs[u]) = xh;
+                        *reinterpret_cast<__nv_bfloat16 *>(lo + offs[u]) =
+                            __float2bfloat16_rn(x - __bfloat162float(xh));
+                        m *= v ? av[u] : 1.f;
+                        if (m < 0x1p-60f) {
+                            m *= 0x1p64f;
+                            E -= 64;
+                            scale = pow2f(E);
+                        }
                     }
                 }
             }
@@ -396,10 +414,23 @@ bool scan_sd_tc_supported(const ScanArgs &a) {
            encode_fn() != nullptr;
 }
 
+#ifndef HYPIC_SD_SCALAR_C
+#define HYPIC_SD_SCALAR_C 64
+#endif
+#ifndef HYPIC_SD_SCALAR_NS
+#define HYPIC_SD_SCALAR_NS 2
+#endif
+#ifndef HYPIC_SD_DIAG_C
+#define HYPIC_SD_DIAG_C 32
+#endif
+#ifndef HYPIC_SD_DIAG_NS
+#define HYPIC_SD_DIAG_NS 2
+#endif
+
 cudaError_t launch_scan_sd_tc(const ScanArgs &a, cudaStream_t s) {
     if ((int64_t)a.n_layers * a.n_seg * a.H == 0) return cudaSuccess;
-    if (a.fam == HYPIC_SCALAR) return launch_tc<HYPIC_SCALAR, 64, 2>(a, s);
-    return launch_tc<HYPIC_DIAG, 32, 2>(a, s);
+    if (a.fam == HYPIC_SCALAR) return launch_tc<HYPIC_SCALAR, HYPIC_SD_SCALAR_C, HYPIC_SD_SCALAR_NS>(a, s);
+    return launch_tc<HYPIC_DIAG, HYPIC_SD_DIAG_C, HYPIC_SD_DIAG_NS>(a, s);
 }
 
 }  // namespace hypic
