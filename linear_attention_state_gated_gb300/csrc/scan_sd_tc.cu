@@ -11,16 +11,21 @@
 // transition is lambda = sum_t log alpha_t (log alpha per channel for diag).
 //
 // Per CTA one (layer, segment, head) chain, d_k = d_v = 128:
-//   warp 0     TMA producer: K, V (and the diagonal gates) of a chunk of C
-//              tokens into a ring of NS shared-memory stages (128B swizzle);
-//   warps 2-5  weight the keys: K~ = w * beta * k, split exactly into
-//              bf16 hi + lo (K~ - hi), written over K / into a lo tile in the
-//              same swizzled positions; later the epilogue (TMEM -> S);
-//   warp 1     one thread issues tcgen05.mma: D[128x128] += K~hi^T V + K~lo^T V
-//              (both operands MN-major, M = key channel, N = value channel,
-//              K = token), commits each stage back to the producer.
+//   warp 0       TMA producer: K, V (and the diagonal gates) of a chunk of C
+//                tokens into a ring of NS shared-memory stages (128B swizzle);
+//   warps 2..    TW "weighting" warps: K~ = w * beta * k, split exactly into
+//                bf16 hi + lo (K~ - hi), hi written over K, lo into a separate
+//                tile, same swizzled positions; at the end the epilogue
+//                (TMEM -> S rows);
+//   warp 1       one thread issues tcgen05.mma: D[128x128] += K~hi^T V + K~lo^T V
+//                (both operands MN-major, M = key channel, N = value channel,
+//                K = token) and commits each stage back to the producer.
 // V is used exactly (bf16 input); the hi/lo split keeps K~ to ~2^-17 relative.
-// Every wait is time-bounded; a timeout is reported as HYPIC_ETIMEOUT.
+// Scalar gates: per-token log alpha, suffix sums by warp shuffles, Kahan-summed
+// lambda.  Diagonal gates: per channel, the running product of later gates
+// (underflow to 0 is the right limit for a weight); lambda from the logs of
+// products over groups of rows.  Every wait is time-bounded; a timeout is
+// reported as HYPIC_ETIMEOUT.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -33,29 +38,42 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kThreads = 192;
 constexpr int kTmemCols = 128;
 
-template <int FAM, int C, int NS>
+template <int FAM, int C, int NS, int TW>
 struct SdCfg {
+    static constexpr int THREADS = 64 + 32 * TW;
+    static constexpr int WT = 32 * TW;                     // weighting threads
     static constexpr int BOX = C * 128;                    // 64 channels x C tokens, bf16
     static constexpr int TILE = 2 * BOX;                   // 128 channels
     static constexpr int ATILE = FAM == HYPIC_DIAG ? C * 512 : 0;   // fp32 gates
     static constexpr int STAGE = 2 * TILE + ATILE;         // TMA ring stage: K (-> K~hi), V, gates
     static constexpr uint32_t TX = STAGE;                  // bytes TMA brings per stage
     static constexpr int LO = NS * STAGE;                  // two K~lo tiles (chunk parity) after the ring
-    static constexpr int SMEM = NS * STAGE + 2 * TILE + 2048;   // + control block + alignment slack
+    static constexpr int NG = WT / 64;                     // diag: row groups (64 channel pairs each)
+    static constexpr int RPG = C / NG;                     // diag: rows per group
     static_assert(C == 32 || C == 64, "chunk of 32 or 64 tokens");
     static_assert(NS >= 2 && NS <= 8, "2 to 8 stages");
+    static_assert(TW == 4 || TW == 8, "4 or 8 weighting warps");
     static_assert(STAGE % 1024 == 0, "stages stay 1024-byte aligned");
+    static_assert((16 * C) % WT == 0, "whole 16-byte chunks per thread");
 };
 
 struct SdCtrl {
     uint64_t full[8], ready[8], empty[8], lofree[2], accf;
-    float rowf[2][64];
+    float rowf[2][64];          // per-row factor of the chunk (weight * beta, or beta)
+    float2 gprod[2][4][64];     // diag: gate product of each row group per channel pair
+    float2 lamp[4][64];         // diag: per-group partial lambda
     uint32_t tmem;
     int abort;
 };
+
+// ring + two lo tiles + control block + slack for the 1024-byte alignment
+template <int FAM, int C, int NS, int TW>
+constexpr int sd_smem_bytes() {
+    using Cfg = SdCfg<FAM, C, NS, TW>;
+    return Cfg::LO + 2 * Cfg::TILE + (int)sizeof(SdCtrl) + 1024;
+}
 
 __device__ __forceinline__ float warp_suffix_incl(float x, int lane) {
 #pragma unroll
@@ -66,32 +84,46 @@ __device__ __forceinline__ float warp_suffix_incl(float x, int lane) {
     return x;
 }
 
+__device__ __forceinline__ uint32_t bf2_bits(__nv_bfloat162 v) { return *reinterpret_cast<uint32_t *>(&v); }
+
+// Two fp32 values -> bf16 hi pair and bf16 lo pair (x = hi + lo to ~2^-17 relative).
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    const __nv_bfloat162 hh = __floats2bfloat162_rn(x0, x1);
+    const __nv_bfloat162 ll = __floats2bfloat162_rn(x0 - __low2float(hh), x1 - __high2float(hh));
+    hi = bf2_bits(hh);
+    lo = bf2_bits(ll);
+}
+
 __device__ __forceinline__ void split8(const uint4 raw, const float w, uint4 &hi, uint4 &lo) {
     const uint32_t in[4] = {raw.x, raw.y, raw.z, raw.w};
     uint32_t h[4], l[4];
 #pragma unroll
-    for (int p = 0; p < 4; ++p) {
-        const float x0 = __uint_as_float(in[p] << 16) * w;
-        const float x1 = __uint_as_float(in[p] & 0xFFFF0000u) * w;
-        const __nv_bfloat162 hh = __floats2bfloat162_rn(x0, x1);
-        const float r0 = x0 - __low2float(hh), r1 = x1 - __high2float(hh);
-        const __nv_bfloat162 ll = __floats2bfloat162_rn(r0, r1);
-        h[p] = *reinterpret_cast<const uint32_t *>(&hh);
-        l[p] = *reinterpret_cast<const uint32_t *>(&ll);
-    }
+    for (int p = 0; p < 4; ++p)
+        split2(__uint_as_float(in[p] << 16) * w, __uint_as_float(in[p] & 0xFFFF0000u) * w, h[p], l[p]);
     hi = make_uint4(h[0], h[1], h[2], h[3]);
     lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
-__device__ __forceinline__ float pow2f(int e) {   // 2^e, 0 below the normal range
-    return e < -126 ? 0.f : __int_as_float((e + 127) << 23);
+__device__ __forceinline__ void kahan(float &sum, float &comp, float v) {
+    const float y = v - comp;
+    const float t = sum + y;
+    comp = (t - sum) - y;
+    sum = t;
 }
 
-template <int FAM, int C, int NS>
-__global__ void __launch_bounds__(kThreads, 1)
+// log of a product of gates; exact fallback when the product left the normal range
+__device__ __forceinline__ float log_group(float prod, const float *a, int n, int stride) {
+    if (prod >= 0x1p-100f) return logf(prod);
+    float s = 0.f;
+    for (int i = 0; i < n; ++i) s += logf(a[i * stride]);
+    return s;
+}
+
+template <int FAM, int C, int NS, int TW>
+__global__ void __launch_bounds__(SdCfg<FAM, C, NS, TW>::THREADS, 2)
     scan_sd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_a, const ScanArgs a) {
-    using Cfg = SdCfg<FAM, C, NS>;
+    using Cfg = SdCfg<FAM, C, NS, TW>;
     constexpr bool kDiag = FAM == HYPIC_DIAG;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -114,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (bad) flag_index_error(a.d_err);
         for (int s = 0; s < NS; ++s) {
             mbar_init(&ctl->full[s], 1);
-            mbar_init(&ctl->ready[s], 4);
+            mbar_init(&ctl->ready[s], TW);
             mbar_init(&ctl->empty[s], 1);
         }
         mbar_init(&ctl->lofree[0], 1);
@@ -122,13 +154,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&ctl->accf, 1);
         ctl->abort = 0;
         mbar_fence_init();
-    }
-    if (warp == 1) tmem_alloc(&ctl->tmem, kTmemCols);
-    if (threadIdx.x == 32 * 0) {
         tma_prefetch(&tm_k);
         tma_prefetch(&tm_v);
         if (kDiag) tma_prefetch(&tm_a);
     }
+    if (warp == 1) tmem_alloc(&ctl->tmem, kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -192,13 +222,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ key weighting
-        const int ti = threadIdx.x - 64;   // 0..127
+        const int ti = threadIdx.x - 64;   // 0 .. WT-1
         const float *beta = a.beta;
         // scalar: running log-sum of the gates of tokens after the current chunk
         float rend = 0.f, rcomp = 0.f;
-        // diag: running product of later gates for channel ti, as m * 2^E
-        float m = 1.f, scale = 1.f;
-        int E = 0;
+        // diag: thread owns channel pair cp (channels 2cp, 2cp+1) and row group rg
+        const int cp = ti & 63, rg = ti >> 6;
+        float2 m = make_float2(1.f, 1.f);           // product of the gates after the chunk
+        float2 lam = make_float2(0.f, 0.f), lamc = make_float2(0.f, 0.f);
         constexpr int Q = C / 32;
         float pa[Q], pb[Q];
         auto prefetch = [&](int j) {
@@ -232,11 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
 #pragma unroll
                     for (int q = 0; q < Q; ++q) ctl->rowf[par][lane + 32 * q] = pb[q] * expf(rend + ex[q]);
-                    // Kahan-compensated running sum of the chunk totals
-                    const float y = later - rcomp;
-                    const float t = rend + y;
-                    rcomp = (t - rend) - y;
-                    rend = t;
+                    kahan(rend, rcomp, later);
                 } else {
 #pragma unroll
                     for (int q = 0; q < Q; ++q) ctl->rowf[par][lane + 32 * q] = pb[q];
@@ -245,56 +272,66 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const bool ok = mbar_wait(&ctl->full[s], ph) &&
                             mbar_wait(&ctl->lofree[par], ((uint32_t)(j >> 1) & 1u) ^ 1u) && !*abortp;
-            if (!bar_and(1, 128, ok)) {
+            if (!bar_and(1, Cfg::WT, ok)) {
                 *abortp = 1;
                 break;
             }
             uint8_t *kt = smem + s * Cfg::STAGE;
             uint8_t *lo = smem + Cfg::LO + par * Cfg::TILE;
+            const float *rf = ctl->rowf[par];
             if (!kDiag) {
-#pragma unroll 4
-                for (int i = 0; i < 16 * C / 128; ++i) {
-                    const int q = ti + 128 * i;             // 16-byte chunk index over both boxes
+#pragma unroll
+                for (int i = 0; i < 16 * C / Cfg::WT; ++i) {
+                    const int q = ti + Cfg::WT * i;          // 16-byte chunk index over both boxes
                     const int row = (q >> 3) & (C - 1);
-                    const float w = ctl->rowf[par][row];
                     uint4 hi, lw;
-                    split8(*reinterpret_cast<const uint4 *>(kt + q * 16), w, hi, lw);
+                    split8(*reinterpret_cast<const uint4 *>(kt + q * 16), rf[row], hi, lw);
                     *reinterpret_cast<uint4 *>(kt + q * 16) = hi;
                     *reinterpret_cast<uint4 *>(lo + q * 16) = lw;
                 }
             } else {
                 const float *at = reinterpret_cast<const float *>(kt + 2 * Cfg::TILE);
-                const int box = ti >> 6, ci = ti & 63, c16 = ci >> 3, within = ci & 7;
-                const float *rf = ctl->rowf[par];
-                // rows in groups of 8, last row first: all loads of a group are
-                // issued before the sequential product over its rows
+                const int box = cp >> 5, c16 = (cp >> 2) & 7, within = (cp & 3) << 2;
+                const int r0 = rg * Cfg::RPG;
+                float2 av[Cfg::RPG];
+                float2 gp = make_float2(1.f, 1.f);
 #pragma unroll
-                for (int g = C / 8 - 1; g >= 0; --g) {
-                    float av[8], kv[8];
-                    int offs[8];
+                for (int u = 0; u < Cfg::RPG; ++u) {
+                    const int r = r0 + u;
+                    const bool v = tbase + r >= t0;          // rows before the segment: gate 1
+                    const float2 x = *reinterpret_cast<const float2 *>(at + r * 128 + 2 * cp);
+                    av[u] = v ? x : make_float2(1.f, 1.f);
+                    gp.x *= av[u].x;
+                    gp.y *= av[u].y;
+                }
+                ctl->gprod[par][rg][cp] = gp;
+                bar_sync(2, Cfg::WT);
+                float2 ms = m;                               // start: product over later groups
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const int r = 8 * g + u;
-                        offs[u] = box * Cfg::BOX + r * 128 + (((c16 ^ (r & 7)) << 4) | (within << 1));
-                        av[u] = at[r * 128 + ti];
-                        kv[u] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(kt + offs[u]));
+                for (int g = Cfg::NG - 1; g >= 0; --g) {
+                    const float2 p = ctl->gprod[par][g][cp];
+                    if (g > rg) {
+                        ms.x *= p.x;
+                        ms.y *= p.y;
                     }
+                    m.x *= p.x;
+                    m.y *= p.y;
+                }
+                kahan(lam.x, lamc.x, log_group(gp.x, &av[0].x, Cfg::RPG, 2));
+                kahan(lam.y, lamc.y, log_group(gp.y, &av[0].y, Cfg::RPG, 2));
 #pragma unroll
-                    for (int u = 7; u >= 0; --u) {
-                        const int r = 8 * g + u;
-                        const bool v = tbase + r >= t0;          // rows before the segment add nothing
-                        const float x = rf[r] * (m * scale) * kv[u];   // rf = beta (0 outside)
-                        const __nv_bfloat16 xh = __float2bfloat16_rn(x);
-                        *reinterpret_cast<__nv_bfloat16 *>(kt + offs[u]) = xh;
-                        *reinterpret_cast<__nv_bfloat16 *>(lo + offs[u]) =
-                            __float2bfloat16_rn(x - __bfloat162float(xh));
-                        m *= v ? av[u] : 1.f;
-                        if (m < 0x1p-60f) {
-                            m *= 0x1p64f;
-                            E -= 64;
-                            scale = pow2f(E);
-                        }
-                    }
+                for (int u = Cfg::RPG - 1; u >= 0; --u) {
+                    const int r = r0 + u;
+                    const int off = box * Cfg::BOX + r * 128 + (((c16 ^ (r & 7)) << 4) | within);
+                    const uint32_t kk = *reinterpret_cast<const uint32_t *>(kt + off);
+                    const float f = rf[r];                   // beta, 0 outside the segment
+                    uint32_t hi, lw;
+                    split2(f * ms.x * __uint_as_float(kk << 16), f * ms.y * __uint_as_float(kk & 0xFFFF0000u),
+                           hi, lw);
+                    *reinterpret_cast<uint32_t *>(kt + off) = hi;
+                    *reinterpret_cast<uint32_t *>(lo + off) = lw;
+                    ms.x *= av[u].x;
+                    ms.y *= av[u].y;
                 }
             }
             fence_async_smem();
@@ -304,16 +341,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // ------------------------------------------------------------ epilogue
         const int64_t u_out = ((int64_t)l * a.n_seg + seg) * a.H + h;
-        if (!*abortp) {
+        if (bar_and(1, Cfg::WT, !*abortp)) {   // uniform over the weighting warps
             bool ok = true;
             if (nc > 0) ok = mbar_wait(&ctl->accf, 0);
             ok = __all_sync(0xffffffffu, ok);
             tc_fence_after();
             const int quarter = warp & 3;               // TMEM lanes this warp may read
             const int row = quarter * 32 + lane;        // key channel = accumulator row
+            constexpr int kCbPerWarp = 4 / (TW / 4);    // 32-column blocks per warp
+            const int cb0 = ((warp - 2) >> 2) * kCbPerWarp;
             float *So = a.S_out + u_out * 128 * 128 + (int64_t)row * 128;
 #pragma unroll 1
-            for (int cb = 0; cb < 4; ++cb) {
+            for (int cb = cb0; cb < cb0 + kCbPerWarp; ++cb) {
                 uint32_t r[32];
                 if (nc > 0 && ok) {
                     tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(cb * 32), r);
@@ -330,8 +369,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) *abortp = 1;
             if (kDiag) {
-                const double lam = (double)logf(m) + (double)E * 0.69314718055994530942;
-                a.lam_out[u_out * 128 + ti] = (float)lam;
+                ctl->lamp[rg][cp] = make_float2(lam.x - lamc.x, lam.y - lamc.y);
+                bar_sync(2, Cfg::WT);
+                if (rg == 0) {
+                    double lx = 0.0, ly = 0.0;
+                    for (int g = 0; g < Cfg::NG; ++g) {
+                        lx += (double)ctl->lamp[g][cp].x;
+                        ly += (double)ctl->lamp[g][cp].y;
+                    }
+                    reinterpret_cast<float2 *>(a.lam_out + u_out * 128)[cp] = make_float2((float)lx, (float)ly);
+                }
             } else if (ti == 0) {
                 a.lam_out[u_out] = (float)((double)rend - (double)rcomp);
             }
@@ -381,9 +428,9 @@ bool make_map(CUtensorMap *m, CUtensorMapDataType dt, int esize, const void *bas
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int FAM, int C, int NS>
+template <int FAM, int C, int NS, int TW>
 cudaError_t launch_tc(const ScanArgs &a, cudaStream_t s) {
-    using Cfg = SdCfg<FAM, C, NS>;
+    using Cfg = SdCfg<FAM, C, NS, TW>;
     const uint64_t rows = (uint64_t)a.n_layers * (uint64_t)a.N;
     CUtensorMap mk, mv, ma;
     if (!make_map(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.k, 128, a.H, rows, 64, C,
@@ -398,11 +445,12 @@ cudaError_t launch_tc(const ScanArgs &a, cudaStream_t s) {
     } else {
         ma = mk;   // unused
     }
-    auto kern = scan_sd_tc_kernel<FAM, C, NS>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+    auto kern = scan_sd_tc_kernel<FAM, C, NS, TW>;
+    constexpr int smem = sd_smem_bytes<FAM, C, NS, TW>();
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int64_t units = (int64_t)a.n_layers * a.n_seg * a.H;
-    kern<<<(unsigned)units, kThreads, Cfg::SMEM, s>>>(mk, mv, ma, a);
+    kern<<<(unsigned)units, Cfg::THREADS, smem, s>>>(mk, mv, ma, a);
     return cudaGetLastError();
 }
 
@@ -426,11 +474,15 @@ bool scan_sd_tc_supported(const ScanArgs &a) {
 #ifndef HYPIC_SD_DIAG_NS
 #define HYPIC_SD_DIAG_NS 2
 #endif
+#ifndef HYPIC_SD_TW
+#define HYPIC_SD_TW 8
+#endif
 
 cudaError_t launch_scan_sd_tc(const ScanArgs &a, cudaStream_t s) {
     if ((int64_t)a.n_layers * a.n_seg * a.H == 0) return cudaSuccess;
-    if (a.fam == HYPIC_SCALAR) return launch_tc<HYPIC_SCALAR, HYPIC_SD_SCALAR_C, HYPIC_SD_SCALAR_NS>(a, s);
-    return launch_tc<HYPIC_DIAG, HYPIC_SD_DIAG_C, HYPIC_SD_DIAG_NS>(a, s);
+    if (a.fam == HYPIC_SCALAR)
+        return launch_tc<HYPIC_SCALAR, HYPIC_SD_SCALAR_C, HYPIC_SD_SCALAR_NS, HYPIC_SD_TW>(a, s);
+    return launch_tc<HYPIC_DIAG, HYPIC_SD_DIAG_C, HYPIC_SD_DIAG_NS, HYPIC_SD_TW>(a, s);
 }
 
 }  // namespace hypic
