@@ -80,6 +80,7 @@ int hypic_segment_scan(int fam, int in_dtype, int n_layers, int n_seg, int64_t t
     a.d_err = d_err;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     if (hypic::scan_sd_tc_supported(a)) return from_cuda(hypic::launch_scan_sd_tc(a, s));
+    if (hypic::scan_dense_tc_supported(a)) return from_cuda(hypic::launch_scan_dense_tc(a, s));
     return from_cuda(hypic::launch_scan_recurrent(a, s));
 }
 

@@ -46,6 +46,10 @@ cudaError_t launch_scan_recurrent(const ScanArgs &a, cudaStream_t s);
 bool scan_sd_tc_supported(const ScanArgs &a);
 cudaError_t launch_scan_sd_tc(const ScanArgs &a, cudaStream_t s);
 
+// Gated delta rule scan on tcgen05 tensor cores (bf16 inputs, d_k = d_v = 128, no o_t).
+bool scan_dense_tc_supported(const ScanArgs &a);
+cudaError_t launch_scan_dense_tc(const ScanArgs &a, cudaStream_t s);
+
 cudaError_t launch_compose(const ComposeArgs &a, cudaStream_t s);
 cudaError_t launch_compose_chain(const ChainArgs &a, cudaStream_t s);
 

@@ -1,0 +1,609 @@
+// scan_dense_tc.cu -- gated delta rule segment scan on tcgen05 tensor cores.
+//
+// Chunked WY/UT form of S_t = alpha_t (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T
+// (C = 64 tokens per chunk; b_t = in-chunk cumulative decay, b_C its total):
+//   L_ts = beta_t (b_t / b_s) k_t.k_s  (s < t),   A = (I + L)^-1
+//   for X = [M | S] (the transition and the state side by side, d x 2d):
+//   P = K X_0,  R = diag(beta) [0 | V] - diag(beta b) P,  Delta = A R,
+//   X <- b_C X_0 + K^T diag(b_C / b) Delta.
+// Within a chunk delta_t = beta_t (v_t - alpha_t S_{t-1}^T k_t) satisfies
+// (I + L) Delta = R, which is where the triangular system comes from.
+//
+// The kernel keeps X^T in TMEM (row m of X^T = column m of X on TMEM lane m,
+// key channel k along the columns), so every product is an M = 128 MMA:
+//   Gram   G   = K K^T                    (bf16 keys, exact products)
+//   P^T_h      = X0_h^T K^T               (h = M half: hi+lo split of X0; S half: bf16)
+//   Delta^T_h  = R^T_h A^T                (3-term bf16 split of both operands)
+//   X^T_h     += (Delta~)^T_h K           (Delta~ split hi+lo, K exact)
+// R^T and Delta~^T are written by the math warps straight into TMEM as the MMA
+// A operand; X0 and A go through shared memory.  The transition half is
+// rescaled by a power of two every chunk (exponent into lambda), so
+// T_C = exp(lambda) M with max|M| in [1, 2) at the end.
+// Warp 0: TMA (K, V tiles), warp 1: MMA issue, warps 2-9: everything else
+// (gates, Gram -> L -> blocked inverse, TMEM round trips, epilogue).
+// Every wait is time-bounded; a timeout is reported as HYPIC_ETIMEOUT.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "internal.cuh"
+#include "sm100.cuh"
+
+namespace hypic {
+namespace {
+
+using namespace sm100;
+
+constexpr int kC = 64;          // tokens per chunk
+constexpr int kD = 128;         // d_k = d_v
+constexpr int kNS = 2;          // TMA stages
+constexpr int kThreads = 320;   // 10 warps
+constexpr int kMath = 256;      // warps 2..9
+constexpr int kLd = 65;         // padded row stride of the fp32 L / A work tiles
+
+// shared memory map (offsets from the 1024-aligned base)
+constexpr int kBox = kC * 128;              // 64 channels x 64 tokens, bf16: 8 KB
+constexpr int kTile = 2 * kBox;             // 128 channels: 16 KB
+constexpr int kStage = 2 * kTile;           // K tile, V tile
+constexpr int kXop = kNS * kStage;          // X0^T operands: M hi, M lo, S hi (32 KB each)
+constexpr int kXopPart = 32768;
+constexpr int kAop = kXop + 3 * kXopPart;   // A operand (row t, s contiguous): hi, lo (8 KB each)
+constexpr int kLws = kAop + 2 * 8192;       // fp32 L (64 x 65)
+constexpr int kAws = kLws + kC * kLd * 4;   // fp32 A (64 x 65)
+constexpr int kTws = kAws + kC * kLd * 4;   // fp32 temporaries for the off-diagonal blocks (3 x 16 x 16)
+constexpr int kCtl = kTws + 3 * 256 * 4;
+
+// TMEM column map (512 columns allocated)
+constexpr uint32_t kTxM = 0, kTxS = 128, kTaccM = 256, kTaccS = 320;
+constexpr uint32_t kTopr = 384;   // R / Delta~ operands: M hi, M lo, S hi, S lo (32 columns each)
+constexpr uint32_t kTgram = 384;  // Gram overlays the operand columns (64 columns)
+
+struct DenseCtrl {
+    uint64_t full[kNS], empty[kNS];
+    uint64_t gram_done, p_done, d_done, x_done;
+    uint64_t ops_ready, r_ready, dt_ready;
+    float gl[2][kC], gbb[2][kC], gw[2][kC], gbeta[2][kC];   // per chunk parity: Lambda_t, beta_t b_t,
+    float bC[2];                                             // b_C / b_t, beta_t; b_C
+    float redmax[4];
+    uint32_t tmem;
+    int abort;
+};
+
+constexpr int kSmem = kCtl + (int)sizeof(DenseCtrl) + 1024;
+static_assert(kSmem <= 232448, "fits in one SM's shared memory");
+
+// x = hi + lo with both in bf16 (pairs packed for elements 2c, 2c+1)
+__device__ __forceinline__ void split_pair(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - __low2float(h), x1 - __high2float(h));
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
+}
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abortp) {
+    if (*abortp) return false;
+    if (!mbar_wait(bar, parity)) {
+        *abortp = 1;
+        return false;
+    }
+    return true;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    scan_dense_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                         const ScanArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    DenseCtrl *ctl = reinterpret_cast<DenseCtrl *>(smem + kCtl);
+    volatile int *abortp = &ctl->abort;
+    float *Lw = reinterpret_cast<float *>(smem + kLws);
+    float *Aw = reinterpret_cast<float *>(smem + kAws);
+    float *Tw = reinterpret_cast<float *>(smem + kTws);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const int unit = blockIdx.x;
+    const int h = unit % a.H;
+    const int seg = (unit / a.H) % a.n_seg;
+    const int l = unit / (a.H * a.n_seg);
+    int64_t t0 = a.seg_offsets[seg], t1 = a.seg_offsets[seg + 1];
+    const bool bad = !(t0 >= 0 && t0 <= t1 && t1 <= a.N);
+    if (bad) t0 = t1 = 0;
+    const int nc = (int)((t1 - t0 + kC - 1) / kC);
+    const int64_t row0 = (int64_t)l * a.N + t0;   // token row of the segment's first token
+
+    if (threadIdx.x == 0) {
+        if (bad) flag_index_error(a.d_err);
+        for (int s = 0; s < kNS; ++s) {
+            mbar_init(&ctl->full[s], 1);
+            mbar_init(&ctl->empty[s], 1);
+        }
+        mbar_init(&ctl->gram_done, 1);
+        mbar_init(&ctl->p_done, 1);
+        mbar_init(&ctl->d_done, 1);
+        mbar_init(&ctl->x_done, 1);
+        mbar_init(&ctl->ops_ready, kMath / 32);
+        mbar_init(&ctl->r_ready, kMath / 32);
+        mbar_init(&ctl->dt_ready, kMath / 32);
+        ctl->abort = 0;
+        mbar_fence_init();
+        tma_prefetch(&tm_k);
+        tma_prefetch(&tm_v);
+    }
+    if (warp == 1) tmem_alloc(&ctl->tmem, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int issued = 0;
+            for (int j = 0; j < nc; ++j) {
+                const int s = j % kNS;
+                if (!wait_or_abort(&ctl->empty[s], ((uint32_t)(j / kNS) & 1u) ^ 1u, abortp)) break;
+                uint8_t *st = smem + s * kStage;
+                const int row = (int)(row0 + (int64_t)j * kC);
+                mbar_expect_tx(&ctl->full[s], (uint32_t)kStage);
+                tma_load_3d(st, &tm_k, &ctl->full[s], 0, h, row);
+                tma_load_3d(st + kBox, &tm_k, &ctl->full[s], 64, h, row);
+                tma_load_3d(st + kTile, &tm_v, &ctl->full[s], 0, h, row);
+                tma_load_3d(st + kTile + kBox, &tm_v, &ctl->full[s], 64, h, row);
+                issued = j + 1;
+            }
+            if (*abortp)
+                for (int j = issued - kNS < 0 ? 0 : issued - kNS; j < issued; ++j)
+                    mbar_wait(&ctl->full[j % kNS], (uint32_t)(j / kNS) & 1u);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t id_n64 = idesc_bf16_f32(128, 64, false, false);     // A, B K-major
+            constexpr uint32_t id_u = idesc_bf16_f32(128, 128, false, true);       // B = K (MN-major)
+            const uint32_t xop = smem_addr(smem + kXop), aop = smem_addr(smem + kAop);
+            for (int j = 0; j < nc; ++j) {
+                const int s = j % kNS;
+                const uint32_t par = (uint32_t)j & 1u;
+                const uint32_t kb = smem_addr(smem + s * kStage);
+                if (!wait_or_abort(&ctl->full[s], (uint32_t)(j / kNS) & 1u, abortp)) break;
+                // the Gram overlays the operand columns that the previous update read
+                if (j > 0 && !wait_or_abort(&ctl->x_done, par ^ 1u, abortp)) break;
+                tc_fence_after();
+                // G = K K^T (M padded to 128 rows; rows >= 64 are not used)
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t off = (uint32_t)(ks >> 2) * kBox + (uint32_t)(ks & 3) * 32u;
+                    mma_f16(tmem + kTgram, smem_desc_sw128(kb + off, 0, 1024), smem_desc_sw128(kb + off, 0, 1024),
+                            id_n64, ks > 0);
+                }
+                mma_commit(&ctl->gram_done);
+                // P^T = X0^T K^T: transition half hi + lo, state half hi
+                if (!wait_or_abort(&ctl->ops_ready, par, abortp)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t ka = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
+                    const uint32_t kk = (uint32_t)(ks >> 2) * kBox + (uint32_t)(ks & 3) * 32u;
+                    const uint64_t bd = smem_desc_sw128(kb + kk, 0, 1024);
+                    mma_f16(tmem + kTaccM, smem_desc_sw128(xop + ka, 0, 1024), bd, id_n64, ks > 0);
+                    mma_f16(tmem + kTaccM, smem_desc_sw128(xop + kXopPart + ka, 0, 1024), bd, id_n64, 1u);
+                    mma_f16(tmem + kTaccS, smem_desc_sw128(xop + 2 * kXopPart + ka, 0, 1024), bd, id_n64, ks > 0);
+                }
+                mma_commit(&ctl->p_done);
+                // Delta^T = R^T A^T, three-term split for both halves
+                if (!wait_or_abort(&ctl->r_ready, par, abortp)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint64_t ah = smem_desc_sw128(aop + (uint32_t)ks * 32u, 0, 1024);
+                    const uint64_t al = smem_desc_sw128(aop + 8192u + (uint32_t)ks * 32u, 0, 1024);
+                    const uint32_t c = (uint32_t)ks * 8u;
+                    mma_f16_ta(tmem + kTaccM, tmem + kTopr + c, ah, id_n64, ks > 0);
+                    mma_f16_ta(tmem + kTaccM, tmem + kTopr + c, al, id_n64, 1u);
+                    mma_f16_ta(tmem + kTaccM, tmem + kTopr + 32 + c, ah, id_n64, 1u);
+                    mma_f16_ta(tmem + kTaccS, tmem + kTopr + 64 + c, ah, id_n64, ks > 0);
+                    mma_f16_ta(tmem + kTaccS, tmem + kTopr + 64 + c, al, id_n64, 1u);
+                    mma_f16_ta(tmem + kTaccS, tmem + kTopr + 96 + c, ah, id_n64, 1u);
+                }
+                mma_commit(&ctl->d_done);
+                // X^T += Delta~^T K (K as the MN-major B operand: row t, channels contiguous)
+                if (!wait_or_abort(&ctl->dt_ready, par, abortp)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint64_t bd = smem_desc_sw128(kb + (uint32_t)ks * 2048u, kBox, 1024);
+                    const uint32_t c = (uint32_t)ks * 8u;
+                    mma_f16_ta(tmem + kTxM, tmem + kTopr + c, bd, id_u, 1u);
+                    mma_f16_ta(tmem + kTxM, tmem + kTopr + 32 + c, bd, id_u, 1u);
+                    mma_f16_ta(tmem + kTxS, tmem + kTopr + 64 + c, bd, id_u, 1u);
+                    mma_f16_ta(tmem + kTxS, tmem + kTopr + 96 + c, bd, id_u, 1u);
+                }
+                mma_commit(&ctl->x_done);
+                mma_commit(&ctl->empty[s]);
+            }
+            if (*abortp) {
+                mma_commit(&ctl->gram_done);   // drain: completes once issued MMAs are done
+                mbar_wait(&ctl->gram_done, nc & 1);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ math warps
+        const int mt = threadIdx.x - 64;            // 0..255
+        const int half = (warp - 2) >> 2;           // 0: transition (M), 1: state (S)
+        const int quarter = warp & 3;               // TMEM lanes this warp may touch
+        const int m = quarter * 32 + lane;          // column of X = TMEM lane
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t tx = tmem + lane_off + (half ? kTxS : kTxM);
+        const uint32_t tacc = tmem + lane_off + (half ? kTaccS : kTaccM);
+        const uint32_t topr = tmem + lane_off + kTopr + (half ? 64u : 0u);
+        uint8_t *xop = smem + kXop + half * 2 * kXopPart;   // hi part (lo follows for the M half)
+        int lam_exp = 0;                            // power-of-two exponent moved out of M
+
+        // initial X^T = [I ; 0]
+        {
+            uint32_t r[32];
+            for (int cb = 0; cb < 4; ++cb) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    r[i] = __float_as_uint((half == 0 && cb * 32 + i == m) ? 1.f : 0.f);
+                tmem_st32(tx + (uint32_t)(cb * 32), r);
+            }
+            tmem_wait_st();
+        }
+
+        float pa[2], pb[2];
+        auto prefetch = [&](int j) {
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int64_t t = t0 + (int64_t)j * kC + lane + 32 * q;
+                const bool v = j < nc && t < t1;
+                const int64_t row = ((int64_t)l * a.N + t) * a.H + h;
+                pa[q] = v ? a.alpha[row] : 1.f;
+                pb[q] = v ? (a.beta ? a.beta[row] : 1.f) : 0.f;
+            }
+        };
+        if (warp == 2) prefetch(0);
+
+        for (int j = 0; j < nc; ++j) {
+            const int s = j % kNS;
+            const uint32_t par = (uint32_t)j & 1u;
+            // ---- gates: Lambda (inclusive in-chunk log decay), beta b, b_C / b
+            if (warp == 2) {
+                float lg[2], inc[2];
+#pragma unroll
+                for (int q = 0; q < 2; ++q) lg[q] = logf(pa[q]);
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    float x = lg[q];
+#pragma unroll
+                    for (int off = 1; off < 32; off <<= 1) {
+                        const float y = __shfl_up_sync(0xffffffffu, x, off);
+                        if (lane >= off) x += y;
+                    }
+                    inc[q] = x;
+                }
+                const float tot0 = __shfl_sync(0xffffffffu, inc[0], 31);
+                inc[1] += tot0;
+                const float total = __shfl_sync(0xffffffffu, inc[1], 31);
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int t = lane + 32 * q;
+                    ctl->gl[par][t] = inc[q];
+                    ctl->gbb[par][t] = pb[q] * expf(inc[q]);
+                    ctl->gw[par][t] = expf(total - inc[q]);
+                    ctl->gbeta[par][t] = pb[q];
+                }
+                if (lane == 0) ctl->bC[par] = expf(total);
+                if (j + 1 < nc) prefetch(j + 1);
+            }
+            const bool ok_full = mbar_wait(&ctl->full[s], (uint32_t)(j / kNS) & 1u);
+            const bool ok_g = ok_full && mbar_wait(&ctl->gram_done, par);
+            if (!bar_and(1, kMath, ok_g && !*abortp)) {
+                *abortp = 1;
+                break;
+            }
+            tc_fence_after();
+            // ---- L[t][s] = beta_t exp(Lambda_t - Lambda_s) G[t][s] for s < t (rows t < 64)
+            if (quarter < 2) {
+                const int t = m;   // 0..63
+                uint32_t r[32];
+                const int cb = half;   // columns [32*half, 32*half + 32)
+                tmem_ld32(tmem + lane_off + kTgram + (uint32_t)(cb * 32), r);
+                tmem_wait_ld();
+                const float lt = ctl->gl[par][t], bt = ctl->gbeta[par][t];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int sc = cb * 32 + i;
+                    Lw[t * kLd + sc] = sc < t ? bt * expf(lt - ctl->gl[par][sc]) * __uint_as_float(r[i]) : 0.f;
+                }
+            }
+            tc_fence_before();
+            bar_sync(1, kMath);
+            // ---- A = (I + L)^-1: 16 x 16 diagonal blocks by forward substitution
+            if (mt < 64) {
+                const int b0 = (mt >> 4) * 16, jc = mt & 15, col = b0 + jc;
+                for (int i = 0; i < 16; ++i) Aw[(b0 + i) * kLd + col] = i == jc ? 1.f : 0.f;
+                for (int i = jc + 1; i < 16; ++i) {
+                    float acc = -Lw[(b0 + i) * kLd + col];
+                    for (int k = jc + 1; k < i; ++k) acc -= Lw[(b0 + i) * kLd + b0 + k] * Aw[(b0 + k) * kLd + col];
+                    Aw[(b0 + i) * kLd + col] = acc;
+                }
+            } else {
+                // zero the strictly upper off-diagonal blocks
+                for (int e = mt - 64; e < 6 * 256; e += kMath - 64) {
+                    const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15;
+                    const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+                    const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+                    Aw[(bi * 16 + r) * kLd + bj * 16 + c] = 0.f;
+                }
+            }
+            bar_sync(1, kMath);
+            // off-diagonal blocks, one sub-diagonal at a time:
+            //   T = sum_{k=j}^{i-1} L_ik A_kj,  A_ij = -A_ii T
+            for (int dist = 1; dist < 4; ++dist) {
+                const int nblk = 4 - dist;
+                for (int e = mt; e < nblk * 256; e += kMath) {
+                    const int bi = (e >> 8) + dist, bj = bi - dist, r = (e >> 4) & 15, c = e & 15;
+                    float acc = 0.f;
+                    for (int k = bj * 16; k < bi * 16; ++k)
+                        acc += Lw[(bi * 16 + r) * kLd + k] * Aw[k * kLd + bj * 16 + c];
+                    Tw[(e >> 8) * 256 + r * 16 + c] = acc;
+                }
+                bar_sync(1, kMath);
+                for (int e = mt; e < nblk * 256; e += kMath) {
+                    const int bi = (e >> 8) + dist, bj = bi - dist, r = (e >> 4) & 15, c = e & 15;
+                    float acc = 0.f;
+                    for (int k = 0; k <= r; ++k)
+                        acc += Aw[(bi * 16 + r) * kLd + bi * 16 + k] * Tw[(e >> 8) * 256 + k * 16 + c];
+                    Aw[(bi * 16 + r) * kLd + bj * 16 + c] = -acc;
+                }
+                bar_sync(1, kMath);
+            }
+            // A -> bf16 hi / lo operand tiles (row t, s contiguous, 128-byte swizzle)
+            {
+                const int t = mt >> 2, c0 = (mt & 3) * 2;   // two 8-element chunks per thread
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int c = c0 + cc;
+                    uint32_t hi[4], lo[4];
+#pragma unroll
+                    for (int p = 0; p < 4; ++p)
+                        split_pair(Aw[t * kLd + c * 8 + 2 * p], Aw[t * kLd + c * 8 + 2 * p + 1], hi[p], lo[p]);
+                    const int off = t * 128 + ((c ^ (t & 7)) << 4);
+                    *reinterpret_cast<uint4 *>(smem + kAop + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4 *>(smem + kAop + 8192 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                }
+            }
+            // ---- X round trip: operand X0 (scaled), TMEM <- b_C * X0 (scaled)
+            if (j > 0) {
+                const bool okx = mbar_wait(&ctl->x_done, par ^ 1u);
+                if (!bar_and(1, kMath, okx && !*abortp)) {
+                    *abortp = 1;
+                    break;
+                }
+            }
+            tc_fence_after();
+            float g = 1.f;
+            if (half == 0) {
+                float mx = 0.f;
+                for (int cb = 0; cb < 4; ++cb) {
+                    uint32_t r[32];
+                    tmem_ld32(tx + (uint32_t)(cb * 32), r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fabsf(__uint_as_float(r[i])));
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                if (lane == 0) ctl->redmax[quarter] = mx;
+                bar_sync(2, 128);
+                mx = fmaxf(fmaxf(ctl->redmax[0], ctl->redmax[1]), fmaxf(ctl->redmax[2], ctl->redmax[3]));
+                bar_sync(2, 128);
+                int e = 0;
+                if (mx > 0.f) {
+                    int ex;
+                    frexpf(mx, &ex);
+                    e = ex - 1;
+                }
+                g = ldexpf(1.f, -e);
+                lam_exp += e;
+            }
+            const float bC = ctl->bC[par];
+            for (int cb = 0; cb < 4; ++cb) {
+                uint32_t r[32];
+                tmem_ld32(tx + (uint32_t)(cb * 32), r);
+                tmem_wait_ld();
+                // operand row m: channels k = cb*32 .. cb*32+31 -> atom cb/2, chunks (cb&1)*4 ..
+                const int atom = cb >> 1;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t hi[4], lo[4];
+#pragma unroll
+                    for (int p = 0; p < 4; ++p)
+                        split_pair(g * __uint_as_float(r[q * 8 + 2 * p]), g * __uint_as_float(r[q * 8 + 2 * p + 1]),
+                                   hi[p], lo[p]);
+                    const int c = (cb & 1) * 4 + q;
+                    const int off = atom * 16384 + m * 128 + ((c ^ (m & 7)) << 4);
+                    *reinterpret_cast<uint4 *>(xop + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    if (half == 0)
+                        *reinterpret_cast<uint4 *>(xop + kXopPart + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                }
+                const float sc = g * bC;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(sc * __uint_as_float(r[i]));
+                tmem_st32(tx + (uint32_t)(cb * 32), r);
+            }
+            tmem_wait_st();
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->ops_ready);
+            // ---- R^T = beta [0 | V]^T - (beta b) P^T  -> TMEM operand (hi, lo)
+            if (!bar_and(1, kMath, mbar_wait(&ctl->p_done, par) && !*abortp)) {
+                *abortp = 1;
+                break;
+            }
+            tc_fence_after();
+            {
+                const uint8_t *vt = smem + s * kStage + kTile;
+                const int vbox = m >> 6, vc = (m & 63) >> 3, vw = (m & 7) * 2;
+                for (int cb = 0; cb < 2; ++cb) {
+                    uint32_t r[32], hi[16], lo[16];
+                    tmem_ld32(tacc + (uint32_t)(cb * 32), r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int p = 0; p < 16; ++p) {
+                        float x[2];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int t = cb * 32 + 2 * p + e;
+                            float val = -ctl->gbb[par][t] * __uint_as_float(r[2 * p + e]);
+                            if (half) {
+                                const uint16_t vb = *reinterpret_cast<const uint16_t *>(
+                                    vt + vbox * kBox + t * 128 + ((vc ^ (t & 7)) << 4) + vw);
+                                val = fmaf(ctl->gbeta[par][t], __uint_as_float((uint32_t)vb << 16), val);
+                            }
+                            x[e] = val;
+                        }
+                        split_pair(x[0], x[1], hi[p], lo[p]);
+                    }
+                    tmem_st16(topr + (uint32_t)(cb * 16), hi);
+                    tmem_st16(topr + 32u + (uint32_t)(cb * 16), lo);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->r_ready);
+            // ---- Delta~^T = Delta^T diag(b_C / b)  -> TMEM operand (hi, lo)
+            if (!bar_and(1, kMath, mbar_wait(&ctl->d_done, par) && !*abortp)) {
+                *abortp = 1;
+                break;
+            }
+            tc_fence_after();
+            for (int cb = 0; cb < 2; ++cb) {
+                uint32_t r[32], hi[16], lo[16];
+                tmem_ld32(tacc + (uint32_t)(cb * 32), r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int p = 0; p < 16; ++p) {
+                    const int t = cb * 32 + 2 * p;
+                    split_pair(ctl->gw[par][t] * __uint_as_float(r[2 * p]),
+                               ctl->gw[par][t + 1] * __uint_as_float(r[2 * p + 1]),
+                               hi[p], lo[p]);
+                }
+                tmem_st16(topr + (uint32_t)(cb * 16), hi);
+                tmem_st16(topr + 32u + (uint32_t)(cb * 16), lo);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->dt_ready);
+        }
+
+        // ------------------------------------------------------------ epilogue
+        bool ok = true;
+        if (nc > 0) ok = mbar_wait(&ctl->x_done, (uint32_t)(nc - 1) & 1u);
+        if (bar_and(1, kMath, ok && !*abortp)) {
+            tc_fence_after();
+            const int64_t u_out = ((int64_t)l * a.n_seg + seg) * a.H + h;
+            float scale = 1.f;
+            if (half == 0) {
+                float mx = 0.f;
+                for (int cb = 0; cb < 4; ++cb) {
+                    uint32_t r[32];
+                    tmem_ld32(tx + (uint32_t)(cb * 32), r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fabsf(__uint_as_float(r[i])));
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                if (lane == 0) ctl->redmax[quarter] = mx;
+                bar_sync(2, 128);
+                mx = fmaxf(fmaxf(ctl->redmax[0], ctl->redmax[1]), fmaxf(ctl->redmax[2], ctl->redmax[3]));
+                int e = 0;
+                if (mx > 0.f) {
+                    int ex;
+                    frexpf(mx, &ex);
+                    e = ex - 1;
+                }
+                scale = ldexpf(1.f, -e);
+                lam_exp += e;
+                if (mt == 0) a.lam_out[u_out] = (float)((double)lam_exp * 0.69314718055994530942);
+            }
+            float *out = half == 0 ? a.M_out + u_out * kD * kD : a.S_out + u_out * kD * kD;
+            for (int cb = 0; cb < 4; ++cb) {
+                uint32_t r[32];
+                tmem_ld32(tx + (uint32_t)(cb * 32), r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) out[(int64_t)(cb * 32 + i) * kD + m] = scale * __uint_as_float(r[i]);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0 && *abortp && a.d_err) atomicExch(a.d_err, (int)HYPIC_ETIMEOUT);
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                 const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                 CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                 CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_fn() {
+    static EncodeTiled fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(p);
+    });
+    return fn;
+}
+
+bool make_map_bf16(CUtensorMap *m, const void *base, uint64_t H, uint64_t rows) {
+    EncodeTiled enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {128, H, rows};
+    const cuuint64_t strides[2] = {256, 256 * H};
+    const cuuint32_t box[3] = {64, 1, kC};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool scan_dense_tc_supported(const ScanArgs &a) {
+    return a.fam == HYPIC_DENSE && a.in_dtype == HYPIC_BF16 && a.dk == 128 && a.dv == 128 &&
+           a.o_out == nullptr && a.N > 0 && (int64_t)a.n_layers * a.N < ((int64_t)1 << 31) &&
+           encode_fn() != nullptr;
+}
+
+cudaError_t launch_scan_dense_tc(const ScanArgs &a, cudaStream_t s) {
+    const int64_t units = (int64_t)a.n_layers * a.n_seg * a.H;
+    if (units == 0) return cudaSuccess;
+    const uint64_t rows = (uint64_t)a.n_layers * (uint64_t)a.N;
+    CUtensorMap mk, mv;
+    if (!make_map_bf16(&mk, a.k, a.H, rows) || !make_map_bf16(&mv, a.v, a.H, rows)) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(scan_dense_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    scan_dense_tc_kernel<<<(unsigned)units, kThreads, kSmem, s>>>(mk, mv, a);
+    return cudaGetLastError();
+}
+
+}  // namespace hypic

@@ -144,6 +144,23 @@ def test_dense_full_stack_sampled(L):
         check(DENSE, sub, ref, TOL_SCAN_BF16)
 
 
+def test_dense_long_segment_and_special_gates():
+    """Gated delta rule on long segments (many chunks of transition renormalisation),
+    beta = 0 (pure decay: S = 0, T = prod(alpha) I) and alpha = beta = 1 (plain delta rule)."""
+    w = wl.dense_stack(lengths=[8192, 3000], n_layers=1, H=2, d=128, seed=13)
+    check(DENSE, host(gpu_scan(w)), oracle_scan(w), TOL_SCAN_BF16)
+    w0 = dict(w)
+    w0["beta"] = np.zeros_like(w["beta"])
+    got = host(gpu_scan(w0))
+    ref = oracle_scan(w0)
+    check(DENSE, got, ref, TOL_SCAN_BF16)
+    assert np.all(got["S"] == 0)
+    w1 = wl.dense_stack(lengths=[700, 129], n_layers=1, H=2, d=128, seed=14)
+    w1["alpha"] = np.ones_like(w1["alpha"])
+    w1["beta"] = np.ones_like(w1["beta"])
+    check(DENSE, host(gpu_scan(w1)), oracle_scan(w1), TOL_SCAN_BF16)
+
+
 @pytest.mark.parametrize("fam", [SCALAR, DIAG, DENSE], ids=["scalar", "diag", "dense"])
 def test_segment_independence_bitwise(fam):
     """T_C and S(C|0) depend only on the segment's tokens: the same segment
