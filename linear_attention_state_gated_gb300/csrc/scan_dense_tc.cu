@@ -12,7 +12,7 @@
 // The kernel keeps X^T in TMEM (row m of X^T = column m of X on TMEM lane m,
 // key channel k along the columns), so every product is an M = 128 MMA:
 //   Gram   G   = K K^T                    (bf16 keys, exact products)
-//   P^T_h      = X0_h^T K^T               (h = M half: hi+lo split of X0; S half: bf16)
+//   P^T_h      = X0_h^T K^T               (hi + lo split of X0, both halves)
 //   Delta^T_h  = R^T_h A^T                (3-term bf16 split of both operands)
 //   X^T_h     += (Delta~)^T_h K           (Delta~ split hi+lo, K exact)
 // R^T and Delta~^T are written by the math warps straight into TMEM as the MMA
@@ -45,13 +45,17 @@ constexpr int kLd = 65;         // padded row stride of the fp32 L / A work tile
 constexpr int kBox = kC * 128;              // 64 channels x 64 tokens, bf16: 8 KB
 constexpr int kTile = 2 * kBox;             // 128 channels: 16 KB
 constexpr int kStage = 2 * kTile;           // K tile, V tile
-constexpr int kXop = kNS * kStage;          // X0^T operands: M hi, M lo, S hi (32 KB each)
+constexpr int kXop = kNS * kStage;          // X0^T operands: M hi, M lo, S hi, S lo (32 KB each)
 constexpr int kXopPart = 32768;
-constexpr int kAop = kXop + 3 * kXopPart;   // A operand (row t, s contiguous): hi, lo (8 KB each)
-constexpr int kLws = kAop + 2 * 8192;       // fp32 L (64 x 65)
+constexpr int kAop = kXop + 4 * kXopPart;   // A operand (row t, s contiguous): hi, lo (8 KB each)
+// fp32 work tiles of the triangular inverse, overlaid on the X0 operands (the
+// inverse is finished and converted before the operands are written, and the
+// operands are consumed before the next chunk's inverse starts)
+constexpr int kLws = kXop;                  // fp32 L (64 x 65)
 constexpr int kAws = kLws + kC * kLd * 4;   // fp32 A (64 x 65)
 constexpr int kTws = kAws + kC * kLd * 4;   // fp32 temporaries for the off-diagonal blocks (3 x 16 x 16)
-constexpr int kCtl = kTws + 3 * 256 * 4;
+static_assert(kTws + 3 * 256 * 4 <= kAop, "work tiles fit in the operand region");
+constexpr int kCtl = kAop + 2 * 8192;
 
 // TMEM column map (512 columns allocated)
 constexpr uint32_t kTxM = 0, kTxS = 128, kTaccM = 256, kTaccS = 320;
@@ -178,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             id_n64, ks > 0);
                 }
                 mma_commit(&ctl->gram_done);
-                // P^T = X0^T K^T: transition half hi + lo, state half hi
+                // P^T = X0^T K^T: hi + lo of X0 for both halves
                 if (!wait_or_abort(&ctl->ops_ready, par, abortp)) break;
                 tc_fence_after();
 #pragma unroll
@@ -189,6 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_f16(tmem + kTaccM, smem_desc_sw128(xop + ka, 0, 1024), bd, id_n64, ks > 0);
                     mma_f16(tmem + kTaccM, smem_desc_sw128(xop + kXopPart + ka, 0, 1024), bd, id_n64, 1u);
                     mma_f16(tmem + kTaccS, smem_desc_sw128(xop + 2 * kXopPart + ka, 0, 1024), bd, id_n64, ks > 0);
+                    mma_f16(tmem + kTaccS, smem_desc_sw128(xop + 3 * kXopPart + ka, 0, 1024), bd, id_n64, 1u);
                 }
                 mma_commit(&ctl->p_done);
                 // Delta^T = R^T A^T, three-term split for both halves
@@ -237,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tx = tmem + lane_off + (half ? kTxS : kTxM);
         const uint32_t tacc = tmem + lane_off + (half ? kTaccS : kTaccM);
         const uint32_t topr = tmem + lane_off + kTopr + (half ? 64u : 0u);
-        uint8_t *xop = smem + kXop + half * 2 * kXopPart;   // hi part (lo follows for the M half)
+        uint8_t *xop = smem + kXop + half * 2 * kXopPart;   // hi part, lo follows
         int lam_exp = 0;                            // power-of-two exponent moved out of M
 
         // initial X^T = [I ; 0]
@@ -375,6 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *reinterpret_cast<uint4 *>(smem + kAop + 8192 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                 }
             }
+            bar_sync(1, kMath);   // the work tiles are dead from here; the operands overwrite them
             // ---- X round trip: operand X0 (scaled), TMEM <- b_C * X0 (scaled)
             if (j > 0) {
                 const bool okx = mbar_wait(&ctl->x_done, par ^ 1u);
@@ -426,8 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int c = (cb & 1) * 4 + q;
                     const int off = atom * 16384 + m * 128 + ((c ^ (m & 7)) << 4);
                     *reinterpret_cast<uint4 *>(xop + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                    if (half == 0)
-                        *reinterpret_cast<uint4 *>(xop + kXopPart + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    *reinterpret_cast<uint4 *>(xop + kXopPart + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                 }
                 const float sc = g * bC;
 #pragma unroll
