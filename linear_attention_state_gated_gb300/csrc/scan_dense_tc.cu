@@ -9,19 +9,22 @@
 // Within a chunk delta_t = beta_t (v_t - alpha_t S_{t-1}^T k_t) satisfies
 // (I + L) Delta = R, which is where the triangular system comes from.
 //
-// The kernel keeps X^T in TMEM (row m of X^T = column m of X on TMEM lane m,
-// key channel k along the columns), so every product is an M = 128 MMA:
-//   Gram   G   = K K^T                    (bf16 keys, exact products)
-//   P^T_h      = X0_h^T K^T               (hi + lo split of X0, both halves)
-//   Delta^T_h  = R^T_h A^T                (3-term bf16 split of both operands)
-//   X^T_h     += (Delta~)^T_h K           (Delta~ split hi+lo, K exact)
-// R^T and Delta~^T are written by the math warps straight into TMEM as the MMA
-// A operand; X0 and A go through shared memory.  The transition half is
-// rescaled by a power of two every chunk (exponent into lambda), so
-// T_C = exp(lambda) M with max|M| in [1, 2) at the end.
-// Warp 0: TMA (K, V tiles), warp 1: MMA issue, warps 2-9: everything else
-// (gates, Gram -> L -> blocked inverse, TMEM round trips, epilogue).
-// Every wait is time-bounded; a timeout is reported as HYPIC_ETIMEOUT.
+// Every product above acts on one column of X at a time, so the transition
+// half M and the state half S of a chain are handled by two CTAs (launched
+// side by side); each repeats the cheap per-chunk preparation (gates, Gram,
+// inverse).  A CTA keeps its half transposed in TMEM (column m of X on TMEM
+// lane m, key channel k along the columns), so every product is M = 128:
+//   Gram   G   = K K^T                  (bf16 keys, exact products)
+//   P^T        = X0^T K^T               (X0 split into bf16 hi + lo, from TMEM)
+//   Delta^T    = R^T A^T                (3-term bf16 split of both operands)
+//   X^T       += (Delta~)^T K           (Delta~ split hi + lo, K exact)
+// The X0, R and Delta~ operands never leave TMEM (math warps convert them in
+// place with tcgen05.ld / st); only A goes through shared memory.  The
+// transition half is rescaled by a power of two every chunk (exponent into
+// lambda), so T_C = exp(lambda) M with max|M| in [1, 2) at the end.
+// Warp 0: TMA, warp 1: MMA issue, warps 2-9: gates, Gram -> L -> blocked
+// inverse, the TMEM conversions and the epilogue.  Every wait is
+// time-bounded; a timeout is reported as HYPIC_ETIMEOUT.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -45,22 +48,18 @@ constexpr int kLd = 65;         // padded row stride of the fp32 L / A work tile
 constexpr int kBox = kC * 128;              // 64 channels x 64 tokens, bf16: 8 KB
 constexpr int kTile = 2 * kBox;             // 128 channels: 16 KB
 constexpr int kStage = 2 * kTile;           // K tile, V tile
-constexpr int kXop = kNS * kStage;          // X0^T operands: M hi, M lo, S hi, S lo (32 KB each)
-constexpr int kXopPart = 32768;
-constexpr int kAop = kXop + 4 * kXopPart;   // A operand (row t, s contiguous): hi, lo (8 KB each)
-// fp32 work tiles of the triangular inverse, overlaid on the X0 operands (the
-// inverse is finished and converted before the operands are written, and the
-// operands are consumed before the next chunk's inverse starts)
-constexpr int kLws = kXop;                  // fp32 L (64 x 65)
+constexpr int kAop = kNS * kStage;          // A operand (row t, s contiguous): hi, lo (8 KB each)
+constexpr int kLws = kAop + 2 * 8192;       // fp32 L (64 x 65)
 constexpr int kAws = kLws + kC * kLd * 4;   // fp32 A (64 x 65)
 constexpr int kTws = kAws + kC * kLd * 4;   // fp32 temporaries for the off-diagonal blocks (3 x 16 x 16)
-static_assert(kTws + 3 * 256 * 4 <= kAop, "work tiles fit in the operand region");
-constexpr int kCtl = kAop + 2 * 8192;
+constexpr int kCtl = kTws + 3 * 256 * 4;
 
 // TMEM column map (512 columns allocated)
-constexpr uint32_t kTxM = 0, kTxS = 128, kTaccM = 256, kTaccS = 320;
-constexpr uint32_t kTopr = 384;   // R / Delta~ operands: M hi, M lo, S hi, S lo (32 columns each)
-constexpr uint32_t kTgram = 384;  // Gram overlays the operand columns (64 columns)
+constexpr uint32_t kTx = 0;       // X^T half, fp32 (128 columns)
+constexpr uint32_t kTxop = 128;   // X0^T operand: hi [128, 192), lo [192, 256), bf16 pairs
+constexpr uint32_t kTacc = 256;   // P^T / Delta^T accumulator (64 columns)
+constexpr uint32_t kTopr = 320;   // R^T / Delta~^T operand: hi [320, 352), lo [352, 384)
+constexpr uint32_t kTgram = 384;  // Gram (64 columns)
 
 struct DenseCtrl {
     uint64_t full[kNS], empty[kNS];
@@ -68,7 +67,7 @@ struct DenseCtrl {
     uint64_t ops_ready, r_ready, dt_ready;
     float gl[2][kC], gbb[2][kC], gw[2][kC], gbeta[2][kC];   // per chunk parity: Lambda_t, beta_t b_t,
     float bC[2];                                             // b_C / b_t, beta_t; b_C
-    float redmax[4];
+    float redmax[8];
     uint32_t tmem;
     int abort;
 };
@@ -93,6 +92,26 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
     return true;
 }
 
+// max over the 8 math warps (named barrier 1)
+__device__ __forceinline__ float math_max(float mx, DenseCtrl *ctl, int mw, int lane) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (lane == 0) ctl->redmax[mw] = mx;
+    bar_sync(1, kMath);
+    mx = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) mx = fmaxf(mx, ctl->redmax[w]);
+    bar_sync(1, kMath);
+    return mx;
+}
+
+__device__ __forceinline__ int exponent_of(float mx) {   // 2^e <= mx < 2^(e+1)
+    if (!(mx > 0.f)) return 0;
+    int ex;
+    frexpf(mx, &ex);
+    return ex - 1;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     scan_dense_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                          const ScanArgs a) {
@@ -106,7 +125,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *Tw = reinterpret_cast<float *>(smem + kTws);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    const int unit = blockIdx.x;
+    const int half = blockIdx.x & 1;   // 0: transition M, 1: state S
+    const int unit = blockIdx.x >> 1;
     const int h = unit % a.H;
     const int seg = (unit / a.H) % a.n_seg;
     const int l = unit / (a.H * a.n_seg);
@@ -132,7 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ctl->abort = 0;
         mbar_fence_init();
         tma_prefetch(&tm_k);
-        tma_prefetch(&tm_v);
+        if (half) tma_prefetch(&tm_v);
     }
     if (warp == 1) tmem_alloc(&ctl->tmem, 512);
     tc_fence_before();
@@ -149,11 +169,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!wait_or_abort(&ctl->empty[s], ((uint32_t)(j / kNS) & 1u) ^ 1u, abortp)) break;
                 uint8_t *st = smem + s * kStage;
                 const int row = (int)(row0 + (int64_t)j * kC);
-                mbar_expect_tx(&ctl->full[s], (uint32_t)kStage);
+                mbar_expect_tx(&ctl->full[s], (uint32_t)(half ? 2 * kTile : kTile));
                 tma_load_3d(st, &tm_k, &ctl->full[s], 0, h, row);
                 tma_load_3d(st + kBox, &tm_k, &ctl->full[s], 64, h, row);
-                tma_load_3d(st + kTile, &tm_v, &ctl->full[s], 0, h, row);
-                tma_load_3d(st + kTile + kBox, &tm_v, &ctl->full[s], 64, h, row);
+                if (half) {   // V only feeds the state half
+                    tma_load_3d(st + kTile, &tm_v, &ctl->full[s], 0, h, row);
+                    tma_load_3d(st + kTile + kBox, &tm_v, &ctl->full[s], 64, h, row);
+                }
                 issued = j + 1;
             }
             if (*abortp)
@@ -165,14 +187,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t id_n64 = idesc_bf16_f32(128, 64, false, false);     // A, B K-major
             constexpr uint32_t id_u = idesc_bf16_f32(128, 128, false, true);       // B = K (MN-major)
-            const uint32_t xop = smem_addr(smem + kXop), aop = smem_addr(smem + kAop);
+            const uint32_t aop = smem_addr(smem + kAop);
             for (int j = 0; j < nc; ++j) {
                 const int s = j % kNS;
                 const uint32_t par = (uint32_t)j & 1u;
                 const uint32_t kb = smem_addr(smem + s * kStage);
                 if (!wait_or_abort(&ctl->full[s], (uint32_t)(j / kNS) & 1u, abortp)) break;
-                // the Gram overlays the operand columns that the previous update read
-                if (j > 0 && !wait_or_abort(&ctl->x_done, par ^ 1u, abortp)) break;
                 tc_fence_after();
                 // G = K K^T (M padded to 128 rows; rows >= 64 are not used)
 #pragma unroll
@@ -182,21 +202,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                             id_n64, ks > 0);
                 }
                 mma_commit(&ctl->gram_done);
-                // P^T = X0^T K^T: hi + lo of X0 for both halves
+                // P^T = X0^T K^T, X0 as hi + lo
                 if (!wait_or_abort(&ctl->ops_ready, par, abortp)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t ka = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
                     const uint32_t kk = (uint32_t)(ks >> 2) * kBox + (uint32_t)(ks & 3) * 32u;
                     const uint64_t bd = smem_desc_sw128(kb + kk, 0, 1024);
-                    mma_f16(tmem + kTaccM, smem_desc_sw128(xop + ka, 0, 1024), bd, id_n64, ks > 0);
-                    mma_f16(tmem + kTaccM, smem_desc_sw128(xop + kXopPart + ka, 0, 1024), bd, id_n64, 1u);
-                    mma_f16(tmem + kTaccS, smem_desc_sw128(xop + 2 * kXopPart + ka, 0, 1024), bd, id_n64, ks > 0);
-                    mma_f16(tmem + kTaccS, smem_desc_sw128(xop + 3 * kXopPart + ka, 0, 1024), bd, id_n64, 1u);
+                    mma_f16_ta(tmem + kTacc, tmem + kTxop + (uint32_t)ks * 8u, bd, id_n64, ks > 0);
+                    mma_f16_ta(tmem + kTacc, tmem + kTxop + 64u + (uint32_t)ks * 8u, bd, id_n64, 1u);
                 }
                 mma_commit(&ctl->p_done);
-                // Delta^T = R^T A^T, three-term split for both halves
+                // Delta^T = R^T A^T, three-term split
                 if (!wait_or_abort(&ctl->r_ready, par, abortp)) break;
                 tc_fence_after();
 #pragma unroll
@@ -204,12 +221,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t ah = smem_desc_sw128(aop + (uint32_t)ks * 32u, 0, 1024);
                     const uint64_t al = smem_desc_sw128(aop + 8192u + (uint32_t)ks * 32u, 0, 1024);
                     const uint32_t c = (uint32_t)ks * 8u;
-                    mma_f16_ta(tmem + kTaccM, tmem + kTopr + c, ah, id_n64, ks > 0);
-                    mma_f16_ta(tmem + kTaccM, tmem + kTopr + c, al, id_n64, 1u);
-                    mma_f16_ta(tmem + kTaccM, tmem + kTopr + 32 + c, ah, id_n64, 1u);
-                    mma_f16_ta(tmem + kTaccS, tmem + kTopr + 64 + c, ah, id_n64, ks > 0);
-                    mma_f16_ta(tmem + kTaccS, tmem + kTopr + 64 + c, al, id_n64, 1u);
-                    mma_f16_ta(tmem + kTaccS, tmem + kTopr + 96 + c, ah, id_n64, 1u);
+                    mma_f16_ta(tmem + kTacc, tmem + kTopr + c, ah, id_n64, ks > 0);
+                    mma_f16_ta(tmem + kTacc, tmem + kTopr + c, al, id_n64, 1u);
+                    mma_f16_ta(tmem + kTacc, tmem + kTopr + 32u + c, ah, id_n64, 1u);
                 }
                 mma_commit(&ctl->d_done);
                 // X^T += Delta~^T K (K as the MN-major B operand: row t, channels contiguous)
@@ -219,10 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int ks = 0; ks < 4; ++ks) {
                     const uint64_t bd = smem_desc_sw128(kb + (uint32_t)ks * 2048u, kBox, 1024);
                     const uint32_t c = (uint32_t)ks * 8u;
-                    mma_f16_ta(tmem + kTxM, tmem + kTopr + c, bd, id_u, 1u);
-                    mma_f16_ta(tmem + kTxM, tmem + kTopr + 32 + c, bd, id_u, 1u);
-                    mma_f16_ta(tmem + kTxS, tmem + kTopr + 64 + c, bd, id_u, 1u);
-                    mma_f16_ta(tmem + kTxS, tmem + kTopr + 96 + c, bd, id_u, 1u);
+                    mma_f16_ta(tmem + kTx, tmem + kTopr + c, bd, id_u, 1u);
+                    mma_f16_ta(tmem + kTx, tmem + kTopr + 32u + c, bd, id_u, 1u);
                 }
                 mma_commit(&ctl->x_done);
                 mma_commit(&ctl->empty[s]);
@@ -235,23 +247,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------ math warps
         const int mt = threadIdx.x - 64;            // 0..255
-        const int half = (warp - 2) >> 2;           // 0: transition (M), 1: state (S)
+        const int mw = warp - 2;                    // 0..7
+        const int ch = mw >> 2;                     // which half of the columns this warp converts
         const int quarter = warp & 3;               // TMEM lanes this warp may touch
         const int m = quarter * 32 + lane;          // column of X = TMEM lane
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const uint32_t tx = tmem + lane_off + (half ? kTxS : kTxM);
-        const uint32_t tacc = tmem + lane_off + (half ? kTaccS : kTaccM);
-        const uint32_t topr = tmem + lane_off + kTopr + (half ? 64u : 0u);
-        uint8_t *xop = smem + kXop + half * 2 * kXopPart;   // hi part, lo follows
+        const uint32_t tx = tmem + lane_off + kTx + (uint32_t)(ch * 64);
+        const uint32_t txop = tmem + lane_off + kTxop + (uint32_t)(ch * 32);
+        const uint32_t tacc = tmem + lane_off + kTacc + (uint32_t)(ch * 32);
+        const uint32_t topr = tmem + lane_off + kTopr + (uint32_t)(ch * 16);
         int lam_exp = 0;                            // power-of-two exponent moved out of M
 
-        // initial X^T = [I ; 0]
+        // initial X^T: identity (transition) or zero (state)
         {
             uint32_t r[32];
-            for (int cb = 0; cb < 4; ++cb) {
+            for (int cb = 0; cb < 2; ++cb) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
-                    r[i] = __float_as_uint((half == 0 && cb * 32 + i == m) ? 1.f : 0.f);
+                    r[i] = __float_as_uint((half == 0 && ch * 64 + cb * 32 + i == m) ? 1.f : 0.f);
                 tmem_st32(tx + (uint32_t)(cb * 32), r);
             }
             tmem_wait_st();
@@ -313,14 +326,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (quarter < 2) {
                 const int t = m;   // 0..63
                 uint32_t r[32];
-                const int cb = half;   // columns [32*half, 32*half + 32)
-                tmem_ld32(tmem + lane_off + kTgram + (uint32_t)(cb * 32), r);
+                tmem_ld32(tmem + lane_off + kTgram + (uint32_t)(ch * 32), r);
                 tmem_wait_ld();
                 const float lt = ctl->gl[par][t], bt = ctl->gbeta[par][t];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const int sc = cb * 32 + i;
-                    Lw[t * kLd + sc] = sc < t ? bt * expf(lt - ctl->gl[par][sc]) * __uint_as_float(r[i]) : 0.f;
+                    const int sc = ch * 32 + i;
+                    Lw[t * kLd + sc] = sc < t ? bt * __expf(lt - ctl->gl[par][sc]) * __uint_as_float(r[i]) : 0.f;
                 }
             }
             tc_fence_before();
@@ -328,12 +340,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---- A = (I + L)^-1: 16 x 16 diagonal blocks by forward substitution
             if (mt < 64) {
                 const int b0 = (mt >> 4) * 16, jc = mt & 15, col = b0 + jc;
-                for (int i = 0; i < 16; ++i) Aw[(b0 + i) * kLd + col] = i == jc ? 1.f : 0.f;
-                for (int i = jc + 1; i < 16; ++i) {
-                    float acc = -Lw[(b0 + i) * kLd + col];
-                    for (int k = jc + 1; k < i; ++k) acc -= Lw[(b0 + i) * kLd + b0 + k] * Aw[(b0 + k) * kLd + col];
-                    Aw[(b0 + i) * kLd + col] = acc;
+                float ac[16];   // column jc of the block inverse, in registers
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float sum = 0.f;
+#pragma unroll
+                    for (int k = 0; k < i; ++k) sum = fmaf(Lw[(b0 + i) * kLd + b0 + k], ac[k], sum);
+                    ac[i] = i < jc ? 0.f : (i == jc ? 1.f : -sum);
                 }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) Aw[(b0 + i) * kLd + col] = ac[i];
             } else {
                 // zero the strictly upper off-diagonal blocks
                 for (int e = mt - 64; e < 6 * 256; e += kMath - 64) {
@@ -352,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int bi = (e >> 8) + dist, bj = bi - dist, r = (e >> 4) & 15, c = e & 15;
                     float acc = 0.f;
                     for (int k = bj * 16; k < bi * 16; ++k)
-                        acc += Lw[(bi * 16 + r) * kLd + k] * Aw[k * kLd + bj * 16 + c];
+                        acc = fmaf(Lw[(bi * 16 + r) * kLd + k], Aw[k * kLd + bj * 16 + c], acc);
                     Tw[(e >> 8) * 256 + r * 16 + c] = acc;
                 }
                 bar_sync(1, kMath);
@@ -360,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int bi = (e >> 8) + dist, bj = bi - dist, r = (e >> 4) & 15, c = e & 15;
                     float acc = 0.f;
                     for (int k = 0; k <= r; ++k)
-                        acc += Aw[(bi * 16 + r) * kLd + bi * 16 + k] * Tw[(e >> 8) * 256 + k * 16 + c];
+                        acc = fmaf(Aw[(bi * 16 + r) * kLd + bi * 16 + k], Tw[(e >> 8) * 256 + k * 16 + c], acc);
                     Aw[(bi * 16 + r) * kLd + bj * 16 + c] = -acc;
                 }
                 bar_sync(1, kMath);
@@ -380,8 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *reinterpret_cast<uint4 *>(smem + kAop + 8192 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                 }
             }
-            bar_sync(1, kMath);   // the work tiles are dead from here; the operands overwrite them
-            // ---- X round trip: operand X0 (scaled), TMEM <- b_C * X0 (scaled)
+            // ---- X round trip (TMEM only): operand X0 (scaled, hi + lo), X <- b_C X0 (scaled)
             if (j > 0) {
                 const bool okx = mbar_wait(&ctl->x_done, par ^ 1u);
                 if (!bar_and(1, kMath, okx && !*abortp)) {
@@ -390,55 +405,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             tc_fence_after();
+            uint32_t xa[32], xb[32];   // this thread's 64 columns of its X^T row
+            tmem_ld32(tx, xa);
+            tmem_ld32(tx + 32u, xb);
+            tmem_wait_ld();
             float g = 1.f;
             if (half == 0) {
                 float mx = 0.f;
-                for (int cb = 0; cb < 4; ++cb) {
-                    uint32_t r[32];
-                    tmem_ld32(tx + (uint32_t)(cb * 32), r);
-                    tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fabsf(__uint_as_float(r[i])));
-                }
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-                if (lane == 0) ctl->redmax[quarter] = mx;
-                bar_sync(2, 128);
-                mx = fmaxf(fmaxf(ctl->redmax[0], ctl->redmax[1]), fmaxf(ctl->redmax[2], ctl->redmax[3]));
-                bar_sync(2, 128);
-                int e = 0;
-                if (mx > 0.f) {
-                    int ex;
-                    frexpf(mx, &ex);
-                    e = ex - 1;
-                }
+                for (int i = 0; i < 32; ++i)
+                    mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(xa[i])), fabsf(__uint_as_float(xb[i]))));
+                const int e = exponent_of(math_max(mx, ctl, mw, lane));
                 g = ldexpf(1.f, -e);
                 lam_exp += e;
             }
-            const float bC = ctl->bC[par];
-            for (int cb = 0; cb < 4; ++cb) {
-                uint32_t r[32];
-                tmem_ld32(tx + (uint32_t)(cb * 32), r);
-                tmem_wait_ld();
-                // operand row m: channels k = cb*32 .. cb*32+31 -> atom cb/2, chunks (cb&1)*4 ..
-                const int atom = cb >> 1;
+            {
+                uint32_t hi[32], lo[32];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint32_t hi[4], lo[4];
-#pragma unroll
-                    for (int p = 0; p < 4; ++p)
-                        split_pair(g * __uint_as_float(r[q * 8 + 2 * p]), g * __uint_as_float(r[q * 8 + 2 * p + 1]),
-                                   hi[p], lo[p]);
-                    const int c = (cb & 1) * 4 + q;
-                    const int off = atom * 16384 + m * 128 + ((c ^ (m & 7)) << 4);
-                    *reinterpret_cast<uint4 *>(xop + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                    *reinterpret_cast<uint4 *>(xop + kXopPart + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                for (int p = 0; p < 16; ++p) {
+                    split_pair(g * __uint_as_float(xa[2 * p]), g * __uint_as_float(xa[2 * p + 1]), hi[p], lo[p]);
+                    split_pair(g * __uint_as_float(xb[2 * p]), g * __uint_as_float(xb[2 * p + 1]), hi[16 + p],
+                               lo[16 + p]);
                 }
-                const float sc = g * bC;
-#pragma unroll
-                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(sc * __uint_as_float(r[i]));
-                tmem_st32(tx + (uint32_t)(cb * 32), r);
+                tmem_st32(txop, hi);
+                tmem_st32(txop + 64u, lo);
             }
+            const float sc = g * ctl->bC[par];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                xa[i] = __float_as_uint(sc * __uint_as_float(xa[i]));
+                xb[i] = __float_as_uint(sc * __uint_as_float(xb[i]));
+            }
+            tmem_st32(tx, xa);
+            tmem_st32(tx + 32u, xb);
             tmem_wait_st();
             fence_async_smem();
             tc_fence_before();
@@ -453,29 +452,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             {
                 const uint8_t *vt = smem + s * kStage + kTile;
                 const int vbox = m >> 6, vc = (m & 63) >> 3, vw = (m & 7) * 2;
-                for (int cb = 0; cb < 2; ++cb) {
-                    uint32_t r[32], hi[16], lo[16];
-                    tmem_ld32(tacc + (uint32_t)(cb * 32), r);
-                    tmem_wait_ld();
+                uint32_t r[32], hi[16], lo[16];
+                tmem_ld32(tacc, r);
+                tmem_wait_ld();
 #pragma unroll
-                    for (int p = 0; p < 16; ++p) {
-                        float x[2];
+                for (int p = 0; p < 16; ++p) {
+                    float xv[2];
 #pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int t = cb * 32 + 2 * p + e;
-                            float val = -ctl->gbb[par][t] * __uint_as_float(r[2 * p + e]);
-                            if (half) {
-                                const uint16_t vb = *reinterpret_cast<const uint16_t *>(
-                                    vt + vbox * kBox + t * 128 + ((vc ^ (t & 7)) << 4) + vw);
-                                val = fmaf(ctl->gbeta[par][t], __uint_as_float((uint32_t)vb << 16), val);
-                            }
-                            x[e] = val;
+                    for (int e = 0; e < 2; ++e) {
+                        const int t = ch * 32 + 2 * p + e;
+                        float val = -ctl->gbb[par][t] * __uint_as_float(r[2 * p + e]);
+                        if (half) {
+                            const uint16_t vb = *reinterpret_cast<const uint16_t *>(
+                                vt + vbox * kBox + t * 128 + ((vc ^ (t & 7)) << 4) + vw);
+                            val = fmaf(ctl->gbeta[par][t], __uint_as_float((uint32_t)vb << 16), val);
                         }
-                        split_pair(x[0], x[1], hi[p], lo[p]);
+                        xv[e] = val;
                     }
-                    tmem_st16(topr + (uint32_t)(cb * 16), hi);
-                    tmem_st16(topr + 32u + (uint32_t)(cb * 16), lo);
+                    split_pair(xv[0], xv[1], hi[p], lo[p]);
                 }
+                tmem_st16(topr, hi);
+                tmem_st16(topr + 32u, lo);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -487,19 +484,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            for (int cb = 0; cb < 2; ++cb) {
+            {
                 uint32_t r[32], hi[16], lo[16];
-                tmem_ld32(tacc + (uint32_t)(cb * 32), r);
+                tmem_ld32(tacc, r);
                 tmem_wait_ld();
 #pragma unroll
                 for (int p = 0; p < 16; ++p) {
-                    const int t = cb * 32 + 2 * p;
+                    const int t = ch * 32 + 2 * p;
                     split_pair(ctl->gw[par][t] * __uint_as_float(r[2 * p]),
-                               ctl->gw[par][t + 1] * __uint_as_float(r[2 * p + 1]),
-                               hi[p], lo[p]);
+                               ctl->gw[par][t + 1] * __uint_as_float(r[2 * p + 1]), hi[p], lo[p]);
                 }
-                tmem_st16(topr + (uint32_t)(cb * 16), hi);
-                tmem_st16(topr + 32u + (uint32_t)(cb * 16), lo);
+                tmem_st16(topr, hi);
+                tmem_st16(topr + 32u, lo);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -513,38 +509,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (bar_and(1, kMath, ok && !*abortp)) {
             tc_fence_after();
             const int64_t u_out = ((int64_t)l * a.n_seg + seg) * a.H + h;
+            uint32_t xa[32], xb[32];
+            tmem_ld32(tx, xa);
+            tmem_ld32(tx + 32u, xb);
+            tmem_wait_ld();
             float scale = 1.f;
             if (half == 0) {
                 float mx = 0.f;
-                for (int cb = 0; cb < 4; ++cb) {
-                    uint32_t r[32];
-                    tmem_ld32(tx + (uint32_t)(cb * 32), r);
-                    tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fabsf(__uint_as_float(r[i])));
-                }
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-                if (lane == 0) ctl->redmax[quarter] = mx;
-                bar_sync(2, 128);
-                mx = fmaxf(fmaxf(ctl->redmax[0], ctl->redmax[1]), fmaxf(ctl->redmax[2], ctl->redmax[3]));
-                int e = 0;
-                if (mx > 0.f) {
-                    int ex;
-                    frexpf(mx, &ex);
-                    e = ex - 1;
-                }
+                for (int i = 0; i < 32; ++i)
+                    mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(xa[i])), fabsf(__uint_as_float(xb[i]))));
+                const int e = exponent_of(math_max(mx, ctl, mw, lane));
                 scale = ldexpf(1.f, -e);
                 lam_exp += e;
                 if (mt == 0) a.lam_out[u_out] = (float)((double)lam_exp * 0.69314718055994530942);
             }
-            float *out = half == 0 ? a.M_out + u_out * kD * kD : a.S_out + u_out * kD * kD;
-            for (int cb = 0; cb < 4; ++cb) {
-                uint32_t r[32];
-                tmem_ld32(tx + (uint32_t)(cb * 32), r);
-                tmem_wait_ld();
+            float *out = (half == 0 ? a.M_out : a.S_out) + u_out * kD * kD;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) out[(int64_t)(cb * 32 + i) * kD + m] = scale * __uint_as_float(r[i]);
+            for (int i = 0; i < 32; ++i) {
+                out[(int64_t)(ch * 64 + i) * kD + m] = scale * __uint_as_float(xa[i]);
+                out[(int64_t)(ch * 64 + 32 + i) * kD + m] = scale * __uint_as_float(xb[i]);
             }
         }
     }
@@ -596,6 +580,7 @@ bool make_map_bf16(CUtensorMap *m, const void *base, uint64_t H, uint64_t rows) 
 bool scan_dense_tc_supported(const ScanArgs &a) {
     return a.fam == HYPIC_DENSE && a.in_dtype == HYPIC_BF16 && a.dk == 128 && a.dv == 128 &&
            a.o_out == nullptr && a.N > 0 && (int64_t)a.n_layers * a.N < ((int64_t)1 << 31) &&
+           (int64_t)a.n_layers * a.n_seg * a.H < ((int64_t)1 << 30) &&
            encode_fn() != nullptr;
 }
 
@@ -607,7 +592,7 @@ cudaError_t launch_scan_dense_tc(const ScanArgs &a, cudaStream_t s) {
     if (!make_map_bf16(&mk, a.k, a.H, rows) || !make_map_bf16(&mv, a.v, a.H, rows)) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(scan_dense_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    scan_dense_tc_kernel<<<(unsigned)units, kThreads, kSmem, s>>>(mk, mv, a);
+    scan_dense_tc_kernel<<<(unsigned)(2 * units), kThreads, kSmem, s>>>(mk, mv, a);
     return cudaGetLastError();
 }
 
