@@ -11,20 +11,22 @@
 //
 // Every product above acts on one column of X at a time, so the transition
 // half M and the state half S of a chain are handled by two CTAs (launched
-// side by side); each repeats the cheap per-chunk preparation (gates, Gram,
-// inverse).  A CTA keeps its half transposed in TMEM (column m of X on TMEM
-// lane m, key channel k along the columns), so every product is M = 128:
+// side by side).  A CTA keeps its half transposed in TMEM (column m of X on
+// TMEM lane m, key channel k along the columns), so every product is M = 128:
 //   Gram   G   = K K^T                  (bf16 keys, exact products)
 //   P^T        = X0^T K^T               (X0 split into bf16 hi + lo, from TMEM)
 //   Delta^T    = R^T A^T                (3-term bf16 split of both operands)
 //   X^T       += (Delta~)^T K           (Delta~ split hi + lo, K exact)
-// The X0, R and Delta~ operands never leave TMEM (math warps convert them in
-// place with tcgen05.ld / st); only A goes through shared memory.  The
-// transition half is rescaled by a power of two every chunk (exponent into
-// lambda), so T_C = exp(lambda) M with max|M| in [1, 2) at the end.
-// Warp 0: TMA, warp 1: MMA issue, warps 2-9: gates, Gram -> L -> blocked
-// inverse, the TMEM conversions and the epilogue.  Every wait is
-// time-bounded; a timeout is reported as HYPIC_ETIMEOUT.
+// X0, R and Delta~ never leave TMEM (the state warps convert them in place
+// with tcgen05.ld / st); A goes through shared memory.  The transition half is
+// rescaled by a power of two every chunk (exponent into lambda), so
+// T_C = exp(lambda) M with max|M| in [1, 2) at the end.
+//
+// Warp roles: 0 TMA; 1 MMA issue; 2-9 "prep" (gates, Gram -> L -> blocked
+// (I+L)^-1 -> A operand), which depends only on the chunk's keys and gates and
+// runs one chunk ahead; 10-17 "state" (TMEM round trip of X, R, Delta~,
+// epilogue).  Every wait is time-bounded; a timeout is reported as
+// HYPIC_ETIMEOUT.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -40,16 +42,17 @@ using namespace sm100;
 constexpr int kC = 64;          // tokens per chunk
 constexpr int kD = 128;         // d_k = d_v
 constexpr int kNS = 2;          // TMA stages
-constexpr int kThreads = 320;   // 10 warps
-constexpr int kMath = 256;      // warps 2..9
+constexpr int kThreads = 576;   // 18 warps
+constexpr int kPrep = 256;      // warps 2..9
+constexpr int kState = 256;     // warps 10..17
 constexpr int kLd = 65;         // padded row stride of the fp32 L / A work tiles
 
 // shared memory map (offsets from the 1024-aligned base)
 constexpr int kBox = kC * 128;              // 64 channels x 64 tokens, bf16: 8 KB
 constexpr int kTile = 2 * kBox;             // 128 channels: 16 KB
 constexpr int kStage = 2 * kTile;           // K tile, V tile
-constexpr int kAop = kNS * kStage;          // A operand (row t, s contiguous): hi, lo (8 KB each)
-constexpr int kLws = kAop + 2 * 8192;       // fp32 L (64 x 65)
+constexpr int kAop = kNS * kStage;          // A operands, two buffers x (hi, lo) (8 KB each)
+constexpr int kLws = kAop + 4 * 8192;       // fp32 L (64 x 65)
 constexpr int kAws = kLws + kC * kLd * 4;   // fp32 A (64 x 65)
 constexpr int kTws = kAws + kC * kLd * 4;   // fp32 temporaries for the off-diagonal blocks (3 x 16 x 16)
 constexpr int kCtl = kTws + 3 * 256 * 4;
@@ -63,8 +66,9 @@ constexpr uint32_t kTgram = 384;  // Gram (64 columns)
 
 struct DenseCtrl {
     uint64_t full[kNS], empty[kNS];
-    uint64_t gram_done, p_done, d_done, x_done;
+    uint64_t gram_done, gfree, p_done, d_done, x_done;
     uint64_t ops_ready, r_ready, dt_ready;
+    uint64_t gates_ready[2], aop_ready[2], aop_free[2];
     float gl[2][kC], gbb[2][kC], gw[2][kC], gbeta[2][kC];   // per chunk parity: Lambda_t, beta_t b_t,
     float bC[2];                                             // b_C / b_t, beta_t; b_C
     float redmax[8];
@@ -92,19 +96,6 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
     return true;
 }
 
-// max over the 8 math warps (named barrier 1)
-__device__ __forceinline__ float math_max(float mx, DenseCtrl *ctl, int mw, int lane) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    if (lane == 0) ctl->redmax[mw] = mx;
-    bar_sync(1, kMath);
-    mx = 0.f;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) mx = fmaxf(mx, ctl->redmax[w]);
-    bar_sync(1, kMath);
-    return mx;
-}
-
 __device__ __forceinline__ int exponent_of(float mx) {   // 2^e <= mx < 2^(e+1)
     if (!(mx > 0.f)) return 0;
     int ex;
@@ -112,7 +103,47 @@ __device__ __forceinline__ int exponent_of(float mx) {   // 2^e <= mx < 2^(e+1)
     return ex - 1;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// max over the 8 state warps (named barrier 2)
+__device__ __forceinline__ float state_max(float mx, DenseCtrl *ctl, int sw, int lane) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (lane == 0) ctl->redmax[sw] = mx;
+    bar_sync(2, kState);
+    mx = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) mx = fmaxf(mx, ctl->redmax[w]);
+    bar_sync(2, kState);
+    return mx;
+}
+
+// Off-diagonal blocks of A = (I + L)^-1 at block distance DIST:
+//   T = sum_{k=j}^{i-1} L_ik A_kj,  A_ij = -A_ii T   (16 x 16 blocks).
+template <int DIST>
+__device__ __forceinline__ void inverse_level(const float *Lw, float *Aw, float *Tw, int pt) {
+    constexpr int NB = 4 - DIST;
+    for (int e = pt; e < NB * 256; e += kPrep) {
+        const int bi = (e >> 8) + DIST, bj = bi - DIST, r = (e >> 4) & 15, c = e & 15;
+        const float *lrow = Lw + (bi * 16 + r) * kLd + bj * 16;
+        const float *acol = Aw + (bj * 16) * kLd + bj * 16 + c;
+        float acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16 * DIST; ++k) acc = fmaf(lrow[k], acol[k * kLd], acc);
+        Tw[(e >> 8) * 256 + r * 16 + c] = acc;
+    }
+    bar_sync(1, kPrep);
+    for (int e = pt; e < NB * 256; e += kPrep) {
+        const int bi = (e >> 8) + DIST, bj = bi - DIST, r = (e >> 4) & 15, c = e & 15;
+        const float *arow = Aw + (bi * 16 + r) * kLd + bi * 16;   // A_ii, zero above the diagonal
+        const float *tcol = Tw + (e >> 8) * 256 + c;
+        float acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) acc = fmaf(arow[k], tcol[k * 16], acc);
+        Aw[(bi * 16 + r) * kLd + bj * 16 + c] = -acc;
+    }
+    bar_sync(1, kPrep);
+}
+
+__global__ void __maxnreg__(112)
     scan_dense_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                          const ScanArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -120,9 +151,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                 ~static_cast<uintptr_t>(1023));
     DenseCtrl *ctl = reinterpret_cast<DenseCtrl *>(smem + kCtl);
     volatile int *abortp = &ctl->abort;
-    float *Lw = reinterpret_cast<float *>(smem + kLws);
-    float *Aw = reinterpret_cast<float *>(smem + kAws);
-    float *Tw = reinterpret_cast<float *>(smem + kTws);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     const int half = blockIdx.x & 1;   // 0: transition M, 1: state S
@@ -143,12 +171,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&ctl->empty[s], 1);
         }
         mbar_init(&ctl->gram_done, 1);
+        mbar_init(&ctl->gfree, 4);
         mbar_init(&ctl->p_done, 1);
         mbar_init(&ctl->d_done, 1);
         mbar_init(&ctl->x_done, 1);
-        mbar_init(&ctl->ops_ready, kMath / 32);
-        mbar_init(&ctl->r_ready, kMath / 32);
-        mbar_init(&ctl->dt_ready, kMath / 32);
+        mbar_init(&ctl->ops_ready, kState / 32);
+        mbar_init(&ctl->r_ready, kState / 32);
+        mbar_init(&ctl->dt_ready, kState / 32);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&ctl->gates_ready[b], 1);
+            mbar_init(&ctl->aop_ready[b], kPrep / 32);
+            mbar_init(&ctl->aop_free[b], 1);
+        }
         ctl->abort = 0;
         mbar_fence_init();
         tma_prefetch(&tm_k);
@@ -187,14 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t id_n64 = idesc_bf16_f32(128, 64, false, false);     // A, B K-major
             constexpr uint32_t id_u = idesc_bf16_f32(128, 128, false, true);       // B = K (MN-major)
-            const uint32_t aop = smem_addr(smem + kAop);
-            for (int j = 0; j < nc; ++j) {
-                const int s = j % kNS;
-                const uint32_t par = (uint32_t)j & 1u;
-                const uint32_t kb = smem_addr(smem + s * kStage);
-                if (!wait_or_abort(&ctl->full[s], (uint32_t)(j / kNS) & 1u, abortp)) break;
-                tc_fence_after();
-                // G = K K^T (M padded to 128 rows; rows >= 64 are not used)
+            auto gram = [&](int j) {   // G = K K^T (M padded to 128 rows; rows >= 64 unused)
+                const uint32_t kb = smem_addr(smem + (j % kNS) * kStage);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     const uint32_t off = (uint32_t)(ks >> 2) * kBox + (uint32_t)(ks & 3) * 32u;
@@ -202,6 +230,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                             id_n64, ks > 0);
                 }
                 mma_commit(&ctl->gram_done);
+            };
+            bool run = nc > 0 && wait_or_abort(&ctl->full[0], 0, abortp);
+            if (run) {
+                tc_fence_after();
+                gram(0);
+            }
+            for (int j = 0; run && j < nc; ++j) {
+                const int s = j % kNS;
+                const uint32_t par = (uint32_t)j & 1u;
+                const uint32_t kb = smem_addr(smem + s * kStage);
                 // P^T = X0^T K^T, X0 as hi + lo
                 if (!wait_or_abort(&ctl->ops_ready, par, abortp)) break;
                 tc_fence_after();
@@ -213,9 +251,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_f16_ta(tmem + kTacc, tmem + kTxop + 64u + (uint32_t)ks * 8u, bd, id_n64, 1u);
                 }
                 mma_commit(&ctl->p_done);
+                // next chunk's Gram as soon as its keys are in and the prep warps read this one
+                if (j + 1 < nc) {
+                    if (!wait_or_abort(&ctl->full[(j + 1) % kNS], (uint32_t)((j + 1) / kNS) & 1u, abortp) ||
+                        !wait_or_abort(&ctl->gfree, par, abortp))
+                        break;
+                    tc_fence_after();
+                    gram(j + 1);
+                }
                 // Delta^T = R^T A^T, three-term split
-                if (!wait_or_abort(&ctl->r_ready, par, abortp)) break;
+                if (!wait_or_abort(&ctl->r_ready, par, abortp) ||
+                    !wait_or_abort(&ctl->aop_ready[par], (uint32_t)(j >> 1) & 1u, abortp))
+                    break;
                 tc_fence_after();
+                const uint32_t aop = smem_addr(smem + kAop + (int)par * 16384);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
                     const uint64_t ah = smem_desc_sw128(aop + (uint32_t)ks * 32u, 0, 1024);
@@ -226,6 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_f16_ta(tmem + kTacc, tmem + kTopr + 32u + c, ah, id_n64, 1u);
                 }
                 mma_commit(&ctl->d_done);
+                mma_commit(&ctl->aop_free[par]);
                 // X^T += Delta~^T K (K as the MN-major B operand: row t, channels contiguous)
                 if (!wait_or_abort(&ctl->dt_ready, par, abortp)) break;
                 tc_fence_after();
@@ -240,36 +290,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(&ctl->empty[s]);
             }
             if (*abortp) {
-                mma_commit(&ctl->gram_done);   // drain: completes once issued MMAs are done
-                mbar_wait(&ctl->gram_done, nc & 1);
+                mma_commit(&ctl->p_done);   // drain: completes once issued MMAs are done
+                mbar_wait(&ctl->p_done, nc & 1);
             }
         }
-    } else {
-        // ------------------------------------------------------------ math warps
-        const int mt = threadIdx.x - 64;            // 0..255
-        const int mw = warp - 2;                    // 0..7
-        const int ch = mw >> 2;                     // which half of the columns this warp converts
-        const int quarter = warp & 3;               // TMEM lanes this warp may touch
-        const int m = quarter * 32 + lane;          // column of X = TMEM lane
-        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const uint32_t tx = tmem + lane_off + kTx + (uint32_t)(ch * 64);
-        const uint32_t txop = tmem + lane_off + kTxop + (uint32_t)(ch * 32);
-        const uint32_t tacc = tmem + lane_off + kTacc + (uint32_t)(ch * 32);
-        const uint32_t topr = tmem + lane_off + kTopr + (uint32_t)(ch * 16);
-        int lam_exp = 0;                            // power-of-two exponent moved out of M
-
-        // initial X^T: identity (transition) or zero (state)
-        {
-            uint32_t r[32];
-            for (int cb = 0; cb < 2; ++cb) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    r[i] = __float_as_uint((half == 0 && ch * 64 + cb * 32 + i == m) ? 1.f : 0.f);
-                tmem_st32(tx + (uint32_t)(cb * 32), r);
-            }
-            tmem_wait_st();
-        }
-
+    } else if (warp < 10) {
+        // ------------------------------------------------------------ prep warps
+        const int pt = threadIdx.x - 64;            // 0..255
+        const int quarter = warp & 3;
+        const int gcol = (warp - 2) >> 2;           // Gram column half this warp reads
+        float *Lw = reinterpret_cast<float *>(smem + kLws);
+        float *Aw = reinterpret_cast<float *>(smem + kAws);
+        float *Tw = reinterpret_cast<float *>(smem + kTws);
         float pa[2], pb[2];
         auto prefetch = [&](int j) {
 #pragma unroll
@@ -282,11 +314,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         };
         if (warp == 2) prefetch(0);
-
         for (int j = 0; j < nc; ++j) {
-            const int s = j % kNS;
             const uint32_t par = (uint32_t)j & 1u;
-            // ---- gates: Lambda (inclusive in-chunk log decay), beta b, b_C / b
+            if (!bar_and(1, kPrep, mbar_wait(&ctl->gram_done, par) && !*abortp)) {
+                *abortp = 1;
+                break;
+            }
+            // ---- gates: Lambda (inclusive in-chunk log decay), beta b, b_C / b.  Written only
+            // after Gram(j) exists: the state warps are then done with chunk j-2 (same buffer).
             if (warp == 2) {
                 float lg[2], inc[2];
 #pragma unroll
@@ -313,34 +348,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ctl->gbeta[par][t] = pb[q];
                 }
                 if (lane == 0) ctl->bC[par] = expf(total);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->gates_ready[par]);
                 if (j + 1 < nc) prefetch(j + 1);
             }
-            const bool ok_full = mbar_wait(&ctl->full[s], (uint32_t)(j / kNS) & 1u);
-            const bool ok_g = ok_full && mbar_wait(&ctl->gram_done, par);
-            if (!bar_and(1, kMath, ok_g && !*abortp)) {
-                *abortp = 1;
-                break;
-            }
+            bar_sync(1, kPrep);
             tc_fence_after();
             // ---- L[t][s] = beta_t exp(Lambda_t - Lambda_s) G[t][s] for s < t (rows t < 64)
             if (quarter < 2) {
-                const int t = m;   // 0..63
+                const int t = quarter * 32 + lane;   // 0..63
                 uint32_t r[32];
-                tmem_ld32(tmem + lane_off + kTgram + (uint32_t)(ch * 32), r);
+                tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + kTgram + (uint32_t)(gcol * 32), r);
                 tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->gfree);   // the Gram columns may be overwritten
                 const float lt = ctl->gl[par][t], bt = ctl->gbeta[par][t];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const int sc = ch * 32 + i;
+                    const int sc = gcol * 32 + i;
                     Lw[t * kLd + sc] = sc < t ? bt * __expf(lt - ctl->gl[par][sc]) * __uint_as_float(r[i]) : 0.f;
                 }
             }
-            tc_fence_before();
-            bar_sync(1, kMath);
-            // ---- A = (I + L)^-1: 16 x 16 diagonal blocks by forward substitution
-            if (mt < 64) {
-                const int b0 = (mt >> 4) * 16, jc = mt & 15, col = b0 + jc;
-                float ac[16];   // column jc of the block inverse, in registers
+            bar_sync(1, kPrep);
+            // ---- A = (I + L)^-1: 16 x 16 diagonal blocks by forward substitution (registers)
+            if (pt < 64) {
+                const int b0 = (pt >> 4) * 16, jc = pt & 15, col = b0 + jc;
+                float ac[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     float sum = 0.f;
@@ -352,38 +386,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < 16; ++i) Aw[(b0 + i) * kLd + col] = ac[i];
             } else {
                 // zero the strictly upper off-diagonal blocks
-                for (int e = mt - 64; e < 6 * 256; e += kMath - 64) {
+                for (int e = pt - 64; e < 6 * 256; e += kPrep - 64) {
                     const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15;
                     const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
                     const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
                     Aw[(bi * 16 + r) * kLd + bj * 16 + c] = 0.f;
                 }
             }
-            bar_sync(1, kMath);
-            // off-diagonal blocks, one sub-diagonal at a time:
-            //   T = sum_{k=j}^{i-1} L_ik A_kj,  A_ij = -A_ii T
-            for (int dist = 1; dist < 4; ++dist) {
-                const int nblk = 4 - dist;
-                for (int e = mt; e < nblk * 256; e += kMath) {
-                    const int bi = (e >> 8) + dist, bj = bi - dist, r = (e >> 4) & 15, c = e & 15;
-                    float acc = 0.f;
-                    for (int k = bj * 16; k < bi * 16; ++k)
-                        acc = fmaf(Lw[(bi * 16 + r) * kLd + k], Aw[k * kLd + bj * 16 + c], acc);
-                    Tw[(e >> 8) * 256 + r * 16 + c] = acc;
-                }
-                bar_sync(1, kMath);
-                for (int e = mt; e < nblk * 256; e += kMath) {
-                    const int bi = (e >> 8) + dist, bj = bi - dist, r = (e >> 4) & 15, c = e & 15;
-                    float acc = 0.f;
-                    for (int k = 0; k <= r; ++k)
-                        acc = fmaf(Aw[(bi * 16 + r) * kLd + bi * 16 + k], Tw[(e >> 8) * 256 + k * 16 + c], acc);
-                    Aw[(bi * 16 + r) * kLd + bj * 16 + c] = -acc;
-                }
-                bar_sync(1, kMath);
+            bar_sync(1, kPrep);
+            inverse_level<1>(Lw, Aw, Tw, pt);
+            inverse_level<2>(Lw, Aw, Tw, pt);
+            inverse_level<3>(Lw, Aw, Tw, pt);
+            // ---- A -> bf16 hi / lo operand tiles (row t, s contiguous, 128-byte swizzle)
+            if (!bar_and(1, kPrep, mbar_wait(&ctl->aop_free[par], ((uint32_t)(j >> 1) & 1u) ^ 1u) && !*abortp)) {
+                *abortp = 1;
+                break;
             }
-            // A -> bf16 hi / lo operand tiles (row t, s contiguous, 128-byte swizzle)
             {
-                const int t = mt >> 2, c0 = (mt & 3) * 2;   // two 8-element chunks per thread
+                uint8_t *aop = smem + kAop + (int)par * 16384;
+                const int t = pt >> 2, c0 = (pt & 3) * 2;   // two 8-element chunks per thread
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
                     const int c = c0 + cc;
@@ -392,59 +413,87 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int p = 0; p < 4; ++p)
                         split_pair(Aw[t * kLd + c * 8 + 2 * p], Aw[t * kLd + c * 8 + 2 * p + 1], hi[p], lo[p]);
                     const int off = t * 128 + ((c ^ (t & 7)) << 4);
-                    *reinterpret_cast<uint4 *>(smem + kAop + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                    *reinterpret_cast<uint4 *>(smem + kAop + 8192 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    *reinterpret_cast<uint4 *>(aop + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4 *>(aop + 8192 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                 }
             }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->aop_ready[par]);
+            bar_sync(1, kPrep);   // the work tiles are reused by the next chunk
+        }
+    } else {
+        // ------------------------------------------------------------ state warps
+        const int st = threadIdx.x - 320;           // 0..255
+        const int sw = warp - 10;                   // 0..7
+        const int ch = sw >> 2;                     // which half of the columns this warp converts
+        const int quarter = warp & 3;               // TMEM lanes this warp may touch
+        const int m = quarter * 32 + lane;          // column of X = TMEM lane
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t tx = tmem + lane_off + kTx + (uint32_t)(ch * 64);
+        const uint32_t txop = tmem + lane_off + kTxop + (uint32_t)(ch * 32);
+        const uint32_t tacc = tmem + lane_off + kTacc + (uint32_t)(ch * 32);
+        const uint32_t topr = tmem + lane_off + kTopr + (uint32_t)(ch * 16);
+        int lam_exp = 0;                            // power-of-two exponent moved out of M
+
+        // initial X^T: identity (transition) or zero (state)
+        {
+            uint32_t r[32];
+            for (int cb = 0; cb < 2; ++cb) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    r[i] = __float_as_uint((half == 0 && ch * 64 + cb * 32 + i == m) ? 1.f : 0.f);
+                tmem_st32(tx + (uint32_t)(cb * 32), r);
+            }
+            tmem_wait_st();
+        }
+
+        for (int j = 0; j < nc; ++j) {
+            const int s = j % kNS;
+            const uint32_t par = (uint32_t)j & 1u;
             // ---- X round trip (TMEM only): operand X0 (scaled, hi + lo), X <- b_C X0 (scaled)
-            if (j > 0) {
-                const bool okx = mbar_wait(&ctl->x_done, par ^ 1u);
-                if (!bar_and(1, kMath, okx && !*abortp)) {
-                    *abortp = 1;
-                    break;
-                }
+            bool ok = mbar_wait(&ctl->gates_ready[par], (uint32_t)(j >> 1) & 1u);
+            if (j > 0) ok = ok && mbar_wait(&ctl->x_done, par ^ 1u);
+            if (!bar_and(2, kState, ok && !*abortp)) {
+                *abortp = 1;
+                break;
             }
             tc_fence_after();
-            uint32_t xa[32], xb[32];   // this thread's 64 columns of its X^T row
-            tmem_ld32(tx, xa);
-            tmem_ld32(tx + 32u, xb);
-            tmem_wait_ld();
             float g = 1.f;
             if (half == 0) {
                 float mx = 0.f;
+                for (int cb = 0; cb < 2; ++cb) {
+                    uint32_t r[32];
+                    tmem_ld32(tx + (uint32_t)(cb * 32), r);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(xa[i])), fabsf(__uint_as_float(xb[i]))));
-                const int e = exponent_of(math_max(mx, ctl, mw, lane));
+                    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fabsf(__uint_as_float(r[i])));
+                }
+                const int e = exponent_of(state_max(mx, ctl, sw, lane));
                 g = ldexpf(1.f, -e);
                 lam_exp += e;
             }
-            {
-                uint32_t hi[32], lo[32];
-#pragma unroll
-                for (int p = 0; p < 16; ++p) {
-                    split_pair(g * __uint_as_float(xa[2 * p]), g * __uint_as_float(xa[2 * p + 1]), hi[p], lo[p]);
-                    split_pair(g * __uint_as_float(xb[2 * p]), g * __uint_as_float(xb[2 * p + 1]), hi[16 + p],
-                               lo[16 + p]);
-                }
-                tmem_st32(txop, hi);
-                tmem_st32(txop + 64u, lo);
-            }
             const float sc = g * ctl->bC[par];
+            for (int cb = 0; cb < 2; ++cb) {
+                uint32_t r[32], hi[16], lo[16];
+                tmem_ld32(tx + (uint32_t)(cb * 32), r);
+                tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                xa[i] = __float_as_uint(sc * __uint_as_float(xa[i]));
-                xb[i] = __float_as_uint(sc * __uint_as_float(xb[i]));
+                for (int p = 0; p < 16; ++p)
+                    split_pair(g * __uint_as_float(r[2 * p]), g * __uint_as_float(r[2 * p + 1]), hi[p], lo[p]);
+                tmem_st16(txop + (uint32_t)(cb * 16), hi);
+                tmem_st16(txop + 64u + (uint32_t)(cb * 16), lo);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(sc * __uint_as_float(r[i]));
+                tmem_st32(tx + (uint32_t)(cb * 32), r);
             }
-            tmem_st32(tx, xa);
-            tmem_st32(tx + 32u, xb);
             tmem_wait_st();
-            fence_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->ops_ready);
             // ---- R^T = beta [0 | V]^T - (beta b) P^T  -> TMEM operand (hi, lo)
-            if (!bar_and(1, kMath, mbar_wait(&ctl->p_done, par) && !*abortp)) {
+            ok = mbar_wait(&ctl->p_done, par) && mbar_wait(&ctl->full[s], (uint32_t)(j / kNS) & 1u);
+            if (!bar_and(2, kState, ok && !*abortp)) {
                 *abortp = 1;
                 break;
             }
@@ -479,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->r_ready);
             // ---- Delta~^T = Delta^T diag(b_C / b)  -> TMEM operand (hi, lo)
-            if (!bar_and(1, kMath, mbar_wait(&ctl->d_done, par) && !*abortp)) {
+            if (!bar_and(2, kState, mbar_wait(&ctl->d_done, par) && !*abortp)) {
                 *abortp = 1;
                 break;
             }
@@ -506,29 +555,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ epilogue
         bool ok = true;
         if (nc > 0) ok = mbar_wait(&ctl->x_done, (uint32_t)(nc - 1) & 1u);
-        if (bar_and(1, kMath, ok && !*abortp)) {
+        if (bar_and(2, kState, ok && !*abortp)) {
             tc_fence_after();
             const int64_t u_out = ((int64_t)l * a.n_seg + seg) * a.H + h;
-            uint32_t xa[32], xb[32];
-            tmem_ld32(tx, xa);
-            tmem_ld32(tx + 32u, xb);
-            tmem_wait_ld();
             float scale = 1.f;
             if (half == 0) {
                 float mx = 0.f;
+                for (int cb = 0; cb < 2; ++cb) {
+                    uint32_t r[32];
+                    tmem_ld32(tx + (uint32_t)(cb * 32), r);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(xa[i])), fabsf(__uint_as_float(xb[i]))));
-                const int e = exponent_of(math_max(mx, ctl, mw, lane));
+                    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fabsf(__uint_as_float(r[i])));
+                }
+                const int e = exponent_of(state_max(mx, ctl, sw, lane));
                 scale = ldexpf(1.f, -e);
                 lam_exp += e;
-                if (mt == 0) a.lam_out[u_out] = (float)((double)lam_exp * 0.69314718055994530942);
+                if (st == 0) a.lam_out[u_out] = (float)((double)lam_exp * 0.69314718055994530942);
             }
             float *out = (half == 0 ? a.M_out : a.S_out) + u_out * kD * kD;
+            for (int cb = 0; cb < 2; ++cb) {
+                uint32_t r[32];
+                tmem_ld32(tx + (uint32_t)(cb * 32), r);
+                tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                out[(int64_t)(ch * 64 + i) * kD + m] = scale * __uint_as_float(xa[i]);
-                out[(int64_t)(ch * 64 + 32 + i) * kD + m] = scale * __uint_as_float(xb[i]);
+                for (int i = 0; i < 32; ++i)
+                    out[(int64_t)(ch * 64 + cb * 32 + i) * kD + m] = scale * __uint_as_float(r[i]);
             }
         }
     }
