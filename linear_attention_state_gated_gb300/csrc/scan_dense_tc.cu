@@ -143,7 +143,7 @@ __device__ __forceinline__ void inverse_level(const float *Lw, float *Aw, float 
     bar_sync(1, kPrep);
 }
 
-__global__ void __maxnreg__(112)
+__global__ void __launch_bounds__(kThreads, 1)   // 18 warps: <= 96 registers per thread
     scan_dense_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                          const ScanArgs a) {
     extern __shared__ uint8_t smem_raw[];
