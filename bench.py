@@ -342,6 +342,89 @@ def run_chain(args):
     return res
 
 
+def run_long_mix(args):
+    """131072-token prompt = 64 x 2048-token segments, gated delta rule, 30 layers
+    x 32 heads: 48 cached segments (scanned before the timed region), then per
+    step: scan the 16 uncached segments with o_t and fold all 64 pairs in prompt
+    order (one chain per (layer, head))."""
+    import torch
+    import linear_attention_state_gated_gb300 as hy
+    from linear_attention_state_gated_gb300 import workloads as wl
+    n_seg, L, Lyr, H, d = 64, 2048, 30, 32, 128
+    unc = [int(x) for x in wl.long_mix_split(n_seg=n_seg)]
+    dev = torch.device("cuda")
+    segs = [wl.long_mix_segment_device(s, seg_len=L, n_layers=Lyr, H=H, d=d, with_q=s in unc)
+            for s in range(n_seg)]
+    offs = torch.tensor([0, L], dtype=torch.int64, device=dev)
+    pool_lam = torch.empty((n_seg, Lyr, H), dtype=torch.float32, device=dev)
+    pool_M = torch.empty((n_seg, Lyr, H, d, d), dtype=torch.float32, device=dev)
+    pool_S = torch.empty((n_seg, Lyr, H, d, d), dtype=torch.float32, device=dev)
+    o = {s: torch.empty((Lyr, L, H, d), dtype=torch.bfloat16, device=dev) for s in unc}
+
+    def scan(s, want_o):
+        w = segs[s]
+        out = {"lam": pool_lam[s].view(Lyr, 1, H), "M": pool_M[s].view(Lyr, 1, H, d, d),
+               "S": pool_S[s].view(Lyr, 1, H, d, d)}
+        if want_o:
+            out["o"] = o[s]
+        hy.segment_scan(2, w["k"], w["v"], w["alpha"], offs, beta=w["beta"], q=w.get("q"),
+                        want_o=want_o, out=out)
+
+    for s in range(n_seg):
+        if s not in unc:
+            scan(s, False)
+    clen = torch.tensor([n_seg], dtype=torch.int32, device=dev)
+    idx = torch.arange(n_seg, dtype=torch.int32, device=dev)[None]
+    S_fin = torch.empty((1, Lyr, H, d, d), dtype=torch.float32, device=dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record()
+        for s in unc:
+            scan(s, True)
+        if ev is not None:
+            ev[1].record()
+        hy.compose_chain(2, clen, idx, pool_lam, pool_S, pool_M=pool_M, S_out=S_fin)
+        if ev is not None:
+            ev[2].record()
+
+    step()
+    torch.cuda.synchronize()
+    reps = 2
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps)]
+    for e in evs:
+        step(e)
+    torch.cuda.synchronize()
+    t_scan = sum(e[0].elapsed_time(e[1]) for e in evs) / reps / 1e3
+    t_chain = sum(e[1].elapsed_time(e[2]) for e in evs) / reps / 1e3
+    t = t_scan + t_chain
+    # state-only scan of one uncached segment (the tensor-core path) for reference
+    w = segs[unc[0]]
+    tmp = {"lam": torch.empty((Lyr, 1, H), device=dev), "M": torch.empty((Lyr, 1, H, d, d), device=dev),
+           "S": torch.empty((Lyr, 1, H, d, d), device=dev)}
+    hy.segment_scan(2, w["k"], w["v"], w["alpha"], offs, beta=w["beta"], out=tmp)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    hy.segment_scan(2, w["k"], w["v"], w["alpha"], offs, beta=w["beta"], out=tmp)
+    e1.record()
+    torch.cuda.synchronize()
+    t_state_only = e0.elapsed_time(e1) / 1e3
+    hbm, _, _, src = peaks()
+    chain_bytes = n_seg * Lyr * H * (2 * 4 * d * d + 4) + Lyr * H * 4 * d * d
+    res = {"workload": "131072-token prompt, 64 x 2048-token segments (48 cached, 16 uncached), gated delta "
+                       "rule, 30 layers x 32 heads x 128",
+           "value": n_seg * L / t, "unit": "prompt tokens/s", "ms": t * 1e3,
+           "scan_uncached_with_o_ms": t_scan * 1e3, "chain_ms": t_chain * 1e3,
+           "composes_per_s": n_seg * Lyr / t_chain,
+           "scan_state_only_one_segment_ms": t_state_only * 1e3,
+           "chain_roofline": {"bound": "hbm", "achieved": chain_bytes / t_chain / 1e9, "peak": hbm,
+                              "unit": "GB/s", "frac": chain_bytes / t_chain / 1e9 / hbm,
+                              "peak_kind": f"copy, {src}"}}
+    del segs, pool_M, pool_S, o
+    torch.cuda.empty_cache()
+    return res
+
+
 # ------------------------------------------------------------------ oracle (CPU)
 
 _SAMPLE_CACHE = {}
@@ -421,7 +504,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="hypic", choices=["hypic", "reference"])
     ap.add_argument("--L", type=int, default=8192)
-    ap.add_argument("--rows", default="dense,chain", help="extra rows: dense,chain or none")
+    ap.add_argument("--rows", default="dense,chain,mix", help="extra rows: dense,chain,mix or none")
     ap.add_argument("--dense-L", type=int, default=2048)
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args()
@@ -443,6 +526,8 @@ def main():
         rows["dense_scan"] = run_dense(args, args.dense_L)
     if rank == 0 and "chain" in args.rows:
         rows["rag_chain"] = run_chain(args)
+    if rank == 0 and "mix" in args.rows:
+        rows["long_mix"] = run_long_mix(args)
     if rank != 0:
         barrier(world)
         return

@@ -244,14 +244,45 @@ def rag_requests(R: int = 64, n: int = 20, P: int = 200, zipf_s: float = 1.1, se
     return np.full(R, n, dtype=np.int32), idx
 
 
-def long_mix(n_seg: int = 64, seg_len: int = 2048, n_uncached: int = 16, n_layers: int = 30,
-             H: int = 32, d: int = 128, seed: int = 4):
-    """A long prompt of n_seg equal segments (dense gate law of ``dense_stack``).
-
-    Returns the full-prompt inputs plus which segments are uncached (a seeded
-    choice of n_uncached); the others are cached.
-    """
-    w = dense_stack(seg_len, n_layers=n_layers, H=H, d=d, seed=seed, with_q=True, n_seg=n_seg)
+def long_mix_split(n_seg: int = 64, n_uncached: int = 16, seed: int = 4):
+    """Which segments of the long prompt are uncached: a seeded choice of n_uncached."""
     g = rng(seed + 1000)
-    w["uncached"] = np.sort(g.permutation(n_seg)[:n_uncached]).astype(np.int64)
-    return w
+    return np.sort(g.permutation(n_seg)[:n_uncached]).astype(np.int64)
+
+
+def long_mix_segment_device(seg: int, seg_len: int = 2048, n_layers: int = 30, H: int = 32,
+                            d: int = 128, seed: int = 4, with_q: bool = True, device="cuda",
+                            layers=None, heads=None):
+    """One segment of the long-context mix, drawn on the GPU (torch's seeded
+    generator; the full prompt is ~72 GB of inputs, too much to draw on the host).
+
+    Gate law of ``dense_stack``: bf16 q, v ~ N(0,1), k L2-normalised N(0,1);
+    alpha = exp(-0.1 softplus(N(0,1))), beta = sigmoid(N(0,1)).  Layer l draws
+    from a generator seeded with (seed, segment, layer), so any layer (and head
+    slice) can be drawn again alone.  Tensors: q, k, v [Lyr, L, H, d] bf16,
+    alpha, beta [Lyr, L, H] fp32, contiguous per segment.
+    """
+    import torch
+    layers = list(range(n_layers)) if layers is None else list(layers)
+    nl = len(layers)
+    out = {"k": torch.empty((nl, seg_len, H, d), dtype=torch.bfloat16, device=device),
+           "v": torch.empty((nl, seg_len, H, d), dtype=torch.bfloat16, device=device),
+           "alpha": torch.empty((nl, seg_len, H), dtype=torch.float32, device=device),
+           "beta": torch.empty((nl, seg_len, H), dtype=torch.float32, device=device)}
+    if with_q:
+        out["q"] = torch.empty((nl, seg_len, H, d), dtype=torch.bfloat16, device=device)
+    for i, l in enumerate(layers):
+        g = torch.Generator(device=device)
+        g.manual_seed(((seed * 1000003 + seg) * 1000003 + l) % (2 ** 63))
+        k = torch.randn((seg_len, H, d), generator=g, device=device)
+        out["k"][i] = (k / k.norm(dim=-1, keepdim=True).clamp_min(1e-30)).to(torch.bfloat16)
+        out["v"][i] = torch.randn((seg_len, H, d), generator=g, device=device).to(torch.bfloat16)
+        q = torch.randn((seg_len, H, d), generator=g, device=device)
+        if with_q:
+            out["q"][i] = q.to(torch.bfloat16)
+        a = torch.randn((seg_len, H), generator=g, device=device)
+        out["alpha"][i] = torch.exp(-0.1 * torch.nn.functional.softplus(a))
+        out["beta"][i] = torch.sigmoid(torch.randn((seg_len, H), generator=g, device=device))
+    if heads is not None:
+        out = {key: t[:, :, heads].contiguous() for key, t in out.items()}
+    return out

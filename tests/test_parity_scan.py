@@ -191,3 +191,59 @@ def test_bad_offsets_flag_error_without_fault():
     torch.cuda.synchronize()
     assert int(err.item()) == -5
     assert torch.all(got["S"][:, 1] == 0)
+
+
+def test_long_mix_full_size_sampled():
+    """131072-token prompt, 64 x 2048 segments (48 cached / 16 uncached), gated
+    delta rule, 30 layers x 32 heads (the benchmark's launches): the state folded
+    over all 64 pairs equals the straight recurrence over the prompt (sampled
+    layer and head, oracle), segment-boundary states equal the oracle's own
+    composition of its pairs, and o_t of an uncached segment equals the
+    oracle's isolated scan."""
+    import torch
+    import linear_attention_state_gated_gb300 as hy
+    n_seg, L, Lyr, H, d = 64, 2048, 30, 32, 128
+    unc = [int(x) for x in wl.long_mix_split(n_seg=n_seg)]
+    dev = torch.device("cuda")
+    offs = torch.tensor([0, L], dtype=torch.int64, device=dev)
+    pool_lam = torch.empty((n_seg, Lyr, H), dtype=torch.float32, device=dev)
+    pool_M = torch.empty((n_seg, Lyr, H, d, d), dtype=torch.float32, device=dev)
+    pool_S = torch.empty((n_seg, Lyr, H, d, d), dtype=torch.float32, device=dev)
+    o_first = None
+    for s in range(n_seg):
+        w = wl.long_mix_segment_device(s, seg_len=L, n_layers=Lyr, H=H, d=d, with_q=s in unc)
+        out = {"lam": pool_lam[s].view(Lyr, 1, H), "M": pool_M[s].view(Lyr, 1, H, d, d),
+               "S": pool_S[s].view(Lyr, 1, H, d, d)}
+        r = hy.segment_scan(2, w["k"], w["v"], w["alpha"], offs, beta=w["beta"], q=w.get("q"),
+                            want_o=s == unc[0], out=out)
+        if s == unc[0]:
+            o_first = r["o"]
+        del w
+    # prefix chains: request r folds segments 0..r
+    clen = torch.arange(1, n_seg + 1, dtype=torch.int32, device=dev)
+    idx = torch.arange(n_seg, dtype=torch.int32, device=dev)[None].repeat(n_seg, 1).contiguous()
+    l, h = 17, 5
+    S_pref = hy.compose_chain(2, clen, idx, pool_lam[:, l:l + 1].contiguous(),
+                              pool_S[:, l:l + 1].contiguous(), pool_M=pool_M[:, l:l + 1].contiguous())
+    S_pref = to_host(S_pref[:, 0, h])
+    # oracle: inputs of the sampled layer and head for every segment
+    parts = [wl.long_mix_segment_device(s, seg_len=L, n_layers=Lyr, H=H, d=d, layers=[l], heads=[h])
+             for s in range(n_seg)]
+    cat = {key: torch.cat([p[key] for p in parts], dim=1).float().cpu().numpy().astype(np.float64)
+           for key in ("k", "v", "alpha", "beta", "q")}
+    seq = oracle.sequential(DENSE, cat["k"], cat["v"], cat["alpha"], cat["beta"])
+    assert rel_fro(S_pref[-1], seq["S"][0, 0]) <= TOL_SCAN_BF16
+    seg_pairs = oracle.segment_scan(DENSE, cat["k"], cat["v"], cat["alpha"],
+                                    np.arange(n_seg + 1, dtype=np.int64) * L, beta=cat["beta"])
+    pl = np.moveaxis(seg_pairs["lam"], 1, 0)
+    pS = np.moveaxis(seg_pairs["S"], 1, 0)
+    pM = np.moveaxis(seg_pairs["M"], 1, 0)
+    for r in (0, 15, 31, 62):
+        ref = oracle.compose_chain(DENSE, [r + 1], np.arange(n_seg, dtype=np.int32)[None], pl, pS, pool_M=pM)
+        assert rel_fro(S_pref[r], ref[0, 0, 0]) <= TOL_SCAN_BF16, r
+    # o_t of the first uncached segment from its own zero start
+    a0 = unc[0] * L
+    iso = oracle.segment_scan(DENSE, cat["k"][:, a0:a0 + L], cat["v"][:, a0:a0 + L], cat["alpha"][:, a0:a0 + L],
+                              [0, L], beta=cat["beta"][:, a0:a0 + L], q=cat["q"][:, a0:a0 + L], want_o=True)
+    go = to_host(o_first[l, :, h])
+    assert rel_fro(go, iso["o"][0, :, 0], axes=(-2, -1)) <= TOL_O_BF16
