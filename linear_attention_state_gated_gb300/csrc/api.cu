@@ -3,7 +3,39 @@
 // global state, no synchronisation.
 #include <stdint.h>
 
+#include <mutex>
+
 #include "internal.cuh"
+
+namespace hypic {
+
+EncodeTiledFn tensor_map_encoder() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+bool make_tensor_map_3d(CUtensorMap *m, CUtensorMapDataType dt, int esize, const void *base, uint64_t inner,
+                        uint64_t mid, uint64_t rows, uint32_t box0, uint32_t box2, CUtensorMapSwizzle sw) {
+    EncodeTiledFn enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {inner, mid, rows};
+    const cuuint64_t strides[2] = {inner * esize, inner * mid * esize};
+    const cuuint32_t box[3] = {box0, 1, box2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace hypic
 
 namespace {
 

@@ -229,6 +229,17 @@ __global__ void __launch_bounds__(256) chain_sd_kernel(const ChainArgs a) {
 #pragma unroll
             for (int i = 0; i < MAXV; ++i)
                 if (tid + i * 256 < per4) s[i] = axpy4(sc, s[i], x[i]);
+        } else if (DV == 128) {
+            // float4 slot i of warp w covers row w + 8 i: 16 lanes compute the 16
+            // row scales of the warp, shuffles hand them out (no block barrier)
+            const int w = tid >> 5, lane = tid & 31;
+            const int row = w + 8 * lane;
+            const float ex = (lane < 16 && row < DK) ? expf(a.pool_lam[e * DK + row]) : 0.f;
+#pragma unroll
+            for (int i = 0; i < MAXV; ++i) {
+                const float sc = __shfl_sync(0xffffffffu, ex, i);
+                if (tid + i * 256 < per4) s[i] = axpy4(sc, s[i], x[i]);
+            }
         } else {
             float *rs = row_scale[c & 1];
             if (tid < DK) rs[tid] = expf(a.pool_lam[e * DK + tid]);
@@ -346,6 +357,7 @@ cudaError_t launch_compose(const ComposeArgs &a, cudaStream_t s) {
 cudaError_t launch_compose_chain(const ChainArgs &a, cudaStream_t s) {
     const int64_t units = (int64_t)a.R * a.n_layers * a.H;
     if (units == 0) return cudaSuccess;
+    if (chain_dense_tc_supported(a)) return launch_chain_dense_tc(a, s);
     if (a.fam == HYPIC_DENSE) return dispatch_dd<DenseChainF>(a, s, a.dk, a.dv);
     if (a.fam == HYPIC_DIAG)
         chain_sd_kernel<true><<<(unsigned)units, 256, 0, s>>>(a);

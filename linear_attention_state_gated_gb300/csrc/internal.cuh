@@ -2,6 +2,7 @@
 // Launchers return a cudaError_t; api.cu turns that into a hypic_status.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -39,6 +40,17 @@ struct ChainArgs {
     int *d_err;
 };
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (nullptr if unavailable).
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+EncodeTiledFn tensor_map_encoder();
+
+// 3-D tiled map over a [rows][mid][inner] array (element size esize) with box {box0, 1, box2}.
+bool make_tensor_map_3d(CUtensorMap *m, CUtensorMapDataType dt, int esize, const void *base, uint64_t inner,
+                        uint64_t mid, uint64_t rows, uint32_t box0, uint32_t box2, CUtensorMapSwizzle sw);
+
 // Token-by-token fp32 recurrence on CUDA cores, every family, optional o_t.
 cudaError_t launch_scan_recurrent(const ScanArgs &a, cudaStream_t s);
 
@@ -49,6 +61,10 @@ cudaError_t launch_scan_sd_tc(const ScanArgs &a, cudaStream_t s);
 // Gated delta rule scan on tcgen05 tensor cores (bf16 inputs, d_k = d_v = 128, no o_t).
 bool scan_dense_tc_supported(const ScanArgs &a);
 cudaError_t launch_scan_dense_tc(const ScanArgs &a, cudaStream_t s);
+
+// Dense chained composition on tcgen05 (3 x TF32), d_k = d_v = 128.
+bool chain_dense_tc_supported(const ChainArgs &a);
+cudaError_t launch_chain_dense_tc(const ChainArgs &a, cudaStream_t s);
 
 cudaError_t launch_compose(const ComposeArgs &a, cudaStream_t s);
 cudaError_t launch_compose_chain(const ChainArgs &a, cudaStream_t s);

@@ -27,10 +27,6 @@
 // runs one chunk ahead; 10-17 "state" (TMEM round trip of X, R, Delta~,
 // epilogue).  Every wait is time-bounded; a timeout is reported as
 // HYPIC_ETIMEOUT.
-#include <cudaTypedefs.h>
-
-#include <mutex>
-
 #include "internal.cuh"
 #include "sm100.cuh"
 
@@ -596,44 +592,13 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: <= 96 registers pe
 
 // ---------------------------------------------------------------- host side
 
-using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                 const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
-                                 CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
-                                 CUtensorMapFloatOOBfill);
-
-EncodeTiled encode_fn() {
-    static EncodeTiled fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiled>(p);
-    });
-    return fn;
-}
-
-bool make_map_bf16(CUtensorMap *m, const void *base, uint64_t H, uint64_t rows) {
-    EncodeTiled enc = encode_fn();
-    if (!enc) return false;
-    const cuuint64_t dims[3] = {128, H, rows};
-    const cuuint64_t strides[2] = {256, 256 * H};
-    const cuuint32_t box[3] = {64, 1, kC};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 bool scan_dense_tc_supported(const ScanArgs &a) {
     return a.fam == HYPIC_DENSE && a.in_dtype == HYPIC_BF16 && a.dk == 128 && a.dv == 128 &&
            a.o_out == nullptr && a.N > 0 && (int64_t)a.n_layers * a.N < ((int64_t)1 << 31) &&
            (int64_t)a.n_layers * a.n_seg * a.H < ((int64_t)1 << 30) &&
-           encode_fn() != nullptr;
+           tensor_map_encoder() != nullptr;
 }
 
 cudaError_t launch_scan_dense_tc(const ScanArgs &a, cudaStream_t s) {
@@ -641,7 +606,11 @@ cudaError_t launch_scan_dense_tc(const ScanArgs &a, cudaStream_t s) {
     if (units == 0) return cudaSuccess;
     const uint64_t rows = (uint64_t)a.n_layers * (uint64_t)a.N;
     CUtensorMap mk, mv;
-    if (!make_map_bf16(&mk, a.k, a.H, rows) || !make_map_bf16(&mv, a.v, a.H, rows)) return cudaErrorInvalidValue;
+    if (!make_tensor_map_3d(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.k, 128, a.H, rows, 64, kC,
+                            CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map_3d(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.v, 128, a.H, rows, 64, kC,
+                            CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(scan_dense_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     scan_dense_tc_kernel<<<(unsigned)(2 * units), kThreads, kSmem, s>>>(mk, mv, a);

@@ -26,10 +26,6 @@
 // (underflow to 0 is the right limit for a weight); lambda from the logs of
 // products over groups of rows.  Every wait is time-bounded; a timeout is
 // reported as HYPIC_ETIMEOUT.
-#include <cudaTypedefs.h>
-
-#include <mutex>
-
 #include "internal.cuh"
 #include "sm100.cuh"
 
@@ -396,50 +392,18 @@ __global__ void __launch_bounds__(SdCfg<FAM, C, NS, TW>::THREADS, 2)
 
 // ---------------------------------------------------------------- host side
 
-using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                 const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
-                                 CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
-                                 CUtensorMapFloatOOBfill);
-
-EncodeTiled encode_fn() {
-    static EncodeTiled fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiled>(p);
-    });
-    return fn;
-}
-
-// 3-D map over [rows][H][inner] with box {box0, 1, box2}.
-bool make_map(CUtensorMap *m, CUtensorMapDataType dt, int esize, const void *base, uint64_t inner, uint64_t H,
-              uint64_t rows, uint32_t box0, uint32_t box2, CUtensorMapSwizzle sw) {
-    EncodeTiled enc = encode_fn();
-    if (!enc) return false;
-    const cuuint64_t dims[3] = {inner, H, rows};
-    const cuuint64_t strides[2] = {inner * esize, inner * H * esize};
-    const cuuint32_t box[3] = {box0, 1, box2};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    return enc(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int FAM, int C, int NS, int TW>
 cudaError_t launch_tc(const ScanArgs &a, cudaStream_t s) {
     using Cfg = SdCfg<FAM, C, NS, TW>;
     const uint64_t rows = (uint64_t)a.n_layers * (uint64_t)a.N;
     CUtensorMap mk, mv, ma;
-    if (!make_map(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.k, 128, a.H, rows, 64, C,
+    if (!make_tensor_map_3d(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.k, 128, a.H, rows, 64, C,
                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.v, 128, a.H, rows, 64, C,
+        !make_tensor_map_3d(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.v, 128, a.H, rows, 64, C,
                   CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     if (FAM == HYPIC_DIAG) {
-        if (!make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.alpha, 128, a.H, rows, 128, C,
+        if (!make_tensor_map_3d(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.alpha, 128, a.H, rows, 128, C,
                       CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;
     } else {
@@ -459,7 +423,7 @@ cudaError_t launch_tc(const ScanArgs &a, cudaStream_t s) {
 bool scan_sd_tc_supported(const ScanArgs &a) {
     return (a.fam == HYPIC_SCALAR || a.fam == HYPIC_DIAG) && a.in_dtype == HYPIC_BF16 && a.dk == 128 &&
            a.dv == 128 && a.o_out == nullptr && a.N > 0 && (int64_t)a.n_layers * a.N < ((int64_t)1 << 31) &&
-           encode_fn() != nullptr;
+           tensor_map_encoder() != nullptr;
 }
 
 #ifndef HYPIC_SD_SCALAR_C

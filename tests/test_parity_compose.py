@@ -127,3 +127,35 @@ def test_rag_chain_full_size_sampled(fam):
         ref = oracle.compose_chain(fam, clen[r:r + 1], idx[r:r + 1], sub_lam, sub_S)
         g = to_host(got[r, l, h])
         assert rel_fro(g, ref[0, 0, 0]) <= TOL_F32
+
+
+@pytest.mark.parametrize("fam,dk,dv", [(DIAG, 64, 128), (SCALAR, 128, 64), (DENSE, 128, 128), (DENSE, 64, 64)])
+def test_chain_shapes_and_long_chains(fam, dk, dv):
+    """Random pool pairs, chains of 0..40 steps with repeats, other head sizes."""
+    import linear_attention_state_gated_gb300 as hy
+    P, Lyr, H = 9, 2, 3
+    lam, S, M = random_pairs(fam, P * Lyr, H, dk, dv, seed=dk + dv + 7 * fam)
+    lam = lam.reshape((P, Lyr) + lam.shape[1:])
+    S = S.reshape(P, Lyr, H, dk, dv)
+    M = None if M is None else M.reshape(P, Lyr, H, dk, dk)
+    lam = np.minimum(lam, -0.05).astype(np.float32)        # decaying operators keep the state bounded
+    g = np.random.default_rng(31)
+    clen = np.array([40, 0, 1, 17], np.int32)
+    idx = g.integers(0, P, size=(4, 40)).astype(np.int32)
+    ref = oracle.compose_chain(fam, clen, idx, lam, S, pool_M=M)
+    got = to_host(hy.compose_chain(fam, to_dev(clen), to_dev(idx), to_dev(lam), to_dev(S), pool_M=to_dev(M)))
+    assert rel_fro(got, ref).max() <= TOL_F32
+    assert np.all(got[1] == 0)
+
+
+def test_dense_chain_bad_index_is_flagged_not_faulted():
+    import torch
+    import linear_attention_state_gated_gb300 as hy
+    P, Lyr, H, d = 3, 1, 2, 128
+    lam, S, M = random_pairs(DENSE, P * Lyr, H, d, d, seed=5)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    hy.compose_chain(DENSE, to_dev(np.array([3], np.int32)), to_dev(np.array([[0, 7, -1]], np.int32)),
+                     to_dev(lam.reshape(P, Lyr, H)), to_dev(S.reshape(P, Lyr, H, d, d)),
+                     pool_M=to_dev(M.reshape(P, Lyr, H, d, d)), d_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == -5
