@@ -2,10 +2,11 @@
 //
 // For one (request, layer, head) the combine step folds pool entries in order,
 //     S <- exp(lambda_p) M_p S + S_p,
-// one 128 x 128 x 128 product per step.  The product runs as 3 x TF32 on the
-// tensor cores (kind::tf32; M_p and S split into tf32 hi + lo, the lo x lo term
-// dropped: ~2^-21 relative per product), which keeps the fp32 composition
-// accurate to well below 1e-5.  The exact fp32 running state stays in the math
+// one 128 x 128 x 128 product per step.  The product runs on the tensor cores
+// in bf16 with both operands split three ways (x = hi + mid + lo, residual
+// ~2^-27) and the six partial products down to order 2^-18 kept
+// (~2^-26 relative per product), which keeps the fp32 composition accurate to
+// well below 1e-5 at the cost of three TF32 products.  The exact fp32 running state stays in the math
 // warps' registers (row i of S on TMEM lane i, two warps per lane quarter).
 // Warp 0 brings each M_p into shared memory by TMA (128-byte swizzle, so the
 // row-per-lane reads are conflict-free) while the previous step's MMAs run;
@@ -22,9 +23,9 @@ using namespace sm100;
 constexpr int kD = 128;
 constexpr int kThreads = 320;           // warp 0: TMA, warp 1: MMA, warps 2..9: math
 constexpr int kMath = 256;
-constexpr uint32_t kTaHi = 0, kTaLo = 128, kTd = 256;   // TMEM columns (512 allocated)
-constexpr int kBpart = 65536;           // one tf32 B tile: 128 k-rows x 128 n, 4 atoms of 32 n
-constexpr int kMstage = 2 * kBpart;     // M_p, fp32, 4 boxes of 32 columns x 128 rows
+constexpr uint32_t kTa = 0, kTd = 256;  // TMEM: A hi / mid / lo at 0, 64, 128 (bf16 pairs); D at 256
+constexpr int kBpart = 32768;           // one bf16 B tile: 128 k-rows x 128 n, 2 atoms of 64 n
+constexpr int kMstage = 3 * kBpart;     // M_p, fp32, 4 boxes of 32 columns x 128 rows
 constexpr int kCtl = kMstage + 65536;
 constexpr int kSmem = kCtl + 1024 + 1024;
 
@@ -34,25 +35,15 @@ struct ChainCtrl {
     int abort;
 };
 
-// Instruction descriptor, kind::tf32: tf32 A (TMEM) and B (MN-major), fp32 D, M = N = 128.
-constexpr uint32_t kIdescTf32 = (1u << 4) | (2u << 7) | (2u << 10) | (1u << 16) | ((128u >> 3) << 17) |
-                                ((128u >> 4) << 24);
-
-__device__ __forceinline__ void mma_tf32_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(bdesc), "r"(kIdescTf32), "r"(accumulate)
-        : "memory");
-}
-
-// fp32 -> tf32 hi (round to nearest even on the 10-bit significand) + lo = x - hi
-__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
-    uint32_t u = __float_as_uint(x);
-    u = (u + 0xFFFu + ((u >> 13) & 1u)) & 0xFFFFE000u;
-    hi = u;
-    lo = __float_as_uint(x - __uint_as_float(u));
+// Two fp32 values -> three packed bf16 pairs with x = hi + mid + lo (to ~2^-27 relative).
+__device__ __forceinline__ void split3_pair(float x0, float x1, uint32_t &hi, uint32_t &mid, uint32_t &lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    const float r0 = x0 - __low2float(h), r1 = x1 - __high2float(h);
+    const __nv_bfloat162 m = __floats2bfloat162_rn(r0, r1);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(r0 - __low2float(m), r1 - __high2float(m));
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    mid = *reinterpret_cast<const uint32_t *>(&m);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -114,21 +105,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            const uint32_t bhi = smem_addr(smem), blo = smem_addr(smem + kBpart);
+            constexpr uint32_t idesc = idesc_bf16_f32(128, 128, false, true);   // A TMEM, B MN-major
+            const uint32_t b0 = smem_addr(smem);
             for (int c = 0; c < n; ++c) {
                 if (!mbar_wait(&ctl->ops_ready, (uint32_t)c & 1u) || *abortp) {
                     *abortp = 1;
                     break;
                 }
                 tc_fence_after();
-#pragma unroll 4
-                for (int ks = 0; ks < 16; ++ks) {   // K = 128 in steps of 8 (one 8-row group of B)
-                    const uint32_t off = (uint32_t)ks * 1024u;
-                    const uint64_t dh = smem_desc_sw128(bhi + off, 16384, 1024);
-                    const uint64_t dl = smem_desc_sw128(blo + off, 16384, 1024);
-                    mma_tf32_ta(tmem + kTd, tmem + kTaHi + (uint32_t)ks * 8u, dh, ks > 0);
-                    mma_tf32_ta(tmem + kTd, tmem + kTaHi + (uint32_t)ks * 8u, dl, 1u);
-                    mma_tf32_ta(tmem + kTd, tmem + kTaLo + (uint32_t)ks * 8u, dh, 1u);
+#pragma unroll 2
+                for (int ks = 0; ks < 8; ++ks) {   // K = 128 in steps of 16 (two 8-row groups of B)
+                    const uint32_t off = (uint32_t)ks * 2048u;
+                    const uint64_t bh = smem_desc_sw128(b0 + off, 16384, 1024);
+                    const uint64_t bm = smem_desc_sw128(b0 + kBpart + off, 16384, 1024);
+                    const uint64_t bl = smem_desc_sw128(b0 + 2 * kBpart + off, 16384, 1024);
+                    const uint32_t ah = tmem + kTa + (uint32_t)ks * 8u, am = ah + 64u, al = ah + 128u;
+                    mma_f16_ta(tmem + kTd, ah, bh, idesc, ks > 0);
+                    mma_f16_ta(tmem + kTd, ah, bm, idesc, 1u);
+                    mma_f16_ta(tmem + kTd, am, bh, idesc, 1u);
+                    mma_f16_ta(tmem + kTd, ah, bl, idesc, 1u);
+                    mma_f16_ta(tmem + kTd, am, bm, idesc, 1u);
+                    mma_f16_ta(tmem + kTd, al, bh, idesc, 1u);
                 }
                 mma_commit(&ctl->d_done);
             }
@@ -154,44 +151,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int c = 0; c < n; ++c) {
             const int64_t e = entry(c);
-            // A = M_p (tf32 hi / lo) -> TMEM, row i on lane i, column k
+            // A = M_p (bf16 hi / mid / lo pairs) -> TMEM, row i on lane i, column k / 2
             if (!bar_and(1, kMath, mbar_wait(&ctl->mfull, (uint32_t)c & 1u) && !*abortp)) {
                 *abortp = 1;
                 break;
             }
 #pragma unroll
-            for (int cb = 0; cb < 4; ++cb) {             // 16 columns at a time
-                uint32_t hi[16], lo[16];
+            for (int cb = 0; cb < 2; ++cb) {             // 32 columns (16 packed pairs) at a time
+                uint32_t hi[16], mid[16], lo[16];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int col = ch * 64 + cb * 16 + 4 * q;
+                for (int q = 0; q < 8; ++q) {
+                    const int col = ch * 64 + cb * 32 + 4 * q;
                     const int box = col >> 5, chunk = (col & 31) >> 2;
                     const float4 m4 = *reinterpret_cast<const float4 *>(smem + kMstage + box * 16384 + i * 128 +
                                                                         ((chunk ^ (i & 7)) << 4));
-                    split_tf32(m4.x, hi[4 * q], lo[4 * q]);
-                    split_tf32(m4.y, hi[4 * q + 1], lo[4 * q + 1]);
-                    split_tf32(m4.z, hi[4 * q + 2], lo[4 * q + 2]);
-                    split_tf32(m4.w, hi[4 * q + 3], lo[4 * q + 3]);
+                    split3_pair(m4.x, m4.y, hi[2 * q], mid[2 * q], lo[2 * q]);
+                    split3_pair(m4.z, m4.w, hi[2 * q + 1], mid[2 * q + 1], lo[2 * q + 1]);
                 }
-                tmem_st16(tmem + lane_off + kTaHi + (uint32_t)(ch * 64 + cb * 16), hi);
-                tmem_st16(tmem + lane_off + kTaLo + (uint32_t)(ch * 64 + cb * 16), lo);
+                const uint32_t col2 = (uint32_t)(ch * 32 + cb * 16);
+                tmem_st16(tmem + lane_off + kTa + col2, hi);
+                tmem_st16(tmem + lane_off + kTa + 64u + col2, mid);
+                tmem_st16(tmem + lane_off + kTa + 128u + col2, lo);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->mfree);     // the stage may take the next M_p
-            // B = S (tf32 hi / lo) -> shared memory, MN-major: row k = i, n contiguous,
-            // 4 atoms of 32 columns, 128-byte swizzle
+            // B = S (bf16 hi / mid / lo) -> shared memory, MN-major: row k = i, n contiguous,
+            // 2 atoms of 64 columns, 128-byte swizzle
 #pragma unroll
-            for (int q = 0; q < 16; ++q) {
-                const int ncol = ch * 64 + 4 * q;
-                const int atom = ncol >> 5, chunk = (ncol & 31) >> 2;
-                const int off = atom * 16384 + i * 128 + ((chunk ^ (i & 7)) << 4);
-                uint32_t h0, l0, h1, l1, h2, l2, h3, l3;
-                split_tf32(srow[4 * q], h0, l0);
-                split_tf32(srow[4 * q + 1], h1, l1);
-                split_tf32(srow[4 * q + 2], h2, l2);
-                split_tf32(srow[4 * q + 3], h3, l3);
-                *reinterpret_cast<uint4 *>(smem + off) = make_uint4(h0, h1, h2, h3);
-                *reinterpret_cast<uint4 *>(smem + kBpart + off) = make_uint4(l0, l1, l2, l3);
+            for (int q = 0; q < 8; ++q) {                  // 8 columns (one 16-byte chunk) at a time
+                const int chunk = q;                       // this thread's 64 columns are atom ch
+                const int off = ch * 16384 + i * 128 + ((chunk ^ (i & 7)) << 4);
+                uint32_t h[4], md[4], l[4];
+#pragma unroll
+                for (int p = 0; p < 4; ++p) split3_pair(srow[8 * q + 2 * p], srow[8 * q + 2 * p + 1], h[p], md[p], l[p]);
+                *reinterpret_cast<uint4 *>(smem + off) = make_uint4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<uint4 *>(smem + kBpart + off) = make_uint4(md[0], md[1], md[2], md[3]);
+                *reinterpret_cast<uint4 *>(smem + 2 * kBpart + off) = make_uint4(l[0], l[1], l[2], l[3]);
             }
             tmem_wait_st();
             fence_async_smem();
