@@ -41,7 +41,7 @@ constexpr int kNS = 2;          // TMA stages
 constexpr int kThreads = 576;   // 18 warps
 constexpr int kPrep = 256;      // warps 2..9
 constexpr int kState = 256;     // warps 10..17
-constexpr int kLd = 65;         // padded row stride of the fp32 L / A work tiles
+constexpr int kLd = 68;         // padded row stride of the fp32 L / A work tiles (16-byte rows)
 
 // shared memory map (offsets from the 1024-aligned base)
 constexpr int kBox = kC * 128;              // 64 channels x 64 tokens, bf16: 8 KB
@@ -113,28 +113,46 @@ __device__ __forceinline__ float state_max(float mx, DenseCtrl *ctl, int sw, int
 }
 
 // Off-diagonal blocks of A = (I + L)^-1 at block distance DIST:
-//   T = sum_{k=j}^{i-1} L_ik A_kj,  A_ij = -A_ii T   (16 x 16 blocks).
+//   T = sum_{k=j}^{i-1} L_ik A_kj,  A_ij = -A_ii T   (16 x 16 blocks),
+// four adjacent columns of one row per thread (16-byte loads of A and T).
 template <int DIST>
 __device__ __forceinline__ void inverse_level(const float *Lw, float *Aw, float *Tw, int pt) {
     constexpr int NB = 4 - DIST;
-    for (int e = pt; e < NB * 256; e += kPrep) {
-        const int bi = (e >> 8) + DIST, bj = bi - DIST, r = (e >> 4) & 15, c = e & 15;
+    if (pt < NB * 64) {
+        const int blk = pt >> 6, r = (pt >> 2) & 15, c4 = (pt & 3) * 4;
+        const int bi = blk + DIST, bj = bi - DIST;
         const float *lrow = Lw + (bi * 16 + r) * kLd + bj * 16;
-        const float *acol = Aw + (bj * 16) * kLd + bj * 16 + c;
-        float acc = 0.f;
+        const float *acol = Aw + (bj * 16) * kLd + bj * 16 + c4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int k = 0; k < 16 * DIST; ++k) acc = fmaf(lrow[k], acol[k * kLd], acc);
-        Tw[(e >> 8) * 256 + r * 16 + c] = acc;
+        for (int k = 0; k < 16 * DIST; ++k) {
+            const float lv = lrow[k];
+            const float4 av = *reinterpret_cast<const float4 *>(acol + k * kLd);
+            acc.x = fmaf(lv, av.x, acc.x);
+            acc.y = fmaf(lv, av.y, acc.y);
+            acc.z = fmaf(lv, av.z, acc.z);
+            acc.w = fmaf(lv, av.w, acc.w);
+        }
+        *reinterpret_cast<float4 *>(Tw + blk * 256 + r * 16 + c4) = acc;
     }
     bar_sync(1, kPrep);
-    for (int e = pt; e < NB * 256; e += kPrep) {
-        const int bi = (e >> 8) + DIST, bj = bi - DIST, r = (e >> 4) & 15, c = e & 15;
+    if (pt < NB * 64) {
+        const int blk = pt >> 6, r = (pt >> 2) & 15, c4 = (pt & 3) * 4;
+        const int bi = blk + DIST, bj = bi - DIST;
         const float *arow = Aw + (bi * 16 + r) * kLd + bi * 16;   // A_ii, zero above the diagonal
-        const float *tcol = Tw + (e >> 8) * 256 + c;
-        float acc = 0.f;
+        const float *tcol = Tw + blk * 256 + c4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int k = 0; k < 16; ++k) acc = fmaf(arow[k], tcol[k * 16], acc);
-        Aw[(bi * 16 + r) * kLd + bj * 16 + c] = -acc;
+        for (int k = 0; k < 16; ++k) {
+            const float av = arow[k];
+            const float4 tv = *reinterpret_cast<const float4 *>(tcol + k * 16);
+            acc.x = fmaf(av, tv.x, acc.x);
+            acc.y = fmaf(av, tv.y, acc.y);
+            acc.z = fmaf(av, tv.z, acc.z);
+            acc.w = fmaf(av, tv.w, acc.w);
+        }
+        *reinterpret_cast<float4 *>(Aw + (bi * 16 + r) * kLd + bj * 16 + c4) =
+            make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
     }
     bar_sync(1, kPrep);
 }
@@ -430,7 +448,14 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: <= 96 registers pe
         const uint32_t txop = tmem + lane_off + kTxop + (uint32_t)(ch * 32);
         const uint32_t tacc = tmem + lane_off + kTacc + (uint32_t)(ch * 32);
         const uint32_t topr = tmem + lane_off + kTopr + (uint32_t)(ch * 16);
-        int lam_exp = 0;                            // power-of-two exponent moved out of M
+        // Transition half: M_true = exp(lam_d + lam_exp ln2) M_stored, and each chunk
+        // stores T_chunk M / b_C (log b_C into lam_d).  State half: S_true =
+        // exp(ls) S_stored.  Either way the update only accumulates into TMEM; X is
+        // rewritten only to renormalise (every 8 chunks for M, when ls < -20 for S)
+        // or on a chunk whose total decay exceeds e^-40 (exact write-back form).
+        int lam_exp = 0;
+        double lam_d = 0.0;
+        float ls = 0.f;
 
         // initial X^T: identity (transition) or zero (state)
         {
@@ -455,21 +480,49 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: <= 96 registers pe
                 break;
             }
             tc_fence_after();
-            float g = 1.f;
+            const float LC = ctl->gl[par][kC - 1];      // log of the chunk's total decay
+            const bool slow = LC < -40.f;
+            const bool renorm = slow || (half == 0 ? (j % 8 == 0) : (ls < -20.f));
+            float g = 1.f;        // operand = g * X_stored
+            float wscale = 1.f;   // X_stored <- g * wscale * X_stored when rewritten
+            float fP, fD;         // multipliers of beta*b (in R) and b_C / b (in Delta~)
             if (half == 0) {
-                float mx = 0.f;
-                for (int cb = 0; cb < 2; ++cb) {
-                    uint32_t r[32];
-                    tmem_ld32(tx + (uint32_t)(cb * 32), r);
-                    tmem_wait_ld();
+                if (renorm) {
+                    float mx = 0.f;
+                    for (int cb = 0; cb < 2; ++cb) {
+                        uint32_t r[32];
+                        tmem_ld32(tx + (uint32_t)(cb * 32), r);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fabsf(__uint_as_float(r[i])));
+                        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fabsf(__uint_as_float(r[i])));
+                    }
+                    const int e = exponent_of(state_max(mx, ctl, sw, lane));
+                    g = ldexpf(1.f, -e);
+                    lam_exp += e;
                 }
-                const int e = exponent_of(state_max(mx, ctl, sw, lane));
-                g = ldexpf(1.f, -e);
-                lam_exp += e;
+                wscale = slow ? ctl->bC[par] : 1.f;
+                fP = 1.f;
+                fD = slow ? 1.f : expf(-LC);
+                if (!slow) lam_d += (double)LC;
+            } else {
+                if (slow) {
+                    g = expf(ls);
+                    wscale = ctl->bC[par];
+                    fP = 1.f;
+                    fD = 1.f;
+                    ls = 0.f;
+                } else {
+                    if (renorm) {
+                        const int q = (int)rintf(ls * 1.44269504088896341f);
+                        g = ldexpf(1.f, q);
+                        ls -= (float)q * 0.69314718055994531f;
+                    }
+                    fP = expf(ls);
+                    fD = expf(-(ls + LC));
+                    ls += LC;
+                }
             }
-            const float sc = g * ctl->bC[par];
+            const float sc = g * wscale;
             for (int cb = 0; cb < 2; ++cb) {
                 uint32_t r[32], hi[16], lo[16];
                 tmem_ld32(tx + (uint32_t)(cb * 32), r);
@@ -479,9 +532,11 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: <= 96 registers pe
                     split_pair(g * __uint_as_float(r[2 * p]), g * __uint_as_float(r[2 * p + 1]), hi[p], lo[p]);
                 tmem_st16(txop + (uint32_t)(cb * 16), hi);
                 tmem_st16(txop + 64u + (uint32_t)(cb * 16), lo);
+                if (renorm) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(sc * __uint_as_float(r[i]));
-                tmem_st32(tx + (uint32_t)(cb * 32), r);
+                    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(sc * __uint_as_float(r[i]));
+                    tmem_st32(tx + (uint32_t)(cb * 32), r);
+                }
             }
             tmem_wait_st();
             tc_fence_before();
@@ -506,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: <= 96 registers pe
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int t = ch * 32 + 2 * p + e;
-                        float val = -ctl->gbb[par][t] * __uint_as_float(r[2 * p + e]);
+                        float val = -fP * ctl->gbb[par][t] * __uint_as_float(r[2 * p + e]);
                         if (half) {
                             const uint16_t vb = *reinterpret_cast<const uint16_t *>(
                                 vt + vbox * kBox + t * 128 + ((vc ^ (t & 7)) << 4) + vw);
@@ -536,8 +591,8 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: <= 96 registers pe
 #pragma unroll
                 for (int p = 0; p < 16; ++p) {
                     const int t = ch * 32 + 2 * p;
-                    split_pair(ctl->gw[par][t] * __uint_as_float(r[2 * p]),
-                               ctl->gw[par][t + 1] * __uint_as_float(r[2 * p + 1]), hi[p], lo[p]);
+                    split_pair(fD * ctl->gw[par][t] * __uint_as_float(r[2 * p]),
+                               fD * ctl->gw[par][t + 1] * __uint_as_float(r[2 * p + 1]), hi[p], lo[p]);
                 }
                 tmem_st16(topr, hi);
                 tmem_st16(topr + 32u, lo);
@@ -567,7 +622,9 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: <= 96 registers pe
                 const int e = exponent_of(state_max(mx, ctl, sw, lane));
                 scale = ldexpf(1.f, -e);
                 lam_exp += e;
-                if (st == 0) a.lam_out[u_out] = (float)((double)lam_exp * 0.69314718055994530942);
+                if (st == 0) a.lam_out[u_out] = (float)(lam_d + (double)lam_exp * 0.69314718055994530942);
+            } else {
+                scale = expf(ls);
             }
             float *out = (half == 0 ? a.M_out : a.S_out) + u_out * kD * kD;
             for (int cb = 0; cb < 2; ++cb) {

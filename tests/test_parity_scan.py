@@ -159,6 +159,11 @@ def test_dense_long_segment_and_special_gates():
     w1["alpha"] = np.ones_like(w1["alpha"])
     w1["beta"] = np.ones_like(w1["beta"])
     check(DENSE, host(gpu_scan(w1)), oracle_scan(w1), TOL_SCAN_BF16)
+    # strong decay: chunks whose total decay is below e^-40 alternate with mild ones
+    w2 = wl.dense_stack(lengths=[1000, 333], n_layers=1, H=2, d=128, seed=15)
+    t = np.arange(w2["alpha"].shape[1])
+    w2["alpha"][:, (t // 64) % 3 == 1] = 0.3
+    check(DENSE, host(gpu_scan(w2)), oracle_scan(w2), TOL_SCAN_BF16)
 
 
 @pytest.mark.parametrize("fam", [SCALAR, DIAG, DENSE], ids=["scalar", "diag", "dense"])
