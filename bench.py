@@ -126,13 +126,20 @@ def barrier(world):
 
 
 def max_over_ranks(x, world):
+    """Max of a per-rank timing over all ranks (the job's wall time)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(units_per_rank, world, t_max):
+    """Whole-job throughput of independent replicas: units of all ranks / slowest rank's time."""
+    return units_per_rank * world / t_max
 
 
 # ------------------------------------------------------------------ workloads
@@ -220,7 +227,7 @@ def run_headline(args, rank, world):
         per_kernel[fam] = [a.elapsed_time(b) / 1e3 for a, b in ev[fam]]
     t_max = max_over_ranks(elapsed, world)
     tokens_per_step = 2 * B * L
-    value = tokens_per_step * args.steps * world / t_max
+    value = job_throughput(tokens_per_step * args.steps, world, t_max)
 
     # end to end: pinned host inputs -> device -> scan -> host results, every step
     e2e_steps = max(3, min(args.steps, 10))
@@ -248,7 +255,7 @@ def run_headline(args, rank, world):
     e2.record()
     torch.cuda.synchronize()
     e2e_t = max_over_ranks(s2.elapsed_time(e2) / 1e3, world)
-    e2e_value = tokens_per_step * e2e_steps * world / e2e_t
+    e2e_value = job_throughput(tokens_per_step * e2e_steps, world, e2e_t)
 
     hbm, bf16, bf16_sus, src = peaks()
     n_tok_heads = B * L * H
