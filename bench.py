@@ -142,6 +142,24 @@ def job_throughput(units_per_rank, world, t_max):
     return units_per_rank * world / t_max
 
 
+def profiled_traffic(summary, source):
+    """DRAM bytes per launch recorded in a committed ncu summary, or None when the
+    kernel source changed since the counters were taken."""
+    import hashlib
+    try:
+        vals = {}
+        for line in open(os.path.join(ROOT, "profiles", summary)):
+            if ":" in line and not line.startswith(("|", "#", " ")):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+        sha = hashlib.sha256(open(os.path.join(ROOT, source), "rb").read()).hexdigest()[:16]
+        if vals.get("source_sha256_prefix") != sha:
+            return None
+        return float(vals["traffic_bytes_per_launch_L8192"])
+    except Exception:
+        return None
+
+
 # ------------------------------------------------------------------ workloads
 
 HEAD = dict(B=8, H=32, d=128)
@@ -552,7 +570,10 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": headline_config(args.L),
         "roofline": {"bound": "hbm", "achieved": kd["gbs"], "peak": h["hbm"], "unit": "GB/s",
-                     "frac": kd["gbs"] / h["hbm"], "traffic": None,
+                     "frac": kd["gbs"] / h["hbm"],
+                     "traffic": (profiled_traffic("scan_sd_tc_diag_B8x2048_H32.md",
+                                                  "linear_attention_state_gated_gb300/csrc/scan_sd_tc.cu")
+                                 if h["dom"] == 1 and args.L == 8192 else None),
                      "kernel": f"segment scan, {fam_name[h['dom']]} gate",
                      "algorithmic_bytes": kd["bytes"], "avg_launch_ms": kd["avg_s"] * 1e3,
                      "peak_kind": f"HBM copy, {h['src']}"},
