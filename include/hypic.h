@@ -101,6 +101,41 @@ int hypic_segment_scan(int fam, int in_dtype, int n_layers, int n_seg,
                        int *d_err, void *cuda_stream);
 
 /*
+ * hypic_segment_scan_workspace_bytes -- bytes of device scratch that
+ * hypic_segment_scan_ws needs for these sizes, or 0 when that call uses none
+ * (then its workspace may be NULL).  A negative hypic_status on bad counts.
+ * Today the scratch is used by the dense family with bf16 inputs, d_k = d_v =
+ * 128 and no o_t: one 17184-byte record per (layer, head, 64-token chunk slot),
+ * n_layers * n_heads * (n_seg + total_tokens / 64) records.
+ */
+int64_t hypic_segment_scan_workspace_bytes(int fam, int in_dtype, int n_layers, int n_seg,
+                                           int64_t total_tokens, int n_heads, int d_k, int d_v,
+                                           int with_o);
+
+/*
+ * hypic_segment_scan_ws -- hypic_segment_scan with caller-owned device
+ * scratch; same arguments, layouts, results and error behaviour, plus
+ *   workspace        device memory, 256-byte aligned, at least
+ *                    hypic_segment_scan_workspace_bytes(...) bytes (NULL allowed
+ *                    when that is 0).  Its contents on entry do not matter; the
+ *                    call overwrites them, and two calls in flight at once
+ *                    must not share it.
+ *   workspace_bytes  its size; too small returns HYPIC_EINVAL.
+ * With the scratch the dense scan runs in two passes: every 64-token chunk's
+ * intra-chunk solve (Gram matrix, L, (I + L)^-1, decays) in parallel over all
+ * chunks, then the ordered state pass (the chunked WY/UT form of the gated
+ * delta rule; the pages give no chunked algorithm).  Other cases run exactly
+ * as hypic_segment_scan.
+ */
+int hypic_segment_scan_ws(int fam, int in_dtype, int n_layers, int n_seg,
+                          int64_t total_tokens, int n_heads, int d_k, int d_v,
+                          const int64_t *seg_offsets, const void *q, const void *k,
+                          const void *v, const float *alpha, const float *beta,
+                          float *lam_out, float *M_out, float *S_out, void *o_out,
+                          void *workspace, int64_t workspace_bytes, int *d_err,
+                          void *cuda_stream);
+
+/*
  * hypic_compose -- S = T_C S_prev + S_C for n items x H heads, with
  * T_C = exp(lambda) M.  (xix.ai/fr, linear-layer paragraph:
  * S(C1.C2) = T(C2) S(C1) + S(C2); left-multiplication by the cached T then an

@@ -32,7 +32,7 @@ BF16, F32 = 0, 1
 STATUS = {0: "HYPIC_OK", -1: "HYPIC_EINVAL", -2: "HYPIC_EUNSUPPORTED", -3: "HYPIC_EALIGN",
           -4: "HYPIC_ECUDA", -5: "HYPIC_EINDEX", -6: "HYPIC_ETIMEOUT"}
 
-__all__ = ["segment_scan", "compose", "compose_chain", "status_string", "library", "use_library",
+__all__ = ["segment_scan", "segment_scan_workspace_bytes", "compose", "compose_chain", "status_string", "library", "use_library",
            "HypicError", "SCALAR", "DIAG", "DENSE"]
 
 
@@ -50,6 +50,9 @@ _P, _I32, _I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
 SIGNATURES = {
     "hypic_segment_scan": (_I32, [_I32, _I32, _I32, _I32, _I64, _I32, _I32, _I32,
                                   _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "hypic_segment_scan_ws": (_I32, [_I32, _I32, _I32, _I32, _I64, _I32, _I32, _I32,
+                                     _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _P, _P]),
+    "hypic_segment_scan_workspace_bytes": (_I64, [_I32, _I32, _I32, _I32, _I64, _I32, _I32, _I32, _I32]),
     "hypic_compose": (_I32, [_I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "hypic_compose_chain": (_I32, [_I32, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _I32,
                                    _P, _P, _P, _P, _P, _P, _P]),
@@ -124,14 +127,31 @@ def _check(fn, status):
         raise HypicError(fn, status)
 
 
+def segment_scan_workspace_bytes(family, dtype, n_layers, n_seg, total_tokens, n_heads, d_k, d_v,
+                                 with_o=False):
+    """Bytes of device scratch the workspace form of the scan uses for these sizes
+    (0: that form needs none for this family / size)."""
+    n = library().hypic_segment_scan_workspace_bytes(
+        _fam(family), BF16 if dtype == torch.bfloat16 else F32, n_layers, n_seg, total_tokens, n_heads,
+        d_k, d_v, int(bool(with_o)))
+    if n < 0:
+        raise HypicError("hypic_segment_scan_workspace_bytes", n)
+    return n
+
+
 def segment_scan(family, k, v, alpha, seg_offsets, beta=None, q=None, want_o=False,
-                 out=None, d_err=None, stream=None):
+                 out=None, d_err=None, stream=None, workspace="auto"):
     """(T_C, S(C|0)) for every (layer, segment, head); optionally o_t.
 
     k [Lyr,N,H,dk], v [Lyr,N,H,dv] (bf16 or fp32), alpha fp32 [Lyr,N,H] or
     [Lyr,N,H,dk] (diag), beta fp32 [Lyr,N,H] or None, q like k (for o_t),
     seg_offsets int64 [n_seg+1] on the device.  ``out`` may hold preallocated
     ``lam``, ``M``, ``S``, ``o`` tensors.  Returns a dict with lam, S, M (dense), o.
+
+    ``workspace``: "auto" (default) allocates the device scratch the two-pass
+    form needs (through torch, on the launch stream) and calls
+    hypic_segment_scan_ws; a uint8 CUDA tensor is used as that scratch; None
+    calls hypic_segment_scan (the single-pass kernels, no scratch).
     """
     fam = _fam(family)
     k = _dev(k, "k")
@@ -158,12 +178,29 @@ def segment_scan(family, k, v, alpha, seg_offsets, beta=None, q=None, want_o=Fal
         out["M"] = torch.empty((Lyr, n_seg, H, dk, dk), dtype=torch.float32, device=dev)
     if want_o and "o" not in out:
         out["o"] = torch.empty((Lyr, N, H, dv), dtype=dt, device=dev)
-    st = library().hypic_segment_scan(
-        fam, BF16 if dt == torch.bfloat16 else F32, Lyr, n_seg, N, H, dk, dv,
-        _ptr(seg_offsets), _ptr(q if want_o else None), _ptr(k), _ptr(v), _ptr(alpha),
-        _ptr(beta), _ptr(out["lam"]), _ptr(out.get("M") if fam == DENSE else None),
-        _ptr(out["S"]), _ptr(out.get("o") if want_o else None), _ptr(d_err), _stream(stream))
-    _check("hypic_segment_scan", st)
+    args = (fam, BF16 if dt == torch.bfloat16 else F32, Lyr, n_seg, N, H, dk, dv,
+            _ptr(seg_offsets), _ptr(q if want_o else None), _ptr(k), _ptr(v), _ptr(alpha),
+            _ptr(beta), _ptr(out["lam"]), _ptr(out.get("M") if fam == DENSE else None),
+            _ptr(out["S"]), _ptr(out.get("o") if want_o else None))
+    if workspace is None:
+        st = library().hypic_segment_scan(*args, _ptr(d_err), _stream(stream))
+        _check("hypic_segment_scan", st)
+        return out
+    if isinstance(workspace, str):
+        if workspace != "auto":
+            raise ValueError("workspace must be 'auto', None or a uint8 CUDA tensor")
+        nbytes = segment_scan_workspace_bytes(fam, dt, Lyr, n_seg, N, H, dk, dv, want_o)
+        if nbytes > 0:
+            with torch.cuda.stream(stream if stream is not None else torch.cuda.current_stream()):
+                workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        else:
+            workspace = None
+    else:
+        workspace = _dev(workspace, "workspace", torch.uint8)
+    st = library().hypic_segment_scan_ws(*args, _ptr(workspace),
+                                         0 if workspace is None else workspace.numel(),
+                                         _ptr(d_err), _stream(stream))
+    _check("hypic_segment_scan_ws", st)
     return out
 
 

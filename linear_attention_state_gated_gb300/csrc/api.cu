@@ -64,18 +64,27 @@ const char *hypic_status_string(int status) {
     return "unknown status";
 }
 
-int hypic_segment_scan(int fam, int in_dtype, int n_layers, int n_seg, int64_t total_tokens,
-                       int n_heads, int d_k, int d_v, const int64_t *seg_offsets, const void *q,
-                       const void *k, const void *v, const float *alpha, const float *beta,
-                       float *lam_out, float *M_out, float *S_out, void *o_out, int *d_err,
-                       void *cuda_stream) {
+}  // extern "C"
+
+namespace {
+
+// Host checks shared by hypic_segment_scan and hypic_segment_scan_ws; fills `a`.
+// Returns HYPIC_OK and sets *nothing_to_do when there is no work.
+int scan_args(int fam, int in_dtype, int n_layers, int n_seg, int64_t total_tokens, int n_heads, int d_k,
+              int d_v, const int64_t *seg_offsets, const void *q, const void *k, const void *v,
+              const float *alpha, const float *beta, float *lam_out, float *M_out, float *S_out, void *o_out,
+              int *d_err, hypic::ScanArgs &a, bool &nothing_to_do) {
+    nothing_to_do = false;
     if (fam < HYPIC_SCALAR || fam > HYPIC_DENSE) return HYPIC_EINVAL;
     if (in_dtype != HYPIC_BF16 && in_dtype != HYPIC_F32) return HYPIC_EINVAL;
     if (n_layers < 0 || n_seg < 0 || total_tokens < 0 || n_heads <= 0) return HYPIC_EINVAL;
     if (!head_size_ok(d_k) || !head_size_ok(d_v)) return HYPIC_EUNSUPPORTED;
     if ((int64_t)n_layers * n_seg * n_heads > INT32_MAX) return HYPIC_EUNSUPPORTED;
     if ((int64_t)n_layers * total_tokens * n_heads > (INT64_MAX / 256)) return HYPIC_EUNSUPPORTED;
-    if (n_layers == 0 || n_seg == 0) return HYPIC_OK;
+    if (n_layers == 0 || n_seg == 0) {
+        nothing_to_do = true;
+        return HYPIC_OK;
+    }
     const bool has_tokens = total_tokens > 0;
     if (!seg_offsets || !lam_out || !S_out) return HYPIC_EINVAL;
     if (has_tokens && (!k || !v || !alpha)) return HYPIC_EINVAL;
@@ -90,7 +99,6 @@ int hypic_segment_scan(int fam, int in_dtype, int n_layers, int n_seg, int64_t t
     for (const void *p : a4)
         if (p && !aligned(p, 4)) return HYPIC_EALIGN;
 
-    hypic::ScanArgs a;
     a.fam = fam;
     a.in_dtype = in_dtype;
     a.n_layers = n_layers;
@@ -110,7 +118,69 @@ int hypic_segment_scan(int fam, int in_dtype, int n_layers, int n_seg, int64_t t
     a.S_out = S_out;
     a.o_out = o_out;
     a.d_err = d_err;
+    a.ws = nullptr;
+    return HYPIC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int hypic_segment_scan(int fam, int in_dtype, int n_layers, int n_seg, int64_t total_tokens,
+                       int n_heads, int d_k, int d_v, const int64_t *seg_offsets, const void *q,
+                       const void *k, const void *v, const float *alpha, const float *beta,
+                       float *lam_out, float *M_out, float *S_out, void *o_out, int *d_err,
+                       void *cuda_stream) {
+    hypic::ScanArgs a;
+    bool none;
+    const int rc = scan_args(fam, in_dtype, n_layers, n_seg, total_tokens, n_heads, d_k, d_v, seg_offsets, q, k,
+                             v, alpha, beta, lam_out, M_out, S_out, o_out, d_err, a, none);
+    if (rc != HYPIC_OK || none) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    if (hypic::scan_sd_tc_supported(a)) return from_cuda(hypic::launch_scan_sd_tc(a, s));
+    if (hypic::scan_dense_tc_supported(a)) return from_cuda(hypic::launch_scan_dense_tc(a, s));
+    return from_cuda(hypic::launch_scan_recurrent(a, s));
+}
+
+int64_t hypic_segment_scan_workspace_bytes(int fam, int in_dtype, int n_layers, int n_seg,
+                                           int64_t total_tokens, int n_heads, int d_k, int d_v,
+                                           int with_o) {
+    if (fam < HYPIC_SCALAR || fam > HYPIC_DENSE || n_layers < 0 || n_seg < 0 || total_tokens < 0 || n_heads <= 0)
+        return HYPIC_EINVAL;
+    hypic::ScanArgs a{};
+    a.fam = fam;
+    a.in_dtype = in_dtype;
+    a.n_layers = n_layers;
+    a.n_seg = n_seg;
+    a.H = n_heads;
+    a.dk = d_k;
+    a.dv = d_v;
+    a.N = total_tokens;
+    a.o_out = with_o ? reinterpret_cast<void *>(16) : nullptr;   // only tested against NULL
+    if (n_layers == 0 || n_seg == 0 || !hypic::scan_dense_ws_shape(a)) return 0;
+    return hypic::scan_dense_ws_bytes(a);
+}
+
+int hypic_segment_scan_ws(int fam, int in_dtype, int n_layers, int n_seg, int64_t total_tokens,
+                          int n_heads, int d_k, int d_v, const int64_t *seg_offsets, const void *q,
+                          const void *k, const void *v, const float *alpha, const float *beta,
+                          float *lam_out, float *M_out, float *S_out, void *o_out, void *workspace,
+                          int64_t workspace_bytes, int *d_err, void *cuda_stream) {
+    hypic::ScanArgs a;
+    bool none;
+    const int rc = scan_args(fam, in_dtype, n_layers, n_seg, total_tokens, n_heads, d_k, d_v, seg_offsets, q, k,
+                             v, alpha, beta, lam_out, M_out, S_out, o_out, d_err, a, none);
+    if (rc != HYPIC_OK || none) return rc;
+    if (workspace_bytes < 0) return HYPIC_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    if (hypic::scan_dense_ws_shape(a)) {
+        if (!workspace || workspace_bytes < hypic::scan_dense_ws_bytes(a)) return HYPIC_EINVAL;
+        if (!aligned(workspace, 256)) return HYPIC_EALIGN;
+    }
+    if (hypic::scan_dense_ws_supported(a)) {
+        a.ws = static_cast<float *>(workspace);
+        return from_cuda(hypic::launch_scan_dense_ws(a, s));
+    }
     if (hypic::scan_sd_tc_supported(a)) return from_cuda(hypic::launch_scan_sd_tc(a, s));
     if (hypic::scan_dense_tc_supported(a)) return from_cuda(hypic::launch_scan_dense_tc(a, s));
     return from_cuda(hypic::launch_scan_recurrent(a, s));

@@ -21,6 +21,7 @@ struct ScanArgs {
     const float *alpha, *beta;
     float *lam_out, *M_out, *S_out;
     void *o_out;
+    float *ws;        // caller-owned scratch of the two-pass dense scan (or NULL)
     int *d_err;
 };
 
@@ -61,6 +62,10 @@ cudaError_t launch_scan_sd_tc(const ScanArgs &a, cudaStream_t s);
 // Gated delta rule scan on tcgen05 tensor cores (bf16 inputs, d_k = d_v = 128, no o_t).
 bool scan_dense_tc_supported(const ScanArgs &a);
 cudaError_t launch_scan_dense_tc(const ScanArgs &a, cudaStream_t s);
+bool scan_dense_ws_shape(const ScanArgs &a);       // sizes / options the two-pass form takes
+bool scan_dense_ws_supported(const ScanArgs &a);   // ... and the runtime can encode its tensor maps
+int64_t scan_dense_ws_bytes(const ScanArgs &a);
+cudaError_t launch_scan_dense_ws(const ScanArgs &a, cudaStream_t s);
 
 // Dense chained composition on tcgen05 (3 x TF32), d_k = d_v = 128.
 bool chain_dense_tc_supported(const ChainArgs &a);

@@ -28,20 +28,24 @@
 // epilogue).  Every wait is time-bounded; a timeout is reported as
 // HYPIC_ETIMEOUT.
 #include "internal.cuh"
+#include "dense_common.cuh"
 #include "sm100.cuh"
 
 namespace hypic {
 namespace {
 
 using namespace sm100;
+using dense::split_pair;
+using dense::wait_or_abort;
+using dense::exponent_of;
 
-constexpr int kC = 64;          // tokens per chunk
+constexpr int kC = dense::kC;    // tokens per chunk
 constexpr int kD = 128;         // d_k = d_v
 constexpr int kNS = 2;          // TMA stages
 constexpr int kThreads = 576;   // 18 warps
 constexpr int kPrep = 256;      // warps 2..9
 constexpr int kState = 256;     // warps 10..17
-constexpr int kLd = 68;         // padded row stride of the fp32 L / A work tiles (16-byte rows)
+constexpr int kLd = dense::kLd;  // padded row stride of the fp32 L / A work tiles
 
 // shared memory map (offsets from the 1024-aligned base)
 constexpr int kBox = kC * 128;              // 64 channels x 64 tokens, bf16: 8 KB
@@ -75,30 +79,6 @@ struct DenseCtrl {
 constexpr int kSmem = kCtl + (int)sizeof(DenseCtrl) + 1024;
 static_assert(kSmem <= 232448, "fits in one SM's shared memory");
 
-// x = hi + lo with both in bf16 (pairs packed for elements 2c, 2c+1)
-__device__ __forceinline__ void split_pair(float x0, float x1, uint32_t &hi, uint32_t &lo) {
-    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - __low2float(h), x1 - __high2float(h));
-    hi = *reinterpret_cast<const uint32_t *>(&h);
-    lo = *reinterpret_cast<const uint32_t *>(&l);
-}
-
-__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abortp) {
-    if (*abortp) return false;
-    if (!mbar_wait(bar, parity)) {
-        *abortp = 1;
-        return false;
-    }
-    return true;
-}
-
-__device__ __forceinline__ int exponent_of(float mx) {   // 2^e <= mx < 2^(e+1)
-    if (!(mx > 0.f)) return 0;
-    int ex;
-    frexpf(mx, &ex);
-    return ex - 1;
-}
-
 // max over the 8 state warps (named barrier 2)
 __device__ __forceinline__ float state_max(float mx, DenseCtrl *ctl, int sw, int lane) {
 #pragma unroll
@@ -110,51 +90,6 @@ __device__ __forceinline__ float state_max(float mx, DenseCtrl *ctl, int sw, int
     for (int w = 0; w < 8; ++w) mx = fmaxf(mx, ctl->redmax[w]);
     bar_sync(2, kState);
     return mx;
-}
-
-// Off-diagonal blocks of A = (I + L)^-1 at block distance DIST:
-//   T = sum_{k=j}^{i-1} L_ik A_kj,  A_ij = -A_ii T   (16 x 16 blocks),
-// four adjacent columns of one row per thread (16-byte loads of A and T).
-template <int DIST>
-__device__ __forceinline__ void inverse_level(const float *Lw, float *Aw, float *Tw, int pt) {
-    constexpr int NB = 4 - DIST;
-    if (pt < NB * 64) {
-        const int blk = pt >> 6, r = (pt >> 2) & 15, c4 = (pt & 3) * 4;
-        const int bi = blk + DIST, bj = bi - DIST;
-        const float *lrow = Lw + (bi * 16 + r) * kLd + bj * 16;
-        const float *acol = Aw + (bj * 16) * kLd + bj * 16 + c4;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int k = 0; k < 16 * DIST; ++k) {
-            const float lv = lrow[k];
-            const float4 av = *reinterpret_cast<const float4 *>(acol + k * kLd);
-            acc.x = fmaf(lv, av.x, acc.x);
-            acc.y = fmaf(lv, av.y, acc.y);
-            acc.z = fmaf(lv, av.z, acc.z);
-            acc.w = fmaf(lv, av.w, acc.w);
-        }
-        *reinterpret_cast<float4 *>(Tw + blk * 256 + r * 16 + c4) = acc;
-    }
-    bar_sync(1, kPrep);
-    if (pt < NB * 64) {
-        const int blk = pt >> 6, r = (pt >> 2) & 15, c4 = (pt & 3) * 4;
-        const int bi = blk + DIST, bj = bi - DIST;
-        const float *arow = Aw + (bi * 16 + r) * kLd + bi * 16;   // A_ii, zero above the diagonal
-        const float *tcol = Tw + blk * 256 + c4;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const float av = arow[k];
-            const float4 tv = *reinterpret_cast<const float4 *>(tcol + k * 16);
-            acc.x = fmaf(av, tv.x, acc.x);
-            acc.y = fmaf(av, tv.y, acc.y);
-            acc.z = fmaf(av, tv.z, acc.z);
-            acc.w = fmaf(av, tv.w, acc.w);
-        }
-        *reinterpret_cast<float4 *>(Aw + (bi * 16 + r) * kLd + bj * 16 + c4) =
-            make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-    }
-    bar_sync(1, kPrep);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: <= 96 registers per thread
@@ -385,32 +320,8 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: <= 96 registers pe
                 }
             }
             bar_sync(1, kPrep);
-            // ---- A = (I + L)^-1: 16 x 16 diagonal blocks by forward substitution (registers)
-            if (pt < 64) {
-                const int b0 = (pt >> 4) * 16, jc = pt & 15, col = b0 + jc;
-                float ac[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float sum = 0.f;
-#pragma unroll
-                    for (int k = 0; k < i; ++k) sum = fmaf(Lw[(b0 + i) * kLd + b0 + k], ac[k], sum);
-                    ac[i] = i < jc ? 0.f : (i == jc ? 1.f : -sum);
-                }
-#pragma unroll
-                for (int i = 0; i < 16; ++i) Aw[(b0 + i) * kLd + col] = ac[i];
-            } else {
-                // zero the strictly upper off-diagonal blocks
-                for (int e = pt - 64; e < 6 * 256; e += kPrep - 64) {
-                    const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15;
-                    const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-                    const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-                    Aw[(bi * 16 + r) * kLd + bj * 16 + c] = 0.f;
-                }
-            }
-            bar_sync(1, kPrep);
-            inverse_level<1>(Lw, Aw, Tw, pt);
-            inverse_level<2>(Lw, Aw, Tw, pt);
-            inverse_level<3>(Lw, Aw, Tw, pt);
+            // ---- A = (I + L)^-1 (blocked, shared memory)
+            dense::tri_inverse<kPrep, 1>(Lw, Aw, Tw, pt);
             // ---- A -> bf16 hi / lo operand tiles (row t, s contiguous, 128-byte swizzle)
             if (!bar_and(1, kPrep, mbar_wait(&ctl->aop_free[par], ((uint32_t)(j >> 1) & 1u) ^ 1u) && !*abortp)) {
                 *abortp = 1;

@@ -1,0 +1,685 @@
+// scan_dense_ws.cu -- gated delta rule segment scan in two passes over a
+// caller-owned workspace: a chunk-parallel preparation pass and the state pass.
+//
+// Chunked WY/UT form of S_t = alpha_t (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T
+// (C = 64 tokens per chunk; b_t = in-chunk cumulative decay, b_C its total):
+//   L_ts = beta_t (b_t / b_s) k_t.k_s  (s < t),   A = (I + L)^-1
+//   W = A diag(beta b) K,   U = A diag(beta) V
+//   for X = [M | S] (transition and state side by side, d x 2d):
+//   Delta = [0 | U] - W X_0,   X <- b_C X_0 + K^T diag(b_C / b) Delta.
+// (Within a chunk delta_t = beta_t (v_t - alpha_t S_{t-1}^T k_t) satisfies
+// (I + L) Delta = diag(beta) V - diag(beta b) K S_0.)
+//
+// Pass 1 (dense_prep_kernel) depends only on a chunk's own keys and gates, so
+// every chunk of every (layer, segment, head) runs in parallel: gates, the Gram
+// matrix on tcgen05, L, and the blocked inverse A, written to one workspace
+// record per chunk.  Pass 2 (dense_state_kernel) walks the chunks of a chain in
+// order with X^T in TMEM (two CTAs per chain: transition half, state half):
+//   W^T = K^T (A diag(beta b))^T, U^T = V^T (A diag(beta))^T  (A split bf16 hi + lo)
+//   Delta^T = U^T - X0^T W^T    (X0 and W each split hi + lo: three products)
+//   X^T    += Delta~^T K        (Delta~ = Delta diag(b_C / b), split hi + lo)
+// W and U are built by their own warps one chunk ahead of the state warps.
+#include "dense_common.cuh"
+#include "internal.cuh"
+#include "sm100.cuh"
+
+namespace hypic {
+namespace {
+
+using namespace sm100;
+using dense::exponent_of;
+using dense::kC;
+using dense::kLd;
+using dense::split_pair;
+using dense::wait_or_abort;
+
+constexpr int kD = 128;
+
+// ---------------------------------------------------------------- workspace record
+// One record per (layer, head, chunk slot), floats:
+//   [0, 4096)      A = (I + L)^-1, row t at 64 t; the 16-byte group g of row t is
+//                  stored at group position g ^ (t & 15) (conflict-free row reads)
+//   4096 + t       b_C / b_t
+//   4160 + t       beta_t b_t
+//   4224 + t       beta_t
+//   4288, 4289     log b_C, b_C
+// Chunk j of segment s (tokens from t0) uses slot s + floor(t0 / 64) + j, so the
+// slots of different segments never collide and a (layer, head) needs at most
+// n_seg + floor(N / 64) of them.
+constexpr int kRecA = 0, kRecGw = 4096, kRecGbb = 4160, kRecGbeta = 4224, kRecLC = 4288, kRecBC = 4289;
+constexpr int kRecFloats = 4296;                  // padded to a multiple of 4 floats
+constexpr int kRecBytes = kRecFloats * 4;         // 17184
+
+__host__ __device__ inline int64_t n_slots(int64_t N, int n_seg) { return (int64_t)n_seg + N / kC; }
+
+// ================================================================ pass 1: preparation
+
+constexpr int kPThreads = 128;
+// shared memory (from the 1024-aligned base): K boxes 0 / 1 and 8 KB the padded
+// Gram rows read (the fp32 L tile overlays all of it once the Gram is done),
+// the fp32 A tile, temporaries, control.
+constexpr int kPK = 0;
+constexpr int kPAw = 24576;
+constexpr int kPTw = kPAw + kC * kLd * 4;
+constexpr int kPCtl = kPTw + 3 * 256 * 4;
+static_assert(kC * kLd * 4 <= 24576, "L overlays the key tile");
+
+struct PrepCtl {
+    uint64_t full, mma;
+    uint32_t tmem;
+    float gl[kC], gbeta[kC];
+};
+constexpr int kPSmem = kPCtl + (int)sizeof(PrepCtl) + 1024;
+
+__global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_constant__ CUtensorMap tm_k,
+                                                               const ScanArgs a, int64_t slots) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    PrepCtl *ctl = reinterpret_cast<PrepCtl *>(smem + kPCtl);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h = (int)(blockIdx.x % (unsigned)a.H);
+    const int64_t slot = blockIdx.x / (unsigned)a.H;
+    const int l = blockIdx.y;
+
+    // slot -> (segment, chunk): the last segment s with s + floor(t0_s / 64) <= slot
+    int lo = 0, hi = a.n_seg - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((int64_t)mid + a.seg_offsets[mid] / kC <= slot) lo = mid;
+        else hi = mid - 1;
+    }
+    const int seg = lo;
+    const int64_t t0 = a.seg_offsets[seg], t1 = a.seg_offsets[seg + 1];
+    if (!(t0 >= 0 && t0 <= t1 && t1 <= a.N)) return;   // the state pass flags it
+    const int64_t j = slot - (seg + t0 / kC);
+    if (j < 0 || j * kC >= t1 - t0) return;            // a slot no chunk uses
+    const int64_t c0 = t0 + j * kC;                     // first token of the chunk
+    float *rec = a.ws + ((int64_t)l * a.H + h) * slots * kRecFloats + slot * kRecFloats;
+
+    if (tid == 0) {
+        mbar_init(&ctl->full, 1);
+        mbar_init(&ctl->mma, 1);
+        mbar_fence_init();
+        mbar_expect_tx(&ctl->full, 2 * kC * 128);
+        const int row = (int)((int64_t)l * a.N + c0);
+        tma_load_3d(smem + kPK, &tm_k, &ctl->full, 0, h, row);
+        tma_load_3d(smem + kPK + 8192, &tm_k, &ctl->full, 64, h, row);
+    }
+    if (warp == 0) tmem_alloc(&ctl->tmem, 64);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem;
+    bool ok = true;
+
+    // ---- gates (warp 0): Lambda, b_C / b, beta b, beta, log b_C, b_C
+    if (warp == 0) {
+        float lg[2], pb[2], inc[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int64_t t = c0 + lane + 32 * q;
+            const bool v = t < t1;
+            const int64_t row = ((int64_t)l * a.N + t) * a.H + h;
+            lg[q] = v ? logf(a.alpha[row]) : 0.f;
+            pb[q] = v ? (a.beta ? a.beta[row] : 1.f) : 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            float x = lg[q];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, x, off);
+                if (lane >= off) x += y;
+            }
+            inc[q] = x;
+        }
+        inc[1] += __shfl_sync(0xffffffffu, inc[0], 31);
+        const float total = __shfl_sync(0xffffffffu, inc[1], 31);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int t = lane + 32 * q;
+            ctl->gl[t] = inc[q];
+            ctl->gbeta[t] = pb[q];
+            rec[kRecGw + t] = expf(total - inc[q]);
+            rec[kRecGbb + t] = pb[q] * expf(inc[q]);
+            rec[kRecGbeta + t] = pb[q];
+        }
+        if (lane == 0) {
+            rec[kRecLC] = total;
+            rec[kRecBC] = expf(total);
+        }
+        // Gram G = K K^T: M = 128 rows of which 64..127 read past the keys and are unused
+        if (lane == 0) {
+            ok = mbar_wait(&ctl->full, 0);
+            if (ok) {
+                tc_fence_after();
+                constexpr uint32_t id_gram = idesc_bf16_f32(128, 64, false, false);
+                const uint32_t kb = smem_addr(smem + kPK);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t off = (uint32_t)(ks >> 2) * 8192u + (uint32_t)(ks & 3) * 32u;
+                    const uint64_t d = smem_desc_sw128(kb + off, 0, 1024);
+                    mma_f16(tmem, d, d, id_gram, ks > 0);
+                }
+            }
+            mma_commit(&ctl->mma);
+        }
+    }
+    ok = __syncthreads_and(ok && mbar_wait(&ctl->mma, 0));
+    tc_fence_after();
+    float *Lw = reinterpret_cast<float *>(smem + kPK);
+    float *Aw = reinterpret_cast<float *>(smem + kPAw);
+    float *Tw = reinterpret_cast<float *>(smem + kPTw);
+    if (ok) {
+        // ---- L[t][s] = beta_t exp(Lambda_t - Lambda_s) G[t][s] for s < t (warps 0, 1: rows 0..63)
+        if (warp < 2) {
+            const int t = warp * 32 + lane;
+            const float lt = ctl->gl[t], bt = ctl->gbeta[t];
+            for (int cb = 0; cb < 2; ++cb) {
+                uint32_t r[32];
+                tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(cb * 32), r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int sc = cb * 32 + i;
+                    Lw[t * kLd + sc] = sc < t ? bt * __expf(lt - ctl->gl[sc]) * __uint_as_float(r[i]) : 0.f;
+                }
+            }
+        }
+        __syncthreads();
+        dense::tri_inverse<kPThreads, 1>(Lw, Aw, Tw, tid);
+        // ---- A -> the record (16-byte groups, swizzled by row)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int f = tid + kPThreads * i;   // 0 .. 1023
+            const int t = f >> 4, g = f & 15;
+            const float4 v = *reinterpret_cast<const float4 *>(Aw + t * kLd + g * 4);
+            *reinterpret_cast<float4 *>(rec + kRecA + t * 64 + ((g ^ (t & 15)) << 2)) = v;
+        }
+    } else if (tid == 0 && a.d_err) {
+        atomicExch(a.d_err, (int)HYPIC_ETIMEOUT);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 64);
+    }
+}
+
+// ================================================================ pass 2: state
+
+constexpr int kNS = 2;            // stages
+constexpr int kThreads = 672;     // 21 warps: 0 TMA, 1-4 W/U operands, 5-20 state
+constexpr int kWT = 128;          // W warps' threads
+constexpr int kState = 512;       // state warps' threads
+
+// stage: K (two 64-channel boxes), V (state half), the chunk's record
+constexpr int kBox = kC * 128;                         // 64 channels x 64 tokens, bf16: 8 KB
+constexpr int kSK = 0, kSV = 2 * kBox, kSRec = 4 * kBox;
+constexpr int kStage = kSRec + ((kRecBytes + 1023) / 1024) * 1024;   // 50176
+constexpr int kWt = kNS * kStage;           // -W^T tiles, hi / lo (128 rows x 128 B each)
+constexpr int kAb2 = kWt + 2 * 16384;       // A diag(beta b), hi / lo (64 rows x 128 B each)
+constexpr int kAb = kAb2 + 2 * 8192;        // A diag(beta), hi / lo
+constexpr int kCtl = kAb + 2 * 8192;
+static_assert(kStage % 1024 == 0 && kWt % 1024 == 0, "operand tiles 1024-byte aligned");
+
+// TMEM column map (512 allocated)
+constexpr uint32_t kTx = 0;       // X^T half, fp32 (128 columns)
+constexpr uint32_t kTxop = 128;   // X0^T operand: hi [128, 192), lo [192, 256), bf16 pairs
+constexpr uint32_t kTacc = 256;   // U^T - X0^T W^T, then Delta~^T operand in place (64)
+constexpr uint32_t kTw = 320;     // W^T accumulator (64 columns)
+
+struct StateCtl {
+    uint64_t full[kNS], empty[kNS];
+    uint64_t aop_ready, wop_ready, w_done, wfree, d_done, x_done;
+    uint64_t drain[2];
+    float redmax[16];
+    uint32_t tmem;
+    int abort;
+};
+constexpr int kSmem = kCtl + (int)sizeof(StateCtl) + 1024;
+static_assert(kSmem <= 232448, "fits in one SM's shared memory");
+
+// max over the 16 state warps (named barrier 2)
+__device__ __forceinline__ float state_max(float mx, StateCtl *ctl, int sw, int lane) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (lane == 0) ctl->redmax[sw] = mx;
+    bar_sync(2, kState);
+    mx = 0.f;
+#pragma unroll
+    for (int w = 0; w < 16; ++w) mx = fmaxf(mx, ctl->redmax[w]);
+    bar_sync(2, kState);
+    return mx;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers per thread
+    dense_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                       const ScanArgs a, int64_t slots) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    StateCtl *ctl = reinterpret_cast<StateCtl *>(smem + kCtl);
+    volatile int *abortp = &ctl->abort;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const int half = blockIdx.x & 1;   // 0: transition M, 1: state S
+    const int unit = blockIdx.x >> 1;
+    const int h = unit % a.H;
+    const int seg = (unit / a.H) % a.n_seg;
+    const int l = unit / (a.H * a.n_seg);
+    int64_t t0 = a.seg_offsets[seg], t1 = a.seg_offsets[seg + 1];
+    const bool bad = !(t0 >= 0 && t0 <= t1 && t1 <= a.N);
+    if (bad) t0 = t1 = 0;
+    const int nc = (int)((t1 - t0 + kC - 1) / kC);
+    const int64_t row0 = (int64_t)l * a.N + t0;
+    const float *recs = a.ws + (((int64_t)l * a.H + h) * slots + seg + t0 / kC) * kRecFloats;
+
+    if (threadIdx.x == 0) {
+        if (bad) flag_index_error(a.d_err);
+        for (int s = 0; s < kNS; ++s) {
+            mbar_init(&ctl->full[s], 1);
+            mbar_init(&ctl->empty[s], 1);
+        }
+        mbar_init(&ctl->aop_ready, kWT / 32);
+        mbar_init(&ctl->wop_ready, kWT / 32);
+        mbar_init(&ctl->w_done, 1);
+        mbar_init(&ctl->wfree, 1);
+        mbar_init(&ctl->d_done, 1);
+        mbar_init(&ctl->x_done, 1);
+        mbar_init(&ctl->drain[0], 1);
+        mbar_init(&ctl->drain[1], 1);
+        ctl->abort = 0;
+        mbar_fence_init();
+        tma_prefetch(&tm_k);
+        if (half) tma_prefetch(&tm_v);
+    }
+    if (warp == 0) tmem_alloc(&ctl->tmem, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem;
+
+    constexpr uint32_t id_wu = idesc_bf16_f32(128, 64, true, false);   // K^T / V^T (MN-major) x A tiles
+    constexpr uint32_t id_d = idesc_bf16_f32(128, 64, false, true);    // X0^T (TMEM) x W^T (MN-major)
+    constexpr uint32_t id_x = idesc_bf16_f32(128, 128, false, true);   // Delta~^T (TMEM) x K (MN-major)
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int issued = 0;
+            for (int j = 0; j < nc; ++j) {
+                const int s = j % kNS;
+                if (!wait_or_abort(&ctl->empty[s], ((uint32_t)(j / kNS) & 1u) ^ 1u, abortp)) break;
+                uint8_t *st = smem + s * kStage;
+                const int row = (int)(row0 + (int64_t)j * kC);
+                mbar_expect_tx(&ctl->full[s], (uint32_t)((half ? 4 : 2) * kBox + kRecBytes));
+                tma_load_3d(st + kSK, &tm_k, &ctl->full[s], 0, h, row);
+                tma_load_3d(st + kSK + kBox, &tm_k, &ctl->full[s], 64, h, row);
+                if (half) {   // V only feeds the state half
+                    tma_load_3d(st + kSV, &tm_v, &ctl->full[s], 0, h, row);
+                    tma_load_3d(st + kSV + kBox, &tm_v, &ctl->full[s], 64, h, row);
+                }
+                bulk_load(st + kSRec, recs + (int64_t)j * kRecFloats, (uint32_t)kRecBytes, &ctl->full[s]);
+                issued = j + 1;
+            }
+            if (*abortp)
+                for (int j = issued - kNS < 0 ? 0 : issued - kNS; j < issued; ++j)
+                    mbar_wait(&ctl->full[j % kNS], (uint32_t)(j / kNS) & 1u);
+        }
+    } else if (warp <= 4) {
+        // ------------------------------------------------------------ W / U operand warps
+        const int wt = threadIdx.x - 32;   // 0..127
+        const bool issuer = wt == 0;
+        const int quarter = warp & 3;
+        for (int j = 0; j < nc; ++j) {
+            const int s = j % kNS;
+            const uint32_t par = (uint32_t)j & 1u;
+            const uint8_t *st = smem + s * kStage;
+            const float *rec = reinterpret_cast<const float *>(st + kSRec);
+            // the chunk is in, and the previous chunk's operand tiles are consumed
+            bool ok = wait_or_abort(&ctl->full[s], (uint32_t)(j / kNS) & 1u, abortp);
+            if (j > 0) ok = ok && wait_or_abort(&ctl->wfree, par ^ 1u, abortp);
+            if (!bar_and(1, kWT, ok)) {
+                *abortp = 1;
+                break;
+            }
+            // ---- A diag(beta b) and A diag(beta) -> bf16 hi / lo tiles (row t, s contiguous, 128B swizzle)
+            {
+                const int t = wt & 63, cb = (wt >> 6) * 4;   // four 8-column groups per thread
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const int c = cb + cc;
+                    const float4 x0 = *reinterpret_cast<const float4 *>(rec + kRecA + t * 64 + (((2 * c) ^ (t & 15)) << 2));
+                    const float4 x1 =
+                        *reinterpret_cast<const float4 *>(rec + kRecA + t * 64 + (((2 * c + 1) ^ (t & 15)) << 2));
+                    const float av[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+                    const int off = t * 128 + ((c ^ (t & 7)) << 4);
+                    uint32_t hi[4], lo[4];
+#pragma unroll
+                    for (int p = 0; p < 4; ++p)
+                        split_pair(av[2 * p] * rec[kRecGbb + c * 8 + 2 * p],
+                                   av[2 * p + 1] * rec[kRecGbb + c * 8 + 2 * p + 1], hi[p], lo[p]);
+                    *reinterpret_cast<uint4 *>(smem + kAb2 + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4 *>(smem + kAb2 + 8192 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    if (half) {
+#pragma unroll
+                        for (int p = 0; p < 4; ++p)
+                            split_pair(av[2 * p] * rec[kRecGbeta + c * 8 + 2 * p],
+                                       av[2 * p + 1] * rec[kRecGbeta + c * 8 + 2 * p + 1], hi[p], lo[p]);
+                        *reinterpret_cast<uint4 *>(smem + kAb + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                        *reinterpret_cast<uint4 *>(smem + kAb + 8192 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    }
+                }
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->aop_ready);
+            bar_sync(1, kWT);
+            // ---- W^T = K^T (A diag(beta b))^T
+            if (issuer) {
+                tc_fence_after();
+                const uint32_t kb = smem_addr(st + kSK);
+                const uint32_t ab2 = smem_addr(smem + kAb2);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint64_t ad = smem_desc_sw128(kb + (uint32_t)ks * 2048u, kBox, 1024);
+                    mma_f16(tmem + kTw, ad, smem_desc_sw128(ab2 + (uint32_t)ks * 32u, 0, 1024), id_wu, ks > 0);
+                    mma_f16(tmem + kTw, ad, smem_desc_sw128(ab2 + 8192u + (uint32_t)ks * 32u, 0, 1024), id_wu, 1u);
+                }
+                mma_commit(&ctl->w_done);
+            }
+            if (!bar_and(1, kWT, wait_or_abort(&ctl->w_done, par, abortp))) {
+                *abortp = 1;
+                break;
+            }
+            tc_fence_after();
+            // ---- -W^T -> bf16 hi / lo tiles, MN-major (row k, t contiguous, 128B swizzle)
+            {
+                const int k = quarter * 32 + lane;
+                for (int cb = 0; cb < 2; ++cb) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + kTw + (uint32_t)(cb * 32), r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const int c = cb * 4 + cc;
+                        uint32_t hi[4], lo[4];
+#pragma unroll
+                        for (int p = 0; p < 4; ++p)
+                            split_pair(-__uint_as_float(r[cc * 8 + 2 * p]), -__uint_as_float(r[cc * 8 + 2 * p + 1]),
+                                       hi[p], lo[p]);
+                        const int off = k * 128 + ((c ^ (k & 7)) << 4);
+                        *reinterpret_cast<uint4 *>(smem + kWt + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                        *reinterpret_cast<uint4 *>(smem + kWt + 16384 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->wop_ready);
+        }
+        if (issuer && *abortp) {   // drain: completes once this thread's MMAs are done
+            mma_commit(&ctl->drain[0]);
+            mbar_wait(&ctl->drain[0], 0);
+        }
+    } else {
+        // ------------------------------------------------------------ state warps
+        const int st = threadIdx.x - 160;           // 0..511
+        const bool issuer = st == 0;
+        const int sw = warp - 5;                    // 0..15
+        const int cg = sw >> 2;                     // column group of this warp
+        const int quarter = warp & 3;               // TMEM lanes this warp may touch
+        const int m = quarter * 32 + lane;          // column of X = TMEM lane
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t tx = tmem + lane_off + kTx + (uint32_t)(cg * 32);
+        const uint32_t txop = tmem + lane_off + kTxop + (uint32_t)(cg * 16);
+        const uint32_t tacc = tmem + lane_off + kTacc + (uint32_t)(cg * 16);
+        // Transition half: M_true = exp(lam_d + lam_exp ln2) M_stored, and each chunk
+        // stores T_chunk M / b_C (log b_C into lam_d).  State half: S_true =
+        // exp(ls) S_stored.  Either way the update only accumulates into TMEM; X is
+        // rewritten only to renormalise (every 8 chunks for M, when ls < -20 for S)
+        // or on a chunk whose total decay is below e^-40 (exact write-back form).
+        int lam_exp = 0;
+        double lam_d = 0.0;
+        float ls = 0.f;
+
+        {   // initial X^T: identity (transition) or zero (state)
+            uint32_t r[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint((half == 0 && cg * 32 + i == m) ? 1.f : 0.f);
+            tmem_st32(tx, r);
+            tmem_wait_st();
+        }
+
+        for (int j = 0; j < nc; ++j) {
+            const int s = j % kNS;
+            const uint32_t par = (uint32_t)j & 1u;
+            const uint8_t *stg = smem + s * kStage;
+            const float *rec = reinterpret_cast<const float *>(stg + kSRec);
+            bool ok = wait_or_abort(&ctl->full[s], (uint32_t)(j / kNS) & 1u, abortp);
+            if (j > 0) ok = ok && wait_or_abort(&ctl->x_done, par ^ 1u, abortp);
+            if (!bar_and(2, kState, ok)) {
+                *abortp = 1;
+                break;
+            }
+            tc_fence_after();
+            // ---- U^T = V^T (A diag(beta))^T into the accumulator (state half), on the
+            // tensor cores while the X operand is converted below
+            if (issuer && half) {
+                if (wait_or_abort(&ctl->aop_ready, par, abortp)) {
+                    tc_fence_after();
+                    const uint32_t vb = smem_addr(stg + kSV), ab = smem_addr(smem + kAb);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const uint64_t ad = smem_desc_sw128(vb + (uint32_t)ks * 2048u, kBox, 1024);
+                        mma_f16(tmem + kTacc, ad, smem_desc_sw128(ab + (uint32_t)ks * 32u, 0, 1024), id_wu, ks > 0);
+                        mma_f16(tmem + kTacc, ad, smem_desc_sw128(ab + 8192u + (uint32_t)ks * 32u, 0, 1024), id_wu,
+                                1u);
+                    }
+                }
+            }
+            // ---- scales of this chunk
+            const float LC = rec[kRecLC];               // log of the chunk's total decay
+            const bool slow = LC < -40.f;
+            const bool renorm = slow || (half == 0 ? (j % 8 == 0) : (ls < -20.f));
+            float g = 1.f;        // X_stored <- g * wscale * X_stored when rewritten
+            float wscale = 1.f;
+            float fP, fD;         // X0_true = fP * g * X_stored;  Delta~ = fD * (b_C / b) * Delta
+            if (half == 0) {
+                if (renorm) {
+                    uint32_t r[32];
+                    tmem_ld32(tx, r);
+                    tmem_wait_ld();
+                    float mx = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fabsf(__uint_as_float(r[i])));
+                    const int e = exponent_of(state_max(mx, ctl, sw, lane));
+                    g = ldexpf(1.f, -e);
+                    lam_exp += e;
+                }
+                wscale = slow ? rec[kRecBC] : 1.f;
+                fP = 1.f;
+                fD = slow ? 1.f : expf(-LC);
+                if (!slow) lam_d += (double)LC;
+            } else {
+                if (slow) {
+                    g = expf(ls);
+                    wscale = rec[kRecBC];
+                    fP = 1.f;
+                    fD = 1.f;
+                    ls = 0.f;
+                } else {
+                    if (renorm) {
+                        const int q = (int)rintf(ls * 1.44269504088896341f);
+                        g = ldexpf(1.f, q);
+                        ls -= (float)q * 0.69314718055994531f;
+                    }
+                    fP = expf(ls);
+                    fD = expf(-(ls + LC));
+                    ls += LC;
+                }
+            }
+            // ---- X round trip (TMEM only): operand X0_true (hi + lo), X_stored rescaled if due
+            {
+                const float mult = g * fP, sc = g * wscale;
+                uint32_t r[32], hi[16], lo[16];
+                tmem_ld32(tx, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int p = 0; p < 16; ++p)
+                    split_pair(mult * __uint_as_float(r[2 * p]), mult * __uint_as_float(r[2 * p + 1]), hi[p], lo[p]);
+                tmem_st16(txop, hi);
+                tmem_st16(txop + 64u, lo);
+                if (renorm) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(sc * __uint_as_float(r[i]));
+                    tmem_st32(tx, r);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            bar_sync(2, kState);
+            // ---- Delta^T = U^T - X0^T W^T (three-term split)
+            if (issuer) {
+                if (wait_or_abort(&ctl->wop_ready, par, abortp)) {
+                    tc_fence_after();
+                    const uint32_t wtile = smem_addr(smem + kWt);
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint64_t bh = smem_desc_sw128(wtile + (uint32_t)ks * 2048u, 16384, 1024);
+                        const uint64_t bl = smem_desc_sw128(wtile + 16384u + (uint32_t)ks * 2048u, 16384, 1024);
+                        const uint32_t ah = tmem + kTxop + (uint32_t)ks * 8u, al = ah + 64u;
+                        mma_f16_ta(tmem + kTacc, ah, bh, id_d, (half || ks > 0) ? 1u : 0u);
+                        mma_f16_ta(tmem + kTacc, ah, bl, id_d, 1u);
+                        mma_f16_ta(tmem + kTacc, al, bh, id_d, 1u);
+                    }
+                }
+                mma_commit(&ctl->d_done);
+                mma_commit(&ctl->wfree);
+            }
+            // ---- Delta~^T = fD Delta^T diag(b_C / b) -> bf16 hi / lo in place
+            if (!bar_and(2, kState, wait_or_abort(&ctl->d_done, par, abortp))) {
+                *abortp = 1;
+                break;
+            }
+            tc_fence_after();
+            {
+                uint32_t r[16], hi[8], lo[8];
+                tmem_ld16(tacc, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int p = 0; p < 8; ++p) {
+                    const int t = cg * 16 + 2 * p;
+                    split_pair(fD * rec[kRecGw + t] * __uint_as_float(r[2 * p]),
+                               fD * rec[kRecGw + t + 1] * __uint_as_float(r[2 * p + 1]), hi[p], lo[p]);
+                }
+                tmem_st8(tacc, hi);          // tokens cg*16 .. +15: hi in the first 8 columns,
+                tmem_st8(tacc + 8u, lo);     // lo in the next 8 (this thread's own columns)
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            bar_sync(2, kState);
+            // ---- X^T += Delta~^T K (K as the MN-major B operand: row t, channels contiguous)
+            if (issuer) {
+                tc_fence_after();
+                const uint32_t kb = smem_addr(stg + kSK);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint64_t bd = smem_desc_sw128(kb + (uint32_t)ks * 2048u, kBox, 1024);
+                    const uint32_t ah = tmem + kTacc + (uint32_t)ks * 16u;
+                    mma_f16_ta(tmem + kTx, ah, bd, id_x, 1u);
+                    mma_f16_ta(tmem + kTx, ah + 8u, bd, id_x, 1u);
+                }
+                mma_commit(&ctl->x_done);
+                mma_commit(&ctl->empty[s]);
+            }
+        }
+        if (issuer && *abortp) {
+            mma_commit(&ctl->drain[1]);
+            mbar_wait(&ctl->drain[1], 0);
+        }
+
+        // ------------------------------------------------------------ epilogue
+        bool ok = true;
+        if (nc > 0) ok = wait_or_abort(&ctl->x_done, (uint32_t)(nc - 1) & 1u, abortp);
+        if (bar_and(2, kState, ok)) {
+            tc_fence_after();
+            const int64_t u_out = ((int64_t)l * a.n_seg + seg) * a.H + h;
+            uint32_t r[32];
+            tmem_ld32(tx, r);
+            tmem_wait_ld();
+            float scale;
+            if (half == 0) {
+                float mx = 0.f;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fabsf(__uint_as_float(r[i])));
+                const int e = exponent_of(state_max(mx, ctl, sw, lane));
+                scale = ldexpf(1.f, -e);
+                lam_exp += e;
+                if (st == 0) a.lam_out[u_out] = (float)(lam_d + (double)lam_exp * 0.69314718055994530942);
+            } else {
+                scale = expf(ls);
+            }
+            float *out = (half == 0 ? a.M_out : a.S_out) + u_out * kD * kD;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) out[(int64_t)(cg * 32 + i) * kD + m] = scale * __uint_as_float(r[i]);
+        } else {
+            *abortp = 1;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0 && *abortp && a.d_err) atomicExch(a.d_err, (int)HYPIC_ETIMEOUT);
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- host side
+
+bool scan_dense_ws_shape(const ScanArgs &a) {
+    return a.fam == HYPIC_DENSE && a.in_dtype == HYPIC_BF16 && a.dk == 128 && a.dv == 128 &&
+           a.o_out == nullptr && a.N > 0 && (int64_t)a.n_layers * a.N < ((int64_t)1 << 31) &&
+           (int64_t)a.n_layers * a.n_seg * a.H < ((int64_t)1 << 30) &&
+           n_slots(a.N, a.n_seg) * a.H < ((int64_t)1 << 31) && a.n_layers <= 65535;
+}
+
+bool scan_dense_ws_supported(const ScanArgs &a) {
+    return scan_dense_ws_shape(a) && tensor_map_encoder() != nullptr;
+}
+
+int64_t scan_dense_ws_bytes(const ScanArgs &a) {
+    return (int64_t)a.n_layers * a.H * n_slots(a.N, a.n_seg) * kRecBytes;
+}
+
+cudaError_t launch_scan_dense_ws(const ScanArgs &a, cudaStream_t s) {
+    const int64_t units = (int64_t)a.n_layers * a.n_seg * a.H;
+    if (units == 0) return cudaSuccess;
+    const uint64_t rows = (uint64_t)a.n_layers * (uint64_t)a.N;
+    CUtensorMap mk, mv;
+    if (!make_tensor_map_3d(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.k, 128, a.H, rows, 64, kC,
+                            CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map_3d(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.v, 128, a.H, rows, 64, kC,
+                            CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    const int64_t slots = n_slots(a.N, a.n_seg);
+    cudaError_t e = cudaFuncSetAttribute(dense_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(dense_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    dense_prep_kernel<<<dim3((unsigned)(slots * a.H), (unsigned)a.n_layers), kPThreads, kPSmem, s>>>(mk, a, slots);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    dense_state_kernel<<<(unsigned)(2 * units), kThreads, kSmem, s>>>(mk, mv, a, slots);
+    return cudaGetLastError();
+}
+
+}  // namespace hypic

@@ -82,6 +82,34 @@ def test_scan_rejects_bad_arguments(lib):
     assert scan(lib, S=0) == OK
 
 
+def scan_ws(lib, fam=2, dtype=0, L=1, S=2, N=64, H=2, dk=128, dv=128, ws=0x40000000, ws_bytes=1 << 30,
+            M=A + 0x1000000, o=0, q=0):
+    return lib.hypic_segment_scan_ws(fam, dtype, L, S, N, H, dk, dv, P(A), P(q or None), P(A), P(A), P(A),
+                                     P(None), P(A), P(M or None), P(A + 0x2000000), P(o or None),
+                                     P(ws or None), ws_bytes, P(None), P(None))
+
+
+def test_workspace_size_and_checks(lib):
+    """The two-pass dense scan: one 17184-byte record per (layer, head, chunk
+    slot), n_seg + N / 64 slots; other families and options take none."""
+    ws = lib.hypic_segment_scan_workspace_bytes
+    assert ws(2, 0, 30, 1, 2048, 32, 128, 128, 0) == 30 * 32 * (1 + 32) * 17184
+    assert ws(2, 0, 1, 3, 200, 2, 128, 128, 0) == 2 * (3 + 3) * 17184
+    assert ws(2, 0, 1, 1, 2048, 2, 128, 128, 1) == 0     # with o_t: single-pass kernels
+    assert ws(2, 1, 1, 1, 2048, 2, 128, 128, 0) == 0     # fp32 inputs
+    assert ws(2, 0, 1, 1, 2048, 2, 64, 64, 0) == 0
+    assert ws(0, 0, 1, 1, 2048, 2, 128, 128, 0) == 0
+    assert ws(2, 0, 1, 1, 2048, 0, 128, 128, 0) == EINVAL
+    need = ws(2, 0, 1, 2, 64, 2, 128, 128, 0)
+    assert scan_ws(lib, ws_bytes=need - 16) == EINVAL
+    assert scan_ws(lib, ws=0) == EINVAL
+    assert scan_ws(lib, ws=0x40000000 + 16) == EALIGN
+    assert scan_ws(lib, ws_bytes=-1) == EINVAL
+    assert scan_ws(lib, dk=96) == EUNSUP
+    assert scan_ws(lib, M=0) == EINVAL
+    assert scan_ws(lib, L=0) == OK
+
+
 def compose(lib, fam=0, n=3, H=2, dk=64, dv=64, lam=A, M=0, Sp=A, Sc=A + 0x100000,
             So=A + 0x200000, lp=0, Mp=0, lo=0, Mo=0):
     return lib.hypic_compose(fam, n, H, dk, dv, P(lam or None), P(M or None), P(Sp or None),

@@ -16,12 +16,18 @@ pytestmark = pytest.mark.gpu
 SCALAR, DIAG, DENSE = wl.SCALAR, wl.DIAG, wl.DENSE
 
 
-def gpu_scan(w, want_o=False, d_err=None):
+def gpu_scan(w, want_o=False, d_err=None, workspace="auto"):
     import linear_attention_state_gated_gb300 as hy
     dt = w["dtype"]
     return hy.segment_scan(w["family"], to_dev(w["k"], dt), to_dev(w["v"], dt),
                            to_dev(w["alpha"]), to_dev(w["seg_offsets"]), beta=to_dev(w["beta"]),
-                           q=to_dev(w["q"], dt) if want_o else None, want_o=want_o, d_err=d_err)
+                           q=to_dev(w["q"], dt) if want_o else None, want_o=want_o, d_err=d_err,
+                           workspace=workspace)
+
+
+# the dense bf16 d = 128 scan has two forms: two passes over scratch (the
+# default, "auto") and the single-pass kernel (no scratch, None)
+DENSE_FORMS = pytest.mark.parametrize("form", ["auto", None], ids=["two_pass", "single_pass"])
 
 
 def host(out):
@@ -131,11 +137,12 @@ def test_scalar_diag_full_size_sampled(fam, L):
         check(fam, sub, ref, TOL_SCAN_BF16)
 
 
+@DENSE_FORMS
 @pytest.mark.parametrize("L", [512, 2048])
-def test_dense_full_stack_sampled(L):
+def test_dense_full_stack_sampled(L, form):
     """30 layers x 32 heads x 128, one segment per layer (the benchmark's launch)."""
     w = wl.dense_stack(seg_len=L)
-    got = host(gpu_scan(w))
+    got = host(gpu_scan(w, workspace=form))
     for l, h in [(0, 0), (29, 31), (13, 7)]:
         ref = oracle.sequential(DENSE, w["k"][l:l + 1, :, h:h + 1], w["v"][l:l + 1, :, h:h + 1],
                                 w["alpha"][l:l + 1, :, h:h + 1], w["beta"][l:l + 1, :, h:h + 1])
@@ -144,26 +151,27 @@ def test_dense_full_stack_sampled(L):
         check(DENSE, sub, ref, TOL_SCAN_BF16)
 
 
-def test_dense_long_segment_and_special_gates():
+@DENSE_FORMS
+def test_dense_long_segment_and_special_gates(form):
     """Gated delta rule on long segments (many chunks of transition renormalisation),
     beta = 0 (pure decay: S = 0, T = prod(alpha) I) and alpha = beta = 1 (plain delta rule)."""
     w = wl.dense_stack(lengths=[8192, 3000], n_layers=1, H=2, d=128, seed=13)
-    check(DENSE, host(gpu_scan(w)), oracle_scan(w), TOL_SCAN_BF16)
+    check(DENSE, host(gpu_scan(w, workspace=form)), oracle_scan(w), TOL_SCAN_BF16)
     w0 = dict(w)
     w0["beta"] = np.zeros_like(w["beta"])
-    got = host(gpu_scan(w0))
+    got = host(gpu_scan(w0, workspace=form))
     ref = oracle_scan(w0)
     check(DENSE, got, ref, TOL_SCAN_BF16)
     assert np.all(got["S"] == 0)
     w1 = wl.dense_stack(lengths=[700, 129], n_layers=1, H=2, d=128, seed=14)
     w1["alpha"] = np.ones_like(w1["alpha"])
     w1["beta"] = np.ones_like(w1["beta"])
-    check(DENSE, host(gpu_scan(w1)), oracle_scan(w1), TOL_SCAN_BF16)
+    check(DENSE, host(gpu_scan(w1, workspace=form)), oracle_scan(w1), TOL_SCAN_BF16)
     # strong decay: chunks whose total decay is below e^-40 alternate with mild ones
     w2 = wl.dense_stack(lengths=[1000, 333], n_layers=1, H=2, d=128, seed=15)
     t = np.arange(w2["alpha"].shape[1])
     w2["alpha"][:, (t // 64) % 3 == 1] = 0.3
-    check(DENSE, host(gpu_scan(w2)), oracle_scan(w2), TOL_SCAN_BF16)
+    check(DENSE, host(gpu_scan(w2, workspace=form)), oracle_scan(w2), TOL_SCAN_BF16)
 
 
 @pytest.mark.parametrize("fam", [SCALAR, DIAG, DENSE], ids=["scalar", "diag", "dense"])
@@ -184,6 +192,25 @@ def test_segment_independence_bitwise(fam):
     g1 = gpu_scan(alone)
     for key in g1:
         assert torch.equal(g1[key][:, 0], got[key][:, 1]), key
+
+
+@DENSE_FORMS
+def test_dense_ragged_batch_and_bad_offsets(form):
+    """Several segments of ragged lengths in one call (chunk slots of neighbours
+    interleave in the scratch), and a segment whose offsets leave [0, N]:
+    reported through d_err, treated as empty (S = 0, T = I)."""
+    import torch
+    lens = [1, 63, 64, 65, 0, 300, 129]
+    w = wl.dense_stack(lengths=lens, n_layers=2, H=3, d=128, seed=21)
+    check(DENSE, host(gpu_scan(w, workspace=form)), oracle_scan(w), TOL_SCAN_BF16)
+    w["seg_offsets"] = np.concatenate([w["seg_offsets"][:-1], [w["seg_offsets"][-1] + 5000]])
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = gpu_scan(w, d_err=err, workspace=form)
+    torch.cuda.synchronize()
+    assert int(err.item()) == -5
+    assert torch.all(got["S"][:, -1] == 0)
+    assert torch.all(got["lam"][:, -1] == 0)
+    assert torch.equal(got["M"][:, -1], torch.eye(128, device="cuda").expand_as(got["M"][:, -1]))
 
 
 def test_bad_offsets_flag_error_without_fault():
