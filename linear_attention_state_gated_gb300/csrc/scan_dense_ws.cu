@@ -18,7 +18,8 @@
 //   W^T = K^T (A diag(beta b))^T, U^T = V^T (A diag(beta))^T  (A split bf16 hi + lo)
 //   Delta^T = U^T - X0^T W^T    (X0 and W each split hi + lo: three products)
 //   X^T    += Delta~^T K        (Delta~ = Delta diag(b_C / b), split hi + lo)
-// W and U are built by their own warps one chunk ahead of the state warps.
+// W and U are built by their own warps up to one chunk ahead of the state warps
+// (two operand buffers).
 #include "dense_common.cuh"
 #include "internal.cuh"
 #include "sm100.cuh"
@@ -74,8 +75,7 @@ constexpr int kPSmem = kPCtl + (int)sizeof(PrepCtl) + 1024;
 __global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                                const ScanArgs a, int64_t slots) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~static_cast<uintptr_t>(1023));
+    uint8_t *smem = smem_align1024(smem_raw);
     PrepCtl *ctl = reinterpret_cast<PrepCtl *>(smem + kPCtl);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int h = (int)(blockIdx.x % (unsigned)a.H);
@@ -219,10 +219,10 @@ constexpr int kState = 512;       // state warps' threads
 constexpr int kBox = kC * 128;                         // 64 channels x 64 tokens, bf16: 8 KB
 constexpr int kSK = 0, kSV = 2 * kBox, kSRec = 4 * kBox;
 constexpr int kStage = kSRec + ((kRecBytes + 1023) / 1024) * 1024;   // 50176
-constexpr int kWt = kNS * kStage;           // -W^T tiles, hi / lo (128 rows x 128 B each)
-constexpr int kAb2 = kWt + 2 * 16384;       // A diag(beta b), hi / lo (64 rows x 128 B each)
-constexpr int kAb = kAb2 + 2 * 8192;        // A diag(beta), hi / lo
-constexpr int kCtl = kAb + 2 * 8192;
+constexpr int kWt = kNS * kStage;           // -W^T tiles, two buffers x (hi, lo) (128 rows x 128 B each)
+constexpr int kAb2 = kWt + 4 * 16384;       // A diag(beta b), hi / lo (64 rows x 128 B each)
+constexpr int kAb = kAb2 + 2 * 8192;        // A diag(beta), two buffers x (hi, lo)
+constexpr int kCtl = kAb + 4 * 8192;
 static_assert(kStage % 1024 == 0 && kWt % 1024 == 0, "operand tiles 1024-byte aligned");
 
 // TMEM column map (512 allocated)
@@ -233,7 +233,8 @@ constexpr uint32_t kTw = 320;     // W^T accumulator (64 columns)
 
 struct StateCtl {
     uint64_t full[kNS], empty[kNS];
-    uint64_t aop_ready, wop_ready, w_done, wfree, d_done, x_done;
+    uint64_t aop_ready[2], wop_ready[2], wfree[2];   // per operand buffer (chunk parity)
+    uint64_t w_done, d_done, x_done;
     uint64_t drain[2];
     float redmax[16];
     uint32_t tmem;
@@ -259,8 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
     dense_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                        const ScanArgs a, int64_t slots) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~static_cast<uintptr_t>(1023));
+    uint8_t *smem = smem_align1024(smem_raw);
     StateCtl *ctl = reinterpret_cast<StateCtl *>(smem + kCtl);
     volatile int *abortp = &ctl->abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -283,10 +283,12 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
             mbar_init(&ctl->full[s], 1);
             mbar_init(&ctl->empty[s], 1);
         }
-        mbar_init(&ctl->aop_ready, kWT / 32);
-        mbar_init(&ctl->wop_ready, kWT / 32);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&ctl->aop_ready[b], kWT / 32);
+            mbar_init(&ctl->wop_ready[b], kWT / 32);
+            mbar_init(&ctl->wfree[b], 1);
+        }
         mbar_init(&ctl->w_done, 1);
-        mbar_init(&ctl->wfree, 1);
         mbar_init(&ctl->d_done, 1);
         mbar_init(&ctl->x_done, 1);
         mbar_init(&ctl->drain[0], 1);
@@ -339,9 +341,9 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
             const uint32_t par = (uint32_t)j & 1u;
             const uint8_t *st = smem + s * kStage;
             const float *rec = reinterpret_cast<const float *>(st + kSRec);
-            // the chunk is in, and the previous chunk's operand tiles are consumed
+            // the chunk is in, and the operand buffer's previous use (chunk j - 2) is consumed
             bool ok = wait_or_abort(&ctl->full[s], (uint32_t)(j / kNS) & 1u, abortp);
-            if (j > 0) ok = ok && wait_or_abort(&ctl->wfree, par ^ 1u, abortp);
+            if (j > 1) ok = ok && wait_or_abort(&ctl->wfree[par], ((uint32_t)(j >> 1) - 1u) & 1u, abortp);
             if (!bar_and(1, kWT, ok)) {
                 *abortp = 1;
                 break;
@@ -365,18 +367,19 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
                     *reinterpret_cast<uint4 *>(smem + kAb2 + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
                     *reinterpret_cast<uint4 *>(smem + kAb2 + 8192 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                     if (half) {
+                        uint8_t *ab = smem + kAb + (int)par * 16384;
 #pragma unroll
                         for (int p = 0; p < 4; ++p)
                             split_pair(av[2 * p] * rec[kRecGbeta + c * 8 + 2 * p],
                                        av[2 * p + 1] * rec[kRecGbeta + c * 8 + 2 * p + 1], hi[p], lo[p]);
-                        *reinterpret_cast<uint4 *>(smem + kAb + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                        *reinterpret_cast<uint4 *>(smem + kAb + 8192 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                        *reinterpret_cast<uint4 *>(ab + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                        *reinterpret_cast<uint4 *>(ab + 8192 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                     }
                 }
             }
             fence_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->aop_ready);
+            if (lane == 0) mbar_arrive(&ctl->aop_ready[par]);
             bar_sync(1, kWT);
             // ---- W^T = K^T (A diag(beta b))^T
             if (issuer) {
@@ -399,6 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
             // ---- -W^T -> bf16 hi / lo tiles, MN-major (row k, t contiguous, 128B swizzle)
             {
                 const int k = quarter * 32 + lane;
+                uint8_t *wtile = smem + kWt + (int)par * 32768;
                 for (int cb = 0; cb < 2; ++cb) {
                     uint32_t r[32];
                     tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + kTw + (uint32_t)(cb * 32), r);
@@ -412,15 +416,15 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
                             split_pair(-__uint_as_float(r[cc * 8 + 2 * p]), -__uint_as_float(r[cc * 8 + 2 * p + 1]),
                                        hi[p], lo[p]);
                         const int off = k * 128 + ((c ^ (k & 7)) << 4);
-                        *reinterpret_cast<uint4 *>(smem + kWt + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                        *reinterpret_cast<uint4 *>(smem + kWt + 16384 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                        *reinterpret_cast<uint4 *>(wtile + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                        *reinterpret_cast<uint4 *>(wtile + 16384 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                     }
                 }
             }
             tc_fence_before();
             fence_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->wop_ready);
+            if (lane == 0) mbar_arrive(&ctl->wop_ready[par]);
         }
         if (issuer && *abortp) {   // drain: completes once this thread's MMAs are done
             mma_commit(&ctl->drain[0]);
@@ -470,9 +474,9 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
             // ---- U^T = V^T (A diag(beta))^T into the accumulator (state half), on the
             // tensor cores while the X operand is converted below
             if (issuer && half) {
-                if (wait_or_abort(&ctl->aop_ready, par, abortp)) {
+                if (wait_or_abort(&ctl->aop_ready[par], (uint32_t)(j >> 1) & 1u, abortp)) {
                     tc_fence_after();
-                    const uint32_t vb = smem_addr(stg + kSV), ab = smem_addr(smem + kAb);
+                    const uint32_t vb = smem_addr(stg + kSV), ab = smem_addr(smem + kAb + (int)par * 16384);
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {
                         const uint64_t ad = smem_desc_sw128(vb + (uint32_t)ks * 2048u, kBox, 1024);
@@ -545,9 +549,9 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
             bar_sync(2, kState);
             // ---- Delta^T = U^T - X0^T W^T (three-term split)
             if (issuer) {
-                if (wait_or_abort(&ctl->wop_ready, par, abortp)) {
+                if (wait_or_abort(&ctl->wop_ready[par], (uint32_t)(j >> 1) & 1u, abortp)) {
                     tc_fence_after();
-                    const uint32_t wtile = smem_addr(smem + kWt);
+                    const uint32_t wtile = smem_addr(smem + kWt + (int)par * 32768);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
                         const uint64_t bh = smem_desc_sw128(wtile + (uint32_t)ks * 2048u, 16384, 1024);
@@ -559,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
                     }
                 }
                 mma_commit(&ctl->d_done);
-                mma_commit(&ctl->wfree);
+                mma_commit(&ctl->wfree[par]);
             }
             // ---- Delta~^T = fD Delta^T diag(b_C / b) -> bf16 hi / lo in place
             if (!bar_and(2, kState, wait_or_abort(&ctl->d_done, par, abortp))) {

@@ -18,6 +18,13 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p) {
 
 // ------------------------------------------------------------------ mbarrier
 
+// The dynamic shared-memory window aligned up to 1024 bytes.  Offsetting the
+// __shared__ array itself (not an integer round trip) keeps the pointer in the
+// shared state space, so accesses through it compile to shared loads / stores.
+__device__ __forceinline__ uint8_t *smem_align1024(uint8_t *raw) {
+    return raw + ((1024u - (smem_addr(raw) & 1023u)) & 1023u);
+}
+
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
 }
