@@ -136,6 +136,32 @@ int hypic_segment_scan_ws(int fam, int in_dtype, int n_layers, int n_seg,
                           void *cuda_stream);
 
 /*
+ * hypic_segment_scan_static -- the two-pass dense scan of hypic_segment_scan_ws
+ * with its scratch taken from a fixed 64 MiB device array inside the library
+ * instead of a caller workspace; the call allocates nothing.  The HYPIC pages
+ * have no counterpart of this entry point.  It is meant for callers that cannot
+ * allocate device memory at call time (an engine that gave all free memory to
+ * its KV-cache pool at start-up; a host path that must not enter the allocator,
+ * which can synchronise the device).
+ *   Arguments as hypic_segment_scan without q / o_out.  Only fam = HYPIC_DENSE,
+ *   in_dtype = HYPIC_BF16, d_k = d_v = 128 is served; other inputs, or a problem
+ *   whose records need more than the 64 MiB (hypic_segment_scan_workspace_bytes
+ *   gives the need; 64 MiB hold 3905 records of 17184 bytes), return
+ *   HYPIC_EUNSUPPORTED and launch nothing.
+ *   The scratch's contents never need to start at zero.  It is one array per
+ *   device for the whole process: two calls in flight at the same time (other
+ *   streams or host threads) race on it, so callers serialise them.
+ *   The first call on each device looks up the array's address
+ *   (cudaGetSymbolAddress, with that device current) and caches it; a caller
+ *   that will later capture its stream makes one call before capturing.
+ */
+int hypic_segment_scan_static(int fam, int in_dtype, int n_layers, int n_seg,
+                              int64_t total_tokens, int n_heads, int d_k, int d_v,
+                              const int64_t *seg_offsets, const void *k, const void *v,
+                              const float *alpha, const float *beta, float *lam_out,
+                              float *M_out, float *S_out, int *d_err, void *cuda_stream);
+
+/*
  * hypic_compose -- S = T_C S_prev + S_C for n items x H heads, with
  * T_C = exp(lambda) M.  (xix.ai/fr, linear-layer paragraph:
  * S(C1.C2) = T(C2) S(C1) + S(C2); left-multiplication by the cached T then an

@@ -32,7 +32,7 @@ BF16, F32 = 0, 1
 STATUS = {0: "HYPIC_OK", -1: "HYPIC_EINVAL", -2: "HYPIC_EUNSUPPORTED", -3: "HYPIC_EALIGN",
           -4: "HYPIC_ECUDA", -5: "HYPIC_EINDEX", -6: "HYPIC_ETIMEOUT"}
 
-__all__ = ["segment_scan", "segment_scan_workspace_bytes", "compose", "compose_chain", "status_string", "library", "use_library",
+__all__ = ["segment_scan", "segment_scan_workspace_bytes", "segment_scan_static", "compose", "compose_chain", "status_string", "library", "use_library",
            "HypicError", "SCALAR", "DIAG", "DENSE"]
 
 
@@ -52,6 +52,8 @@ SIGNATURES = {
                                   _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "hypic_segment_scan_ws": (_I32, [_I32, _I32, _I32, _I32, _I64, _I32, _I32, _I32,
                                      _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _P, _P]),
+    "hypic_segment_scan_static": (_I32, [_I32, _I32, _I32, _I32, _I64, _I32, _I32, _I32,
+                                         _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "hypic_segment_scan_workspace_bytes": (_I64, [_I32, _I32, _I32, _I32, _I64, _I32, _I32, _I32, _I32]),
     "hypic_compose": (_I32, [_I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "hypic_compose_chain": (_I32, [_I32, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _I32,
@@ -201,6 +203,27 @@ def segment_scan(family, k, v, alpha, seg_offsets, beta=None, q=None, want_o=Fal
                                          0 if workspace is None else workspace.numel(),
                                          _ptr(d_err), _stream(stream))
     _check("hypic_segment_scan_ws", st)
+    return out
+
+
+def segment_scan_static(k, v, alpha, seg_offsets, out, beta=None, d_err=None, stream=None):
+    """Dense (gated delta rule) scan through hypic_segment_scan_static: the
+    library's fixed device scratch, no allocation anywhere in the call.  ``out``
+    must hold caller-allocated ``lam`` [Lyr,n_seg,H], ``M`` and ``S``
+    [Lyr,n_seg,H,128,128] fp32 tensors; k, v bf16 with d_k = d_v = 128."""
+    k = _dev(k, "k", torch.bfloat16)
+    v = _dev(v, "v", torch.bfloat16)
+    alpha = _dev(alpha, "alpha", torch.float32)
+    beta = _dev(beta, "beta", torch.float32, allow_none=True)
+    seg_offsets = _dev(seg_offsets, "seg_offsets", torch.int64)
+    lam = _dev(out.get("lam"), "out['lam']", torch.float32)
+    M = _dev(out.get("M"), "out['M']", torch.float32)
+    S = _dev(out.get("S"), "out['S']", torch.float32)
+    Lyr, N, H, dk = k.shape
+    st = library().hypic_segment_scan_static(
+        DENSE, BF16, Lyr, seg_offsets.numel() - 1, N, H, dk, v.shape[-1], _ptr(seg_offsets), _ptr(k),
+        _ptr(v), _ptr(alpha), _ptr(beta), _ptr(lam), _ptr(M), _ptr(S), _ptr(d_err), _stream(stream))
+    _check("hypic_segment_scan_static", st)
     return out
 
 

@@ -186,6 +186,24 @@ int hypic_segment_scan_ws(int fam, int in_dtype, int n_layers, int n_seg, int64_
     return from_cuda(hypic::launch_scan_recurrent(a, s));
 }
 
+int hypic_segment_scan_static(int fam, int in_dtype, int n_layers, int n_seg, int64_t total_tokens,
+                              int n_heads, int d_k, int d_v, const int64_t *seg_offsets, const void *k,
+                              const void *v, const float *alpha, const float *beta, float *lam_out,
+                              float *M_out, float *S_out, int *d_err, void *cuda_stream) {
+    hypic::ScanArgs a;
+    bool none;
+    const int rc = scan_args(fam, in_dtype, n_layers, n_seg, total_tokens, n_heads, d_k, d_v, seg_offsets,
+                             nullptr, k, v, alpha, beta, lam_out, M_out, S_out, nullptr, d_err, a, none);
+    if (rc != HYPIC_OK || none) return rc;
+    if (!hypic::scan_dense_ws_shape(a)) return HYPIC_EUNSUPPORTED;
+    if (hypic::scan_dense_ws_bytes(a) > hypic::static_scratch_bytes()) return HYPIC_EUNSUPPORTED;
+    if (!hypic::scan_dense_ws_supported(a)) return HYPIC_ECUDA;
+    void *scratch = nullptr;
+    if (hypic::static_scratch(&scratch) != cudaSuccess || !scratch) return HYPIC_ECUDA;
+    a.ws = static_cast<float *>(scratch);
+    return from_cuda(hypic::launch_scan_dense_ws(a, static_cast<cudaStream_t>(cuda_stream)));
+}
+
 int hypic_compose(int fam, int n, int n_heads, int d_k, int d_v, const float *lam, const float *M,
                   const float *S_prev, const float *S_C, float *S_out, const float *lam_prev,
                   const float *M_prev, float *lam_out, float *M_out, void *cuda_stream) {

@@ -66,6 +66,8 @@ bool scan_dense_ws_shape(const ScanArgs &a);       // sizes / options the two-pa
 bool scan_dense_ws_supported(const ScanArgs &a);   // ... and the runtime can encode its tensor maps
 int64_t scan_dense_ws_bytes(const ScanArgs &a);
 cudaError_t launch_scan_dense_ws(const ScanArgs &a, cudaStream_t s);
+int64_t static_scratch_bytes();            // size of the fixed scratch of hypic_segment_scan_static
+cudaError_t static_scratch(void **p);      // its address on the current device
 
 // Dense chained composition on tcgen05 (3 x TF32), d_k = d_v = 128.
 bool chain_dense_tc_supported(const ChainArgs &a);

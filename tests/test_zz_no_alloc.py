@@ -1,0 +1,60 @@
+"""hypic_segment_scan_static: the two-pass dense scan out of the library's fixed
+device scratch (no allocation inside the call).  Its results must equal the
+caller-workspace form, hypic_segment_scan_ws, bit for bit, on two calls in a
+row (the second call finds the first one's records in the scratch); a problem
+larger than the scratch is refused before any launch."""
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+
+def _inputs(lengths, n_layers, H, seed):
+    import torch
+    from linear_attention_state_gated_gb300 import workloads as wl
+    w = wl.dense_stack(lengths=lengths, n_layers=n_layers, H=H, d=128, seed=seed)
+    dev = torch.device("cuda")
+    return (torch.from_numpy(w["k"]).to(torch.bfloat16).to(dev),
+            torch.from_numpy(w["v"]).to(torch.bfloat16).to(dev),
+            torch.from_numpy(w["alpha"]).to(dev), torch.from_numpy(w["beta"]).to(dev),
+            torch.from_numpy(w["seg_offsets"]).to(dev))
+
+
+def _nan_out(Lyr, n_seg, H):
+    import torch
+    f = dict(dtype=torch.float32, device="cuda")
+    return {"lam": torch.full((Lyr, n_seg, H), float("nan"), **f),
+            "M": torch.full((Lyr, n_seg, H, 128, 128), float("nan"), **f),
+            "S": torch.full((Lyr, n_seg, H, 128, 128), float("nan"), **f)}
+
+
+def test_static_scratch_equals_workspace_form_on_two_calls_in_a_row():
+    import torch
+    import linear_attention_state_gated_gb300 as hy
+    lengths, Lyr, H = [2048, 700, 129], 2, 4
+    k, v, a, b, offs = _inputs(lengths, Lyr, H, seed=31)
+    need = hy.segment_scan_workspace_bytes("dense", torch.bfloat16, Lyr, len(lengths), k.shape[1], H, 128, 128)
+    assert 0 < need <= 64 << 20
+    ref = hy.segment_scan("dense", k, v, a, offs, beta=b, workspace="auto")
+    outs = []
+    for _ in range(2):
+        out = _nan_out(Lyr, len(lengths), H)
+        hy.segment_scan_static(k, v, a, offs, out, beta=b)
+        outs.append(out)
+    torch.cuda.synchronize()
+    for out in outs:
+        for key in ("lam", "M", "S"):
+            assert torch.equal(out[key], ref[key]), key
+
+
+def test_static_scratch_refuses_a_problem_beyond_its_size():
+    import torch
+    import linear_attention_state_gated_gb300 as hy
+    Lyr, H, L = 1, 32, 8192           # 32 x 129 records of 17184 bytes: 70.9 MB > 64 MiB
+    k, v, a, b, offs = _inputs([L], Lyr, H, seed=32)
+    out = _nan_out(Lyr, 1, H)
+    with pytest.raises(hy.HypicError) as e:
+        hy.segment_scan_static(k, v, a, offs, out, beta=b)
+    assert e.value.status == -2
+    torch.cuda.synchronize()
+    assert torch.isnan(out["S"]).all() and torch.isnan(out["lam"]).all()
