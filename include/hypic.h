@@ -104,9 +104,10 @@ int hypic_segment_scan(int fam, int in_dtype, int n_layers, int n_seg,
  * hypic_segment_scan_workspace_bytes -- bytes of device scratch that
  * hypic_segment_scan_ws needs for these sizes, or 0 when that call uses none
  * (then its workspace may be NULL).  A negative hypic_status on bad counts.
- * Today the scratch is used by the dense family with bf16 inputs, d_k = d_v =
- * 128 and no o_t: one 17184-byte record per (layer, head, 64-token chunk slot),
- * n_layers * n_heads * (n_seg + total_tokens / 64) records.
+ * Today the scratch is used by the dense family with bf16 inputs and d_k = d_v
+ * = 128: one record per (layer, head, 64-token chunk slot) of 17184 bytes
+ * (33808 bytes with o_t), n_layers * n_heads * (n_seg + total_tokens / 64)
+ * records.
  */
 int64_t hypic_segment_scan_workspace_bytes(int fam, int in_dtype, int n_layers, int n_seg,
                                            int64_t total_tokens, int n_heads, int d_k, int d_v,

@@ -1,5 +1,6 @@
 // scan_dense_ws.cu -- gated delta rule segment scan in two passes over a
-// caller-owned workspace: a chunk-parallel preparation pass and the state pass.
+// caller-owned workspace: a chunk-parallel preparation pass and the state pass,
+// optionally with the per-token outputs o_t = S_t^T q_t.
 //
 // Chunked WY/UT form of S_t = alpha_t (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T
 // (C = 64 tokens per chunk; b_t = in-chunk cumulative decay, b_C its total):
@@ -9,17 +10,22 @@
 //   Delta = [0 | U] - W X_0,   X <- b_C X_0 + K^T diag(b_C / b) Delta.
 // (Within a chunk delta_t = beta_t (v_t - alpha_t S_{t-1}^T k_t) satisfies
 // (I + L) Delta = diag(beta) V - diag(beta b) K S_0.)
+// Outputs: S_t = b_t S_0 + sum_{s<=t} (b_t / b_s) k_s delta_s^T, so
+//   o_t = b_t S_0^T q_t + sum_{s<=t} (b_t / b_s)(q_t.k_s) delta_s
+//       = b_t (O1)_t + (O2)_t,  O1 = S_0^T Q^T,  O2 = Delta^T Gq^T,
+//   Gq[t][s] = [s <= t] (b_t / b_s) q_t.k_s.
 //
-// Pass 1 (dense_prep_kernel) depends only on a chunk's own keys and gates, so
-// every chunk of every (layer, segment, head) runs in parallel: gates, the Gram
-// matrix on tcgen05, L, and the blocked inverse A, written to one workspace
-// record per chunk.  Pass 2 (dense_state_kernel) walks the chunks of a chain in
-// order with X^T in TMEM (two CTAs per chain: transition half, state half):
+// Pass 1 (dense_prep_kernel) depends only on a chunk's own keys, queries and
+// gates, so every chunk of every (layer, segment, head) runs in parallel: gates,
+// the Gram matrix [K; Q] K^T on tcgen05, L, Gq, and the blocked inverse A,
+// written to one workspace record per chunk.  Pass 2 (dense_state_kernel) walks
+// the chunks of a chain in order with X^T in TMEM (two CTAs per chain:
+// transition half, state half):
 //   W^T = K^T (A diag(beta b))^T, U^T = V^T (A diag(beta))^T  (A split bf16 hi + lo)
 //   Delta^T = U^T - X0^T W^T    (X0 and W each split hi + lo: three products)
 //   X^T    += Delta~^T K        (Delta~ = Delta diag(b_C / b), split hi + lo)
-// W and U are built by their own warps up to one chunk ahead of the state warps
-// (two operand buffers).
+//   O1^T = X0^T Q^T (X0 hi + lo),  O2^T = Delta^T Gq^T (three products)
+// W and U are built by their own warps ahead of the state warps.
 #include "dense_common.cuh"
 #include "internal.cuh"
 #include "sm100.cuh"
@@ -35,35 +41,45 @@ using dense::split_pair;
 using dense::wait_or_abort;
 
 constexpr int kD = 128;
+constexpr int kBox = kC * 128;   // 64 channels x 64 tokens, bf16: 8 KB
 
 // ---------------------------------------------------------------- workspace record
 // One record per (layer, head, chunk slot), floats:
-//   [0, 4096)      A = (I + L)^-1, row t at 64 t; the 16-byte group g of row t is
-//                  stored at group position g ^ (t & 15) (conflict-free row reads)
-//   4096 + t       b_C / b_t
-//   4160 + t       beta_t b_t
-//   4224 + t       beta_t
-//   4288, 4289     log b_C, b_C
+//   [0, 4096)        A = (I + L)^-1, row t at 64 t; the 16-byte group g of row t is
+//                    stored at group position g ^ (t & 15) (conflict-free row reads)
+//   [4096, 8192)     with o_t only: Gq as bf16 hi / lo operand tiles (row t, s
+//                    contiguous, 128-byte swizzle), 8 KB each
+//   G + t            b_C / b_t        (G = 4096, or 8192 with o_t)
+//   G + 64 + t       beta_t b_t
+//   G + 128 + t      beta_t
+//   G + 192, G + 193 log b_C, b_C
+//   G + 196 + t      with o_t only: b_t
 // Chunk j of segment s (tokens from t0) uses slot s + floor(t0 / 64) + j, so the
 // slots of different segments never collide and a (layer, head) needs at most
 // n_seg + floor(N / 64) of them.
-constexpr int kRecA = 0, kRecGw = 4096, kRecGbb = 4160, kRecGbeta = 4224, kRecLC = 4288, kRecBC = 4289;
-constexpr int kRecFloats = 4296;                  // padded to a multiple of 4 floats
-constexpr int kRecBytes = kRecFloats * 4;         // 17184
+template <bool O>
+struct Rec {
+    static constexpr int A = 0, Gq = 4096;
+    static constexpr int G = O ? 8192 : 4096;
+    static constexpr int Gw = G, Gbb = G + 64, Gbeta = G + 128, LC = G + 192, BC = G + 193, B = G + 196;
+    static constexpr int Floats = O ? G + 260 : G + 200;   // multiples of 4 floats
+    static constexpr int Bytes = Floats * 4;               // 17184 / 33808
+};
 
 __host__ __device__ inline int64_t n_slots(int64_t N, int n_seg) { return (int64_t)n_seg + N / kC; }
 
 // ================================================================ pass 1: preparation
 
 constexpr int kPThreads = 128;
-// shared memory (from the 1024-aligned base): K boxes 0 / 1 and 8 KB the padded
-// Gram rows read (the fp32 L tile overlays all of it once the Gram is done),
-// the fp32 A tile, temporaries, control.
-constexpr int kPK = 0;
-constexpr int kPAw = 24576;
+// shared memory (from the 1024-aligned base): the Gram's A operand rows, keys
+// 0..63 then queries 64..127 (without o_t the query boxes are simply not
+// loaded: those rows of the Gram are unused), per 64-channel box; the fp32 L
+// tile overlays them once the Gram is done; the fp32 A tile, temporaries, control.
+constexpr int kPK = 0;           // K0 | Q0 | K1 | Q1
+constexpr int kPAw = 4 * kBox;
 constexpr int kPTw = kPAw + kC * kLd * 4;
 constexpr int kPCtl = kPTw + 3 * 256 * 4;
-static_assert(kC * kLd * 4 <= 24576, "L overlays the key tile");
+static_assert(kC * kLd * 4 <= 4 * kBox, "L overlays the key / query tile");
 
 struct PrepCtl {
     uint64_t full, mma;
@@ -72,8 +88,11 @@ struct PrepCtl {
 };
 constexpr int kPSmem = kPCtl + (int)sizeof(PrepCtl) + 1024;
 
+template <bool O>
 __global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_constant__ CUtensorMap tm_k,
+                                                               const __grid_constant__ CUtensorMap tm_q,
                                                                const ScanArgs a, int64_t slots) {
+    using R = Rec<O>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_align1024(smem_raw);
     PrepCtl *ctl = reinterpret_cast<PrepCtl *>(smem + kPCtl);
@@ -95,16 +114,20 @@ __global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_cons
     const int64_t j = slot - (seg + t0 / kC);
     if (j < 0 || j * kC >= t1 - t0) return;            // a slot no chunk uses
     const int64_t c0 = t0 + j * kC;                     // first token of the chunk
-    float *rec = a.ws + ((int64_t)l * a.H + h) * slots * kRecFloats + slot * kRecFloats;
+    float *rec = a.ws + ((int64_t)l * a.H + h) * slots * R::Floats + slot * R::Floats;
 
     if (tid == 0) {
         mbar_init(&ctl->full, 1);
         mbar_init(&ctl->mma, 1);
         mbar_fence_init();
-        mbar_expect_tx(&ctl->full, 2 * kC * 128);
+        mbar_expect_tx(&ctl->full, (O ? 4 : 2) * kBox);
         const int row = (int)((int64_t)l * a.N + c0);
         tma_load_3d(smem + kPK, &tm_k, &ctl->full, 0, h, row);
-        tma_load_3d(smem + kPK + 8192, &tm_k, &ctl->full, 64, h, row);
+        tma_load_3d(smem + kPK + 2 * kBox, &tm_k, &ctl->full, 64, h, row);
+        if (O) {
+            tma_load_3d(smem + kPK + kBox, &tm_q, &ctl->full, 0, h, row);
+            tma_load_3d(smem + kPK + 3 * kBox, &tm_q, &ctl->full, 64, h, row);
+        }
     }
     if (warp == 0) tmem_alloc(&ctl->tmem, 64);
     tc_fence_before();
@@ -113,7 +136,7 @@ __global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_cons
     const uint32_t tmem = ctl->tmem;
     bool ok = true;
 
-    // ---- gates (warp 0): Lambda, b_C / b, beta b, beta, log b_C, b_C
+    // ---- gates (warp 0): Lambda, b_C / b, beta b, beta, log b_C, b_C (, b)
     if (warp == 0) {
         float lg[2], pb[2], inc[2];
 #pragma unroll
@@ -139,17 +162,19 @@ __global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_cons
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
             const int t = lane + 32 * q;
+            const float bt = expf(inc[q]);
             ctl->gl[t] = inc[q];
             ctl->gbeta[t] = pb[q];
-            rec[kRecGw + t] = expf(total - inc[q]);
-            rec[kRecGbb + t] = pb[q] * expf(inc[q]);
-            rec[kRecGbeta + t] = pb[q];
+            rec[R::Gw + t] = expf(total - inc[q]);
+            rec[R::Gbb + t] = pb[q] * bt;
+            rec[R::Gbeta + t] = pb[q];
+            if (O) rec[R::B + t] = bt;
         }
         if (lane == 0) {
-            rec[kRecLC] = total;
-            rec[kRecBC] = expf(total);
+            rec[R::LC] = total;
+            rec[R::BC] = expf(total);
         }
-        // Gram G = K K^T: M = 128 rows of which 64..127 read past the keys and are unused
+        // Gram [K; Q] K^T: lanes 0..63 K K^T, lanes 64..127 Q K^T (unused without o_t)
         if (lane == 0) {
             ok = mbar_wait(&ctl->full, 0);
             if (ok) {
@@ -158,7 +183,7 @@ __global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_cons
                 const uint32_t kb = smem_addr(smem + kPK);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t off = (uint32_t)(ks >> 2) * 8192u + (uint32_t)(ks & 3) * 32u;
+                    const uint32_t off = (uint32_t)(ks >> 2) * (2u * kBox) + (uint32_t)(ks & 3) * 32u;
                     const uint64_t d = smem_desc_sw128(kb + off, 0, 1024);
                     mma_f16(tmem, d, d, id_gram, ks > 0);
                 }
@@ -172,10 +197,11 @@ __global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_cons
     float *Aw = reinterpret_cast<float *>(smem + kPAw);
     float *Tw = reinterpret_cast<float *>(smem + kPTw);
     if (ok) {
-        // ---- L[t][s] = beta_t exp(Lambda_t - Lambda_s) G[t][s] for s < t (warps 0, 1: rows 0..63)
+        const int t = (warp & 1) * 32 + lane;   // token row 0..63 of this thread
+        const float lt = ctl->gl[t];
         if (warp < 2) {
-            const int t = warp * 32 + lane;
-            const float lt = ctl->gl[t], bt = ctl->gbeta[t];
+            // ---- L[t][s] = beta_t exp(Lambda_t - Lambda_s) G[t][s] for s < t
+            const float bt = ctl->gbeta[t];
             for (int cb = 0; cb < 2; ++cb) {
                 uint32_t r[32];
                 tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(cb * 32), r);
@@ -186,6 +212,32 @@ __global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_cons
                     Lw[t * kLd + sc] = sc < t ? bt * __expf(lt - ctl->gl[sc]) * __uint_as_float(r[i]) : 0.f;
                 }
             }
+        } else if (O) {
+            // ---- Gq[t][s] = [s <= t] exp(Lambda_t - Lambda_s) (q_t.k_s) -> bf16 hi / lo tiles
+            uint8_t *gq = reinterpret_cast<uint8_t *>(rec + R::Gq);
+            for (int cb = 0; cb < 2; ++cb) {
+                uint32_t r[32];
+                tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(cb * 32), r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const int c = cb * 4 + cc;
+                    uint32_t hv[4], lv[4];
+#pragma unroll
+                    for (int p = 0; p < 4; ++p) {
+                        float x[2];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int sc = c * 8 + 2 * p + e;
+                            x[e] = sc <= t ? __expf(lt - ctl->gl[sc]) * __uint_as_float(r[cc * 8 + 2 * p + e]) : 0.f;
+                        }
+                        split_pair(x[0], x[1], hv[p], lv[p]);
+                    }
+                    const int off = t * 128 + ((c ^ (t & 7)) << 4);
+                    *reinterpret_cast<uint4 *>(gq + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                    *reinterpret_cast<uint4 *>(gq + 8192 + off) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+                }
+            }
         }
         __syncthreads();
         dense::tri_inverse<kPThreads, 1>(Lw, Aw, Tw, tid);
@@ -193,9 +245,9 @@ __global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_cons
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int f = tid + kPThreads * i;   // 0 .. 1023
-            const int t = f >> 4, g = f & 15;
-            const float4 v = *reinterpret_cast<const float4 *>(Aw + t * kLd + g * 4);
-            *reinterpret_cast<float4 *>(rec + kRecA + t * 64 + ((g ^ (t & 15)) << 2)) = v;
+            const int tt = f >> 4, g = f & 15;
+            const float4 v = *reinterpret_cast<const float4 *>(Aw + tt * kLd + g * 4);
+            *reinterpret_cast<float4 *>(rec + R::A + tt * 64 + ((g ^ (tt & 15)) << 2)) = v;
         }
     } else if (tid == 0 && a.d_err) {
         atomicExch(a.d_err, (int)HYPIC_ETIMEOUT);
@@ -215,33 +267,42 @@ constexpr int kThreads = 672;     // 21 warps: 0 TMA, 1-4 W/U operands, 5-20 sta
 constexpr int kWT = 128;          // W warps' threads
 constexpr int kState = 512;       // state warps' threads
 
-// stage: K (two 64-channel boxes), V (state half), the chunk's record
-constexpr int kBox = kC * 128;                         // 64 channels x 64 tokens, bf16: 8 KB
-constexpr int kSK = 0, kSV = 2 * kBox, kSRec = 4 * kBox;
-constexpr int kStage = kSRec + ((kRecBytes + 1023) / 1024) * 1024;   // 50176
-constexpr int kWt = kNS * kStage;           // -W^T tiles, two buffers x (hi, lo) (128 rows x 128 B each)
-constexpr int kAb2 = kWt + 4 * 16384;       // A diag(beta b), hi / lo (64 rows x 128 B each)
-constexpr int kAb = kAb2 + 2 * 8192;        // A diag(beta), two buffers x (hi, lo)
-constexpr int kCtl = kAb + 4 * 8192;
-static_assert(kStage % 1024 == 0 && kWt % 1024 == 0, "operand tiles 1024-byte aligned");
+// stage: K (two 64-channel boxes), V (state half), Q (o_t), the chunk's record;
+// then the -W^T and A diag(beta) operand tiles (two buffers without o_t, one
+// with).  A diag(beta b) is written over the record's A once it is read.
+template <bool O>
+struct Smem {
+    static constexpr int K = 0, V = 2 * kBox, Q = 4 * kBox, Rec = (O ? 6 : 4) * kBox;
+    static constexpr int Stage = Rec + ((hypic::Rec<O>::Bytes + 1023) / 1024) * 1024;
+    static constexpr int NB = O ? 1 : 2;               // operand buffers
+    static constexpr int Wt = kNS * Stage;             // -W^T, per buffer hi / lo (128 rows x 128 B each)
+    static constexpr int Ab = Wt + NB * 32768;         // A diag(beta), per buffer hi / lo (64 x 128 B each)
+    static constexpr int Ctl = Ab + NB * 16384;
+};
 
 // TMEM column map (512 allocated)
 constexpr uint32_t kTx = 0;       // X^T half, fp32 (128 columns)
-constexpr uint32_t kTxop = 128;   // X0^T operand: hi [128, 192), lo [192, 256), bf16 pairs
+constexpr uint32_t kTxop = 128;   // X0^T operand: hi [128, 192), lo [192, 256), bf16 pairs;
+                                  // with o_t then Delta^T hi / lo (O2 operand) in [128, 192)
 constexpr uint32_t kTacc = 256;   // U^T - X0^T W^T, then Delta~^T operand in place (64)
 constexpr uint32_t kTw = 320;     // W^T accumulator (64 columns)
+constexpr uint32_t kTo1 = 384;    // O1^T accumulator (64 columns, o_t)
+constexpr uint32_t kTo2 = 448;    // O2^T accumulator (64 columns, o_t)
 
 struct StateCtl {
     uint64_t full[kNS], empty[kNS];
-    uint64_t aop_ready[2], wop_ready[2], wfree[2];   // per operand buffer (chunk parity)
+    uint64_t aop_ready[2], wop_ready[2], wfree[2];   // per operand buffer
     uint64_t w_done, d_done, x_done;
     uint64_t drain[2];
     float redmax[16];
+    float bo[kC];          // b_t of the chunk whose o_t is pending
     uint32_t tmem;
     int abort;
 };
-constexpr int kSmem = kCtl + (int)sizeof(StateCtl) + 1024;
-static_assert(kSmem <= 232448, "fits in one SM's shared memory");
+template <bool O>
+constexpr int state_smem() { return Smem<O>::Ctl + (int)sizeof(StateCtl) + 1024; }
+static_assert(state_smem<false>() <= 232448 && state_smem<true>() <= 232448, "fits in one SM's shared memory");
+static_assert(Smem<true>::Stage % 1024 == 0 && Smem<false>::Stage % 1024 == 0, "operand tiles 1024-byte aligned");
 
 // max over the 16 state warps (named barrier 2)
 __device__ __forceinline__ float state_max(float mx, StateCtl *ctl, int sw, int lane) {
@@ -256,12 +317,34 @@ __device__ __forceinline__ float state_max(float mx, StateCtl *ctl, int sw, int 
     return mx;
 }
 
+// o_t = b_t O1 + O2 for this thread's 16 tokens (column group cg) of one chunk,
+// whose first token is row `crow` of [n_layers * N]; bf16 out
+__device__ __forceinline__ void store_o(const ScanArgs &a, int h, uint32_t to1, uint32_t to2, const float *b,
+                                        int cg, int m, int64_t crow, int nvalid) {
+    uint32_t r1[16], r2[16];
+    tmem_ld16(to1, r1);
+    tmem_ld16(to2, r2);
+    tmem_wait_ld();
+    __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.o_out);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int t = cg * 16 + i;
+        if (t < nvalid) {
+            const float val = fmaf(b[t], __uint_as_float(r1[i]), __uint_as_float(r2[i]));
+            o[((crow + t) * a.H + h) * kD + m] = __float2bfloat16_rn(val);
+        }
+    }
+}
+
+template <bool O>
 __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers per thread
     dense_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                       const ScanArgs a, int64_t slots) {
+                       const __grid_constant__ CUtensorMap tm_q, const ScanArgs a, int64_t slots) {
+    using R = Rec<O>;
+    using SM = Smem<O>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_align1024(smem_raw);
-    StateCtl *ctl = reinterpret_cast<StateCtl *>(smem + kCtl);
+    StateCtl *ctl = reinterpret_cast<StateCtl *>(smem + SM::Ctl);
     volatile int *abortp = &ctl->abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -275,7 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
     if (bad) t0 = t1 = 0;
     const int nc = (int)((t1 - t0 + kC - 1) / kC);
     const int64_t row0 = (int64_t)l * a.N + t0;
-    const float *recs = a.ws + (((int64_t)l * a.H + h) * slots + seg + t0 / kC) * kRecFloats;
+    const float *recs = a.ws + (((int64_t)l * a.H + h) * slots + seg + t0 / kC) * R::Floats;
+    const bool with_o = O && half == 1;   // o_t comes from the state half
 
     if (threadIdx.x == 0) {
         if (bad) flag_index_error(a.d_err);
@@ -297,6 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
         mbar_fence_init();
         tma_prefetch(&tm_k);
         if (half) tma_prefetch(&tm_v);
+        if (with_o) tma_prefetch(&tm_q);
     }
     if (warp == 0) tmem_alloc(&ctl->tmem, 512);
     tc_fence_before();
@@ -304,9 +389,10 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
     tc_fence_after();
     const uint32_t tmem = ctl->tmem;
 
-    constexpr uint32_t id_wu = idesc_bf16_f32(128, 64, true, false);   // K^T / V^T (MN-major) x A tiles
-    constexpr uint32_t id_d = idesc_bf16_f32(128, 64, false, true);    // X0^T (TMEM) x W^T (MN-major)
-    constexpr uint32_t id_x = idesc_bf16_f32(128, 128, false, true);   // Delta~^T (TMEM) x K (MN-major)
+    constexpr uint32_t id_wu = idesc_bf16_f32(128, 64, true, false);    // K^T / V^T (MN-major) x A tiles
+    constexpr uint32_t id_d = idesc_bf16_f32(128, 64, false, true);     // X0^T (TMEM) x W^T (MN-major)
+    constexpr uint32_t id_x = idesc_bf16_f32(128, 128, false, true);    // Delta~^T (TMEM) x K (MN-major)
+    constexpr uint32_t id_o = idesc_bf16_f32(128, 64, false, false);    // TMEM x Q / Gq (K-major)
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -315,16 +401,21 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
             for (int j = 0; j < nc; ++j) {
                 const int s = j % kNS;
                 if (!wait_or_abort(&ctl->empty[s], ((uint32_t)(j / kNS) & 1u) ^ 1u, abortp)) break;
-                uint8_t *st = smem + s * kStage;
+                uint8_t *st = smem + s * SM::Stage;
                 const int row = (int)(row0 + (int64_t)j * kC);
-                mbar_expect_tx(&ctl->full[s], (uint32_t)((half ? 4 : 2) * kBox + kRecBytes));
-                tma_load_3d(st + kSK, &tm_k, &ctl->full[s], 0, h, row);
-                tma_load_3d(st + kSK + kBox, &tm_k, &ctl->full[s], 64, h, row);
+                mbar_expect_tx(&ctl->full[s],
+                               (uint32_t)((2 + (half ? 2 : 0) + (with_o ? 2 : 0)) * kBox + R::Bytes));
+                tma_load_3d(st + SM::K, &tm_k, &ctl->full[s], 0, h, row);
+                tma_load_3d(st + SM::K + kBox, &tm_k, &ctl->full[s], 64, h, row);
                 if (half) {   // V only feeds the state half
-                    tma_load_3d(st + kSV, &tm_v, &ctl->full[s], 0, h, row);
-                    tma_load_3d(st + kSV + kBox, &tm_v, &ctl->full[s], 64, h, row);
+                    tma_load_3d(st + SM::V, &tm_v, &ctl->full[s], 0, h, row);
+                    tma_load_3d(st + SM::V + kBox, &tm_v, &ctl->full[s], 64, h, row);
                 }
-                bulk_load(st + kSRec, recs + (int64_t)j * kRecFloats, (uint32_t)kRecBytes, &ctl->full[s]);
+                if (with_o) {
+                    tma_load_3d(st + SM::Q, &tm_q, &ctl->full[s], 0, h, row);
+                    tma_load_3d(st + SM::Q + kBox, &tm_q, &ctl->full[s], 64, h, row);
+                }
+                bulk_load(st + SM::Rec, recs + (int64_t)j * R::Floats, (uint32_t)R::Bytes, &ctl->full[s]);
                 issued = j + 1;
             }
             if (*abortp)
@@ -338,40 +429,51 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
         const int quarter = warp & 3;
         for (int j = 0; j < nc; ++j) {
             const int s = j % kNS;
-            const uint32_t par = (uint32_t)j & 1u;
-            const uint8_t *st = smem + s * kStage;
-            const float *rec = reinterpret_cast<const float *>(st + kSRec);
-            // the chunk is in, and the operand buffer's previous use (chunk j - 2) is consumed
+            const int b = j % SM::NB;
+            const uint32_t use = (uint32_t)(j / SM::NB);
+            uint8_t *st = smem + s * SM::Stage;
+            const float *rec = reinterpret_cast<const float *>(st + SM::Rec);
+            // the chunk is in, and the operand buffer's previous use is consumed
             bool ok = wait_or_abort(&ctl->full[s], (uint32_t)(j / kNS) & 1u, abortp);
-            if (j > 1) ok = ok && wait_or_abort(&ctl->wfree[par], ((uint32_t)(j >> 1) - 1u) & 1u, abortp);
+            if (j >= SM::NB) ok = ok && wait_or_abort(&ctl->wfree[b], (use - 1u) & 1u, abortp);
             if (!bar_and(1, kWT, ok)) {
                 *abortp = 1;
                 break;
             }
-            // ---- A diag(beta b) and A diag(beta) -> bf16 hi / lo tiles (row t, s contiguous, 128B swizzle)
+            // ---- A diag(beta b) (over the record's A) and A diag(beta) -> bf16 hi / lo
+            // tiles (row t, s contiguous, 128-byte swizzle)
             {
                 const int t = wt & 63, cb = (wt >> 6) * 4;   // four 8-column groups per thread
+                float av[4][8];
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
                     const int c = cb + cc;
-                    const float4 x0 = *reinterpret_cast<const float4 *>(rec + kRecA + t * 64 + (((2 * c) ^ (t & 15)) << 2));
+                    const float4 x0 =
+                        *reinterpret_cast<const float4 *>(rec + R::A + t * 64 + (((2 * c) ^ (t & 15)) << 2));
                     const float4 x1 =
-                        *reinterpret_cast<const float4 *>(rec + kRecA + t * 64 + (((2 * c + 1) ^ (t & 15)) << 2));
-                    const float av[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+                        *reinterpret_cast<const float4 *>(rec + R::A + t * 64 + (((2 * c + 1) ^ (t & 15)) << 2));
+                    av[cc][0] = x0.x; av[cc][1] = x0.y; av[cc][2] = x0.z; av[cc][3] = x0.w;
+                    av[cc][4] = x1.x; av[cc][5] = x1.y; av[cc][6] = x1.z; av[cc][7] = x1.w;
+                }
+                bar_sync(1, kWT);   // all of A is in registers: its bytes may be overwritten
+                uint8_t *ab2 = st + SM::Rec;
+                uint8_t *ab = smem + SM::Ab + b * 16384;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const int c = cb + cc;
                     const int off = t * 128 + ((c ^ (t & 7)) << 4);
                     uint32_t hi[4], lo[4];
 #pragma unroll
                     for (int p = 0; p < 4; ++p)
-                        split_pair(av[2 * p] * rec[kRecGbb + c * 8 + 2 * p],
-                                   av[2 * p + 1] * rec[kRecGbb + c * 8 + 2 * p + 1], hi[p], lo[p]);
-                    *reinterpret_cast<uint4 *>(smem + kAb2 + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                    *reinterpret_cast<uint4 *>(smem + kAb2 + 8192 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                        split_pair(av[cc][2 * p] * rec[R::Gbb + c * 8 + 2 * p],
+                                   av[cc][2 * p + 1] * rec[R::Gbb + c * 8 + 2 * p + 1], hi[p], lo[p]);
+                    *reinterpret_cast<uint4 *>(ab2 + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4 *>(ab2 + 8192 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                     if (half) {
-                        uint8_t *ab = smem + kAb + (int)par * 16384;
 #pragma unroll
                         for (int p = 0; p < 4; ++p)
-                            split_pair(av[2 * p] * rec[kRecGbeta + c * 8 + 2 * p],
-                                       av[2 * p + 1] * rec[kRecGbeta + c * 8 + 2 * p + 1], hi[p], lo[p]);
+                            split_pair(av[cc][2 * p] * rec[R::Gbeta + c * 8 + 2 * p],
+                                       av[cc][2 * p + 1] * rec[R::Gbeta + c * 8 + 2 * p + 1], hi[p], lo[p]);
                         *reinterpret_cast<uint4 *>(ab + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
                         *reinterpret_cast<uint4 *>(ab + 8192 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                     }
@@ -379,13 +481,13 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
             }
             fence_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->aop_ready[par]);
+            if (lane == 0) mbar_arrive(&ctl->aop_ready[b]);
             bar_sync(1, kWT);
             // ---- W^T = K^T (A diag(beta b))^T
             if (issuer) {
                 tc_fence_after();
-                const uint32_t kb = smem_addr(st + kSK);
-                const uint32_t ab2 = smem_addr(smem + kAb2);
+                const uint32_t kb = smem_addr(st + SM::K);
+                const uint32_t ab2 = smem_addr(st + SM::Rec);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
                     const uint64_t ad = smem_desc_sw128(kb + (uint32_t)ks * 2048u, kBox, 1024);
@@ -394,15 +496,15 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
                 }
                 mma_commit(&ctl->w_done);
             }
-            if (!bar_and(1, kWT, wait_or_abort(&ctl->w_done, par, abortp))) {
+            if (!bar_and(1, kWT, wait_or_abort(&ctl->w_done, (uint32_t)j & 1u, abortp))) {
                 *abortp = 1;
                 break;
             }
             tc_fence_after();
-            // ---- -W^T -> bf16 hi / lo tiles, MN-major (row k, t contiguous, 128B swizzle)
+            // ---- -W^T -> bf16 hi / lo tiles, MN-major (row k, t contiguous, 128-byte swizzle)
             {
                 const int k = quarter * 32 + lane;
-                uint8_t *wtile = smem + kWt + (int)par * 32768;
+                uint8_t *wtile = smem + SM::Wt + b * 32768;
                 for (int cb = 0; cb < 2; ++cb) {
                     uint32_t r[32];
                     tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + kTw + (uint32_t)(cb * 32), r);
@@ -424,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
             tc_fence_before();
             fence_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->wop_ready[par]);
+            if (lane == 0) mbar_arrive(&ctl->wop_ready[b]);
         }
         if (issuer && *abortp) {   // drain: completes once this thread's MMAs are done
             mma_commit(&ctl->drain[0]);
@@ -442,6 +544,8 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
         const uint32_t tx = tmem + lane_off + kTx + (uint32_t)(cg * 32);
         const uint32_t txop = tmem + lane_off + kTxop + (uint32_t)(cg * 16);
         const uint32_t tacc = tmem + lane_off + kTacc + (uint32_t)(cg * 16);
+        const uint32_t to1 = tmem + lane_off + kTo1 + (uint32_t)(cg * 16);
+        const uint32_t to2 = tmem + lane_off + kTo2 + (uint32_t)(cg * 16);
         // Transition half: M_true = exp(lam_d + lam_exp ln2) M_stored, and each chunk
         // stores T_chunk M / b_C (log b_C into lam_d).  State half: S_true =
         // exp(ls) S_stored.  Either way the update only accumulates into TMEM; X is
@@ -461,11 +565,12 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
 
         for (int j = 0; j < nc; ++j) {
             const int s = j % kNS;
-            const uint32_t par = (uint32_t)j & 1u;
-            const uint8_t *stg = smem + s * kStage;
-            const float *rec = reinterpret_cast<const float *>(stg + kSRec);
+            const int b = j % SM::NB;
+            const uint32_t use = (uint32_t)(j / SM::NB);
+            const uint8_t *stg = smem + s * SM::Stage;
+            const float *rec = reinterpret_cast<const float *>(stg + SM::Rec);
             bool ok = wait_or_abort(&ctl->full[s], (uint32_t)(j / kNS) & 1u, abortp);
-            if (j > 0) ok = ok && wait_or_abort(&ctl->x_done, par ^ 1u, abortp);
+            if (j > 0) ok = ok && wait_or_abort(&ctl->x_done, (uint32_t)(j - 1) & 1u, abortp);
             if (!bar_and(2, kState, ok)) {
                 *abortp = 1;
                 break;
@@ -474,9 +579,9 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
             // ---- U^T = V^T (A diag(beta))^T into the accumulator (state half), on the
             // tensor cores while the X operand is converted below
             if (issuer && half) {
-                if (wait_or_abort(&ctl->aop_ready[par], (uint32_t)(j >> 1) & 1u, abortp)) {
+                if (wait_or_abort(&ctl->aop_ready[b], use & 1u, abortp)) {
                     tc_fence_after();
-                    const uint32_t vb = smem_addr(stg + kSV), ab = smem_addr(smem + kAb + (int)par * 16384);
+                    const uint32_t vb = smem_addr(stg + SM::V), ab = smem_addr(smem + SM::Ab + b * 16384);
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {
                         const uint64_t ad = smem_desc_sw128(vb + (uint32_t)ks * 2048u, kBox, 1024);
@@ -486,8 +591,10 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
                     }
                 }
             }
+            // ---- o_t of the previous chunk (its O1, O2 are complete: x_done)
+            if (with_o && j > 0) store_o(a, h, to1, to2, ctl->bo, cg, m, row0 + (int64_t)(j - 1) * kC, kC);
             // ---- scales of this chunk
-            const float LC = rec[kRecLC];               // log of the chunk's total decay
+            const float LC = rec[R::LC];                // log of the chunk's total decay
             const bool slow = LC < -40.f;
             const bool renorm = slow || (half == 0 ? (j % 8 == 0) : (ls < -20.f));
             float g = 1.f;        // X_stored <- g * wscale * X_stored when rewritten
@@ -505,14 +612,14 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
                     g = ldexpf(1.f, -e);
                     lam_exp += e;
                 }
-                wscale = slow ? rec[kRecBC] : 1.f;
+                wscale = slow ? rec[R::BC] : 1.f;
                 fP = 1.f;
                 fD = slow ? 1.f : expf(-LC);
                 if (!slow) lam_d += (double)LC;
             } else {
                 if (slow) {
                     g = expf(ls);
-                    wscale = rec[kRecBC];
+                    wscale = rec[R::BC];
                     fP = 1.f;
                     fD = 1.f;
                     ls = 0.f;
@@ -547,11 +654,11 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
             tmem_wait_st();
             tc_fence_before();
             bar_sync(2, kState);
-            // ---- Delta^T = U^T - X0^T W^T (three-term split)
+            // ---- Delta^T = U^T - X0^T W^T (three-term split); O1^T = X0^T Q^T
             if (issuer) {
-                if (wait_or_abort(&ctl->wop_ready[par], (uint32_t)(j >> 1) & 1u, abortp)) {
+                if (wait_or_abort(&ctl->wop_ready[b], use & 1u, abortp)) {
                     tc_fence_after();
-                    const uint32_t wtile = smem_addr(smem + kWt + (int)par * 32768);
+                    const uint32_t wtile = smem_addr(smem + SM::Wt + b * 32768);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
                         const uint64_t bh = smem_desc_sw128(wtile + (uint32_t)ks * 2048u, 16384, 1024);
@@ -561,12 +668,24 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
                         mma_f16_ta(tmem + kTacc, ah, bl, id_d, 1u);
                         mma_f16_ta(tmem + kTacc, al, bh, id_d, 1u);
                     }
+                    if (with_o) {
+                        const uint32_t qb = smem_addr(stg + SM::Q);
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks) {
+                            const uint64_t bq =
+                                smem_desc_sw128(qb + (uint32_t)(ks >> 2) * kBox + (uint32_t)(ks & 3) * 32u, 0, 1024);
+                            const uint32_t ah = tmem + kTxop + (uint32_t)ks * 8u;
+                            mma_f16_ta(tmem + kTo1, ah, bq, id_o, ks > 0);
+                            mma_f16_ta(tmem + kTo1, ah + 64u, bq, id_o, 1u);
+                        }
+                    }
                 }
                 mma_commit(&ctl->d_done);
-                mma_commit(&ctl->wfree[par]);
+                mma_commit(&ctl->wfree[b]);
             }
             // ---- Delta~^T = fD Delta^T diag(b_C / b) -> bf16 hi / lo in place
-            if (!bar_and(2, kState, wait_or_abort(&ctl->d_done, par, abortp))) {
+            // (with o_t also Delta^T itself, hi / lo, into the X0 operand columns)
+            if (!bar_and(2, kState, wait_or_abort(&ctl->d_done, (uint32_t)j & 1u, abortp))) {
                 *abortp = 1;
                 break;
             }
@@ -575,22 +694,31 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
                 uint32_t r[16], hi[8], lo[8];
                 tmem_ld16(tacc, r);
                 tmem_wait_ld();
+                if (with_o) {
+#pragma unroll
+                    for (int p = 0; p < 8; ++p)
+                        split_pair(__uint_as_float(r[2 * p]), __uint_as_float(r[2 * p + 1]), hi[p], lo[p]);
+                    tmem_st8(txop, hi);
+                    tmem_st8(txop + 8u, lo);
+                }
 #pragma unroll
                 for (int p = 0; p < 8; ++p) {
                     const int t = cg * 16 + 2 * p;
-                    split_pair(fD * rec[kRecGw + t] * __uint_as_float(r[2 * p]),
-                               fD * rec[kRecGw + t + 1] * __uint_as_float(r[2 * p + 1]), hi[p], lo[p]);
+                    split_pair(fD * rec[R::Gw + t] * __uint_as_float(r[2 * p]),
+                               fD * rec[R::Gw + t + 1] * __uint_as_float(r[2 * p + 1]), hi[p], lo[p]);
                 }
                 tmem_st8(tacc, hi);          // tokens cg*16 .. +15: hi in the first 8 columns,
                 tmem_st8(tacc + 8u, lo);     // lo in the next 8 (this thread's own columns)
+                if (with_o && st < kC) ctl->bo[st] = rec[R::B + st];   // for this chunk's o store
             }
             tmem_wait_st();
             tc_fence_before();
             bar_sync(2, kState);
-            // ---- X^T += Delta~^T K (K as the MN-major B operand: row t, channels contiguous)
+            // ---- X^T += Delta~^T K (K as the MN-major B operand: row t, channels contiguous);
+            // O2^T = Delta^T Gq^T (three-term split)
             if (issuer) {
                 tc_fence_after();
-                const uint32_t kb = smem_addr(stg + kSK);
+                const uint32_t kb = smem_addr(stg + SM::K);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
                     const uint64_t bd = smem_desc_sw128(kb + (uint32_t)ks * 2048u, kBox, 1024);
@@ -598,8 +726,20 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
                     mma_f16_ta(tmem + kTx, ah, bd, id_x, 1u);
                     mma_f16_ta(tmem + kTx, ah + 8u, bd, id_x, 1u);
                 }
+                if (with_o) {
+                    const uint32_t gq = smem_addr(stg + SM::Rec + R::Gq * 4);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const uint64_t gh = smem_desc_sw128(gq + (uint32_t)ks * 32u, 0, 1024);
+                        const uint64_t gl = smem_desc_sw128(gq + 8192u + (uint32_t)ks * 32u, 0, 1024);
+                        const uint32_t ah = tmem + kTxop + (uint32_t)ks * 16u;
+                        mma_f16_ta(tmem + kTo2, ah, gh, id_o, ks > 0);
+                        mma_f16_ta(tmem + kTo2, ah, gl, id_o, 1u);
+                        mma_f16_ta(tmem + kTo2, ah + 8u, gh, id_o, 1u);
+                    }
+                }
                 mma_commit(&ctl->x_done);
-                mma_commit(&ctl->empty[s]);
+                mma_commit(&ctl->empty[s]);   // the stage is free once X (and O2) have read it
             }
         }
         if (issuer && *abortp) {
@@ -612,6 +752,9 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
         if (nc > 0) ok = wait_or_abort(&ctl->x_done, (uint32_t)(nc - 1) & 1u, abortp);
         if (bar_and(2, kState, ok)) {
             tc_fence_after();
+            if (with_o && nc > 0)
+                store_o(a, h, to1, to2, ctl->bo, cg, m, row0 + (int64_t)(nc - 1) * kC,
+                        (int)(t1 - t0 - (int64_t)(nc - 1) * kC));
             const int64_t u_out = ((int64_t)l * a.n_seg + seg) * a.H + h;
             uint32_t r[32];
             tmem_ld32(tx, r);
@@ -645,13 +788,38 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
     }
 }
 
+template <bool O>
+cudaError_t launch_two_pass(const ScanArgs &a, cudaStream_t s) {
+    const int64_t units = (int64_t)a.n_layers * a.n_seg * a.H;
+    const uint64_t rows = (uint64_t)a.n_layers * (uint64_t)a.N;
+    CUtensorMap mk, mv, mq;
+    if (!make_tensor_map_3d(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.k, 128, a.H, rows, 64, kC,
+                            CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map_3d(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.v, 128, a.H, rows, 64, kC,
+                            CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map_3d(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, O ? a.q : a.k, 128, a.H, rows, 64, kC,
+                            CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    const int64_t slots = n_slots(a.N, a.n_seg);
+    cudaError_t e = cudaFuncSetAttribute(dense_prep_kernel<O>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(dense_state_kernel<O>, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem<O>());
+    if (e != cudaSuccess) return e;
+    dense_prep_kernel<O><<<dim3((unsigned)(slots * a.H), (unsigned)a.n_layers), kPThreads, kPSmem, s>>>(mk, mq, a,
+                                                                                                     slots);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    dense_state_kernel<O><<<(unsigned)(2 * units), kThreads, state_smem<O>(), s>>>(mk, mv, mq, a, slots);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------- host side
 
 bool scan_dense_ws_shape(const ScanArgs &a) {
-    return a.fam == HYPIC_DENSE && a.in_dtype == HYPIC_BF16 && a.dk == 128 && a.dv == 128 &&
-           a.o_out == nullptr && a.N > 0 && (int64_t)a.n_layers * a.N < ((int64_t)1 << 31) &&
+    return a.fam == HYPIC_DENSE && a.in_dtype == HYPIC_BF16 && a.dk == 128 && a.dv == 128 && a.N > 0 &&
+           (int64_t)a.n_layers * a.N < ((int64_t)1 << 31) &&
            (int64_t)a.n_layers * a.n_seg * a.H < ((int64_t)1 << 30) &&
            n_slots(a.N, a.n_seg) * a.H < ((int64_t)1 << 31) && a.n_layers <= 65535;
 }
@@ -661,29 +829,12 @@ bool scan_dense_ws_supported(const ScanArgs &a) {
 }
 
 int64_t scan_dense_ws_bytes(const ScanArgs &a) {
-    return (int64_t)a.n_layers * a.H * n_slots(a.N, a.n_seg) * kRecBytes;
+    return (int64_t)a.n_layers * a.H * n_slots(a.N, a.n_seg) * (a.o_out ? Rec<true>::Bytes : Rec<false>::Bytes);
 }
 
 cudaError_t launch_scan_dense_ws(const ScanArgs &a, cudaStream_t s) {
-    const int64_t units = (int64_t)a.n_layers * a.n_seg * a.H;
-    if (units == 0) return cudaSuccess;
-    const uint64_t rows = (uint64_t)a.n_layers * (uint64_t)a.N;
-    CUtensorMap mk, mv;
-    if (!make_tensor_map_3d(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.k, 128, a.H, rows, 64, kC,
-                            CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tensor_map_3d(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.v, 128, a.H, rows, 64, kC,
-                            CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
-    const int64_t slots = n_slots(a.N, a.n_seg);
-    cudaError_t e = cudaFuncSetAttribute(dense_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(dense_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (e != cudaSuccess) return e;
-    dense_prep_kernel<<<dim3((unsigned)(slots * a.H), (unsigned)a.n_layers), kPThreads, kPSmem, s>>>(mk, a, slots);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    dense_state_kernel<<<(unsigned)(2 * units), kThreads, kSmem, s>>>(mk, mv, a, slots);
-    return cudaGetLastError();
+    if ((int64_t)a.n_layers * a.n_seg * a.H == 0) return cudaSuccess;
+    return a.o_out ? launch_two_pass<true>(a, s) : launch_two_pass<false>(a, s);
 }
 
 }  // namespace hypic

@@ -174,6 +174,27 @@ def test_dense_long_segment_and_special_gates(form):
     check(DENSE, host(gpu_scan(w2, workspace=form)), oracle_scan(w2), TOL_SCAN_BF16)
 
 
+@DENSE_FORMS
+def test_dense_o_long_and_special_gates(form):
+    """o_t of the gated delta rule over several chunks (both forms): a long
+    segment with a ragged tail, alpha = beta = 1, and strong decay (chunks below
+    e^-40 alternating with mild ones)."""
+    w = wl.dense_stack(lengths=[2048 + 17, 700], n_layers=1, H=2, d=128, seed=16, with_q=True)
+    got = host(gpu_scan(w, want_o=True, workspace=form))
+    check(DENSE, got, oracle_scan(w, want_o=True), TOL_SCAN_BF16, o_tol=TOL_O_BF16, seg_offsets=w["seg_offsets"])
+    w1 = dict(w)
+    w1["alpha"] = np.ones_like(w["alpha"])
+    w1["beta"] = np.ones_like(w["beta"])
+    got = host(gpu_scan(w1, want_o=True, workspace=form))
+    check(DENSE, got, oracle_scan(w1, want_o=True), TOL_SCAN_BF16, o_tol=TOL_O_BF16, seg_offsets=w["seg_offsets"])
+    w2 = dict(w)
+    w2["alpha"] = w["alpha"].copy()
+    t = np.arange(w2["alpha"].shape[1])
+    w2["alpha"][:, (t // 64) % 3 == 1] = 0.3
+    got = host(gpu_scan(w2, want_o=True, workspace=form))
+    check(DENSE, got, oracle_scan(w2, want_o=True), TOL_SCAN_BF16, o_tol=TOL_O_BF16, seg_offsets=w["seg_offsets"])
+
+
 @pytest.mark.parametrize("fam", [SCALAR, DIAG, DENSE], ids=["scalar", "diag", "dense"])
 def test_segment_independence_bitwise(fam):
     """T_C and S(C|0) depend only on the segment's tokens: the same segment
