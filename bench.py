@@ -305,14 +305,19 @@ def run_dense(args, L):
            "S": torch.empty((Lyr, 1, H, d, d), dtype=torch.float32, device=dev),
            "M": torch.empty((Lyr, 1, H, d, d), dtype=torch.float32, device=dev)}
     del w
+    # two passes over a workspace (the default) or the single-pass kernel
+    ws = None
+    if args.dense_form == "two_pass":
+        ws = torch.empty(hy.segment_scan_workspace_bytes(2, torch.bfloat16, Lyr, 1, L, H, d, d),
+                         dtype=torch.uint8, device=dev)
     for _ in range(2):
-        hy.segment_scan(2, k, v, a, offs, beta=b, out=out)
+        hy.segment_scan(2, k, v, a, offs, beta=b, out=out, workspace=ws)
     torch.cuda.synchronize()
     reps = 3
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
     for s, e in evs:
         s.record()
-        hy.segment_scan(2, k, v, a, offs, beta=b, out=out)
+        hy.segment_scan(2, k, v, a, offs, beta=b, out=out, workspace=ws)
         e.record()
     torch.cuda.synchronize()
     t = sum(s.elapsed_time(e) for s, e in evs) / reps / 1e3
@@ -321,7 +326,7 @@ def run_dense(args, L):
     _, bf16, bf16_sus, src = peaks()
     return {"workload": f"gated delta rule, {Lyr} layers x {H} heads x {d}, one segment of {L} tokens per layer",
             "value": L / t, "unit": "tokens/s (all 30 layers)", "head_tokens_per_s": tok_heads / t,
-            "ms": t * 1e3,
+            "ms": t * 1e3, "form": args.dense_form,
             "roofline": {"bound": "tensor", "achieved": flops / t / 1e12, "peak": bf16,
                          "unit": "TFLOP/s", "frac": flops / t / 1e12 / bf16, "traffic": None,
                          "peak_kind": f"bf16 burst, {src}"}}
@@ -531,6 +536,8 @@ def main():
     ap.add_argument("--L", type=int, default=8192)
     ap.add_argument("--rows", default="dense,chain,mix", help="extra rows: dense,chain,mix or none")
     ap.add_argument("--dense-L", type=int, default=2048)
+    ap.add_argument("--dense-form", choices=["two_pass", "single"], default="two_pass",
+                    help="dense row: two passes over a workspace, or the single-pass kernel")
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
