@@ -71,15 +71,16 @@ __host__ __device__ inline int64_t n_slots(int64_t N, int n_seg) { return (int64
 // ================================================================ pass 1: preparation
 
 constexpr int kPThreads = 128;
-// shared memory (from the 1024-aligned base): the Gram's A operand rows, keys
-// 0..63 then queries 64..127 (without o_t the query boxes are simply not
-// loaded: those rows of the Gram are unused), per 64-channel box; the fp32 L
-// tile overlays them once the Gram is done; the fp32 A tile, temporaries, control.
-constexpr int kPK = 0;           // K0 | Q0 | K1 | Q1
-constexpr int kPAw = 4 * kBox;
+// shared memory (from the 1024-aligned base): the Gram's A operand rows per
+// 64-channel box, keys 0..63 then queries 64..127 (without o_t the keys again,
+// so that every TMEM lane quarter holds K K^T rows and all four warps share the
+// L work).  Once the Gram is done the fp32 L and A tiles overlay that region,
+// then temporaries and control: 39.5 KB, five CTAs per SM.
+constexpr int kPK = 0;                        // K0 | Q0 (or K0) | K1 | Q1 (or K1)
+constexpr int kPAw = kC * kLd * 4;            // L at [0, kPAw), A after it
 constexpr int kPTw = kPAw + kC * kLd * 4;
 constexpr int kPCtl = kPTw + 3 * 256 * 4;
-static_assert(kC * kLd * 4 <= 4 * kBox, "L overlays the key / query tile");
+static_assert(kPTw >= 4 * kBox, "the Gram operands end before the temporaries");
 
 struct PrepCtl {
     uint64_t full, mma;
@@ -120,14 +121,12 @@ __global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_cons
         mbar_init(&ctl->full, 1);
         mbar_init(&ctl->mma, 1);
         mbar_fence_init();
-        mbar_expect_tx(&ctl->full, (O ? 4 : 2) * kBox);
+        mbar_expect_tx(&ctl->full, 4 * kBox);
         const int row = (int)((int64_t)l * a.N + c0);
         tma_load_3d(smem + kPK, &tm_k, &ctl->full, 0, h, row);
         tma_load_3d(smem + kPK + 2 * kBox, &tm_k, &ctl->full, 64, h, row);
-        if (O) {
-            tma_load_3d(smem + kPK + kBox, &tm_q, &ctl->full, 0, h, row);
-            tma_load_3d(smem + kPK + 3 * kBox, &tm_q, &ctl->full, 64, h, row);
-        }
+        tma_load_3d(smem + kPK + kBox, O ? &tm_q : &tm_k, &ctl->full, 0, h, row);
+        tma_load_3d(smem + kPK + 3 * kBox, O ? &tm_q : &tm_k, &ctl->full, 64, h, row);
     }
     if (warp == 0) tmem_alloc(&ctl->tmem, 64);
     tc_fence_before();
@@ -174,7 +173,7 @@ __global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_cons
             rec[R::LC] = total;
             rec[R::BC] = expf(total);
         }
-        // Gram [K; Q] K^T: lanes 0..63 K K^T, lanes 64..127 Q K^T (unused without o_t)
+        // Gram [K; Q] K^T: lanes 0..63 K K^T, lanes 64..127 Q K^T (K K^T again without o_t)
         if (lane == 0) {
             ok = mbar_wait(&ctl->full, 0);
             if (ok) {
@@ -199,7 +198,20 @@ __global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_cons
     if (ok) {
         const int t = (warp & 1) * 32 + lane;   // token row 0..63 of this thread
         const float lt = ctl->gl[t];
-        if (warp < 2) {
+        if (!O) {
+            // ---- L[t][s] = beta_t exp(Lambda_t - Lambda_s) G[t][s] for s < t; warps 0, 1
+            // take columns 0..31, warps 2, 3 columns 32..63 (from the second copy)
+            const float bt = ctl->gbeta[t];
+            const int cbase = (warp >> 1) * 32;
+            uint32_t r[32];
+            tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)cbase, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int sc = cbase + i;
+                Lw[t * kLd + sc] = sc < t ? bt * __expf(lt - ctl->gl[sc]) * __uint_as_float(r[i]) : 0.f;
+            }
+        } else if (warp < 2) {
             // ---- L[t][s] = beta_t exp(Lambda_t - Lambda_s) G[t][s] for s < t
             const float bt = ctl->gbeta[t];
             for (int cb = 0; cb < 2; ++cb) {
