@@ -87,24 +87,27 @@ __device__ __forceinline__ void inverse_level(const float *Lw, float *Aw, float 
 
 // A = (I + L)^-1 for the strictly lower 64 x 64 L in Lw (row stride kLd; entries
 // on and above the diagonal are not read).  Diagonal 16 x 16 blocks by forward
-// substitution (one column per thread, registers), then three block levels.
-// Needs NT >= 64; Tw holds 3 x 256 floats.  Ends with a barrier.
-template <int NT, int BAR>
+// substitution in column (axpy) order -- one column per thread in registers, a
+// dependent chain of 16 steps -- then three block levels.  ZERO_UPPER also
+// writes the zero blocks above the diagonal (else the caller never reads them).
+// Needs NT >= 128; Tw holds 3 x 256 floats.  Ends with a barrier.
+template <int NT, int BAR, bool ZERO_UPPER = true>
 __device__ __forceinline__ void tri_inverse(const float *Lw, float *Aw, float *Tw, int pt) {
     static_assert(NT >= 128, "one column per thread for the diagonal blocks, the rest zero the upper blocks");
     if (pt < 64) {
         const int b0 = (pt >> 4) * 16, jc = pt & 15, col = b0 + jc;
         float ac[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            float sum = 0.f;
+        for (int i = 0; i < 16; ++i) ac[i] = i == jc ? 1.f : 0.f;
 #pragma unroll
-            for (int k = 0; k < i; ++k) sum = fmaf(Lw[(b0 + i) * kLd + b0 + k], ac[k], sum);
-            ac[i] = i < jc ? 0.f : (i == jc ? 1.f : -sum);
+        for (int k = 0; k < 15; ++k) {
+            // ac[k] is final here; push its contribution down the column
+#pragma unroll
+            for (int i = k + 1; i < 16; ++i) ac[i] = fmaf(-Lw[(b0 + i) * kLd + b0 + k], ac[k], ac[i]);
         }
 #pragma unroll
         for (int i = 0; i < 16; ++i) Aw[(b0 + i) * kLd + col] = ac[i];
-    } else {
+    } else if (ZERO_UPPER) {
         // zero the strictly upper off-diagonal blocks
         for (int e = pt - 64; e < 6 * 256; e += NT - 64) {
             const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15;

@@ -252,13 +252,14 @@ __global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_cons
             }
         }
         __syncthreads();
-        dense::tri_inverse<kPThreads, 1>(Lw, Aw, Tw, tid);
-        // ---- A -> the record (16-byte groups, swizzled by row)
+        dense::tri_inverse<kPThreads, 1, false>(Lw, Aw, Tw, tid);
+        // ---- A -> the record (16-byte groups, swizzled by row; zero above the diagonal blocks)
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int f = tid + kPThreads * i;   // 0 .. 1023
             const int tt = f >> 4, g = f & 15;
-            const float4 v = *reinterpret_cast<const float4 *>(Aw + tt * kLd + g * 4);
+            const float4 v = (g >> 2) > (tt >> 4) ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                                  : *reinterpret_cast<const float4 *>(Aw + tt * kLd + g * 4);
             *reinterpret_cast<float4 *>(rec + R::A + tt * 64 + ((g ^ (tt & 15)) << 2)) = v;
         }
     } else if (tid == 0 && a.d_err) {
