@@ -205,11 +205,14 @@ __global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_cons
             const int cbase = (warp >> 1) * 32;
             uint32_t r[32];
             tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)cbase, r);
+            float gs[32];   // all loads before the first store (the L tile could alias them)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) gs[i] = ctl->gl[cbase + i];
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 const int sc = cbase + i;
-                Lw[t * kLd + sc] = sc < t ? bt * __expf(lt - ctl->gl[sc]) * __uint_as_float(r[i]) : 0.f;
+                Lw[t * kLd + sc] = sc < t ? bt * __expf(lt - gs[i]) * __uint_as_float(r[i]) : 0.f;
             }
         } else if (warp < 2) {
             // ---- L[t][s] = beta_t exp(Lambda_t - Lambda_s) G[t][s] for s < t
@@ -217,11 +220,14 @@ __global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_cons
             for (int cb = 0; cb < 2; ++cb) {
                 uint32_t r[32];
                 tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(cb * 32), r);
+                float gs[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) gs[i] = ctl->gl[cb * 32 + i];
                 tmem_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const int sc = cb * 32 + i;
-                    Lw[t * kLd + sc] = sc < t ? bt * __expf(lt - ctl->gl[sc]) * __uint_as_float(r[i]) : 0.f;
+                    Lw[t * kLd + sc] = sc < t ? bt * __expf(lt - gs[i]) * __uint_as_float(r[i]) : 0.f;
                 }
             }
         } else if (O) {
@@ -230,6 +236,9 @@ __global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_cons
             for (int cb = 0; cb < 2; ++cb) {
                 uint32_t r[32];
                 tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(cb * 32), r);
+                float gs[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) gs[i] = ctl->gl[cb * 32 + i];
                 tmem_wait_ld();
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
@@ -241,7 +250,8 @@ __global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_cons
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
                             const int sc = c * 8 + 2 * p + e;
-                            x[e] = sc <= t ? __expf(lt - ctl->gl[sc]) * __uint_as_float(r[cc * 8 + 2 * p + e]) : 0.f;
+                            x[e] = sc <= t ? __expf(lt - gs[cc * 8 + 2 * p + e]) * __uint_as_float(r[cc * 8 + 2 * p + e])
+                                           : 0.f;
                         }
                         split_pair(x[0], x[1], hv[p], lv[p]);
                     }
@@ -254,13 +264,19 @@ __global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_cons
         __syncthreads();
         dense::tri_inverse<kPThreads, 1, false>(Lw, Aw, Tw, tid);
         // ---- A -> the record (16-byte groups, swizzled by row; zero above the diagonal blocks)
+        float4 v[8];   // all loads before the first store
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int f = tid + kPThreads * i;   // 0 .. 1023
             const int tt = f >> 4, g = f & 15;
-            const float4 v = (g >> 2) > (tt >> 4) ? make_float4(0.f, 0.f, 0.f, 0.f)
-                                                  : *reinterpret_cast<const float4 *>(Aw + tt * kLd + g * 4);
-            *reinterpret_cast<float4 *>(rec + R::A + tt * 64 + ((g ^ (tt & 15)) << 2)) = v;
+            v[i] = (g >> 2) > (tt >> 4) ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                        : *reinterpret_cast<const float4 *>(Aw + tt * kLd + g * 4);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int f = tid + kPThreads * i;
+            const int tt = f >> 4, g = f & 15;
+            *reinterpret_cast<float4 *>(rec + R::A + tt * 64 + ((g ^ (tt & 15)) << 2)) = v[i];
         }
     } else if (tid == 0 && a.d_err) {
         atomicExch(a.d_err, (int)HYPIC_ETIMEOUT);
