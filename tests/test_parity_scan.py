@@ -152,6 +152,22 @@ def test_dense_full_stack_sampled(L, form):
 
 
 @DENSE_FORMS
+@pytest.mark.parametrize("L", [8192, 32768])
+def test_dense_longest_segments_sampled(L, form):
+    """The dense stack's longest segments (8192 and 32768 tokens: 128 / 512
+    chunks, transitions far below fp32 range) on 2 layers x 32 heads (the
+    benchmark's launch shape per layer); sampled heads against the oracle."""
+    w = wl.dense_stack(seg_len=L, n_layers=2, H=32, d=128, seed=2)
+    got = host(gpu_scan(w, workspace=form))
+    for l, h in [(0, 0), (1, 31), (1, 9)]:
+        ref = oracle.sequential(DENSE, w["k"][l:l + 1, :, h:h + 1], w["v"][l:l + 1, :, h:h + 1],
+                                w["alpha"][l:l + 1, :, h:h + 1], w["beta"][l:l + 1, :, h:h + 1])
+        sub = {"S": got["S"][l:l + 1, 0, h:h + 1], "lam": got["lam"][l:l + 1, 0, h:h + 1],
+               "M": got["M"][l:l + 1, 0, h:h + 1]}
+        check(DENSE, sub, ref, TOL_SCAN_BF16)
+
+
+@DENSE_FORMS
 def test_dense_long_segment_and_special_gates(form):
     """Gated delta rule on long segments (many chunks of transition renormalisation),
     beta = 0 (pure decay: S = 0, T = prod(alpha) I) and alpha = beta = 1 (plain delta rule)."""
