@@ -332,6 +332,45 @@ def run_dense(args, L):
                          "peak_kind": f"bf16 burst, {src}"}}
 
 
+def run_compose(args):
+    """One composition step S = T S_prev + S_C (hypic_compose) over 64 requests x
+    30 layers = 1920 items x 32 heads x 128 x 128, per family; synthetic fp32
+    states drawn on the device (values do not change the work)."""
+    import torch
+    import linear_attention_state_gated_gb300 as hy
+    res = {}
+    hbm, _, _, src = peaks()
+    n, H, d = 1920, 32, 128
+    dev = torch.device("cuda")
+    g = torch.Generator(device=dev)
+    g.manual_seed(5)
+    S_prev = torch.randn((n, H, d, d), generator=g, device=dev)
+    S_C = torch.randn((n, H, d, d), generator=g, device=dev)
+    S_out = torch.empty_like(S_prev)
+    for fam, name in ((0, "scalar"), (1, "diag"), (2, "dense")):
+        lam = -torch.rand((n, H, d) if fam == 1 else (n, H), generator=g, device=dev) * 50
+        M = torch.randn((n, H, d, d), generator=g, device=dev) * 0.1 if fam == 2 else None
+        for _ in range(3):
+            hy.compose(fam, lam, S_C, S_prev=S_prev, M=M, S_out=S_out)
+        torch.cuda.synchronize()
+        reps = 5
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(reps):
+            hy.compose(fam, lam, S_C, S_prev=S_prev, M=M, S_out=S_out)
+        e.record()
+        torch.cuda.synchronize()
+        t = s.elapsed_time(e) / reps / 1e3
+        by = n * H * (3 * 4 * d * d + (4 * d if fam == 1 else 4) + (4 * d * d if fam == 2 else 0))
+        res[name] = {"value": n / t, "unit": "composes/s (all 32 heads)", "ms": t * 1e3,
+                     "roofline": {"bound": "hbm", "achieved": by / t / 1e9, "peak": hbm, "unit": "GB/s",
+                                  "frac": by / t / 1e9 / hbm, "traffic": None, "peak_kind": f"copy, {src}"}}
+        del M, lam
+    del S_prev, S_C, S_out
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_chain(args):
     import torch
     import linear_attention_state_gated_gb300 as hy
@@ -534,7 +573,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="hypic", choices=["hypic", "reference"])
     ap.add_argument("--L", type=int, default=8192)
-    ap.add_argument("--rows", default="dense,chain,mix", help="extra rows: dense,chain,mix or none")
+    ap.add_argument("--rows", default="dense,compose,chain,mix",
+                    help="extra rows: dense,compose,chain,mix or none")
     ap.add_argument("--dense-L", type=int, default=2048)
     ap.add_argument("--dense-form", choices=["two_pass", "single"], default="two_pass",
                     help="dense row: two passes over a workspace, or the single-pass kernel")
@@ -556,6 +596,8 @@ def main():
     rows = {}
     if rank == 0 and "dense" in args.rows:
         rows["dense_scan"] = run_dense(args, args.dense_L)
+    if rank == 0 and "compose" in args.rows:
+        rows["compose"] = run_compose(args)
     if rank == 0 and "chain" in args.rows:
         rows["rag_chain"] = run_chain(args)
     if rank == 0 and "mix" in args.rows:

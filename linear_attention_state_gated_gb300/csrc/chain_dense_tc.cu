@@ -8,6 +8,8 @@
 // (~2^-26 relative per product), which keeps the fp32 composition accurate to
 // well below 1e-5 at the cost of three TF32 products.  The exact fp32 running state stays in the math
 // warps' registers (row i of S on TMEM lane i, two warps per lane quarter).
+// Without a chain list (chain_len and seg_idx NULL) request r takes one step
+// with pool entry r: the single composition S = exp(lambda) M S_prev + S_C.
 // Warp 0 brings each M_p into shared memory by TMA (128-byte swizzle, so the
 // row-per-lane reads are conflict-free) while the previous step's MMAs run;
 // the math warps split it into TMEM as the A operand and split S into shared
@@ -58,7 +60,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = (int)(u / ((int64_t)a.n_layers * a.H));
     const int64_t lh = u % ((int64_t)a.n_layers * a.H);
 
-    int n = a.chain_len[r];
+    int n = a.chain_len ? a.chain_len[r] : 1;   // no list: one step, entry r (a single composition)
     if (n < 0 || n > a.max_chain) {
         if (threadIdx.x == 0) flag_index_error(a.d_err);
         n = n < 0 ? 0 : a.max_chain;
@@ -79,7 +81,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = ctl->tmem;
 
     auto entry = [&](int c) -> int64_t {   // pool entry of step c for this layer / head
-        int p = a.seg_idx[(int64_t)r * a.max_chain + c];
+        int p = a.seg_idx ? a.seg_idx[(int64_t)r * a.max_chain + c] : r;
         if (p < 0 || p >= a.P) {
             flag_index_error(a.d_err);
             p = p < 0 ? 0 : a.P - 1;

@@ -337,6 +337,29 @@ cudaError_t launch_compose(const ComposeArgs &a, cudaStream_t s) {
     const int64_t units = (int64_t)a.n * a.H;
     if (units == 0) return cudaSuccess;
     if (a.fam == HYPIC_DENSE) {
+        if (a.S_prev && a.dk == 128 && a.dv == 128) {
+            // the state on the tensor cores: a one-step chain per item, pool entry = item
+            ChainArgs c{};
+            c.fam = HYPIC_DENSE;
+            c.R = a.n;
+            c.n_layers = 1;
+            c.H = a.H;
+            c.dk = c.dv = 128;
+            c.max_chain = 1;
+            c.P = a.n;
+            c.pool_lam = a.lam;
+            c.pool_M = a.M;
+            c.pool_S = a.S_C;
+            c.S_init = a.S_prev;
+            c.S_out = a.S_out;
+            if (chain_dense_tc_supported(c)) {
+                cudaError_t e = launch_chain_dense_tc(c, s);
+                if (e != cudaSuccess || !a.lam_out) return e;
+                ComposeArgs b = a;   // then the operator T(C1.C2) alone
+                b.S_prev = nullptr;
+                return dispatch_dd<DenseComposeF>(b, s, a.dk, a.dv);
+            }
+        }
         if (!a.S_prev) {
             // no previous state: S_out = S_C (a copy); only the operator needs the GEMM
             ComposeArgs b = a;
