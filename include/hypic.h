@@ -104,10 +104,14 @@ int hypic_segment_scan(int fam, int in_dtype, int n_layers, int n_seg,
  * hypic_segment_scan_workspace_bytes -- bytes of device scratch that
  * hypic_segment_scan_ws needs for these sizes, or 0 when that call uses none
  * (then its workspace may be NULL).  A negative hypic_status on bad counts.
- * Today the scratch is used by the dense family with bf16 inputs and d_k = d_v
- * = 128: one record per (layer, head, 64-token chunk slot) of 17184 bytes
- * (33808 bytes with o_t), n_layers * n_heads * (n_seg + total_tokens / 64)
- * records.
+ * Today the scratch is used with bf16 inputs and d_k = d_v = 128 by
+ *   the dense family: one record per (layer, head, 64-token chunk slot) of
+ *     17184 bytes (33808 bytes with o_t), n_layers * n_heads * (n_seg +
+ *     total_tokens / 64) records;
+ *   the diagonal family without o_t and with n_seg <= 512: 2 x 512 partial
+ *     states of 66048 bytes (67.6 MB), for a schedule that spreads all
+ *     segments' chunks evenly over the GPU and then folds the pieces of
+ *     segments split between CTAs with the composition rule.
  */
 int64_t hypic_segment_scan_workspace_bytes(int fam, int in_dtype, int n_layers, int n_seg,
                                            int64_t total_tokens, int n_heads, int d_k, int d_v,
@@ -125,8 +129,10 @@ int64_t hypic_segment_scan_workspace_bytes(int fam, int in_dtype, int n_layers, 
  * With the scratch the dense scan runs in two passes: every 64-token chunk's
  * intra-chunk solve (Gram matrix, L, (I + L)^-1, decays) in parallel over all
  * chunks, then the ordered state pass (the chunked WY/UT form of the gated
- * delta rule; the pages give no chunked algorithm).  Other cases run exactly
- * as hypic_segment_scan.
+ * delta rule; the pages give no chunked algorithm); the diagonal scan balances
+ * its work over the GPU (results equal to hypic_segment_scan's up to rounding;
+ * they depend on the batch's total work, not on a segment's position).  Other
+ * cases run exactly as hypic_segment_scan.
  */
 int hypic_segment_scan_ws(int fam, int in_dtype, int n_layers, int n_seg,
                           int64_t total_tokens, int n_heads, int d_k, int d_v,

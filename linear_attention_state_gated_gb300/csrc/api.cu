@@ -157,8 +157,10 @@ int64_t hypic_segment_scan_workspace_bytes(int fam, int in_dtype, int n_layers, 
     a.dv = d_v;
     a.N = total_tokens;
     a.o_out = with_o ? reinterpret_cast<void *>(16) : nullptr;   // only tested against NULL
-    if (n_layers == 0 || n_seg == 0 || !hypic::scan_dense_ws_shape(a)) return 0;
-    return hypic::scan_dense_ws_bytes(a);
+    if (n_layers == 0 || n_seg == 0) return 0;
+    if (hypic::scan_dense_ws_shape(a)) return hypic::scan_dense_ws_bytes(a);
+    if (hypic::scan_sd_bal_shape(a)) return hypic::scan_sd_bal_bytes();
+    return 0;
 }
 
 int hypic_segment_scan_ws(int fam, int in_dtype, int n_layers, int n_seg, int64_t total_tokens,
@@ -180,6 +182,12 @@ int hypic_segment_scan_ws(int fam, int in_dtype, int n_layers, int n_seg, int64_
     if (hypic::scan_dense_ws_supported(a)) {
         a.ws = static_cast<float *>(workspace);
         return from_cuda(hypic::launch_scan_dense_ws(a, s));
+    }
+    if (hypic::scan_sd_bal_shape(a) && hypic::scan_sd_tc_supported(a)) {
+        if (!workspace || workspace_bytes < hypic::scan_sd_bal_bytes()) return HYPIC_EINVAL;
+        if (!aligned(workspace, 256)) return HYPIC_EALIGN;
+        a.ws = static_cast<float *>(workspace);
+        return from_cuda(hypic::launch_scan_sd_bal(a, s));
     }
     if (hypic::scan_sd_tc_supported(a)) return from_cuda(hypic::launch_scan_sd_tc(a, s));
     if (hypic::scan_dense_tc_supported(a)) return from_cuda(hypic::launch_scan_dense_tc(a, s));

@@ -58,6 +58,9 @@ cudaError_t launch_scan_recurrent(const ScanArgs &a, cudaStream_t s);
 // Scalar / diagonal scan on tcgen05 tensor cores (bf16 inputs, d_k = d_v = 128, no o_t).
 bool scan_sd_tc_supported(const ScanArgs &a);
 cudaError_t launch_scan_sd_tc(const ScanArgs &a, cudaStream_t s);
+bool scan_sd_bal_shape(const ScanArgs &a);        // the balanced schedule (scratch) takes it
+int64_t scan_sd_bal_bytes();                      // its scratch
+cudaError_t launch_scan_sd_bal(const ScanArgs &a, cudaStream_t s);
 
 // Gated delta rule scan on tcgen05 tensor cores (bf16 inputs, d_k = d_v = 128, no o_t).
 bool scan_dense_tc_supported(const ScanArgs &a);

@@ -91,15 +91,21 @@ def scan_ws(lib, fam=2, dtype=0, L=1, S=2, N=64, H=2, dk=128, dv=128, ws=0x40000
 
 def test_workspace_size_and_checks(lib):
     """The two-pass dense scan: one 17184-byte record (33808 with o_t) per
-    (layer, head, chunk slot), n_seg + N / 64 slots; other families and
-    options take none."""
+    (layer, head, chunk slot), n_seg + N / 64 slots; the balanced
+    diagonal scan: a fixed 2 x 512 partial slots; other options take none."""
     ws = lib.hypic_segment_scan_workspace_bytes
     assert ws(2, 0, 30, 1, 2048, 32, 128, 128, 0) == 30 * 32 * (1 + 32) * 17184
     assert ws(2, 0, 1, 3, 200, 2, 128, 128, 0) == 2 * (3 + 3) * 17184
     assert ws(2, 0, 1, 1, 2048, 2, 128, 128, 1) == 2 * (1 + 32) * 33808   # with o_t: Gq tiles and b_t too
     assert ws(2, 1, 1, 1, 2048, 2, 128, 128, 0) == 0     # fp32 inputs
     assert ws(2, 0, 1, 1, 2048, 2, 64, 64, 0) == 0
-    assert ws(0, 0, 1, 1, 2048, 2, 128, 128, 0) == 0
+    sd = 2 * 512 * (128 + 128 * 128) * 4      # diag: two partial slots per CTA, up to 512 CTAs
+    assert ws(1, 0, 1, 1, 2048, 2, 128, 128, 0) == sd
+    assert ws(1, 0, 30, 8, 8192, 32, 128, 128, 0) == sd
+    assert ws(0, 0, 1, 1, 2048, 2, 128, 128, 0) == 0     # scalar: one chain per CTA, no scratch
+    assert ws(1, 0, 1, 1, 2048, 2, 128, 128, 1) == 0     # o_t: the recurrent kernel
+    assert ws(1, 0, 1, 600, 2048, 2, 128, 128, 0) == 0   # more segments than the schedule indexes
+    assert ws(1, 0, 1, 1, 2048, 2, 64, 64, 0) == 0
     assert ws(2, 0, 1, 1, 2048, 0, 128, 128, 0) == EINVAL
     need = ws(2, 0, 1, 2, 64, 2, 128, 128, 0)
     assert scan_ws(lib, ws_bytes=need - 16) == EINVAL

@@ -219,14 +219,17 @@ def test_segment_independence_bitwise(fam):
     lens = [200, 77, 130]
     mk = wl.dense_stack if fam == DENSE else (lambda **kw: wl.scalar_diag(fam, **kw))
     w = mk(lengths=lens, n_layers=1, H=2, d=128, seed=11)
-    got = gpu_scan(w)
+    # the per-chain kernels (the balanced diagonal schedule splits chains
+    # by the batch's total work, so its rounding depends on the batch)
+    form = "auto" if fam == DENSE else None
+    got = gpu_scan(w, workspace=form)
     a, b = w["seg_offsets"][1], w["seg_offsets"][2]
     alone = dict(w)
     for key in ("k", "v", "alpha", "beta"):
         if w[key] is not None:
             alone[key] = np.ascontiguousarray(w[key][:, a:b])
     alone["seg_offsets"] = np.array([0, b - a], dtype=np.int64)
-    g1 = gpu_scan(alone)
+    g1 = gpu_scan(alone, workspace=form)
     for key in g1:
         assert torch.equal(g1[key][:, 0], got[key][:, 1]), key
 
@@ -248,6 +251,43 @@ def test_dense_ragged_batch_and_bad_offsets(form):
     assert torch.all(got["S"][:, -1] == 0)
     assert torch.all(got["lam"][:, -1] == 0)
     assert torch.equal(got["M"][:, -1], torch.eye(128, device="cuda").expand_as(got["M"][:, -1]))
+
+
+@pytest.mark.parametrize("fam", [DIAG], ids=["diag"])
+def test_balanced_schedule_matches_per_chain(fam):
+    """With scratch the diagonal scan splits all chains' chunks evenly
+    over two CTAs per SM and folds the pieces of chains that straddle CTAs
+    (S = T_late S_early + S_late).  It must match the oracle and the
+    one-chain-per-CTA kernel (rounding only), for ragged, empty and
+    one-token segments and for chains shorter and longer than a CTA's share."""
+    lens = [5000, 0, 1, 64, 65, 3000, 129, 7000, 33]
+    w = wl.scalar_diag(fam, lengths=lens, n_layers=2, H=7, d=128, seed=23)
+    bal = host(gpu_scan(w))
+    per = host(gpu_scan(w, workspace=None))
+    check(fam, bal, oracle_scan(w), TOL_SCAN_BF16)
+    # both forms sit ~1e-5 from the oracle; they round the weighted keys to bf16
+    # hi + lo at different weights (relative to the piece's end, not the segment's)
+    assert rel_fro(bal["S"], per["S"]).max() <= 1e-4
+    assert np.abs(bal["lam"] - per["lam"]).max() <= 1e-5 * max(1.0, float(np.abs(per["lam"]).max()))
+    assert np.all(bal["S"][:, 1] == 0) and np.all(bal["lam"][:, 1] == 0)
+    # a chain longer than several CTAs' shares: one long segment, one head
+    w1 = wl.scalar_diag(fam, lengths=[40000], n_layers=1, H=1, d=128, seed=24)
+    check(fam, host(gpu_scan(w1)), oracle_scan(w1), TOL_SCAN_BF16)
+
+
+@pytest.mark.parametrize("fam", [DIAG], ids=["diag"])
+def test_balanced_schedule_bad_offsets(fam):
+    """Offsets out of [0, N] on the balanced path: reported, segment empty."""
+    import torch
+    w = wl.scalar_diag(fam, lengths=[640, 64], n_layers=1, H=2, d=128, seed=3)
+    w["seg_offsets"] = np.array([0, 640, 5000], dtype=np.int64)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = gpu_scan(w, d_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == -5
+    assert torch.all(got["S"][:, 1] == 0) and torch.all(got["lam"][:, 1] == 0)
+    ref = oracle.sequential(fam, w["k"][:, :640], w["v"][:, :640], w["alpha"][:, :640])
+    check(fam, {"S": host(got)["S"][:, 0], "lam": host(got)["lam"][:, 0]}, ref, TOL_SCAN_BF16)
 
 
 def test_bad_offsets_flag_error_without_fault():
