@@ -344,7 +344,7 @@ def run_compose(args):
     import linear_attention_state_gated_gb300 as hy
     res = {}
     hbm, _, _, src = peaks()
-    n, H, d = 1920, 32, 128
+    n, H, d = args.compose_n, 32, 128
     dev = torch.device("cuda")
     g = torch.Generator(device=dev)
     g.manual_seed(5)
@@ -366,7 +366,7 @@ def run_compose(args):
         torch.cuda.synchronize()
         t = s.elapsed_time(e) / reps / 1e3
         by = n * H * (3 * 4 * d * d + (4 * d if fam == 1 else 4) + (4 * d * d if fam == 2 else 0))
-        res[name] = {"value": n / t, "unit": "composes/s (all 32 heads)", "ms": t * 1e3,
+        res[name] = {"value": n / t, "unit": "composes/s (all 32 heads)", "ms": t * 1e3, "items": n,
                      "roofline": {"bound": "hbm", "achieved": by / t / 1e9, "peak": hbm, "unit": "GB/s",
                                   "frac": by / t / 1e9 / hbm, "traffic": None, "peak_kind": f"copy, {src}"}}
         del M, lam
@@ -384,12 +384,13 @@ def run_chain(args):
     clen, idx = wl.rag_requests()
     dev = torch.device("cuda")
     cl, ix = torch.from_numpy(clen).to(dev), torch.from_numpy(idx).to(dev)
+    Lyr = args.chain_layers
     for fam, name in ((0, "scalar"), (1, "diag")):
-        pool = wl.rag_pool(fam)
+        pool = wl.rag_pool(fam, n_layers=Lyr)
         pl = torch.from_numpy(pool["lam"]).to(dev)
         pS = torch.from_numpy(pool["S"]).to(dev)
         del pool
-        R, Lyr, H, d = 64, 30, 32, 128
+        R, H, d = 64, 32, 128
         out = torch.empty((R, Lyr, H, d, d), dtype=torch.float32, device=dev)
         for _ in range(3):
             hy.compose_chain(fam, cl, ix, pl, pS, S_out=out)
@@ -407,6 +408,7 @@ def run_chain(args):
         lam_b = 4 * d if fam == 1 else 4
         by = n_steps * Lyr * H * (4 * d * d + lam_b) + R * Lyr * H * 4 * d * d
         res[name] = {"value": composes / t, "unit": "composes/s (all 32 heads)", "ms": t * 1e3,
+                     "layers": Lyr,
                      "roofline": {"bound": "hbm", "achieved": by / t / 1e9, "peak": hbm,
                                   "unit": "GB/s", "frac": by / t / 1e9 / hbm, "traffic": None,
                                   "peak_kind": f"copy, {src}"}}
@@ -582,6 +584,10 @@ def main():
     ap.add_argument("--dense-L", type=int, default=2048)
     ap.add_argument("--dense-form", choices=["two_pass", "single"], default="two_pass",
                     help="dense row: two passes over a workspace, or the single-pass kernel")
+    ap.add_argument("--compose-n", type=int, default=1920,
+                    help="compose row: items (64 requests x 30 layers by default)")
+    ap.add_argument("--chain-layers", type=int, default=30,
+                    help="RAG chain row: layers of the pool (30 by default)")
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
