@@ -25,7 +25,9 @@
 //   Delta^T = U^T - X0^T W^T    (X0 and W each split hi + lo: three products)
 //   X^T    += Delta~^T K        (Delta~ = Delta diag(b_C / b), split hi + lo)
 //   O1^T = X0^T Q^T (X0 hi + lo),  O2^T = Delta^T Gq^T (three products)
-// W and U are built by their own warps ahead of the state warps.
+// W and U are built by their own warps ahead of the state warps; one more warp
+// issues the state pass's products, starting on each half of X0 as soon as it
+// is converted.
 #include "dense_common.cuh"
 #include "internal.cuh"
 #include "sm100.cuh"
@@ -292,7 +294,7 @@ __global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_cons
 // ================================================================ pass 2: state
 
 constexpr int kNS = 2;            // stages
-constexpr int kThreads = 672;     // 21 warps: 0 TMA, 1-4 W/U operands, 5-20 state
+constexpr int kThreads = 704;     // 22 warps: 0 TMA, 1-4 W/U operands, 5-20 state, 21 MMA issue
 constexpr int kWT = 128;          // W warps' threads
 constexpr int kState = 512;       // state warps' threads
 
@@ -321,6 +323,7 @@ constexpr uint32_t kTo2 = 448;    // O2^T accumulator (64 columns, o_t)
 struct StateCtl {
     uint64_t full[kNS], empty[kNS];
     uint64_t aop_ready[2], wop_ready[2], wfree[2];   // per operand buffer
+    uint64_t xop_ready[2], dt_ready;                 // state warps -> MMA issuer
     uint64_t w_done, d_done, x_done;
     uint64_t drain[2];
     float redmax[16];
@@ -365,8 +368,9 @@ __device__ __forceinline__ void store_o(const ScanArgs &a, int h, uint32_t to1, 
     }
 }
 
+// 22 warps: six on some sub-partitions, 16384 / (6 x 32) registers -> at most 80 per thread
 template <bool O>
-__global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers per thread
+__global__ void __maxnreg__(80)
     dense_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_q, const ScanArgs a, int64_t slots) {
     using R = Rec<O>;
@@ -401,6 +405,9 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
             mbar_init(&ctl->wop_ready[b], kWT / 32);
             mbar_init(&ctl->wfree[b], 1);
         }
+        mbar_init(&ctl->xop_ready[0], kState / 32);
+        mbar_init(&ctl->xop_ready[1], kState / 32);
+        mbar_init(&ctl->dt_ready, kState / 32);
         mbar_init(&ctl->w_done, 1);
         mbar_init(&ctl->d_done, 1);
         mbar_init(&ctl->x_done, 1);
@@ -561,17 +568,19 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
             mma_commit(&ctl->drain[0]);
             mbar_wait(&ctl->drain[0], 0);
         }
-    } else {
+    } else if (warp < 21) {
         // ------------------------------------------------------------ state warps
         const int st = threadIdx.x - 160;           // 0..511
-        const bool issuer = st == 0;
         const int sw = warp - 5;                    // 0..15
         const int cg = sw >> 2;                     // column group of this warp
         const int quarter = warp & 3;               // TMEM lanes this warp may touch
         const int m = quarter * 32 + lane;          // column of X = TMEM lane
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const uint32_t tx = tmem + lane_off + kTx + (uint32_t)(cg * 32);
-        const uint32_t txop = tmem + lane_off + kTxop + (uint32_t)(cg * 16);
+        // this thread's X^T columns: k = p * 64 + cg * 16 .. +15 for the halves p = 0, 1,
+        // converted half by half so the issuer can start on half 0 while half 1 converts
+        const uint32_t tx0 = tmem + lane_off + kTx + (uint32_t)(cg * 16);
+        const uint32_t txop = tmem + lane_off + kTxop + (uint32_t)(cg * 8);   // hi (+32: half 1; +64: lo)
+        const uint32_t tdo = tmem + lane_off + kTxop + (uint32_t)(cg * 16);   // o_t: Delta^T hi / lo (tokens)
         const uint32_t tacc = tmem + lane_off + kTacc + (uint32_t)(cg * 16);
         const uint32_t to1 = tmem + lane_off + kTo1 + (uint32_t)(cg * 16);
         const uint32_t to2 = tmem + lane_off + kTo2 + (uint32_t)(cg * 16);
@@ -585,17 +594,19 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
         float ls = 0.f;
 
         {   // initial X^T: identity (transition) or zero (state)
-            uint32_t r[32];
+            uint32_t r[16];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint((half == 0 && cg * 32 + i == m) ? 1.f : 0.f);
-            tmem_st32(tx, r);
+            for (int p = 0; p < 2; ++p) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    r[i] = __float_as_uint((half == 0 && p * 64 + cg * 16 + i == m) ? 1.f : 0.f);
+                tmem_st16(tx0 + (uint32_t)(p * 64), r);
+            }
             tmem_wait_st();
         }
 
         for (int j = 0; j < nc; ++j) {
             const int s = j % kNS;
-            const int b = j % SM::NB;
-            const uint32_t use = (uint32_t)(j / SM::NB);
             const uint8_t *stg = smem + s * SM::Stage;
             const float *rec = reinterpret_cast<const float *>(stg + SM::Rec);
             bool ok = wait_or_abort(&ctl->full[s], (uint32_t)(j / kNS) & 1u, abortp);
@@ -605,21 +616,6 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
                 break;
             }
             tc_fence_after();
-            // ---- U^T = V^T (A diag(beta))^T into the accumulator (state half), on the
-            // tensor cores while the X operand is converted below
-            if (issuer && half) {
-                if (wait_or_abort(&ctl->aop_ready[b], use & 1u, abortp)) {
-                    tc_fence_after();
-                    const uint32_t vb = smem_addr(stg + SM::V), ab = smem_addr(smem + SM::Ab + b * 16384);
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        const uint64_t ad = smem_desc_sw128(vb + (uint32_t)ks * 2048u, kBox, 1024);
-                        mma_f16(tmem + kTacc, ad, smem_desc_sw128(ab + (uint32_t)ks * 32u, 0, 1024), id_wu, ks > 0);
-                        mma_f16(tmem + kTacc, ad, smem_desc_sw128(ab + 8192u + (uint32_t)ks * 32u, 0, 1024), id_wu,
-                                1u);
-                    }
-                }
-            }
             // ---- o_t of the previous chunk (its O1, O2 are complete: x_done)
             if (with_o && j > 0) store_o(a, h, to1, to2, ctl->bo, cg, m, row0 + (int64_t)(j - 1) * kC, kC);
             // ---- scales of this chunk
@@ -631,12 +627,15 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
             float fP, fD;         // X0_true = fP * g * X_stored;  Delta~ = fD * (b_C / b) * Delta
             if (half == 0) {
                 if (renorm) {
-                    uint32_t r[32];
-                    tmem_ld32(tx, r);
-                    tmem_wait_ld();
                     float mx = 0.f;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fabsf(__uint_as_float(r[i])));
+                    for (int p = 0; p < 2; ++p) {
+                        uint32_t r[16];
+                        tmem_ld16(tx0 + (uint32_t)(p * 64), r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) mx = fmaxf(mx, fabsf(__uint_as_float(r[i])));
+                    }
                     const int e = exponent_of(state_max(mx, ctl, sw, lane));
                     g = ldexpf(1.f, -e);
                     lam_exp += e;
@@ -663,54 +662,31 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
                     ls += LC;
                 }
             }
-            // ---- X round trip (TMEM only): operand X0_true (hi + lo), X_stored rescaled if due
+            // ---- X round trip (TMEM only), per k half: operand X0_true (hi + lo), X_stored
+            // rescaled if due; each half is announced as soon as it is in place
             {
                 const float mult = g * fP, sc = g * wscale;
-                uint32_t r[32], hi[16], lo[16];
-                tmem_ld32(tx, r);
-                tmem_wait_ld();
 #pragma unroll
-                for (int p = 0; p < 16; ++p)
-                    split_pair(mult * __uint_as_float(r[2 * p]), mult * __uint_as_float(r[2 * p + 1]), hi[p], lo[p]);
-                tmem_st16(txop, hi);
-                tmem_st16(txop + 64u, lo);
-                if (renorm) {
+                for (int p = 0; p < 2; ++p) {
+                    uint32_t r[16], hi[8], lo[8];
+                    tmem_ld16(tx0 + (uint32_t)(p * 64), r);
+                    tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(sc * __uint_as_float(r[i]));
-                    tmem_st32(tx, r);
-                }
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            bar_sync(2, kState);
-            // ---- Delta^T = U^T - X0^T W^T (three-term split); O1^T = X0^T Q^T
-            if (issuer) {
-                if (wait_or_abort(&ctl->wop_ready[b], use & 1u, abortp)) {
-                    tc_fence_after();
-                    const uint32_t wtile = smem_addr(smem + SM::Wt + b * 32768);
+                    for (int q = 0; q < 8; ++q)
+                        split_pair(mult * __uint_as_float(r[2 * q]), mult * __uint_as_float(r[2 * q + 1]), hi[q],
+                                   lo[q]);
+                    tmem_st8(txop + (uint32_t)(p * 32), hi);
+                    tmem_st8(txop + 64u + (uint32_t)(p * 32), lo);
+                    if (renorm) {
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint64_t bh = smem_desc_sw128(wtile + (uint32_t)ks * 2048u, 16384, 1024);
-                        const uint64_t bl = smem_desc_sw128(wtile + 16384u + (uint32_t)ks * 2048u, 16384, 1024);
-                        const uint32_t ah = tmem + kTxop + (uint32_t)ks * 8u, al = ah + 64u;
-                        mma_f16_ta(tmem + kTacc, ah, bh, id_d, (half || ks > 0) ? 1u : 0u);
-                        mma_f16_ta(tmem + kTacc, ah, bl, id_d, 1u);
-                        mma_f16_ta(tmem + kTacc, al, bh, id_d, 1u);
+                        for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(sc * __uint_as_float(r[i]));
+                        tmem_st16(tx0 + (uint32_t)(p * 64), r);
                     }
-                    if (with_o) {
-                        const uint32_t qb = smem_addr(stg + SM::Q);
-#pragma unroll
-                        for (int ks = 0; ks < 8; ++ks) {
-                            const uint64_t bq =
-                                smem_desc_sw128(qb + (uint32_t)(ks >> 2) * kBox + (uint32_t)(ks & 3) * 32u, 0, 1024);
-                            const uint32_t ah = tmem + kTxop + (uint32_t)ks * 8u;
-                            mma_f16_ta(tmem + kTo1, ah, bq, id_o, ks > 0);
-                            mma_f16_ta(tmem + kTo1, ah + 64u, bq, id_o, 1u);
-                        }
-                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ctl->xop_ready[p]);
                 }
-                mma_commit(&ctl->d_done);
-                mma_commit(&ctl->wfree[b]);
             }
             // ---- Delta~^T = fD Delta^T diag(b_C / b) -> bf16 hi / lo in place
             // (with o_t also Delta^T itself, hi / lo, into the X0 operand columns)
@@ -725,16 +701,16 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
                 tmem_wait_ld();
                 if (with_o) {
 #pragma unroll
-                    for (int p = 0; p < 8; ++p)
-                        split_pair(__uint_as_float(r[2 * p]), __uint_as_float(r[2 * p + 1]), hi[p], lo[p]);
-                    tmem_st8(txop, hi);
-                    tmem_st8(txop + 8u, lo);
+                    for (int q = 0; q < 8; ++q)
+                        split_pair(__uint_as_float(r[2 * q]), __uint_as_float(r[2 * q + 1]), hi[q], lo[q]);
+                    tmem_st8(tdo, hi);
+                    tmem_st8(tdo + 8u, lo);
                 }
 #pragma unroll
-                for (int p = 0; p < 8; ++p) {
-                    const int t = cg * 16 + 2 * p;
-                    split_pair(fD * rec[R::Gw + t] * __uint_as_float(r[2 * p]),
-                               fD * rec[R::Gw + t + 1] * __uint_as_float(r[2 * p + 1]), hi[p], lo[p]);
+                for (int q = 0; q < 8; ++q) {
+                    const int t = cg * 16 + 2 * q;
+                    split_pair(fD * rec[R::Gw + t] * __uint_as_float(r[2 * q]),
+                               fD * rec[R::Gw + t + 1] * __uint_as_float(r[2 * q + 1]), hi[q], lo[q]);
                 }
                 tmem_st8(tacc, hi);          // tokens cg*16 .. +15: hi in the first 8 columns,
                 tmem_st8(tacc + 8u, lo);     // lo in the next 8 (this thread's own columns)
@@ -742,38 +718,8 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
             }
             tmem_wait_st();
             tc_fence_before();
-            bar_sync(2, kState);
-            // ---- X^T += Delta~^T K (K as the MN-major B operand: row t, channels contiguous);
-            // O2^T = Delta^T Gq^T (three-term split)
-            if (issuer) {
-                tc_fence_after();
-                const uint32_t kb = smem_addr(stg + SM::K);
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    const uint64_t bd = smem_desc_sw128(kb + (uint32_t)ks * 2048u, kBox, 1024);
-                    const uint32_t ah = tmem + kTacc + (uint32_t)ks * 16u;
-                    mma_f16_ta(tmem + kTx, ah, bd, id_x, 1u);
-                    mma_f16_ta(tmem + kTx, ah + 8u, bd, id_x, 1u);
-                }
-                if (with_o) {
-                    const uint32_t gq = smem_addr(stg + SM::Rec + R::Gq * 4);
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        const uint64_t gh = smem_desc_sw128(gq + (uint32_t)ks * 32u, 0, 1024);
-                        const uint64_t gl = smem_desc_sw128(gq + 8192u + (uint32_t)ks * 32u, 0, 1024);
-                        const uint32_t ah = tmem + kTxop + (uint32_t)ks * 16u;
-                        mma_f16_ta(tmem + kTo2, ah, gh, id_o, ks > 0);
-                        mma_f16_ta(tmem + kTo2, ah, gl, id_o, 1u);
-                        mma_f16_ta(tmem + kTo2, ah + 8u, gh, id_o, 1u);
-                    }
-                }
-                mma_commit(&ctl->x_done);
-                mma_commit(&ctl->empty[s]);   // the stage is free once X (and O2) have read it
-            }
-        }
-        if (issuer && *abortp) {
-            mma_commit(&ctl->drain[1]);
-            mbar_wait(&ctl->drain[1], 0);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->dt_ready);
         }
 
         // ------------------------------------------------------------ epilogue
@@ -785,14 +731,17 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
                 store_o(a, h, to1, to2, ctl->bo, cg, m, row0 + (int64_t)(nc - 1) * kC,
                         (int)(t1 - t0 - (int64_t)(nc - 1) * kC));
             const int64_t u_out = ((int64_t)l * a.n_seg + seg) * a.H + h;
-            uint32_t r[32];
-            tmem_ld32(tx, r);
+            uint32_t r[2][16];
+            tmem_ld16(tx0, r[0]);
+            tmem_ld16(tx0 + 64u, r[1]);
             tmem_wait_ld();
             float scale;
             if (half == 0) {
                 float mx = 0.f;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fabsf(__uint_as_float(r[i])));
+                for (int p = 0; p < 2; ++p)
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) mx = fmaxf(mx, fabsf(__uint_as_float(r[p][i])));
                 const int e = exponent_of(state_max(mx, ctl, sw, lane));
                 scale = ldexpf(1.f, -e);
                 lam_exp += e;
@@ -802,9 +751,100 @@ __global__ void __launch_bounds__(kThreads, 1)   // 21 warps: <= 80 registers pe
             }
             float *out = (half == 0 ? a.M_out : a.S_out) + u_out * kD * kD;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) out[(int64_t)(cg * 32 + i) * kD + m] = scale * __uint_as_float(r[i]);
+            for (int p = 0; p < 2; ++p)
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    out[(int64_t)(p * 64 + cg * 16 + i) * kD + m] = scale * __uint_as_float(r[p][i]);
         } else {
             *abortp = 1;
+        }
+    } else if (lane == 0) {
+        // ------------------------------------------------------------ MMA issuer (warp 21)
+        for (int j = 0; j < nc; ++j) {
+            const int s = j % kNS;
+            const int b = j % SM::NB;
+            const uint32_t use = (uint32_t)(j / SM::NB);
+            const uint32_t par = (uint32_t)j & 1u;
+            const uint8_t *stg = smem + s * SM::Stage;
+            // the accumulator is free (the previous update has read Delta~), the chunk is in
+            if (j > 0 && !wait_or_abort(&ctl->x_done, par ^ 1u, abortp)) break;
+            if (!wait_or_abort(&ctl->full[s], (uint32_t)(j / kNS) & 1u, abortp)) break;
+            // ---- U^T = V^T (A diag(beta))^T into the accumulator (state half)
+            if (half) {
+                if (!wait_or_abort(&ctl->aop_ready[b], use & 1u, abortp)) break;
+                tc_fence_after();
+                const uint32_t vb = smem_addr(stg + SM::V), ab = smem_addr(smem + SM::Ab + b * 16384);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint64_t ad = smem_desc_sw128(vb + (uint32_t)ks * 2048u, kBox, 1024);
+                    mma_f16(tmem + kTacc, ad, smem_desc_sw128(ab + (uint32_t)ks * 32u, 0, 1024), id_wu, ks > 0);
+                    mma_f16(tmem + kTacc, ad, smem_desc_sw128(ab + 8192u + (uint32_t)ks * 32u, 0, 1024), id_wu, 1u);
+                }
+            }
+            // ---- Delta^T = U^T - X0^T W^T (three-term split), O1^T = X0^T Q^T, per k half
+            if (!wait_or_abort(&ctl->wop_ready[b], use & 1u, abortp)) break;
+            const uint32_t wtile = smem_addr(smem + SM::Wt + b * 32768);
+            bool ok = true;
+            for (int p = 0; p < 2 && ok; ++p) {
+                ok = wait_or_abort(&ctl->xop_ready[p], par, abortp);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kq = 0; kq < 4; ++kq) {
+                    const int ks = p * 4 + kq;
+                    const uint64_t bh = smem_desc_sw128(wtile + (uint32_t)ks * 2048u, 16384, 1024);
+                    const uint64_t bl = smem_desc_sw128(wtile + 16384u + (uint32_t)ks * 2048u, 16384, 1024);
+                    const uint32_t ah = tmem + kTxop + (uint32_t)ks * 8u, al = ah + 64u;
+                    mma_f16_ta(tmem + kTacc, ah, bh, id_d, (half || ks > 0) ? 1u : 0u);
+                    mma_f16_ta(tmem + kTacc, ah, bl, id_d, 1u);
+                    mma_f16_ta(tmem + kTacc, al, bh, id_d, 1u);
+                }
+                if (with_o) {
+                    const uint32_t qb = smem_addr(stg + SM::Q);
+#pragma unroll
+                    for (int kq = 0; kq < 4; ++kq) {
+                        const int ks = p * 4 + kq;
+                        const uint64_t bq =
+                            smem_desc_sw128(qb + (uint32_t)(ks >> 2) * kBox + (uint32_t)(ks & 3) * 32u, 0, 1024);
+                        const uint32_t ah = tmem + kTxop + (uint32_t)ks * 8u;
+                        mma_f16_ta(tmem + kTo1, ah, bq, id_o, ks > 0);
+                        mma_f16_ta(tmem + kTo1, ah + 64u, bq, id_o, 1u);
+                    }
+                }
+            }
+            if (!ok) break;
+            mma_commit(&ctl->d_done);
+            mma_commit(&ctl->wfree[b]);
+            // ---- X^T += Delta~^T K (K as the MN-major B operand: row t, channels contiguous);
+            // O2^T = Delta^T Gq^T (three-term split)
+            if (!wait_or_abort(&ctl->dt_ready, par, abortp)) break;
+            tc_fence_after();
+            const uint32_t kb = smem_addr(stg + SM::K);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                const uint64_t bd = smem_desc_sw128(kb + (uint32_t)ks * 2048u, kBox, 1024);
+                const uint32_t ah = tmem + kTacc + (uint32_t)ks * 16u;
+                mma_f16_ta(tmem + kTx, ah, bd, id_x, 1u);
+                mma_f16_ta(tmem + kTx, ah + 8u, bd, id_x, 1u);
+            }
+            if (with_o) {
+                const uint32_t gq = smem_addr(stg + SM::Rec + R::Gq * 4);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint64_t gh = smem_desc_sw128(gq + (uint32_t)ks * 32u, 0, 1024);
+                    const uint64_t gl = smem_desc_sw128(gq + 8192u + (uint32_t)ks * 32u, 0, 1024);
+                    const uint32_t ah = tmem + kTxop + (uint32_t)ks * 16u;
+                    mma_f16_ta(tmem + kTo2, ah, gh, id_o, ks > 0);
+                    mma_f16_ta(tmem + kTo2, ah, gl, id_o, 1u);
+                    mma_f16_ta(tmem + kTo2, ah + 8u, gh, id_o, 1u);
+                }
+            }
+            mma_commit(&ctl->x_done);
+            mma_commit(&ctl->empty[s]);   // the stage is free once X (and O2) have read it
+        }
+        if (*abortp) {   // drain: completes once this thread's MMAs are done
+            mma_commit(&ctl->drain[1]);
+            mbar_wait(&ctl->drain[1], 0);
         }
     }
 
