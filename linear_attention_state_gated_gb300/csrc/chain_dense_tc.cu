@@ -4,16 +4,20 @@
 //     S <- exp(lambda_p) M_p S + S_p,
 // one 128 x 128 x 128 product per step.  The product runs on the tensor cores
 // in bf16 with both operands split three ways (x = hi + mid + lo, residual
-// ~2^-27) and the six partial products down to order 2^-18 kept
-// (~2^-26 relative per product), which keeps the fp32 composition accurate to
-// well below 1e-5 at the cost of three TF32 products.  The exact fp32 running state stays in the math
-// warps' registers (row i of S on TMEM lane i, two warps per lane quarter).
-// Without a chain list (chain_len and seg_idx NULL) request r takes one step
-// with pool entry r: the single composition S = exp(lambda) M S_prev + S_C.
-// Warp 0 brings each M_p into shared memory by TMA (128-byte swizzle, so the
-// row-per-lane reads are conflict-free) while the previous step's MMAs run;
-// the math warps split it into TMEM as the A operand and split S into shared
-// memory as the MN-major B operand; warp 1 issues the MMAs.
+// ~2^-27) and the six partial products down to order 2^-16 kept (~2^-24
+// relative per product), which keeps the fp32 composition well inside 1e-5.
+// The exact fp32 running state stays in the math warps' registers (row i of S
+// on TMEM lane i, four warps per lane quarter, 32 columns each).
+//
+// Persistent: one CTA per SM walks its units (a unit is one chain; without a
+// chain list it is one composition S = exp(lambda) M S_prev + S_C) step after
+// step.  Warp 0 brings each M_p (lane 0) and S_p (lane 1) into shared memory by
+// TMA (128-byte swizzle, so the row-per-lane reads are conflict-free); the math
+// warps split M_p into one of two TMEM operand buffers -- the NEXT step's M_p
+// while the current step's products run -- and split S into shared memory as
+// the MN-major B operand; warp 1 issues the products.  While a unit's last
+// products run, the registers the state left prefetch the next unit's S_init,
+// and the last update goes straight to S_out.
 #include "internal.cuh"
 #include "sm100.cuh"
 
@@ -23,16 +27,19 @@ namespace {
 using namespace sm100;
 
 constexpr int kD = 128;
-constexpr int kThreads = 320;           // warp 0: TMA, warp 1: MMA, warps 2..9: math
-constexpr int kMath = 256;
-constexpr uint32_t kTa = 0, kTd = 256;  // TMEM: A hi / mid / lo at 0, 64, 128 (bf16 pairs); D at 256
+constexpr int kThreads = 576;           // warp 0: TMA, warp 1: MMA, warps 2..17: math
+constexpr int kMath = 512;
+constexpr uint32_t kTa = 0;             // TMEM: A buffers at 0 and 192 (hi / mid / lo at +0, +64, +128)
+constexpr uint32_t kTd = 384;           // D (128 columns)
 constexpr int kBpart = 32768;           // one bf16 B tile: 128 k-rows x 128 n, 2 atoms of 64 n
-constexpr int kMstage = 3 * kBpart;     // M_p, fp32, 4 boxes of 32 columns x 128 rows
-constexpr int kCtl = kMstage + 65536;
-constexpr int kSmem = kCtl + 1024 + 1024;
+constexpr int kMstage = 3 * kBpart;     // M_p stage, fp32, 4 boxes of 32 columns x 128 rows
+constexpr int kSstage = kMstage + 65536; // S_p stage, same layout
+constexpr int kCtl = kSstage + 65536;
+constexpr int kSmem = kCtl + 128 + 1024;
+static_assert(kSmem <= 232448, "fits in one SM's shared memory");
 
 struct ChainCtrl {
-    uint64_t mfull, mfree, ops_ready, d_done;
+    uint64_t mfull, mfree, sfull, sfree, ops_ready, d_done;
     uint32_t tmem;
     int abort;
 };
@@ -48,31 +55,51 @@ __device__ __forceinline__ void split3_pair(float x0, float x1, uint32_t &hi, ui
     lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-    chain_dense_tc_kernel(const __grid_constant__ CUtensorMap tm_m, const ChainArgs a) {
+// Steps of unit u (a chain of request r; one step without a chain list), clamped.
+__device__ __forceinline__ int unit_steps(const ChainArgs &a, int64_t u, bool flag) {
+    if (!a.chain_len) return 1;
+    const int r = (int)(u / ((int64_t)a.n_layers * a.H));
+    int n = a.chain_len[r];
+    if (n < 0 || n > a.max_chain) {
+        if (flag) flag_index_error(a.d_err);
+        n = n < 0 ? 0 : a.max_chain;
+    }
+    return n;
+}
+
+// Pool row (entry, layer, head) of step c of unit u, clamped.
+__device__ __forceinline__ int64_t step_entry(const ChainArgs &a, int64_t u, int c, bool flag) {
+    const int64_t lhn = (int64_t)a.n_layers * a.H;
+    const int r = (int)(u / lhn);
+    const int64_t lh = u % lhn;
+    int p = a.seg_idx ? a.seg_idx[(int64_t)r * a.max_chain + c] : r;
+    if (p < 0 || p >= a.P) {
+        if (flag) flag_index_error(a.d_err);
+        p = p < 0 ? 0 : a.P - 1;
+    }
+    return (int64_t)p * lhn + lh;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)   // 18 warps: <= 96 registers per thread
+    chain_dense_tc_kernel(const __grid_constant__ CUtensorMap tm_m, const __grid_constant__ CUtensorMap tm_s,
+                          const ChainArgs a, int64_t units) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~static_cast<uintptr_t>(1023));
+    uint8_t *smem = smem_align1024(smem_raw);
     ChainCtrl *ctl = reinterpret_cast<ChainCtrl *>(smem + kCtl);
     volatile int *abortp = &ctl->abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t u = blockIdx.x;                  // (r * Lyr + l) * H + h
-    const int r = (int)(u / ((int64_t)a.n_layers * a.H));
-    const int64_t lh = u % ((int64_t)a.n_layers * a.H);
 
-    int n = a.chain_len ? a.chain_len[r] : 1;   // no list: one step, entry r (a single composition)
-    if (n < 0 || n > a.max_chain) {
-        if (threadIdx.x == 0) flag_index_error(a.d_err);
-        n = n < 0 ? 0 : a.max_chain;
-    }
     if (threadIdx.x == 0) {
         mbar_init(&ctl->mfull, 1);
         mbar_init(&ctl->mfree, kMath / 32);
+        mbar_init(&ctl->sfull, 1);
+        mbar_init(&ctl->sfree, kMath / 32);
         mbar_init(&ctl->ops_ready, kMath / 32);
         mbar_init(&ctl->d_done, 1);
         ctl->abort = 0;
         mbar_fence_init();
         tma_prefetch(&tm_m);
+        tma_prefetch(&tm_s);
     }
     if (warp == 1) tmem_alloc(&ctl->tmem, 512);
     tc_fence_before();
@@ -80,150 +107,202 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = ctl->tmem;
 
-    auto entry = [&](int c) -> int64_t {   // pool entry of step c for this layer / head
-        int p = a.seg_idx ? a.seg_idx[(int64_t)r * a.max_chain + c] : r;
-        if (p < 0 || p >= a.P) {
-            flag_index_error(a.d_err);
-            p = p < 0 ? 0 : a.P - 1;
-        }
-        return (int64_t)p * a.n_layers * a.H + lh;
-    };
-
     if (warp == 0) {
-        if (lane == 0) {
-            int issued = 0;
-            for (int c = 0; c < n; ++c) {
-                if (c > 0 && (!mbar_wait(&ctl->mfree, (uint32_t)(c - 1) & 1u) || *abortp)) {
-                    *abortp = 1;
-                    break;
-                }
-                const int row = (int)(entry(c) * kD);
-                mbar_expect_tx(&ctl->mfull, 65536u);
+        // ------------------------------------------------------------ producers: M_p (lane 0), S_p (lane 1)
+        if (lane < 2) {
+            const CUtensorMap *tm = lane == 0 ? &tm_m : &tm_s;
+            uint64_t *full = lane == 0 ? &ctl->mfull : &ctl->sfull;
+            uint64_t *fre = lane == 0 ? &ctl->mfree : &ctl->sfree;
+            uint8_t *stage = smem + (lane == 0 ? kMstage : kSstage);
+            int64_t g = 0;   // steps of this CTA so far
+            for (int64_t u = blockIdx.x; u < units && !*abortp; u += gridDim.x) {
+                const int n = unit_steps(a, u, lane == 0);
+                for (int c = 0; c < n; ++c, ++g) {
+                    // the stage's previous step has been read (M_p split into TMEM / S_p used)
+                    if (g >= 1 && !mbar_wait(fre, (uint32_t)(g - 1) & 1u)) *abortp = 1;
+                    if (*abortp) break;
+                    const int row = (int)(step_entry(a, u, c, lane == 0) * kD);
+                    mbar_expect_tx(full, 65536u);
 #pragma unroll
-                for (int b = 0; b < 4; ++b) tma_load_3d(smem + kMstage + b * 16384, &tm_m, &ctl->mfull, 32 * b, 0, row);
-                issued = c + 1;
+                    for (int bx = 0; bx < 4; ++bx) tma_load_3d(stage + bx * 16384, tm, full, 32 * bx, 0, row);
+                }
             }
-            if (*abortp && issued > 0) mbar_wait(&ctl->mfull, (uint32_t)(issued - 1) & 1u);
+            if (*abortp && g > 0) mbar_wait(full, (uint32_t)(g - 1) & 1u);   // the last copy lands
         }
     } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(128, 128, false, true);   // A TMEM, B MN-major
             const uint32_t b0 = smem_addr(smem);
-            for (int c = 0; c < n; ++c) {
-                if (!mbar_wait(&ctl->ops_ready, (uint32_t)c & 1u) || *abortp) {
-                    *abortp = 1;
-                    break;
-                }
-                tc_fence_after();
+            int64_t g = 0;
+            for (int64_t u = blockIdx.x; u < units && !*abortp; u += gridDim.x) {
+                const int n = unit_steps(a, u, false);
+                for (int c = 0; c < n; ++c, ++g) {
+                    if (!mbar_wait(&ctl->ops_ready, (uint32_t)g & 1u) || *abortp) {
+                        *abortp = 1;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t abuf = tmem + kTa + (uint32_t)(g & 1) * 192u;
 #pragma unroll 2
-                for (int ks = 0; ks < 8; ++ks) {   // K = 128 in steps of 16 (two 8-row groups of B)
-                    const uint32_t off = (uint32_t)ks * 2048u;
-                    const uint64_t bh = smem_desc_sw128(b0 + off, 16384, 1024);
-                    const uint64_t bm = smem_desc_sw128(b0 + kBpart + off, 16384, 1024);
-                    const uint64_t bl = smem_desc_sw128(b0 + 2 * kBpart + off, 16384, 1024);
-                    const uint32_t ah = tmem + kTa + (uint32_t)ks * 8u, am = ah + 64u, al = ah + 128u;
-                    mma_f16_ta(tmem + kTd, ah, bh, idesc, ks > 0);
-                    mma_f16_ta(tmem + kTd, ah, bm, idesc, 1u);
-                    mma_f16_ta(tmem + kTd, am, bh, idesc, 1u);
-                    mma_f16_ta(tmem + kTd, ah, bl, idesc, 1u);
-                    mma_f16_ta(tmem + kTd, am, bm, idesc, 1u);
-                    mma_f16_ta(tmem + kTd, al, bh, idesc, 1u);
+                    for (int ks = 0; ks < 8; ++ks) {   // K = 128 in steps of 16 (two 8-row groups of B)
+                        const uint32_t off = (uint32_t)ks * 2048u;
+                        const uint64_t bh = smem_desc_sw128(b0 + off, 16384, 1024);
+                        const uint64_t bm = smem_desc_sw128(b0 + kBpart + off, 16384, 1024);
+                        const uint64_t bl = smem_desc_sw128(b0 + 2 * kBpart + off, 16384, 1024);
+                        const uint32_t ah = abuf + (uint32_t)ks * 8u, am = ah + 64u, al = ah + 128u;
+                        mma_f16_ta(tmem + kTd, ah, bh, idesc, ks > 0);
+                        mma_f16_ta(tmem + kTd, ah, bm, idesc, 1u);
+                        mma_f16_ta(tmem + kTd, am, bh, idesc, 1u);
+                        mma_f16_ta(tmem + kTd, ah, bl, idesc, 1u);
+                        mma_f16_ta(tmem + kTd, am, bm, idesc, 1u);
+                        mma_f16_ta(tmem + kTd, al, bh, idesc, 1u);
+                    }
+                    mma_commit(&ctl->d_done);
                 }
-                mma_commit(&ctl->d_done);
             }
-            if (*abortp) {
+            if (*abortp) {   // drain: completes once every issued MMA is done
                 mma_commit(&ctl->d_done);
-                mbar_wait(&ctl->d_done, (uint32_t)n & 1u);
+                mbar_wait(&ctl->d_done, (uint32_t)g & 1u);
             }
         }
     } else {
-        const int ch = (warp - 2) >> 2;              // column half: [64 ch, 64 ch + 64)
+        // ------------------------------------------------------------ math warps
+        const int cq = (warp - 2) >> 2;              // column quarter: [32 cq, 32 cq + 32)
         const int quarter = warp & 3;
         const int i = quarter * 32 + lane;           // row of S / of M_p
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        float srow[64];                              // exact running state, row i
-        {
-            const float4 *init = a.S_init ? reinterpret_cast<const float4 *>(a.S_init + u * kD * kD + i * kD + ch * 64)
-                                          : nullptr;
+        const int64_t DD = (int64_t)kD * kD;
+        float srow[32];                              // exact running state, row i, 32 columns
+
+        // split M_p of step g (stage g & 1) into TMEM operand buffer g & 1
+        auto split_m = [&](int64_t g) -> bool {
+            if (!bar_and(1, kMath, mbar_wait(&ctl->mfull, (uint32_t)g & 1u) && !*abortp)) return false;
+            const uint8_t *ms = smem + kMstage;
+            uint32_t hi[16], mid[16], lo[16];
 #pragma unroll
-            for (int q = 0; q < 16; ++q) {
+            for (int q = 0; q < 8; ++q) {
+                const int col = cq * 32 + 4 * q;
+                const int box = col >> 5, chunk = (col & 31) >> 2;
+                const float4 m4 =
+                    *reinterpret_cast<const float4 *>(ms + box * 16384 + i * 128 + ((chunk ^ (i & 7)) << 4));
+                split3_pair(m4.x, m4.y, hi[2 * q], mid[2 * q], lo[2 * q]);
+                split3_pair(m4.z, m4.w, hi[2 * q + 1], mid[2 * q + 1], lo[2 * q + 1]);
+            }
+            const uint32_t ab = tmem + lane_off + kTa + (uint32_t)(g & 1) * 192u + (uint32_t)(cq * 16);
+            tmem_st16(ab, hi);
+            tmem_st16(ab + 64u, mid);
+            tmem_st16(ab + 128u, lo);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->mfree);   // the stage may take the next step's M_p
+            return true;
+        };
+        // a unit without steps: S_out = S_init (or 0)
+        auto copy_init = [&](int64_t u) {
+            const float4 *init =
+                a.S_init ? reinterpret_cast<const float4 *>(a.S_init + u * DD + i * kD + cq * 32) : nullptr;
+            float4 *out = reinterpret_cast<float4 *>(a.S_out + u * DD + i * kD + cq * 32);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) out[q] = init ? init[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+        };
+
+        auto load_init = [&](int64_t uu) {   // S_init row of unit uu (or 0) into srow
+            const float4 *init =
+                a.S_init ? reinterpret_cast<const float4 *>(a.S_init + uu * DD + i * kD + cq * 32) : nullptr;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
                 const float4 v = init ? init[q] : make_float4(0.f, 0.f, 0.f, 0.f);
                 srow[4 * q] = v.x; srow[4 * q + 1] = v.y; srow[4 * q + 2] = v.z; srow[4 * q + 3] = v.w;
             }
-        }
-        for (int c = 0; c < n; ++c) {
-            const int64_t e = entry(c);
-            // A = M_p (bf16 hi / mid / lo pairs) -> TMEM, row i on lane i, column k / 2
-            if (!bar_and(1, kMath, mbar_wait(&ctl->mfull, (uint32_t)c & 1u) && !*abortp)) {
-                *abortp = 1;
-                break;
+        };
+        // the next unit of this CTA after uu that has steps (units without steps are written here)
+        auto next_unit = [&](int64_t uu) {
+            uu += gridDim.x;
+            while (uu < units && unit_steps(a, uu, false) == 0) {
+                copy_init(uu);
+                uu += gridDim.x;
             }
+            return uu;
+        };
+
+        int64_t g = 0;
+        bool ok = true;
+        int64_t u = next_unit((int64_t)blockIdx.x - gridDim.x);
+        if (u < units) {
+            load_init(u);
+            ok = split_m(0);   // the first step's operand
+        }
+        while (ok && u < units) {
+            const int n = unit_steps(a, u, false);
+            const int64_t un = next_unit(u);
+            for (int c = 0; c < n && ok; ++c, ++g) {
+                const bool last = c + 1 == n;
+                const int64_t e = step_entry(a, u, c, false);
+                // B = S (bf16 hi / mid / lo) -> shared memory, MN-major: row k = i, n contiguous,
+                // 2 atoms of 64 columns, 128-byte swizzle.  B is free: the last products are done.
 #pragma unroll
-            for (int cb = 0; cb < 2; ++cb) {             // 32 columns (16 packed pairs) at a time
-                uint32_t hi[16], mid[16], lo[16];
+                for (int q = 0; q < 4; ++q) {              // 8 columns (one 16-byte chunk) at a time
+                    const int chunk = (cq & 1) * 4 + q;
+                    const int off = (cq >> 1) * 16384 + i * 128 + ((chunk ^ (i & 7)) << 4);
+                    uint32_t h[4], md[4], l[4];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int col = ch * 64 + cb * 32 + 4 * q;
-                    const int box = col >> 5, chunk = (col & 31) >> 2;
-                    const float4 m4 = *reinterpret_cast<const float4 *>(smem + kMstage + box * 16384 + i * 128 +
-                                                                        ((chunk ^ (i & 7)) << 4));
-                    split3_pair(m4.x, m4.y, hi[2 * q], mid[2 * q], lo[2 * q]);
-                    split3_pair(m4.z, m4.w, hi[2 * q + 1], mid[2 * q + 1], lo[2 * q + 1]);
+                    for (int p = 0; p < 4; ++p)
+                        split3_pair(srow[8 * q + 2 * p], srow[8 * q + 2 * p + 1], h[p], md[p], l[p]);
+                    *reinterpret_cast<uint4 *>(smem + off) = make_uint4(h[0], h[1], h[2], h[3]);
+                    *reinterpret_cast<uint4 *>(smem + kBpart + off) = make_uint4(md[0], md[1], md[2], md[3]);
+                    *reinterpret_cast<uint4 *>(smem + 2 * kBpart + off) = make_uint4(l[0], l[1], l[2], l[3]);
                 }
-                const uint32_t col2 = (uint32_t)(ch * 32 + cb * 16);
-                tmem_st16(tmem + lane_off + kTa + col2, hi);
-                tmem_st16(tmem + lane_off + kTa + 64u + col2, mid);
-                tmem_st16(tmem + lane_off + kTa + 128u + col2, lo);
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->mfree);     // the stage may take the next M_p
-            // B = S (bf16 hi / mid / lo) -> shared memory, MN-major: row k = i, n contiguous,
-            // 2 atoms of 64 columns, 128-byte swizzle
+                tmem_wait_st();   // this step's A operand (split in the previous step) is in TMEM
+                fence_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->ops_ready);
+                // while the products run: the next step's M_p into the other operand buffer,
+                // and after a unit's last step the next unit's S_init into the freed registers
+                if ((!last || un < units) && !split_m(g + 1)) {
+                    ok = false;
+                    break;
+                }
+                if (last && un < units) load_init(un);
+                const float scale = expf(a.pool_lam[e]);
+                if (!bar_and(1, kMath,
+                             mbar_wait(&ctl->sfull, (uint32_t)g & 1u) && mbar_wait(&ctl->d_done, (uint32_t)g & 1u) &&
+                                 !*abortp)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // S <- scale D + S_p (S_p from the stage: box cq holds this thread's 32 columns),
+                // 16 columns at a time
+                const uint8_t *sp = smem + kSstage + cq * 16384 + i * 128;
+                float4 *out = reinterpret_cast<float4 *>(a.S_out + u * DD + i * kD + cq * 32);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {                  // 8 columns (one 16-byte chunk) at a time
-                const int chunk = q;                       // this thread's 64 columns are atom ch
-                const int off = ch * 16384 + i * 128 + ((chunk ^ (i & 7)) << 4);
-                uint32_t h[4], md[4], l[4];
+                for (int hb = 0; hb < 2; ++hb) {
+                    uint32_t dv[16];
+                    tmem_ld16(tmem + lane_off + kTd + (uint32_t)(cq * 32 + hb * 16), dv);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int p = 0; p < 4; ++p) split3_pair(srow[8 * q + 2 * p], srow[8 * q + 2 * p + 1], h[p], md[p], l[p]);
-                *reinterpret_cast<uint4 *>(smem + off) = make_uint4(h[0], h[1], h[2], h[3]);
-                *reinterpret_cast<uint4 *>(smem + kBpart + off) = make_uint4(md[0], md[1], md[2], md[3]);
-                *reinterpret_cast<uint4 *>(smem + 2 * kBpart + off) = make_uint4(l[0], l[1], l[2], l[3]);
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const int q = hb * 4 + q4;
+                        const float4 v = *reinterpret_cast<const float4 *>(sp + ((q ^ (i & 7)) << 4));
+                        const float4 r = make_float4(fmaf(scale, __uint_as_float(dv[4 * q4]), v.x),
+                                                     fmaf(scale, __uint_as_float(dv[4 * q4 + 1]), v.y),
+                                                     fmaf(scale, __uint_as_float(dv[4 * q4 + 2]), v.z),
+                                                     fmaf(scale, __uint_as_float(dv[4 * q4 + 3]), v.w));
+                        if (last) {
+                            out[q] = r;
+                        } else {
+                            srow[4 * q] = r.x; srow[4 * q + 1] = r.y; srow[4 * q + 2] = r.z; srow[4 * q + 3] = r.w;
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->sfree);   // the stage may take the next step's S_p
             }
-            tmem_wait_st();
-            fence_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->ops_ready);
-            // this step's S_p row and decay, loaded while the MMAs run
-            const float scale = expf(a.pool_lam[e]);
-            const float4 *sp = reinterpret_cast<const float4 *>(a.pool_S + e * kD * kD + i * kD + ch * 64);
-#pragma unroll
-            for (int q = 0; q < 16; ++q) {
-                const float4 v = __ldcs(sp + q);
-                srow[4 * q] = v.x; srow[4 * q + 1] = v.y; srow[4 * q + 2] = v.z; srow[4 * q + 3] = v.w;
-            }
-            if (!bar_and(1, kMath, mbar_wait(&ctl->d_done, (uint32_t)c & 1u) && !*abortp)) {
-                *abortp = 1;
-                break;
-            }
-            tc_fence_after();
-#pragma unroll
-            for (int cb = 0; cb < 2; ++cb) {
-                uint32_t dv[32];
-                tmem_ld32(tmem + lane_off + kTd + (uint32_t)(ch * 64 + cb * 32), dv);
-                tmem_wait_ld();
-#pragma unroll
-                for (int t = 0; t < 32; ++t) srow[cb * 32 + t] = fmaf(scale, __uint_as_float(dv[t]), srow[cb * 32 + t]);
-            }
-            tc_fence_before();
+            u = un;
         }
-        if (!*abortp) {
-            float4 *out = reinterpret_cast<float4 *>(a.S_out + u * kD * kD + i * kD + ch * 64);
-#pragma unroll
-            for (int q = 0; q < 16; ++q)
-                out[q] = make_float4(srow[4 * q], srow[4 * q + 1], srow[4 * q + 2], srow[4 * q + 3]);
-        }
+        if (!ok) *abortp = 1;
     }
 
     tc_fence_before();
@@ -245,14 +324,21 @@ bool chain_dense_tc_supported(const ChainArgs &a) {
 cudaError_t launch_chain_dense_tc(const ChainArgs &a, cudaStream_t s) {
     const int64_t units = (int64_t)a.R * a.n_layers * a.H;
     if (units == 0) return cudaSuccess;
-    CUtensorMap tm;
+    CUtensorMap tm, ts;
     const uint64_t rows = (uint64_t)a.P * a.n_layers * a.H * 128;
     if (!make_tensor_map_3d(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.pool_M, 128, 1, rows, 32, 128,
+                            CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map_3d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.pool_S, 128, 1, rows, 32, 128,
                             CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(chain_dense_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    chain_dense_tc_kernel<<<(unsigned)units, kThreads, kSmem, s>>>(tm, a);
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int64_t grid = units < sms ? units : sms;   // persistent: one CTA per SM
+    chain_dense_tc_kernel<<<(unsigned)grid, kThreads, kSmem, s>>>(tm, ts, a, units);
     return cudaGetLastError();
 }
 
