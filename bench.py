@@ -258,10 +258,32 @@ def run_headline(args, rank, world):
     h2d = sum(t.numel() * t.element_size() for fam in (0, 1) for t in host[fam].values())
     d2h = sum(t.numel() * t.element_size() for fam in (0, 1) for t in res_host[fam].values())
 
+    # host -> device copies spread over several streams (one copy stream does not fill
+    # the host link), each family's scan waits for its own inputs only
+    n_cs = 4
+    cstreams = [torch.cuda.Stream() for _ in range(n_cs)]
+    main = torch.cuda.current_stream()
+
     def e2e_step():
+        ready = {}
         for fam in (0, 1):
-            for key in devt[fam]:
-                devt[fam][key].copy_(host[fam][key], non_blocking=True)
+            evs = []
+            for j, key in enumerate(devt[fam]):
+                src, dst = host[fam][key].view(-1), devt[fam][key].view(-1)
+                parts = n_cs if dst.numel() >= (1 << 20) * n_cs else 1
+                bounds = [dst.numel() * q // parts for q in range(parts + 1)]
+                for q in range(parts):
+                    cs = cstreams[(j + q) % n_cs]
+                    cs.wait_stream(main)           # the previous step's scan has read the buffer
+                    with torch.cuda.stream(cs):
+                        dst[bounds[q]:bounds[q + 1]].copy_(src[bounds[q]:bounds[q + 1]], non_blocking=True)
+                        ev = torch.cuda.Event()
+                        ev.record(cs)
+                        evs.append(ev)
+            ready[fam] = evs
+        for fam in (0, 1):
+            for ev in ready[fam]:
+                main.wait_event(ev)
             hy.segment_scan(fam, devt[fam]["k"], devt[fam]["v"], devt[fam]["alpha"],
                             devt[fam]["offs"], out=outs[fam], workspace=wsb[fam])
             for key in outs[fam]:
