@@ -106,7 +106,7 @@ int hypic_segment_scan(int fam, int in_dtype, int n_layers, int n_seg,
  * (then its workspace may be NULL).  A negative hypic_status on bad counts.
  * Today the scratch is used with bf16 inputs and d_k = d_v = 128 by
  *   the dense family: one record per (layer, head, 64-token chunk slot) of
- *     17184 bytes (33808 bytes with o_t), n_layers * n_heads * (n_seg +
+ *     33568 bytes (33808 bytes with o_t), n_layers * n_heads * (n_seg +
  *     total_tokens / 64) records;
  *   the diagonal family without o_t and with n_seg <= 512: 2 x 512 partial
  *     states of 66048 bytes (67.6 MB), for a schedule that spreads all
@@ -153,7 +153,7 @@ int hypic_segment_scan_ws(int fam, int in_dtype, int n_layers, int n_seg,
  *   Arguments as hypic_segment_scan without q / o_out.  Only fam = HYPIC_DENSE,
  *   in_dtype = HYPIC_BF16, d_k = d_v = 128 is served; other inputs, or a problem
  *   whose records need more than the 64 MiB (hypic_segment_scan_workspace_bytes
- *   gives the need; 64 MiB hold 3905 records of 17184 bytes), return
+ *   gives the need; 64 MiB hold 1999 records of 33568 bytes), return
  *   HYPIC_EUNSUPPORTED and launch nothing.
  *   The scratch's contents never need to start at zero.  It is one array per
  *   device for the whole process: two calls in flight at the same time (other

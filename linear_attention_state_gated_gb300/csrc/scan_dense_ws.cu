@@ -47,11 +47,17 @@ constexpr int kBox = kC * 128;   // 64 channels x 64 tokens, bf16: 8 KB
 
 // ---------------------------------------------------------------- workspace record
 // One record per (layer, head, chunk slot), floats:
+//   without o_t:
+//   [0, 4096)        A diag(beta b) as bf16 hi / lo operand tiles (row t, s
+//                    contiguous, 128-byte swizzle), 8 KB each
+//   [4096, 8192)     A diag(beta), the same way
+//   with o_t:
 //   [0, 4096)        A = (I + L)^-1, row t at 64 t; the 16-byte group g of row t is
 //                    stored at group position g ^ (t & 15) (conflict-free row reads)
-//   [4096, 8192)     with o_t only: Gq as bf16 hi / lo operand tiles (row t, s
-//                    contiguous, 128-byte swizzle), 8 KB each
-//   G + t            b_C / b_t        (G = 4096, or 8192 with o_t)
+//   [4096, 8192)     Gq as bf16 hi / lo operand tiles (row t, s contiguous,
+//                    128-byte swizzle), 8 KB each
+//   then (G = 8192)
+//   G + t            b_C / b_t
 //   G + 64 + t       beta_t b_t
 //   G + 128 + t      beta_t
 //   G + 192, G + 193 log b_C, b_C
@@ -61,11 +67,12 @@ constexpr int kBox = kC * 128;   // 64 channels x 64 tokens, bf16: 8 KB
 // n_seg + floor(N / 64) of them.
 template <bool O>
 struct Rec {
-    static constexpr int A = 0, Gq = 4096;
-    static constexpr int G = O ? 8192 : 4096;
+    static constexpr int A = 0, Gq = 4096;   // with o_t
+    static constexpr int Abb = 0, Ab = 4096;  // without o_t
+    static constexpr int G = 8192;
     static constexpr int Gw = G, Gbb = G + 64, Gbeta = G + 128, LC = G + 192, BC = G + 193, B = G + 196;
     static constexpr int Floats = O ? G + 260 : G + 200;   // multiples of 4 floats
-    static constexpr int Bytes = Floats * 4;               // 17184 / 33808
+    static constexpr int Bytes = Floats * 4;               // 33568 / 33808
 };
 
 __host__ __device__ inline int64_t n_slots(int64_t N, int n_seg) { return (int64_t)n_seg + N / kC; }
@@ -87,7 +94,7 @@ static_assert(kPTw >= 4 * kBox, "the Gram operands end before the temporaries");
 struct PrepCtl {
     uint64_t full, mma;
     uint32_t tmem;
-    float gl[kC], gbeta[kC];
+    float gl[kC], gbeta[kC], gbb[kC];
 };
 constexpr int kPSmem = kPCtl + (int)sizeof(PrepCtl) + 1024;
 
@@ -166,6 +173,7 @@ __global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_cons
             const float bt = expf(inc[q]);
             ctl->gl[t] = inc[q];
             ctl->gbeta[t] = pb[q];
+            ctl->gbb[t] = pb[q] * bt;
             rec[R::Gw + t] = expf(total - inc[q]);
             rec[R::Gbb + t] = pb[q] * bt;
             rec[R::Gbeta + t] = pb[q];
@@ -265,6 +273,40 @@ __global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_cons
         }
         __syncthreads();
         dense::tri_inverse<kPThreads, 1, false>(Lw, Aw, Tw, tid);
+        if (!O) {
+            // ---- A diag(beta b) and A diag(beta) -> bf16 hi / lo tiles in the record (row t,
+            // 8-column group c at 16-byte position c ^ (t & 7); zero above the diagonal blocks)
+            uint8_t *tiles = reinterpret_cast<uint8_t *>(rec + R::Abb);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int f = tid + kPThreads * i;   // 0 .. 511
+                const int tt = f >> 3, c = f & 7;
+                float x[8];
+                if ((c >> 1) > (tt >> 4)) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) x[e] = 0.f;
+                } else {
+                    const float4 x0 = *reinterpret_cast<const float4 *>(Aw + tt * kLd + c * 8);
+                    const float4 x1 = *reinterpret_cast<const float4 *>(Aw + tt * kLd + c * 8 + 4);
+                    x[0] = x0.x; x[1] = x0.y; x[2] = x0.z; x[3] = x0.w;
+                    x[4] = x1.x; x[5] = x1.y; x[6] = x1.z; x[7] = x1.w;
+                }
+                const int off = tt * 128 + ((c ^ (tt & 7)) << 4);
+                uint32_t hv[4], lv[4];
+#pragma unroll
+                for (int p = 0; p < 4; ++p)
+                    split_pair(x[2 * p] * ctl->gbb[c * 8 + 2 * p], x[2 * p + 1] * ctl->gbb[c * 8 + 2 * p + 1], hv[p],
+                               lv[p]);
+                *reinterpret_cast<uint4 *>(tiles + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                *reinterpret_cast<uint4 *>(tiles + 8192 + off) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+#pragma unroll
+                for (int p = 0; p < 4; ++p)
+                    split_pair(x[2 * p] * ctl->gbeta[c * 8 + 2 * p], x[2 * p + 1] * ctl->gbeta[c * 8 + 2 * p + 1],
+                               hv[p], lv[p]);
+                *reinterpret_cast<uint4 *>(tiles + 16384 + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                *reinterpret_cast<uint4 *>(tiles + 24576 + off) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+            }
+        } else {
         // ---- A -> the record (16-byte groups, swizzled by row; zero above the diagonal blocks)
         float4 v[8];   // all loads before the first store
 #pragma unroll
@@ -280,6 +322,7 @@ __global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_cons
             const int tt = f >> 4, g = f & 15;
             *reinterpret_cast<float4 *>(rec + R::A + tt * 64 + ((g ^ (tt & 15)) << 2)) = v[i];
         }
+        }
     } else if (tid == 0 && a.d_err) {
         atomicExch(a.d_err, (int)HYPIC_ETIMEOUT);
     }
@@ -294,21 +337,27 @@ __global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_cons
 // ================================================================ pass 2: state
 
 constexpr int kNS = 2;            // stages
-constexpr int kThreads = 704;     // 22 warps: 0 TMA, 1-4 W/U operands, 5-20 state, 21 MMA issue
+// 22 or 23 warps: 0 TMA, 1-4 W/U operands, 5-20 state, 21 MMA issue, and without
+// o_t 22: a second MMA-issue warp for the second k half of Delta (a single thread
+// issues N = 64 products at about one per 60 cycles; two threads nearly double that)
+template <bool O>
+constexpr int state_threads() { return O ? 704 : 736; }
 constexpr int kWT = 128;          // W warps' threads
 constexpr int kState = 512;       // state warps' threads
 
 // stage: K (two 64-channel boxes), V (state half), Q (o_t), the chunk's record;
-// then the -W^T and A diag(beta) operand tiles (two buffers without o_t, one
-// with).  A diag(beta b) is written over the record's A once it is read.
+// then the -W^T operand tiles (two buffers without o_t, one with) and, with o_t,
+// the A diag(beta) tiles, built from the record's fp32 A (A diag(beta b) is
+// written over that A once it is read).  Without o_t both A tiles come ready in
+// the record.
 template <bool O>
 struct Smem {
     static constexpr int K = 0, V = 2 * kBox, Q = 4 * kBox, Rec = (O ? 6 : 4) * kBox;
     static constexpr int Stage = Rec + ((hypic::Rec<O>::Bytes + 1023) / 1024) * 1024;
     static constexpr int NB = O ? 1 : 2;               // operand buffers
     static constexpr int Wt = kNS * Stage;             // -W^T, per buffer hi / lo (128 rows x 128 B each)
-    static constexpr int Ab = Wt + NB * 32768;         // A diag(beta), per buffer hi / lo (64 x 128 B each)
-    static constexpr int Ctl = Ab + NB * 16384;
+    static constexpr int Ab = Wt + NB * 32768;         // with o_t: A diag(beta), hi / lo (64 x 128 B each)
+    static constexpr int Ctl = Ab + (O ? NB * 16384 : 0);
 };
 
 // TMEM column map (512 allocated)
@@ -319,13 +368,14 @@ constexpr uint32_t kTacc = 256;   // U^T - X0^T W^T, then Delta~^T operand in pl
 constexpr uint32_t kTw = 320;     // W^T accumulator (64 columns)
 constexpr uint32_t kTo1 = 384;    // O1^T accumulator (64 columns, o_t)
 constexpr uint32_t kTo2 = 448;    // O2^T accumulator (64 columns, o_t)
+constexpr uint32_t kTacc2 = 384;  // without o_t: the second k half of X0^T W^T (64 columns)
 
 struct StateCtl {
     uint64_t full[kNS], empty[kNS];
     uint64_t aop_ready[2], wop_ready[2], wfree[2];   // per operand buffer
     uint64_t xop_ready[2], dt_ready;                 // state warps -> MMA issuer
     uint64_t w_done, d_done, x_done;
-    uint64_t drain[2];
+    uint64_t drain[3];
     float redmax[16];
     float bo[kC];          // b_t of the chunk whose o_t is pending
     uint32_t tmem;
@@ -368,7 +418,7 @@ __device__ __forceinline__ void store_o(const ScanArgs &a, int h, uint32_t to1, 
     }
 }
 
-// 22 warps: six on some sub-partitions, 16384 / (6 x 32) registers -> at most 80 per thread
+// 22 or 23 warps: six on some sub-partitions, 16384 / (6 x 32) registers -> at most 80 per thread
 template <bool O>
 __global__ void __maxnreg__(80)
     dense_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -403,16 +453,15 @@ __global__ void __maxnreg__(80)
         for (int b = 0; b < 2; ++b) {
             mbar_init(&ctl->aop_ready[b], kWT / 32);
             mbar_init(&ctl->wop_ready[b], kWT / 32);
-            mbar_init(&ctl->wfree[b], 1);
+            mbar_init(&ctl->wfree[b], O ? 1 : 2);   // every issuer of Delta products commits
         }
         mbar_init(&ctl->xop_ready[0], kState / 32);
         mbar_init(&ctl->xop_ready[1], kState / 32);
         mbar_init(&ctl->dt_ready, kState / 32);
         mbar_init(&ctl->w_done, 1);
-        mbar_init(&ctl->d_done, 1);
+        mbar_init(&ctl->d_done, O ? 1 : 2);
         mbar_init(&ctl->x_done, 1);
-        mbar_init(&ctl->drain[0], 1);
-        mbar_init(&ctl->drain[1], 1);
+        for (int d = 0; d < 3; ++d) mbar_init(&ctl->drain[d], 1);
         ctl->abort = 0;
         mbar_fence_init();
         tma_prefetch(&tm_k);
@@ -439,8 +488,10 @@ __global__ void __maxnreg__(80)
                 if (!wait_or_abort(&ctl->empty[s], ((uint32_t)(j / kNS) & 1u) ^ 1u, abortp)) break;
                 uint8_t *st = smem + s * SM::Stage;
                 const int row = (int)(row0 + (int64_t)j * kC);
-                mbar_expect_tx(&ctl->full[s],
-                               (uint32_t)((2 + (half ? 2 : 0) + (with_o ? 2 : 0)) * kBox + R::Bytes));
+                // the transition half without o_t takes A diag(beta b) and the gates only
+                const bool whole = O || half;
+                const uint32_t rbytes = whole ? (uint32_t)R::Bytes : 16384u + (uint32_t)(R::Floats - R::G) * 4u;
+                mbar_expect_tx(&ctl->full[s], (uint32_t)((2 + (half ? 2 : 0) + (with_o ? 2 : 0)) * kBox) + rbytes);
                 tma_load_3d(st + SM::K, &tm_k, &ctl->full[s], 0, h, row);
                 tma_load_3d(st + SM::K + kBox, &tm_k, &ctl->full[s], 64, h, row);
                 if (half) {   // V only feeds the state half
@@ -451,7 +502,13 @@ __global__ void __maxnreg__(80)
                     tma_load_3d(st + SM::Q, &tm_q, &ctl->full[s], 0, h, row);
                     tma_load_3d(st + SM::Q + kBox, &tm_q, &ctl->full[s], 64, h, row);
                 }
-                bulk_load(st + SM::Rec, recs + (int64_t)j * R::Floats, (uint32_t)R::Bytes, &ctl->full[s]);
+                const float *rj = recs + (int64_t)j * R::Floats;
+                if (whole) {
+                    bulk_load(st + SM::Rec, rj, (uint32_t)R::Bytes, &ctl->full[s]);
+                } else {
+                    bulk_load(st + SM::Rec, rj, 16384u, &ctl->full[s]);
+                    bulk_load(st + SM::Rec + R::G * 4, rj + R::G, (uint32_t)(R::Floats - R::G) * 4u, &ctl->full[s]);
+                }
                 issued = j + 1;
             }
             if (*abortp)
@@ -476,9 +533,9 @@ __global__ void __maxnreg__(80)
                 *abortp = 1;
                 break;
             }
-            // ---- A diag(beta b) (over the record's A) and A diag(beta) -> bf16 hi / lo
-            // tiles (row t, s contiguous, 128-byte swizzle)
-            {
+            // ---- with o_t: A diag(beta b) (over the record's A) and A diag(beta) -> bf16
+            // hi / lo tiles (row t, s contiguous, 128-byte swizzle)
+            if (O) {
                 const int t = wt & 63, cb = (wt >> 6) * 4;   // four 8-column groups per thread
                 float av[4][8];
 #pragma unroll
@@ -515,10 +572,12 @@ __global__ void __maxnreg__(80)
                     }
                 }
             }
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->aop_ready[b]);
-            bar_sync(1, kWT);
+            if (O) {
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->aop_ready[b]);
+                bar_sync(1, kWT);
+            }
             // ---- W^T = K^T (A diag(beta b))^T
             if (issuer) {
                 tc_fence_after();
@@ -610,15 +669,7 @@ __global__ void __maxnreg__(80)
             const uint8_t *stg = smem + s * SM::Stage;
             const float *rec = reinterpret_cast<const float *>(stg + SM::Rec);
             bool ok = wait_or_abort(&ctl->full[s], (uint32_t)(j / kNS) & 1u, abortp);
-            if (j > 0) ok = ok && wait_or_abort(&ctl->x_done, (uint32_t)(j - 1) & 1u, abortp);
-            if (!bar_and(2, kState, ok)) {
-                *abortp = 1;
-                break;
-            }
-            tc_fence_after();
-            // ---- o_t of the previous chunk (its O1, O2 are complete: x_done)
-            if (with_o && j > 0) store_o(a, h, to1, to2, ctl->bo, cg, m, row0 + (int64_t)(j - 1) * kC, kC);
-            // ---- scales of this chunk
+            // ---- scales of this chunk, from its record (while the previous update runs)
             const float LC = rec[R::LC];                // log of the chunk's total decay
             const bool slow = LC < -40.f;
             const bool renorm = slow || (half == 0 ? (j % 8 == 0) : (ls < -20.f));
@@ -626,24 +677,10 @@ __global__ void __maxnreg__(80)
             float wscale = 1.f;
             float fP, fD;         // X0_true = fP * g * X_stored;  Delta~ = fD * (b_C / b) * Delta
             if (half == 0) {
-                if (renorm) {
-                    float mx = 0.f;
-#pragma unroll
-                    for (int p = 0; p < 2; ++p) {
-                        uint32_t r[16];
-                        tmem_ld16(tx0 + (uint32_t)(p * 64), r);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) mx = fmaxf(mx, fabsf(__uint_as_float(r[i])));
-                    }
-                    const int e = exponent_of(state_max(mx, ctl, sw, lane));
-                    g = ldexpf(1.f, -e);
-                    lam_exp += e;
-                }
                 wscale = slow ? rec[R::BC] : 1.f;
                 fP = 1.f;
                 fD = slow ? 1.f : expf(-LC);
-                if (!slow) lam_d += (double)LC;
+                if (!slow && st == 0) lam_d += (double)LC;   // only this thread writes lambda
             } else {
                 if (slow) {
                     g = expf(ls);
@@ -661,6 +698,28 @@ __global__ void __maxnreg__(80)
                     fD = expf(-(ls + LC));
                     ls += LC;
                 }
+            }
+            if (j > 0) ok = ok && wait_or_abort(&ctl->x_done, (uint32_t)(j - 1) & 1u, abortp);
+            if (!bar_and(2, kState, ok)) {
+                *abortp = 1;
+                break;
+            }
+            tc_fence_after();
+            // ---- o_t of the previous chunk (its O1, O2 are complete: x_done)
+            if (with_o && j > 0) store_o(a, h, to1, to2, ctl->bo, cg, m, row0 + (int64_t)(j - 1) * kC, kC);
+            if (half == 0 && renorm) {   // the transition's power-of-two renormalisation
+                float mx = 0.f;
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    uint32_t r[16];
+                    tmem_ld16(tx0 + (uint32_t)(p * 64), r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) mx = fmaxf(mx, fabsf(__uint_as_float(r[i])));
+                }
+                const int e = exponent_of(state_max(mx, ctl, sw, lane));
+                g = ldexpf(1.f, -e);
+                lam_exp += e;
             }
             // ---- X round trip (TMEM only), per k half: operand X0_true (hi + lo), X_stored
             // rescaled if due; each half is announced as soon as it is in place
@@ -698,6 +757,13 @@ __global__ void __maxnreg__(80)
             {
                 uint32_t r[16], hi[8], lo[8];
                 tmem_ld16(tacc, r);
+                if (!O) {   // plus the second k half's accumulator
+                    uint32_t r2[16];
+                    tmem_ld16(tacc + (kTacc2 - kTacc), r2);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) r[q] = __float_as_uint(__uint_as_float(r[q]) + __uint_as_float(r2[q]));
+                }
                 tmem_wait_ld();
                 if (with_o) {
 #pragma unroll
@@ -758,6 +824,38 @@ __global__ void __maxnreg__(80)
         } else {
             *abortp = 1;
         }
+    } else if (!O && warp == 22) {
+        // ------------------------------------------------------------ second MMA issuer (no o_t):
+        // the second k half of X0^T W^T into its own accumulator
+        if (lane == 0) {
+            for (int j = 0; j < nc; ++j) {
+                const int b = j % SM::NB;
+                const uint32_t use = (uint32_t)(j / SM::NB);
+                const uint32_t par = (uint32_t)j & 1u;
+                // its accumulator has been read (Delta~ of the previous chunk is converted)
+                if (j > 0 && !wait_or_abort(&ctl->x_done, par ^ 1u, abortp)) break;
+                if (!wait_or_abort(&ctl->wop_ready[b], use & 1u, abortp)) break;
+                if (!wait_or_abort(&ctl->xop_ready[1], par, abortp)) break;
+                tc_fence_after();
+                const uint32_t wtile = smem_addr(smem + SM::Wt + b * 32768);
+#pragma unroll
+                for (int kq = 0; kq < 4; ++kq) {
+                    const int ks = 4 + kq;
+                    const uint64_t bh = smem_desc_sw128(wtile + (uint32_t)ks * 2048u, 16384, 1024);
+                    const uint64_t bl = smem_desc_sw128(wtile + 16384u + (uint32_t)ks * 2048u, 16384, 1024);
+                    const uint32_t ah = tmem + kTxop + (uint32_t)ks * 8u, al = ah + 64u;
+                    mma_f16_ta(tmem + kTacc2, ah, bh, id_d, kq > 0 ? 1u : 0u);
+                    mma_f16_ta(tmem + kTacc2, ah, bl, id_d, 1u);
+                    mma_f16_ta(tmem + kTacc2, al, bh, id_d, 1u);
+                }
+                mma_commit(&ctl->d_done);
+                mma_commit(&ctl->wfree[b]);
+            }
+            if (*abortp) {   // drain: completes once this thread's MMAs are done
+                mma_commit(&ctl->drain[2]);
+                mbar_wait(&ctl->drain[2], 0);
+            }
+        }
     } else if (lane == 0) {
         // ------------------------------------------------------------ MMA issuer (warp 21)
         for (int j = 0; j < nc; ++j) {
@@ -771,9 +869,10 @@ __global__ void __maxnreg__(80)
             if (!wait_or_abort(&ctl->full[s], (uint32_t)(j / kNS) & 1u, abortp)) break;
             // ---- U^T = V^T (A diag(beta))^T into the accumulator (state half)
             if (half) {
-                if (!wait_or_abort(&ctl->aop_ready[b], use & 1u, abortp)) break;
+                if (O && !wait_or_abort(&ctl->aop_ready[b], use & 1u, abortp)) break;
                 tc_fence_after();
-                const uint32_t vb = smem_addr(stg + SM::V), ab = smem_addr(smem + SM::Ab + b * 16384);
+                const uint32_t vb = smem_addr(stg + SM::V);
+                const uint32_t ab = O ? smem_addr(smem + SM::Ab + b * 16384) : smem_addr(stg + SM::Rec + R::Ab * 4);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
                     const uint64_t ad = smem_desc_sw128(vb + (uint32_t)ks * 2048u, kBox, 1024);
@@ -785,7 +884,7 @@ __global__ void __maxnreg__(80)
             if (!wait_or_abort(&ctl->wop_ready[b], use & 1u, abortp)) break;
             const uint32_t wtile = smem_addr(smem + SM::Wt + b * 32768);
             bool ok = true;
-            for (int p = 0; p < 2 && ok; ++p) {
+            for (int p = 0; p < (O ? 2 : 1) && ok; ++p) {   // without o_t the second half is warp 22's
                 ok = wait_or_abort(&ctl->xop_ready[p], par, abortp);
                 if (!ok) break;
                 tc_fence_after();
@@ -878,7 +977,7 @@ cudaError_t launch_two_pass(const ScanArgs &a, cudaStream_t s) {
                                                                                                      slots);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    dense_state_kernel<O><<<(unsigned)(2 * units), kThreads, state_smem<O>(), s>>>(mk, mv, mq, a, slots);
+    dense_state_kernel<O><<<(unsigned)(2 * units), state_threads<O>(), state_smem<O>(), s>>>(mk, mv, mq, a, slots);
     return cudaGetLastError();
 }
 
