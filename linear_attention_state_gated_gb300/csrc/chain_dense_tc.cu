@@ -15,9 +15,12 @@
 // TMA (128-byte swizzle, so the row-per-lane reads are conflict-free); the math
 // warps split M_p into one of two TMEM operand buffers -- the NEXT step's M_p
 // while the current step's products run -- and split S into shared memory as
-// the MN-major B operand; warp 1 issues the products.  While a unit's last
-// products run, the registers the state left prefetch the next unit's S_init,
-// and the last update goes straight to S_out.
+// the MN-major B operand; warp 1 issues the products.  Each unit's S_init comes
+// through the M_p stage too (one more TMA fill, after the unit's first M_p, in
+// flight during the previous unit's last products and update); the last update
+// is written over S_p in its stage and leaves by TMA store.
+// All global traffic of the state thus moves by TMA, none through per-thread
+// row loads and stores.
 #include "internal.cuh"
 #include "sm100.cuh"
 
@@ -82,6 +85,7 @@ __device__ __forceinline__ int64_t step_entry(const ChainArgs &a, int64_t u, int
 
 __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: <= 96 registers per thread
     chain_dense_tc_kernel(const __grid_constant__ CUtensorMap tm_m, const __grid_constant__ CUtensorMap tm_s,
+                          const __grid_constant__ CUtensorMap tm_i, const __grid_constant__ CUtensorMap tm_o,
                           const ChainArgs a, int64_t units) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_align1024(smem_raw);
@@ -100,6 +104,8 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: <= 96 registers pe
         mbar_fence_init();
         tma_prefetch(&tm_m);
         tma_prefetch(&tm_s);
+        if (a.S_init) tma_prefetch(&tm_i);
+        tma_prefetch(&tm_o);
     }
     if (warp == 1) tmem_alloc(&ctl->tmem, 512);
     tc_fence_before();
@@ -108,26 +114,50 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: <= 96 registers pe
     const uint32_t tmem = ctl->tmem;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ producers: M_p (lane 0), S_p (lane 1)
-        if (lane < 2) {
-            const CUtensorMap *tm = lane == 0 ? &tm_m : &tm_s;
-            uint64_t *full = lane == 0 ? &ctl->mfull : &ctl->sfull;
-            uint64_t *fre = lane == 0 ? &ctl->mfree : &ctl->sfree;
-            uint8_t *stage = smem + (lane == 0 ? kMstage : kSstage);
+        // ------------------------------------------------------------ producers: M_p and S_init (lane 0), S_p (lane 1)
+        if (lane == 0) {
+            // fills of the M_p stage, in the order the math warps take them: the first
+            // unit's S_init, then per unit its M_p in step order with the unit's S_init
+            // after its first M_p (for the first unit: before it)
+            uint32_t f = 0;
+            bool first = true;
+            auto fill = [&](const CUtensorMap *tm, int row) -> bool {
+                if (f >= 1 && !mbar_wait(&ctl->mfree, (f - 1) & 1u)) *abortp = 1;
+                if (*abortp) return false;
+                mbar_expect_tx(&ctl->mfull, 65536u);
+#pragma unroll
+                for (int bx = 0; bx < 4; ++bx)
+                    tma_load_3d(smem + kMstage + bx * 16384, tm, &ctl->mfull, 32 * bx, 0, row);
+                ++f;
+                return true;
+            };
+            for (int64_t u = blockIdx.x; u < units && !*abortp; u += gridDim.x) {
+                const int n = unit_steps(a, u, true);
+                if (n == 0) continue;   // the math warps copy S_init over
+                if (first && a.S_init && !fill(&tm_i, (int)(u * kD))) break;
+                for (int c = 0; c < n; ++c) {
+                    if (!fill(&tm_m, (int)(step_entry(a, u, c, true) * kD))) break;
+                    if (c == 0 && !first && a.S_init && !fill(&tm_i, (int)(u * kD))) break;
+                }
+                first = false;
+            }
+            if (*abortp && f > 0) mbar_wait(&ctl->mfull, (f - 1) & 1u);   // the last copy lands
+        } else if (lane == 1) {
             int64_t g = 0;   // steps of this CTA so far
             for (int64_t u = blockIdx.x; u < units && !*abortp; u += gridDim.x) {
-                const int n = unit_steps(a, u, lane == 0);
+                const int n = unit_steps(a, u, false);
                 for (int c = 0; c < n; ++c, ++g) {
-                    // the stage's previous step has been read (M_p split into TMEM / S_p used)
-                    if (g >= 1 && !mbar_wait(fre, (uint32_t)(g - 1) & 1u)) *abortp = 1;
+                    // the stage's previous step is done with (S_p read, a result stored from it)
+                    if (g >= 1 && !mbar_wait(&ctl->sfree, (uint32_t)(g - 1) & 1u)) *abortp = 1;
                     if (*abortp) break;
-                    const int row = (int)(step_entry(a, u, c, lane == 0) * kD);
-                    mbar_expect_tx(full, 65536u);
+                    const int row = (int)(step_entry(a, u, c, false) * kD);
+                    mbar_expect_tx(&ctl->sfull, 65536u);
 #pragma unroll
-                    for (int bx = 0; bx < 4; ++bx) tma_load_3d(stage + bx * 16384, tm, full, 32 * bx, 0, row);
+                    for (int bx = 0; bx < 4; ++bx)
+                        tma_load_3d(smem + kSstage + bx * 16384, &tm_s, &ctl->sfull, 32 * bx, 0, row);
                 }
             }
-            if (*abortp && g > 0) mbar_wait(full, (uint32_t)(g - 1) & 1u);   // the last copy lands
+            if (*abortp && g > 0) mbar_wait(&ctl->sfull, (uint32_t)(g - 1) & 1u);   // the last copy lands
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -174,10 +204,11 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: <= 96 registers pe
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const int64_t DD = (int64_t)kD * kD;
         float srow[32];                              // exact running state, row i, 32 columns
+        uint32_t f = 0;                              // fills of the M_p stage taken (parity)
 
-        // split M_p of step g (stage g & 1) into TMEM operand buffer g & 1
+        // split M_p of step g (the stage's next fill) into TMEM operand buffer g & 1
         auto split_m = [&](int64_t g) -> bool {
-            if (!bar_and(1, kMath, mbar_wait(&ctl->mfull, (uint32_t)g & 1u) && !*abortp)) return false;
+            if (!bar_and(1, kMath, mbar_wait(&ctl->mfull, f & 1u) && !*abortp)) return false;
             const uint8_t *ms = smem + kMstage;
             uint32_t hi[16], mid[16], lo[16];
 #pragma unroll
@@ -194,7 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: <= 96 registers pe
             tmem_st16(ab + 64u, mid);
             tmem_st16(ab + 128u, lo);
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->mfree);   // the stage may take the next step's M_p
+            if (lane == 0) mbar_arrive(&ctl->mfree);   // the stage may take its next fill
+            ++f;
             return true;
         };
         // a unit without steps: S_out = S_init (or 0)
@@ -206,14 +238,23 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: <= 96 registers pe
             for (int q = 0; q < 8; ++q) out[q] = init ? init[q] : make_float4(0.f, 0.f, 0.f, 0.f);
         };
 
-        auto load_init = [&](int64_t uu) {   // S_init row of unit uu (or 0) into srow
-            const float4 *init =
-                a.S_init ? reinterpret_cast<const float4 *>(a.S_init + uu * DD + i * kD + cq * 32) : nullptr;
+        auto load_init = [&]() -> bool {   // S_init row of the next unit (the stage's next fill, or 0) into srow
+            if (!a.S_init) {
+#pragma unroll
+                for (int q = 0; q < 32; ++q) srow[q] = 0.f;
+                return true;
+            }
+            if (!bar_and(1, kMath, mbar_wait(&ctl->mfull, f & 1u) && !*abortp)) return false;
+            const uint8_t *ms = smem + kMstage + cq * 16384 + i * 128;   // box cq: this thread's 32 columns
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
-                const float4 v = init ? init[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float4 v = *reinterpret_cast<const float4 *>(ms + ((q ^ (i & 7)) << 4));
                 srow[4 * q] = v.x; srow[4 * q + 1] = v.y; srow[4 * q + 2] = v.z; srow[4 * q + 3] = v.w;
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->mfree);
+            ++f;
+            return true;
         };
         // the next unit of this CTA after uu that has steps (units without steps are written here)
         auto next_unit = [&](int64_t uu) {
@@ -228,10 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: <= 96 registers pe
         int64_t g = 0;
         bool ok = true;
         int64_t u = next_unit((int64_t)blockIdx.x - gridDim.x);
-        if (u < units) {
-            load_init(u);
-            ok = split_m(0);   // the first step's operand
-        }
+        if (u < units) ok = load_init() && split_m(0);   // the first unit's state, its first step's operand
         while (ok && u < units) {
             const int n = unit_steps(a, u, false);
             const int64_t un = next_unit(u);
@@ -257,13 +295,11 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: <= 96 registers pe
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ctl->ops_ready);
-                // while the products run: the next step's M_p into the other operand buffer,
-                // and after a unit's last step the next unit's S_init into the freed registers
+                // while the products run: the next step's M_p into the other operand buffer
                 if ((!last || un < units) && !split_m(g + 1)) {
                     ok = false;
                     break;
                 }
-                if (last && un < units) load_init(un);
                 const float scale = expf(a.pool_lam[e]);
                 if (!bar_and(1, kMath,
                              mbar_wait(&ctl->sfull, (uint32_t)g & 1u) && mbar_wait(&ctl->d_done, (uint32_t)g & 1u) &&
@@ -274,8 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: <= 96 registers pe
                 tc_fence_after();
                 // S <- scale D + S_p (S_p from the stage: box cq holds this thread's 32 columns),
                 // 16 columns at a time
-                const uint8_t *sp = smem + kSstage + cq * 16384 + i * 128;
-                float4 *out = reinterpret_cast<float4 *>(a.S_out + u * DD + i * kD + cq * 32);
+                uint8_t *sp = smem + kSstage + cq * 16384 + i * 128;
 #pragma unroll
                 for (int hb = 0; hb < 2; ++hb) {
                     uint32_t dv[16];
@@ -289,20 +324,38 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: <= 96 registers pe
                                                      fmaf(scale, __uint_as_float(dv[4 * q4 + 1]), v.y),
                                                      fmaf(scale, __uint_as_float(dv[4 * q4 + 2]), v.z),
                                                      fmaf(scale, __uint_as_float(dv[4 * q4 + 3]), v.w));
-                        if (last) {
-                            out[q] = r;
+                        if (last) {   // in place: the stage then leaves by TMA store
+                            *reinterpret_cast<float4 *>(sp + ((q ^ (i & 7)) << 4)) = r;
                         } else {
                             srow[4 * q] = r.x; srow[4 * q + 1] = r.y; srow[4 * q + 2] = r.z; srow[4 * q + 3] = r.w;
                         }
                     }
                 }
                 tc_fence_before();
+                if (last) {
+                    fence_async_smem();    // the results, visible to the TMA store
+                    bar_sync(1, kMath);
+                    if (threadIdx.x == 64) {
+#pragma unroll
+                        for (int bx = 0; bx < 4; ++bx)
+                            tma_store_3d(&tm_o, smem + kSstage + bx * 16384, 32 * bx, 0, (int)(u * kD));
+                        bulk_commit();
+                        bulk_wait_read_all();   // the stage is read: it may take the next S_p
+                    }
+                }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ctl->sfree);   // the stage may take the next step's S_p
+                // after a unit's last step: the next unit's S_init (its fill has been in flight
+                // since the next unit's first M_p was split)
+                if (last && un < units && !load_init()) {
+                    ok = false;
+                    break;
+                }
             }
             u = un;
         }
         if (!ok) *abortp = 1;
+        if (threadIdx.x == 64) bulk_wait_all();   // the stores of S_out are complete
     }
 
     tc_fence_before();
@@ -317,19 +370,27 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: <= 96 registers pe
 }  // namespace
 
 bool chain_dense_tc_supported(const ChainArgs &a) {
+    const int64_t units = (int64_t)a.R * a.n_layers * a.H;
     return a.fam == HYPIC_DENSE && a.dk == 128 && a.dv == 128 && a.P > 0 &&
-           (int64_t)a.P * a.n_layers * a.H * 128 < ((int64_t)1 << 31) && tensor_map_encoder() != nullptr;
+           (int64_t)a.P * a.n_layers * a.H * 128 < ((int64_t)1 << 31) && units * 128 < ((int64_t)1 << 31) &&
+           tensor_map_encoder() != nullptr;
 }
 
 cudaError_t launch_chain_dense_tc(const ChainArgs &a, cudaStream_t s) {
     const int64_t units = (int64_t)a.R * a.n_layers * a.H;
     if (units == 0) return cudaSuccess;
-    CUtensorMap tm, ts;
-    const uint64_t rows = (uint64_t)a.P * a.n_layers * a.H * 128;
+    CUtensorMap tm, ts, ti, to;
+    const uint64_t rows = (uint64_t)a.P * a.n_layers * a.H * 128, urows = (uint64_t)units * 128;
     if (!make_tensor_map_3d(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.pool_M, 128, 1, rows, 32, 128,
                             CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tensor_map_3d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.pool_S, 128, 1, rows, 32, 128,
+                            CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map_3d(&to, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.S_out, 128, 1, urows, 32, 128,
                             CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    ti = to;   // unused without S_init
+    if (a.S_init && !make_tensor_map_3d(&ti, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.S_init, 128, 1, urows, 32, 128,
+                                        CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(chain_dense_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
@@ -338,7 +399,7 @@ cudaError_t launch_chain_dense_tc(const ChainArgs &a, cudaStream_t s) {
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     const int64_t grid = units < sms ? units : sms;   // persistent: one CTA per SM
-    chain_dense_tc_kernel<<<(unsigned)grid, kThreads, kSmem, s>>>(tm, ts, a, units);
+    chain_dense_tc_kernel<<<(unsigned)grid, kThreads, kSmem, s>>>(tm, ts, ti, to, a, units);
     return cudaGetLastError();
 }
 
