@@ -47,32 +47,30 @@ constexpr int kBox = kC * 128;   // 64 channels x 64 tokens, bf16: 8 KB
 
 // ---------------------------------------------------------------- workspace record
 // One record per (layer, head, chunk slot), floats:
-//   without o_t:
 //   [0, 4096)        A diag(beta b) as bf16 hi / lo operand tiles (row t, s
 //                    contiguous, 128-byte swizzle), 8 KB each
 //   [4096, 8192)     A diag(beta), the same way
-//   with o_t:
-//   [0, 4096)        A = (I + L)^-1, row t at 64 t; the 16-byte group g of row t is
-//                    stored at group position g ^ (t & 15) (conflict-free row reads)
-//   [4096, 8192)     Gq as bf16 hi / lo operand tiles (row t, s contiguous,
-//                    128-byte swizzle), 8 KB each
-//   then (G = 8192)
-//   G + t            b_C / b_t
+//   G + t            b_C / b_t        (G = 8192)
 //   G + 64 + t       beta_t b_t
 //   G + 128 + t      beta_t
 //   G + 192, G + 193 log b_C, b_C
-//   G + 196 + t      with o_t only: b_t
-// Chunk j of segment s (tokens from t0) uses slot s + floor(t0 / 64) + j, so the
-// slots of different segments never collide and a (layer, head) needs at most
-// n_seg + floor(N / 64) of them.
+//   with o_t only:
+//   G + 196 + t      b_t
+//   [G + 260, +4096) Gq as bf16 hi / lo operand tiles (row t, s contiguous,
+//                    128-byte swizzle), 8 KB each
+// The state pass stages the head of a record (all but Gq) with the chunk's keys;
+// Gq has a buffer of its own.  Chunk j of segment s (tokens from t0) uses slot
+// s + floor(t0 / 64) + j, so the slots of different segments never collide and a
+// (layer, head) needs at most n_seg + floor(N / 64) of them.
 template <bool O>
 struct Rec {
-    static constexpr int A = 0, Gq = 4096;   // with o_t
-    static constexpr int Abb = 0, Ab = 4096;  // without o_t
-    static constexpr int G = 8192;
+    static constexpr int Abb = 0, Ab = 4096, G = 8192;
     static constexpr int Gw = G, Gbb = G + 64, Gbeta = G + 128, LC = G + 192, BC = G + 193, B = G + 196;
-    static constexpr int Floats = O ? G + 260 : G + 200;   // multiples of 4 floats
-    static constexpr int Bytes = Floats * 4;               // 33568 / 33808
+    static constexpr int Head = O ? G + 260 : G + 200;     // floats staged with the chunk (multiples of 4)
+    static constexpr int Gq = G + 260;                      // with o_t
+    static constexpr int Floats = O ? Gq + 4096 : Head;
+    static constexpr int Bytes = Floats * 4;                // 33568 / 50192
+    static constexpr int HeadBytes = Head * 4;              // 33568 / 33808
 };
 
 __host__ __device__ inline int64_t n_slots(int64_t N, int n_seg) { return (int64_t)n_seg + N / kC; }
@@ -273,7 +271,7 @@ __global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_cons
         }
         __syncthreads();
         dense::tri_inverse<kPThreads, 1, false>(Lw, Aw, Tw, tid);
-        if (!O) {
+        {
             // ---- A diag(beta b) and A diag(beta) -> bf16 hi / lo tiles in the record (row t,
             // 8-column group c at 16-byte position c ^ (t & 7); zero above the diagonal blocks)
             uint8_t *tiles = reinterpret_cast<uint8_t *>(rec + R::Abb);
@@ -306,22 +304,6 @@ __global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_cons
                 *reinterpret_cast<uint4 *>(tiles + 16384 + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
                 *reinterpret_cast<uint4 *>(tiles + 24576 + off) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
             }
-        } else {
-        // ---- A -> the record (16-byte groups, swizzled by row; zero above the diagonal blocks)
-        float4 v[8];   // all loads before the first store
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int f = tid + kPThreads * i;   // 0 .. 1023
-            const int tt = f >> 4, g = f & 15;
-            v[i] = (g >> 2) > (tt >> 4) ? make_float4(0.f, 0.f, 0.f, 0.f)
-                                        : *reinterpret_cast<const float4 *>(Aw + tt * kLd + g * 4);
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int f = tid + kPThreads * i;
-            const int tt = f >> 4, g = f & 15;
-            *reinterpret_cast<float4 *>(rec + R::A + tt * 64 + ((g ^ (tt & 15)) << 2)) = v[i];
-        }
         }
     } else if (tid == 0 && a.d_err) {
         atomicExch(a.d_err, (int)HYPIC_ETIMEOUT);
@@ -345,19 +327,17 @@ constexpr int state_threads() { return O ? 704 : 736; }
 constexpr int kWT = 128;          // W warps' threads
 constexpr int kState = 512;       // state warps' threads
 
-// stage: K (two 64-channel boxes), V (state half), Q (o_t), the chunk's record;
-// then the -W^T operand tiles (two buffers without o_t, one with) and, with o_t,
-// the A diag(beta) tiles, built from the record's fp32 A (A diag(beta b) is
-// written over that A once it is read).  Without o_t both A tiles come ready in
-// the record.
+// stage: K (two 64-channel boxes), V (state half), Q (o_t), the head of the
+// chunk's record (A tiles, gates); then, with o_t, one Gq buffer; then the -W^T
+// operand tiles (two buffers without o_t, one with).
 template <bool O>
 struct Smem {
     static constexpr int K = 0, V = 2 * kBox, Q = 4 * kBox, Rec = (O ? 6 : 4) * kBox;
-    static constexpr int Stage = Rec + ((hypic::Rec<O>::Bytes + 1023) / 1024) * 1024;
+    static constexpr int Stage = Rec + ((hypic::Rec<O>::HeadBytes + 1023) / 1024) * 1024;
     static constexpr int NB = O ? 1 : 2;               // operand buffers
-    static constexpr int Wt = kNS * Stage;             // -W^T, per buffer hi / lo (128 rows x 128 B each)
-    static constexpr int Ab = Wt + NB * 32768;         // with o_t: A diag(beta), hi / lo (64 x 128 B each)
-    static constexpr int Ctl = Ab + (O ? NB * 16384 : 0);
+    static constexpr int Gqb = kNS * Stage;            // with o_t: Gq hi / lo (64 x 128 B each)
+    static constexpr int Wt = Gqb + (O ? 16384 : 0);   // -W^T, per buffer hi / lo (128 rows x 128 B each)
+    static constexpr int Ctl = Wt + NB * 32768;
 };
 
 // TMEM column map (512 allocated)
@@ -372,7 +352,8 @@ constexpr uint32_t kTacc2 = 384;  // without o_t: the second k half of X0^T W^T 
 
 struct StateCtl {
     uint64_t full[kNS], empty[kNS];
-    uint64_t aop_ready[2], wop_ready[2], wfree[2];   // per operand buffer
+    uint64_t wop_ready[2], wfree[2];                 // per operand buffer
+    uint64_t gfull;                                  // o_t: Gq of the next chunk is in
     uint64_t xop_ready[2], dt_ready;                 // state warps -> MMA issuer
     uint64_t w_done, d_done, x_done;
     uint64_t drain[3];
@@ -451,7 +432,6 @@ __global__ void __maxnreg__(80)
             mbar_init(&ctl->empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&ctl->aop_ready[b], kWT / 32);
             mbar_init(&ctl->wop_ready[b], kWT / 32);
             mbar_init(&ctl->wfree[b], O ? 1 : 2);   // every issuer of Delta products commits
         }
@@ -462,6 +442,7 @@ __global__ void __maxnreg__(80)
         mbar_init(&ctl->d_done, O ? 1 : 2);
         mbar_init(&ctl->x_done, 1);
         for (int d = 0; d < 3; ++d) mbar_init(&ctl->drain[d], 1);
+        mbar_init(&ctl->gfull, 1);
         ctl->abort = 0;
         mbar_fence_init();
         tma_prefetch(&tm_k);
@@ -488,9 +469,8 @@ __global__ void __maxnreg__(80)
                 if (!wait_or_abort(&ctl->empty[s], ((uint32_t)(j / kNS) & 1u) ^ 1u, abortp)) break;
                 uint8_t *st = smem + s * SM::Stage;
                 const int row = (int)(row0 + (int64_t)j * kC);
-                // the transition half without o_t takes A diag(beta b) and the gates only
-                const bool whole = O || half;
-                const uint32_t rbytes = whole ? (uint32_t)R::Bytes : 16384u + (uint32_t)(R::Floats - R::G) * 4u;
+                // the transition half takes A diag(beta b) and the gates only
+                const uint32_t rbytes = half ? (uint32_t)R::HeadBytes : 16384u + (uint32_t)(R::Head - R::G) * 4u;
                 mbar_expect_tx(&ctl->full[s], (uint32_t)((2 + (half ? 2 : 0) + (with_o ? 2 : 0)) * kBox) + rbytes);
                 tma_load_3d(st + SM::K, &tm_k, &ctl->full[s], 0, h, row);
                 tma_load_3d(st + SM::K + kBox, &tm_k, &ctl->full[s], 64, h, row);
@@ -503,17 +483,28 @@ __global__ void __maxnreg__(80)
                     tma_load_3d(st + SM::Q + kBox, &tm_q, &ctl->full[s], 64, h, row);
                 }
                 const float *rj = recs + (int64_t)j * R::Floats;
-                if (whole) {
-                    bulk_load(st + SM::Rec, rj, (uint32_t)R::Bytes, &ctl->full[s]);
+                if (half) {
+                    bulk_load(st + SM::Rec, rj, (uint32_t)R::HeadBytes, &ctl->full[s]);
                 } else {
                     bulk_load(st + SM::Rec, rj, 16384u, &ctl->full[s]);
-                    bulk_load(st + SM::Rec + R::G * 4, rj + R::G, (uint32_t)(R::Floats - R::G) * 4u, &ctl->full[s]);
+                    bulk_load(st + SM::Rec + R::G * 4, rj + R::G, (uint32_t)(R::Head - R::G) * 4u, &ctl->full[s]);
                 }
                 issued = j + 1;
             }
             if (*abortp)
                 for (int j = issued - kNS < 0 ? 0 : issued - kNS; j < issued; ++j)
                     mbar_wait(&ctl->full[j % kNS], (uint32_t)(j / kNS) & 1u);
+        } else if (lane == 1 && with_o) {
+            // Gq of chunk j into its buffer once chunk j - 1's O2 products have read it
+            // (x_done of j - 1 cannot pass before this copy: O2 of j waits for it)
+            int issued = 0;
+            for (int j = 0; j < nc; ++j) {
+                if (j > 0 && !wait_or_abort(&ctl->x_done, (uint32_t)(j - 1) & 1u, abortp)) break;
+                mbar_expect_tx(&ctl->gfull, 16384u);
+                bulk_load(smem + SM::Gqb, recs + (int64_t)j * R::Floats + R::Gq, 16384u, &ctl->gfull);
+                issued = j + 1;
+            }
+            if (*abortp && issued > 0) mbar_wait(&ctl->gfull, (uint32_t)(issued - 1) & 1u);
         }
     } else if (warp <= 4) {
         // ------------------------------------------------------------ W / U operand warps
@@ -532,51 +523,6 @@ __global__ void __maxnreg__(80)
             if (!bar_and(1, kWT, ok)) {
                 *abortp = 1;
                 break;
-            }
-            // ---- with o_t: A diag(beta b) (over the record's A) and A diag(beta) -> bf16
-            // hi / lo tiles (row t, s contiguous, 128-byte swizzle)
-            if (O) {
-                const int t = wt & 63, cb = (wt >> 6) * 4;   // four 8-column groups per thread
-                float av[4][8];
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    const int c = cb + cc;
-                    const float4 x0 =
-                        *reinterpret_cast<const float4 *>(rec + R::A + t * 64 + (((2 * c) ^ (t & 15)) << 2));
-                    const float4 x1 =
-                        *reinterpret_cast<const float4 *>(rec + R::A + t * 64 + (((2 * c + 1) ^ (t & 15)) << 2));
-                    av[cc][0] = x0.x; av[cc][1] = x0.y; av[cc][2] = x0.z; av[cc][3] = x0.w;
-                    av[cc][4] = x1.x; av[cc][5] = x1.y; av[cc][6] = x1.z; av[cc][7] = x1.w;
-                }
-                bar_sync(1, kWT);   // all of A is in registers: its bytes may be overwritten
-                uint8_t *ab2 = st + SM::Rec;
-                uint8_t *ab = smem + SM::Ab + b * 16384;
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    const int c = cb + cc;
-                    const int off = t * 128 + ((c ^ (t & 7)) << 4);
-                    uint32_t hi[4], lo[4];
-#pragma unroll
-                    for (int p = 0; p < 4; ++p)
-                        split_pair(av[cc][2 * p] * rec[R::Gbb + c * 8 + 2 * p],
-                                   av[cc][2 * p + 1] * rec[R::Gbb + c * 8 + 2 * p + 1], hi[p], lo[p]);
-                    *reinterpret_cast<uint4 *>(ab2 + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                    *reinterpret_cast<uint4 *>(ab2 + 8192 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                    if (half) {
-#pragma unroll
-                        for (int p = 0; p < 4; ++p)
-                            split_pair(av[cc][2 * p] * rec[R::Gbeta + c * 8 + 2 * p],
-                                       av[cc][2 * p + 1] * rec[R::Gbeta + c * 8 + 2 * p + 1], hi[p], lo[p]);
-                        *reinterpret_cast<uint4 *>(ab + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                        *reinterpret_cast<uint4 *>(ab + 8192 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                    }
-                }
-            }
-            if (O) {
-                fence_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&ctl->aop_ready[b]);
-                bar_sync(1, kWT);
             }
             // ---- W^T = K^T (A diag(beta b))^T
             if (issuer) {
@@ -869,10 +815,8 @@ __global__ void __maxnreg__(80)
             if (!wait_or_abort(&ctl->full[s], (uint32_t)(j / kNS) & 1u, abortp)) break;
             // ---- U^T = V^T (A diag(beta))^T into the accumulator (state half)
             if (half) {
-                if (O && !wait_or_abort(&ctl->aop_ready[b], use & 1u, abortp)) break;
                 tc_fence_after();
-                const uint32_t vb = smem_addr(stg + SM::V);
-                const uint32_t ab = O ? smem_addr(smem + SM::Ab + b * 16384) : smem_addr(stg + SM::Rec + R::Ab * 4);
+                const uint32_t vb = smem_addr(stg + SM::V), ab = smem_addr(stg + SM::Rec + R::Ab * 4);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
                     const uint64_t ad = smem_desc_sw128(vb + (uint32_t)ks * 2048u, kBox, 1024);
@@ -927,7 +871,9 @@ __global__ void __maxnreg__(80)
                 mma_f16_ta(tmem + kTx, ah + 8u, bd, id_x, 1u);
             }
             if (with_o) {
-                const uint32_t gq = smem_addr(stg + SM::Rec + R::Gq * 4);
+                if (!wait_or_abort(&ctl->gfull, par, abortp)) break;
+                tc_fence_after();
+                const uint32_t gq = smem_addr(smem + SM::Gqb);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
                     const uint64_t gh = smem_desc_sw128(gq + (uint32_t)ks * 32u, 0, 1024);

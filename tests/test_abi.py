@@ -90,13 +90,13 @@ def scan_ws(lib, fam=2, dtype=0, L=1, S=2, N=64, H=2, dk=128, dv=128, ws=0x40000
 
 
 def test_workspace_size_and_checks(lib):
-    """The two-pass dense scan: one 33568-byte record (33808 with o_t) per
+    """The two-pass dense scan: one 33568-byte record (50192 with o_t) per
     (layer, head, chunk slot), n_seg + N / 64 slots; the balanced
     diagonal scan: a fixed 2 x 512 partial slots; other options take none."""
     ws = lib.hypic_segment_scan_workspace_bytes
     assert ws(2, 0, 30, 1, 2048, 32, 128, 128, 0) == 30 * 32 * (1 + 32) * 33568
     assert ws(2, 0, 1, 3, 200, 2, 128, 128, 0) == 2 * (3 + 3) * 33568
-    assert ws(2, 0, 1, 1, 2048, 2, 128, 128, 1) == 2 * (1 + 32) * 33808   # with o_t: Gq tiles and b_t too
+    assert ws(2, 0, 1, 1, 2048, 2, 128, 128, 1) == 2 * (1 + 32) * 50192   # with o_t: Gq tiles and b_t too
     assert ws(2, 1, 1, 1, 2048, 2, 128, 128, 0) == 0     # fp32 inputs
     assert ws(2, 0, 1, 1, 2048, 2, 64, 64, 0) == 0
     sd = 2 * 512 * (128 + 128 * 128) * 4      # diag: two partial slots per CTA, up to 512 CTAs
