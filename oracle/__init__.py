@@ -71,6 +71,8 @@ def open_library(path: str):
     lib.oracle_compose_chain.argtypes = [i32, i32, i32, i32, i32, i32, i32, P, P, i32,
                                          P, P, P, P, P, i32]
     lib.oracle_compose_chain.restype = i32
+    lib.oracle_seam_compose.argtypes = [i32, i32, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P, P]
+    lib.oracle_seam_compose.restype = i32
     lib.oracle_max_threads.restype = i32
     return lib
 
@@ -216,6 +218,33 @@ def compose_chain(fam, chain_len, seg_idx, pool_lam, pool_S, pool_M=None, S_init
     if rc != 0:
         raise ValueError(f"oracle_compose_chain: bad arguments ({rc})")
     return S
+
+
+def seam_compose(fam, k, v, alpha, lam, S_C, S_prev=None, M=None, beta=None, q=None,
+                 want_o=False):
+    """Seam-window advance then composition, per item and head, in fp64.
+
+    k [n,w,H,dk], v [n,w,H,dv], alpha [n,w,H] or [n,w,H,dk] (diag), beta
+    [n,w,H] or None, q [n,w,H,dk] (needed iff want_o); lam [n,H] or [n,H,dk],
+    M [n,H,dk,dk] (dense), S_prev (or None) and S_C [n,H,dk,dv].
+    Returns dict S [n,H,dk,dv] and, if asked, o [n,w,H,dv].
+    """
+    fam = _fam(fam)
+    k, v, alpha, beta, q = _f64(k), _f64(v), _f64(alpha), _f64(beta), _f64(q)
+    lam, S_C, S_prev, M = _f64(lam), _f64(S_C), _f64(S_prev), _f64(M)
+    n, H, dk, dv = S_C.shape
+    w = k.shape[1]
+    S = np.zeros_like(S_C)
+    o = np.zeros((n, w, H, dv), np.float64) if want_o else None
+    rc = _load().oracle_seam_compose(fam, n, w, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(alpha),
+                                     _ptr(beta), _ptr(lam), _ptr(M), _ptr(S_prev), _ptr(S_C), _ptr(S),
+                                     _ptr(o))
+    if rc != 0:
+        raise ValueError(f"oracle_seam_compose: bad arguments ({rc})")
+    out = {"S": S}
+    if o is not None:
+        out["o"] = o
+    return out
 
 
 def transition(out, fam=None):

@@ -317,6 +317,85 @@ int oracle_compose_chain(int fam, int R, int Lyr, int H, int dk, int dv, int max
     return 0;
 }
 
+/*
+ * Seam-window advance with composition ([xix-fr], paragraph on full-attention
+ * layers, "fenetres de jonction"): the first w tokens of every reused segment
+ * are left out of its cache and recomputed at reuse under the full prefix; the
+ * linear layers advance the running state through them, hand each seam
+ * token's output to the layer above, and the rest of the segment enters by
+ * its cached pair.  Per item i and head h, token by token in fp64:
+ *   S = S_prev (or 0);
+ *   for t = 0 .. w-1:  S = T_t S + beta_t k_t v_t^T;  o_t = S^T q_t;
+ *   S_out = T_body S + S_body      (T_body = exp(lam) M, as in compose_one).
+ * Layouts: q, k [n, w, H, dk], v [n, w, H, dv], alpha [n, w, H] or
+ * [n, w, H, dk] (diag), beta [n, w, H] or NULL (=> 1); lam [n, H] or [n, H, dk];
+ * M [n, H, dk, dk] (dense); S_prev (or NULL), S_C, S_out [n, H, dk, dv];
+ * o_out [n, w, H, dv] or NULL.
+ */
+int oracle_seam_compose(int fam, int n, int w, int H, int dk, int dv,
+                        const double *q, const double *k, const double *v,
+                        const double *alpha, const double *beta,
+                        const double *lam, const double *M, const double *S_prev,
+                        const double *S_C, double *S_out, double *o_out)
+{
+    if (fam < 0 || fam > 2 || n < 0 || w < 0 || H <= 0 || dk <= 0 || dv <= 0 ||
+        (w > 0 && (!k || !v || !alpha)) || (o_out && w > 0 && !q) || !lam || !S_C ||
+        !S_out || (fam == OR_DENSE && !M))
+        return -1;
+    const int nl = fam == OR_DIAG ? dk : 1;
+    double *S = malloc(sizeof(double) * (size_t)dk * dv);
+    double *kS = malloc(sizeof(double) * (size_t)dv);
+    for (int64_t u = 0; u < (int64_t)n * H; ++u) {
+        const int64_t i = u / H, h = u % H;
+        if (S_prev)
+            memcpy(S, S_prev + u * dk * dv, sizeof(double) * (size_t)dk * dv);
+        else
+            memset(S, 0, sizeof(double) * (size_t)dk * dv);
+        for (int t = 0; t < w; ++t) {
+            const int64_t row = (i * w + t) * H + h;   /* seam token-head row */
+            const double *kt = k + row * dk;
+            const double *vt = v + row * dv;
+            const double b = beta ? beta[row] : 1.0;
+            if (fam == OR_SCALAR) {
+                const double a = alpha[row];
+                for (int r = 0; r < dk; ++r)
+                    for (int j = 0; j < dv; ++j)
+                        S[(size_t)r * dv + j] = a * S[(size_t)r * dv + j] + b * kt[r] * vt[j];
+            } else if (fam == OR_DIAG) {
+                const double *at = alpha + row * dk;
+                for (int r = 0; r < dk; ++r)
+                    for (int j = 0; j < dv; ++j)
+                        S[(size_t)r * dv + j] = at[r] * S[(size_t)r * dv + j] + b * kt[r] * vt[j];
+            } else {
+                const double a = alpha[row];
+                for (int j = 0; j < dv; ++j) {
+                    double acc = 0.0;
+                    for (int r = 0; r < dk; ++r) acc += kt[r] * S[(size_t)r * dv + j];
+                    kS[j] = acc;
+                }
+                for (int r = 0; r < dk; ++r)
+                    for (int j = 0; j < dv; ++j)
+                        S[(size_t)r * dv + j] =
+                            a * (S[(size_t)r * dv + j] - b * kt[r] * kS[j]) + b * kt[r] * vt[j];
+            }
+            if (o_out) {
+                const double *qt = q + row * dk;
+                double *ot = o_out + row * dv;
+                for (int j = 0; j < dv; ++j) {
+                    double acc = 0.0;
+                    for (int r = 0; r < dk; ++r) acc += S[(size_t)r * dv + j] * qt[r];
+                    ot[j] = acc;
+                }
+            }
+        }
+        compose_one(fam, dk, dv, lam + u * nl, fam == OR_DENSE ? M + u * dk * dk : NULL, S,
+                    S_C + u * dk * dv, S_out + u * dk * dv);
+    }
+    free(S);
+    free(kS);
+    return 0;
+}
+
 int oracle_max_threads(void)
 {
 #ifdef _OPENMP

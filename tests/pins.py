@@ -442,6 +442,78 @@ def check_segment_independence():
             assert np.array_equal(batch["M"][0, 1, 0], np.eye(4))
 
 
+def _seam_inputs(fam, n_pre, w, n_body, H, dk, dv, seed):
+    """One layer of tokens laid out as prefix | seam window | rest of the segment."""
+    N = n_pre + w + n_body
+    k, v, alpha, beta, q = _inputs(fam, 1, N, H, dk, dv, seed=seed, q=True)
+    return k, v, alpha, beta, q, slice(0, n_pre), slice(n_pre, n_pre + w), slice(n_pre + w, N)
+
+
+def check_seam_window_equals_sequential():
+    """[xix-fr], paragraph on full-attention layers: the first w tokens of a
+    reused segment are recomputed at reuse under the full prefix -- the linear
+    layers advance the running state through them and hand up each one's
+    output -- and the rest of the segment enters by its cached pair.  State
+    after the segment and seam outputs equal the straight recurrence over
+    prefix + segment; the outputs also equal the unrolled definition."""
+    for fam in FAMS:
+        n_pre, w, n_body, H, dk, dv = 5, 3, 6, 2, 5, 4
+        k, v, alpha, beta, q, pre, seam, body = _seam_inputs(fam, n_pre, w, n_body, H, dk, dv, 170 + fam)
+        whole = oracle.sequential(fam, k, v, alpha, beta, q=q, want_o=True)
+        S_prev = oracle.sequential(fam, k[:, pre], v[:, pre], alpha[:, pre], beta[:, pre])["S"]
+        cached = oracle.sequential(fam, k[:, body], v[:, body], alpha[:, body], beta[:, body])
+        got = oracle.seam_compose(fam, k[:, seam], v[:, seam], alpha[:, seam], cached["lam"], cached["S"],
+                                  S_prev=S_prev, M=cached.get("M"), beta=beta[:, seam], q=q[:, seam],
+                                  want_o=True)
+        assert rel(got["S"], whole["S"]) < TOL, ("S", fam, rel(got["S"], whole["S"]))
+        assert rel(got["o"], whole["o"][:, seam]) < TOL, ("o", fam)
+        for h in range(H):
+            idx = slice(0, n_pre + w)
+            _, states = unrolled(fam, k[0, idx, h], v[0, idx, h], _head(alpha, 0, h)[idx],
+                                 _head(beta, 0, h)[idx])
+            o_ref = np.stack([states[n_pre + t].T @ q[0, n_pre + t, h] for t in range(w)])
+            assert rel(got["o"][0, :, h], o_ref) < TOL, ("o unrolled", fam, h)
+        # no seam window: plain composition; no previous state: the window from zero
+        plain = oracle.seam_compose(fam, k[:, :0], v[:, :0], alpha[:, :0], cached["lam"], cached["S"],
+                                    S_prev=S_prev, M=cached.get("M"))
+        ref = oracle.compose(fam, cached["lam"], cached["S"], S_prev=S_prev, M=cached.get("M"))
+        assert rel(plain["S"], ref["S"]) < TOL, ("w = 0", fam)
+
+
+def check_seam_window_pure_decay_closed_form():
+    """beta = 0 inside the window: the state only decays, S_t = (prod_{s<=t} alpha_s) S_prev,
+    so o_t = (prod alpha) S_prev^T q_t and S_out = T_body (prod alpha) S_prev + S_body,
+    written out with numpy products."""
+    g = np.random.default_rng(181)
+    n, w, H, dk, dv = 2, 4, 2, 5, 3
+    for fam in FAMS:
+        k = g.standard_normal((n, w, H, dk))
+        v = g.standard_normal((n, w, H, dv))
+        q = g.standard_normal((n, w, H, dk))
+        alpha = g.uniform(0.7, 1.0, size=(n, w, H, dk) if fam == DIAG else (n, w, H))
+        beta = np.zeros((n, w, H))
+        S_prev = g.standard_normal((n, H, dk, dv))
+        S_C = g.standard_normal((n, H, dk, dv))
+        lam = -g.uniform(0.0, 2.0, size=(n, H, dk) if fam == DIAG else (n, H))
+        M = g.standard_normal((n, H, dk, dk)) if fam == DENSE else None
+        got = oracle.seam_compose(fam, k, v, alpha, lam, S_C, S_prev=S_prev, M=M, beta=beta, q=q,
+                                  want_o=True)
+        for i in range(n):
+            for h in range(H):
+                S = S_prev[i, h].copy()
+                for t in range(w):
+                    a = alpha[i, t, h]
+                    S = (a[:, None] if fam == DIAG else a) * S
+                    assert rel(got["o"][i, t, h], S.T @ q[i, t, h]) < TOL, ("o", fam, i, t, h)
+                if fam == DENSE:
+                    Sref = np.exp(lam[i, h]) * (M[i, h] @ S) + S_C[i, h]
+                elif fam == DIAG:
+                    Sref = np.exp(lam[i, h])[:, None] * S + S_C[i, h]
+                else:
+                    Sref = np.exp(lam[i, h]) * S + S_C[i, h]
+                assert rel(got["S"][i, h], Sref) < TOL, ("S", fam, i, h)
+
+
 ALL_CHECKS = [
     check_transition_is_ordered_product,
     check_state_and_output_unrolled,
@@ -458,4 +530,6 @@ ALL_CHECKS = [
     check_brute_force_rational,
     check_chain_equals_sequential,
     check_segment_independence,
+    check_seam_window_equals_sequential,
+    check_seam_window_pure_decay_closed_form,
 ]

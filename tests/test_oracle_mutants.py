@@ -36,6 +36,13 @@ MUTANTS = [
      "const int64_t p = seg_idx[r * max_chain + (chain_len[r] - 1 - j)];", 0),
     ("chain_ignores_init", "memcpy(S, S_init + u * dk * dv, sizeof(double) * (size_t)dk * dv);",
      "memset(S, 0, sizeof(double) * (size_t)dk * dv);", 0),
+    ("seam_ignores_prev", "memcpy(S, S_prev + u * dk * dv, sizeof(double) * (size_t)dk * dv);",
+     "memset(S, 0, sizeof(double) * (size_t)dk * dv);", 0),
+    ("seam_dense_erase_sign", "a * (S[(size_t)r * dv + j] - b * kt[r] * kS[j])",
+     "a * (S[(size_t)r * dv + j] + b * kt[r] * kS[j])", 0),
+    ("seam_diag_gate_index", "at[r] * S[(size_t)r * dv + j]", "at[0] * S[(size_t)r * dv + j]", 0),
+    ("seam_output_reads_key", "acc += S[(size_t)r * dv + j] * qt[r];", "acc += S[(size_t)r * dv + j] * kt[r];", 0),
+    ("seam_token_order", "const int64_t row = (i * w + t) * H + h;", "const int64_t row = (i * w + (w - 1 - t)) * H + h;", 0),
 ]
 
 
