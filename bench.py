@@ -397,6 +397,61 @@ def run_compose(args):
     return res
 
 
+def run_seam(args):
+    """Reuse with a seam window (hypic_seam_compose): per item, the first 8 tokens
+    of a reused segment advance the running state from S_prev (emitting their
+    outputs), then the cached rest of the segment is composed; 1920 items x 32
+    heads x 128 x 128 per family, inputs drawn on the device (values do not change
+    the work)."""
+    import torch
+    import linear_attention_state_gated_gb300 as hy
+    res = {}
+    hbm, _, _, src = peaks()
+    n, w, H, d = args.compose_n, 8, 32, 128
+    dev = torch.device("cuda")
+    g = torch.Generator(device=dev)
+    g.manual_seed(6)
+    f = dict(device=dev, generator=g)
+    k = torch.nn.functional.normalize(torch.randn((n, w, H, d), **f), dim=-1).to(torch.bfloat16)
+    q = torch.randn((n, w, H, d), **f).to(torch.bfloat16)
+    v = torch.randn((n, w, H, d), **f).to(torch.bfloat16)
+    beta = torch.sigmoid(torch.randn((n, w, H), **f))
+    S_prev = torch.randn((n, H, d, d), **f)
+    S_C = torch.randn((n, H, d, d), **f)
+    S_out = torch.empty_like(S_prev)
+    o = torch.empty((n, w, H, d), dtype=torch.bfloat16, device=dev)
+    for fam, name in ((0, "scalar"), (1, "diag"), (2, "dense")):
+        alpha = 0.85 + 0.15 * torch.rand((n, w, H, d) if fam == 1 else (n, w, H), **f)
+        lam = -torch.rand((n, H, d) if fam == 1 else (n, H), **f) * 5
+        M = torch.randn((n, H, d, d), **f) * 0.1 if fam == 2 else None
+        call = lambda: hy.seam_compose(fam, k, v, alpha, lam, S_C, S_prev=S_prev, M=M, beta=beta, q=q,
+                                       want_o=True, S_out=S_out, o_out=o)
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        reps = 5
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(reps):
+            call()
+        e.record()
+        torch.cuda.synchronize()
+        t = s.elapsed_time(e) / reps / 1e3
+        # states in and out (S_prev, S_C, S_out; M for dense), lambda, the window's
+        # q, k, v (bf16), alpha, beta and outputs
+        per_head = 3 * 4 * d * d + (4 * d * d if fam == 2 else 0) + (4 * d if fam == 1 else 4) + \
+            w * (3 * 2 * d + (4 * d if fam == 1 else 4) + 4 + 2 * d)
+        by = n * H * per_head
+        res[name] = {"value": n / t, "unit": "seam composes/s (all 32 heads, w = 8)", "ms": t * 1e3,
+                     "items": n, "window": w,
+                     "roofline": {"bound": "hbm", "achieved": by / t / 1e9, "peak": hbm, "unit": "GB/s",
+                                  "frac": by / t / 1e9 / hbm, "traffic": None, "peak_kind": f"copy, {src}"}}
+        del alpha, lam, M
+    del k, q, v, beta, S_prev, S_C, S_out, o
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_chain(args):
     import torch
     import linear_attention_state_gated_gb300 as hy
@@ -601,8 +656,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="hypic", choices=["hypic", "reference"])
     ap.add_argument("--L", type=int, default=8192)
-    ap.add_argument("--rows", default="dense,compose,chain,mix",
-                    help="extra rows: dense,compose,chain,mix or none")
+    ap.add_argument("--rows", default="dense,compose,seam,chain,mix",
+                    help="extra rows: dense,compose,seam,chain,mix or none")
     ap.add_argument("--dense-L", type=int, default=2048)
     ap.add_argument("--dense-form", choices=["two_pass", "single"], default="two_pass",
                     help="dense row: two passes over a workspace, or the single-pass kernel")
@@ -630,6 +685,8 @@ def main():
         rows["dense_scan"] = run_dense(args, args.dense_L)
     if rank == 0 and "compose" in args.rows:
         rows["compose"] = run_compose(args)
+    if rank == 0 and "seam" in args.rows:
+        rows["seam"] = run_seam(args)
     if rank == 0 and "chain" in args.rows:
         rows["rag_chain"] = run_chain(args)
     if rank == 0 and "mix" in args.rows:

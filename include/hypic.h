@@ -214,6 +214,38 @@ int hypic_compose_chain(int fam, int n_req, int n_layers, int n_heads, int d_k, 
                         const float *pool_S, const float *S_init, float *S_out,
                         int *d_err, void *cuda_stream);
 
+/*
+ * hypic_seam_compose -- reuse of a cached segment whose first w tokens (the
+ * seam window) were left out of its cache.  (xix.ai/fr, paragraph on
+ * full-attention layers: at reuse the seam tokens are recomputed under the full
+ * prefix; the linear layers advance the running state through them and hand
+ * each seam token's output to the layer above.  The rest of the segment then
+ * enters by its cached pair, as in hypic_compose.)  For n items x H heads:
+ *   S = S_prev;  for t = 0 .. w-1:  S = T_t S + beta_t k_t v_t^T,  o_t = S^T q_t;
+ *   S_out = T_body S + S_body,  T_body = exp(lambda) M.
+ *   in_dtype  HYPIC_BF16 or HYPIC_F32: q, k, v and o_out
+ *   q, k    [n, w, H, d_k];  v [n, w, H, d_v]      -- the seam tokens (q may be
+ *                                                   NULL when o_out is NULL)
+ *   alpha   fp32 [n, w, H] (scalar, dense) or [n, w, H, d_k] (diag)
+ *   beta    fp32 [n, w, H] or NULL (=> 1)
+ *   lam     fp32 [n, H] or [n, H, d_k] (diag)     -- T_body of the cached rest
+ *   M       fp32 [n, H, d_k, d_k] (dense; NULL otherwise)
+ *   S_prev  fp32 [n, H, d_k, d_v] or NULL (=> 0)   -- state before the segment
+ *   S_C     fp32 [n, H, d_k, d_v]                  -- S_body of the cached rest
+ *   S_out   fp32 [n, H, d_k, d_v]; may be the same pointer as S_prev, must not
+ *           overlap any other argument
+ *   o_out   [n, w, H, d_v] or NULL
+ * 0 <= w <= 4096; w = 0 is hypic_compose.  The window runs on CUDA cores in
+ * fp32; the dense family writes the advanced state to S_out and then composes
+ * it in place (so S_out holds the intermediate state between two launches on
+ * the stream).  Pointers 16-byte aligned (alpha, beta, scalar/dense lam:
+ * 4-byte; bf16 q, k, v, o_out: 2-byte with rows of 16-byte multiples).
+ */
+int hypic_seam_compose(int fam, int in_dtype, int n, int w, int n_heads, int d_k, int d_v,
+                       const void *q, const void *k, const void *v, const float *alpha,
+                       const float *beta, const float *lam, const float *M, const float *S_prev,
+                       const float *S_C, float *S_out, void *o_out, void *cuda_stream);
+
 /* Human-readable name of a hypic_status value (static string, never NULL). */
 const char *hypic_status_string(int status);
 

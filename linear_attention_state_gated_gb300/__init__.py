@@ -58,6 +58,8 @@ SIGNATURES = {
     "hypic_compose": (_I32, [_I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "hypic_compose_chain": (_I32, [_I32, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _I32,
                                    _P, _P, _P, _P, _P, _P, _P]),
+    "hypic_seam_compose": (_I32, [_I32, _I32, _I32, _I32, _I32, _I32, _I32,
+                                  _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "hypic_status_string": (ctypes.c_char_p, [_I32]),
     "hypic_version": (_I32, []),
 }
@@ -260,6 +262,47 @@ def compose(family, lam, S_C, S_prev=None, M=None, lam_prev=None, M_prev=None, S
         res["lam"] = lam_out
         if fam == DENSE:
             res["M"] = M_out
+    return res
+
+
+def seam_compose(family, k, v, alpha, lam, S_C, S_prev=None, M=None, beta=None, q=None,
+                 want_o=False, S_out=None, o_out=None, stream=None):
+    """Seam-window advance, then the cached rest of the segment (hypic_seam_compose).
+
+    k [n,w,H,dk], v [n,w,H,dv] (bf16 or fp32), alpha [n,w,H] or [n,w,H,dk], beta
+    [n,w,H] or None, q [n,w,H,dk] (needed iff want_o); lam [n,H] or [n,H,dk],
+    M [n,H,dk,dk] (dense), S_prev (or None) and S_C [n,H,dk,dv] fp32.  Returns a
+    dict with S [n,H,dk,dv] and, if asked, o [n,w,H,dv] in the input dtype.
+    S_out may be S_prev (in place).
+    """
+    fam = _fam(family)
+    k = _dev(k, "k")
+    dt = k.dtype
+    if dt not in (torch.bfloat16, torch.float32):
+        raise ValueError("k must be bf16 or fp32")
+    v = _dev(v, "v", dt)
+    alpha = _dev(alpha, "alpha", torch.float32)
+    beta = _dev(beta, "beta", torch.float32, allow_none=True)
+    lam = _dev(lam, "lam", torch.float32)
+    S_C = _dev(S_C, "S_C", torch.float32)
+    S_prev = _dev(S_prev, "S_prev", torch.float32, allow_none=True)
+    M = _dev(M, "M", torch.float32, allow_none=True)
+    if want_o:
+        q = _dev(q, "q", dt)
+    n, w, H, dk = k.shape
+    dv = v.shape[-1]
+    if S_out is None:
+        S_out = torch.empty_like(S_C)
+    if want_o and o_out is None:
+        o_out = torch.empty((n, w, H, dv), dtype=dt, device=k.device)
+    st = library().hypic_seam_compose(fam, BF16 if dt == torch.bfloat16 else F32, n, w, H, dk, dv,
+                                      _ptr(q if want_o else None), _ptr(k), _ptr(v), _ptr(alpha),
+                                      _ptr(beta), _ptr(lam), _ptr(M), _ptr(S_prev), _ptr(S_C),
+                                      _ptr(S_out), _ptr(o_out if want_o else None), _stream(stream))
+    _check("hypic_seam_compose", st)
+    res = {"S": S_out}
+    if want_o:
+        res["o"] = o_out
     return res
 
 

@@ -270,6 +270,69 @@ int hypic_compose(int fam, int n, int n_heads, int d_k, int d_v, const float *la
     return from_cuda(hypic::launch_compose(a, static_cast<cudaStream_t>(cuda_stream)));
 }
 
+int hypic_seam_compose(int fam, int in_dtype, int n, int w, int n_heads, int d_k, int d_v, const void *q,
+                       const void *k, const void *v, const float *alpha, const float *beta, const float *lam,
+                       const float *M, const float *S_prev, const float *S_C, float *S_out, void *o_out,
+                       void *cuda_stream) {
+    if (fam < HYPIC_SCALAR || fam > HYPIC_DENSE) return HYPIC_EINVAL;
+    if (in_dtype != HYPIC_BF16 && in_dtype != HYPIC_F32) return HYPIC_EINVAL;
+    if (n < 0 || n_heads <= 0 || w < 0) return HYPIC_EINVAL;
+    if (w > 4096) return HYPIC_EUNSUPPORTED;
+    if (!head_size_ok(d_k) || !head_size_ok(d_v)) return HYPIC_EUNSUPPORTED;
+    if ((int64_t)n * n_heads * (d_v / 32) > INT32_MAX) return HYPIC_EUNSUPPORTED;   // one CTA per 32 columns
+    if (n == 0) return HYPIC_OK;
+    if (!lam || !S_C || !S_out) return HYPIC_EINVAL;
+    if ((fam == HYPIC_DENSE) != (M != nullptr)) return HYPIC_EINVAL;
+    if (w > 0 && (!k || !v || !alpha || (o_out && !q))) return HYPIC_EINVAL;
+    const void *a16[] = {M, S_prev, S_C, S_out, fam == HYPIC_DIAG ? lam : nullptr};
+    for (const void *p : a16)
+        if (p && !aligned(p, 16)) return HYPIC_EALIGN;
+    const void *a4[] = {lam, alpha, beta};
+    for (const void *p : a4)
+        if (p && !aligned(p, 4)) return HYPIC_EALIGN;
+    const uintptr_t ea = in_dtype == HYPIC_BF16 ? 2 : 4;
+    const void *ae[] = {q, k, v, o_out};
+    for (const void *p : ae)
+        if (p && !aligned(p, ea)) return HYPIC_EALIGN;
+    const size_t sbytes = (size_t)n * n_heads * d_k * d_v * sizeof(float);
+    const size_t mbytes = (size_t)n * n_heads * d_k * d_k * sizeof(float);
+    const size_t es = in_dtype == HYPIC_BF16 ? 2 : 4;
+    const size_t obytes = (size_t)n * w * n_heads * d_v * es;
+    auto overlaps = [](const void *x, size_t xb, const void *y, size_t yb) {
+        if (!x || !y) return false;
+        const char *a = static_cast<const char *>(x), *b = static_cast<const char *>(y);
+        return a < b + yb && b < a + xb;
+    };
+    if (overlaps(S_out, sbytes, S_C, sbytes) || overlaps(S_out, sbytes, M, mbytes)) return HYPIC_EINVAL;
+    if (S_prev && S_out != S_prev && overlaps(S_out, sbytes, S_prev, sbytes)) return HYPIC_EINVAL;
+    if (o_out && (overlaps(o_out, obytes, S_out, sbytes) || overlaps(o_out, obytes, S_prev, sbytes) ||
+                  overlaps(o_out, obytes, q, (size_t)n * w * n_heads * d_k * es) ||
+                  overlaps(o_out, obytes, k, (size_t)n * w * n_heads * d_k * es) ||
+                  overlaps(o_out, obytes, v, obytes)))
+        return HYPIC_EINVAL;
+
+    hypic::SeamArgs a;
+    a.fam = fam;
+    a.in_dtype = in_dtype;
+    a.n = n;
+    a.w = w;
+    a.H = n_heads;
+    a.dk = d_k;
+    a.dv = d_v;
+    a.q = o_out ? q : nullptr;
+    a.k = k;
+    a.v = v;
+    a.alpha = alpha;
+    a.beta = beta;
+    a.lam = lam;
+    a.M = M;
+    a.S_prev = S_prev;
+    a.S_C = S_C;
+    a.S_out = S_out;
+    a.o_out = w > 0 ? o_out : nullptr;
+    return from_cuda(hypic::launch_seam_compose(a, static_cast<cudaStream_t>(cuda_stream)));
+}
+
 int hypic_compose_chain(int fam, int n_req, int n_layers, int n_heads, int d_k, int d_v,
                         int max_chain, const int32_t *chain_len, const int32_t *seg_idx,
                         int pool_size, const float *pool_lam, const float *pool_M,

@@ -79,6 +79,17 @@ cudaError_t launch_chain_dense_tc(const ChainArgs &a, cudaStream_t s);
 cudaError_t launch_compose(const ComposeArgs &a, cudaStream_t s);
 cudaError_t launch_compose_chain(const ChainArgs &a, cudaStream_t s);
 
+// Seam-window advance, then the composition of the rest of the segment.
+struct SeamArgs {
+    int fam, in_dtype, n, w, H, dk, dv;
+    const void *q, *k, *v;
+    const float *alpha, *beta;
+    const float *lam, *M, *S_prev, *S_C;
+    float *S_out;
+    void *o_out;
+};
+cudaError_t launch_seam_compose(const SeamArgs &a, cudaStream_t s);
+
 // Report a device-side index problem without trapping.
 __device__ __forceinline__ void flag_index_error(int *d_err) {
     if (d_err) atomicExch(d_err, (int)HYPIC_EINDEX);

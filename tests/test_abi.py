@@ -157,6 +157,31 @@ def test_chain_rejects_bad_arguments(lib):
     assert chain(lib, R=0) == OK
 
 
+def seam(lib, fam=0, dtype=0, n=2, w=8, H=2, dk=64, dv=64, q=0, k=A, v=A, alpha=A, beta=0,
+         lam=A + 0x200000, M=0, Sp=0, Sc=A + 0x400000, So=A + 0x600000, o=0):
+    return lib.hypic_seam_compose(fam, dtype, n, w, H, dk, dv, P(q or None), P(k or None), P(v or None),
+                                  P(alpha or None), P(beta or None), P(lam or None), P(M or None),
+                                  P(Sp or None), P(Sc or None), P(So or None), P(o or None), P(None))
+
+
+def test_seam_rejects_bad_arguments(lib):
+    assert seam(lib, fam=3) == EINVAL
+    assert seam(lib, dtype=2) == EINVAL
+    assert seam(lib, w=-1) == EINVAL
+    assert seam(lib, w=5000) == EUNSUP
+    assert seam(lib, dk=48) == EUNSUP
+    assert seam(lib, lam=0) == EINVAL
+    assert seam(lib, Sc=0) == EINVAL
+    assert seam(lib, fam=2, M=0) == EINVAL
+    assert seam(lib, fam=1, M=A + 0x800000) == EINVAL
+    assert seam(lib, k=0) == EINVAL                   # a window needs its tokens
+    assert seam(lib, o=A + 0x900000) == EINVAL       # outputs need q
+    assert seam(lib, Sc=A + 0x400008) == EALIGN
+    assert seam(lib, k=A + 1) == EALIGN               # bf16 rows need 2-byte alignment
+    assert seam(lib, So=A + 0x400000 + 64) == EINVAL  # S_out overlaps S_C
+    assert seam(lib, n=0) == OK
+
+
 def test_python_binding_refuses_host_tensors():
     import torch
     import linear_attention_state_gated_gb300 as hy
