@@ -30,7 +30,7 @@ namespace {
 using namespace sm100;
 
 constexpr int kD = 128;
-constexpr int kThreads = 576;           // warp 0: TMA, warp 1: MMA, warps 2..17: math
+constexpr int kThreads = 608;           // warp 0: TMA, warps 1 and 18: MMA (one column half each), 2..17: math
 constexpr int kMath = 512;
 constexpr uint32_t kTa = 0;             // TMEM: A buffers at 0 and 192 (hi / mid / lo at +0, +64, +128)
 constexpr uint32_t kTd = 384;           // D (128 columns)
@@ -83,7 +83,7 @@ __device__ __forceinline__ int64_t step_entry(const ChainArgs &a, int64_t u, int
     return (int64_t)p * lhn + lh;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)   // 18 warps: <= 96 registers per thread
+__global__ void __launch_bounds__(kThreads, 1)   // 19 warps: <= 96 registers per thread
     chain_dense_tc_kernel(const __grid_constant__ CUtensorMap tm_m, const __grid_constant__ CUtensorMap tm_s,
                           const __grid_constant__ CUtensorMap tm_i, const __grid_constant__ CUtensorMap tm_o,
                           const ChainArgs a, int64_t units) {
@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: <= 96 registers pe
         mbar_init(&ctl->sfull, 1);
         mbar_init(&ctl->sfree, kMath / 32);
         mbar_init(&ctl->ops_ready, kMath / 32);
-        mbar_init(&ctl->d_done, 1);
+        mbar_init(&ctl->d_done, 2);   // both issuers commit
         ctl->abort = 0;
         mbar_fence_init();
         tma_prefetch(&tm_m);
@@ -159,11 +159,15 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: <= 96 registers pe
             }
             if (*abortp && g > 0) mbar_wait(&ctl->sfull, (uint32_t)(g - 1) & 1u);   // the last copy lands
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == 1 || warp == 18) {
+        // ------------------------------------------------------------ MMA issuers: warp 1 takes
+        // columns 0..63 of D, warp 18 columns 64..127 (N = 64 products from two threads issue
+        // at nearly twice the rate of N = 128 products from one)
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(128, 128, false, true);   // A TMEM, B MN-major
-            const uint32_t b0 = smem_addr(smem);
+            constexpr uint32_t idesc = idesc_bf16_f32(128, 64, false, true);   // A TMEM, B MN-major
+            const uint32_t nh = warp == 1 ? 0u : 1u;
+            const uint32_t b0 = smem_addr(smem) + nh * 16384u;   // the B atom of this column half
+            const uint32_t dcol = tmem + kTd + nh * 64u;
             int64_t g = 0;
             for (int64_t u = blockIdx.x; u < units && !*abortp; u += gridDim.x) {
                 const int n = unit_steps(a, u, false);
@@ -181,17 +185,17 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: <= 96 registers pe
                         const uint64_t bm = smem_desc_sw128(b0 + kBpart + off, 16384, 1024);
                         const uint64_t bl = smem_desc_sw128(b0 + 2 * kBpart + off, 16384, 1024);
                         const uint32_t ah = abuf + (uint32_t)ks * 8u, am = ah + 64u, al = ah + 128u;
-                        mma_f16_ta(tmem + kTd, ah, bh, idesc, ks > 0);
-                        mma_f16_ta(tmem + kTd, ah, bm, idesc, 1u);
-                        mma_f16_ta(tmem + kTd, am, bh, idesc, 1u);
-                        mma_f16_ta(tmem + kTd, ah, bl, idesc, 1u);
-                        mma_f16_ta(tmem + kTd, am, bm, idesc, 1u);
-                        mma_f16_ta(tmem + kTd, al, bh, idesc, 1u);
+                        mma_f16_ta(dcol, ah, bh, idesc, ks > 0);
+                        mma_f16_ta(dcol, ah, bm, idesc, 1u);
+                        mma_f16_ta(dcol, am, bh, idesc, 1u);
+                        mma_f16_ta(dcol, ah, bl, idesc, 1u);
+                        mma_f16_ta(dcol, am, bm, idesc, 1u);
+                        mma_f16_ta(dcol, al, bh, idesc, 1u);
                     }
                     mma_commit(&ctl->d_done);
                 }
             }
-            if (*abortp) {   // drain: completes once every issued MMA is done
+            if (*abortp) {   // drain: completes once every issued MMA of both issuers is done
                 mma_commit(&ctl->d_done);
                 mbar_wait(&ctl->d_done, (uint32_t)g & 1u);
             }
