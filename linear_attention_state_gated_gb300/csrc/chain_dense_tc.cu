@@ -15,7 +15,9 @@
 // TMA (128-byte swizzle, so the row-per-lane reads are conflict-free); the math
 // warps split M_p into one of two TMEM operand buffers -- the NEXT step's M_p
 // while the current step's products run -- and split S into shared memory as
-// the MN-major B operand; warp 1 issues the products.  Each unit's S_init comes
+// the MN-major B operand.  The columns of S evolve independently, so the two
+// 64-column halves run as two pipelines (their own math warps, barriers and MMA
+// issuer, warps 1 and 18), sharing only the M_p operand.  Each unit's S_init comes
 // through the M_p stage too (one more TMA fill, after the unit's first M_p, in
 // flight during the previous unit's last products and update); the last update
 // is written over S_p in its stage and leaves by TMA store.
@@ -42,10 +44,14 @@ constexpr int kSmem = kCtl + 128 + 1024;
 static_assert(kSmem <= 232448, "fits in one SM's shared memory");
 
 struct ChainCtrl {
-    uint64_t mfull, mfree, sfull, sfree, ops_ready, d_done;
+    uint64_t mfull, mfree, sfull, sfree;
+    uint64_t ops_ready[2], d_done[2];   // per column half: B half in shared memory / its products done
+    uint64_t aready[2], afree[2];       // per A operand buffer: split into TMEM / read by both halves
     uint32_t tmem;
     int abort;
 };
+
+static_assert(sizeof(ChainCtrl) <= 128, "the control block fits its reserved bytes");
 
 // Two fp32 values -> three packed bf16 pairs with x = hi + mid + lo (to ~2^-27 relative).
 __device__ __forceinline__ void split3_pair(float x0, float x1, uint32_t &hi, uint32_t &mid, uint32_t &lo) {
@@ -98,8 +104,12 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: <= 96 registers pe
         mbar_init(&ctl->mfree, kMath / 32);
         mbar_init(&ctl->sfull, 1);
         mbar_init(&ctl->sfree, kMath / 32);
-        mbar_init(&ctl->ops_ready, kMath / 32);
-        mbar_init(&ctl->d_done, 2);   // both issuers commit
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&ctl->ops_ready[x], kMath / 64);   // the eight warps of a column half
+            mbar_init(&ctl->d_done[x], 1);
+            mbar_init(&ctl->aready[x], kMath / 32);      // all sixteen math warps
+            mbar_init(&ctl->afree[x], 2);                // both issuers
+        }
         ctl->abort = 0;
         mbar_fence_init();
         tma_prefetch(&tm_m);
@@ -172,7 +182,9 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: <= 96 registers pe
             for (int64_t u = blockIdx.x; u < units && !*abortp; u += gridDim.x) {
                 const int n = unit_steps(a, u, false);
                 for (int c = 0; c < n; ++c, ++g) {
-                    if (!mbar_wait(&ctl->ops_ready, (uint32_t)g & 1u) || *abortp) {
+                    // this half's B and the step's A operand are in place
+                    if (!mbar_wait(&ctl->ops_ready[nh], (uint32_t)g & 1u) ||
+                        !mbar_wait(&ctl->aready[g & 1], (uint32_t)(g >> 1) & 1u) || *abortp) {
                         *abortp = 1;
                         break;
                     }
@@ -192,17 +204,20 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: <= 96 registers pe
                         mma_f16_ta(dcol, am, bm, idesc, 1u);
                         mma_f16_ta(dcol, al, bh, idesc, 1u);
                     }
-                    mma_commit(&ctl->d_done);
+                    mma_commit(&ctl->d_done[nh]);
+                    mma_commit(&ctl->afree[g & 1]);
                 }
             }
-            if (*abortp) {   // drain: completes once every issued MMA of both issuers is done
-                mma_commit(&ctl->d_done);
-                mbar_wait(&ctl->d_done, (uint32_t)g & 1u);
+            if (*abortp) {   // drain: completes once every MMA this thread issued is done
+                mma_commit(&ctl->d_done[nh]);
+                mbar_wait(&ctl->d_done[nh], (uint32_t)g & 1u);
             }
         }
     } else {
         // ------------------------------------------------------------ math warps
         const int cq = (warp - 2) >> 2;              // column quarter: [32 cq, 32 cq + 32)
+        const int hh = cq >> 1;                      // column half: its own pipeline
+        const int hbar = 2 + hh;                     // named barrier of the half's 256 threads
         const int quarter = warp & 3;
         const int i = quarter * 32 + lane;           // row of S / of M_p
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
@@ -210,9 +225,14 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: <= 96 registers pe
         float srow[32];                              // exact running state, row i, 32 columns
         uint32_t f = 0;                              // fills of the M_p stage taken (parity)
 
-        // split M_p of step g (the stage's next fill) into TMEM operand buffer g & 1
+        // split M_p of step g (the stage's next fill) into TMEM operand buffer g & 1, once
+        // both halves' products of step g - 2 are done with that buffer
         auto split_m = [&](int64_t g) -> bool {
-            if (!bar_and(1, kMath, mbar_wait(&ctl->mfull, f & 1u) && !*abortp)) return false;
+            if (!bar_and(hbar, kMath / 2,
+                         (g < 2 || mbar_wait(&ctl->afree[g & 1], (uint32_t)((g - 2) >> 1) & 1u)) &&
+                             mbar_wait(&ctl->mfull, f & 1u) && !*abortp))
+                return false;
+            tc_fence_after();
             const uint8_t *ms = smem + kMstage;
             uint32_t hi[16], mid[16], lo[16];
 #pragma unroll
@@ -228,8 +248,13 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: <= 96 registers pe
             tmem_st16(ab, hi);
             tmem_st16(ab + 64u, mid);
             tmem_st16(ab + 128u, lo);
+            tmem_wait_st();
+            tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->mfree);   // the stage may take its next fill
+            if (lane == 0) {
+                mbar_arrive(&ctl->mfree);            // the stage may take its next fill
+                mbar_arrive(&ctl->aready[g & 1]);    // this warp's share of the A operand is in
+            }
             ++f;
             return true;
         };
@@ -248,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: <= 96 registers pe
                 for (int q = 0; q < 32; ++q) srow[q] = 0.f;
                 return true;
             }
-            if (!bar_and(1, kMath, mbar_wait(&ctl->mfull, f & 1u) && !*abortp)) return false;
+            if (!bar_and(hbar, kMath / 2, mbar_wait(&ctl->mfull, f & 1u) && !*abortp)) return false;
             const uint8_t *ms = smem + kMstage + cq * 16384 + i * 128;   // box cq: this thread's 32 columns
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
@@ -294,20 +319,18 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: <= 96 registers pe
                     *reinterpret_cast<uint4 *>(smem + kBpart + off) = make_uint4(md[0], md[1], md[2], md[3]);
                     *reinterpret_cast<uint4 *>(smem + 2 * kBpart + off) = make_uint4(l[0], l[1], l[2], l[3]);
                 }
-                tmem_wait_st();   // this step's A operand (split in the previous step) is in TMEM
                 fence_async_smem();
-                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&ctl->ops_ready);
+                if (lane == 0) mbar_arrive(&ctl->ops_ready[hh]);
                 // while the products run: the next step's M_p into the other operand buffer
                 if ((!last || un < units) && !split_m(g + 1)) {
                     ok = false;
                     break;
                 }
                 const float scale = expf(a.pool_lam[e]);
-                if (!bar_and(1, kMath,
-                             mbar_wait(&ctl->sfull, (uint32_t)g & 1u) && mbar_wait(&ctl->d_done, (uint32_t)g & 1u) &&
-                                 !*abortp)) {
+                if (!bar_and(hbar, kMath / 2,
+                             mbar_wait(&ctl->sfull, (uint32_t)g & 1u) &&
+                                 mbar_wait(&ctl->d_done[hh], (uint32_t)g & 1u) && !*abortp)) {
                     ok = false;
                     break;
                 }
@@ -338,10 +361,10 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: <= 96 registers pe
                 tc_fence_before();
                 if (last) {
                     fence_async_smem();    // the results, visible to the TMA store
-                    bar_sync(1, kMath);
-                    if (threadIdx.x == 64) {
+                    bar_sync(hbar, kMath / 2);
+                    if (threadIdx.x == 64 + hh * 256) {   // each half stores its two boxes
 #pragma unroll
-                        for (int bx = 0; bx < 4; ++bx)
+                        for (int bx = 2 * hh; bx < 2 * hh + 2; ++bx)
                             tma_store_3d(&tm_o, smem + kSstage + bx * 16384, 32 * bx, 0, (int)(u * kD));
                         bulk_commit();
                         bulk_wait_read_all();   // the stage is read: it may take the next S_p
@@ -359,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: <= 96 registers pe
             u = un;
         }
         if (!ok) *abortp = 1;
-        if (threadIdx.x == 64) bulk_wait_all();   // the stores of S_out are complete
+        if (threadIdx.x == 64 || threadIdx.x == 320) bulk_wait_all();   // the stores of S_out are complete
     }
 
     tc_fence_before();
