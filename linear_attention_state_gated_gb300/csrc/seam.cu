@@ -46,6 +46,26 @@ __device__ __forceinline__ void cp_async_wait_all() {
 
 constexpr int kCW = 32;   // columns of S per CTA
 
+// packed pairs of fp32 (one f32x2 instruction does two lanes' worth of work)
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void upk2(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {   // a * b + c
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 template <int FAM, int DK, int DV, typename T>
 __global__ void __launch_bounds__(kCW *(DK / 32)) seam_kernel(const SeamArgs a) {
     constexpr int RS = DK / 32;               // row groups
@@ -53,8 +73,10 @@ __global__ void __launch_bounds__(kCW *(DK / 32)) seam_kernel(const SeamArgs a) 
     constexpr int NS = DV / kCW;              // column slices per (item, head)
     constexpr int NA = FAM == HYPIC_DIAG ? DK : 1;   // gates per token
     __shared__ float sk[kTB][DK], sq[kTB][DK], sv[kTB][kCW], sa[kTB][NA], sb[kTB];
-    __shared__ float red[RS][kCW];
+    __shared__ float red[2][RS][kCW];                        // S^T k partials, by token parity
+    __shared__ float ro[RS][kTB][kCW];                       // output partials of a block of tokens
     __shared__ float sc[FAM == HYPIC_DENSE ? 1 : DK][kCW];   // S_body slice (scalar, diag)
+    __shared__ float sl[FAM == HYPIC_DIAG ? DK : 1];         // exp(lambda_body) per row (diag)
 
     const int tid = threadIdx.x;
     const int jl = tid % kCW, g = tid / kCW;  // column in the slice, row group
@@ -75,11 +97,14 @@ __global__ void __launch_bounds__(kCW *(DK / 32)) seam_kernel(const SeamArgs a) 
 #pragma unroll
     for (int r = 0; r < 32; ++r) S[r] = a.S_prev ? a.S_prev[so + (int64_t)(g * 32 + r) * DV + j] : 0.f;
 
+    if (FAM == HYPIC_DIAG)
+        for (int r = tid; r < DK; r += NT) sl[r] = expf(a.lam[unit * DK + r]);
+
     const T *q = static_cast<const T *>(a.q), *k = static_cast<const T *>(a.k), *v = static_cast<const T *>(a.v);
     T *o = static_cast<T *>(a.o_out);
     for (int t0 = 0; t0 < a.w; t0 += kTB) {
         const int nt = a.w - t0 < kTB ? a.w - t0 : kTB;
-        __syncthreads();   // the previous block's inputs are no longer read
+        __syncthreads();   // the previous block's inputs and output partials are no longer read
         for (int e = tid; e < nt * DK; e += NT) {
             const int t = e / DK, c = e % DK;
             const int64_t row = (item * a.w + t0 + t) * a.H + h;   // seam token-head row
@@ -97,59 +122,92 @@ __global__ void __launch_bounds__(kCW *(DK / 32)) seam_kernel(const SeamArgs a) 
             sb[tid] = a.beta ? a.beta[row] : 1.f;
         }
         __syncthreads();
-        for (int t = 0; t < nt; ++t) {
-            const float b = sb[t];
-            if (FAM == HYPIC_DENSE) {
-                // S <- alpha (S - beta k (k^T S)) + beta k v^T = alpha S + k (beta (v - alpha u))^T, u = S^T k
-                float p = 0.f;
+        float po[kTB];   // this thread's partial outputs (its 32 rows) of the block's tokens
 #pragma unroll
-                for (int r = 0; r < 32; ++r) p = fmaf(sk[t][g * 32 + r], S[r], p);
-                red[g][jl] = p;
-                __syncthreads();
-                float u = 0.f;
+        for (int t = 0; t < kTB; ++t) {
+            if (t < nt) {
+                const float b = sb[t];
+                const float *kt = &sk[t][g * 32];
+                float c;   // S <- alpha S + k c^T, column entry c_j
+                if (FAM == HYPIC_DENSE) {
+                    // gated delta rule: c = beta (v - alpha u), u = S^T k (rows summed over the groups)
+                    uint64_t p2 = 0;
 #pragma unroll
-                for (int x = 0; x < RS; ++x) u += red[x][jl];
-                const float al = sa[t][0];
-                const float c = b * (sv[t][jl] - al * u);
+                    for (int rq = 0; rq < 8; ++rq) {
+                        const float4 k4 = *reinterpret_cast<const float4 *>(kt + 4 * rq);
+                        p2 = fma2(pk2(k4.x, k4.y), pk2(S[4 * rq], S[4 * rq + 1]), p2);
+                        p2 = fma2(pk2(k4.z, k4.w), pk2(S[4 * rq + 2], S[4 * rq + 3]), p2);
+                    }
+                    float plo, phi;
+                    upk2(p2, plo, phi);
+                    red[t & 1][g][jl] = plo + phi;
+                    __syncthreads();   // (red alternates by token, so one barrier a token suffices)
+                    float u = 0.f;
 #pragma unroll
-                for (int r = 0; r < 32; ++r) S[r] = fmaf(al, S[r], sk[t][g * 32 + r] * c);
-                __syncthreads();   // red is reused below
-            } else {
-                const float bv = b * sv[t][jl];
+                    for (int x = 0; x < RS; ++x) u += red[t & 1][x][jl];
+                    c = b * (sv[t][jl] - sa[t][0] * u);
+                } else {
+                    c = b * sv[t][jl];
+                }
+                const uint64_t cc = pk2(c, c);
 #pragma unroll
-                for (int r = 0; r < 32; ++r) {
-                    const float al = FAM == HYPIC_DIAG ? sa[t][g * 32 + r] : sa[t][0];
-                    S[r] = fmaf(al, S[r], sk[t][g * 32 + r] * bv);
+                for (int rq = 0; rq < 8; ++rq) {
+                    const float4 k4 = *reinterpret_cast<const float4 *>(kt + 4 * rq);
+                    uint64_t a01, a23;
+                    if (FAM == HYPIC_DIAG) {
+                        const float4 a4 = *reinterpret_cast<const float4 *>(&sa[t][g * 32 + 4 * rq]);
+                        a01 = pk2(a4.x, a4.y);
+                        a23 = pk2(a4.z, a4.w);
+                    } else {
+                        a01 = a23 = pk2(sa[t][0], sa[t][0]);
+                    }
+                    const uint64_t s01 = fma2(a01, pk2(S[4 * rq], S[4 * rq + 1]), mul2(pk2(k4.x, k4.y), cc));
+                    const uint64_t s23 = fma2(a23, pk2(S[4 * rq + 2], S[4 * rq + 3]), mul2(pk2(k4.z, k4.w), cc));
+                    upk2(s01, S[4 * rq], S[4 * rq + 1]);
+                    upk2(s23, S[4 * rq + 2], S[4 * rq + 3]);
+                }
+                if (o) {   // this thread's part of o_t = S_t^T q_t
+                    const float *qt = &sq[t][g * 32];
+                    uint64_t p2 = 0;
+#pragma unroll
+                    for (int rq = 0; rq < 8; ++rq) {
+                        const float4 q4 = *reinterpret_cast<const float4 *>(qt + 4 * rq);
+                        p2 = fma2(pk2(q4.x, q4.y), pk2(S[4 * rq], S[4 * rq + 1]), p2);
+                        p2 = fma2(pk2(q4.z, q4.w), pk2(S[4 * rq + 2], S[4 * rq + 3]), p2);
+                    }
+                    float plo, phi;
+                    upk2(p2, plo, phi);
+                    po[t] = plo + phi;
                 }
             }
-            if (o) {   // o_t = S_t^T q_t
-                float p = 0.f;
+        }
+        if (o) {   // the block's outputs: row groups summed once for all its tokens
 #pragma unroll
-                for (int r = 0; r < 32; ++r) p = fmaf(sq[t][g * 32 + r], S[r], p);
-                red[g][jl] = p;
-                __syncthreads();
-                if (g == 0) {
-                    float s = 0.f;
+            for (int t = 0; t < kTB; ++t)
+                if (t < nt) ro[g][t][jl] = po[t];
+            __syncthreads();
+            if (g == 0) {
+                for (int t = 0; t < nt; ++t) {
+                    float sum = 0.f;
 #pragma unroll
-                    for (int x = 0; x < RS; ++x) s += red[x][jl];
-                    o[((item * a.w + t0 + t) * a.H + h) * DV + j] = from_f32<T>(s);
+                    for (int x = 0; x < RS; ++x) sum += ro[x][t][jl];
+                    o[((item * a.w + t0 + t) * a.H + h) * DV + j] = from_f32<T>(sum);
                 }
-                __syncthreads();
             }
         }
     }
 
     // the rest of the segment: S_out = T_body S + S_body (dense: the advanced state only)
     if (FAM != HYPIC_DENSE) cp_async_wait_all();
+    if (FAM == HYPIC_DIAG) __syncthreads();   // sl is in (also without a window)
+    const float el = FAM == HYPIC_SCALAR ? expf(a.lam[unit]) : 1.f;
 #pragma unroll
     for (int r = 0; r < 32; ++r) {
         const int64_t e = so + (int64_t)(g * 32 + r) * DV + j;
-        if (FAM == HYPIC_DENSE) {
+        if (FAM == HYPIC_DENSE)
             a.S_out[e] = S[r];
-        } else {
-            const float lam = FAM == HYPIC_DIAG ? a.lam[unit * DK + g * 32 + r] : a.lam[unit];
-            a.S_out[e] = fmaf(expf(lam), S[r], sc[g * 32 + r][jl]);
-        }
+        else
+            a.S_out[e] = fmaf(FAM == HYPIC_DIAG ? sl[g * 32 + r] : el, S[r], sc[g * 32 + r][jl]);
     }
 }
 
