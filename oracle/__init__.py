@@ -31,8 +31,9 @@ import threading
 
 import numpy as np
 
-SCALAR, DIAG, DENSE = 0, 1, 2
-FAMILIES = {"scalar": SCALAR, "diag": DIAG, "dense": DENSE}
+SCALAR, DIAG, DENSE, KDA = 0, 1, 2, 3
+FAMILIES = {"scalar": SCALAR, "diag": DIAG, "dense": DENSE, "kda": KDA}
+WITH_M = (DENSE, KDA)   # families whose operator is exp(lambda) * M
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
@@ -131,7 +132,7 @@ def segment_scan(fam, k, v, alpha, seg_offsets, beta=None, q=None, want_o=False,
                  n_threads=0):
     """Scan every (layer, segment, head) token by token in fp64.
 
-    k [Lyr,N,H,dk], v [Lyr,N,H,dv], alpha [Lyr,N,H] or [Lyr,N,H,dk] (diag),
+    k [Lyr,N,H,dk], v [Lyr,N,H,dv], alpha [Lyr,N,H] or [Lyr,N,H,dk] (diag, kda),
     beta [Lyr,N,H] or None, q [Lyr,N,H,dk] (needed iff want_o),
     seg_offsets [n_seg+1] int64.  Returns dict lam, M (dense), S, o (if asked).
     """
@@ -142,7 +143,7 @@ def segment_scan(fam, k, v, alpha, seg_offsets, beta=None, q=None, want_o=False,
     offs = np.ascontiguousarray(np.asarray(seg_offsets, dtype=np.int64))
     n_seg = offs.shape[0] - 1
     lam = np.zeros((Lyr, n_seg, H, dk) if fam == DIAG else (Lyr, n_seg, H), np.float64)
-    M = np.zeros((Lyr, n_seg, H, dk, dk), np.float64) if fam == DENSE else None
+    M = np.zeros((Lyr, n_seg, H, dk, dk), np.float64) if fam in WITH_M else None
     S = np.zeros((Lyr, n_seg, H, dk, dv), np.float64)
     o = np.zeros((Lyr, N, H, dv), np.float64) if want_o else None
     rc = _load().oracle_segment_scan(fam, Lyr, n_seg, N, H, dk, dv, _ptr(offs), _ptr(q),
@@ -182,7 +183,7 @@ def compose(fam, lam, S_C, S_prev=None, M=None, lam_prev=None, M_prev=None):
     n, H, dk, dv = S_C.shape
     S = np.zeros_like(S_C)
     lam_out = np.zeros_like(lam) if lam_prev is not None else None
-    M_out = np.zeros_like(M) if (lam_prev is not None and fam == DENSE) else None
+    M_out = np.zeros_like(M) if (lam_prev is not None and fam in WITH_M) else None
     rc = _load().oracle_compose(fam, n, H, dk, dv, _ptr(lam), _ptr(M), _ptr(S_prev), _ptr(S_C),
                                 _ptr(S), _ptr(lam_prev), _ptr(M_prev), _ptr(lam_out), _ptr(M_out))
     if rc != 0:

@@ -23,6 +23,10 @@
  *     scalar : T_t = alpha_t I                      (RetNet / Mamba2)
  *     diag   : T_t = diag(alpha_t), alpha_t in R^dk (GLA, gates the key axis)
  *     dense  : T_t = alpha_t (I - beta_t k_t k_t^T) (gated delta rule)
+ *     kda    : T_t = diag(alpha_t) (I - beta_t k_t k_t^T), alpha_t in R^dk
+ *              (the pages name KDA among the delta-erasure variants and give no
+ *              rule; this is the gated delta rule with its scalar gate made
+ *              per channel)
  *   beta_t defaults to 1 when no beta is given.
  *   T_C = T_L ... T_1 ;  S(C|0) = S_L from S_0 = 0 ;  o_t = S_t^T q_t.
  * T_C is returned as (lambda, M) with T_C = exp(lambda) * M:
@@ -31,6 +35,8 @@
  *   dense : M = prod (I - beta_t k_t k_t^T) scaled to max|M| = 1,
  *           lambda = sum log alpha_t + log(scale).  If M is exactly zero it is
  *           left at zero and lambda keeps sum log alpha_t.
+ *   kda   : the per-channel gates do not factor out, so M = prod T_t itself,
+ *           scaled to max|M| = 1, and lambda = log(scale) only.
  * Everything here is token by token, one (layer, segment, head) at a time,
  * in the order the recurrence states it.  No blocking, no chunking.
  */
@@ -42,7 +48,9 @@
 #include <omp.h>
 #endif
 
-enum { OR_SCALAR = 0, OR_DIAG = 1, OR_DENSE = 2 };
+enum { OR_SCALAR = 0, OR_DIAG = 1, OR_DENSE = 2, OR_KDA = 3 };
+/* families whose operator is exp(lambda) * M with a matrix M */
+#define HAS_M(fam) ((fam) == OR_DENSE || (fam) == OR_KDA)
 
 /* Scale M by an exact power of two whenever its largest entry leaves
  * [2^-256, 2^256]; the factor goes into *lam.  Exact in binary floating point,
@@ -79,11 +87,11 @@ static void normalise_maxabs(double *M, int n, double *lam)
 /*
  * Segment scan.  Layouts (row-major, innermost last):
  *   q, k  [n_layers, N, H, dk]    v [n_layers, N, H, dv]
- *   alpha [n_layers, N, H] (scalar, dense) or [n_layers, N, H, dk] (diag)
+ *   alpha [n_layers, N, H] (scalar, dense) or [n_layers, N, H, dk] (diag, kda)
  *   beta  [n_layers, N, H] or NULL (=> 1)
  *   seg_offsets [n_seg + 1], ascending, seg_offsets[0] = 0, last = N
  *   lam_out [n_layers, n_seg, H] or [n_layers, n_seg, H, dk] (diag)
- *   M_out   [n_layers, n_seg, H, dk, dk] (dense only; may be NULL)
+ *   M_out   [n_layers, n_seg, H, dk, dk] (dense, kda; may be NULL)
  *   S_out   [n_layers, n_seg, H, dk, dv]
  *   o_out   [n_layers, N, H, dv] or NULL; needs q.
  * Returns 0, or -1 on bad arguments.
@@ -95,7 +103,7 @@ int oracle_segment_scan(int fam, int n_layers, int n_seg, int64_t N, int H,
                         double *lam_out, double *M_out, double *S_out,
                         double *o_out, int n_threads)
 {
-    if (fam < 0 || fam > 2 || n_layers < 0 || n_seg < 0 || N < 0 || H <= 0 ||
+    if (fam < 0 || fam > 3 || n_layers < 0 || n_seg < 0 || N < 0 || H <= 0 ||
         dk <= 0 || dv <= 0 || !seg_offsets || !k || !v || !alpha || !lam_out ||
         !S_out || (o_out && !q))
         return -1;
@@ -113,10 +121,11 @@ int oracle_segment_scan(int fam, int n_layers, int n_seg, int64_t N, int H,
         const int seg = (int)((u / H) % n_seg);
         const int l = (int)(u / ((int64_t)H * n_seg));
         double *S = calloc((size_t)dk * dv, sizeof(double));
-        double *M = fam == OR_DENSE ? calloc((size_t)dk * dk, sizeof(double)) : NULL;
+        const int has_M = fam == OR_DENSE || fam == OR_KDA;
+        double *M = has_M ? calloc((size_t)dk * dk, sizeof(double)) : NULL;
         double *kS = malloc(sizeof(double) * (size_t)(dv > dk ? dv : dk));
         double *lam = calloc((size_t)dk, sizeof(double));
-        if (fam == OR_DENSE)
+        if (has_M)
             for (int i = 0; i < dk; ++i) M[(size_t)i * dk + i] = 1.0;
 
         for (int64_t t = seg_offsets[seg]; t < seg_offsets[seg + 1]; ++t) {
@@ -139,7 +148,7 @@ int oracle_segment_scan(int fam, int n_layers, int n_seg, int64_t N, int H,
                         S[(size_t)i * dv + j] = at[i] * S[(size_t)i * dv + j] + b * kt[i] * vt[j];
                     lam[i] += log(at[i]);
                 }
-            } else {
+            } else if (fam == OR_DENSE) {
                 const double a = alpha[row];
                 /* S <- a (S - b k (k^T S)) + b k v^T */
                 for (int j = 0; j < dv; ++j) {
@@ -161,6 +170,28 @@ int oracle_segment_scan(int fam, int n_layers, int n_seg, int64_t N, int H,
                     for (int j = 0; j < dk; ++j)
                         M[(size_t)i * dk + j] -= b * kt[i] * kS[j];
                 lam[0] += log(a);
+                keep_in_range(M, dk * dk, &lam[0]);
+            } else {
+                const double *at = alpha + row * dk;
+                /* S <- diag(a) (S - b k (k^T S)) + b k v^T */
+                for (int j = 0; j < dv; ++j) {
+                    double acc = 0.0;
+                    for (int i = 0; i < dk; ++i) acc += kt[i] * S[(size_t)i * dv + j];
+                    kS[j] = acc;
+                }
+                for (int i = 0; i < dk; ++i)
+                    for (int j = 0; j < dv; ++j)
+                        S[(size_t)i * dv + j] =
+                            at[i] * (S[(size_t)i * dv + j] - b * kt[i] * kS[j]) + b * kt[i] * vt[j];
+                /* T <- diag(a) (I - b k k^T) T: the gates stay inside M */
+                for (int j = 0; j < dk; ++j) {
+                    double acc = 0.0;
+                    for (int i = 0; i < dk; ++i) acc += kt[i] * M[(size_t)i * dk + j];
+                    kS[j] = acc;
+                }
+                for (int i = 0; i < dk; ++i)
+                    for (int j = 0; j < dk; ++j)
+                        M[(size_t)i * dk + j] = at[i] * (M[(size_t)i * dk + j] - b * kt[i] * kS[j]);
                 keep_in_range(M, dk * dk, &lam[0]);
             }
             if (o_out) {
@@ -226,29 +257,29 @@ static void compose_one(int fam, int dk, int dv, const double *lam, const double
 
 /*
  * Batched composition over n items x H heads:
- *   lam [n,H] or [n,H,dk] (diag);  M [n,H,dk,dk] (dense);
+ *   lam [n,H] or [n,H,dk] (diag);  M [n,H,dk,dk] (dense, kda);
  *   S_prev [n,H,dk,dv] or NULL (=> 0);  S_C, S_out [n,H,dk,dv].
  * Optional operator composition T(C1.C2) = T(C2) T(C1):
- *   lam_out = lam + lam_prev;  dense: M_out = M M_prev, max-abs normalised.
- * lam_prev/lam_out (and M_prev/M_out for dense) are both given or both NULL.
+ *   lam_out = lam + lam_prev;  dense, kda: M_out = M M_prev, max-abs normalised.
+ * lam_prev/lam_out (and M_prev/M_out for dense, kda) are both given or both NULL.
  */
 int oracle_compose(int fam, int n, int H, int dk, int dv, const double *lam,
                    const double *M, const double *S_prev, const double *S_C,
                    double *S_out, const double *lam_prev, const double *M_prev,
                    double *lam_out, double *M_out)
 {
-    if (fam < 0 || fam > 2 || n < 0 || H <= 0 || dk <= 0 || dv <= 0 || !lam ||
-        !S_C || !S_out || (fam == OR_DENSE && !M) || (!lam_prev) != (!lam_out))
+    if (fam < 0 || fam > 3 || n < 0 || H <= 0 || dk <= 0 || dv <= 0 || !lam ||
+        !S_C || !S_out || (HAS_M(fam) && !M) || (!lam_prev) != (!lam_out))
         return -1;
-    if (fam == OR_DENSE && lam_out && ((!M_prev) || (!M_out))) return -1;
+    if (HAS_M(fam) && lam_out && ((!M_prev) || (!M_out))) return -1;
     const int nl = fam == OR_DIAG ? dk : 1;
     for (int64_t u = 0; u < (int64_t)n * H; ++u) {
-        const double *Mu = fam == OR_DENSE ? M + u * dk * dk : NULL;
+        const double *Mu = HAS_M(fam) ? M + u * dk * dk : NULL;
         compose_one(fam, dk, dv, lam + u * nl, Mu, S_prev ? S_prev + u * dk * dv : NULL,
                     S_C + u * dk * dv, S_out + u * dk * dv);
         if (lam_out) {
             for (int i = 0; i < nl; ++i) lam_out[u * nl + i] = lam[u * nl + i] + lam_prev[u * nl + i];
-            if (fam == OR_DENSE) {
+            if (HAS_M(fam)) {
                 const double *Mp = M_prev + u * dk * dk;
                 double *P = malloc(sizeof(double) * (size_t)dk * dk);
                 for (int i = 0; i < dk; ++i)
@@ -273,7 +304,7 @@ int oracle_compose(int fam, int n, int H, int dk, int dv, const double *lam,
  * head h, starting from S_init (or 0):
  *   for j = 0 .. chain_len[r]-1:  p = seg_idx[r, j];  S = T_p S + S_p.
  * Layouts: seg_idx [R, max_chain]; pool_lam [P, Lyr, H] or [P, Lyr, H, dk];
- * pool_M [P, Lyr, H, dk, dk] (dense); pool_S [P, Lyr, H, dk, dv];
+ * pool_M [P, Lyr, H, dk, dk] (dense, kda); pool_S [P, Lyr, H, dk, dv];
  * S_init, S_out [R, Lyr, H, dk, dv].  Returns -2 on an index out of range.
  */
 int oracle_compose_chain(int fam, int R, int Lyr, int H, int dk, int dv, int max_chain,
@@ -282,9 +313,9 @@ int oracle_compose_chain(int fam, int R, int Lyr, int H, int dk, int dv, int max
                          const double *pool_S, const double *S_init, double *S_out,
                          int n_threads)
 {
-    if (fam < 0 || fam > 2 || R < 0 || Lyr < 0 || H <= 0 || dk <= 0 || dv <= 0 ||
+    if (fam < 0 || fam > 3 || R < 0 || Lyr < 0 || H <= 0 || dk <= 0 || dv <= 0 ||
         max_chain < 0 || !chain_len || (max_chain > 0 && !seg_idx) || P < 0 ||
-        !pool_lam || !pool_S || (fam == OR_DENSE && !pool_M) || !S_out)
+        !pool_lam || !pool_S || (HAS_M(fam) && !pool_M) || !S_out)
         return -1;
     for (int r = 0; r < R; ++r) {
         if (chain_len[r] < 0 || chain_len[r] > max_chain) return -1;
@@ -310,7 +341,7 @@ int oracle_compose_chain(int fam, int R, int Lyr, int H, int dk, int dv, int max
             const int64_t p = seg_idx[r * max_chain + j];
             const int64_t e = p * Lyr * H + lh;       /* pool entry for this layer, head */
             compose_one(fam, dk, dv, pool_lam + e * nl,
-                        fam == OR_DENSE ? pool_M + e * dk * dk : NULL, S,
+                        HAS_M(fam) ? pool_M + e * dk * dk : NULL, S,
                         pool_S + e * dk * dv, S);
         }
     }
@@ -328,8 +359,9 @@ int oracle_compose_chain(int fam, int R, int Lyr, int H, int dk, int dv, int max
  *   for t = 0 .. w-1:  S = T_t S + beta_t k_t v_t^T;  o_t = S^T q_t;
  *   S_out = T_body S + S_body      (T_body = exp(lam) M, as in compose_one).
  * Layouts: q, k [n, w, H, dk], v [n, w, H, dv], alpha [n, w, H] or
- * [n, w, H, dk] (diag), beta [n, w, H] or NULL (=> 1); lam [n, H] or [n, H, dk];
- * M [n, H, dk, dk] (dense); S_prev (or NULL), S_C, S_out [n, H, dk, dv];
+ * [n, w, H, dk] (diag, kda), beta [n, w, H] or NULL (=> 1); lam [n, H] or
+ * [n, H, dk] (diag); M [n, H, dk, dk] (dense, kda); S_prev (or NULL), S_C,
+ * S_out [n, H, dk, dv];
  * o_out [n, w, H, dv] or NULL.
  */
 int oracle_seam_compose(int fam, int n, int w, int H, int dk, int dv,
@@ -338,9 +370,9 @@ int oracle_seam_compose(int fam, int n, int w, int H, int dk, int dv,
                         const double *lam, const double *M, const double *S_prev,
                         const double *S_C, double *S_out, double *o_out)
 {
-    if (fam < 0 || fam > 2 || n < 0 || w < 0 || H <= 0 || dk <= 0 || dv <= 0 ||
+    if (fam < 0 || fam > 3 || n < 0 || w < 0 || H <= 0 || dk <= 0 || dv <= 0 ||
         (w > 0 && (!k || !v || !alpha)) || (o_out && w > 0 && !q) || !lam || !S_C ||
-        !S_out || (fam == OR_DENSE && !M))
+        !S_out || (HAS_M(fam) && !M))
         return -1;
     const int nl = fam == OR_DIAG ? dk : 1;
     double *S = malloc(sizeof(double) * (size_t)dk * dv);
@@ -367,16 +399,18 @@ int oracle_seam_compose(int fam, int n, int w, int H, int dk, int dv,
                     for (int j = 0; j < dv; ++j)
                         S[(size_t)r * dv + j] = at[r] * S[(size_t)r * dv + j] + b * kt[r] * vt[j];
             } else {
-                const double a = alpha[row];
+                /* gated delta rule (one gate) or KDA (a gate per channel) */
                 for (int j = 0; j < dv; ++j) {
                     double acc = 0.0;
                     for (int r = 0; r < dk; ++r) acc += kt[r] * S[(size_t)r * dv + j];
                     kS[j] = acc;
                 }
-                for (int r = 0; r < dk; ++r)
+                for (int r = 0; r < dk; ++r) {
+                    const double a = fam == OR_KDA ? alpha[row * dk + r] : alpha[row];
                     for (int j = 0; j < dv; ++j)
                         S[(size_t)r * dv + j] =
                             a * (S[(size_t)r * dv + j] - b * kt[r] * kS[j]) + b * kt[r] * vt[j];
+                }
             }
             if (o_out) {
                 const double *qt = q + row * dk;
@@ -388,7 +422,7 @@ int oracle_seam_compose(int fam, int n, int w, int H, int dk, int dv,
                 }
             }
         }
-        compose_one(fam, dk, dv, lam + u * nl, fam == OR_DENSE ? M + u * dk * dk : NULL, S,
+        compose_one(fam, dk, dv, lam + u * nl, HAS_M(fam) ? M + u * dk * dk : NULL, S,
                     S_C + u * dk * dv, S_out + u * dk * dv);
     }
     free(S);

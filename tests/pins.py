@@ -19,8 +19,10 @@ import numpy as np
 
 import oracle
 
-SCALAR, DIAG, DENSE = oracle.SCALAR, oracle.DIAG, oracle.DENSE
-FAMS = (SCALAR, DIAG, DENSE)
+SCALAR, DIAG, DENSE, KDA = oracle.SCALAR, oracle.DIAG, oracle.DENSE, oracle.KDA
+FAMS = (SCALAR, DIAG, DENSE, KDA)
+PER_CH = (DIAG, KDA)      # a gate per channel
+WITH_M = (DENSE, KDA)     # operator kept as exp(lambda) * M
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
 TOL = 1e-12
@@ -37,7 +39,7 @@ def _inputs(fam, Lyr, N, H, dk, dv, seed, beta=True, q=False, alpha_lo=0.8):
     k = g.standard_normal((Lyr, N, H, dk))
     k /= np.linalg.norm(k, axis=-1, keepdims=True)
     v = g.standard_normal((Lyr, N, H, dv))
-    ash = (Lyr, N, H, dk) if fam == DIAG else (Lyr, N, H)
+    ash = (Lyr, N, H, dk) if fam in PER_CH else (Lyr, N, H)
     alpha = g.uniform(alpha_lo, 1.0, size=ash)
     b = g.uniform(0.1, 1.0, size=(Lyr, N, H)) if beta else None
     qq = g.standard_normal((Lyr, N, H, dk)) if q else None
@@ -45,12 +47,15 @@ def _inputs(fam, Lyr, N, H, dk, dv, seed, beta=True, q=False, alpha_lo=0.8):
 
 
 def token_T(fam, a, b, k):
-    """Per-token transition matrix: alpha I, diag(alpha) or alpha (I - beta k k^T)."""
+    """Per-token transition matrix: alpha I, diag(alpha), alpha (I - beta k k^T) or
+    diag(alpha) (I - beta k k^T)."""
     d = k.shape[0]
     if fam == SCALAR:
         return a * np.eye(d)
     if fam == DIAG:
         return np.diag(a)
+    if fam == KDA:
+        return np.diag(a) @ (np.eye(d) - b * np.outer(k, k))
     return a * (np.eye(d) - b * np.outer(k, k))
 
 
@@ -89,9 +94,9 @@ def check_transition_is_ordered_product():
         out = oracle.sequential(fam, k, v, alpha, beta)
         for h in range(2):
             T, _ = unrolled(fam, k[0, :, h], v[0, :, h], _head(alpha, 0, h), _head(beta, 0, h))
-            if fam == DENSE:
+            if fam in WITH_M:
                 Tg = np.exp(out["lam"][0, h]) * out["M"][0, h]
-                assert rel(Tg, T) < TOL, ("dense T_C", rel(Tg, T))
+                assert rel(Tg, T) < TOL, ("T_C", rel(Tg, T))
                 assert abs(np.max(np.abs(out["M"][0, h])) - 1.0) < 1e-15
             elif fam == DIAG:
                 assert rel(np.diag(np.exp(out["lam"][0, h])), T) < TOL
@@ -124,7 +129,7 @@ def check_composition_identity():
         comp = oracle.compose(fam, c2["lam"], c2["S"], S_prev=c1["S"], M=c2.get("M"),
                               lam_prev=c1["lam"], M_prev=c1.get("M"))
         assert rel(comp["S"], whole["S"]) < TOL, ("S", fam, rel(comp["S"], whole["S"]))
-        if fam == DENSE:
+        if fam in WITH_M:
             Tg = np.exp(comp["lam"])[..., None, None] * comp["M"]
             Tw = np.exp(whole["lam"])[..., None, None] * whole["M"]
             assert rel(Tg, Tw) < TOL
@@ -248,7 +253,7 @@ def check_associativity_and_linearity():
         left = comp(comp(A, B), C)
         right = comp(A, comp(B, C))
         assert rel(left["S"], right["S"]) < TOL
-        if fam == DENSE:
+        if fam in WITH_M:
             tl = np.exp(left["lam"])[..., None, None] * left["M"]
             tr = np.exp(right["lam"])[..., None, None] * right["M"]
             assert rel(tl, tr) < TOL
@@ -335,6 +340,9 @@ def _frac_unrolled(fam, k, v, alpha, beta, q):
             return [[alpha[t] if i == j else Fraction(0) for j in range(dk)] for i in range(dk)]
         if fam == DIAG:
             return [[alpha[t][i] if i == j else Fraction(0) for j in range(dk)] for i in range(dk)]
+        if fam == KDA:
+            return [[alpha[t][i] * (Fraction(int(i == j)) - beta[t] * k[t][i] * k[t][j])
+                     for j in range(dk)] for i in range(dk)]
         return [[alpha[t] * (Fraction(int(i == j)) - beta[t] * k[t][i] * k[t][j])
                  for j in range(dk)] for i in range(dk)]
 
@@ -370,7 +378,7 @@ def check_brute_force_rational():
         v = [[rnd(-32, 33) for _ in range(dv)] for _ in range(L)]
         q = [[rnd(-16, 17) for _ in range(dk)] for _ in range(L)]
         beta = [rnd(1, 17) for _ in range(L)]
-        if fam == DIAG:
+        if fam in PER_CH:
             alpha = [[rnd(8, 17) for _ in range(dk)] for _ in range(L)]
         else:
             alpha = [rnd(8, 17) for _ in range(L)]
@@ -381,7 +389,7 @@ def check_brute_force_rational():
         bb = f(beta)[None, :, None]
         out = oracle.sequential(fam, kk, vv, aa, bb, q=qq, want_o=True)
         Tref = np.array([[float(x) for x in row] for row in T])
-        if fam == DENSE:
+        if fam in WITH_M:
             Tg = np.exp(out["lam"][0, 0]) * out["M"][0, 0]
         elif fam == DIAG:
             Tg = np.diag(np.exp(out["lam"][0, 0]))
@@ -405,7 +413,7 @@ def check_chain_equals_sequential():
         # pool arrays [Lyr, P, ...] -> [P, Lyr, ...]
         pl = np.moveaxis(pool["lam"], 1, 0)
         pS = np.moveaxis(pool["S"], 1, 0)
-        pM = np.moveaxis(pool["M"], 1, 0) if fam == DENSE else None
+        pM = np.moveaxis(pool["M"], 1, 0) if fam in WITH_M else None
         orders = np.array([[3, 0, 4, 1], [2, 2, 1, 0], [4, 3, 0, 0]], dtype=np.int32)
         chain_len = np.array([4, 3, 2], dtype=np.int32)
         # request 1 starts from the state of a prefix (segment 1 scanned alone)
@@ -438,7 +446,7 @@ def check_segment_independence():
                 assert np.array_equal(alone[key][:, 0], batch[key][:, s]), (fam, s, key)
         # the empty segment: lambda = 0, M = I, S = 0
         assert np.all(batch["S"][:, 1] == 0) and np.all(batch["lam"][:, 1] == 0)
-        if fam == DENSE:
+        if fam in WITH_M:
             assert np.array_equal(batch["M"][0, 1, 0], np.eye(4))
 
 
@@ -490,12 +498,12 @@ def check_seam_window_pure_decay_closed_form():
         k = g.standard_normal((n, w, H, dk))
         v = g.standard_normal((n, w, H, dv))
         q = g.standard_normal((n, w, H, dk))
-        alpha = g.uniform(0.7, 1.0, size=(n, w, H, dk) if fam == DIAG else (n, w, H))
+        alpha = g.uniform(0.7, 1.0, size=(n, w, H, dk) if fam in PER_CH else (n, w, H))
         beta = np.zeros((n, w, H))
         S_prev = g.standard_normal((n, H, dk, dv))
         S_C = g.standard_normal((n, H, dk, dv))
         lam = -g.uniform(0.0, 2.0, size=(n, H, dk) if fam == DIAG else (n, H))
-        M = g.standard_normal((n, H, dk, dk)) if fam == DENSE else None
+        M = g.standard_normal((n, H, dk, dk)) if fam in WITH_M else None
         got = oracle.seam_compose(fam, k, v, alpha, lam, S_C, S_prev=S_prev, M=M, beta=beta, q=q,
                                   want_o=True)
         for i in range(n):
@@ -503,15 +511,41 @@ def check_seam_window_pure_decay_closed_form():
                 S = S_prev[i, h].copy()
                 for t in range(w):
                     a = alpha[i, t, h]
-                    S = (a[:, None] if fam == DIAG else a) * S
+                    S = (a[:, None] if fam in PER_CH else a) * S
                     assert rel(got["o"][i, t, h], S.T @ q[i, t, h]) < TOL, ("o", fam, i, t, h)
-                if fam == DENSE:
+                if fam in WITH_M:
                     Sref = np.exp(lam[i, h]) * (M[i, h] @ S) + S_C[i, h]
                 elif fam == DIAG:
                     Sref = np.exp(lam[i, h])[:, None] * S + S_C[i, h]
                 else:
                     Sref = np.exp(lam[i, h]) * S + S_C[i, h]
                 assert rel(got["S"][i, h], Sref) < TOL, ("S", fam, i, h)
+
+
+def check_kda_with_one_gate_is_dense():
+    """KDA (a gate per channel) with every channel's gate equal to one value is the
+    gated delta rule: same state, outputs and operator as the dense family."""
+    k, v, alpha, beta, q = _inputs(KDA, 1, 17, 2, 6, 4, seed=190, q=True)
+    one = np.ascontiguousarray(alpha[..., 0])
+    same = np.repeat(one[..., None], 6, axis=-1)
+    kda = oracle.sequential(KDA, k, v, same, beta, q=q, want_o=True)
+    dense = oracle.sequential(DENSE, k, v, one, beta, q=q, want_o=True)
+    assert rel(kda["S"], dense["S"]) < TOL and rel(kda["o"], dense["o"]) < TOL
+    Tk = np.exp(kda["lam"])[..., None, None] * kda["M"]
+    Td = np.exp(dense["lam"])[..., None, None] * dense["M"]
+    assert rel(Tk, Td) < TOL
+
+
+def check_kda_without_erasure_is_per_channel_decay():
+    """beta = 0: nothing is written or erased, and T_C is diag(prod_t alpha_t), the
+    diagonal family's operator (closed form)."""
+    k, v, alpha, _, _ = _inputs(KDA, 1, 12, 2, 5, 3, seed=191)
+    beta = np.zeros(alpha.shape[:3])
+    out = oracle.sequential(KDA, k, v, alpha, beta)
+    assert np.all(out["S"] == 0)
+    T = np.exp(out["lam"])[..., None, None] * out["M"]
+    for h in range(2):
+        assert rel(T[0, h], np.diag(np.prod(alpha[0, :, h], axis=0))) < TOL
 
 
 ALL_CHECKS = [
@@ -532,4 +566,6 @@ ALL_CHECKS = [
     check_segment_independence,
     check_seam_window_equals_sequential,
     check_seam_window_pure_decay_closed_form,
+    check_kda_with_one_gate_is_dense,
+    check_kda_without_erasure_is_per_channel_decay,
 ]

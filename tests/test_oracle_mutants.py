@@ -42,6 +42,12 @@ MUTANTS = [
      "a * (S[(size_t)r * dv + j] + b * kt[r] * kS[j])", 0),
     ("seam_diag_gate_index", "at[r] * S[(size_t)r * dv + j]", "at[0] * S[(size_t)r * dv + j]", 0),
     ("seam_output_reads_key", "acc += S[(size_t)r * dv + j] * qt[r];", "acc += S[(size_t)r * dv + j] * kt[r];", 0),
+    ("kda_gate_index", "at[i] * (S[(size_t)i * dv + j] - b * kt[i] * kS[j])",
+     "at[0] * (S[(size_t)i * dv + j] - b * kt[i] * kS[j])", 0),
+    ("kda_M_drops_gate", "M[(size_t)i * dk + j] = at[i] * (M[(size_t)i * dk + j] - b * kt[i] * kS[j]);",
+     "M[(size_t)i * dk + j] = (M[(size_t)i * dk + j] - b * kt[i] * kS[j]);", 0),
+    ("seam_kda_one_gate", "const double a = fam == OR_KDA ? alpha[row * dk + r] : alpha[row];",
+     "const double a = fam == OR_KDA ? alpha[row * dk] : alpha[row];", 0),
     ("seam_token_order", "const int64_t row = (i * w + t) * H + h;", "const int64_t row = (i * w + (w - 1 - t)) * H + h;", 0),
 ]
 
