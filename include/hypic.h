@@ -14,12 +14,14 @@
  *   requests become parallel": a combine step folds the pairs of many segments
  *   into the request's running state.
  *
- * The pages print no per-token rule.  This library reads the three families
- * named there as (state S in R^{dk x dv}, fp32):
+ * The pages print no per-token rule.  This library reads the families named
+ * there as (state S in R^{dk x dv}, fp32):
  *   S_t = T_t S_{t-1} + beta_t k_t v_t^T,  o_t = S_t^T q_t  (state after token t)
  *     HYPIC_SCALAR : T_t = alpha_t I                       (RetNet, Mamba2)
  *     HYPIC_DIAG   : T_t = diag(alpha_t), alpha_t in R^dk  (GLA; gates the key axis)
  *     HYPIC_DENSE  : T_t = alpha_t (I - beta_t k_t k_t^T)  (gated delta rule)
+ *     HYPIC_KDA    : T_t = diag(alpha_t) (I - beta_t k_t k_t^T), alpha_t in R^dk
+ *                    (KDA-style: the gated delta rule with a gate per channel)
  *   T_C = T_L ... T_1,  S(C|0) = S_L from S_0 = 0.
  * T_C is stored in log-scaled form T_C = exp(lambda) * M, because the plain
  * product underflows fp32 (and fp64) at the segment lengths of long prompts:
@@ -27,6 +29,8 @@
  *   diag  : lambda [.., H, dk] = sum_t log alpha_{t,i};      M is I (not stored)
  *   dense : lambda [.., H], M [.., H, dk, dk] with max|M| in [1, 2)
  *           (M == 0 exactly only for a product that is exactly zero).
+ *   kda   : as dense, with the per-channel gates inside M (lambda holds only
+ *           the power-of-two rescaling).
  *
  * Conventions for every entry point:
  *   - All tensor pointers are DEVICE pointers owned by the caller; the library
@@ -64,7 +68,7 @@ typedef enum {
                                 the kernel left its outputs incomplete and released its resources */
 } hypic_status;
 
-typedef enum { HYPIC_SCALAR = 0, HYPIC_DIAG = 1, HYPIC_DENSE = 2 } hypic_family;
+typedef enum { HYPIC_SCALAR = 0, HYPIC_DIAG = 1, HYPIC_DENSE = 2, HYPIC_KDA = 3 } hypic_family;
 
 typedef enum { HYPIC_BF16 = 0, HYPIC_F32 = 1 } hypic_dtype;
 
@@ -82,16 +86,17 @@ typedef enum { HYPIC_BF16 = 0, HYPIC_F32 = 1 } hypic_dtype;
  *   q                  [n_layers, N, H, d_k]; required iff o_out != NULL
  *   k                  [n_layers, N, H, d_k]
  *   v                  [n_layers, N, H, d_v]
- *   alpha   fp32       [n_layers, N, H] (scalar, dense) or [n_layers, N, H, d_k] (diag)
+ *   alpha   fp32       [n_layers, N, H] (scalar, dense) or [n_layers, N, H, d_k] (diag, kda)
  *   beta    fp32       [n_layers, N, H] or NULL (=> 1 for every token)
  *   lam_out fp32       [n_layers, n_seg, H] or [n_layers, n_seg, H, d_k] (diag)
- *   M_out   fp32       [n_layers, n_seg, H, d_k, d_k]; dense: required; else must be NULL
+ *   M_out   fp32       [n_layers, n_seg, H, d_k, d_k]; dense, kda: required; else NULL
  *   S_out   fp32       [n_layers, n_seg, H, d_k, d_v]
  *   o_out   in_dtype   [n_layers, N, H, d_v] or NULL; o_t = S_t^T q_t
  *   d_err              device int or NULL (see conventions)
  * An empty segment yields lambda = 0, M = I, S = 0.
- * Alignment: q, k, v, o_out, S_out, M_out and the diag alpha / lambda must be
- * 16-byte aligned; other pointers 4-byte (seg_offsets 8-byte).
+ * Alignment: q, k, v, o_out, S_out, M_out, the diag / kda alpha and the diag
+ * lambda must be 16-byte aligned; other pointers 4-byte (seg_offsets 8-byte).
+ * The KDA family runs on the token-by-token fp32 kernel (CUDA cores).
  */
 int hypic_segment_scan(int fam, int in_dtype, int n_layers, int n_seg,
                        int64_t total_tokens, int n_heads, int d_k, int d_v,
@@ -175,13 +180,13 @@ int hypic_segment_scan_static(int fam, int in_dtype, int n_layers, int n_seg,
  * addition.)  Optionally also the operator of the concatenation,
  * T(C1.C2) = T(C2) T(C1), which makes compositions chainable in any grouping.
  *   lam     fp32  [n, H] (scalar, dense) or [n, H, d_k] (diag)   -- T(C2)
- *   M       fp32  [n, H, d_k, d_k] (dense; must be NULL otherwise)
+ *   M       fp32  [n, H, d_k, d_k] (dense, kda; must be NULL otherwise)
  *   S_prev  fp32  [n, H, d_k, d_v] or NULL (=> 0)                 -- S(C1)
  *   S_C     fp32  [n, H, d_k, d_v]                                -- S(C2)
  *   S_out   fp32  [n, H, d_k, d_v]; may be the same pointer as S_prev
  *                 (scalar, diag and dense); must not overlap S_C otherwise
  *   lam_prev, lam_out  like lam; both NULL or both given          -- T(C1), T(C1.C2)
- *   M_prev, M_out      like M (dense; given iff lam_out is)
+ *   M_prev, M_out      like M (dense, kda; given iff lam_out is)
  * Dense M_out has max|M_out| in [1, 2) (exact power-of-two scaling into lam_out).
  * All pointers 16-byte aligned except scalar/dense lambdas (4-byte).
  */
@@ -201,7 +206,7 @@ int hypic_compose(int fam, int n, int n_heads, int d_k, int d_v, const float *la
  *   chain_len  int32 [n_req]            0 <= chain_len[r] <= max_chain
  *   seg_idx    int32 [n_req, max_chain] pool indices in prompt order
  *   pool_lam   fp32  [pool_size, n_layers, H] or [pool_size, n_layers, H, d_k] (diag)
- *   pool_M     fp32  [pool_size, n_layers, H, d_k, d_k] (dense; NULL otherwise)
+ *   pool_M     fp32  [pool_size, n_layers, H, d_k, d_k] (dense, kda; NULL otherwise)
  *   pool_S     fp32  [pool_size, n_layers, H, d_k, d_v]
  *   S_init     fp32  [n_req, n_layers, H, d_k, d_v] or NULL (=> 0)
  *   S_out      fp32  [n_req, n_layers, H, d_k, d_v]; may alias S_init
@@ -226,10 +231,10 @@ int hypic_compose_chain(int fam, int n_req, int n_layers, int n_heads, int d_k, 
  *   in_dtype  HYPIC_BF16 or HYPIC_F32: q, k, v and o_out
  *   q, k    [n, w, H, d_k];  v [n, w, H, d_v]      -- the seam tokens (q may be
  *                                                   NULL when o_out is NULL)
- *   alpha   fp32 [n, w, H] (scalar, dense) or [n, w, H, d_k] (diag)
+ *   alpha   fp32 [n, w, H] (scalar, dense) or [n, w, H, d_k] (diag, kda)
  *   beta    fp32 [n, w, H] or NULL (=> 1)
  *   lam     fp32 [n, H] or [n, H, d_k] (diag)     -- T_body of the cached rest
- *   M       fp32 [n, H, d_k, d_k] (dense; NULL otherwise)
+ *   M       fp32 [n, H, d_k, d_k] (dense, kda; NULL otherwise)
  *   S_prev  fp32 [n, H, d_k, d_v] or NULL (=> 0)   -- state before the segment
  *   S_C     fp32 [n, H, d_k, d_v]                  -- S_body of the cached rest
  *   S_out   fp32 [n, H, d_k, d_v]; may be the same pointer as S_prev, must not

@@ -26,14 +26,15 @@ import torch
 
 from . import _build
 
-SCALAR, DIAG, DENSE = 0, 1, 2
-FAMILIES = {"scalar": SCALAR, "diag": DIAG, "dense": DENSE}
+SCALAR, DIAG, DENSE, KDA = 0, 1, 2, 3
+FAMILIES = {"scalar": SCALAR, "diag": DIAG, "dense": DENSE, "kda": KDA}
+WITH_M = (DENSE, KDA)   # families whose operator is exp(lambda) M
 BF16, F32 = 0, 1
 STATUS = {0: "HYPIC_OK", -1: "HYPIC_EINVAL", -2: "HYPIC_EUNSUPPORTED", -3: "HYPIC_EALIGN",
           -4: "HYPIC_ECUDA", -5: "HYPIC_EINDEX", -6: "HYPIC_ETIMEOUT"}
 
 __all__ = ["segment_scan", "segment_scan_workspace_bytes", "segment_scan_static", "compose", "compose_chain", "status_string", "library", "use_library",
-           "HypicError", "SCALAR", "DIAG", "DENSE"]
+           "HypicError", "SCALAR", "DIAG", "DENSE", "KDA"]
 
 
 class HypicError(RuntimeError):
@@ -148,9 +149,9 @@ def segment_scan(family, k, v, alpha, seg_offsets, beta=None, q=None, want_o=Fal
     """(T_C, S(C|0)) for every (layer, segment, head); optionally o_t.
 
     k [Lyr,N,H,dk], v [Lyr,N,H,dv] (bf16 or fp32), alpha fp32 [Lyr,N,H] or
-    [Lyr,N,H,dk] (diag), beta fp32 [Lyr,N,H] or None, q like k (for o_t),
+    [Lyr,N,H,dk] (diag, kda), beta fp32 [Lyr,N,H] or None, q like k (for o_t),
     seg_offsets int64 [n_seg+1] on the device.  ``out`` may hold preallocated
-    ``lam``, ``M``, ``S``, ``o`` tensors.  Returns a dict with lam, S, M (dense), o.
+    ``lam``, ``M``, ``S``, ``o`` tensors.  Returns a dict with lam, S, M (dense, kda), o.
 
     ``workspace``: "auto" (default) allocates the device scratch the two-pass
     form needs (through torch, on the launch stream) and calls
@@ -178,13 +179,13 @@ def segment_scan(family, k, v, alpha, seg_offsets, beta=None, q=None, want_o=Fal
         out["lam"] = torch.empty(lam_shape, dtype=torch.float32, device=dev)
     if "S" not in out:
         out["S"] = torch.empty((Lyr, n_seg, H, dk, dv), dtype=torch.float32, device=dev)
-    if fam == DENSE and "M" not in out:
+    if fam in WITH_M and "M" not in out:
         out["M"] = torch.empty((Lyr, n_seg, H, dk, dk), dtype=torch.float32, device=dev)
     if want_o and "o" not in out:
         out["o"] = torch.empty((Lyr, N, H, dv), dtype=dt, device=dev)
     args = (fam, BF16 if dt == torch.bfloat16 else F32, Lyr, n_seg, N, H, dk, dv,
             _ptr(seg_offsets), _ptr(q if want_o else None), _ptr(k), _ptr(v), _ptr(alpha),
-            _ptr(beta), _ptr(out["lam"]), _ptr(out.get("M") if fam == DENSE else None),
+            _ptr(beta), _ptr(out["lam"]), _ptr(out.get("M") if fam in WITH_M else None),
             _ptr(out["S"]), _ptr(out.get("o") if want_o else None))
     if workspace is None:
         st = library().hypic_segment_scan(*args, _ptr(d_err), _stream(stream))
@@ -249,18 +250,18 @@ def compose(family, lam, S_C, S_prev=None, M=None, lam_prev=None, M_prev=None, S
     want_T = lam_prev is not None
     if want_T and lam_out is None:
         lam_out = torch.empty_like(lam)
-    if want_T and fam == DENSE and M_out is None:
+    if want_T and fam in WITH_M and M_out is None:
         M_out = torch.empty_like(M)
     st = library().hypic_compose(fam, n, H, dk, dv, _ptr(lam), _ptr(M), _ptr(S_prev), _ptr(S_C),
                                  _ptr(S_out), _ptr(lam_prev), _ptr(M_prev),
                                  _ptr(lam_out if want_T else None),
-                                 _ptr(M_out if (want_T and fam == DENSE) else None),
+                                 _ptr(M_out if (want_T and fam in WITH_M) else None),
                                  _stream(stream))
     _check("hypic_compose", st)
     res = {"S": S_out}
     if want_T:
         res["lam"] = lam_out
-        if fam == DENSE:
+        if fam in WITH_M:
             res["M"] = M_out
     return res
 
@@ -271,7 +272,7 @@ def seam_compose(family, k, v, alpha, lam, S_C, S_prev=None, M=None, beta=None, 
 
     k [n,w,H,dk], v [n,w,H,dv] (bf16 or fp32), alpha [n,w,H] or [n,w,H,dk], beta
     [n,w,H] or None, q [n,w,H,dk] (needed iff want_o); lam [n,H] or [n,H,dk],
-    M [n,H,dk,dk] (dense), S_prev (or None) and S_C [n,H,dk,dv] fp32.  Returns a
+    M [n,H,dk,dk] (dense, kda), S_prev (or None) and S_C [n,H,dk,dv] fp32.  Returns a
     dict with S [n,H,dk,dv] and, if asked, o [n,w,H,dv] in the input dtype.
     S_out may be S_prev (in place).
     """
@@ -310,7 +311,7 @@ def compose_chain(family, chain_len, seg_idx, pool_lam, pool_S, pool_M=None, S_i
                   S_out=None, d_err=None, stream=None):
     """Fold pool entries seg_idx[r, :chain_len[r]] in order: S <- T_p S + S_p.
 
-    pool_lam [P,Lyr,H] or [P,Lyr,H,dk], pool_M [P,Lyr,H,dk,dk] (dense),
+    pool_lam [P,Lyr,H] or [P,Lyr,H,dk], pool_M [P,Lyr,H,dk,dk] (dense, kda),
     pool_S [P,Lyr,H,dk,dv], S_init [R,Lyr,H,dk,dv] or None.  Returns S [R,Lyr,H,dk,dv].
     """
     fam = _fam(family)

@@ -43,6 +43,12 @@ bool aligned(const void *p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0;
 
 bool head_size_ok(int d) { return d == 32 || d == 64 || d == 128; }
 
+bool family_ok(int fam) { return fam >= HYPIC_SCALAR && fam <= HYPIC_KDA; }
+bool has_m(int fam) { return fam == HYPIC_DENSE || fam == HYPIC_KDA; }        // operator exp(lambda) M
+bool gate_per_channel(int fam) { return fam == HYPIC_DIAG || fam == HYPIC_KDA; }
+// the composition of a KDA pair is that of a dense pair: both are (lambda, M)
+int compose_family(int fam) { return fam == HYPIC_KDA ? HYPIC_DENSE : fam; }
+
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? HYPIC_OK : HYPIC_ECUDA; }
 
 }  // namespace
@@ -75,7 +81,7 @@ int scan_args(int fam, int in_dtype, int n_layers, int n_seg, int64_t total_toke
               const float *alpha, const float *beta, float *lam_out, float *M_out, float *S_out, void *o_out,
               int *d_err, hypic::ScanArgs &a, bool &nothing_to_do) {
     nothing_to_do = false;
-    if (fam < HYPIC_SCALAR || fam > HYPIC_DENSE) return HYPIC_EINVAL;
+    if (!family_ok(fam)) return HYPIC_EINVAL;
     if (in_dtype != HYPIC_BF16 && in_dtype != HYPIC_F32) return HYPIC_EINVAL;
     if (n_layers < 0 || n_seg < 0 || total_tokens < 0 || n_heads <= 0) return HYPIC_EINVAL;
     if (!head_size_ok(d_k) || !head_size_ok(d_v)) return HYPIC_EUNSUPPORTED;
@@ -88,10 +94,10 @@ int scan_args(int fam, int in_dtype, int n_layers, int n_seg, int64_t total_toke
     const bool has_tokens = total_tokens > 0;
     if (!seg_offsets || !lam_out || !S_out) return HYPIC_EINVAL;
     if (has_tokens && (!k || !v || !alpha)) return HYPIC_EINVAL;
-    if ((fam == HYPIC_DENSE) != (M_out != nullptr)) return HYPIC_EINVAL;
+    if (has_m(fam) != (M_out != nullptr)) return HYPIC_EINVAL;
     if (o_out && !q && has_tokens) return HYPIC_EINVAL;
     if (!aligned(seg_offsets, 8)) return HYPIC_EALIGN;
-    const void *a16[] = {q, k, v, o_out, S_out, M_out, fam == HYPIC_DIAG ? alpha : nullptr,
+    const void *a16[] = {q, k, v, o_out, S_out, M_out, gate_per_channel(fam) ? alpha : nullptr,
                          fam == HYPIC_DIAG ? lam_out : nullptr};
     for (const void *p : a16)
         if (p && !aligned(p, 16)) return HYPIC_EALIGN;
@@ -145,8 +151,7 @@ int hypic_segment_scan(int fam, int in_dtype, int n_layers, int n_seg, int64_t t
 int64_t hypic_segment_scan_workspace_bytes(int fam, int in_dtype, int n_layers, int n_seg,
                                            int64_t total_tokens, int n_heads, int d_k, int d_v,
                                            int with_o) {
-    if (fam < HYPIC_SCALAR || fam > HYPIC_DENSE || n_layers < 0 || n_seg < 0 || total_tokens < 0 || n_heads <= 0)
-        return HYPIC_EINVAL;
+    if (!family_ok(fam) || n_layers < 0 || n_seg < 0 || total_tokens < 0 || n_heads <= 0) return HYPIC_EINVAL;
     hypic::ScanArgs a{};
     a.fam = fam;
     a.in_dtype = in_dtype;
@@ -215,15 +220,15 @@ int hypic_segment_scan_static(int fam, int in_dtype, int n_layers, int n_seg, in
 int hypic_compose(int fam, int n, int n_heads, int d_k, int d_v, const float *lam, const float *M,
                   const float *S_prev, const float *S_C, float *S_out, const float *lam_prev,
                   const float *M_prev, float *lam_out, float *M_out, void *cuda_stream) {
-    if (fam < HYPIC_SCALAR || fam > HYPIC_DENSE) return HYPIC_EINVAL;
+    if (!family_ok(fam)) return HYPIC_EINVAL;
     if (n < 0 || n_heads <= 0) return HYPIC_EINVAL;
     if (!head_size_ok(d_k) || !head_size_ok(d_v)) return HYPIC_EUNSUPPORTED;
     if ((int64_t)n * n_heads > INT32_MAX) return HYPIC_EUNSUPPORTED;
     if (n == 0) return HYPIC_OK;
     if (!lam || !S_C || !S_out) return HYPIC_EINVAL;
-    if ((fam == HYPIC_DENSE) != (M != nullptr)) return HYPIC_EINVAL;
+    if (has_m(fam) != (M != nullptr)) return HYPIC_EINVAL;
     if ((lam_prev == nullptr) != (lam_out == nullptr)) return HYPIC_EINVAL;
-    if (fam == HYPIC_DENSE) {
+    if (has_m(fam)) {
         if ((M_prev == nullptr) != (lam_out == nullptr) || (M_out == nullptr) != (lam_out == nullptr))
             return HYPIC_EINVAL;
     } else if (M_prev || M_out) {
@@ -247,13 +252,13 @@ int hypic_compose(int fam, int n, int n_heads, int d_k, int d_v, const float *la
     };
     if (S_out != S_C && overlaps(S_out, sbytes, S_C, sbytes)) return HYPIC_EINVAL;
     if (S_prev && S_out != S_prev && overlaps(S_out, sbytes, S_prev, sbytes)) return HYPIC_EINVAL;
-    if (fam == HYPIC_DENSE &&
+    if (has_m(fam) &&
         (overlaps(S_out, sbytes, M, mbytes) || overlaps(S_out, sbytes, M_prev, mbytes) ||
          overlaps(M_out, mbytes, M, mbytes) || overlaps(M_out, mbytes, M_prev, mbytes)))
         return HYPIC_EINVAL;
 
     hypic::ComposeArgs a;
-    a.fam = fam;
+    a.fam = compose_family(fam);
     a.n = n;
     a.H = n_heads;
     a.dk = d_k;
@@ -274,7 +279,7 @@ int hypic_seam_compose(int fam, int in_dtype, int n, int w, int n_heads, int d_k
                        const void *k, const void *v, const float *alpha, const float *beta, const float *lam,
                        const float *M, const float *S_prev, const float *S_C, float *S_out, void *o_out,
                        void *cuda_stream) {
-    if (fam < HYPIC_SCALAR || fam > HYPIC_DENSE) return HYPIC_EINVAL;
+    if (!family_ok(fam)) return HYPIC_EINVAL;
     if (in_dtype != HYPIC_BF16 && in_dtype != HYPIC_F32) return HYPIC_EINVAL;
     if (n < 0 || n_heads <= 0 || w < 0) return HYPIC_EINVAL;
     if (w > 4096) return HYPIC_EUNSUPPORTED;
@@ -282,7 +287,7 @@ int hypic_seam_compose(int fam, int in_dtype, int n, int w, int n_heads, int d_k
     if ((int64_t)n * n_heads * (d_v / 32) > INT32_MAX) return HYPIC_EUNSUPPORTED;   // one CTA per 32 columns
     if (n == 0) return HYPIC_OK;
     if (!lam || !S_C || !S_out) return HYPIC_EINVAL;
-    if ((fam == HYPIC_DENSE) != (M != nullptr)) return HYPIC_EINVAL;
+    if (has_m(fam) != (M != nullptr)) return HYPIC_EINVAL;
     if (w > 0 && (!k || !v || !alpha || (o_out && !q))) return HYPIC_EINVAL;
     const void *a16[] = {M, S_prev, S_C, S_out, fam == HYPIC_DIAG ? lam : nullptr};
     for (const void *p : a16)
@@ -338,7 +343,7 @@ int hypic_compose_chain(int fam, int n_req, int n_layers, int n_heads, int d_k, 
                         int pool_size, const float *pool_lam, const float *pool_M,
                         const float *pool_S, const float *S_init, float *S_out, int *d_err,
                         void *cuda_stream) {
-    if (fam < HYPIC_SCALAR || fam > HYPIC_DENSE) return HYPIC_EINVAL;
+    if (!family_ok(fam)) return HYPIC_EINVAL;
     if (n_req < 0 || n_layers < 0 || n_heads <= 0 || max_chain < 0 || pool_size < 0)
         return HYPIC_EINVAL;
     if (!head_size_ok(d_k) || !head_size_ok(d_v)) return HYPIC_EUNSUPPORTED;
@@ -346,7 +351,7 @@ int hypic_compose_chain(int fam, int n_req, int n_layers, int n_heads, int d_k, 
     if (n_req == 0 || n_layers == 0) return HYPIC_OK;
     if (!chain_len || !S_out) return HYPIC_EINVAL;
     if (max_chain > 0 && (!seg_idx || pool_size == 0 || !pool_lam || !pool_S)) return HYPIC_EINVAL;
-    if (max_chain > 0 && (fam == HYPIC_DENSE) != (pool_M != nullptr)) return HYPIC_EINVAL;
+    if (max_chain > 0 && has_m(fam) != (pool_M != nullptr)) return HYPIC_EINVAL;
     const void *a16[] = {pool_M, pool_S, S_init, S_out, fam == HYPIC_DIAG ? pool_lam : nullptr};
     for (const void *p : a16)
         if (p && !aligned(p, 16)) return HYPIC_EALIGN;
@@ -355,7 +360,7 @@ int hypic_compose_chain(int fam, int n_req, int n_layers, int n_heads, int d_k, 
         if (p && !aligned(p, 4)) return HYPIC_EALIGN;
 
     hypic::ChainArgs a;
-    a.fam = fam;
+    a.fam = compose_family(fam);
     a.R = n_req;
     a.n_layers = n_layers;
     a.H = n_heads;

@@ -3,9 +3,10 @@
 // One CTA walks one (layer, segment, head) chain token by token, exactly the
 // recurrence of the family (S_t = T_t S_{t-1} + beta_t k_t v_t^T, see hypic.h),
 // keeping the state in registers.  It serves every family and the optional
-// per-token output o_t = S_t^T q_t, and is the path for fp32 inputs and for
-// scalar/diagonal scans that ask for o_t.  The transition of the dense family
-// is carried as exp(lambda) * M with M renormalised by exact powers of two.
+// per-token output o_t = S_t^T q_t, and is the path for fp32 inputs, for
+// scalar/diagonal scans that ask for o_t and for the KDA family.  The transition
+// of the dense and KDA families is carried as exp(lambda) * M with M renormalised
+// by exact powers of two (KDA's per-channel gates stay inside M).
 //
 // Thread layout: the state (and, for the dense family, M) is split by
 // columns: thread (g, c) owns column c and rows [g*RPT, (g+1)*RPT).  A token
@@ -29,8 +30,9 @@ template <int FAM, int DK, typename TIn>
 __global__ void __launch_bounds__(512) scan_recurrent_kernel(const ScanArgs a) {
     constexpr int RPT = DK < 64 ? DK : 64;   // rows per thread
     constexpr int G = DK / RPT;              // row groups
-    constexpr bool kDense = FAM == HYPIC_DENSE;
-    constexpr bool kDiag = FAM == HYPIC_DIAG;
+    constexpr bool kDense = FAM == HYPIC_DENSE || FAM == HYPIC_KDA;   // erasing update, M columns
+    constexpr bool kKda = FAM == HYPIC_KDA;
+    constexpr bool kDiag = FAM == HYPIC_DIAG || FAM == HYPIC_KDA;     // a gate per channel
     const int DV = a.dv;
     const int NCOL = (kDense ? DK : 0) + DV;
     const int NT = NCOL * G;
@@ -99,7 +101,31 @@ __global__ void __launch_bounds__(512) scan_recurrent_kernel(const ScanArgs a) {
         for (int tt = 0; tt < nt; ++tt) {
             const float *kt = sk + tt * DK + row0;
             const float b = sb[tt];
-            if (kDense) {
+            if (kKda) {
+                // T_t = diag(alpha) (I - beta k k^T): erase, then gate each row
+                const float *at = sa + tt * DK + row0;
+                float p = 0.f;
+#pragma unroll
+                for (int r = 0; r < RPT; ++r) p = fmaf(kt[r], x[r], p);
+                float u = p;
+                if (G > 1) {
+                    float *rb = red + (tt & 1) * G * NCOL;
+                    rb[g * NCOL + c] = p;
+                    __syncthreads();
+                    u = 0.f;
+#pragma unroll
+                    for (int gg = 0; gg < G; ++gg) u += rb[gg * NCOL + c];
+                }
+                const float w = -b * u;
+                if (mcol) {
+#pragma unroll
+                    for (int r = 0; r < RPT; ++r) x[r] = at[r] * fmaf(kt[r], w, x[r]);
+                } else {
+                    const float bv = b * sv[tt * DV + scol];
+#pragma unroll
+                    for (int r = 0; r < RPT; ++r) x[r] = fmaf(kt[r], bv, at[r] * fmaf(kt[r], w, x[r]));
+                }
+            } else if (kDense) {
                 const float al = sa[tt];
                 float p = 0.f;
 #pragma unroll
@@ -200,7 +226,7 @@ __global__ void __launch_bounds__(512) scan_recurrent_kernel(const ScanArgs a) {
 #pragma unroll
         for (int r = 0; r < RPT; ++r) Mo[(int64_t)(row0 + r) * DK + c] = x[r];
     }
-    if (kDiag) {
+    if (FAM == HYPIC_DIAG) {   // lambda per channel
         if (tid < DK) a.lam_out[u_out * DK + tid] = lam_sum;
     } else if (tid == 0) {
         const double lam = (double)lam_sum + (double)lam_exp * 0.69314718055994530942;
@@ -212,11 +238,12 @@ template <int FAM, int DK, typename TIn>
 cudaError_t launch_one(const ScanArgs &a, cudaStream_t s) {
     constexpr int RPT = DK < 64 ? DK : 64;
     constexpr int G = DK / RPT;
-    const int ncol = (FAM == HYPIC_DENSE ? DK : 0) + a.dv;
+    constexpr bool kM = FAM == HYPIC_DENSE || FAM == HYPIC_KDA;
+    const int ncol = (kM ? DK : 0) + a.dv;
     const int nt = ncol * G;
     const bool want_o = a.o_out != nullptr;
     size_t floats = (size_t)kTB * DK + (size_t)kTB * a.dv + (want_o ? (size_t)kTB * DK : 0) +
-                    (size_t)kTB * (FAM == HYPIC_DIAG ? DK : 1) + kTB + 2 * G * ncol + G * a.dv + 32;
+                    (size_t)kTB * (FAM == HYPIC_DIAG || FAM == HYPIC_KDA ? DK : 1) + kTB + 2 * G * ncol + G * a.dv + 32;
     const size_t smem = floats * sizeof(float);
     auto kern = scan_recurrent_kernel<FAM, DK, TIn>;
     if (smem > 48 * 1024) {
@@ -244,6 +271,7 @@ cudaError_t launch_fam(const ScanArgs &a, cudaStream_t s) {
         case HYPIC_SCALAR: return launch_dk<HYPIC_SCALAR, TIn>(a, s);
         case HYPIC_DIAG: return launch_dk<HYPIC_DIAG, TIn>(a, s);
         case HYPIC_DENSE: return launch_dk<HYPIC_DENSE, TIn>(a, s);
+        case HYPIC_KDA: return launch_dk<HYPIC_KDA, TIn>(a, s);
     }
     return cudaErrorInvalidValue;
 }

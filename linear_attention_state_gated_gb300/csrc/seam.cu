@@ -19,9 +19,9 @@
 // the gated delta rule, S^T q for the output) go through shared memory across
 // the row groups.  The window's inputs are staged in shared memory a block of
 // tokens at a time.  Scalar and diagonal T_body (exp(lambda) per head or per
-// row) are applied here; for the dense family this kernel writes the advanced
-// state and the product with T_body = exp(lambda) M runs as a composition
-// afterwards.
+// row) are applied here; for the dense and KDA families (the latter a gate per
+// channel inside the erasing update) this kernel writes the advanced state and
+// the product with T_body = exp(lambda) M runs as a composition afterwards.
 #include "internal.cuh"
 
 namespace hypic {
@@ -71,11 +71,13 @@ __global__ void __launch_bounds__(kCW *(DK / 32)) seam_kernel(const SeamArgs a) 
     constexpr int RS = DK / 32;               // row groups
     constexpr int NT = kCW * RS;
     constexpr int NS = DV / kCW;              // column slices per (item, head)
-    constexpr int NA = FAM == HYPIC_DIAG ? DK : 1;   // gates per token
+    constexpr bool kDelta = FAM == HYPIC_DENSE || FAM == HYPIC_KDA;   // erasing update, operator exp(lambda) M
+    constexpr bool kGateRow = FAM == HYPIC_DIAG || FAM == HYPIC_KDA;  // a gate per channel
+    constexpr int NA = kGateRow ? DK : 1;            // gates per token
     __shared__ float sk[kTB][DK], sq[kTB][DK], sv[kTB][kCW], sa[kTB][NA], sb[kTB];
     __shared__ float red[2][RS][kCW];                        // S^T k partials, by token parity
     __shared__ float ro[RS][kTB][kCW];                       // output partials of a block of tokens
-    __shared__ float sc[FAM == HYPIC_DENSE ? 1 : DK][kCW];   // S_body slice (scalar, diag)
+    __shared__ float sc[kDelta ? 1 : DK][kCW];               // S_body slice (scalar, diag)
     __shared__ float sl[FAM == HYPIC_DIAG ? DK : 1];         // exp(lambda_body) per row (diag)
 
     const int tid = threadIdx.x;
@@ -89,7 +91,7 @@ __global__ void __launch_bounds__(kCW *(DK / 32)) seam_kernel(const SeamArgs a) 
 
     // S_body's slice starts on its way to shared memory now, so its latency overlaps
     // the window (each thread copies, and later reads, its own elements)
-    if (FAM != HYPIC_DENSE) {
+    if (!kDelta) {
 #pragma unroll
         for (int r = 0; r < 32; ++r) cp_async4(&sc[g * 32 + r][jl], a.S_C + so + (int64_t)(g * 32 + r) * DV + j);
     }
@@ -110,7 +112,7 @@ __global__ void __launch_bounds__(kCW *(DK / 32)) seam_kernel(const SeamArgs a) 
             const int64_t row = (item * a.w + t0 + t) * a.H + h;   // seam token-head row
             sk[t][c] = ld_in(k, row * DK + c);
             if (o) sq[t][c] = ld_in(q, row * DK + c);
-            if (FAM == HYPIC_DIAG) sa[t][c] = a.alpha[row * DK + c];
+            if (kGateRow) sa[t][c] = a.alpha[row * DK + c];
         }
         for (int e = tid; e < nt * kCW; e += NT) {
             const int t = e / kCW, c = e % kCW;
@@ -118,7 +120,7 @@ __global__ void __launch_bounds__(kCW *(DK / 32)) seam_kernel(const SeamArgs a) 
         }
         if (tid < nt) {
             const int64_t row = (item * a.w + t0 + tid) * a.H + h;
-            if (FAM != HYPIC_DIAG) sa[tid][0] = a.alpha[row];
+            if (!kGateRow) sa[tid][0] = a.alpha[row];
             sb[tid] = a.beta ? a.beta[row] : 1.f;
         }
         __syncthreads();
@@ -129,7 +131,8 @@ __global__ void __launch_bounds__(kCW *(DK / 32)) seam_kernel(const SeamArgs a) 
                 const float b = sb[t];
                 const float *kt = &sk[t][g * 32];
                 float c;   // S <- alpha S + k c^T, column entry c_j
-                if (FAM == HYPIC_DENSE) {
+                float nbu = 0.f;   // KDA: -beta u_j (the erasure, before the per-row gate)
+                if (kDelta) {
                     // gated delta rule: c = beta (v - alpha u), u = S^T k (rows summed over the groups)
                     uint64_t p2 = 0;
 #pragma unroll
@@ -145,7 +148,12 @@ __global__ void __launch_bounds__(kCW *(DK / 32)) seam_kernel(const SeamArgs a) 
                     float u = 0.f;
 #pragma unroll
                     for (int x = 0; x < RS; ++x) u += red[t & 1][x][jl];
-                    c = b * (sv[t][jl] - sa[t][0] * u);
+                    if (FAM == HYPIC_DENSE) {
+                        c = b * (sv[t][jl] - sa[t][0] * u);
+                    } else {   // KDA: S <- diag(alpha) (S - beta k u^T) + beta k v^T
+                        c = b * sv[t][jl];
+                        nbu = -b * u;
+                    }
                 } else {
                     c = b * sv[t][jl];
                 }
@@ -154,15 +162,21 @@ __global__ void __launch_bounds__(kCW *(DK / 32)) seam_kernel(const SeamArgs a) 
                 for (int rq = 0; rq < 8; ++rq) {
                     const float4 k4 = *reinterpret_cast<const float4 *>(kt + 4 * rq);
                     uint64_t a01, a23;
-                    if (FAM == HYPIC_DIAG) {
+                    if (kGateRow) {
                         const float4 a4 = *reinterpret_cast<const float4 *>(&sa[t][g * 32 + 4 * rq]);
                         a01 = pk2(a4.x, a4.y);
                         a23 = pk2(a4.z, a4.w);
                     } else {
                         a01 = a23 = pk2(sa[t][0], sa[t][0]);
                     }
-                    const uint64_t s01 = fma2(a01, pk2(S[4 * rq], S[4 * rq + 1]), mul2(pk2(k4.x, k4.y), cc));
-                    const uint64_t s23 = fma2(a23, pk2(S[4 * rq + 2], S[4 * rq + 3]), mul2(pk2(k4.z, k4.w), cc));
+                    uint64_t x01 = pk2(S[4 * rq], S[4 * rq + 1]), x23 = pk2(S[4 * rq + 2], S[4 * rq + 3]);
+                    if (FAM == HYPIC_KDA) {   // the erasure first, then the per-row gate
+                        const uint64_t nb = pk2(nbu, nbu);
+                        x01 = fma2(pk2(k4.x, k4.y), nb, x01);
+                        x23 = fma2(pk2(k4.z, k4.w), nb, x23);
+                    }
+                    const uint64_t s01 = fma2(a01, x01, mul2(pk2(k4.x, k4.y), cc));
+                    const uint64_t s23 = fma2(a23, x23, mul2(pk2(k4.z, k4.w), cc));
                     upk2(s01, S[4 * rq], S[4 * rq + 1]);
                     upk2(s23, S[4 * rq + 2], S[4 * rq + 3]);
                 }
@@ -198,13 +212,13 @@ __global__ void __launch_bounds__(kCW *(DK / 32)) seam_kernel(const SeamArgs a) 
     }
 
     // the rest of the segment: S_out = T_body S + S_body (dense: the advanced state only)
-    if (FAM != HYPIC_DENSE) cp_async_wait_all();
+    if (!kDelta) cp_async_wait_all();
     if (FAM == HYPIC_DIAG) __syncthreads();   // sl is in (also without a window)
     const float el = FAM == HYPIC_SCALAR ? expf(a.lam[unit]) : 1.f;
 #pragma unroll
     for (int r = 0; r < 32; ++r) {
         const int64_t e = so + (int64_t)(g * 32 + r) * DV + j;
-        if (FAM == HYPIC_DENSE)
+        if (kDelta)
             a.S_out[e] = S[r];
         else
             a.S_out[e] = fmaf(FAM == HYPIC_DIAG ? sl[g * 32 + r] : el, S[r], sc[g * 32 + r][jl]);
@@ -239,8 +253,8 @@ cudaError_t launch_seam_compose(const SeamArgs &a, cudaStream_t s) {
     cudaError_t e;
     if (a.fam == HYPIC_SCALAR) return launch_fam<HYPIC_SCALAR>(a, s);
     if (a.fam == HYPIC_DIAG) return launch_fam<HYPIC_DIAG>(a, s);
-    // dense: the window in place into S_out, then S_out = exp(lambda) M S_out + S_body
-    e = launch_fam<HYPIC_DENSE>(a, s);
+    // dense, KDA: the window in place into S_out, then S_out = exp(lambda) M S_out + S_body
+    e = a.fam == HYPIC_KDA ? launch_fam<HYPIC_KDA>(a, s) : launch_fam<HYPIC_DENSE>(a, s);
     if (e != cudaSuccess) return e;
     ComposeArgs c{};
     c.fam = HYPIC_DENSE;

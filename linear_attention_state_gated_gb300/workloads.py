@@ -31,7 +31,7 @@ import os
 
 import numpy as np
 
-SCALAR, DIAG, DENSE = 0, 1, 2
+SCALAR, DIAG, DENSE, KDA = 0, 1, 2, 3
 
 
 def rng(seed) -> np.random.Generator:
@@ -199,6 +199,22 @@ def dense_stack(seg_len: int = 512, n_layers: int = 30, H: int = 32, d: int = 12
     beta = _field(seed, 5, n_layers, N, (H,), _dense_beta, layers)
     return dict(family=DENSE, dtype="bf16", q=q, k=k, v=v, alpha=alpha, beta=beta,
                 seg_offsets=offs)
+
+
+def kda_stack(seg_len: int = 512, n_layers: int = 30, H: int = 32, d: int = 128, seed: int = 7,
+              with_q: bool = False, n_seg: int = 1, lengths=None, layers=None):
+    """KDA-style gates: the dense stack's law (bf16 q, v ~ N(0,1), k L2-normalised,
+    beta = sigmoid(N(0,1))) with alpha = exp(-0.1 softplus(N(0,1))) drawn per channel."""
+    if lengths is None:
+        lengths = [seg_len] * n_seg
+    offs = _offsets(lengths)
+    N = int(offs[-1])
+    k = _field(seed, 1, n_layers, N, (H, d), _unit_rows_bf16, layers)
+    v = _field(seed, 2, n_layers, N, (H, d), _normal_bf16, layers)
+    q = _field(seed, 3, n_layers, N, (H, d), _normal_bf16, layers) if with_q else None
+    alpha = _field(seed, 4, n_layers, N, (H, d), _dense_alpha, layers)
+    beta = _field(seed, 5, n_layers, N, (H,), _dense_beta, layers)
+    return dict(family=KDA, dtype="bf16", q=q, k=k, v=v, alpha=alpha, beta=beta, seg_offsets=offs)
 
 
 def rag_pool(family: int, P: int = 200, n_layers: int = 30, H: int = 32, d: int = 128,

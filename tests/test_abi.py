@@ -62,7 +62,7 @@ def scan(lib, fam=0, dtype=0, L=1, S=2, N=64, H=2, dk=128, dv=128, offs=A, q=0, 
 
 
 def test_scan_rejects_bad_arguments(lib):
-    assert scan(lib, fam=3) == EINVAL
+    assert scan(lib, fam=4) == EINVAL
     assert scan(lib, dtype=2) == EINVAL
     assert scan(lib, dk=96) == EUNSUP
     assert scan(lib, dv=256) == EUNSUP
@@ -72,6 +72,8 @@ def test_scan_rejects_bad_arguments(lib):
     assert scan(lib, alpha=0) == EINVAL
     assert scan(lib, Sout=0) == EINVAL
     assert scan(lib, fam=2, M=0) == EINVAL          # dense needs M_out
+    assert scan(lib, fam=3, M=0) == EINVAL          # so does KDA
+    assert scan(lib, fam=3, M=A + 0x100000, alpha=A + 4) == EALIGN   # KDA gates: 16-byte rows
     assert scan(lib, fam=0, M=A) == EINVAL          # scalar must not get M_out
     assert scan(lib, o=A, q=0) == EINVAL            # o_t needs q
     assert scan(lib, k=A + 8) == EALIGN
@@ -98,6 +100,7 @@ def test_workspace_size_and_checks(lib):
     assert ws(2, 0, 1, 3, 200, 2, 128, 128, 0) == 2 * (3 + 3) * 33568
     assert ws(2, 0, 1, 1, 2048, 2, 128, 128, 1) == 2 * (1 + 32) * 50192   # with o_t: Gq tiles and b_t too
     assert ws(2, 1, 1, 1, 2048, 2, 128, 128, 0) == 0     # fp32 inputs
+    assert ws(3, 0, 1, 1, 2048, 2, 128, 128, 0) == 0     # KDA: the token-by-token kernel
     assert ws(2, 0, 1, 1, 2048, 2, 64, 64, 0) == 0
     sd = 2 * 512 * (128 + 128 * 128) * 4      # diag: two partial slots per CTA, up to 512 CTAs
     assert ws(1, 0, 1, 1, 2048, 2, 128, 128, 0) == sd
@@ -126,6 +129,7 @@ def compose(lib, fam=0, n=3, H=2, dk=64, dv=64, lam=A, M=0, Sp=A, Sc=A + 0x10000
 
 def test_compose_rejects_bad_arguments(lib):
     assert compose(lib, fam=5) == EINVAL
+    assert compose(lib, fam=3, M=0) == EINVAL       # KDA composes like dense: needs M
     assert compose(lib, dk=48) == EUNSUP
     assert compose(lib, lam=0) == EINVAL
     assert compose(lib, Sc=0) == EINVAL
@@ -147,6 +151,7 @@ def chain(lib, fam=0, R=2, L=2, H=2, dk=64, dv=64, mc=3, cl=A, idx=A, P_=5, pl=A
 
 def test_chain_rejects_bad_arguments(lib):
     assert chain(lib, fam=4) == EINVAL
+    assert chain(lib, fam=3, pM=0) == EINVAL
     assert chain(lib, dv=16) == EUNSUP
     assert chain(lib, cl=0) == EINVAL
     assert chain(lib, idx=0) == EINVAL
@@ -165,7 +170,8 @@ def seam(lib, fam=0, dtype=0, n=2, w=8, H=2, dk=64, dv=64, q=0, k=A, v=A, alpha=
 
 
 def test_seam_rejects_bad_arguments(lib):
-    assert seam(lib, fam=3) == EINVAL
+    assert seam(lib, fam=4) == EINVAL
+    assert seam(lib, fam=3) == EINVAL               # KDA needs M
     assert seam(lib, dtype=2) == EINVAL
     assert seam(lib, w=-1) == EINVAL
     assert seam(lib, w=5000) == EUNSUP
