@@ -358,6 +358,51 @@ def run_dense(args, L):
                          "peak_kind": f"bf16 burst, {src}"}}
 
 
+# fp32 CUDA-core peak from unit counts: 152 SMs x 128 fp32 lanes x 2 flop (FMA) x 2.07 GHz
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def run_kda(args, L):
+    """KDA-style gates (a gate per channel inside the erasing update), 30 layers x
+    32 heads x 128, one segment of L tokens per layer: the token-by-token fp32 scan."""
+    import torch
+    import linear_attention_state_gated_gb300 as hy
+    from linear_attention_state_gated_gb300 import workloads as wl
+    Lyr, H, d = 30, 32, 128
+    w = wl.kda_stack(seg_len=L, n_layers=Lyr, H=H, d=d)
+    dev = torch.device("cuda")
+    k = torch.from_numpy(w["k"]).to(torch.bfloat16).to(dev)
+    v = torch.from_numpy(w["v"]).to(torch.bfloat16).to(dev)
+    a = torch.from_numpy(w["alpha"]).to(dev)
+    b = torch.from_numpy(w["beta"]).to(dev)
+    offs = torch.from_numpy(w["seg_offsets"]).to(dev)
+    out = {"lam": torch.empty((Lyr, 1, H), dtype=torch.float32, device=dev),
+           "S": torch.empty((Lyr, 1, H, d, d), dtype=torch.float32, device=dev),
+           "M": torch.empty((Lyr, 1, H, d, d), dtype=torch.float32, device=dev)}
+    del w
+    for _ in range(2):
+        hy.segment_scan(hy.KDA, k, v, a, offs, beta=b, out=out)
+    torch.cuda.synchronize()
+    reps = 3
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(reps):
+        hy.segment_scan(hy.KDA, k, v, a, offs, beta=b, out=out)
+    e.record()
+    torch.cuda.synchronize()
+    t = s.elapsed_time(e) / reps / 1e3
+    tok_heads = Lyr * L * H
+    # per token-head: k^T S and k^T M (2 d^2 each), the state's erase, gate and write
+    # (5 d^2) and the operator's erase and gate (3 d^2)
+    flops = tok_heads * 12 * d * d
+    return {"workload": f"KDA-style gates, {Lyr} layers x {H} heads x {d}, one segment of {L} tokens per layer",
+            "value": L / t, "unit": "tokens/s (all 30 layers)", "head_tokens_per_s": tok_heads / t,
+            "ms": t * 1e3, "kernel": "token-by-token fp32 scan (CUDA cores)",
+            "roofline": {"bound": "alu", "achieved": flops / t / 1e12, "peak": FP32_ALU_TFLOPS,
+                         "unit": "TFLOP/s", "frac": flops / t / 1e12 / FP32_ALU_TFLOPS, "traffic": None,
+                         "peak_kind": "fp32 CUDA-core peak from unit counts and the maximum SM clock"}}
+
+
 def run_compose(args):
     """One composition step S = T S_prev + S_C (hypic_compose) over 64 requests x
     30 layers = 1920 items x 32 heads x 128 x 128, per family; synthetic fp32
@@ -656,8 +701,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="hypic", choices=["hypic", "reference"])
     ap.add_argument("--L", type=int, default=8192)
-    ap.add_argument("--rows", default="dense,compose,seam,chain,mix",
-                    help="extra rows: dense,compose,seam,chain,mix or none")
+    ap.add_argument("--rows", default="dense,kda,compose,seam,chain,mix",
+                    help="extra rows: dense,kda,compose,seam,chain,mix or none")
     ap.add_argument("--dense-L", type=int, default=2048)
     ap.add_argument("--dense-form", choices=["two_pass", "single"], default="two_pass",
                     help="dense row: two passes over a workspace, or the single-pass kernel")
@@ -683,6 +728,8 @@ def main():
     rows = {}
     if rank == 0 and "dense" in args.rows:
         rows["dense_scan"] = run_dense(args, args.dense_L)
+    if rank == 0 and "kda" in args.rows:
+        rows["kda_scan"] = run_kda(args, args.dense_L)
     if rank == 0 and "compose" in args.rows:
         rows["compose"] = run_compose(args)
     if rank == 0 and "seam" in args.rows:
