@@ -72,6 +72,8 @@ def open_library(path: str):
     lib.oracle_compose_chain.argtypes = [i32, i32, i32, i32, i32, i32, i32, P, P, i32,
                                          P, P, P, P, P, i32]
     lib.oracle_compose_chain.restype = i32
+    lib.oracle_compose_prefix.argtypes = [i32, i32, i32, i32, i32, i32, i32, P, P, i32, P, P, P, P, P, P]
+    lib.oracle_compose_prefix.restype = i32
     lib.oracle_seam_compose.argtypes = [i32, i32, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P, P]
     lib.oracle_seam_compose.restype = i32
     lib.oracle_max_threads.restype = i32
@@ -219,6 +221,32 @@ def compose_chain(fam, chain_len, seg_idx, pool_lam, pool_S, pool_M=None, S_init
     if rc != 0:
         raise ValueError(f"oracle_compose_chain: bad arguments ({rc})")
     return S
+
+
+def compose_prefix(fam, chain_len, seg_idx, pool_lam, pool_S, pool_M=None):
+    """The cached pair of each request's ordered pool entries (a composed prefix):
+    T = T_{p_n} ... T_{p_1} as lam (and M) and S = S(C_{p_1} ... C_{p_n} | 0).
+    Returns dict lam [R,Lyr,H(,dk)], M [R,Lyr,H,dk,dk] (dense, kda), S [R,Lyr,H,dk,dv]."""
+    fam = _fam(fam)
+    chain_len = np.ascontiguousarray(np.asarray(chain_len, dtype=np.int32))
+    seg_idx = np.ascontiguousarray(np.asarray(seg_idx, dtype=np.int32))
+    pool_lam, pool_S, pool_M = _f64(pool_lam), _f64(pool_S), _f64(pool_M)
+    P, Lyr, H, dk, dv = pool_S.shape
+    R = chain_len.shape[0]
+    max_chain = seg_idx.shape[1] if seg_idx.ndim == 2 else 0
+    S = np.zeros((R, Lyr, H, dk, dv), np.float64)
+    lam = np.zeros((R, Lyr, H, dk) if fam == DIAG else (R, Lyr, H), np.float64)
+    M = np.zeros((R, Lyr, H, dk, dk), np.float64) if fam in WITH_M else None
+    rc = _load().oracle_compose_prefix(fam, R, Lyr, H, dk, dv, max_chain, _ptr(chain_len), _ptr(seg_idx), P,
+                                       _ptr(pool_lam), _ptr(pool_M), _ptr(pool_S), _ptr(lam), _ptr(M), _ptr(S))
+    if rc == -2:
+        raise IndexError("oracle_compose_prefix: pool index out of range")
+    if rc != 0:
+        raise ValueError(f"oracle_compose_prefix: bad arguments ({rc})")
+    out = {"lam": lam, "S": S}
+    if M is not None:
+        out["M"] = M
+    return out
 
 
 def seam_compose(fam, k, v, alpha, lam, S_C, S_prev=None, M=None, beta=None, q=None,

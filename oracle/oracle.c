@@ -349,6 +349,59 @@ int oracle_compose_chain(int fam, int R, int Lyr, int H, int dk, int dv, int max
 }
 
 /*
+ * Composed prefix ([xix-fr]: T(C1.C2) = T(C2) T(C1) makes compositions
+ * chainable, so a popular ordered group of cached segments can itself be
+ * cached as one pair).  For each request r, layer l and head h, the pair of
+ * the concatenation of pool entries seg_idx[r, 0 .. chain_len[r]-1]:
+ *   T = T_{p_n} ... T_{p_1}   (lambda summed; dense / kda: M product, max-abs normalised)
+ *   S = S(C_{p_1} ... C_{p_n} | 0)   (the chain from a zero state)
+ * Layouts as oracle_compose_chain; lam_out [R, Lyr, H] or [R, Lyr, H, dk] (diag),
+ * M_out [R, Lyr, H, dk, dk] (dense, kda), S_out [R, Lyr, H, dk, dv].
+ */
+int oracle_compose_prefix(int fam, int R, int Lyr, int H, int dk, int dv, int max_chain,
+                          const int32_t *chain_len, const int32_t *seg_idx, int P,
+                          const double *pool_lam, const double *pool_M,
+                          const double *pool_S, double *lam_out, double *M_out,
+                          double *S_out)
+{
+    if (!lam_out || (HAS_M(fam) && !M_out)) return -1;
+    const int rc = oracle_compose_chain(fam, R, Lyr, H, dk, dv, max_chain, chain_len, seg_idx, P,
+                                        pool_lam, pool_M, pool_S, NULL, S_out, 0);
+    if (rc != 0) return rc;
+    const int nl = fam == OR_DIAG ? dk : 1;
+    double *P2 = malloc(sizeof(double) * (size_t)dk * dk);
+    for (int64_t u = 0; u < (int64_t)R * Lyr * H; ++u) {
+        const int64_t r = u / ((int64_t)Lyr * H);
+        const int64_t lh = u % ((int64_t)Lyr * H);
+        double *lam = lam_out + u * nl;
+        for (int i = 0; i < nl; ++i) lam[i] = 0.0;
+        double *Mo = HAS_M(fam) ? M_out + u * dk * dk : NULL;
+        if (Mo) {
+            memset(Mo, 0, sizeof(double) * (size_t)dk * dk);
+            for (int i = 0; i < dk; ++i) Mo[(size_t)i * dk + i] = 1.0;
+        }
+        for (int j = 0; j < chain_len[r]; ++j) {
+            const int64_t e = (int64_t)seg_idx[r * max_chain + j] * Lyr * H + lh;
+            for (int i = 0; i < nl; ++i) lam[i] += pool_lam[e * nl + i];
+            if (Mo) {   /* M <- M_p M */
+                const double *Mp = pool_M + e * dk * dk;
+                for (int i = 0; i < dk; ++i)
+                    for (int c = 0; c < dk; ++c) {
+                        double acc = 0.0;
+                        for (int x = 0; x < dk; ++x) acc += Mp[(size_t)i * dk + x] * Mo[(size_t)x * dk + c];
+                        P2[(size_t)i * dk + c] = acc;
+                    }
+                memcpy(Mo, P2, sizeof(double) * (size_t)dk * dk);
+                keep_in_range(Mo, dk * dk, &lam[0]);
+            }
+        }
+        if (Mo) normalise_maxabs(Mo, dk * dk, &lam[0]);
+    }
+    free(P2);
+    return 0;
+}
+
+/*
  * Seam-window advance with composition ([xix-fr], paragraph on full-attention
  * layers, "fenetres de jonction"): the first w tokens of every reused segment
  * are left out of its cache and recomputed at reuse under the full prefix; the

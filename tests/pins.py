@@ -548,6 +548,48 @@ def check_kda_without_erasure_is_per_channel_decay():
         assert rel(T[0, h], np.diag(np.prod(alpha[0, :, h], axis=0))) < TOL
 
 
+def _operator(fam, out, dk):
+    """T = exp(lambda) M (dense, kda), diag(exp(lambda)) or exp(lambda) I, per (.., head)."""
+    if fam in WITH_M:
+        return np.exp(out["lam"])[..., None, None] * out["M"]
+    if fam == DIAG:
+        return np.exp(out["lam"])[..., :, None] * np.eye(dk)
+    return np.exp(out["lam"])[..., None, None] * np.eye(dk)
+
+
+def check_composed_prefix_equals_concatenation():
+    """[xix-fr] T(C1.C2) = T(C2) T(C1): an ordered group of cached pairs composes
+    into the pair of the concatenated tokens (operator and zero-start state), and
+    that pair, cached, stands in for its members in later chains."""
+    for fam in FAMS:
+        lens = [5, 8, 3, 6]
+        offs = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+        Lyr, H, dk, dv = 2, 2, 4, 3
+        k, v, alpha, beta, _ = _inputs(fam, Lyr, int(offs[-1]), H, dk, dv, seed=200 + fam)
+        pool = oracle.segment_scan(fam, k, v, alpha, offs, beta)
+        pl, pS = np.moveaxis(pool["lam"], 1, 0), np.moveaxis(pool["S"], 1, 0)
+        pM = np.moveaxis(pool["M"], 1, 0) if fam in WITH_M else None
+        groups = np.array([[2, 0, 3], [1, 1, 0], [3, 0, 0]], dtype=np.int32)
+        glen = np.array([3, 2, 0], dtype=np.int32)
+        got = oracle.compose_prefix(fam, glen, groups, pl, pS, pool_M=pM)
+        for r in range(3):
+            idx = [i for s in groups[r, :glen[r]] for i in range(offs[s], offs[s + 1])]
+            ref = oracle.sequential(fam, k[:, idx], v[:, idx], alpha[:, idx],
+                                    None if beta is None else beta[:, idx])
+            assert rel(got["S"][r], ref["S"]) < TOL, (fam, r)
+            Tg = _operator(fam, {key: a[r] for key, a in got.items()}, dk)
+            Tw = _operator(fam, ref, dk)
+            assert rel(Tg, Tw) < TOL, (fam, r, "T")
+        # the cached prefix of group 0 as a pool entry: [prefix, 1] == [2, 0, 3, 1]
+        P = pS.shape[0]
+        ext = lambda a, b: np.concatenate([a, b[None]], axis=0)   # noqa: E731
+        pl2, pS2 = ext(pl, got["lam"][0]), ext(pS, got["S"][0])
+        pM2 = ext(pM, got["M"][0]) if fam in WITH_M else None
+        S_a = oracle.compose_chain(fam, [2], [[P, 1]], pl2, pS2, pool_M=pM2)
+        S_b = oracle.compose_chain(fam, [4], [[2, 0, 3, 1]], pl, pS, pool_M=pM)
+        assert rel(S_a, S_b) < TOL, (fam, "reuse")
+
+
 ALL_CHECKS = [
     check_transition_is_ordered_product,
     check_state_and_output_unrolled,
@@ -568,4 +610,5 @@ ALL_CHECKS = [
     check_seam_window_pure_decay_closed_form,
     check_kda_with_one_gate_is_dense,
     check_kda_without_erasure_is_per_channel_decay,
+    check_composed_prefix_equals_concatenation,
 ]

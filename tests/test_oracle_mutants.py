@@ -48,6 +48,10 @@ MUTANTS = [
      "M[(size_t)i * dk + j] = (M[(size_t)i * dk + j] - b * kt[i] * kS[j]);", 0),
     ("seam_kda_one_gate", "const double a = fam == OR_KDA ? alpha[row * dk + r] : alpha[row];",
      "const double a = fam == OR_KDA ? alpha[row * dk] : alpha[row];", 0),
+    ("prefix_operator_order", "acc += Mp[(size_t)i * dk + x] * Mo[(size_t)x * dk + c];",
+     "acc += Mo[(size_t)i * dk + x] * Mp[(size_t)x * dk + c];", 0),
+    ("prefix_drops_lambda", "for (int i = 0; i < nl; ++i) lam[i] += pool_lam[e * nl + i];",
+     "for (int i = 0; i < nl; ++i) lam[i] += 0.0 * pool_lam[e * nl + i];", 0),
     ("seam_token_order", "const int64_t row = (i * w + t) * H + h;", "const int64_t row = (i * w + (w - 1 - t)) * H + h;", 0),
 ]
 
