@@ -220,6 +220,29 @@ int hypic_compose_chain(int fam, int n_req, int n_layers, int n_heads, int d_k, 
                         int *d_err, void *cuda_stream);
 
 /*
+ * hypic_compose_prefix -- a composed prefix: for every request r, layer l and
+ * head h, the cached pair of the concatenation of the pool entries
+ * seg_idx[r, 0 .. chain_len[r]-1] (in that order):
+ *   T = T_{p_n} ... T_{p_1},   S = S(C_{p_1} ... C_{p_n} | 0).
+ * (xix.ai/fr, linear-layer paragraph: T(C1.C2) = T(C2) T(C1) makes the
+ * composition chainable in any grouping, so a popular ordered group of cached
+ * segments can itself be cached as one pair and used as a pool entry.)
+ *   Arguments as hypic_compose_chain without S_init, plus
+ *   lam_out  fp32  [n_req, n_layers, H] or [n_req, n_layers, H, d_k] (diag)
+ *   M_out    fp32  [n_req, n_layers, H, d_k, d_k] (dense, kda; NULL otherwise),
+ *            max|M_out| in [1, 2) (exact power-of-two scaling into lam_out)
+ *   S_out    fp32  [n_req, n_layers, H, d_k, d_v]
+ * The outputs must not overlap one another or the pool.  An empty group gives
+ * lambda = 0, M = I, S = 0.  Dense and KDA run the operator chain M_pn ... M_p1 on
+ * the same kernels as the state's chain (then a pass that folds the power of two).
+ */
+int hypic_compose_prefix(int fam, int n_req, int n_layers, int n_heads, int d_k, int d_v,
+                         int max_chain, const int32_t *chain_len, const int32_t *seg_idx,
+                         int pool_size, const float *pool_lam, const float *pool_M,
+                         const float *pool_S, float *lam_out, float *M_out, float *S_out,
+                         int *d_err, void *cuda_stream);
+
+/*
  * hypic_seam_compose -- reuse of a cached segment whose first w tokens (the
  * seam window) were left out of its cache.  (xix.ai/fr, paragraph on
  * full-attention layers: at reuse the seam tokens are recomputed under the full

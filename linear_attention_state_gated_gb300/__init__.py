@@ -33,7 +33,8 @@ BF16, F32 = 0, 1
 STATUS = {0: "HYPIC_OK", -1: "HYPIC_EINVAL", -2: "HYPIC_EUNSUPPORTED", -3: "HYPIC_EALIGN",
           -4: "HYPIC_ECUDA", -5: "HYPIC_EINDEX", -6: "HYPIC_ETIMEOUT"}
 
-__all__ = ["segment_scan", "segment_scan_workspace_bytes", "segment_scan_static", "compose", "compose_chain", "status_string", "library", "use_library",
+__all__ = ["segment_scan", "segment_scan_workspace_bytes", "segment_scan_static", "compose", "compose_chain",
+           "compose_prefix", "seam_compose", "status_string", "library", "use_library",
            "HypicError", "SCALAR", "DIAG", "DENSE", "KDA"]
 
 
@@ -59,6 +60,8 @@ SIGNATURES = {
     "hypic_compose": (_I32, [_I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "hypic_compose_chain": (_I32, [_I32, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _I32,
                                    _P, _P, _P, _P, _P, _P, _P]),
+    "hypic_compose_prefix": (_I32, [_I32, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _I32,
+                                    _P, _P, _P, _P, _P, _P, _P, _P]),
     "hypic_seam_compose": (_I32, [_I32, _I32, _I32, _I32, _I32, _I32, _I32,
                                   _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "hypic_status_string": (ctypes.c_char_p, [_I32]),
@@ -264,6 +267,36 @@ def compose(family, lam, S_C, S_prev=None, M=None, lam_prev=None, M_prev=None, S
         if fam in WITH_M:
             res["M"] = M_out
     return res
+
+
+def compose_prefix(family, chain_len, seg_idx, pool_lam, pool_S, pool_M=None, out=None, d_err=None,
+                   stream=None):
+    """The cached pair of each request's ordered pool entries (hypic_compose_prefix):
+    T = T_pn ... T_p1 as lam (and M) and S = S(C_p1 ... C_pn | 0).  ``out`` may hold
+    preallocated ``lam``, ``M``, ``S``.  Returns a dict with lam, S and M (dense, kda)."""
+    fam = _fam(family)
+    chain_len = _dev(chain_len, "chain_len", torch.int32)
+    seg_idx = _dev(seg_idx, "seg_idx", torch.int32)
+    pool_lam = _dev(pool_lam, "pool_lam", torch.float32)
+    pool_S = _dev(pool_S, "pool_S", torch.float32)
+    pool_M = _dev(pool_M, "pool_M", torch.float32, allow_none=True)
+    P, Lyr, H, dk, dv = pool_S.shape
+    R = chain_len.numel()
+    max_chain = seg_idx.shape[1] if seg_idx.dim() == 2 else 0
+    out = dict(out or {})
+    f = dict(dtype=torch.float32, device=pool_S.device)
+    if "lam" not in out:
+        out["lam"] = torch.empty((R, Lyr, H, dk) if fam == DIAG else (R, Lyr, H), **f)
+    if "S" not in out:
+        out["S"] = torch.empty((R, Lyr, H, dk, dv), **f)
+    if fam in WITH_M and "M" not in out:
+        out["M"] = torch.empty((R, Lyr, H, dk, dk), **f)
+    st = library().hypic_compose_prefix(fam, R, Lyr, H, dk, dv, max_chain, _ptr(chain_len), _ptr(seg_idx), P,
+                                        _ptr(pool_lam), _ptr(pool_M), _ptr(pool_S), _ptr(out["lam"]),
+                                        _ptr(out.get("M") if fam in WITH_M else None), _ptr(out["S"]),
+                                        _ptr(d_err), _stream(stream))
+    _check("hypic_compose_prefix", st)
+    return out
 
 
 def seam_compose(family, k, v, alpha, lam, S_C, S_prev=None, M=None, beta=None, q=None,

@@ -379,4 +379,67 @@ int hypic_compose_chain(int fam, int n_req, int n_layers, int n_heads, int d_k, 
     return from_cuda(hypic::launch_compose_chain(a, static_cast<cudaStream_t>(cuda_stream)));
 }
 
+int hypic_compose_prefix(int fam, int n_req, int n_layers, int n_heads, int d_k, int d_v, int max_chain,
+                         const int32_t *chain_len, const int32_t *seg_idx, int pool_size, const float *pool_lam,
+                         const float *pool_M, const float *pool_S, float *lam_out, float *M_out, float *S_out,
+                         int *d_err, void *cuda_stream) {
+    if (!family_ok(fam)) return HYPIC_EINVAL;
+    if (n_req < 0 || n_layers < 0 || n_heads <= 0 || max_chain < 0 || pool_size < 0) return HYPIC_EINVAL;
+    if (!head_size_ok(d_k) || !head_size_ok(d_v)) return HYPIC_EUNSUPPORTED;
+    if ((int64_t)n_req * n_layers * n_heads > INT32_MAX) return HYPIC_EUNSUPPORTED;
+    if (n_req == 0 || n_layers == 0) return HYPIC_OK;
+    if (!chain_len || !S_out || !lam_out) return HYPIC_EINVAL;
+    if (has_m(fam) != (M_out != nullptr)) return HYPIC_EINVAL;
+    if (max_chain > 0 && (!seg_idx || pool_size == 0 || !pool_lam || !pool_S)) return HYPIC_EINVAL;
+    if (max_chain > 0 && has_m(fam) != (pool_M != nullptr)) return HYPIC_EINVAL;
+    const void *a16[] = {pool_M, pool_S, M_out, S_out, fam == HYPIC_DIAG ? pool_lam : nullptr,
+                         fam == HYPIC_DIAG ? lam_out : nullptr};
+    for (const void *p : a16)
+        if (p && !aligned(p, 16)) return HYPIC_EALIGN;
+    const void *a4[] = {chain_len, seg_idx, pool_lam, lam_out, d_err};
+    for (const void *p : a4)
+        if (p && !aligned(p, 4)) return HYPIC_EALIGN;
+    // the outputs overlap neither one another nor the pool
+    const int64_t units = (int64_t)n_req * n_layers * n_heads;
+    const int64_t entries = (int64_t)pool_size * n_layers * n_heads;
+    const int nl = fam == HYPIC_DIAG ? d_k : 1;
+    auto overlaps = [](const void *x, size_t xb, const void *y, size_t yb) {
+        if (!x || !y) return false;
+        const char *a = static_cast<const char *>(x), *b = static_cast<const char *>(y);
+        return a < b + yb && b < a + xb;
+    };
+    const size_t sb = (size_t)units * d_k * d_v * 4, mb = (size_t)units * d_k * d_k * 4, lb = (size_t)units * nl * 4;
+    const size_t psb = (size_t)entries * d_k * d_v * 4, pmb = (size_t)entries * d_k * d_k * 4,
+                 plb = (size_t)entries * nl * 4;
+    const void *outs[] = {S_out, M_out, lam_out};
+    const size_t outb[] = {sb, mb, lb};
+    const void *ins[] = {pool_S, pool_M, pool_lam};
+    const size_t inb[] = {psb, pmb, plb};
+    for (int x = 0; x < 3; ++x) {
+        for (int y = 0; y < 3; ++y)
+            if (overlaps(outs[x], outb[x], ins[y], inb[y])) return HYPIC_EINVAL;
+        for (int y = x + 1; y < 3; ++y)
+            if (overlaps(outs[x], outb[x], outs[y], outb[y])) return HYPIC_EINVAL;
+    }
+
+    hypic::ChainArgs a;
+    a.fam = compose_family(fam);
+    a.R = n_req;
+    a.n_layers = n_layers;
+    a.H = n_heads;
+    a.dk = d_k;
+    a.dv = d_v;
+    a.max_chain = max_chain;
+    a.P = pool_size;
+    a.chain_len = chain_len;
+    a.seg_idx = seg_idx;
+    a.pool_lam = pool_lam;
+    a.pool_M = pool_M;
+    a.pool_S = pool_S;
+    a.S_init = nullptr;
+    a.S_out = S_out;
+    a.d_err = d_err;
+    return from_cuda(hypic::launch_compose_prefix(a, lam_out, M_out, static_cast<cudaStream_t>(cuda_stream)));
+}
+
 }  // extern "C"

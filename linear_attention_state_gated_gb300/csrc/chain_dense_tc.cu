@@ -40,18 +40,19 @@ constexpr int kBpart = 32768;           // one bf16 B tile: 128 k-rows x 128 n, 
 constexpr int kMstage = 3 * kBpart;     // M_p stage, fp32, 4 boxes of 32 columns x 128 rows
 constexpr int kSstage = kMstage + 65536; // S_p stage, same layout
 constexpr int kCtl = kSstage + 65536;
-constexpr int kSmem = kCtl + 128 + 1024;
+constexpr int kSmem = kCtl + 256 + 1024;
 static_assert(kSmem <= 232448, "fits in one SM's shared memory");
 
 struct ChainCtrl {
     uint64_t mfull, mfree, sfull, sfree;
     uint64_t ops_ready[2], d_done[2];   // per column half: B half in shared memory / its products done
     uint64_t aready[2], afree[2];       // per A operand buffer: split into TMEM / read by both halves
+    float rmax[2][16];                  // operator mode: the math warps' maxima, by renormalisation parity
     uint32_t tmem;
     int abort;
 };
 
-static_assert(sizeof(ChainCtrl) <= 128, "the control block fits its reserved bytes");
+static_assert(sizeof(ChainCtrl) <= 256, "the control block fits its reserved bytes");
 
 // Two fp32 values -> three packed bf16 pairs with x = hi + mid + lo (to ~2^-27 relative).
 __device__ __forceinline__ void split3_pair(float x0, float x1, uint32_t &hi, uint32_t &mid, uint32_t &lo) {
@@ -89,6 +90,9 @@ __device__ __forceinline__ int64_t step_entry(const ChainArgs &a, int64_t u, int
     return (int64_t)p * lhn + lh;
 }
 
+// OP: operator mode (ChainArgs::op), a compile-time switch so that the state's
+// chain carries none of it
+template <bool OP>
 __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: <= 96 registers per thread
     chain_dense_tc_kernel(const __grid_constant__ CUtensorMap tm_m, const __grid_constant__ CUtensorMap tm_s,
                           const __grid_constant__ CUtensorMap tm_i, const __grid_constant__ CUtensorMap tm_o,
@@ -152,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: <= 96 registers pe
                 first = false;
             }
             if (*abortp && f > 0) mbar_wait(&ctl->mfull, (f - 1) & 1u);   // the last copy lands
-        } else if (lane == 1) {
+        } else if (lane == 1 && !OP) {   // (operator mode reads no S_p)
             int64_t g = 0;   // steps of this CTA so far
             for (int64_t u = blockIdx.x; u < units && !*abortp; u += gridDim.x) {
                 const int n = unit_steps(a, u, false);
@@ -258,19 +262,28 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: <= 96 registers pe
             ++f;
             return true;
         };
-        // a unit without steps: S_out = S_init (or 0)
+        // a unit without steps: S_out = S_init (or 0; operator mode: I)
         auto copy_init = [&](int64_t u) {
             const float4 *init =
                 a.S_init ? reinterpret_cast<const float4 *>(a.S_init + u * DD + i * kD + cq * 32) : nullptr;
             float4 *out = reinterpret_cast<float4 *>(a.S_out + u * DD + i * kD + cq * 32);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) out[q] = init ? init[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int q = 0; q < 8; ++q) {
+                if (OP) {
+                    const int c0 = cq * 32 + 4 * q;
+                    out[q] = make_float4(i == c0 ? 1.f : 0.f, i == c0 + 1 ? 1.f : 0.f, i == c0 + 2 ? 1.f : 0.f,
+                                         i == c0 + 3 ? 1.f : 0.f);
+                } else {
+                    out[q] = init ? init[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+            if (OP && threadIdx.x == 64) a.lam_out[u] = 0.f;
         };
 
         auto load_init = [&]() -> bool {   // S_init row of the next unit (the stage's next fill, or 0) into srow
-            if (!a.S_init) {
+            if (!a.S_init) {   // zero, or the identity in operator mode
 #pragma unroll
-                for (int q = 0; q < 32; ++q) srow[q] = 0.f;
+                for (int q = 0; q < 32; ++q) srow[q] = (OP && i == cq * 32 + q) ? 1.f : 0.f;
                 return true;
             }
             if (!bar_and(hbar, kMath / 2, mbar_wait(&ctl->mfull, f & 1u) && !*abortp)) return false;
@@ -297,6 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: <= 96 registers pe
 
         int64_t g = 0;
         bool ok = true;
+        int op_exp = 0;     // operator mode: power of two taken out of the unit's product so far
+        uint32_t nrn = 0;   // operator mode: renormalisations so far (parity of the maxima buffer)
         int64_t u = next_unit((int64_t)blockIdx.x - gridDim.x);
         if (u < units) ok = load_init() && split_m(0);   // the first unit's state, its first step's operand
         while (ok && u < units) {
@@ -327,9 +342,9 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: <= 96 registers pe
                     ok = false;
                     break;
                 }
-                const float scale = expf(a.pool_lam[e]);
+                const float scale = OP ? 1.f : expf(a.pool_lam[e]);
                 if (!bar_and(hbar, kMath / 2,
-                             mbar_wait(&ctl->sfull, (uint32_t)g & 1u) &&
+                             (OP || mbar_wait(&ctl->sfull, (uint32_t)g & 1u)) &&
                                  mbar_wait(&ctl->d_done[hh], (uint32_t)g & 1u) && !*abortp)) {
                     ok = false;
                     break;
@@ -346,7 +361,8 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: <= 96 registers pe
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
                         const int q = hb * 4 + q4;
-                        const float4 v = *reinterpret_cast<const float4 *>(sp + ((q ^ (i & 7)) << 4));
+                        const float4 v = OP ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                              : *reinterpret_cast<const float4 *>(sp + ((q ^ (i & 7)) << 4));
                         const float4 r = make_float4(fmaf(scale, __uint_as_float(dv[4 * q4]), v.x),
                                                      fmaf(scale, __uint_as_float(dv[4 * q4 + 1]), v.y),
                                                      fmaf(scale, __uint_as_float(dv[4 * q4 + 2]), v.z),
@@ -359,6 +375,30 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: <= 96 registers pe
                     }
                 }
                 tc_fence_before();
+                if (OP && !last && (c & 3) == 3) {
+                    // operator mode: bring max|M| back to [1, 2) by a power of two every 4 steps
+                    // (all sixteen warps agree on it: the scaling must be one for the matrix)
+                    float mx = 0.f;
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) mx = fmaxf(mx, fabsf(srow[q]));
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                    float *rm = ctl->rmax[nrn & 1];
+                    if (lane == 0) rm[warp - 2] = mx;
+                    bar_sync(1, kMath);
+                    mx = 0.f;
+#pragma unroll
+                    for (int x = 0; x < 16; ++x) mx = fmaxf(mx, rm[x]);
+                    ++nrn;
+                    if (mx > 0.f && (mx < 1.f || mx >= 2.f)) {
+                        int ex;
+                        frexpf(mx, &ex);
+                        const float sc = ldexpf(1.f, 1 - ex);
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) srow[q] *= sc;
+                        op_exp += ex - 1;
+                    }
+                }
                 if (last) {
                     fence_async_smem();    // the results, visible to the TMA store
                     bar_sync(hbar, kMath / 2);
@@ -372,6 +412,10 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: <= 96 registers pe
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ctl->sfree);   // the stage may take the next step's S_p
+                if (OP && last) {   // the unit's exponent, then a fresh one for the next
+                    if (threadIdx.x == 64) a.lam_out[u] = (float)op_exp;
+                    op_exp = 0;
+                }
                 // after a unit's last step: the next unit's S_init (its fill has been in flight
                 // since the next unit's first M_p was split)
                 if (last && un < units && !load_init()) {
@@ -419,14 +463,15 @@ cudaError_t launch_chain_dense_tc(const ChainArgs &a, cudaStream_t s) {
     if (a.S_init && !make_tensor_map_3d(&ti, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.S_init, 128, 1, urows, 32, 128,
                                         CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(chain_dense_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    auto kern = a.op ? chain_dense_tc_kernel<true> : chain_dense_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
     e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     const int64_t grid = units < sms ? units : sms;   // persistent: one CTA per SM
-    chain_dense_tc_kernel<<<(unsigned)grid, kThreads, kSmem, s>>>(tm, ts, ti, to, a, units);
+    kern<<<(unsigned)grid, kThreads, kSmem, s>>>(tm, ts, ti, to, a, units);
     return cudaGetLastError();
 }
 

@@ -260,7 +260,9 @@ __global__ void __launch_bounds__(256) chain_sd_kernel(const ChainArgs a) {
 }
 
 // Dense chain: one CTA per (request, layer, head), S kept in shared memory,
-// each step S <- exp(lam_p) M_p S + S_p as a register-tiled fp32 GEMM.
+// each step S <- exp(lam_p) M_p S + S_p as a register-tiled fp32 GEMM.  Operator
+// mode (a.op, DV = D): S <- M_p S from I, brought back to max in [1, 2) by a power
+// of two every 4 steps; the exponent goes to lam_out.
 template <int D, int DV>
 __global__ void __launch_bounds__(256) chain_dense_kernel(const ChainArgs a) {
     using Gm = HeadGemm<D, DV>;
@@ -271,26 +273,52 @@ __global__ void __launch_bounds__(256) chain_dense_kernel(const ChainArgs a) {
     const int r = (int)(u / ((int64_t)a.n_layers * a.H));
     const int64_t lh = u % ((int64_t)a.n_layers * a.H);
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-    for (int i = tid; i < D * DV; i += 256) Ss[i] = a.S_init ? a.S_init[u * D * DV + i] : 0.f;
+    for (int i = tid; i < D * DV; i += 256)
+        Ss[i] = a.op ? (i / DV == i % DV ? 1.f : 0.f) : (a.S_init ? a.S_init[u * D * DV + i] : 0.f);
+    __shared__ float wmax[8];
+    int op_exp = 0;
     const int n = clamp_len(a, r);
     for (int c = 0; c < n; ++c) {
         const int p = clamp_idx(a, r, c);
         const int64_t e = (int64_t)p * a.n_layers * a.H + lh;
         float acc[Gm::TM][Gm::TN] = {};
         Gm::template run<true>(a.pool_M + e * D * D, Ss, As, acc);
-        const float sc = expf(a.pool_lam[e]);
+        const float sc = a.op ? 1.f : expf(a.pool_lam[e]);
         const float *Sp = a.pool_S + e * D * DV;
         __syncthreads();   // all reads of the old state are done
+        float mx = 0.f;
 #pragma unroll
         for (int i = 0; i < Gm::TM; ++i)
 #pragma unroll
             for (int j = 0; j < Gm::TN; ++j) {
                 const int idx = (ty * Gm::TM + i) * DV + tx + 16 * j;
-                Ss[idx] = fmaf(sc, acc[i][j], __ldcs(Sp + idx));
+                Ss[idx] = a.op ? acc[i][j] : fmaf(sc, acc[i][j], __ldcs(Sp + idx));
+                mx = fmaxf(mx, fabsf(acc[i][j]));
             }
+        if (a.op && (c & 3) == 3 && c + 1 < n) {   // one power of two for the whole matrix
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            if ((tid & 31) == 0) wmax[tid >> 5] = mx;
+            __syncthreads();
+            mx = 0.f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) mx = fmaxf(mx, wmax[w]);
+            if (mx > 0.f && (mx < 1.f || mx >= 2.f)) {
+                int ex;
+                frexpf(mx, &ex);
+                const float scl = ldexpf(1.f, 1 - ex);
+#pragma unroll
+                for (int i = 0; i < Gm::TM; ++i)
+#pragma unroll
+                    for (int j = 0; j < Gm::TN; ++j) Ss[(ty * Gm::TM + i) * DV + tx + 16 * j] *= scl;
+                op_exp += ex - 1;
+            }
+            __syncthreads();   // the scaled state is in, wmax is read
+        }
     }
     __syncthreads();
     for (int i = tid; i < D * DV; i += 256) a.S_out[u * D * DV + i] = Ss[i];
+    if (a.op && tid == 0) a.lam_out[u] = (float)op_exp;
 }
 
 template <int D, int DV>
@@ -374,6 +402,79 @@ cudaError_t launch_compose(const ComposeArgs &a, cudaStream_t s) {
         compose_sd_kernel<true><<<(unsigned)units, 256, 0, s>>>(a);
     else
         compose_sd_kernel<false><<<(unsigned)units, 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+// Composed prefix, last pass: lambda of the group = sum of its entries' lambdas
+// (double); for dense / kda also the exponent the operator chain took out and the
+// final power of two that brings max|M| into [1, 2).  One CTA per (request, layer, head).
+template <bool kM, bool kDiag>
+__global__ void __launch_bounds__(256) prefix_finish_kernel(const ChainArgs a, float *lam_out, float *M_out) {
+    const int64_t u = blockIdx.x;
+    const int r = (int)(u / ((int64_t)a.n_layers * a.H));
+    const int64_t lh = u % ((int64_t)a.n_layers * a.H);
+    const int tid = threadIdx.x;
+    const int nl = kDiag ? a.dk : 1;
+    const int n = clamp_len(a, r);
+    __shared__ double lsum[128];
+    __shared__ float wmax[8];
+    for (int x = tid; x < nl; x += 256) {
+        double sum = 0.0;
+        for (int c = 0; c < n; ++c) {
+            const int64_t e = (int64_t)clamp_idx(a, r, c) * a.n_layers * a.H + lh;
+            sum += (double)a.pool_lam[e * nl + x];
+        }
+        if (kM) lsum[x] = sum;
+        else lam_out[u * nl + x] = (float)sum;
+    }
+    if (!kM) return;
+    const int64_t DD = (int64_t)a.dk * a.dk;
+    float *M = M_out + u * DD;
+    const float E = lam_out[u];   // the operator chain's exponent
+    float mx = 0.f;
+    for (int64_t i = tid; i < DD; i += 256) mx = fmaxf(mx, fabsf(M[i]));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if ((tid & 31) == 0) wmax[tid >> 5] = mx;
+    __syncthreads();
+    mx = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) mx = fmaxf(mx, wmax[w]);
+    int f = 0;
+    if (mx > 0.f) {
+        int ex;
+        frexpf(mx, &ex);
+        f = ex - 1;
+    }
+    const float scl = ldexpf(1.f, -f);
+    for (int64_t i = tid; i < DD; i += 256) M[i] *= scl;
+    if (tid == 0) lam_out[u] = (float)(lsum[0] + ((double)E + (double)f) * (double)kLn2);
+}
+
+cudaError_t launch_compose_prefix(const ChainArgs &a0, float *lam_out, float *M_out, cudaStream_t s) {
+    const int64_t units = (int64_t)a0.R * a0.n_layers * a0.H;
+    if (units == 0) return cudaSuccess;
+    ChainArgs c = a0;   // the state of the group from a zero start
+    c.S_init = nullptr;
+    c.op = 0;
+    cudaError_t e = launch_compose_chain(c, s);
+    if (e != cudaSuccess) return e;
+    if (a0.fam == HYPIC_DENSE) {   // the operator chain M_pn ... M_p1
+        ChainArgs o = a0;
+        o.op = 1;
+        o.S_init = nullptr;
+        o.dv = o.dk;
+        o.pool_S = a0.pool_M;   // never read in operator mode; shaped like the operator
+        o.S_out = M_out;
+        o.lam_out = lam_out;
+        e = chain_dense_tc_supported(o) ? launch_chain_dense_tc(o, s) : dispatch_dd<DenseChainF>(o, s, o.dk, o.dk);
+        if (e != cudaSuccess) return e;
+        prefix_finish_kernel<true, false><<<(unsigned)units, 256, 0, s>>>(a0, lam_out, M_out);
+    } else if (a0.fam == HYPIC_DIAG) {
+        prefix_finish_kernel<false, true><<<(unsigned)units, 256, 0, s>>>(a0, lam_out, nullptr);
+    } else {
+        prefix_finish_kernel<false, false><<<(unsigned)units, 256, 0, s>>>(a0, lam_out, nullptr);
+    }
     return cudaGetLastError();
 }
 

@@ -39,6 +39,10 @@ struct ChainArgs {
     const float *pool_lam, *pool_M, *pool_S, *S_init;
     float *S_out;
     int *d_err;
+    // operator mode (dense, kda): S_out <- M_pn ... M_p1 from I (no S_p, no exp(lambda)),
+    // rescaled by powers of two on the way; the exponent per unit goes to lam_out
+    int op = 0;
+    float *lam_out = nullptr;
 };
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (nullptr if unavailable).
@@ -78,6 +82,9 @@ cudaError_t launch_chain_dense_tc(const ChainArgs &a, cudaStream_t s);
 
 cudaError_t launch_compose(const ComposeArgs &a, cudaStream_t s);
 cudaError_t launch_compose_chain(const ChainArgs &a, cudaStream_t s);
+// The cached pair of each request's ordered pool entries: S from a zero state into
+// a.S_out, T = T_pn ... T_p1 into lam_out (and M_out for dense, kda).
+cudaError_t launch_compose_prefix(const ChainArgs &a, float *lam_out, float *M_out, cudaStream_t s);
 
 // Seam-window advance, then the composition of the rest of the segment.
 struct SeamArgs {

@@ -162,6 +162,26 @@ def test_chain_rejects_bad_arguments(lib):
     assert chain(lib, R=0) == OK
 
 
+def prefix(lib, fam=0, R=2, L=2, H=2, dk=64, dv=64, mc=3, cl=A, idx=A, P_=5, pl=A, pM=0, pS=A + 0x100000,
+           lo=A + 0x300000, Mo=0, So=A + 0x400000, err=0):
+    return lib.hypic_compose_prefix(fam, R, L, H, dk, dv, mc, P(cl or None), P(idx or None), P_,
+                                    P(pl or None), P(pM or None), P(pS or None), P(lo or None), P(Mo or None),
+                                    P(So or None), P(err or None), P(None))
+
+
+def test_prefix_rejects_bad_arguments(lib):
+    assert prefix(lib, fam=4) == EINVAL
+    assert prefix(lib, dk=48) == EUNSUP
+    assert prefix(lib, lo=0) == EINVAL                 # the operator's lambda is an output
+    assert prefix(lib, fam=2, pM=A + 0x200000) == EINVAL   # dense needs M_out
+    assert prefix(lib, fam=0, Mo=A + 0x500000) == EINVAL   # scalar must not get one
+    assert prefix(lib, fam=3, pM=0, Mo=A + 0x500000) == EINVAL   # KDA needs pool_M
+    assert prefix(lib, So=A + 0x100000 + 64) == EINVAL  # S_out overlaps the pool
+    assert prefix(lib, lo=A + 0x400000 + 4) == EINVAL   # lambda overlaps S_out
+    assert prefix(lib, pS=A + 0x100004) == EALIGN
+    assert prefix(lib, R=0) == OK
+
+
 def seam(lib, fam=0, dtype=0, n=2, w=8, H=2, dk=64, dv=64, q=0, k=A, v=A, alpha=A, beta=0,
          lam=A + 0x200000, M=0, Sp=0, Sc=A + 0x400000, So=A + 0x600000, o=0):
     return lib.hypic_seam_compose(fam, dtype, n, w, H, dk, dv, P(q or None), P(k or None), P(v or None),
