@@ -497,6 +497,51 @@ def run_seam(args):
     return res
 
 
+def run_prefix(args):
+    """Composed prefix (hypic_compose_prefix): the cached pair of a whole 64-segment
+    prompt, 64 pool entries in order, 30 layers x 32 heads x 128 x 128, per family;
+    synthetic pool drawn on the device (values do not change the work)."""
+    import torch
+    import linear_attention_state_gated_gb300 as hy
+    res = {}
+    hbm, _, _, src = peaks()
+    P, Lyr, H, d = 64, 30, 32, 128
+    dev = torch.device("cuda")
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    clen = torch.tensor([P], dtype=torch.int32, device=dev)
+    idx = torch.arange(P, dtype=torch.int32, device=dev)[None]
+    pool_S = torch.randn((P, Lyr, H, d, d), generator=g, device=dev)
+    for fam, name in ((0, "scalar"), (1, "diag"), (2, "dense")):
+        lam = -torch.rand((P, Lyr, H, d) if fam == 1 else (P, Lyr, H), generator=g, device=dev) * 5
+        M = torch.randn((P, Lyr, H, d, d), generator=g, device=dev) * 0.1 if fam == 2 else None
+        out = {}
+        call = lambda: hy.compose_prefix(fam, clen, idx, lam, pool_S, pool_M=M, out=out)   # noqa: E731
+        out = call()
+        for _ in range(2):
+            call()
+        torch.cuda.synchronize()
+        reps = 3
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(reps):
+            call()
+        e.record()
+        torch.cuda.synchronize()
+        t = s.elapsed_time(e) / reps / 1e3
+        # each entry's S_p (and M_p) once, lambda, and the outputs (S, M) once per (layer, head)
+        per_entry = 4 * d * d + (4 * d * d if fam == 2 else 0) + (4 * d if fam == 1 else 4)
+        by = Lyr * H * (P * per_entry + 4 * d * d + (4 * d * d if fam == 2 else 0))
+        res[name] = {"value": P * Lyr / t, "unit": "composes/s folded into the prefix (all 32 heads)",
+                     "ms": t * 1e3, "entries": P, "layers": Lyr,
+                     "roofline": {"bound": "hbm", "achieved": by / t / 1e9, "peak": hbm, "unit": "GB/s",
+                                  "frac": by / t / 1e9 / hbm, "traffic": None, "peak_kind": f"copy, {src}"}}
+        del lam, M, out
+    del pool_S
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_chain(args):
     import torch
     import linear_attention_state_gated_gb300 as hy
@@ -701,8 +746,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="hypic", choices=["hypic", "reference"])
     ap.add_argument("--L", type=int, default=8192)
-    ap.add_argument("--rows", default="dense,kda,compose,seam,chain,mix",
-                    help="extra rows: dense,kda,compose,seam,chain,mix or none")
+    ap.add_argument("--rows", default="dense,kda,compose,seam,prefix,chain,mix",
+                    help="extra rows: dense,kda,compose,seam,prefix,chain,mix or none")
     ap.add_argument("--dense-L", type=int, default=2048)
     ap.add_argument("--dense-form", choices=["two_pass", "single"], default="two_pass",
                     help="dense row: two passes over a workspace, or the single-pass kernel")
@@ -734,6 +779,8 @@ def main():
         rows["compose"] = run_compose(args)
     if rank == 0 and "seam" in args.rows:
         rows["seam"] = run_seam(args)
+    if rank == 0 and "prefix" in args.rows:
+        rows["prefix"] = run_prefix(args)
     if rank == 0 and "chain" in args.rows:
         rows["rag_chain"] = run_chain(args)
     if rank == 0 and "mix" in args.rows:
