@@ -350,12 +350,48 @@ def run_dense(args, L):
     tok_heads = Lyr * L * H
     flops = tok_heads * 180e3       # algorithmic flops per token-head of the chunked form, C = 64
     _, bf16, bf16_sus, src = peaks()
+    del k, v, a, b, offs, out, ws
+    vl = run_dense_varlen(args) if args.dense_form == "two_pass" else None
     return {"workload": f"gated delta rule, {Lyr} layers x {H} heads x {d}, one segment of {L} tokens per layer",
             "value": L / t, "unit": "tokens/s (all 30 layers)", "head_tokens_per_s": tok_heads / t,
-            "ms": t * 1e3, "form": args.dense_form,
+            "ms": t * 1e3, "form": args.dense_form, "varlen": vl,
             "roofline": {"bound": "tensor", "achieved": flops / t / 1e12, "peak": bf16,
                          "unit": "TFLOP/s", "frac": flops / t / 1e12 / bf16, "traffic": None,
                          "peak_kind": f"bf16 burst, {src}"}}
+
+
+def run_dense_varlen(args):
+    """A varlen batch: 16 segments, lengths U{1024..4096} (seeded), gated delta rule,
+    2 layers x 32 heads x 128 (1024 chains: the ragged tail is visible), one call
+    (the two-pass form)."""
+    import torch
+    import linear_attention_state_gated_gb300 as hy
+    from linear_attention_state_gated_gb300 import workloads as wl
+    Lyr, H, d = 2, 32, 128
+    lens = [int(x) for x in np.random.default_rng(12).integers(1024, 4097, size=16)]
+    w = wl.dense_stack(lengths=lens, n_layers=Lyr, H=H, d=d, seed=12)
+    dev = torch.device("cuda")
+    k = torch.from_numpy(w["k"]).to(torch.bfloat16).to(dev)
+    v = torch.from_numpy(w["v"]).to(torch.bfloat16).to(dev)
+    a = torch.from_numpy(w["alpha"]).to(dev)
+    b = torch.from_numpy(w["beta"]).to(dev)
+    offs = torch.from_numpy(w["seg_offsets"]).to(dev)
+    N = int(w["seg_offsets"][-1])
+    del w
+    ws = torch.empty(hy.segment_scan_workspace_bytes(2, torch.bfloat16, Lyr, len(lens), N, H, d, d),
+                     dtype=torch.uint8, device=dev)
+    out = hy.segment_scan(2, k, v, a, offs, beta=b, workspace=ws)
+    hy.segment_scan(2, k, v, a, offs, beta=b, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    reps = 3
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(reps):
+        hy.segment_scan(2, k, v, a, offs, beta=b, out=out, workspace=ws)
+    e.record()
+    torch.cuda.synchronize()
+    t = s.elapsed_time(e) / reps / 1e3
+    return {"segments": len(lens), "layers": Lyr, "tokens": N, "ms": t * 1e3, "tokens_per_s": N / t}
 
 
 # fp32 CUDA-core peak from unit counts: 152 SMs x 128 fp32 lanes x 2 flop (FMA) x 2.07 GHz

@@ -112,7 +112,9 @@ int hypic_segment_scan(int fam, int in_dtype, int n_layers, int n_seg,
  * Today the scratch is used with bf16 inputs and d_k = d_v = 128 by
  *   the dense family: one record per (layer, head, 64-token chunk slot) of
  *     33568 bytes (50192 bytes with o_t), n_layers * n_heads * (n_seg +
- *     total_tokens / 64) records;
+ *     total_tokens / 64) records, then n_seg int32 (the segments ranked by
+ *     length: the longest chains are started first), each part rounded up to
+ *     256 bytes;
  *   the diagonal family without o_t and with n_seg <= 512: 2 x 512 partial
  *     states of 66048 bytes (67.6 MB), for a schedule that spreads all
  *     segments' chunks evenly over the GPU and then folds the pieces of

@@ -23,6 +23,7 @@ struct ScanArgs {
     void *o_out;
     float *ws;        // caller-owned scratch of the two-pass dense scan (or NULL)
     int *d_err;
+    const int *order = nullptr;   // two-pass dense: segments longest first (or NULL: as given)
 };
 
 struct ComposeArgs {

@@ -413,10 +413,13 @@ __global__ void __maxnreg__(80)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     const int half = blockIdx.x & 1;   // 0: transition M, 1: state S
+    // chains in the order of their segments, longest first (all layers and heads of
+    // a segment together), so that the last wave holds the shortest chains
     const int unit = blockIdx.x >> 1;
+    const int rank = unit / (a.H * a.n_layers);
+    const int l = (unit / a.H) % a.n_layers;
     const int h = unit % a.H;
-    const int seg = (unit / a.H) % a.n_seg;
-    const int l = unit / (a.H * a.n_seg);
+    const int seg = a.order ? a.order[rank] : rank;
     int64_t t0 = a.seg_offsets[seg], t1 = a.seg_offsets[seg + 1];
     const bool bad = !(t0 >= 0 && t0 <= t1 && t1 <= a.N);
     if (bad) t0 = t1 = 0;
@@ -902,8 +905,49 @@ __global__ void __maxnreg__(80)
     }
 }
 
+// ================================================================ longest first
+
+constexpr int kLptMax = 4096;   // segments ranked; beyond this the given order is kept
+
+// order[rank] = segment, by length descending (ties: lower index first); a segment
+// with bad offsets counts as empty.  One CTA.
+__global__ void __launch_bounds__(1024) lpt_order_kernel(const int64_t *seg_offsets, int n_seg, int64_t N,
+                                                         int *order) {
+    __shared__ int64_t len[kLptMax];
+    const bool rank = n_seg <= kLptMax;
+    for (int i = threadIdx.x; i < n_seg && rank; i += blockDim.x) {
+        const int64_t t0 = seg_offsets[i], t1 = seg_offsets[i + 1];
+        len[i] = (t0 >= 0 && t0 <= t1 && t1 <= N) ? t1 - t0 : 0;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < n_seg; i += blockDim.x) {
+        if (!rank) {
+            order[i] = i;
+            continue;
+        }
+        const int64_t li = len[i];
+        int r = 0;
+        for (int j = 0; j < n_seg; ++j) r += (len[j] > li) || (len[j] == li && j < i);
+        order[r] = i;
+    }
+}
+
+// bytes of the records (then the order array, 256-byte aligned)
+int64_t records_bytes(const ScanArgs &a) {
+    const int64_t b = (int64_t)a.n_layers * a.H * n_slots(a.N, a.n_seg) * (a.o_out ? Rec<true>::Bytes : Rec<false>::Bytes);
+    return (b + 255) / 256 * 256;
+}
+
 template <bool O>
-cudaError_t launch_two_pass(const ScanArgs &a, cudaStream_t s) {
+cudaError_t launch_two_pass(const ScanArgs &a0, cudaStream_t s) {
+    ScanArgs a = a0;
+    if (a.n_seg > 1) {   // rank the segments (one segment: nothing to order)
+        int *order = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(a0.ws) + records_bytes(a0));
+        lpt_order_kernel<<<1, 1024, 0, s>>>(a.seg_offsets, a.n_seg, a.N, order);
+        cudaError_t e0 = cudaGetLastError();
+        if (e0 != cudaSuccess) return e0;
+        a.order = order;
+    }
     const int64_t units = (int64_t)a.n_layers * a.n_seg * a.H;
     const uint64_t rows = (uint64_t)a.n_layers * (uint64_t)a.N;
     CUtensorMap mk, mv, mq;
@@ -943,7 +987,7 @@ bool scan_dense_ws_supported(const ScanArgs &a) {
 }
 
 int64_t scan_dense_ws_bytes(const ScanArgs &a) {
-    return (int64_t)a.n_layers * a.H * n_slots(a.N, a.n_seg) * (a.o_out ? Rec<true>::Bytes : Rec<false>::Bytes);
+    return records_bytes(a) + ((int64_t)a.n_seg * 4 + 255) / 256 * 256;
 }
 
 cudaError_t launch_scan_dense_ws(const ScanArgs &a, cudaStream_t s) {
