@@ -55,13 +55,18 @@ struct ChainCtrl {
 static_assert(sizeof(ChainCtrl) <= 256, "the control block fits its reserved bytes");
 
 // Two fp32 values -> three packed bf16 pairs with x = hi + mid + lo (to ~2^-27 relative).
+// (the residuals are exact, so the packed subtractions change no bit)
 __device__ __forceinline__ void split3_pair(float x0, float x1, uint32_t &hi, uint32_t &mid, uint32_t &lo) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-    const float r0 = x0 - __low2float(h), r1 = x1 - __high2float(h);
-    const __nv_bfloat162 m = __floats2bfloat162_rn(r0, r1);
-    const __nv_bfloat162 l = __floats2bfloat162_rn(r0 - __low2float(m), r1 - __high2float(m));
     hi = *reinterpret_cast<const uint32_t *>(&h);
+    const uint64_t r = sub2(pk2(x0, x1), bf16x2_to_f32x2(hi));
+    float r0, r1;
+    upk2(r, r0, r1);
+    const __nv_bfloat162 m = __floats2bfloat162_rn(r0, r1);
     mid = *reinterpret_cast<const uint32_t *>(&m);
+    float q0, q1;
+    upk2(sub2(r, bf16x2_to_f32x2(mid)), q0, q1);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(q0, q1);
     lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
@@ -363,10 +368,14 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: <= 96 registers pe
                         const int q = hb * 4 + q4;
                         const float4 v = OP ? make_float4(0.f, 0.f, 0.f, 0.f)
                                               : *reinterpret_cast<const float4 *>(sp + ((q ^ (i & 7)) << 4));
-                        const float4 r = make_float4(fmaf(scale, __uint_as_float(dv[4 * q4]), v.x),
-                                                     fmaf(scale, __uint_as_float(dv[4 * q4 + 1]), v.y),
-                                                     fmaf(scale, __uint_as_float(dv[4 * q4 + 2]), v.z),
-                                                     fmaf(scale, __uint_as_float(dv[4 * q4 + 3]), v.w));
+                        const uint64_t sc2 = pk2(scale, scale);
+                        float4 r;
+                        upk2(fma2(sc2, pk2(__uint_as_float(dv[4 * q4]), __uint_as_float(dv[4 * q4 + 1])),
+                                  pk2(v.x, v.y)),
+                             r.x, r.y);
+                        upk2(fma2(sc2, pk2(__uint_as_float(dv[4 * q4 + 2]), __uint_as_float(dv[4 * q4 + 3])),
+                                  pk2(v.z, v.w)),
+                             r.z, r.w);
                         if (last) {   // in place: the stage then leaves by TMA store
                             *reinterpret_cast<float4 *>(sp + ((q ^ (i & 7)) << 4)) = r;
                         } else {

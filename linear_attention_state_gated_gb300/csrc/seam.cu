@@ -23,9 +23,12 @@
 // channel inside the erasing update) this kernel writes the advanced state and
 // the product with T_body = exp(lambda) M runs as a composition afterwards.
 #include "internal.cuh"
+#include "sm100.cuh"
 
 namespace hypic {
 namespace {
+
+using namespace sm100;
 
 constexpr int kTB = 8;   // seam tokens staged per block
 
@@ -45,26 +48,6 @@ __device__ __forceinline__ void cp_async_wait_all() {
 }
 
 constexpr int kCW = 32;   // columns of S per CTA
-
-// packed pairs of fp32 (one f32x2 instruction does two lanes' worth of work)
-__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ void upk2(uint64_t v, float &lo, float &hi) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {   // a * b + c
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
 
 template <int FAM, int DK, int DV, typename T>
 __global__ void __launch_bounds__(kCW *(DK / 32)) seam_kernel(const SeamArgs a) {
