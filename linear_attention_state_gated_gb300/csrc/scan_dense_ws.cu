@@ -27,7 +27,8 @@
 //   O1^T = X0^T Q^T (X0 hi + lo),  O2^T = Delta^T Gq^T (three products)
 // W and U are built by their own warps ahead of the state warps; one more warp
 // issues the state pass's products, starting on each half of X0 as soon as it
-// is converted.
+// is converted, and a second issuing warp takes the second k half of Delta (or,
+// with o_t, the output products O1 and O2).
 #include "dense_common.cuh"
 #include "internal.cuh"
 #include "sm100.cuh"
@@ -319,11 +320,11 @@ __global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_cons
 // ================================================================ pass 2: state
 
 constexpr int kNS = 2;            // stages
-// 22 or 23 warps: 0 TMA, 1-4 W/U operands, 5-20 state, 21 MMA issue, and without
-// o_t 22: a second MMA-issue warp for the second k half of Delta (a single thread
-// issues N = 64 products at about one per 60 cycles; two threads nearly double that)
+// 23 warps: 0 TMA, 1-4 W/U operands, 5-20 state, 21 MMA issue, 22 a second MMA-issue
+// warp (a single thread issues N = 64 products at about one per 60 cycles): without
+// o_t it takes the second k half of Delta, with o_t the output products O1 and O2
 template <bool O>
-constexpr int state_threads() { return O ? 704 : 736; }
+constexpr int state_threads() { return 736; }
 constexpr int kWT = 128;          // W warps' threads
 constexpr int kState = 512;       // state warps' threads
 
@@ -337,7 +338,8 @@ struct Smem {
     static constexpr int NB = O ? 1 : 2;               // operand buffers
     static constexpr int Gqb = kNS * Stage;            // with o_t: Gq hi / lo (64 x 128 B each)
     static constexpr int Wt = Gqb + (O ? 16384 : 0);   // -W^T, per buffer hi / lo (128 rows x 128 B each)
-    static constexpr int Ctl = Wt + NB * 32768;
+    static constexpr int Ost = Wt + NB * 32768;        // with o_t: o staging, 8 tokens x 32 channels per state warp
+    static constexpr int Ctl = Ost + (O ? 16 * 512 : 0);
 };
 
 // TMEM column map (512 allocated)
@@ -356,6 +358,8 @@ struct StateCtl {
     uint64_t gfull;                                  // o_t: Gq of the next chunk is in
     uint64_t xop_ready[2], dt_ready;                 // state warps -> MMA issuer
     uint64_t w_done, d_done, x_done;
+    uint64_t o1_done, o2_done;                       // o_t: the output products of a chunk
+    uint64_t o_free;                                 // o_t: the state warps have read O1, O2
     uint64_t drain[3];
     float redmax[16];
     float bo[kC];          // b_t of the chunk whose o_t is pending
@@ -380,26 +384,55 @@ __device__ __forceinline__ float state_max(float mx, StateCtl *ctl, int sw, int 
     return mx;
 }
 
-// o_t = b_t O1 + O2 for this thread's 16 tokens (column group cg) of one chunk,
-// whose first token is row `crow` of [n_layers * N]; bf16 out
-__device__ __forceinline__ void store_o(const ScanArgs &a, int h, uint32_t to1, uint32_t to2, const float *b,
-                                        int cg, int m, int64_t crow, int nvalid) {
+// o_t = b_t O1 + O2 for this thread's 16 tokens (column group cg) of one chunk, as
+// bf16 pairs (tokens 2q, 2q + 1 in opk[q]); then the warp arrives on `freed` (if
+// given): O1 and O2 have been read
+__device__ __forceinline__ void load_o(uint32_t to1, uint32_t to2, const float *b, int cg, int lane,
+                                       uint32_t (&opk)[8], uint64_t *freed) {
     uint32_t r1[16], r2[16];
     tmem_ld16(to1, r1);
     tmem_ld16(to2, r2);
     tmem_wait_ld();
-    __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.o_out);
+    if (freed != nullptr) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(freed);
+    }
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const int t = cg * 16 + i;
-        if (t < nvalid) {
-            const float val = fmaf(b[t], __uint_as_float(r1[i]), __uint_as_float(r2[i]));
-            o[((crow + t) * a.H + h) * kD + m] = __float2bfloat16_rn(val);
-        }
+    for (int q = 0; q < 8; ++q) {
+        const int t = cg * 16 + 2 * q;
+        const __nv_bfloat162 v = __floats2bfloat162_rn(fmaf(b[t], __uint_as_float(r1[2 * q]), __uint_as_float(r2[2 * q])),
+                                                       fmaf(b[t + 1], __uint_as_float(r1[2 * q + 1]),
+                                                            __uint_as_float(r2[2 * q + 1])));
+        opk[q] = *reinterpret_cast<const uint32_t *>(&v);
     }
 }
 
-// 22 or 23 warps: six on some sub-partitions, 16384 / (6 x 32) registers -> at most 80 per thread
+// write those 16 tokens of channel quarter * 32 + lane, whose first token is row
+// `crow` of [n_layers * N]: through the warp's staging tile, 8 tokens at a time,
+// so that each lane stores one 16-byte run of 8 channels of one token
+__device__ __forceinline__ void store_o(const ScanArgs &a, int h, int cg, int quarter, int lane, int64_t crow,
+                                        int nvalid, const uint32_t (&opk)[8], __nv_bfloat16 *stg) {
+    __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.o_out) + (int64_t)h * kD + quarter * 32 + (lane & 3) * 8;
+    const int64_t rs = (int64_t)a.H * kD;   // elements from one token to the next
+    uint16_t *st16 = reinterpret_cast<uint16_t *>(stg);
+#pragma unroll
+    for (int ps = 0; ps < 2; ++ps) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t w = opk[ps * 4 + (i >> 1)];
+            st16[i * 32 + lane] = (uint16_t)((i & 1) ? (w >> 16) : (w & 0xFFFFu));
+        }
+        __syncwarp();
+        const int i = lane >> 2;
+        const int t = cg * 16 + ps * 8 + i;
+        const uint4 val = *reinterpret_cast<const uint4 *>(stg + i * 32 + (lane & 3) * 8);
+        if (t < nvalid) *reinterpret_cast<uint4 *>(o + (crow + t) * rs) = val;
+        __syncwarp();
+    }
+}
+
+// 23 warps: six on some sub-partitions, 16384 / (6 x 32) registers -> at most 80 per thread
 template <bool O>
 __global__ void __maxnreg__(80)
     dense_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -427,23 +460,27 @@ __global__ void __maxnreg__(80)
     const int64_t row0 = (int64_t)l * a.N + t0;
     const float *recs = a.ws + (((int64_t)l * a.H + h) * slots + seg + t0 / kC) * R::Floats;
     const bool with_o = O && half == 1;   // o_t comes from the state half
+    const bool split_d = !with_o;         // the second issuer takes the second k half of Delta
 
     if (threadIdx.x == 0) {
         if (bad) flag_index_error(a.d_err);
         for (int s = 0; s < kNS; ++s) {
             mbar_init(&ctl->full[s], 1);
-            mbar_init(&ctl->empty[s], 1);
+            mbar_init(&ctl->empty[s], with_o ? 2 : 1);   // with o_t both issuers read the stage
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&ctl->wop_ready[b], kWT / 32);
-            mbar_init(&ctl->wfree[b], O ? 1 : 2);   // every issuer of Delta products commits
+            mbar_init(&ctl->wfree[b], split_d ? 2 : 1);   // every issuer of Delta products commits
         }
         mbar_init(&ctl->xop_ready[0], kState / 32);
         mbar_init(&ctl->xop_ready[1], kState / 32);
         mbar_init(&ctl->dt_ready, kState / 32);
         mbar_init(&ctl->w_done, 1);
-        mbar_init(&ctl->d_done, O ? 1 : 2);
+        mbar_init(&ctl->d_done, split_d ? 2 : 1);
         mbar_init(&ctl->x_done, 1);
+        mbar_init(&ctl->o1_done, 1);
+        mbar_init(&ctl->o2_done, 1);
+        mbar_init(&ctl->o_free, kState / 32);
         for (int d = 0; d < 3; ++d) mbar_init(&ctl->drain[d], 1);
         mbar_init(&ctl->gfull, 1);
         ctl->abort = 0;
@@ -499,10 +536,10 @@ __global__ void __maxnreg__(80)
                     mbar_wait(&ctl->full[j % kNS], (uint32_t)(j / kNS) & 1u);
         } else if (lane == 1 && with_o) {
             // Gq of chunk j into its buffer once chunk j - 1's O2 products have read it
-            // (x_done of j - 1 cannot pass before this copy: O2 of j waits for it)
+            // (o2_done of j cannot pass before this copy: O2 of j waits for it)
             int issued = 0;
             for (int j = 0; j < nc; ++j) {
-                if (j > 0 && !wait_or_abort(&ctl->x_done, (uint32_t)(j - 1) & 1u, abortp)) break;
+                if (j > 0 && !wait_or_abort(&ctl->o2_done, (uint32_t)(j - 1) & 1u, abortp)) break;
                 mbar_expect_tx(&ctl->gfull, 16384u);
                 bulk_load(smem + SM::Gqb, recs + (int64_t)j * R::Floats + R::Gq, 16384u, &ctl->gfull);
                 issued = j + 1;
@@ -592,6 +629,7 @@ __global__ void __maxnreg__(80)
         const uint32_t tacc = tmem + lane_off + kTacc + (uint32_t)(cg * 16);
         const uint32_t to1 = tmem + lane_off + kTo1 + (uint32_t)(cg * 16);
         const uint32_t to2 = tmem + lane_off + kTo2 + (uint32_t)(cg * 16);
+        __nv_bfloat16 *ostg = reinterpret_cast<__nv_bfloat16 *>(smem + SM::Ost) + sw * 256;   // o_t staging
         // Transition half: M_true = exp(lam_d + lam_exp ln2) M_stored, and each chunk
         // stores T_chunk M / b_C (log b_C into lam_d).  State half: S_true =
         // exp(ls) S_stored.  Either way the update only accumulates into TMEM; X is
@@ -649,13 +687,17 @@ __global__ void __maxnreg__(80)
                 }
             }
             if (j > 0) ok = ok && wait_or_abort(&ctl->x_done, (uint32_t)(j - 1) & 1u, abortp);
+            if (with_o && j > 0) ok = ok && wait_or_abort(&ctl->o2_done, (uint32_t)(j - 1) & 1u, abortp);
             if (!bar_and(2, kState, ok)) {
                 *abortp = 1;
                 break;
             }
             tc_fence_after();
-            // ---- o_t of the previous chunk (its O1, O2 are complete: x_done)
-            if (with_o && j > 0) store_o(a, h, to1, to2, ctl->bo, cg, m, row0 + (int64_t)(j - 1) * kC, kC);
+            // ---- o_t of the previous chunk into registers (its O1, O2 are complete:
+            // o1_done was awaited in that chunk, o2_done at this one's start); the O1
+            // products of this chunk wait for o_free
+            uint32_t opk[8];
+            if (with_o && j > 0) load_o(to1, to2, ctl->bo, cg, lane, opk, &ctl->o_free);
             if (half == 0 && renorm) {   // the transition's power-of-two renormalisation
                 float mx = 0.f;
 #pragma unroll
@@ -696,9 +738,13 @@ __global__ void __maxnreg__(80)
                     if (lane == 0) mbar_arrive(&ctl->xop_ready[p]);
                 }
             }
+            // ---- and to memory while the Delta products run
+            if (with_o && j > 0) store_o(a, h, cg, quarter, lane, row0 + (int64_t)(j - 1) * kC, kC, opk, ostg);
             // ---- Delta~^T = fD Delta^T diag(b_C / b) -> bf16 hi / lo in place
-            // (with o_t also Delta^T itself, hi / lo, into the X0 operand columns)
-            if (!bar_and(2, kState, wait_or_abort(&ctl->d_done, (uint32_t)j & 1u, abortp))) {
+            // (with o_t also Delta^T itself, hi / lo, into the X0 operand columns, once
+            // the O1 products have read X0 there)
+            if (!bar_and(2, kState, wait_or_abort(&ctl->d_done, (uint32_t)j & 1u, abortp) &&
+                                        (!with_o || wait_or_abort(&ctl->o1_done, (uint32_t)j & 1u, abortp)))) {
                 *abortp = 1;
                 break;
             }
@@ -706,7 +752,7 @@ __global__ void __maxnreg__(80)
             {
                 uint32_t r[16], hi[8], lo[8];
                 tmem_ld16(tacc, r);
-                if (!O) {   // plus the second k half's accumulator
+                if (split_d) {   // plus the second k half's accumulator
                     uint32_t r2[16];
                     tmem_ld16(tacc + (kTacc2 - kTacc), r2);
                     tmem_wait_ld();
@@ -740,11 +786,15 @@ __global__ void __maxnreg__(80)
         // ------------------------------------------------------------ epilogue
         bool ok = true;
         if (nc > 0) ok = wait_or_abort(&ctl->x_done, (uint32_t)(nc - 1) & 1u, abortp);
+        if (with_o && nc > 0) ok = ok && wait_or_abort(&ctl->o2_done, (uint32_t)(nc - 1) & 1u, abortp);
         if (bar_and(2, kState, ok)) {
             tc_fence_after();
-            if (with_o && nc > 0)
-                store_o(a, h, to1, to2, ctl->bo, cg, m, row0 + (int64_t)(nc - 1) * kC,
-                        (int)(t1 - t0 - (int64_t)(nc - 1) * kC));
+            if (with_o && nc > 0) {
+                uint32_t opk[8];
+                load_o(to1, to2, ctl->bo, cg, lane, opk, nullptr);
+                store_o(a, h, cg, quarter, lane, row0 + (int64_t)(nc - 1) * kC,
+                        (int)(t1 - t0 - (int64_t)(nc - 1) * kC), opk, ostg);
+            }
             const int64_t u_out = ((int64_t)l * a.n_seg + seg) * a.H + h;
             uint32_t r[2][16];
             tmem_ld16(tx0, r[0]);
@@ -773,9 +823,9 @@ __global__ void __maxnreg__(80)
         } else {
             *abortp = 1;
         }
-    } else if (!O && warp == 22) {
-        // ------------------------------------------------------------ second MMA issuer (no o_t):
-        // the second k half of X0^T W^T into its own accumulator
+    } else if (warp == 22 && split_d) {
+        // ------------------------------------------------------------ second MMA issuer (no o_t
+        // in this CTA): the second k half of X0^T W^T into its own accumulator
         if (lane == 0) {
             for (int j = 0; j < nc; ++j) {
                 const int b = j % SM::NB;
@@ -805,6 +855,57 @@ __global__ void __maxnreg__(80)
                 mbar_wait(&ctl->drain[2], 0);
             }
         }
+    } else if (warp == 22) {
+        // ------------------------------------------------------------ output-product issuer (o_t):
+        // O1^T = X0^T Q^T per k half as soon as that half of X0 is converted, then
+        // O2^T = Delta^T Gq^T (three-term split) once Delta^T is in place
+        if (lane == 0 && with_o) {
+            for (int j = 0; j < nc; ++j) {
+                const int s = j % kNS;
+                const uint32_t par = (uint32_t)j & 1u;
+                const uint8_t *stg = smem + s * SM::Stage;
+                if (!wait_or_abort(&ctl->full[s], (uint32_t)(j / kNS) & 1u, abortp)) break;
+                const uint32_t qb = smem_addr(stg + SM::Q);
+                bool ok = true;
+                for (int p = 0; p < 2 && ok; ++p) {
+                    ok = wait_or_abort(&ctl->xop_ready[p], par, abortp);
+                    // O1 and O2 of the previous chunk have been read (store_o)
+                    if (p == 0 && j > 0) ok = ok && wait_or_abort(&ctl->o_free, (uint32_t)(j - 1) & 1u, abortp);
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kq = 0; kq < 4; ++kq) {
+                        const int ks = p * 4 + kq;
+                        const uint64_t bq =
+                            smem_desc_sw128(qb + (uint32_t)(ks >> 2) * kBox + (uint32_t)(ks & 3) * 32u, 0, 1024);
+                        const uint32_t ah = tmem + kTxop + (uint32_t)ks * 8u;
+                        mma_f16_ta(tmem + kTo1, ah, bq, id_o, ks > 0);
+                        mma_f16_ta(tmem + kTo1, ah + 64u, bq, id_o, 1u);
+                    }
+                }
+                if (!ok) break;
+                mma_commit(&ctl->o1_done);
+                mma_commit(&ctl->empty[s]);   // its last read of the stage (Q)
+                if (!wait_or_abort(&ctl->dt_ready, par, abortp)) break;
+                if (!wait_or_abort(&ctl->gfull, par, abortp)) break;
+                tc_fence_after();
+                const uint32_t gq = smem_addr(smem + SM::Gqb);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint64_t gh = smem_desc_sw128(gq + (uint32_t)ks * 32u, 0, 1024);
+                    const uint64_t gl = smem_desc_sw128(gq + 8192u + (uint32_t)ks * 32u, 0, 1024);
+                    const uint32_t ah = tmem + kTxop + (uint32_t)ks * 16u;
+                    mma_f16_ta(tmem + kTo2, ah, gh, id_o, ks > 0);
+                    mma_f16_ta(tmem + kTo2, ah, gl, id_o, 1u);
+                    mma_f16_ta(tmem + kTo2, ah + 8u, gh, id_o, 1u);
+                }
+                mma_commit(&ctl->o2_done);
+            }
+            if (*abortp) {   // drain: completes once this thread's MMAs are done
+                mma_commit(&ctl->drain[2]);
+                mbar_wait(&ctl->drain[2], 0);
+            }
+        }
     } else if (lane == 0) {
         // ------------------------------------------------------------ MMA issuer (warp 21)
         for (int j = 0; j < nc; ++j) {
@@ -827,11 +928,11 @@ __global__ void __maxnreg__(80)
                     mma_f16(tmem + kTacc, ad, smem_desc_sw128(ab + 8192u + (uint32_t)ks * 32u, 0, 1024), id_wu, 1u);
                 }
             }
-            // ---- Delta^T = U^T - X0^T W^T (three-term split), O1^T = X0^T Q^T, per k half
+            // ---- Delta^T = U^T - X0^T W^T (three-term split), per k half
             if (!wait_or_abort(&ctl->wop_ready[b], use & 1u, abortp)) break;
             const uint32_t wtile = smem_addr(smem + SM::Wt + b * 32768);
             bool ok = true;
-            for (int p = 0; p < (O ? 2 : 1) && ok; ++p) {   // without o_t the second half is warp 22's
+            for (int p = 0; p < (split_d ? 1 : 2) && ok; ++p) {   // split: the second half is warp 22's
                 ok = wait_or_abort(&ctl->xop_ready[p], par, abortp);
                 if (!ok) break;
                 tc_fence_after();
@@ -845,24 +946,11 @@ __global__ void __maxnreg__(80)
                     mma_f16_ta(tmem + kTacc, ah, bl, id_d, 1u);
                     mma_f16_ta(tmem + kTacc, al, bh, id_d, 1u);
                 }
-                if (with_o) {
-                    const uint32_t qb = smem_addr(stg + SM::Q);
-#pragma unroll
-                    for (int kq = 0; kq < 4; ++kq) {
-                        const int ks = p * 4 + kq;
-                        const uint64_t bq =
-                            smem_desc_sw128(qb + (uint32_t)(ks >> 2) * kBox + (uint32_t)(ks & 3) * 32u, 0, 1024);
-                        const uint32_t ah = tmem + kTxop + (uint32_t)ks * 8u;
-                        mma_f16_ta(tmem + kTo1, ah, bq, id_o, ks > 0);
-                        mma_f16_ta(tmem + kTo1, ah + 64u, bq, id_o, 1u);
-                    }
-                }
             }
             if (!ok) break;
             mma_commit(&ctl->d_done);
             mma_commit(&ctl->wfree[b]);
-            // ---- X^T += Delta~^T K (K as the MN-major B operand: row t, channels contiguous);
-            // O2^T = Delta^T Gq^T (three-term split)
+            // ---- X^T += Delta~^T K (K as the MN-major B operand: row t, channels contiguous)
             if (!wait_or_abort(&ctl->dt_ready, par, abortp)) break;
             tc_fence_after();
             const uint32_t kb = smem_addr(stg + SM::K);
@@ -873,22 +961,8 @@ __global__ void __maxnreg__(80)
                 mma_f16_ta(tmem + kTx, ah, bd, id_x, 1u);
                 mma_f16_ta(tmem + kTx, ah + 8u, bd, id_x, 1u);
             }
-            if (with_o) {
-                if (!wait_or_abort(&ctl->gfull, par, abortp)) break;
-                tc_fence_after();
-                const uint32_t gq = smem_addr(smem + SM::Gqb);
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    const uint64_t gh = smem_desc_sw128(gq + (uint32_t)ks * 32u, 0, 1024);
-                    const uint64_t gl = smem_desc_sw128(gq + 8192u + (uint32_t)ks * 32u, 0, 1024);
-                    const uint32_t ah = tmem + kTxop + (uint32_t)ks * 16u;
-                    mma_f16_ta(tmem + kTo2, ah, gh, id_o, ks > 0);
-                    mma_f16_ta(tmem + kTo2, ah, gl, id_o, 1u);
-                    mma_f16_ta(tmem + kTo2, ah + 8u, gh, id_o, 1u);
-                }
-            }
             mma_commit(&ctl->x_done);
-            mma_commit(&ctl->empty[s]);   // the stage is free once X (and O2) have read it
+            mma_commit(&ctl->empty[s]);   // its last read of the stage (K; with o_t the other issuer reads Q)
         }
         if (*abortp) {   // drain: completes once this thread's MMAs are done
             mma_commit(&ctl->drain[1]);
