@@ -282,6 +282,20 @@ const char *hypic_status_string(int status);
 /* Library version, major * 10000 + minor * 100 + patch. */
 int hypic_version(void);
 
+/* Diagnostic: the bounded pipeline wait that every kernel above uses, on its own.
+ * One thread waits on a fresh shared-memory mbarrier for at most limit_cycles SM
+ * cycles (0 <= limit_cycles <= 4e9, the kernels' own limit).  With arrive != 0 it
+ * arrives on the barrier first and the wait completes at once; with arrive == 0
+ * nothing arrives, the wait gives up after the limit and HYPIC_ETIMEOUT is written
+ * to *d_err -- the status a pipeline kernel leaves when one of its waits runs out.
+ *   d_err     device int32, nullable, 4-byte aligned
+ *   d_cycles  device int64, nullable, 8-byte aligned: the cycles the wait took
+ * Nothing faults or traps and the context stays usable.  Returns HYPIC_EINVAL for
+ * a limit out of range, HYPIC_EALIGN for a misaligned pointer, HYPIC_ECUDA when
+ * the launch fails; asynchronous on the stream like the other entry points. */
+int hypic_selftest_wait(long long limit_cycles, int arrive, int *d_err, long long *d_cycles,
+                        void *cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -34,7 +34,7 @@ STATUS = {0: "HYPIC_OK", -1: "HYPIC_EINVAL", -2: "HYPIC_EUNSUPPORTED", -3: "HYPI
           -4: "HYPIC_ECUDA", -5: "HYPIC_EINDEX", -6: "HYPIC_ETIMEOUT"}
 
 __all__ = ["segment_scan", "segment_scan_workspace_bytes", "segment_scan_static", "compose", "compose_chain",
-           "compose_prefix", "seam_compose", "status_string", "library", "use_library",
+           "compose_prefix", "seam_compose", "selftest_wait", "status_string", "library", "use_library",
            "HypicError", "SCALAR", "DIAG", "DENSE", "KDA"]
 
 
@@ -66,6 +66,7 @@ SIGNATURES = {
                                   _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "hypic_status_string": (ctypes.c_char_p, [_I32]),
     "hypic_version": (_I32, []),
+    "hypic_selftest_wait": (_I32, [ctypes.c_longlong, _I32, _P, _P, _P]),
 }
 
 
@@ -365,3 +366,15 @@ def compose_chain(family, chain_len, seg_idx, pool_lam, pool_S, pool_M=None, S_i
                                        _stream(stream))
     _check("hypic_compose_chain", st)
     return S_out
+
+
+def selftest_wait(limit_cycles, arrive, d_err=None, cycles=None, stream=None):
+    """Run the bounded pipeline wait on its own (hypic_selftest_wait): without
+    ``arrive`` the wait gives up after ``limit_cycles`` SM cycles and writes
+    HYPIC_ETIMEOUT to ``d_err`` (int32 CUDA tensor); ``cycles`` (int64 CUDA
+    tensor) receives the cycles the wait took."""
+    d_err = _dev(d_err, "d_err", torch.int32, allow_none=True)
+    cycles = _dev(cycles, "cycles", torch.int64, allow_none=True)
+    st = library().hypic_selftest_wait(int(limit_cycles), 1 if arrive else 0, _ptr(d_err), _ptr(cycles),
+                                       _stream(stream))
+    _check("hypic_selftest_wait", st)

@@ -220,3 +220,12 @@ def test_python_binding_refuses_host_tensors():
     k = torch.zeros(1, 4, 1, 32)
     with pytest.raises(ValueError):
         hy.segment_scan("scalar", k, k, torch.ones(1, 4, 1), torch.tensor([0, 4]))
+
+
+def test_selftest_wait_rejects_bad_arguments(lib):
+    """The bounded-wait diagnostic checks its limit and pointers before any launch."""
+    f = lib.hypic_selftest_wait
+    assert f(-1, 0, P(A), P(A), P(None)) == EINVAL
+    assert f(4_000_000_001, 0, P(A), P(A), P(None)) == EINVAL
+    assert f(1000, 0, P(A + 2), P(A), P(None)) == EALIGN
+    assert f(1000, 0, P(A), P(A + 4), P(None)) == EALIGN
