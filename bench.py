@@ -291,6 +291,15 @@ def run_headline(args, rank, world):
 
     e2e_step()
     torch.cuda.synchronize()
+    # the host link on this machine: one plain pinned -> device copy of the largest input
+    big_h, big_d = max(((host[f][k], devt[f][k]) for f in (0, 1) for k in host[f]), key=lambda x: x[0].numel() *
+                       x[0].element_size())
+    l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    l0.record()
+    big_d.copy_(big_h, non_blocking=True)
+    l1.record()
+    torch.cuda.synchronize()
+    link_gbs = big_h.numel() * big_h.element_size() / (l0.elapsed_time(l1) / 1e3) / 1e9
     barrier(world)
     s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s2.record()
@@ -311,7 +320,9 @@ def run_headline(args, rank, world):
     dom = max((0, 1), key=lambda f: kern[f]["avg_s"])
     return dict(value=value, elapsed=t_max, clocks=clk, kern=kern, dom=dom, launches_per_step=launches_per_step,
                 e2e=dict(value=e2e_value, unit="tokens/s", h2d_bytes_per_step=h2d,
-                         d2h_bytes_per_step=d2h, steps=e2e_steps),
+                         d2h_bytes_per_step=d2h, steps=e2e_steps,
+                         h2d_gbs=round(h2d / (e2e_t / e2e_steps) / 1e9, 1),
+                         link_copy_gbs=round(link_gbs, 1)),
                 hbm=hbm, src=src)
 
 
