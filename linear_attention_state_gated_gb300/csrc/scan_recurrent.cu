@@ -8,16 +8,36 @@
 // of the dense and KDA families is carried as exp(lambda) * M with M renormalised
 // by exact powers of two (KDA's per-channel gates stay inside M).
 //
-// Thread layout: the state (and, for the dense family, M) is split by
+// Thread layout: the state (and, for the dense and KDA families, M) is split by
 // columns: thread (g, c) owns column c and rows [g*RPT, (g+1)*RPT).  A token
 // is a rank-1 update of every column, so a thread needs only the scalar
 // u_c = k^T X[:, c] (a reduction over its G row groups) and the broadcast key.
+// M and S do not depend on each other, so for the families with M a chain takes
+// two CTAs, one for the columns of M (and lambda) and one for those of S (and
+// o_t): half the threads a CTA, two CTAs an SM whose per-token barriers do not
+// wait for each other.
 #include "internal.cuh"
 
 namespace hypic {
 namespace {
 
 constexpr int kTB = 16;  // tokens staged in shared memory per round
+
+// sum_r a[r] x[r] over RPT rows in four interleaved partial sums (a fixed order:
+// four independent FMA chains instead of one of RPT)
+template <int RPT>
+__device__ __forceinline__ float dot_rows(const float *a, const float (&x)[RPT]) {
+    static_assert(RPT % 4 == 0, "rows in fours");
+    float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+#pragma unroll
+    for (int r = 0; r < RPT; r += 4) {
+        p0 = fmaf(a[r], x[r], p0);
+        p1 = fmaf(a[r + 1], x[r + 1], p1);
+        p2 = fmaf(a[r + 2], x[r + 2], p2);
+        p3 = fmaf(a[r + 3], x[r + 3], p3);
+    }
+    return (p0 + p1) + (p2 + p3);
+}
 
 __device__ __forceinline__ void kahan_add(float &sum, float &comp, float v) {
     const float y = v - comp;
@@ -27,21 +47,25 @@ __device__ __forceinline__ void kahan_add(float &sum, float &comp, float v) {
 }
 
 template <int FAM, int DK, typename TIn>
-__global__ void __launch_bounds__(512) scan_recurrent_kernel(const ScanArgs a) {
-    constexpr int RPT = DK < 64 ? DK : 64;   // rows per thread
+__global__ void __launch_bounds__(256, 2) scan_recurrent_kernel(const ScanArgs a) {
+    constexpr int RPT = DK == 128 ? 64 : 32;   // rows per thread
     constexpr int G = DK / RPT;              // row groups
     constexpr bool kDense = FAM == HYPIC_DENSE || FAM == HYPIC_KDA;   // erasing update, M columns
     constexpr bool kKda = FAM == HYPIC_KDA;
     constexpr bool kDiag = FAM == HYPIC_DIAG || FAM == HYPIC_KDA;     // a gate per channel
     const int DV = a.dv;
-    const int NCOL = (kDense ? DK : 0) + DV;
-    const int NT = NCOL * G;
+    const bool mpart = kDense && (blockIdx.x & 1) == 0;  // this CTA: the columns of M (else of S)
+    const int NCOL = mpart ? DK : DV;
+    const int NT = NCOL * G;                             // working threads
+    const int NTB = (int)blockDim.x;                     // all threads (max(DK, DV) * G with M)
     const int tid = threadIdx.x;
+    const bool active = tid < NT;
     const int c = tid % NCOL, g = tid / NCOL;
-    const int row0 = g * RPT;
-    const bool mcol = kDense && c < DK;                  // column of M
-    const int scol = c - (kDense ? DK : 0);              // column of S (if !mcol)
+    const int row0 = active ? g * RPT : 0;
+    const bool mcol = mpart;                             // column of M
+    const int scol = c;                                  // column of S (if !mcol)
     const bool want_o = a.o_out != nullptr;
+    const bool o_here = want_o && !mpart;                // this CTA writes o_t
 
     extern __shared__ float smem[];
     float *sk = smem;                                    // [kTB][DK]
@@ -53,7 +77,7 @@ __global__ void __launch_bounds__(512) scan_recurrent_kernel(const ScanArgs a) {
     float *redo = red + 2 * G * NCOL;                    // [G][DV]
     float *redm = redo + G * DV;                         // [32]
 
-    const int unit = blockIdx.x;
+    const int unit = kDense ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
     const int h = unit % a.H;
     const int seg = (unit / a.H) % a.n_seg;
     const int l = unit / (a.H * a.n_seg);
@@ -66,7 +90,7 @@ __global__ void __launch_bounds__(512) scan_recurrent_kernel(const ScanArgs a) {
 
     float x[RPT];
 #pragma unroll
-    for (int r = 0; r < RPT; ++r) x[r] = (mcol && row0 + r == c) ? 1.f : 0.f;
+    for (int r = 0; r < RPT; ++r) x[r] = (mcol && active && row0 + r == c) ? 1.f : 0.f;
     float lam_sum = 0.f, lam_comp = 0.f;
     int lam_exp = 0;   // power-of-two exponent moved out of M
 
@@ -79,19 +103,20 @@ __global__ void __launch_bounds__(512) scan_recurrent_kernel(const ScanArgs a) {
     for (int64_t tb = t0; tb < t1; tb += kTB) {
         const int nt = (int)((t1 - tb) < kTB ? (t1 - tb) : kTB);
         __syncthreads();
-        for (int i = tid; i < nt * DK; i += NT) {
+        for (int i = tid; i < nt * DK; i += NTB) {
             const int tt = i / DK, d = i % DK;
             const int64_t row = (layer_row0 + tb + tt) * a.H + h;
             sk[tt * DK + d] = to_f32(Kp[row * DK + d]);
-            if (want_o) sq[tt * DK + d] = to_f32(Qp[row * DK + d]);
+            if (o_here) sq[tt * DK + d] = to_f32(Qp[row * DK + d]);
             if (kDiag) sa[tt * DK + d] = a.alpha[row * DK + d];
         }
-        for (int i = tid; i < nt * DV; i += NT) {
-            const int tt = i / DV, d = i % DV;
-            const int64_t row = (layer_row0 + tb + tt) * a.H + h;
-            sv[tt * DV + d] = to_f32(Vp[row * DV + d]);
-        }
-        for (int i = tid; i < nt; i += NT) {
+        if (!mpart)
+            for (int i = tid; i < nt * DV; i += NTB) {
+                const int tt = i / DV, d = i % DV;
+                const int64_t row = (layer_row0 + tb + tt) * a.H + h;
+                sv[tt * DV + d] = to_f32(Vp[row * DV + d]);
+            }
+        for (int i = tid; i < nt; i += NTB) {
             const int64_t row = (layer_row0 + tb + i) * a.H + h;
             if (!kDiag) sa[i] = a.alpha[row];
             sb[i] = a.beta ? a.beta[row] : 1.f;
@@ -104,13 +129,11 @@ __global__ void __launch_bounds__(512) scan_recurrent_kernel(const ScanArgs a) {
             if (kKda) {
                 // T_t = diag(alpha) (I - beta k k^T): erase, then gate each row
                 const float *at = sa + tt * DK + row0;
-                float p = 0.f;
-#pragma unroll
-                for (int r = 0; r < RPT; ++r) p = fmaf(kt[r], x[r], p);
+                const float p = dot_rows<RPT>(kt, x);
                 float u = p;
                 if (G > 1) {
                     float *rb = red + (tt & 1) * G * NCOL;
-                    rb[g * NCOL + c] = p;
+                    if (active) rb[g * NCOL + c] = p;
                     __syncthreads();
                     u = 0.f;
 #pragma unroll
@@ -127,13 +150,11 @@ __global__ void __launch_bounds__(512) scan_recurrent_kernel(const ScanArgs a) {
                 }
             } else if (kDense) {
                 const float al = sa[tt];
-                float p = 0.f;
-#pragma unroll
-                for (int r = 0; r < RPT; ++r) p = fmaf(kt[r], x[r], p);
+                const float p = dot_rows<RPT>(kt, x);
                 float u = p;
                 if (G > 1) {
                     float *rb = red + (tt & 1) * G * NCOL;
-                    rb[g * NCOL + c] = p;
+                    if (active) rb[g * NCOL + c] = p;
                     __syncthreads();
                     u = 0.f;
 #pragma unroll
@@ -164,17 +185,13 @@ __global__ void __launch_bounds__(512) scan_recurrent_kernel(const ScanArgs a) {
                 for (int r = 0; r < RPT; ++r) x[r] = fmaf(kt[r], w, at[row0 + r] * x[r]);
                 if (tid < DK) kahan_add(lam_sum, lam_comp, logf(at[tid]));
             }
-            if (want_o) {
+            if (o_here) {
                 float po = 0.f;
-                if (!mcol) {
-                    const float *qt = sq + tt * DK + row0;
-#pragma unroll
-                    for (int r = 0; r < RPT; ++r) po = fmaf(qt[r], x[r], po);
-                }
+                if (!mcol) po = dot_rows<RPT>(sq + tt * DK + row0, x);
                 const int64_t orow = (layer_row0 + tb + tt) * a.H + h;
                 if (G > 1) {
                     __syncthreads();
-                    if (!mcol) redo[g * DV + scol] = po;
+                    if (active) redo[g * DV + scol] = po;
                     __syncthreads();
                     if (!mcol && g == 0) {
                         float s = 0.f;
@@ -182,16 +199,16 @@ __global__ void __launch_bounds__(512) scan_recurrent_kernel(const ScanArgs a) {
                         for (int gg = 0; gg < G; ++gg) s += redo[gg * DV + scol];
                         Op[orow * DV + scol] = from_f32<TIn>(s);
                     }
-                } else if (!mcol) {
+                } else if (active) {
                     Op[orow * DV + scol] = from_f32<TIn>(po);
                 }
             }
         }
 
-        if (kDense) {
+        if (kDense && mpart) {
             // keep max|M| in [1, 2) with exact power-of-two scaling
             float mx = 0.f;
-            if (mcol) {
+            if (active) {
 #pragma unroll
                 for (int r = 0; r < RPT; ++r) mx = fmaxf(mx, fabsf(x[r]));
             }
@@ -201,7 +218,7 @@ __global__ void __launch_bounds__(512) scan_recurrent_kernel(const ScanArgs a) {
             if ((tid & 31) == 0) redm[tid >> 5] = mx;
             __syncthreads();
             mx = 0.f;
-            for (int w = 0; w < (NT + 31) / 32; ++w) mx = fmaxf(mx, redm[w]);
+            for (int w = 0; w < NTB / 32; ++w) mx = fmaxf(mx, redm[w]);
             if (mx > 0.f && (mx < 1.f || mx >= 2.f)) {
                 int ex;
                 frexpf(mx, &ex);
@@ -217,7 +234,8 @@ __global__ void __launch_bounds__(512) scan_recurrent_kernel(const ScanArgs a) {
     }
 
     const int64_t u_out = ((int64_t)l * a.n_seg + seg) * a.H + h;
-    if (!mcol) {
+    if (!active) {
+    } else if (!mcol) {
         float *So = a.S_out + u_out * DK * DV;
 #pragma unroll
         for (int r = 0; r < RPT; ++r) So[(int64_t)(row0 + r) * DV + scol] = x[r];
@@ -228,7 +246,7 @@ __global__ void __launch_bounds__(512) scan_recurrent_kernel(const ScanArgs a) {
     }
     if (FAM == HYPIC_DIAG) {   // lambda per channel
         if (tid < DK) a.lam_out[u_out * DK + tid] = lam_sum;
-    } else if (tid == 0) {
+    } else if (tid == 0 && (!kDense || mpart)) {   // with M: the M CTA, which holds the exponent
         const double lam = (double)lam_sum + (double)lam_exp * 0.69314718055994530942;
         a.lam_out[u_out] = (float)lam;
     }
@@ -236,10 +254,10 @@ __global__ void __launch_bounds__(512) scan_recurrent_kernel(const ScanArgs a) {
 
 template <int FAM, int DK, typename TIn>
 cudaError_t launch_one(const ScanArgs &a, cudaStream_t s) {
-    constexpr int RPT = DK < 64 ? DK : 64;
+    constexpr int RPT = DK == 128 ? 64 : 32;
     constexpr int G = DK / RPT;
     constexpr bool kM = FAM == HYPIC_DENSE || FAM == HYPIC_KDA;
-    const int ncol = (kM ? DK : 0) + a.dv;
+    const int ncol = kM ? (DK > a.dv ? DK : a.dv) : a.dv;   // columns of the wider CTA
     const int nt = ncol * G;
     const bool want_o = a.o_out != nullptr;
     size_t floats = (size_t)kTB * DK + (size_t)kTB * a.dv + (want_o ? (size_t)kTB * DK : 0) +
@@ -251,7 +269,7 @@ cudaError_t launch_one(const ScanArgs &a, cudaStream_t s) {
         if (e != cudaSuccess) return e;
     }
     const int64_t units = (int64_t)a.n_layers * a.n_seg * a.H;
-    kern<<<(unsigned)units, nt, smem, s>>>(a);
+    kern<<<(unsigned)(units * (kM ? 2 : 1)), nt, smem, s>>>(a);
     return cudaGetLastError();
 }
 
