@@ -350,8 +350,7 @@ constexpr uint32_t kTacc = 256;   // U^T - X0^T W^T, then Delta~^T operand in pl
 constexpr uint32_t kTw = 320;     // W^T accumulator (64 columns)
 constexpr uint32_t kTo1 = 384;    // O1^T accumulator (64 columns, o_t)
 constexpr uint32_t kTo2 = 448;    // O2^T accumulator (64 columns, o_t)
-constexpr uint32_t kTacc2 = 384;  // CTAs without o_t (also the transition half of the o_t form):
-                                  // the second k half of X0^T W^T (64 columns)
+constexpr uint32_t kTacc2 = 384;  // without o_t: the second k half of X0^T W^T (64 columns)
 
 struct StateCtl {
     uint64_t full[kNS], empty[kNS];
