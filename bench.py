@@ -818,25 +818,28 @@ def main():
     rank, world, local = dist_setup(args.gpus)
     h = run_headline(args, rank, world)
     rows = {}
-    if rank == 0 and "dense" in args.rows:
+    # the extra rows and the oracle baseline run at N = 1 only (with N GPUs every
+    # GPU would wait for rank 0 meanwhile)
+    solo = rank == 0 and world == 1
+    if solo and "dense" in args.rows:
         rows["dense_scan"] = run_dense(args, args.dense_L)
-    if rank == 0 and "kda" in args.rows:
+    if solo and "kda" in args.rows:
         rows["kda_scan"] = run_kda(args, args.dense_L)
-    if rank == 0 and "compose" in args.rows:
+    if solo and "compose" in args.rows:
         rows["compose"] = run_compose(args)
-    if rank == 0 and "seam" in args.rows:
+    if solo and "seam" in args.rows:
         rows["seam"] = run_seam(args)
-    if rank == 0 and "prefix" in args.rows:
+    if solo and "prefix" in args.rows:
         rows["prefix"] = run_prefix(args)
-    if rank == 0 and "chain" in args.rows:
+    if solo and "chain" in args.rows:
         rows["rag_chain"] = run_chain(args)
-    if rank == 0 and "mix" in args.rows:
+    if solo and "mix" in args.rows:
         rows["long_mix"] = run_long_mix(args)
     if rank != 0:
         barrier(world)
         return
     cpu = None
-    if not args.no_cpu:
+    if solo and not args.no_cpu:
         rate, t, cores, desc = oracle_sample_rate(args.L)
         cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc,
                "seconds": round(t, 2)}
