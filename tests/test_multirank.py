@@ -50,3 +50,29 @@ def test_reference_arm_two_ranks_prints_one_line():
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
     assert len(lines) == 1 and '"impl": "reference"' in lines[0]
+
+
+def test_profiled_traffic_follows_the_kernel_source(tmp_path, monkeypatch):
+    """The headline roofline's DRAM traffic comes from the committed ncu summary
+    only while the kernel source still hashes to what was profiled."""
+    import hashlib
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(ROOT, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    # the committed summary against the committed source
+    t = bench.profiled_traffic("scan_sd_tc_diag_B8x2048_H32.md", "linear_attention_state_gated_gb300/csrc/scan_sd_tc.cu")
+    assert t is not None and t > 2e9
+    # a copy of the tree whose kernel source differs: no traffic figure
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "k").mkdir()
+    src = tmp_path / "k" / "kernel.cu"
+    src.write_text("// kernel v1\n")
+    sha = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
+    (tmp_path / "profiles" / "s.md").write_text(
+        "# summary\n| metric | value |\ntraffic_bytes_per_launch_L8192: 1234\nsource_sha256_prefix: " + sha + "\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.profiled_traffic("s.md", "k/kernel.cu") == 1234.0
+    src.write_text("// kernel v2\n")
+    assert bench.profiled_traffic("s.md", "k/kernel.cu") is None
+    assert bench.profiled_traffic("missing.md", "k/kernel.cu") is None
