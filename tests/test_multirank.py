@@ -1,6 +1,7 @@
-"""The multi-rank (replicas) path of the benchmark on CPU: world size 2 over
-gloo.  Each rank runs an independent replica; the job's time is the slowest
-rank's and the throughput counts the units of every rank."""
+"""The benchmark's host-side logic on CPU: the multi-rank (replicas) path with
+world size 2 over gloo -- each rank runs an independent replica, the job's time
+is the slowest rank's and the throughput counts the units of every rank -- and
+the roofline's traffic figure taken from a committed ncu summary."""
 import os
 import subprocess
 import sys
