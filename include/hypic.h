@@ -158,16 +158,21 @@ int hypic_segment_scan_ws(int fam, int in_dtype, int n_layers, int n_seg,
  * its KV-cache pool at start-up; a host path that must not enter the allocator,
  * which can synchronise the device).
  *   Arguments as hypic_segment_scan without q / o_out.  Only fam = HYPIC_DENSE,
- *   in_dtype = HYPIC_BF16, d_k = d_v = 128 is served; other inputs, or a problem
- *   whose records need more than the 64 MiB (hypic_segment_scan_workspace_bytes
- *   gives the need; 64 MiB hold 1999 records of 33568 bytes), return
- *   HYPIC_EUNSUPPORTED and launch nothing.
+ *   in_dtype = HYPIC_BF16, d_k = d_v = 128 is served; another family, input type
+ *   or head size, or a problem whose records need more than the 64 MiB
+ *   (hypic_segment_scan_workspace_bytes gives the need; 64 MiB hold 1999 records
+ *   of 33568 bytes), returns HYPIC_EUNSUPPORTED and launches nothing.  A batch
+ *   whose segments are all empty (total_tokens = 0) needs no scratch and gets
+ *   lambda = 0, M = I, S = 0 as from hypic_segment_scan.
  *   The scratch's contents never need to start at zero.  It is one array per
  *   device for the whole process: two calls in flight at the same time (other
  *   streams or host threads) race on it, so callers serialise them.
- *   The first call on each device looks up the array's address
- *   (cudaGetSymbolAddress, with that device current) and caches it; a caller
- *   that will later capture its stream makes one call before capturing.
+ *   The first call in each CUDA context (per device: its primary context, or
+ *   a context the caller made current) looks up the array's address
+ *   (cudaGetSymbolAddress, with that device current) and caches it under the
+ *   context's id, so a context created later (after cudaDeviceReset, say) gets
+ *   a fresh lookup; a caller that will later capture its stream makes one call
+ *   in that context before capturing.
  */
 int hypic_segment_scan_static(int fam, int in_dtype, int n_layers, int n_seg,
                               int64_t total_tokens, int n_heads, int d_k, int d_v,
@@ -188,6 +193,8 @@ int hypic_segment_scan_static(int fam, int in_dtype, int n_layers, int n_seg,
  *   S_out   fp32  [n, H, d_k, d_v]; may be the same pointer as S_prev
  *                 (scalar, diag and dense); must not overlap S_C otherwise
  *   lam_prev, lam_out  like lam; both NULL or both given          -- T(C1), T(C1.C2)
+ *                      lam_out must not overlap lam, lam_prev, S_out or M_out
+ *                      (HYPIC_EINVAL): no in-place operator accumulation
  *   M_prev, M_out      like M (dense, kda; given iff lam_out is)
  * Dense M_out has max|M_out| in [1, 2) (exact power-of-two scaling into lam_out).
  * All pointers 16-byte aligned except scalar/dense lambdas (4-byte).
@@ -211,7 +218,9 @@ int hypic_compose(int fam, int n, int n_heads, int d_k, int d_v, const float *la
  *   pool_M     fp32  [pool_size, n_layers, H, d_k, d_k] (dense, kda; NULL otherwise)
  *   pool_S     fp32  [pool_size, n_layers, H, d_k, d_v]
  *   S_init     fp32  [n_req, n_layers, H, d_k, d_v] or NULL (=> 0)
- *   S_out      fp32  [n_req, n_layers, H, d_k, d_v]; may alias S_init
+ *   S_out      fp32  [n_req, n_layers, H, d_k, d_v]; may be S_init itself;
+ *              must overlap neither the pool nor (another part of) S_init:
+ *              HYPIC_EINVAL otherwise
  *   d_err      device int or NULL: an index outside [0, pool_size) or a
  *              chain length outside [0, max_chain] is clamped and reported.
  */

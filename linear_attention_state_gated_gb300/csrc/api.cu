@@ -208,13 +208,19 @@ int hypic_segment_scan_static(int fam, int in_dtype, int n_layers, int n_seg, in
     const int rc = scan_args(fam, in_dtype, n_layers, n_seg, total_tokens, n_heads, d_k, d_v, seg_offsets,
                              nullptr, k, v, alpha, beta, lam_out, M_out, S_out, nullptr, d_err, a, none);
     if (rc != HYPIC_OK || none) return rc;
+    if (fam != HYPIC_DENSE || in_dtype != HYPIC_BF16 || d_k != 128 || d_v != 128) return HYPIC_EUNSUPPORTED;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    if (total_tokens == 0) {   // only empty segments: lambda = 0, M = I, S = 0, written without scratch
+        if (hypic::scan_dense_tc_supported(a)) return from_cuda(hypic::launch_scan_dense_tc(a, s));
+        return from_cuda(hypic::launch_scan_recurrent(a, s));
+    }
     if (!hypic::scan_dense_ws_shape(a)) return HYPIC_EUNSUPPORTED;
     if (hypic::scan_dense_ws_bytes(a) > hypic::static_scratch_bytes()) return HYPIC_EUNSUPPORTED;
     if (!hypic::scan_dense_ws_supported(a)) return HYPIC_ECUDA;
     void *scratch = nullptr;
     if (hypic::static_scratch(&scratch) != cudaSuccess || !scratch) return HYPIC_ECUDA;
     a.ws = static_cast<float *>(scratch);
-    return from_cuda(hypic::launch_scan_dense_ws(a, static_cast<cudaStream_t>(cuda_stream)));
+    return from_cuda(hypic::launch_scan_dense_ws(a, s));
 }
 
 int hypic_compose(int fam, int n, int n_heads, int d_k, int d_v, const float *lam, const float *M,
@@ -255,6 +261,12 @@ int hypic_compose(int fam, int n, int n_heads, int d_k, int d_v, const float *la
     if (has_m(fam) &&
         (overlaps(S_out, sbytes, M, mbytes) || overlaps(S_out, sbytes, M_prev, mbytes) ||
          overlaps(M_out, mbytes, M, mbytes) || overlaps(M_out, mbytes, M_prev, mbytes)))
+        return HYPIC_EINVAL;
+    // lam_out is written while other threads (or another part of the grid) still
+    // read lam and lam_prev, so it may alias neither
+    const size_t lbytes = (size_t)n * n_heads * (fam == HYPIC_DIAG ? d_k : 1) * sizeof(float);
+    if (overlaps(lam_out, lbytes, lam, lbytes) || overlaps(lam_out, lbytes, lam_prev, lbytes) ||
+        overlaps(lam_out, lbytes, S_out, sbytes) || overlaps(lam_out, lbytes, M_out, mbytes))
         return HYPIC_EINVAL;
 
     hypic::ComposeArgs a;
@@ -358,6 +370,24 @@ int hypic_compose_chain(int fam, int n_req, int n_layers, int n_heads, int d_k, 
     const void *a4[] = {chain_len, seg_idx, pool_lam, d_err};
     for (const void *p : a4)
         if (p && !aligned(p, 4)) return HYPIC_EALIGN;
+    // S_out is written while other chains still read the pool: no overlap with it
+    // (S_out may be S_init itself, each chain reading its own state before writing it)
+    {
+        const int64_t units = (int64_t)n_req * n_layers * n_heads;
+        const int64_t entries = (int64_t)pool_size * n_layers * n_heads;
+        const int nl = fam == HYPIC_DIAG ? d_k : 1;
+        auto overlaps = [](const void *x, size_t xb, const void *y, size_t yb) {
+            if (!x || !y) return false;
+            const char *a = static_cast<const char *>(x), *b = static_cast<const char *>(y);
+            return a < b + yb && b < a + xb;
+        };
+        const size_t sb = (size_t)units * d_k * d_v * 4;
+        if (overlaps(S_out, sb, pool_S, (size_t)entries * d_k * d_v * 4) ||
+            overlaps(S_out, sb, pool_M, (size_t)entries * d_k * d_k * 4) ||
+            overlaps(S_out, sb, pool_lam, (size_t)entries * nl * 4) ||
+            (S_init && S_init != S_out && overlaps(S_out, sb, S_init, sb)))
+            return HYPIC_EINVAL;
+    }
 
     hypic::ChainArgs a;
     a.fam = compose_family(fam);

@@ -24,23 +24,66 @@ __device__ __align__(256) uint8_t g_scan_scratch[kStaticScratchBytes];
 
 int64_t static_scratch_bytes() { return kStaticScratchBytes; }
 
-// Device address of the scratch on the current device, looked up once per
-// device (with that device current) and cached.
+namespace {
+
+// Unique id of the CUDA context current on this thread (ids are never reused
+// within a process, unlike context handles after a device reset); false when
+// no context is current or the driver does not offer the calls.
+bool current_context_id(unsigned long long *id) {
+    using GetCurrentFn = CUresult (*)(CUcontext *);
+    using GetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+    static GetCurrentFn get_current = nullptr;
+    static GetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetIdFn>(p);
+    });
+    if (!get_current || !get_id) return false;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+// Device address of the scratch in the current context.  It is looked up
+// (cudaGetSymbolAddress) on the first call in a context and cached under that
+// context's id; a new context on the device (after cudaDeviceReset, or a
+// caller-made context) gets its own lookup.
 cudaError_t static_scratch(void **p) {
+    struct Slot {
+        unsigned long long ctx_id;
+        void *addr;
+    };
     static std::mutex mu;
-    static void *addr[kMaxDevices] = {};
+    static Slot slot[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    unsigned long long id = 0;
+    bool have_id = current_context_id(&id);
     std::lock_guard<std::mutex> lk(mu);
-    if (!addr[dev]) {
+    Slot &sl = slot[dev];
+    if (!have_id || !sl.addr || sl.ctx_id != id) {
         void *q = nullptr;
-        e = cudaGetSymbolAddress(&q, g_scan_scratch);
+        e = cudaGetSymbolAddress(&q, g_scan_scratch);   // makes the device's primary context current if none is
         if (e != cudaSuccess) return e;
-        addr[dev] = q;
+        if (!have_id) have_id = current_context_id(&id);
+        sl.addr = have_id ? q : nullptr;   // without a context id nothing is cached: looked up every call
+        sl.ctx_id = id;
+        *p = q;
+        return cudaSuccess;
     }
-    *p = addr[dev];
+    *p = sl.addr;
     return cudaSuccess;
 }
 

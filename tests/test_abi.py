@@ -145,11 +145,17 @@ def test_compose_rejects_bad_arguments(lib):
     assert compose(lib, fam=2, M=A + 0x300000, lp=A, lo=A, Mp=0, Mo=A) == EINVAL
     assert compose(lib, Sc=A + 0x100008) == EALIGN
     assert compose(lib, So=A + 0x100000 + 64) == EINVAL  # S_out overlaps S_C
+    # lam_out aliasing lam or lam_prev (no in-place operator accumulation), any family
+    for fam, M_ in ((0, 0), (1, 0), (2, A + 0x300000)):
+        Mp = A + 0x400000 if fam == 2 else 0
+        Mo = A + 0x500000 if fam == 2 else 0
+        assert compose(lib, fam=fam, M=M_, lp=A + 0x600000, lo=A, Mp=Mp, Mo=Mo) == EINVAL
+        assert compose(lib, fam=fam, M=M_, lp=A + 0x600000, lo=A + 0x600000, Mp=Mp, Mo=Mo) == EINVAL
     assert compose(lib, n=0) == OK
 
 
 def chain(lib, fam=0, R=2, L=2, H=2, dk=64, dv=64, mc=3, cl=A, idx=A, P_=5, pl=A, pM=0,
-          pS=A, Si=0, So=A, err=0):
+          pS=A, Si=0, So=A + 0x800000, err=0):
     return lib.hypic_compose_chain(fam, R, L, H, dk, dv, mc, P(cl or None), P(idx or None), P_,
                                    P(pl or None), P(pM or None), P(pS or None), P(Si or None),
                                    P(So or None), P(err or None), P(None))
@@ -165,6 +171,9 @@ def test_chain_rejects_bad_arguments(lib):
     assert chain(lib, fam=2, pM=0) == EINVAL
     assert chain(lib, pS=A + 4) == EALIGN
     assert chain(lib, cl=A + 2) == EALIGN
+    assert chain(lib, So=A + 0x10000) == EINVAL     # S_out inside the pool's states
+    assert chain(lib, pl=A + 0x801000) == EINVAL    # the pool's lambdas inside S_out
+    assert chain(lib, Si=A + 0x800000 + 0x100) == EINVAL   # S_init partly overlapping S_out
     assert chain(lib, R=0) == OK
 
 
