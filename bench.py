@@ -189,6 +189,18 @@ def scan_bytes(fam, n_tok_heads, n_units, d=128, in_bytes=2):
     return n_tok_heads * per_tok + n_units * per_unit
 
 
+# The pages' own figures, quoted as context (HYPIC evaluation on 8x H20 nodes,
+# model level; xix.ai/fr, evaluation and linear-layer paragraphs).  Not comparable
+# with the kernel measurements of this bench.
+PAGES_CONTEXT = {
+    "mean_ttft_vs_prefix_caching": "3.25x lower (2.77-4.05x)",
+    "slo_qps_vs_prefix_caching": "1.66x at a 1 s TTFT SLO (1.49-1.85x)",
+    "composed_vs_recompute_difference": 6e-5,
+    "state_construction_cost": "5.2-6.7 % of segment prefill (Qwen3.5-35B-A3B)",
+    "hardware": "8x H20 nodes (evaluation as a whole)",
+}
+
+
 # ------------------------------------------------------------------ our arm
 
 def run_headline(args, rank, world):
@@ -326,18 +338,31 @@ def run_headline(args, rank, world):
                 hbm=hbm, src=src)
 
 
+# tensor work one chunk of 64 tokens of one (layer, head) chain issues, in flops
+# (bf16 products, including the hi / lo splits); the algorithmic count is 180 k
+# per token-head (Gram, U and W, W X and K^T Delta at C = 64)
+DENSE_ALG_FLOP_PER_TOKEN_HEAD = 180e3
+
+
+def dense_issued_flop_per_chunk():
+    mm = lambda m, n, k: 2.0 * m * n * k   # noqa: E731
+    gram = mm(128, 64, 128)                  # [K; K or Q] K^T in the preparation pass
+    w = 2 * mm(128, 64, 64)                  # W^T = K^T (A diag(beta b))^T, A split hi / lo
+    u = 2 * mm(128, 64, 64)                  # U^T (state half only)
+    delta = 3 * mm(128, 64, 128)             # U^T - X0^T W^T, three-term split, per half
+    upd = 2 * mm(128, 128, 64)               # X^T += Delta~^T K, Delta~ split, per half
+    return gram + 2 * (w + delta + upd) + u
+
+
 def run_dense(args, L):
     import torch
     import linear_attention_state_gated_gb300 as hy
     from linear_attention_state_gated_gb300 import workloads as wl
     Lyr, H, d = 30, 32, 128
-    w = wl.dense_stack(seg_len=L, n_layers=Lyr, H=H, d=d, seed=2)
     dev = torch.device("cuda")
-    k = torch.from_numpy(w["k"]).to(torch.bfloat16).to(dev)
-    v = torch.from_numpy(w["v"]).to(torch.bfloat16).to(dev)
-    a = torch.from_numpy(w["alpha"]).to(dev)
-    b = torch.from_numpy(w["beta"]).to(dev)
-    offs = torch.from_numpy(w["seg_offsets"]).to(dev)
+    w = wl.dense_stack_device(L, n_layers=Lyr, H=H, d=d, seed=2)
+    k, v, a, b = w["k"], w["v"], w["alpha"], w["beta"]
+    offs = torch.tensor([0, L], dtype=torch.int64, device=dev)
     out = {"lam": torch.empty((Lyr, 1, H), dtype=torch.float32, device=dev),
            "S": torch.empty((Lyr, 1, H, d, d), dtype=torch.float32, device=dev),
            "M": torch.empty((Lyr, 1, H, d, d), dtype=torch.float32, device=dev)}
@@ -352,23 +377,34 @@ def run_dense(args, L):
     torch.cuda.synchronize()
     reps = 3
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
-    for s, e in evs:
-        s.record()
+    for s0, e0 in evs:
+        s0.record()
         hy.segment_scan(2, k, v, a, offs, beta=b, out=out, workspace=ws)
-        e.record()
+        e0.record()
     torch.cuda.synchronize()
-    t = sum(s.elapsed_time(e) for s, e in evs) / reps / 1e3
+    t = sum(s0.elapsed_time(e0) for s0, e0 in evs) / reps / 1e3
     tok_heads = Lyr * L * H
-    flops = tok_heads * 180e3       # algorithmic flops per token-head of the chunked form, C = 64
+    flops = tok_heads * DENSE_ALG_FLOP_PER_TOKEN_HEAD
+    issued = Lyr * H * (L // 64) * dense_issued_flop_per_chunk()
     _, bf16, bf16_sus, src = peaks()
     del k, v, a, b, offs, out, ws
-    vl = run_dense_varlen(args) if args.dense_form == "two_pass" else None
-    return {"workload": f"gated delta rule, {Lyr} layers x {H} heads x {d}, one segment of {L} tokens per layer",
+    torch.cuda.empty_cache()
+    return {"workload": f"gated delta rule, {Lyr} layers x {H} heads x {d}, one segment of {L} tokens per layer "
+                        "(inputs drawn on the device)",
             "value": L / t, "unit": "tokens/s (all 30 layers)", "head_tokens_per_s": tok_heads / t,
-            "ms": t * 1e3, "form": args.dense_form, "varlen": vl,
+            "ms": t * 1e3, "form": args.dense_form,
             "roofline": {"bound": "tensor", "achieved": flops / t / 1e12, "peak": bf16,
                          "unit": "TFLOP/s", "frac": flops / t / 1e12 / bf16, "traffic": None,
-                         "peak_kind": f"bf16 burst, {src}"}}
+                         "peak_kind": f"bf16 burst, {src}",
+                         "algorithmic_flop_per_token_head": DENSE_ALG_FLOP_PER_TOKEN_HEAD,
+                         "issued_tflops": issued / t / 1e12, "issued_frac": issued / t / 1e12 / bf16}}
+
+
+def run_dense_rows(args):
+    rows = {str(L): run_dense(args, L) for L in args.dense_lengths}
+    if args.dense_form == "two_pass":
+        rows["varlen"] = run_dense_varlen(args)
+    return rows
 
 
 def run_dense_varlen(args):
@@ -589,7 +625,43 @@ def run_prefix(args):
     return res
 
 
+def scan_rag_pool(fam, n_layers, H=32, d=128, P=200, timed=None):
+    """The RAG pool: P segments of U{1024..4096} tokens under the scalar/diagonal
+    law, drawn on the device layer by layer and scanned (hypic_segment_scan with
+    a workspace) into pool tensors lam [P, Lyr, H(, d)] and S [P, Lyr, H, d, d].
+    ``timed`` (a list) collects each layer's scan time in seconds."""
+    import torch
+    import linear_attention_state_gated_gb300 as hy
+    from linear_attention_state_gated_gb300 import workloads as wl
+    dev = torch.device("cuda")
+    lens = wl.rag_pool_lengths(P)
+    lam_shape = (P, n_layers, H, d) if fam == 1 else (P, n_layers, H)
+    pool_lam = torch.empty(lam_shape, dtype=torch.float32, device=dev)
+    pool_S = torch.empty((P, n_layers, H, d, d), dtype=torch.float32, device=dev)
+    N = int(lens.sum())
+    need = hy.segment_scan_workspace_bytes(fam, torch.bfloat16, 1, P, N, H, d, d)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev) if need > 0 else None
+    for l in range(n_layers):
+        k, v, a, offs = wl.scalar_diag_layer_device(fam, lens, l, H=H, d=d)
+        offs = torch.from_numpy(offs).to(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        out = hy.segment_scan(fam, k, v, a, offs, workspace=ws)
+        e1.record()
+        pool_lam[:, l].copy_(out["lam"][0])
+        pool_S[:, l].copy_(out["S"][0])
+        if timed is not None:
+            torch.cuda.synchronize()
+            timed.append(e0.elapsed_time(e1) / 1e3)
+        del k, v, a, out
+    torch.cuda.synchronize()
+    return lens, pool_lam, pool_S
+
+
 def run_chain(args):
+    """RAG-style composition: 64 requests x 20 distinct pool entries (Zipf(1.1), in
+    draw order) folded through all layers, over a pool of 200 segments scanned on
+    the device (lengths U{1024..4096}, scalar / diagonal law)."""
     import torch
     import linear_attention_state_gated_gb300 as hy
     from linear_attention_state_gated_gb300 import workloads as wl
@@ -600,35 +672,74 @@ def run_chain(args):
     cl, ix = torch.from_numpy(clen).to(dev), torch.from_numpy(idx).to(dev)
     Lyr = args.chain_layers
     for fam, name in ((0, "scalar"), (1, "diag")):
-        pool = wl.rag_pool(fam, n_layers=Lyr)
-        pl = torch.from_numpy(pool["lam"]).to(dev)
-        pS = torch.from_numpy(pool["S"]).to(dev)
-        del pool
+        scan_t = []
+        lens, pl, pS = scan_rag_pool(fam, Lyr, timed=scan_t)
         R, H, d = 64, 32, 128
         out = torch.empty((R, Lyr, H, d, d), dtype=torch.float32, device=dev)
         for _ in range(3):
             hy.compose_chain(fam, cl, ix, pl, pS, S_out=out)
         torch.cuda.synchronize()
         reps = 5
-        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s.record()
+        s0, e0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record()
         for _ in range(reps):
             hy.compose_chain(fam, cl, ix, pl, pS, S_out=out)
-        e.record()
+        e0.record()
         torch.cuda.synchronize()
-        t = s.elapsed_time(e) / reps / 1e3
+        t = s0.elapsed_time(e0) / reps / 1e3
         n_steps = int(clen.sum())
         composes = n_steps * Lyr                       # (request, segment, layer) triples
         lam_b = 4 * d if fam == 1 else 4
         by = n_steps * Lyr * H * (4 * d * d + lam_b) + R * Lyr * H * 4 * d * d
+        pool_tok = int(lens.sum())
         res[name] = {"value": composes / t, "unit": "composes/s (all 32 heads)", "ms": t * 1e3,
                      "layers": Lyr,
+                     "pool": {"segments": len(lens), "tokens": pool_tok, "layers": Lyr,
+                              "scan_ms_per_layer": 1e3 * sum(scan_t) / len(scan_t),
+                              "scan_tokens_per_s": pool_tok * Lyr / sum(scan_t),
+                              "note": "pool segments drawn on the device and scanned (untimed set-up of the chain)"},
                      "roofline": {"bound": "hbm", "achieved": by / t / 1e9, "peak": hbm,
                                   "unit": "GB/s", "frac": by / t / 1e9 / hbm, "traffic": None,
                                   "peak_kind": f"copy, {src}"}}
         del pl, pS, out
         torch.cuda.empty_cache()
     return res
+
+
+def run_scan_sd(args, L):
+    """Scalar and diagonal scans of 8 segments x L tokens x 32 heads (the headline's
+    kernels at a shorter length), each family timed alone."""
+    import torch
+    import linear_attention_state_gated_gb300 as hy
+    B, H, d = HEAD["B"], HEAD["H"], HEAD["d"]
+    hbm, _, _, src = peaks()
+    dev = torch.device("cuda")
+    res = {}
+    for fam, w in headline_inputs(L, seed=1).items():
+        k = torch.from_numpy(w["k"]).to(torch.bfloat16).to(dev)
+        v = torch.from_numpy(w["v"]).to(torch.bfloat16).to(dev)
+        a = torch.from_numpy(w["alpha"]).to(dev)
+        offs = torch.from_numpy(w["seg_offsets"]).to(dev)
+        need = hy.segment_scan_workspace_bytes(fam, torch.bfloat16, 1, B, B * L, H, d, d)
+        ws = torch.empty(need, dtype=torch.uint8, device=dev) if need > 0 else None
+        out = hy.segment_scan(fam, k, v, a, offs, workspace=ws)
+        torch.cuda.synchronize()
+        reps = 20
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for s0, e0 in evs:
+            s0.record()
+            hy.segment_scan(fam, k, v, a, offs, out=out, workspace=ws)
+            e0.record()
+        torch.cuda.synchronize()
+        t = sum(s0.elapsed_time(e0) for s0, e0 in evs) / reps / 1e3
+        by = scan_bytes(fam, B * L * H, B * H, d)
+        res[{0: "scalar", 1: "diag"}[fam]] = {
+            "tokens_per_s": B * L / t, "ms": t * 1e3,
+            "roofline": {"bound": "hbm", "achieved": by / t / 1e9, "peak": hbm, "unit": "GB/s",
+                         "frac": by / t / 1e9 / hbm, "peak_kind": f"HBM copy, {src}",
+                         "l2": "inputs below 129 MB stay in L2 between launches" if by < 129e6 else "inputs exceed L2"}}
+        del k, v, a, offs, ws, out
+    return {"workload": f"scalar / diagonal scan, batch {B} x {L} tokens, {H} heads, d_k=d_v={d}", **res}
 
 
 def run_long_mix(args):
@@ -793,9 +904,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="hypic", choices=["hypic", "reference"])
     ap.add_argument("--L", type=int, default=8192)
-    ap.add_argument("--rows", default="dense,kda,compose,seam,prefix,chain,mix",
-                    help="extra rows: dense,kda,compose,seam,prefix,chain,mix or none")
-    ap.add_argument("--dense-L", type=int, default=2048)
+    ap.add_argument("--rows", default="sd,dense,kda,compose,seam,prefix,chain,mix",
+                    help="extra rows: sd,dense,kda,compose,seam,prefix,chain,mix or none")
+    ap.add_argument("--dense-lengths", default="512,2048,8192,32768",
+                    help="dense rows: segment lengths of the 30-layer stack")
+    ap.add_argument("--sd-lengths", default="512,2048",
+                    help="scalar / diagonal rows at lengths other than the headline's")
+    ap.add_argument("--kda-L", type=int, default=2048)
     ap.add_argument("--dense-form", choices=["two_pass", "single"], default="two_pass",
                     help="dense row: two passes over a workspace, or the single-pass kernel")
     ap.add_argument("--compose-n", type=int, default=1920,
@@ -805,6 +920,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    args.dense_lengths = [int(x) for x in args.dense_lengths.split(",") if x]
+    args.sd_lengths = [int(x) for x in args.sd_lengths.split(",") if x]
 
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))
@@ -821,10 +938,12 @@ def main():
     # the extra rows and the oracle baseline run at N = 1 only (with N GPUs every
     # GPU would wait for rank 0 meanwhile)
     solo = rank == 0 and world == 1
+    if solo and "sd" in args.rows:
+        rows["scan_sd"] = {str(L): run_scan_sd(args, L) for L in args.sd_lengths}
     if solo and "dense" in args.rows:
-        rows["dense_scan"] = run_dense(args, args.dense_L)
+        rows["dense_scan"] = run_dense_rows(args)
     if solo and "kda" in args.rows:
-        rows["kda_scan"] = run_kda(args, args.dense_L)
+        rows["kda_scan"] = run_kda(args, args.kda_L)
     if solo and "compose" in args.rows:
         rows["compose"] = run_compose(args)
     if solo and "seam" in args.rows:
@@ -860,7 +979,10 @@ def main():
                      "algorithmic_bytes": kd["bytes"], "avg_launch_ms": kd["avg_s"] * 1e3,
                      "peak_kind": f"HBM copy, {h['src']}"},
         "kernels": {fam_name[f]: {"avg_launch_ms": h["kern"][f]["avg_s"] * 1e3,
-                                  "GB/s": h["kern"][f]["gbs"]} for f in (0, 1)},
+                                  "tokens_per_s": HEAD["B"] * args.L / h["kern"][f]["avg_s"],
+                                  "GB/s": h["kern"][f]["gbs"], "frac": h["kern"][f]["gbs"] / h["hbm"],
+                                  "algorithmic_bytes": h["kern"][f]["bytes"]} for f in (0, 1)},
+        "pages_context": PAGES_CONTEXT,
         "cpu_baseline": cpu, "e2e": h["e2e"], "clocks": h["clocks"],
         "gpu_launches": h["launches_per_step"] * args.steps, "rows": rows,
     }

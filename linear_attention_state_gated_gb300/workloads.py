@@ -21,7 +21,11 @@ draws stand in):
                          alpha = exp(-0.1 softplus(N(0,1))), beta = sigmoid(N(0,1)).
 * ``rag_pool`` / ``rag_requests`` -- a pool of cached (lambda, S) pairs and
                          requests drawing distinct pool entries by truncated
-                         Zipf(1.1) weights in random order.
+                         Zipf(1.1) weights in random order;
+                         ``rag_pool_lengths`` / ``scalar_diag_layer_device``
+                         draw the pool's segments themselves (lengths
+                         U{1024..4096}, the scalar/diagonal law) on the GPU,
+                         to be scanned into the pool.
 * ``long_mix``        -- one long prompt split into equal segments, some
                          cached and some not, gated delta rule.
 """
@@ -266,6 +270,26 @@ def long_mix_split(n_seg: int = 64, n_uncached: int = 16, seed: int = 4):
     return np.sort(g.permutation(n_seg)[:n_uncached]).astype(np.int64)
 
 
+def _seed_key(*parts) -> int:
+    x = 0
+    for p in parts:
+        x = (x * 1000003 + int(p)) % (2 ** 63)
+    return x
+
+
+def _dense_layer_device(g, seg_len, H, d, device, with_q):
+    """One layer of the gated delta rule's law, drawn from torch generator ``g``."""
+    import torch
+    k = torch.randn((seg_len, H, d), generator=g, device=device)
+    k = (k / k.norm(dim=-1, keepdim=True).clamp_min(1e-30)).to(torch.bfloat16)
+    v = torch.randn((seg_len, H, d), generator=g, device=device).to(torch.bfloat16)
+    q = torch.randn((seg_len, H, d), generator=g, device=device)
+    a = torch.randn((seg_len, H), generator=g, device=device)
+    alpha = torch.exp(-0.1 * torch.nn.functional.softplus(a))
+    beta = torch.sigmoid(torch.randn((seg_len, H), generator=g, device=device))
+    return k, v, (q.to(torch.bfloat16) if with_q else None), alpha, beta
+
+
 def long_mix_segment_device(seg: int, seg_len: int = 2048, n_layers: int = 30, H: int = 32,
                             d: int = 128, seed: int = 4, with_q: bool = True, device="cuda",
                             layers=None, heads=None):
@@ -289,16 +313,52 @@ def long_mix_segment_device(seg: int, seg_len: int = 2048, n_layers: int = 30, H
         out["q"] = torch.empty((nl, seg_len, H, d), dtype=torch.bfloat16, device=device)
     for i, l in enumerate(layers):
         g = torch.Generator(device=device)
-        g.manual_seed(((seed * 1000003 + seg) * 1000003 + l) % (2 ** 63))
-        k = torch.randn((seg_len, H, d), generator=g, device=device)
-        out["k"][i] = (k / k.norm(dim=-1, keepdim=True).clamp_min(1e-30)).to(torch.bfloat16)
-        out["v"][i] = torch.randn((seg_len, H, d), generator=g, device=device).to(torch.bfloat16)
-        q = torch.randn((seg_len, H, d), generator=g, device=device)
+        g.manual_seed(_seed_key(seed, seg, l))
+        k, v, q, alpha, beta = _dense_layer_device(g, seg_len, H, d, device, with_q)
+        out["k"][i], out["v"][i], out["alpha"][i], out["beta"][i] = k, v, alpha, beta
         if with_q:
-            out["q"][i] = q.to(torch.bfloat16)
-        a = torch.randn((seg_len, H), generator=g, device=device)
-        out["alpha"][i] = torch.exp(-0.1 * torch.nn.functional.softplus(a))
-        out["beta"][i] = torch.sigmoid(torch.randn((seg_len, H), generator=g, device=device))
+            out["q"][i] = q
     if heads is not None:
         out = {key: t[:, :, heads].contiguous() for key, t in out.items()}
     return out
+
+
+def dense_stack_device(seg_len: int, n_layers: int = 30, H: int = 32, d: int = 128, seed: int = 2,
+                       device="cuda"):
+    """The dense stack's law (``dense_stack``) drawn on the GPU, one segment of
+    ``seg_len`` tokens per layer, for lengths whose host draw would take minutes
+    (30 layers x 32768 tokens x 32 heads x 128 is 4 G values a tensor).  Layer l
+    draws from a generator seeded with (seed, 0, l)."""
+    return long_mix_segment_device(0, seg_len=seg_len, n_layers=n_layers, H=H, d=d, seed=seed + 1000,
+                                   with_q=False, device=device)
+
+
+def rag_pool_lengths(P: int = 200, len_lo: int = 1024, len_hi: int = 4096, seed: int = 3) -> np.ndarray:
+    """Segment lengths of the RAG pool: P seeded draws from U{len_lo..len_hi}."""
+    return rng(seed + 2000).integers(len_lo, len_hi + 1, size=P).astype(np.int64)
+
+
+def scalar_diag_layer_device(family: int, lengths, layer: int, H: int = 32, d: int = 128, seed: int = 3,
+                             device="cuda", heads=None):
+    """One layer of a packed batch of segments under the scalar/diagonal law of
+    ``scalar_diag`` (k L2-normalised N(0,1), v ~ N(0,1), bf16; gamma_h per token,
+    or sigmoid(N(2,1))^(1/16) per channel), drawn on the GPU from a generator
+    seeded with (seed, family, layer).  Returns k, v [1, N, H, d] bf16, alpha
+    [1, N, H] or [1, N, H, d] fp32 and the int64 segment offsets (host)."""
+    import torch
+    offs = _offsets(list(lengths))
+    N = int(offs[-1])
+    g = torch.Generator(device=device)
+    g.manual_seed(_seed_key(seed, family, layer))
+    k = torch.randn((N, H, d), generator=g, device=device)
+    k = (k / k.norm(dim=-1, keepdim=True).clamp_min(1e-30)).to(torch.bfloat16)
+    v = torch.randn((N, H, d), generator=g, device=device).to(torch.bfloat16)
+    if family == SCALAR:
+        alpha = torch.from_numpy(retnet_gamma(H)).to(device)[None, :].expand(N, H).contiguous()
+    elif family == DIAG:
+        alpha = torch.sigmoid(torch.randn((N, H, d), generator=g, device=device) + 2.0) ** (1.0 / 16.0)
+    else:
+        raise ValueError("scalar_diag_layer_device: family must be SCALAR or DIAG")
+    if heads is not None:
+        k, v, alpha = k[:, heads].contiguous(), v[:, heads].contiguous(), alpha[:, heads].contiguous()
+    return k[None], v[None], alpha[None], offs

@@ -76,11 +76,9 @@ def test_prefix_long_group_with_growing_operators(d):
     ref = oracle.compose_prefix(wl.DENSE, clen, idx, lam, S, pool_M=M)
     got = hy.compose_prefix(wl.DENSE, to_dev(clen), to_dev(idx), to_dev(lam), to_dev(S), pool_M=to_dev(M))
     M_g = to_host(got["M"])
-    # d = 128 multiplies on the tensor cores (bf16 three-way splits, fp32 accumulation in
-    # the MMA unit): ~1e-6 relative a product on these operators, so an n-step operator
-    # chain is held to n * 1e-6; the CUDA-core fp32 path (d = 64) to the fp32 bound
-    tol = 40 * 1e-6 if d == 128 else TOL_F32
-    assert t_err(2, to_host(got["lam"]), ref["lam"], M_g, ref["M"]).max() <= tol
+    err = t_err(2, to_host(got["lam"]), ref["lam"], M_g, ref["M"])
+    print(f"d={d} operator chain error max {err.max():.3e} mean {err.mean():.3e}")
+    assert err.max() <= TOL_F32
     mx = np.abs(M_g).max(axis=(-2, -1))
     assert np.all((mx >= 1) & (mx < 2))
 
