@@ -111,7 +111,7 @@ int hypic_segment_scan(int fam, int in_dtype, int n_layers, int n_seg,
  * (then its workspace may be NULL).  A negative hypic_status on bad counts.
  * Today the scratch is used with bf16 inputs and d_k = d_v = 128 by
  *   the dense family: one record per (layer, head, 64-token chunk slot) of
- *     33568 bytes (50192 bytes with o_t), n_layers * n_heads * (n_seg +
+ *     49424 bytes (50192 bytes with o_t), n_layers * n_heads * (n_seg +
  *     total_tokens / 64) records, then n_seg int32 (the segments ranked by
  *     length: the longest chains are started first), each part rounded up to
  *     256 bytes;
@@ -160,8 +160,8 @@ int hypic_segment_scan_ws(int fam, int in_dtype, int n_layers, int n_seg,
  *   Arguments as hypic_segment_scan without q / o_out.  Only fam = HYPIC_DENSE,
  *   in_dtype = HYPIC_BF16, d_k = d_v = 128 is served; another family, input type
  *   or head size, or a problem whose records need more than the 64 MiB
- *   (hypic_segment_scan_workspace_bytes gives the need; 64 MiB hold 1999 records
- *   of 33568 bytes), returns HYPIC_EUNSUPPORTED and launches nothing.  A batch
+ *   (hypic_segment_scan_workspace_bytes gives the need; 64 MiB hold 1357 records
+ *   of 49424 bytes), returns HYPIC_EUNSUPPORTED and launches nothing.  A batch
  *   whose segments are all empty (total_tokens = 0) needs no scratch and gets
  *   lambda = 0, M = I, S = 0 as from hypic_segment_scan.
  *   The scratch's contents never need to start at zero.  It is one array per

@@ -43,7 +43,7 @@ __device__ __forceinline__ int exponent_of(float mx) {   // 2^e <= mx < 2^(e+1)
 //   T = sum_{k=j}^{i-1} L_ik A_kj,  A_ij = -A_ii T,
 // four adjacent columns of one row per task (16-byte loads of A and T).
 // NT threads (pt = 0 .. NT-1) take part; named barrier BAR.
-template <int DIST, int NT, int BAR>
+template <int DIST, int NT, int BAR, bool PACKED>
 __device__ __forceinline__ void inverse_level(const float *Lw, float *Aw, float *Tw, int pt) {
     constexpr int NB = 4 - DIST;
     for (int task = pt; task < NB * 64; task += NT) {
@@ -52,14 +52,29 @@ __device__ __forceinline__ void inverse_level(const float *Lw, float *Aw, float 
         const float *lrow = Lw + (bi * 16 + r) * kLd + bj * 16;
         const float *acol = Aw + (bj * 16) * kLd + bj * 16 + c4;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (PACKED) {
+            // packed f32x2 FMAs (two columns an instruction), two partial sums per pair
+            uint64_t a01[2] = {0, 0}, a23[2] = {0, 0};
 #pragma unroll
-        for (int k = 0; k < 16 * DIST; ++k) {
-            const float lv = lrow[k];
-            const float4 av = *reinterpret_cast<const float4 *>(acol + k * kLd);
-            acc.x = fmaf(lv, av.x, acc.x);
-            acc.y = fmaf(lv, av.y, acc.y);
-            acc.z = fmaf(lv, av.z, acc.z);
-            acc.w = fmaf(lv, av.w, acc.w);
+            for (int k = 0; k < 16 * DIST; ++k) {
+                const float lv = lrow[k];
+                const uint64_t l2 = pk2(lv, lv);
+                const float4 av = *reinterpret_cast<const float4 *>(acol + k * kLd);
+                a01[k & 1] = fma2(l2, pk2(av.x, av.y), a01[k & 1]);
+                a23[k & 1] = fma2(l2, pk2(av.z, av.w), a23[k & 1]);
+            }
+            upk2(add2(a01[0], a01[1]), acc.x, acc.y);
+            upk2(add2(a23[0], a23[1]), acc.z, acc.w);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 16 * DIST; ++k) {
+                const float lv = lrow[k];
+                const float4 av = *reinterpret_cast<const float4 *>(acol + k * kLd);
+                acc.x = fmaf(lv, av.x, acc.x);
+                acc.y = fmaf(lv, av.y, acc.y);
+                acc.z = fmaf(lv, av.z, acc.z);
+                acc.w = fmaf(lv, av.w, acc.w);
+            }
         }
         *reinterpret_cast<float4 *>(Tw + blk * 256 + r * 16 + c4) = acc;
     }
@@ -70,14 +85,28 @@ __device__ __forceinline__ void inverse_level(const float *Lw, float *Aw, float 
         const float *arow = Aw + (bi * 16 + r) * kLd + bi * 16;   // A_ii, zero above the diagonal
         const float *tcol = Tw + blk * 256 + c4;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (PACKED) {
+            uint64_t a01[2] = {0, 0}, a23[2] = {0, 0};
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const float av = arow[k];
-            const float4 tv = *reinterpret_cast<const float4 *>(tcol + k * 16);
-            acc.x = fmaf(av, tv.x, acc.x);
-            acc.y = fmaf(av, tv.y, acc.y);
-            acc.z = fmaf(av, tv.z, acc.z);
-            acc.w = fmaf(av, tv.w, acc.w);
+            for (int k = 0; k < 16; ++k) {
+                const float av = arow[k];
+                const uint64_t m2 = pk2(av, av);
+                const float4 tv = *reinterpret_cast<const float4 *>(tcol + k * 16);
+                a01[k & 1] = fma2(m2, pk2(tv.x, tv.y), a01[k & 1]);
+                a23[k & 1] = fma2(m2, pk2(tv.z, tv.w), a23[k & 1]);
+            }
+            upk2(add2(a01[0], a01[1]), acc.x, acc.y);
+            upk2(add2(a23[0], a23[1]), acc.z, acc.w);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const float av = arow[k];
+                const float4 tv = *reinterpret_cast<const float4 *>(tcol + k * 16);
+                acc.x = fmaf(av, tv.x, acc.x);
+                acc.y = fmaf(av, tv.y, acc.y);
+                acc.z = fmaf(av, tv.z, acc.z);
+                acc.w = fmaf(av, tv.w, acc.w);
+            }
         }
         *reinterpret_cast<float4 *>(Aw + (bi * 16 + r) * kLd + bj * 16 + c4) =
             make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
@@ -91,7 +120,8 @@ __device__ __forceinline__ void inverse_level(const float *Lw, float *Aw, float 
 // dependent chain of 16 steps -- then three block levels.  ZERO_UPPER also
 // writes the zero blocks above the diagonal (else the caller never reads them).
 // Needs NT >= 128; Tw holds 3 x 256 floats.  Ends with a barrier.
-template <int NT, int BAR, bool ZERO_UPPER = true>
+// PACKED: the block levels with packed f32x2 FMAs (fewer instructions, more registers).
+template <int NT, int BAR, bool ZERO_UPPER = true, bool PACKED = false>
 __device__ __forceinline__ void tri_inverse(const float *Lw, float *Aw, float *Tw, int pt) {
     static_assert(NT >= 128, "one column per thread for the diagonal blocks, the rest zero the upper blocks");
     if (pt < 64) {
@@ -117,9 +147,9 @@ __device__ __forceinline__ void tri_inverse(const float *Lw, float *Aw, float *T
         }
     }
     bar_sync(BAR, NT);
-    inverse_level<1, NT, BAR>(Lw, Aw, Tw, pt);
-    inverse_level<2, NT, BAR>(Lw, Aw, Tw, pt);
-    inverse_level<3, NT, BAR>(Lw, Aw, Tw, pt);
+    inverse_level<1, NT, BAR, PACKED>(Lw, Aw, Tw, pt);
+    inverse_level<2, NT, BAR, PACKED>(Lw, Aw, Tw, pt);
+    inverse_level<3, NT, BAR, PACKED>(Lw, Aw, Tw, pt);
 }
 
 }  // namespace dense

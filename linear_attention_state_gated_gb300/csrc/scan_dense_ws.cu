@@ -47,31 +47,41 @@ constexpr int kD = 128;
 constexpr int kBox = kC * 128;   // 64 channels x 64 tokens, bf16: 8 KB
 
 // ---------------------------------------------------------------- workspace record
-// One record per (layer, head, chunk slot), floats:
-//   [0, 4096)        A diag(beta b) as bf16 hi / lo operand tiles (row t, s
+// One record per (layer, head, chunk slot), floats.  Without o_t:
+//   [0, 8192)        -W^T as bf16 hi / lo operand tiles (row k of 128, tokens t
+//                    contiguous, 128-byte swizzle), 16 KB each
+//   [8192, 12288)    A diag(beta) as bf16 hi / lo operand tiles (row t, s
 //                    contiguous, 128-byte swizzle), 8 KB each
+//   G = 12288        gates (below)
+// With o_t:
+//   [0, 4096)        A diag(beta b) as bf16 hi / lo operand tiles, 8 KB each
 //   [4096, 8192)     A diag(beta), the same way
-//   G + t            b_C / b_t        (G = 8192)
-//   G + 64 + t       beta_t b_t
-//   G + 128 + t      beta_t
-//   G + 192, G + 193 log b_C, b_C
-//   with o_t only:
+//   G = 8192         gates, then
 //   G + 196 + t      b_t
 //   [G + 260, +4096) Gq as bf16 hi / lo operand tiles (row t, s contiguous,
 //                    128-byte swizzle), 8 KB each
+// Gates without o_t: G + t  b_C / b_t;  G + 64, G + 65  log b_C, b_C.
+// Gates with o_t: G + t  b_C / b_t;  G + 64 + t  beta_t b_t;  G + 128 + t  beta_t;
+//        G + 192, G + 193  log b_C, b_C.
 // The state pass stages the head of a record (all but Gq) with the chunk's keys;
 // Gq has a buffer of its own.  Chunk j of segment s (tokens from t0) uses slot
 // s + floor(t0 / 64) + j, so the slots of different segments never collide and a
 // (layer, head) needs at most n_seg + floor(N / 64) of them.
 template <bool O>
 struct Rec {
-    static constexpr int Abb = 0, Ab = 4096, G = 8192;
-    static constexpr int Gw = G, Gbb = G + 64, Gbeta = G + 128, LC = G + 192, BC = G + 193, B = G + 196;
-    static constexpr int Head = O ? G + 260 : G + 200;     // floats staged with the chunk (multiples of 4)
+    static constexpr int Wt = 0;                            // without o_t
+    static constexpr int Abb = 0;                           // with o_t
+    static constexpr int Ab = O ? 4096 : 8192;
+    static constexpr int G = O ? 8192 : 12288;
+    static constexpr int Gw = G;
+    static constexpr int Gbb = G + 64, Gbeta = G + 128, B = G + 196;   // with o_t
+    static constexpr int LC = O ? G + 192 : G + 64, BC = LC + 1;
+    static constexpr int Head = O ? G + 260 : G + 68;      // floats staged with the chunk (multiples of 4)
     static constexpr int Gq = G + 260;                      // with o_t
     static constexpr int Floats = O ? Gq + 4096 : Head;
-    static constexpr int Bytes = Floats * 4;                // 33568 / 50192
-    static constexpr int HeadBytes = Head * 4;              // 33568 / 33808
+    static constexpr int Bytes = Floats * 4;                // 49424 / 50192
+    static constexpr int HeadBytes = Head * 4;              // 49424 / 33808
+    static constexpr int GateFloats = Head - G;             // without o_t: b_C / b, log b_C, b_C (68)
 };
 
 __host__ __device__ inline int64_t n_slots(int64_t N, int n_seg) { return (int64_t)n_seg + N / kC; }
@@ -88,7 +98,15 @@ constexpr int kPK = 0;                        // K0 | Q0 (or K0) | K1 | Q1 (or K
 constexpr int kPAw = kC * kLd * 4;            // L at [0, kPAw), A after it
 constexpr int kPTw = kPAw + kC * kLd * 4;
 constexpr int kPCtl = kPTw + 3 * 256 * 4;
+// without o_t: the keys again for W^T (over L once the inverse is done) and the
+// A diag(beta b) operand tiles (over A once every thread has read its part)
+constexpr int kPW = 0;
+constexpr int kPAb = kPAw;
+constexpr int kPWst = 0;                      // then -W^T hi / lo (32 KB) staged for the bulk copy
 static_assert(kPTw >= 4 * kBox, "the Gram operands end before the temporaries");
+static_assert(kPW + 2 * kBox <= kPAw, "the keys of W^T fit in L's region");
+static_assert(kPAb % 1024 == 0 && kPAb + 2 * kBox <= kPTw, "the A diag(beta b) tiles fit in A's region");
+static_assert(kPWst + 32768 <= kPTw, "the staged -W^T tiles end before the temporaries");
 
 struct PrepCtl {
     uint64_t full, mma;
@@ -174,13 +192,16 @@ __global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_cons
             ctl->gbeta[t] = pb[q];
             ctl->gbb[t] = pb[q] * bt;
             rec[R::Gw + t] = expf(total - inc[q]);
-            rec[R::Gbb + t] = pb[q] * bt;
-            rec[R::Gbeta + t] = pb[q];
-            if (O) rec[R::B + t] = bt;
+            if (O) {
+                rec[R::Gbb + t] = pb[q] * bt;
+                rec[R::Gbeta + t] = pb[q];
+                rec[R::B + t] = bt;
+            }
         }
         if (lane == 0) {
             rec[R::LC] = total;
             rec[R::BC] = expf(total);
+            if (!O) rec[R::BC + 1] = rec[R::BC + 2] = 0.f;
         }
         // Gram [K; Q] K^T: lanes 0..63 K K^T, lanes 64..127 Q K^T (K K^T again without o_t)
         if (lane == 0) {
@@ -218,10 +239,18 @@ __global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_cons
 #pragma unroll
             for (int i = 0; i < 32; ++i) gs[i] = ctl->gl[cbase + i];
             tmem_wait_ld();
+            // 16-byte stores: rows are kLd floats apart, so 4-byte stores of one column
+            // by the warp's 32 rows would hit 8 banks four times over
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int sc = cbase + i;
-                Lw[t * kLd + sc] = sc < t ? bt * __expf(lt - gs[i]) * __uint_as_float(r[i]) : 0.f;
+            for (int i = 0; i < 32; i += 4) {
+                float4 v;
+                float *vp = &v.x;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int sc = cbase + i + e;
+                    vp[e] = sc < t ? bt * __expf(lt - gs[i + e]) * __uint_as_float(r[i + e]) : 0.f;
+                }
+                *reinterpret_cast<float4 *>(Lw + t * kLd + cbase + i) = v;
             }
         } else if (warp < 2) {
             // ---- L[t][s] = beta_t exp(Lambda_t - Lambda_s) G[t][s] for s < t
@@ -234,9 +263,15 @@ __global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_cons
                 for (int i = 0; i < 32; ++i) gs[i] = ctl->gl[cb * 32 + i];
                 tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int sc = cb * 32 + i;
-                    Lw[t * kLd + sc] = sc < t ? bt * __expf(lt - gs[i]) * __uint_as_float(r[i]) : 0.f;
+                for (int i = 0; i < 32; i += 4) {
+                    float4 v;
+                    float *vp = &v.x;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int sc = cb * 32 + i + e;
+                        vp[e] = sc < t ? bt * __expf(lt - gs[i + e]) * __uint_as_float(r[i + e]) : 0.f;
+                    }
+                    *reinterpret_cast<float4 *>(Lw + t * kLd + cb * 32 + i) = v;
                 }
             }
         } else if (O) {
@@ -270,9 +305,17 @@ __global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_cons
                 }
             }
         }
+        if (!O) fence_async_smem();   // L's region takes the keys again (async proxy) after the inverse
         __syncthreads();
-        dense::tri_inverse<kPThreads, 1, false>(Lw, Aw, Tw, tid);
-        {
+        dense::tri_inverse<kPThreads, 1, false, true>(Lw, Aw, Tw, tid);
+        if (!O && tid == 0) {
+            // the keys again for W^T, into L's dead region, while the tiles are built
+            mbar_expect_tx(&ctl->full, 2 * kBox);
+            const int row = (int)((int64_t)l * a.N + c0);
+            tma_load_3d(smem + kPW, &tm_k, &ctl->full, 0, h, row);
+            tma_load_3d(smem + kPW + kBox, &tm_k, &ctl->full, 64, h, row);
+        }
+        if (O) {
             // ---- A diag(beta b) and A diag(beta) -> bf16 hi / lo tiles in the record (row t,
             // 8-column group c at 16-byte position c ^ (t & 7); zero above the diagonal blocks)
             uint8_t *tiles = reinterpret_cast<uint8_t *>(rec + R::Abb);
@@ -304,6 +347,106 @@ __global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_cons
                                hv[p], lv[p]);
                 *reinterpret_cast<uint4 *>(tiles + 16384 + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
                 *reinterpret_cast<uint4 *>(tiles + 24576 + off) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+            }
+        } else {
+            // ---- A diag(beta) -> bf16 hi / lo tiles in the record, A diag(beta b) -> hi / lo
+            // tiles in shared memory over A itself (the operand of W^T): every thread reads its
+            // A values first (row t, 8-column group c at 16-byte position c ^ (t & 7); zero
+            // above the diagonal blocks)
+            uint8_t *tiles = reinterpret_cast<uint8_t *>(rec + R::Ab);
+            uint32_t wh[4][4], wl[4][4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int f = tid + kPThreads * i;   // 0 .. 511
+                const int tt = f >> 3, c = f & 7;
+                float x[8];
+                if ((c >> 1) > (tt >> 4)) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) x[e] = 0.f;
+                } else {
+                    const float4 x0 = *reinterpret_cast<const float4 *>(Aw + tt * kLd + c * 8);
+                    const float4 x1 = *reinterpret_cast<const float4 *>(Aw + tt * kLd + c * 8 + 4);
+                    x[0] = x0.x; x[1] = x0.y; x[2] = x0.z; x[3] = x0.w;
+                    x[4] = x1.x; x[5] = x1.y; x[6] = x1.z; x[7] = x1.w;
+                }
+                const int off = tt * 128 + ((c ^ (tt & 7)) << 4);
+#pragma unroll
+                for (int p = 0; p < 4; ++p)
+                    split_pair(x[2 * p] * ctl->gbb[c * 8 + 2 * p], x[2 * p + 1] * ctl->gbb[c * 8 + 2 * p + 1],
+                               wh[i][p], wl[i][p]);
+                uint32_t hv[4], lv[4];
+#pragma unroll
+                for (int p = 0; p < 4; ++p)
+                    split_pair(x[2 * p] * ctl->gbeta[c * 8 + 2 * p], x[2 * p + 1] * ctl->gbeta[c * 8 + 2 * p + 1],
+                               hv[p], lv[p]);
+                *reinterpret_cast<uint4 *>(tiles + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                *reinterpret_cast<uint4 *>(tiles + 8192 + off) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+            }
+            __syncthreads();   // A (fp32) is read for the last time
+            uint8_t *wop = smem + kPAb;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int f = tid + kPThreads * i;
+                const int tt = f >> 3, c = f & 7;
+                const int off = tt * 128 + ((c ^ (tt & 7)) << 4);
+                *reinterpret_cast<uint4 *>(wop + off) = make_uint4(wh[i][0], wh[i][1], wh[i][2], wh[i][3]);
+                *reinterpret_cast<uint4 *>(wop + kBox + off) = make_uint4(wl[i][0], wl[i][1], wl[i][2], wl[i][3]);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncthreads();   // the operand tiles are in
+            // ---- W^T = K^T (A diag(beta b))^T on the tensor cores, into the Gram's TMEM columns
+            if (tid == 0) {
+                ok = mbar_wait(&ctl->full, 1);
+                if (ok) {
+                    tc_fence_after();
+                    constexpr uint32_t id_w = idesc_bf16_f32(128, 64, true, false);   // K^T MN-major
+                    const uint32_t kb = smem_addr(smem + kPW), ab = smem_addr(wop);
+                    // the lo products first: the accumulator rounds each instruction's sum
+#pragma unroll
+                    for (int hl = 1; hl >= 0; --hl)
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)
+                            mma_f16(tmem, smem_desc_sw128(kb + (uint32_t)ks * 2048u, kBox, 1024),
+                                    smem_desc_sw128(ab + (uint32_t)hl * kBox + (uint32_t)ks * 32u, 0, 1024), id_w,
+                                    (hl == 0 || ks > 0) ? 1u : 0u);
+                }
+                mma_commit(&ctl->mma);
+            }
+            ok = __syncthreads_and(ok && mbar_wait(&ctl->mma, 1));
+            tc_fence_after();
+            if (ok) {
+                // ---- -W^T -> bf16 hi / lo tiles (row k = this thread's TMEM lane, tokens t
+                // contiguous, 16-byte group c at position c ^ (k & 7)), staged in shared
+                // memory over the dead keys and operand tiles, then one bulk copy to the record
+                const int k = tid;
+                uint8_t *wt = smem + kPWst;
+                for (int cb = 0; cb < 2; ++cb) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(cb * 32), r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const int c = cb * 4 + cc;
+                        uint32_t hv[4], lv[4];
+#pragma unroll
+                        for (int p = 0; p < 4; ++p)
+                            split_pair(-__uint_as_float(r[cc * 8 + 2 * p]), -__uint_as_float(r[cc * 8 + 2 * p + 1]),
+                                       hv[p], lv[p]);
+                        const int off = k * 128 + ((c ^ (k & 7)) << 4);
+                        *reinterpret_cast<uint4 *>(wt + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                        *reinterpret_cast<uint4 *>(wt + 16384 + off) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+                    }
+                }
+                fence_async_smem();
+                __syncthreads();
+                if (tid == 0) {
+                    bulk_store(rec + R::Wt, wt, 32768u);
+                    bulk_commit();
+                    bulk_wait_read_all();   // the staging area stays valid until the copy has read it
+                }
+            } else if (tid == 0 && a.d_err) {
+                atomicExch(a.d_err, (int)HYPIC_ETIMEOUT);
             }
         }
     } else if (tid == 0 && a.d_err) {
@@ -368,8 +511,8 @@ struct StateCtl {
 };
 template <bool O>
 constexpr int state_smem() { return Smem<O>::Ctl + (int)sizeof(StateCtl) + 1024; }
-static_assert(state_smem<false>() <= 232448 && state_smem<true>() <= 232448, "fits in one SM's shared memory");
-static_assert(Smem<true>::Stage % 1024 == 0 && Smem<false>::Stage % 1024 == 0, "operand tiles 1024-byte aligned");
+static_assert(state_smem<true>() <= 232448, "fits in one SM's shared memory");
+static_assert(Smem<true>::Stage % 1024 == 0, "operand tiles 1024-byte aligned");
 
 // max over the 16 state warps (named barrier 2)
 __device__ __forceinline__ float state_max(float mx, StateCtl *ctl, int sw, int lane) {
@@ -979,6 +1122,449 @@ __global__ void __maxnreg__(80)
     }
 }
 
+// ================================================================ pass 2 without o_t: both halves
+//
+// One CTA per chain holds X^T = [M | S]^T whole (two 128-column halves in TMEM) and
+// walks its chunks with the two halves interleaved, so that one half's CUDA-core
+// conversions overlap the other half's tensor products.  -W^T comes ready from
+// the record (the preparation pass built it), so both halves read one copy.
+// Each half has its own X0 operand: hi in TMEM, lo in shared memory (TMEM holds
+// X, X0 hi and Delta of both halves: 2 x (128 + 64 + 64) columns).  Per chunk j
+// the conversion warps run
+//   X0_M(j) | X0_S(j) | Delta~_M(j) | Delta~_S(j)
+// while the two issuing threads (one per half) run, per chunk,
+//   [U^T ->] Delta^T = U^T - X0^T W^T (three-term split) | X^T += Delta~^T K.
+// 19 warps: 0 TMA, 1 issuer for M, 2 issuer for S, 3-18 conversions.
+
+constexpr int kPairThreads = 608;
+struct PairSmem {
+    static constexpr int K = 0, V = 2 * kBox, Tiles = 4 * kBox;          // per stage
+    static constexpr int TileBytes = hypic::Rec<false>::G * 4;           // -W^T and A diag(beta) tiles
+    static constexpr int Stage = Tiles + TileBytes;
+    static constexpr int X0lo = kNS * Stage;                             // per half: 2 k halves x 16 KB
+    static constexpr int Ctl = X0lo + 2 * 32768;
+};
+// TMEM, per half x at 256 x: X^T (fp32, 128 columns), X0^T hi (bf16 pairs, 64),
+// Delta^T accumulator then Delta~^T hi / lo in place (64)
+__device__ __forceinline__ uint32_t kPX(int x) { return (uint32_t)x * 256u; }
+__device__ __forceinline__ uint32_t kPXh(int x) { return (uint32_t)x * 256u + 128u; }
+__device__ __forceinline__ uint32_t kPD(int x) { return (uint32_t)x * 256u + 192u; }
+
+struct PairCtl {
+    uint64_t full[kNS], empty[kNS];
+    uint64_t xop_ready[2][2];   // [half][k half] the half's X0 operand is in place
+    uint64_t dt_ready[2];       // the half's Delta~ is in place
+    uint64_t d_done[2];         // the half's Delta products are done
+    uint64_t x_done[2];         // the half's update is done
+    uint64_t drain[2];
+    float gates[kNS][hypic::Rec<false>::GateFloats];   // b_C / b, log b_C, b_C of the staged chunk
+    float redmax[16];
+    uint32_t tmem;
+    int abort;
+};
+constexpr int pair_smem() { return PairSmem::Ctl + (int)sizeof(PairCtl) + 1024; }
+static_assert(pair_smem() <= 232448, "fits in one SM's shared memory");
+static_assert(PairSmem::Stage % 1024 == 0 && PairSmem::Tiles % 1024 == 0 && PairSmem::X0lo % 1024 == 0,
+              "operand tiles 1024-byte aligned");
+static_assert((hypic::Rec<false>::GateFloats * 4) % 16 == 0, "gate copy in 16-byte units");
+
+// max over the 16 conversion warps (named barrier 2)
+__device__ __forceinline__ float pair_max(float mx, PairCtl *ctl, int sw, int lane) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (lane == 0) ctl->redmax[sw] = mx;
+    bar_sync(2, kState);
+    mx = 0.f;
+#pragma unroll
+    for (int w = 0; w < 16; ++w) mx = fmaxf(mx, ctl->redmax[w]);
+    bar_sync(2, kState);
+    return mx;
+}
+
+// X0 operand of one half: this thread's 2 x 16 rows k of its column m of X, times
+// `mult`, split into bf16 hi (TMEM, A operand) and lo (shared memory, K-major
+// row m, 128-byte swizzle); X rewritten times `sc` when `rewrite`; each k half
+// announced as soon as it is in place
+__device__ __forceinline__ void pair_x0(uint32_t tx, uint32_t txh, uint8_t *lo_tile, int m, int cg, float mult,
+                                       float sc, bool rewrite, uint64_t *ready, int lane) {
+    const uint64_t mult2 = pk2(mult, mult);
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+        uint32_t r[16], hi[8], lo[8];
+        tmem_ld16(tx + (uint32_t)(p * 64), r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            float x0, x1;
+            upk2(mul2(mult2, pk2(__uint_as_float(r[2 * q]), __uint_as_float(r[2 * q + 1]))), x0, x1);
+            split_pair(x0, x1, hi[q], lo[q]);
+        }
+        tmem_st8(txh + (uint32_t)(p * 32), hi);
+        uint8_t *row = lo_tile + p * 16384 + m * 128;
+        const int c0 = 2 * cg;   // this thread's two 16-byte groups of the row
+        *reinterpret_cast<uint4 *>(row + ((c0 ^ (m & 7)) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        *reinterpret_cast<uint4 *>(row + (((c0 + 1) ^ (m & 7)) << 4)) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+        if (rewrite) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(sc * __uint_as_float(r[i]));
+            tmem_st16(tx + (uint32_t)(p * 64), r);
+        }
+        tmem_wait_st();
+        fence_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ready[p]);
+    }
+}
+
+// Delta~^T = fD Delta^T diag(b_C / b) in place (this thread's 16 tokens), bf16 hi / lo
+__device__ __forceinline__ void pair_dt(uint32_t tacc, float fD, const float *gw, int cg, int lane,
+                                        uint64_t *ready) {
+    uint32_t r[16], hi[8], lo[8];
+    tmem_ld16(tacc, r);
+    const float4 *g4 = reinterpret_cast<const float4 *>(gw + cg * 16);
+    float sc[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float4 gv = g4[i];
+        sc[4 * i] = fD * gv.x;
+        sc[4 * i + 1] = fD * gv.y;
+        sc[4 * i + 2] = fD * gv.z;
+        sc[4 * i + 3] = fD * gv.w;
+    }
+    tmem_wait_ld();
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        float x0, x1;
+        upk2(mul2(pk2(sc[2 * q], sc[2 * q + 1]), pk2(__uint_as_float(r[2 * q]), __uint_as_float(r[2 * q + 1]))), x0,
+             x1);
+        split_pair(x0, x1, hi[q], lo[q]);
+    }
+    tmem_st8(tacc, hi);
+    tmem_st8(tacc + 8u, lo);
+    tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(ready);
+}
+
+// Scale bookkeeping of one half for one chunk (as the two-CTA form).  Transition
+// (h = 0): M_true = exp(lam_d + lam_exp ln2) M_stored, each chunk stores T_chunk M /
+// b_C; state (h = 1): S_true = exp(ls) S_stored.  The update only accumulates; X
+// is rewritten to renormalise (M every 8 chunks, S when ls < -20) or on a chunk
+// whose decay is below e^-40 (exact write-back form).
+struct HalfScale {
+    float g, wscale, fP, fD;
+    bool renorm, slow;
+};
+
+__device__ __forceinline__ HalfScale pair_scale(int h, int j, const float *gates, float &ls, double &lam_d,
+                                                bool writer) {
+    using R = Rec<false>;
+    HalfScale z;
+    const float LC = gates[R::LC - R::G];
+    z.slow = LC < -40.f;
+    z.renorm = z.slow || (h == 0 ? (j % 8 == 0) : (ls < -20.f));
+    z.g = 1.f;
+    z.wscale = 1.f;
+    if (h == 0) {
+        z.wscale = z.slow ? gates[R::BC - R::G] : 1.f;
+        z.fP = 1.f;
+        z.fD = z.slow ? 1.f : expf(-LC);
+        if (!z.slow && writer) lam_d += (double)LC;
+    } else if (z.slow) {
+        z.g = expf(ls);
+        z.wscale = gates[R::BC - R::G];
+        z.fP = 1.f;
+        z.fD = 1.f;
+        ls = 0.f;
+    } else {
+        if (z.renorm) {
+            const int q = (int)rintf(ls * 1.44269504088896341f);
+            z.g = ldexpf(1.f, q);
+            ls -= (float)q * 0.69314718055994531f;
+        }
+        z.fP = expf(ls);
+        z.fD = expf(-(ls + LC));
+        ls += LC;
+    }
+    return z;
+}
+
+__global__ void __launch_bounds__(kPairThreads, 1)
+    dense_pair_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                      const ScanArgs a, int64_t slots) {
+    using R = Rec<false>;
+    using SM = PairSmem;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_align1024(smem_raw);
+    PairCtl *ctl = reinterpret_cast<PairCtl *>(smem + SM::Ctl);
+    volatile int *abortp = &ctl->abort;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // chains in the order of their segments, longest first (all layers and heads of
+    // a segment together), so that the last wave holds the shortest chains
+    const int unit = blockIdx.x;
+    const int rank = unit / (a.H * a.n_layers);
+    const int l = (unit / a.H) % a.n_layers;
+    const int h = unit % a.H;
+    const int seg = a.order ? a.order[rank] : rank;
+    int64_t t0 = a.seg_offsets[seg], t1 = a.seg_offsets[seg + 1];
+    const bool bad = !(t0 >= 0 && t0 <= t1 && t1 <= a.N);
+    if (bad) t0 = t1 = 0;
+    const int nc = (int)((t1 - t0 + kC - 1) / kC);
+    const int64_t row0 = (int64_t)l * a.N + t0;
+    const float *recs = a.ws + (((int64_t)l * a.H + h) * slots + seg + t0 / kC) * R::Floats;
+
+    if (threadIdx.x == 0) {
+        if (bad) flag_index_error(a.d_err);
+        for (int s = 0; s < kNS; ++s) {
+            mbar_init(&ctl->full[s], 1);
+            mbar_init(&ctl->empty[s], 2);   // both issuers' updates read the stage last
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&ctl->xop_ready[x][0], kState / 32);
+            mbar_init(&ctl->xop_ready[x][1], kState / 32);
+            mbar_init(&ctl->dt_ready[x], kState / 32);
+            mbar_init(&ctl->d_done[x], 1);
+            mbar_init(&ctl->x_done[x], 1);
+            mbar_init(&ctl->drain[x], 1);
+        }
+        ctl->abort = 0;
+        mbar_fence_init();
+        tma_prefetch(&tm_k);
+        tma_prefetch(&tm_v);
+    }
+    if (warp == 0) tmem_alloc(&ctl->tmem, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem;
+
+    constexpr uint32_t id_wu = idesc_bf16_f32(128, 64, true, false);    // V^T (MN-major) x A tiles
+    constexpr uint32_t id_d = idesc_bf16_f32(128, 64, false, true);     // X0^T (K-major) x W^T (MN-major)
+    constexpr uint32_t id_x = idesc_bf16_f32(128, 128, false, true);    // Delta~^T (TMEM) x K (MN-major)
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int issued = 0;
+            for (int j = 0; j < nc; ++j) {
+                const int s = j % kNS;
+                if (!wait_or_abort(&ctl->empty[s], ((uint32_t)(j / kNS) & 1u) ^ 1u, abortp)) break;
+                uint8_t *st = smem + s * SM::Stage;
+                const int row = (int)(row0 + (int64_t)j * kC);
+                const float *rj = recs + (int64_t)j * R::Floats;
+                mbar_expect_tx(&ctl->full[s], (uint32_t)(4 * kBox + SM::TileBytes + R::GateFloats * 4));
+                tma_load_3d(st + SM::K, &tm_k, &ctl->full[s], 0, h, row);
+                tma_load_3d(st + SM::K + kBox, &tm_k, &ctl->full[s], 64, h, row);
+                tma_load_3d(st + SM::V, &tm_v, &ctl->full[s], 0, h, row);
+                tma_load_3d(st + SM::V + kBox, &tm_v, &ctl->full[s], 64, h, row);
+                bulk_load(st + SM::Tiles, rj, (uint32_t)SM::TileBytes, &ctl->full[s]);
+                bulk_load(ctl->gates[s], rj + R::G, (uint32_t)(R::GateFloats * 4), &ctl->full[s]);
+                issued = j + 1;
+            }
+            if (*abortp)
+                for (int j = issued - kNS < 0 ? 0 : issued - kNS; j < issued; ++j)
+                    mbar_wait(&ctl->full[j % kNS], (uint32_t)(j / kNS) & 1u);
+        }
+    } else if (warp <= 2) {
+        // ------------------------------------------------------------ MMA issuers: warp 1 the
+        // transition half, warp 2 the state half
+        if (lane == 0) {
+            const int x = warp - 1;
+            const uint32_t dacc = tmem + kPD(x);
+            const uint32_t lo_t = smem_addr(smem + SM::X0lo + x * 32768);
+            for (int j = 0; j < nc; ++j) {
+                const int s = j % kNS;
+                const uint32_t par = (uint32_t)j & 1u;
+                const uint8_t *stg = smem + s * SM::Stage;
+                // the accumulator is free (the previous update has read Delta~), the chunk is in
+                if (j > 0 && !wait_or_abort(&ctl->x_done[x], par ^ 1u, abortp)) break;
+                if (!wait_or_abort(&ctl->full[s], (uint32_t)(j / kNS) & 1u, abortp)) break;
+                const uint32_t tb = smem_addr(stg + SM::Tiles);
+                // ---- U^T = V^T (A diag(beta))^T into the accumulator (state half), lo first
+                if (x == 1) {
+                    tc_fence_after();
+                    const uint32_t vb = smem_addr(stg + SM::V), ab = tb + (uint32_t)R::Ab * 4u;
+#pragma unroll
+                    for (int hl = 1; hl >= 0; --hl)
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)
+                            mma_f16(dacc, smem_desc_sw128(vb + (uint32_t)ks * 2048u, kBox, 1024),
+                                    smem_desc_sw128(ab + (uint32_t)hl * 8192u + (uint32_t)ks * 32u, 0, 1024), id_wu,
+                                    (hl == 0 || ks > 0) ? 1u : 0u);
+                }
+                // ---- Delta^T = U^T - X0^T W^T (three-term split), per k half: hi x lo and
+                // lo x hi first, then hi x hi (the accumulator rounds each instruction's sum)
+                const uint32_t wt = tb + (uint32_t)R::Wt * 4u;
+                bool ok = true;
+                for (int p = 0; p < 2 && ok; ++p) {
+                    ok = wait_or_abort(&ctl->xop_ready[x][p], par, abortp);
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kq = 0; kq < 4; ++kq) {
+                        const int ks = p * 4 + kq;
+                        const uint64_t bh = smem_desc_sw128(wt + (uint32_t)ks * 2048u, 16384, 1024);
+                        const uint64_t bl = smem_desc_sw128(wt + 16384u + (uint32_t)ks * 2048u, 16384, 1024);
+                        mma_f16_ta(dacc, tmem + kPXh(x) + (uint32_t)ks * 8u, bl, id_d, (x == 1 || ks > 0) ? 1u : 0u);
+                        mma_f16(dacc, smem_desc_sw128(lo_t + (uint32_t)p * 16384u + (uint32_t)kq * 32u, 0, 1024), bh,
+                                id_d, 1u);
+                    }
+#pragma unroll
+                    for (int kq = 0; kq < 4; ++kq) {
+                        const int ks = p * 4 + kq;
+                        mma_f16_ta(dacc, tmem + kPXh(x) + (uint32_t)ks * 8u,
+                                   smem_desc_sw128(wt + (uint32_t)ks * 2048u, 16384, 1024), id_d, 1u);
+                    }
+                }
+                if (!ok) break;
+                mma_commit(&ctl->d_done[x]);
+                // ---- X^T += Delta~^T K (K as the MN-major B operand: row t, channels contiguous)
+                if (!wait_or_abort(&ctl->dt_ready[x], par, abortp)) break;
+                tc_fence_after();
+                const uint32_t kb = smem_addr(stg + SM::K);
+#pragma unroll
+                for (int hl = 1; hl >= 0; --hl)
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_f16_ta(tmem + kPX(x), dacc + (uint32_t)ks * 16u + (uint32_t)hl * 8u,
+                                   smem_desc_sw128(kb + (uint32_t)ks * 2048u, kBox, 1024), id_x, 1u);
+                mma_commit(&ctl->x_done[x]);
+                mma_commit(&ctl->empty[s]);
+            }
+            if (*abortp) {   // drain: completes once this thread's MMAs are done
+                mma_commit(&ctl->drain[x]);
+                mbar_wait(&ctl->drain[x], 0);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ conversion warps
+        const int st = threadIdx.x - 96;            // 0..511
+        const int sw = warp - 3;                    // 0..15
+        const int cg = sw >> 2;                     // row group of this warp (16 rows k per k half)
+        const int quarter = warp & 3;               // TMEM lanes this warp may touch
+        const int m = quarter * 32 + lane;          // column of X = TMEM lane
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        int lam_exp = 0;
+        double lam_d = 0.0;
+        float ls = 0.f;
+
+        {   // initial X^T: identity (transition) and zero (state)
+            uint32_t r[16];
+#pragma unroll
+            for (int x = 0; x < 2; ++x)
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        r[i] = __float_as_uint((x == 0 && p * 64 + cg * 16 + i == m) ? 1.f : 0.f);
+                    tmem_st16(tmem + lane_off + kPX(x) + (uint32_t)(p * 64 + cg * 16), r);
+                }
+            tmem_wait_st();
+        }
+
+        bool alive = true;
+        for (int j = 0; j < nc && alive; ++j) {
+            const int s = j % kNS;
+            const uint32_t par = (uint32_t)j & 1u;
+            const float *gates = ctl->gates[s];
+            HalfScale z[2];
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+                // ---- X0 of this half: the chunk is in and the half's previous update is done
+                bool ok = wait_or_abort(&ctl->full[s], (uint32_t)(j / kNS) & 1u, abortp);
+                if (j > 0) ok = ok && wait_or_abort(&ctl->x_done[x], par ^ 1u, abortp);
+                if (!bar_and(2, kState, ok)) {
+                    alive = false;
+                    break;
+                }
+                tc_fence_after();
+                z[x] = pair_scale(x, j, gates, ls, lam_d, st == 0);
+                float g = z[x].g;
+                const uint32_t tx = tmem + lane_off + kPX(x) + (uint32_t)(cg * 16);
+                if (x == 0 && z[x].renorm) {   // the transition's power-of-two renormalisation
+                    float mx = 0.f;
+#pragma unroll
+                    for (int p = 0; p < 2; ++p) {
+                        uint32_t r[16];
+                        tmem_ld16(tx + (uint32_t)(p * 64), r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) mx = fmaxf(mx, fabsf(__uint_as_float(r[i])));
+                    }
+                    const int e = exponent_of(pair_max(mx, ctl, sw, lane));
+                    g = ldexpf(1.f, -e);
+                    lam_exp += e;
+                }
+                pair_x0(tx, tmem + lane_off + kPXh(x) + (uint32_t)(cg * 8), smem + SM::X0lo + x * 32768, m, cg,
+                        g * z[x].fP, g * z[x].wscale, z[x].renorm, ctl->xop_ready[x], lane);
+            }
+            if (!alive) break;
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+                // ---- Delta~ of this half, once its Delta products are done
+                if (!bar_and(2, kState, wait_or_abort(&ctl->d_done[x], par, abortp))) {
+                    alive = false;
+                    break;
+                }
+                tc_fence_after();
+                pair_dt(tmem + lane_off + kPD(x) + (uint32_t)(cg * 16), z[x].fD, gates + (R::Gw - R::G), cg, lane,
+                        &ctl->dt_ready[x]);
+            }
+        }
+
+        // ------------------------------------------------------------ epilogue
+        bool ok = alive;
+        if (ok && nc > 0)
+            ok = wait_or_abort(&ctl->x_done[0], (uint32_t)(nc - 1) & 1u, abortp) &&
+                 wait_or_abort(&ctl->x_done[1], (uint32_t)(nc - 1) & 1u, abortp);
+        if (bar_and(2, kState, ok)) {
+            tc_fence_after();
+            const int64_t u_out = ((int64_t)l * a.n_seg + seg) * a.H + h;
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+                const uint32_t tx = tmem + lane_off + kPX(x) + (uint32_t)(cg * 16);
+                uint32_t r[2][16];
+                tmem_ld16(tx, r[0]);
+                tmem_ld16(tx + 64u, r[1]);
+                tmem_wait_ld();
+                float scale;
+                if (x == 0) {
+                    float mx = 0.f;
+#pragma unroll
+                    for (int p = 0; p < 2; ++p)
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) mx = fmaxf(mx, fabsf(__uint_as_float(r[p][i])));
+                    const int e = exponent_of(pair_max(mx, ctl, sw, lane));
+                    scale = ldexpf(1.f, -e);
+                    lam_exp += e;
+                    if (st == 0) a.lam_out[u_out] = (float)(lam_d + (double)lam_exp * 0.69314718055994530942);
+                } else {
+                    scale = expf(ls);
+                }
+                float *out = (x == 0 ? a.M_out : a.S_out) + u_out * kD * kD;
+#pragma unroll
+                for (int p = 0; p < 2; ++p)
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        out[(int64_t)(p * 64 + cg * 16 + i) * kD + m] = scale * __uint_as_float(r[p][i]);
+            }
+        } else {
+            *abortp = 1;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0 && *abortp && a.d_err) atomicExch(a.d_err, (int)HYPIC_ETIMEOUT);
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
 // ================================================================ longest first
 
 constexpr int kLptMax = 4096;   // segments ranked; beyond this the given order is kept
@@ -1035,13 +1621,21 @@ cudaError_t launch_two_pass(const ScanArgs &a0, cudaStream_t s) {
     const int64_t slots = n_slots(a.N, a.n_seg);
     cudaError_t e = cudaFuncSetAttribute(dense_prep_kernel<O>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(dense_state_kernel<O>, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem<O>());
-    if (e != cudaSuccess) return e;
     dense_prep_kernel<O><<<dim3((unsigned)(slots * a.H), (unsigned)a.n_layers), kPThreads, kPSmem, s>>>(mk, mq, a,
                                                                                                      slots);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    dense_state_kernel<O><<<(unsigned)(2 * units), state_threads<O>(), state_smem<O>(), s>>>(mk, mv, mq, a, slots);
+    if (O) {
+        e = cudaFuncSetAttribute(dense_state_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 state_smem<true>());
+        if (e != cudaSuccess) return e;
+        dense_state_kernel<true><<<(unsigned)(2 * units), state_threads<true>(), state_smem<true>(), s>>>(mk, mv, mq,
+                                                                                                      a, slots);
+    } else {
+        e = cudaFuncSetAttribute(dense_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, pair_smem());
+        if (e != cudaSuccess) return e;
+        dense_pair_kernel<<<(unsigned)units, kPairThreads, pair_smem(), s>>>(mk, mv, a, slots);
+    }
     return cudaGetLastError();
 }
 

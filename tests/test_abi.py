@@ -92,7 +92,7 @@ def scan_ws(lib, fam=2, dtype=0, L=1, S=2, N=64, H=2, dk=128, dv=128, ws=0x40000
 
 
 def test_workspace_size_and_checks(lib):
-    """The two-pass dense scan: one 33568-byte record (50192 with o_t) per
+    """The two-pass dense scan: one 49424-byte record (50192 with o_t) per
     (layer, head, chunk slot), n_seg + N / 64 slots, then the segments' order
     (int32 each), both 256-byte aligned; the balanced
     diagonal scan: a fixed 2 x 512 partial slots; other options take none."""
@@ -102,8 +102,8 @@ def test_workspace_size_and_checks(lib):
     def dense(L, n_seg, N, H, rec):   # records, then the segment order (int32 each)
         return up(L * H * (n_seg + N // 64) * rec) + up(4 * n_seg)
 
-    assert ws(2, 0, 30, 1, 2048, 32, 128, 128, 0) == dense(30, 1, 2048, 32, 33568)
-    assert ws(2, 0, 1, 3, 200, 2, 128, 128, 0) == dense(1, 3, 200, 2, 33568)
+    assert ws(2, 0, 30, 1, 2048, 32, 128, 128, 0) == dense(30, 1, 2048, 32, 49424)
+    assert ws(2, 0, 1, 3, 200, 2, 128, 128, 0) == dense(1, 3, 200, 2, 49424)
     assert ws(2, 0, 1, 1, 2048, 2, 128, 128, 1) == dense(1, 1, 2048, 2, 50192)   # with o_t: Gq tiles and b_t too
     assert ws(2, 1, 1, 1, 2048, 2, 128, 128, 0) == 0     # fp32 inputs
     assert ws(3, 0, 1, 1, 2048, 2, 128, 128, 0) == 0     # KDA: the token-by-token kernel

@@ -57,7 +57,7 @@ def test_static_scratch_equals_workspace_form_on_two_calls_in_a_row():
 def test_static_scratch_refuses_a_problem_beyond_its_size():
     import torch
     import linear_attention_state_gated_gb300 as hy
-    Lyr, H, L = 1, 32, 8192           # 32 x 129 records of 33568 bytes: 138.6 MB > 64 MiB
+    Lyr, H, L = 1, 32, 8192           # 32 x 129 records of 49424 bytes: 204.0 MB > 64 MiB
     k, v, a, b, offs = _inputs([L], Lyr, H, seed=32)
     out = _nan_out(Lyr, 1, H)
     with pytest.raises(hy.HypicError) as e:
