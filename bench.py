@@ -706,6 +706,49 @@ def run_chain(args):
     return res
 
 
+def run_tree(args):
+    """Few units, long chains: 1 layer x 4 heads, one request folding 64 pool entries
+    in order, per family; the plain chain (one CTA per (request, layer, head)) against
+    the two-level tree of hypic_compose_chain_ws.  Pool pairs drawn on the device
+    (decaying operators); the 16-32 MB pool stays in L2 between launches."""
+    import torch
+    import linear_attention_state_gated_gb300 as hy
+    dev = torch.device("cuda")
+    g = torch.Generator(device=dev)
+    g.manual_seed(5)
+    P, Lyr, H, d, n = 64, 1, 4, 128, 64
+    res = {"workload": f"1 request x {Lyr} layer x {H} heads x d={d}, chains of {n} pool entries"}
+    clen = torch.tensor([n], dtype=torch.int32, device=dev)
+    idx = torch.arange(n, dtype=torch.int32, device=dev)[None]
+    for fam, name in ((0, "scalar"), (1, "diag"), (2, "dense")):
+        lam = -0.05 * torch.rand((P, Lyr, H, d) if fam == 1 else (P, Lyr, H), generator=g, device=dev)
+        S = torch.randn((P, Lyr, H, d, d), generator=g, device=dev)
+        M = None
+        if fam == 2:
+            M = torch.randn((P, Lyr, H, d, d), generator=g, device=dev) / d ** 0.5
+            M = M / M.abs().amax(dim=(-2, -1), keepdim=True)
+        ws = torch.empty(max(1, hy.compose_chain_workspace_bytes(fam, 1, Lyr, H, d, d, n)), dtype=torch.uint8,
+                         device=dev)
+        out = torch.empty((1, Lyr, H, d, d), device=dev)
+        times = {}
+        for mode in ("chain", "tree"):
+            kw = {"workspace": ws} if mode == "tree" else {}
+            for _ in range(3):
+                hy.compose_chain(fam, clen, idx, lam, S, pool_M=M, S_out=out, **kw)
+            torch.cuda.synchronize()
+            reps = 20
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                hy.compose_chain(fam, clen, idx, lam, S, pool_M=M, S_out=out, **kw)
+            e1.record()
+            torch.cuda.synchronize()
+            times[mode] = e0.elapsed_time(e1) / reps
+        res[name] = {"chain_ms": times["chain"], "tree_ms": times["tree"], "speedup": times["chain"] / times["tree"],
+                     "composes_per_s_tree": n * Lyr / (times["tree"] / 1e3)}
+    return res
+
+
 def run_scan_sd(args, L):
     """Scalar and diagonal scans of 8 segments x L tokens x 32 heads (the headline's
     kernels at a shorter length), each family timed alone."""
@@ -904,8 +947,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="hypic", choices=["hypic", "reference"])
     ap.add_argument("--L", type=int, default=8192)
-    ap.add_argument("--rows", default="sd,dense,kda,compose,seam,prefix,chain,mix",
-                    help="extra rows: sd,dense,kda,compose,seam,prefix,chain,mix or none")
+    ap.add_argument("--rows", default="sd,dense,kda,compose,seam,prefix,chain,tree,mix",
+                    help="extra rows: sd,dense,kda,compose,seam,prefix,chain,tree,mix or none")
     ap.add_argument("--dense-lengths", default="512,2048,8192,32768",
                     help="dense rows: segment lengths of the 30-layer stack")
     ap.add_argument("--sd-lengths", default="512,2048",
@@ -952,6 +995,8 @@ def main():
         rows["prefix"] = run_prefix(args)
     if solo and "chain" in args.rows:
         rows["rag_chain"] = run_chain(args)
+    if solo and "tree" in args.rows:
+        rows["tree"] = run_tree(args)
     if solo and "mix" in args.rows:
         rows["long_mix"] = run_long_mix(args)
     if rank != 0:

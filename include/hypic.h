@@ -231,6 +231,33 @@ int hypic_compose_chain(int fam, int n_req, int n_layers, int n_heads, int d_k, 
                         int *d_err, void *cuda_stream);
 
 /*
+ * hypic_compose_chain_ws -- hypic_compose_chain with caller-owned device scratch,
+ * used when few (request, layer, head) units carry long chains (fewer units than
+ * twice the SM count, chains of 8 or more entries): a chain then runs on few SMs
+ * one entry after another.  Because T(C1.C2) = T(C2) T(C1) (xix.ai/fr,
+ * linear-layer paragraph), consecutive entries can be folded into one cached pair
+ * first: the call folds groups of consecutive entries of every chain in parallel
+ * (composed prefixes, as hypic_compose_prefix), then each chain's group pairs in
+ * order into S_init -- a two-level tree.  Results equal hypic_compose_chain's up
+ * to rounding (the fp32 additions are regrouped).  Other shapes run exactly as
+ * hypic_compose_chain and need no scratch.
+ *   Arguments as hypic_compose_chain, plus
+ *   workspace        device scratch, 256-byte aligned, at least
+ *                    hypic_compose_chain_workspace_bytes(...) bytes (may be NULL when
+ *                    that is 0); it may overlap no other argument.  Caller-owned;
+ *                    its contents need not be initialised and are garbage after.
+ *   workspace_bytes  its size; too small -> HYPIC_EINVAL before any launch.
+ */
+int64_t hypic_compose_chain_workspace_bytes(int fam, int n_req, int n_layers, int n_heads,
+                                            int d_k, int d_v, int max_chain);
+int hypic_compose_chain_ws(int fam, int n_req, int n_layers, int n_heads, int d_k, int d_v,
+                           int max_chain, const int32_t *chain_len, const int32_t *seg_idx,
+                           int pool_size, const float *pool_lam, const float *pool_M,
+                           const float *pool_S, const float *S_init, float *S_out,
+                           void *workspace, int64_t workspace_bytes, int *d_err,
+                           void *cuda_stream);
+
+/*
  * hypic_compose_prefix -- a composed prefix: for every request r, layer l and
  * head h, the cached pair of the concatenation of the pool entries
  * seg_idx[r, 0 .. chain_len[r]-1] (in that order):

@@ -34,6 +34,7 @@ STATUS = {0: "HYPIC_OK", -1: "HYPIC_EINVAL", -2: "HYPIC_EUNSUPPORTED", -3: "HYPI
           -4: "HYPIC_ECUDA", -5: "HYPIC_EINDEX", -6: "HYPIC_ETIMEOUT"}
 
 __all__ = ["segment_scan", "segment_scan_workspace_bytes", "segment_scan_static", "compose", "compose_chain",
+           "compose_chain_workspace_bytes",
            "compose_prefix", "seam_compose", "selftest_wait", "status_string", "library", "use_library",
            "HypicError", "SCALAR", "DIAG", "DENSE", "KDA"]
 
@@ -60,6 +61,9 @@ SIGNATURES = {
     "hypic_compose": (_I32, [_I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "hypic_compose_chain": (_I32, [_I32, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _I32,
                                    _P, _P, _P, _P, _P, _P, _P]),
+    "hypic_compose_chain_workspace_bytes": (_I64, [_I32, _I32, _I32, _I32, _I32, _I32, _I32]),
+    "hypic_compose_chain_ws": (_I32, [_I32, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _I32,
+                                      _P, _P, _P, _P, _P, _P, _I64, _P, _P]),
     "hypic_compose_prefix": (_I32, [_I32, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _I32,
                                     _P, _P, _P, _P, _P, _P, _P, _P]),
     "hypic_seam_compose": (_I32, [_I32, _I32, _I32, _I32, _I32, _I32, _I32,
@@ -341,12 +345,23 @@ def seam_compose(family, k, v, alpha, lam, S_C, S_prev=None, M=None, beta=None, 
     return res
 
 
+def compose_chain_workspace_bytes(family, n_req, n_layers, n_heads, d_k, d_v, max_chain):
+    """Scratch bytes hypic_compose_chain_ws needs for this shape (0: no tree)."""
+    n = library().hypic_compose_chain_workspace_bytes(_fam(family), n_req, n_layers, n_heads, d_k, d_v,
+                                                      max_chain)
+    if n < 0:
+        raise HypicError("hypic_compose_chain_workspace_bytes", int(n))
+    return int(n)
+
+
 def compose_chain(family, chain_len, seg_idx, pool_lam, pool_S, pool_M=None, S_init=None,
-                  S_out=None, d_err=None, stream=None):
+                  S_out=None, d_err=None, stream=None, workspace=None):
     """Fold pool entries seg_idx[r, :chain_len[r]] in order: S <- T_p S + S_p.
 
     pool_lam [P,Lyr,H] or [P,Lyr,H,dk], pool_M [P,Lyr,H,dk,dk] (dense, kda),
     pool_S [P,Lyr,H,dk,dv], S_init [R,Lyr,H,dk,dv] or None.  Returns S [R,Lyr,H,dk,dv].
+    ``workspace`` (a uint8 CUDA tensor, or "auto" to allocate one) selects
+    hypic_compose_chain_ws: few long chains fold as a two-level tree.
     """
     fam = _fam(family)
     chain_len = _dev(chain_len, "chain_len", torch.int32)
@@ -360,11 +375,22 @@ def compose_chain(family, chain_len, seg_idx, pool_lam, pool_S, pool_M=None, S_i
     max_chain = seg_idx.shape[1] if seg_idx.dim() == 2 else 0
     if S_out is None:
         S_out = torch.empty((R, Lyr, H, dk, dv), dtype=torch.float32, device=pool_S.device)
-    st = library().hypic_compose_chain(fam, R, Lyr, H, dk, dv, max_chain, _ptr(chain_len),
-                                       _ptr(seg_idx), P, _ptr(pool_lam), _ptr(pool_M),
-                                       _ptr(pool_S), _ptr(S_init), _ptr(S_out), _ptr(d_err),
-                                       _stream(stream))
-    _check("hypic_compose_chain", st)
+    if workspace is None:
+        st = library().hypic_compose_chain(fam, R, Lyr, H, dk, dv, max_chain, _ptr(chain_len),
+                                           _ptr(seg_idx), P, _ptr(pool_lam), _ptr(pool_M),
+                                           _ptr(pool_S), _ptr(S_init), _ptr(S_out), _ptr(d_err),
+                                           _stream(stream))
+        _check("hypic_compose_chain", st)
+        return S_out
+    if isinstance(workspace, str):
+        need = compose_chain_workspace_bytes(fam, R, Lyr, H, dk, dv, max_chain)
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=pool_S.device)
+    workspace = _dev(workspace, "workspace", torch.uint8)
+    st = library().hypic_compose_chain_ws(fam, R, Lyr, H, dk, dv, max_chain, _ptr(chain_len),
+                                          _ptr(seg_idx), P, _ptr(pool_lam), _ptr(pool_M), _ptr(pool_S),
+                                          _ptr(S_init), _ptr(S_out), _ptr(workspace), workspace.numel(),
+                                          _ptr(d_err), _stream(stream))
+    _check("hypic_compose_chain_ws", st)
     return S_out
 
 

@@ -350,17 +350,26 @@ int hypic_seam_compose(int fam, int in_dtype, int n, int w, int n_heads, int d_k
     return from_cuda(hypic::launch_seam_compose(a, static_cast<cudaStream_t>(cuda_stream)));
 }
 
-int hypic_compose_chain(int fam, int n_req, int n_layers, int n_heads, int d_k, int d_v,
-                        int max_chain, const int32_t *chain_len, const int32_t *seg_idx,
-                        int pool_size, const float *pool_lam, const float *pool_M,
-                        const float *pool_S, const float *S_init, float *S_out, int *d_err,
-                        void *cuda_stream) {
+}  // extern "C"
+
+namespace {
+
+// Host checks of hypic_compose_chain(_ws); fills `a`.  Returns HYPIC_OK and sets
+// *nothing_to_do when there is no work.
+int chain_args(int fam, int n_req, int n_layers, int n_heads, int d_k, int d_v, int max_chain,
+               const int32_t *chain_len, const int32_t *seg_idx, int pool_size, const float *pool_lam,
+               const float *pool_M, const float *pool_S, const float *S_init, float *S_out, int *d_err,
+               hypic::ChainArgs &a, bool &nothing_to_do) {
+    nothing_to_do = false;
     if (!family_ok(fam)) return HYPIC_EINVAL;
     if (n_req < 0 || n_layers < 0 || n_heads <= 0 || max_chain < 0 || pool_size < 0)
         return HYPIC_EINVAL;
     if (!head_size_ok(d_k) || !head_size_ok(d_v)) return HYPIC_EUNSUPPORTED;
     if ((int64_t)n_req * n_layers * n_heads > INT32_MAX) return HYPIC_EUNSUPPORTED;
-    if (n_req == 0 || n_layers == 0) return HYPIC_OK;
+    if (n_req == 0 || n_layers == 0) {
+        nothing_to_do = true;
+        return HYPIC_OK;
+    }
     if (!chain_len || !S_out) return HYPIC_EINVAL;
     if (max_chain > 0 && (!seg_idx || pool_size == 0 || !pool_lam || !pool_S)) return HYPIC_EINVAL;
     if (max_chain > 0 && has_m(fam) != (pool_M != nullptr)) return HYPIC_EINVAL;
@@ -378,8 +387,8 @@ int hypic_compose_chain(int fam, int n_req, int n_layers, int n_heads, int d_k, 
         const int nl = fam == HYPIC_DIAG ? d_k : 1;
         auto overlaps = [](const void *x, size_t xb, const void *y, size_t yb) {
             if (!x || !y) return false;
-            const char *a = static_cast<const char *>(x), *b = static_cast<const char *>(y);
-            return a < b + yb && b < a + xb;
+            const char *p = static_cast<const char *>(x), *q = static_cast<const char *>(y);
+            return p < q + yb && q < p + xb;
         };
         const size_t sb = (size_t)units * d_k * d_v * 4;
         if (overlaps(S_out, sb, pool_S, (size_t)entries * d_k * d_v * 4) ||
@@ -389,7 +398,6 @@ int hypic_compose_chain(int fam, int n_req, int n_layers, int n_heads, int d_k, 
             return HYPIC_EINVAL;
     }
 
-    hypic::ChainArgs a;
     a.fam = compose_family(fam);
     a.R = n_req;
     a.n_layers = n_layers;
@@ -406,7 +414,73 @@ int hypic_compose_chain(int fam, int n_req, int n_layers, int n_heads, int d_k, 
     a.S_init = S_init;
     a.S_out = S_out;
     a.d_err = d_err;
+    return HYPIC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int hypic_compose_chain(int fam, int n_req, int n_layers, int n_heads, int d_k, int d_v,
+                        int max_chain, const int32_t *chain_len, const int32_t *seg_idx,
+                        int pool_size, const float *pool_lam, const float *pool_M,
+                        const float *pool_S, const float *S_init, float *S_out, int *d_err,
+                        void *cuda_stream) {
+    hypic::ChainArgs a;
+    bool none;
+    const int rc = chain_args(fam, n_req, n_layers, n_heads, d_k, d_v, max_chain, chain_len, seg_idx, pool_size,
+                              pool_lam, pool_M, pool_S, S_init, S_out, d_err, a, none);
+    if (rc != HYPIC_OK || none) return rc;
     return from_cuda(hypic::launch_compose_chain(a, static_cast<cudaStream_t>(cuda_stream)));
+}
+
+int64_t hypic_compose_chain_workspace_bytes(int fam, int n_req, int n_layers, int n_heads, int d_k, int d_v,
+                                            int max_chain) {
+    if (!family_ok(fam) || n_req < 0 || n_layers < 0 || n_heads <= 0 || max_chain < 0) return HYPIC_EINVAL;
+    if (!head_size_ok(d_k) || !head_size_ok(d_v)) return HYPIC_EUNSUPPORTED;
+    if (n_req == 0 || n_layers == 0) return 0;
+    hypic::ChainArgs a{};
+    a.fam = compose_family(fam);
+    a.R = n_req;
+    a.n_layers = n_layers;
+    a.H = n_heads;
+    a.dk = d_k;
+    a.dv = d_v;
+    a.max_chain = max_chain;
+    return hypic::tree_bytes(a, hypic::tree_group_size(a));
+}
+
+int hypic_compose_chain_ws(int fam, int n_req, int n_layers, int n_heads, int d_k, int d_v, int max_chain,
+                           const int32_t *chain_len, const int32_t *seg_idx, int pool_size,
+                           const float *pool_lam, const float *pool_M, const float *pool_S,
+                           const float *S_init, float *S_out, void *workspace, int64_t workspace_bytes,
+                           int *d_err, void *cuda_stream) {
+    hypic::ChainArgs a;
+    bool none;
+    const int rc = chain_args(fam, n_req, n_layers, n_heads, d_k, d_v, max_chain, chain_len, seg_idx, pool_size,
+                              pool_lam, pool_M, pool_S, S_init, S_out, d_err, a, none);
+    if (rc != HYPIC_OK || none) return rc;
+    if (workspace_bytes < 0) return HYPIC_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    const int gs = hypic::tree_group_size(a);
+    if (gs == 0) return from_cuda(hypic::launch_compose_chain(a, s));
+    const int64_t need = hypic::tree_bytes(a, gs);
+    if (!workspace || workspace_bytes < need) return HYPIC_EINVAL;
+    if (!aligned(workspace, 256)) return HYPIC_EALIGN;
+    // the scratch may overlap neither the pool nor the states
+    const int64_t units = (int64_t)n_req * n_layers * n_heads;
+    const int64_t entries = (int64_t)pool_size * n_layers * n_heads;
+    const char *w = static_cast<const char *>(workspace);
+    auto hits = [&](const void *p, size_t b) {
+        const char *q = static_cast<const char *>(p);
+        return p && q < w + need && w < q + b;
+    };
+    if (hits(pool_S, (size_t)entries * d_k * d_v * 4) || hits(pool_M, (size_t)entries * d_k * d_k * 4) ||
+        hits(pool_lam, (size_t)entries * d_k * 4) || hits(S_out, (size_t)units * d_k * d_v * 4) ||
+        hits(S_init, (size_t)units * d_k * d_v * 4) || hits(chain_len, (size_t)n_req * 4) ||
+        hits(seg_idx, (size_t)n_req * max_chain * 4))
+        return HYPIC_EINVAL;
+    return from_cuda(hypic::launch_compose_chain_tree(a, gs, workspace, s));
 }
 
 int hypic_compose_prefix(int fam, int n_req, int n_layers, int n_heads, int d_k, int d_v, int max_chain,

@@ -199,34 +199,54 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: <= 96 registers pe
                     }
                     tc_fence_after();
                     const uint32_t abuf = tmem + kTa + (uint32_t)(g & 1) * 192u;
-                    // smallest terms first: the unit rounds each instruction's sum into the
-                    // fp32 accumulator, so the 2^-16-level products (hl, mm, lh) and then the
-                    // 2^-8-level ones (hm, mh) are summed while the accumulator is still
-                    // small, and only the eight hi x hi products round at full magnitude
+                    if (OP) {
+                        // operator chains: smallest terms first.  The unit rounds each
+                        // instruction's sum into the fp32 accumulator; nothing decays an
+                        // operator chain's early error, so the 2^-16-level products (hl, mm,
+                        // lh) and then the 2^-8-level ones (hm, mh) are summed while the
+                        // accumulator is still small and only the eight hi x hi products
+                        // round at full magnitude
 #pragma unroll 2
-                    for (int ks = 0; ks < 8; ++ks) {   // K = 128 in steps of 16 (two 8-row groups of B)
-                        const uint32_t off = (uint32_t)ks * 2048u;
-                        const uint64_t bh = smem_desc_sw128(b0 + off, 16384, 1024);
-                        const uint64_t bm = smem_desc_sw128(b0 + kBpart + off, 16384, 1024);
-                        const uint64_t bl = smem_desc_sw128(b0 + 2 * kBpart + off, 16384, 1024);
-                        const uint32_t ah = abuf + (uint32_t)ks * 8u, am = ah + 64u, al = ah + 128u;
-                        mma_f16_ta(dcol, ah, bl, idesc, ks > 0);
-                        mma_f16_ta(dcol, am, bm, idesc, 1u);
-                        mma_f16_ta(dcol, al, bh, idesc, 1u);
-                    }
+                        for (int ks = 0; ks < 8; ++ks) {   // K = 128 in steps of 16 (two 8-row groups of B)
+                            const uint32_t off = (uint32_t)ks * 2048u;
+                            const uint64_t bh = smem_desc_sw128(b0 + off, 16384, 1024);
+                            const uint64_t bm = smem_desc_sw128(b0 + kBpart + off, 16384, 1024);
+                            const uint64_t bl = smem_desc_sw128(b0 + 2 * kBpart + off, 16384, 1024);
+                            const uint32_t ah = abuf + (uint32_t)ks * 8u, am = ah + 64u, al = ah + 128u;
+                            mma_f16_ta(dcol, ah, bl, idesc, ks > 0);
+                            mma_f16_ta(dcol, am, bm, idesc, 1u);
+                            mma_f16_ta(dcol, al, bh, idesc, 1u);
+                        }
 #pragma unroll 2
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t off = (uint32_t)ks * 2048u;
-                        const uint64_t bh = smem_desc_sw128(b0 + off, 16384, 1024);
-                        const uint64_t bm = smem_desc_sw128(b0 + kBpart + off, 16384, 1024);
-                        const uint32_t ah = abuf + (uint32_t)ks * 8u, am = ah + 64u;
-                        mma_f16_ta(dcol, ah, bm, idesc, 1u);
-                        mma_f16_ta(dcol, am, bh, idesc, 1u);
-                    }
+                        for (int ks = 0; ks < 8; ++ks) {
+                            const uint32_t off = (uint32_t)ks * 2048u;
+                            const uint64_t bh = smem_desc_sw128(b0 + off, 16384, 1024);
+                            const uint64_t bm = smem_desc_sw128(b0 + kBpart + off, 16384, 1024);
+                            const uint32_t ah = abuf + (uint32_t)ks * 8u, am = ah + 64u;
+                            mma_f16_ta(dcol, ah, bm, idesc, 1u);
+                            mma_f16_ta(dcol, am, bh, idesc, 1u);
+                        }
 #pragma unroll 4
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint64_t bh = smem_desc_sw128(b0 + (uint32_t)ks * 2048u, 16384, 1024);
-                        mma_f16_ta(dcol, abuf + (uint32_t)ks * 8u, bh, idesc, 1u);
+                        for (int ks = 0; ks < 8; ++ks) {
+                            const uint64_t bh = smem_desc_sw128(b0 + (uint32_t)ks * 2048u, 16384, 1024);
+                            mma_f16_ta(dcol, abuf + (uint32_t)ks * 8u, bh, idesc, 1u);
+                        }
+                    } else {
+                        // state chains (each step decays the earlier error): per k-step
+#pragma unroll 2
+                        for (int ks = 0; ks < 8; ++ks) {
+                            const uint32_t off = (uint32_t)ks * 2048u;
+                            const uint64_t bh = smem_desc_sw128(b0 + off, 16384, 1024);
+                            const uint64_t bm = smem_desc_sw128(b0 + kBpart + off, 16384, 1024);
+                            const uint64_t bl = smem_desc_sw128(b0 + 2 * kBpart + off, 16384, 1024);
+                            const uint32_t ah = abuf + (uint32_t)ks * 8u, am = ah + 64u, al = ah + 128u;
+                            mma_f16_ta(dcol, ah, bh, idesc, ks > 0);
+                            mma_f16_ta(dcol, ah, bm, idesc, 1u);
+                            mma_f16_ta(dcol, am, bh, idesc, 1u);
+                            mma_f16_ta(dcol, ah, bl, idesc, 1u);
+                            mma_f16_ta(dcol, am, bm, idesc, 1u);
+                            mma_f16_ta(dcol, al, bh, idesc, 1u);
+                        }
                     }
                     mma_commit(&ctl->d_done[nh]);
                     mma_commit(&ctl->afree[g & 1]);

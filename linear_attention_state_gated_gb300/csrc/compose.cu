@@ -478,6 +478,129 @@ cudaError_t launch_compose_prefix(const ChainArgs &a0, float *lam_out, float *M_
     return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------- two-level tree
+//
+// With few (request, layer, head) units a chain runs on few SMs, one pool entry
+// after another.  The operator of a concatenation is the product of the operators,
+// T(C1.C2) = T(C2) T(C1), so any run of consecutive entries can first be folded into
+// one cached pair.  Level 1 folds groups of gs entries of every chain in parallel
+// (the composed-prefix kernels, one virtual request per (request, group)); level 2
+// folds each request's group pairs in order into S_init (the chain kernels).
+
+namespace {
+
+constexpr int kTreeMinChain = 8;   // shorter chains gain nothing from a second level
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess || n <= 0)
+        n = 148;
+    return n;
+}
+
+int64_t up256(int64_t b) { return (b + 255) / 256 * 256; }
+
+struct TreeLayout {
+    int G;                       // groups per request
+    int64_t lam, M, S, si1, cl1, si2, cl2, total;   // byte offsets
+};
+
+TreeLayout tree_layout(const ChainArgs &a, int gs) {
+    TreeLayout t{};
+    t.G = (a.max_chain + gs - 1) / gs;
+    const int64_t entries = (int64_t)a.R * t.G * a.n_layers * a.H;
+    const int nl = a.fam == HYPIC_DIAG ? a.dk : 1;
+    int64_t o = 0;
+    t.lam = o;
+    o += up256(entries * nl * 4);
+    t.M = o;
+    if (a.fam == HYPIC_DENSE) o += up256(entries * a.dk * a.dk * 4);
+    t.S = o;
+    o += up256(entries * a.dk * a.dv * 4);
+    t.si1 = o;
+    o += up256((int64_t)a.R * t.G * gs * 4);
+    t.cl1 = o;
+    o += up256((int64_t)a.R * t.G * 4);
+    t.si2 = o;
+    o += up256((int64_t)a.R * t.G * 4);
+    t.cl2 = o;
+    o += up256((int64_t)a.R * 4);
+    t.total = o;
+    return t;
+}
+
+// one thread per (request, group): the group's entries and length (level 1), the
+// request's group list and count (level 2); a chain length outside [0, max_chain]
+// is clamped and reported like the chain kernels do
+__global__ void tree_index_kernel(const ChainArgs a, int gs, int G, int32_t *si1, int32_t *cl1, int32_t *si2,
+                                  int32_t *cl2) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (int64_t)a.R * G) return;
+    const int r = (int)(i / G), g = (int)(i % G);
+    int n = a.chain_len[r];
+    if (n < 0 || n > a.max_chain) {
+        if (g == 0) flag_index_error(a.d_err);
+        n = n < 0 ? 0 : a.max_chain;
+    }
+    const int rem = n - g * gs;
+    cl1[i] = rem <= 0 ? 0 : (rem < gs ? rem : gs);
+    for (int j = 0; j < gs; ++j) {
+        const int c = g * gs + j;
+        si1[i * gs + j] = c < a.max_chain ? a.seg_idx[(int64_t)r * a.max_chain + c] : 0;
+    }
+    si2[i] = (int32_t)i;
+    if (g == 0) cl2[r] = (n + gs - 1) / gs;
+}
+
+}  // namespace
+
+int tree_group_size(const ChainArgs &a) {
+    const int64_t units = (int64_t)a.R * a.n_layers * a.H;
+    const int sms = sm_count();
+    if (a.max_chain < kTreeMinChain || units >= 2 * (int64_t)sms) return 0;
+    // about four CTAs per SM in level 1, at least 4 entries a group
+    const int64_t want_groups = (4 * (int64_t)sms + units - 1) / units;
+    int gs = (int)((a.max_chain + want_groups - 1) / want_groups);
+    if (gs < 4) gs = 4;
+    return gs >= a.max_chain ? 0 : gs;
+}
+
+int64_t tree_bytes(const ChainArgs &a, int gs) { return gs > 0 ? tree_layout(a, gs).total : 0; }
+
+cudaError_t launch_compose_chain_tree(const ChainArgs &a, int gs, void *ws, cudaStream_t s) {
+    const TreeLayout t = tree_layout(a, gs);
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    int32_t *si1 = reinterpret_cast<int32_t *>(w + t.si1), *cl1 = reinterpret_cast<int32_t *>(w + t.cl1);
+    int32_t *si2 = reinterpret_cast<int32_t *>(w + t.si2), *cl2 = reinterpret_cast<int32_t *>(w + t.cl2);
+    const int64_t groups = (int64_t)a.R * t.G;
+    tree_index_kernel<<<(unsigned)((groups + 255) / 256), 256, 0, s>>>(a, gs, t.G, si1, cl1, si2, cl2);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // level 1: every group's pair (a composed prefix per virtual request)
+    ChainArgs l1 = a;
+    l1.R = (int)groups;
+    l1.max_chain = gs;
+    l1.chain_len = cl1;
+    l1.seg_idx = si1;
+    l1.S_init = nullptr;
+    l1.S_out = reinterpret_cast<float *>(w + t.S);
+    float *lam1 = reinterpret_cast<float *>(w + t.lam);
+    float *M1 = a.fam == HYPIC_DENSE ? reinterpret_cast<float *>(w + t.M) : nullptr;
+    e = launch_compose_prefix(l1, lam1, M1, s);
+    if (e != cudaSuccess) return e;
+    // level 2: each request folds its groups' pairs in order
+    ChainArgs l2 = a;
+    l2.max_chain = t.G;
+    l2.chain_len = cl2;
+    l2.seg_idx = si2;
+    l2.P = (int)groups;
+    l2.pool_lam = lam1;
+    l2.pool_M = M1;
+    l2.pool_S = l1.S_out;
+    return launch_compose_chain(l2, s);
+}
+
 cudaError_t launch_compose_chain(const ChainArgs &a, cudaStream_t s) {
     const int64_t units = (int64_t)a.R * a.n_layers * a.H;
     if (units == 0) return cudaSuccess;

@@ -77,7 +77,7 @@ cudaError_t launch_scan_dense_ws(const ScanArgs &a, cudaStream_t s);
 int64_t static_scratch_bytes();            // size of the fixed scratch of hypic_segment_scan_static
 cudaError_t static_scratch(void **p);      // its address on the current device
 
-// Dense chained composition on tcgen05 (3 x TF32), d_k = d_v = 128.
+// Dense chained composition on tcgen05 (bf16 three-way splits, fp32 state), d_k = d_v = 128.
 bool chain_dense_tc_supported(const ChainArgs &a);
 cudaError_t launch_chain_dense_tc(const ChainArgs &a, cudaStream_t s);
 
@@ -86,6 +86,13 @@ cudaError_t launch_compose_chain(const ChainArgs &a, cudaStream_t s);
 // The cached pair of each request's ordered pool entries: S from a zero state into
 // a.S_out, T = T_pn ... T_p1 into lam_out (and M_out for dense, kda).
 cudaError_t launch_compose_prefix(const ChainArgs &a, float *lam_out, float *M_out, cudaStream_t s);
+// Two-level tree for few (request, layer, head) units with long chains: groups of
+// `gs` consecutive entries fold in parallel into cached pairs (composed prefixes),
+// then each unit folds its groups' pairs in order.  tree_group_size() is 0 where the
+// plain chain is used; tree_bytes() is the scratch the tree needs.
+int tree_group_size(const ChainArgs &a);
+int64_t tree_bytes(const ChainArgs &a, int gs);
+cudaError_t launch_compose_chain_tree(const ChainArgs &a, int gs, void *ws, cudaStream_t s);
 
 // Seam-window advance, then the composition of the rest of the segment.
 struct SeamArgs {

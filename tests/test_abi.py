@@ -177,6 +177,32 @@ def test_chain_rejects_bad_arguments(lib):
     assert chain(lib, R=0) == OK
 
 
+def chain_ws(lib, fam=0, R=2, L=1, H=2, dk=64, dv=64, mc=64, cl=A, idx=A + 0x1000, P_=5, pl=A + 0x2000, pM=0,
+             pS=A + 0x100000, Si=0, So=A + 0x800000, ws=A + 0x1000000, wsb=1 << 30, err=0):
+    return lib.hypic_compose_chain_ws(fam, R, L, H, dk, dv, mc, P(cl or None), P(idx or None), P_,
+                                      P(pl or None), P(pM or None), P(pS or None), P(Si or None),
+                                      P(So or None), P(ws or None), wsb, P(err or None), P(None))
+
+
+def test_chain_ws_rejects_bad_arguments(lib):
+    need = lib.hypic_compose_chain_workspace_bytes(0, 2, 1, 2, 64, 64, 64)
+    assert need > 0                                   # 4 units with 64-entry chains: the two-level tree
+    assert lib.hypic_compose_chain_workspace_bytes(0, 2, 1, 2, 64, 64, 4) == 0     # short chains: plain
+    assert lib.hypic_compose_chain_workspace_bytes(0, 64, 30, 32, 64, 64, 64) == 0  # many units: plain
+    assert lib.hypic_compose_chain_workspace_bytes(5, 2, 1, 2, 64, 64, 64) == EINVAL
+    assert lib.hypic_compose_chain_workspace_bytes(0, 2, 1, 2, 48, 64, 64) == EUNSUP
+    assert chain_ws(lib, wsb=need - 1) == EINVAL     # scratch too small
+    assert chain_ws(lib, ws=0) == EINVAL
+    assert chain_ws(lib, wsb=-1) == EINVAL
+    assert chain_ws(lib, ws=A + 0x1000000 + 16) == EALIGN
+    assert chain_ws(lib, ws=A + 0x100000) == EINVAL   # scratch over the pool
+    assert chain_ws(lib, ws=A + 0x800000) == EINVAL   # scratch over S_out
+    assert chain_ws(lib, So=A + 0x100100) == EINVAL   # S_out inside the pool
+    assert chain_ws(lib, fam=2, pM=0) == EINVAL
+    assert chain_ws(lib, dv=16) == EUNSUP
+    assert chain_ws(lib, R=0) == OK
+
+
 def prefix(lib, fam=0, R=2, L=2, H=2, dk=64, dv=64, mc=3, cl=A, idx=A, P_=5, pl=A, pM=0, pS=A + 0x100000,
            lo=A + 0x300000, Mo=0, So=A + 0x400000, err=0):
     return lib.hypic_compose_prefix(fam, R, L, H, dk, dv, mc, P(cl or None), P(idx or None), P_,
