@@ -706,6 +706,42 @@ def run_chain(args):
     return res
 
 
+def run_scan_sd_o(args, L=2048):
+    """Scalar and diagonal scans with the per-token outputs o_t = S_t^T q_t: 8 segments
+    x L tokens x 32 heads, bf16 q/k/v/o, each family timed alone."""
+    import torch
+    import linear_attention_state_gated_gb300 as hy
+    from linear_attention_state_gated_gb300 import workloads as wl
+    B, H, d = HEAD["B"], HEAD["H"], HEAD["d"]
+    hbm, _, _, src = peaks()
+    dev = torch.device("cuda")
+    res = {"workload": f"scalar / diagonal scan with o_t, batch {B} x {L} tokens, {H} heads, d_k=d_v={d}"}
+    for fam in (0, 1):
+        w = wl.scalar_diag(fam, seg_len=L, n_seg=B, H=H, d=d, seed=1, with_q=True)
+        k = torch.from_numpy(w["k"]).to(torch.bfloat16).to(dev)
+        v = torch.from_numpy(w["v"]).to(torch.bfloat16).to(dev)
+        q = torch.from_numpy(w["q"]).to(torch.bfloat16).to(dev)
+        a = torch.from_numpy(w["alpha"]).to(dev)
+        offs = torch.from_numpy(w["seg_offsets"]).to(dev)
+        out = hy.segment_scan(fam, k, v, a, offs, q=q, want_o=True)
+        torch.cuda.synchronize()
+        reps = 5
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            hy.segment_scan(fam, k, v, a, offs, q=q, want_o=True, out=out)
+        e1.record()
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) / reps / 1e3
+        by = scan_bytes(fam, B * L * H, B * H, d) + B * L * H * d * 2 * 2   # + q read, o written
+        res[{0: "scalar", 1: "diag"}[fam]] = {
+            "tokens_per_s": B * L / t, "ms": t * 1e3,
+            "roofline": {"bound": "hbm", "achieved": by / t / 1e9, "peak": hbm, "unit": "GB/s",
+                         "frac": by / t / 1e9 / hbm, "peak_kind": f"HBM copy, {src}"}}
+        del k, v, q, a, offs, out
+    return res
+
+
 def run_tree(args):
     """Few units, long chains: 1 layer x 4 heads, one request folding 64 pool entries
     in order, per family; the plain chain (one CTA per (request, layer, head)) against
@@ -947,8 +983,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="hypic", choices=["hypic", "reference"])
     ap.add_argument("--L", type=int, default=8192)
-    ap.add_argument("--rows", default="sd,dense,kda,compose,seam,prefix,chain,tree,mix",
-                    help="extra rows: sd,dense,kda,compose,seam,prefix,chain,tree,mix or none")
+    ap.add_argument("--rows", default="sd,sdo,dense,kda,compose,seam,prefix,chain,tree,mix",
+                    help="extra rows: sd,sdo,dense,kda,compose,seam,prefix,chain,tree,mix or none")
     ap.add_argument("--dense-lengths", default="512,2048,8192,32768",
                     help="dense rows: segment lengths of the 30-layer stack")
     ap.add_argument("--sd-lengths", default="512,2048",
@@ -995,6 +1031,8 @@ def main():
         rows["prefix"] = run_prefix(args)
     if solo and "chain" in args.rows:
         rows["rag_chain"] = run_chain(args)
+    if solo and "sdo" in args.rows:
+        rows["scan_sd_o"] = run_scan_sd_o(args)
     if solo and "tree" in args.rows:
         rows["tree"] = run_tree(args)
     if solo and "mix" in args.rows:

@@ -143,6 +143,7 @@ int hypic_segment_scan(int fam, int in_dtype, int n_layers, int n_seg, int64_t t
                              v, alpha, beta, lam_out, M_out, S_out, o_out, d_err, a, none);
     if (rc != HYPIC_OK || none) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    if (hypic::scan_sd_o_supported(a)) return from_cuda(hypic::launch_scan_sd_o(a, s));
     if (hypic::scan_sd_tc_supported(a)) return from_cuda(hypic::launch_scan_sd_tc(a, s));
     if (hypic::scan_dense_tc_supported(a)) return from_cuda(hypic::launch_scan_dense_tc(a, s));
     return from_cuda(hypic::launch_scan_recurrent(a, s));
@@ -194,6 +195,7 @@ int hypic_segment_scan_ws(int fam, int in_dtype, int n_layers, int n_seg, int64_
         a.ws = static_cast<float *>(workspace);
         return from_cuda(hypic::launch_scan_sd_bal(a, s));
     }
+    if (hypic::scan_sd_o_supported(a)) return from_cuda(hypic::launch_scan_sd_o(a, s));
     if (hypic::scan_sd_tc_supported(a)) return from_cuda(hypic::launch_scan_sd_tc(a, s));
     if (hypic::scan_dense_tc_supported(a)) return from_cuda(hypic::launch_scan_dense_tc(a, s));
     return from_cuda(hypic::launch_scan_recurrent(a, s));

@@ -66,6 +66,9 @@ cudaError_t launch_scan_sd_tc(const ScanArgs &a, cudaStream_t s);
 bool scan_sd_bal_shape(const ScanArgs &a);        // the balanced schedule (scratch) takes it
 int64_t scan_sd_bal_bytes();                      // its scratch
 cudaError_t launch_scan_sd_bal(const ScanArgs &a, cudaStream_t s);
+// Scalar gates with the per-token outputs o_t, chunks in order on tcgen05 (bf16, 128 x 128).
+bool scan_sd_o_supported(const ScanArgs &a);
+cudaError_t launch_scan_sd_o(const ScanArgs &a, cudaStream_t s);
 
 // Gated delta rule scan on tcgen05 tensor cores (bf16 inputs, d_k = d_v = 128, no o_t).
 bool scan_dense_tc_supported(const ScanArgs &a);

@@ -122,6 +122,35 @@ def test_scan_with_beta_and_mamba_like_gates():
         check(fam, got, ref, TOL_SCAN_BF16)
 
 
+def test_scalar_o_mamba_like_gates_and_beta():
+    """o_t on the scalar tensor-core path (chunks in order): per-token decays, some
+    strong, a write scale beta in [0, 2], segments across chunk edges and empty."""
+    g = np.random.default_rng(13)
+    lens = [300, 77, 0, 640, 64, 1, 65]
+    w = wl.scalar_diag(SCALAR, lengths=lens, n_layers=2, H=4, d=128, seed=10, with_q=True)
+    w["alpha"] = np.exp(-g.exponential(0.5, size=w["alpha"].shape)).astype(np.float32)
+    w["beta"] = g.uniform(0.0, 2.0, size=w["k"].shape[:3]).astype(np.float32)
+    got = host(gpu_scan(w, want_o=True))
+    ref = oracle_scan(w, want_o=True)
+    check(SCALAR, got, ref, TOL_SCAN_BF16, o_tol=TOL_O_BF16, seg_offsets=w["seg_offsets"])
+    assert np.all(got["S"][:, 2] == 0) and np.all(got["lam"][:, 2] == 0)
+
+
+def test_scalar_o_retnet_full_size_sampled():
+    """RetNet gates, 8 segments x 2048 tokens x 32 heads with o_t (the benchmark's
+    launch), sampled (segment, head) units against the straight recurrence."""
+    w = wl.scalar_diag(SCALAR, seg_len=2048, n_seg=8, with_q=True)
+    got = host(gpu_scan(w, want_o=True))
+    rs = np.random.default_rng(2048)
+    for seg, h in [(0, 0), (7, 31), (3, 26)] + [tuple(x) for x in rs.integers([0, 0], [8, 32], size=(2, 2))]:
+        a, b = w["seg_offsets"][seg], w["seg_offsets"][seg + 1]
+        ref = oracle.sequential(SCALAR, w["k"][:, a:b, h:h + 1], w["v"][:, a:b, h:h + 1],
+                                w["alpha"][:, a:b, h:h + 1], q=w["q"][:, a:b, h:h + 1], want_o=True)
+        sub = {"S": got["S"][:, seg, h:h + 1], "lam": got["lam"][:, seg, h:h + 1],
+               "o": got["o"][:, a:b, h:h + 1]}
+        check(SCALAR, sub, ref, TOL_SCAN_BF16, o_tol=TOL_O_BF16, seg_offsets=[0, b - a])
+
+
 @pytest.mark.parametrize("fam", [SCALAR, DIAG], ids=["scalar", "diag"])
 @pytest.mark.parametrize("L", [512, 8192])
 def test_scalar_diag_full_size_sampled(fam, L):
