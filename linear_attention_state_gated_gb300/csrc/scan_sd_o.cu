@@ -38,15 +38,15 @@ using dense::wait_or_abort;
 constexpr int kC = 64;
 constexpr int kD = 128;
 constexpr int kBox = kC * 128;            // 64 channels x 64 tokens, bf16: 8 KB
-constexpr int kNS = 2;                    // TMA stages
+constexpr int kNS = 3;                    // TMA stages
 constexpr int kCW = 512;                  // conversion threads (16 warps)
 constexpr int kThreads = 64 + kCW;
 
 // shared memory, from the 1024-aligned base
 constexpr int kStage = 6 * kBox;          // K, V, Q: two boxes each
 constexpr int kOffK = 0, kOffV = 2 * kBox, kOffQ = 4 * kBox;
-constexpr int kKt = kNS * kStage;         // K~ hi / lo (16 KB each), two buffers (chunk parity)
-constexpr int kGq = kKt + 2 * 32768;      // Gq hi / lo (8 KB each), two buffers
+constexpr int kKt = kNS * kStage;         // K~ hi / lo (16 KB each)
+constexpr int kGq = kKt + 32768;          // Gq hi / lo (8 KB each), two buffers (chunk parity)
 constexpr int kOst = kGq + 2 * 16384;     // o staging: 8 tokens x 32 channels per warp
 constexpr int kCtl = kOst + 16 * 512;
 
@@ -168,17 +168,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_wait(&ctl->full[j % kNS], (uint32_t)(j / kNS) & 1u);
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+        // ------------------------------------------------------------ MMA issuer: per chunk the
+        // update first (the chain), then the next chunk's Gram (so its Gq and K~ can be
+        // built meanwhile), then the outputs
         if (lane == 0) {
-            for (int j = 0; j < nc; ++j) {
-                const int s = j % kNS;
-                const uint32_t par = (uint32_t)j & 1u;
-                const uint8_t *stg = smem + s * kStage;
-                const uint32_t kb = smem_addr(stg + kOffK), vb = smem_addr(stg + kOffV), qb = smem_addr(stg + kOffQ);
-                if (!wait_or_abort(&ctl->full[s], (uint32_t)(j / kNS) & 1u, abortp)) break;
-                // ---- Gram G = Q K^T (the Gram columns are free once Gq of the previous chunk is built)
-                if (j > 0 && !wait_or_abort(&ctl->gk_ready, par ^ 1u, abortp)) break;
+            auto gram = [&](int jj) -> bool {   // G = Q K^T of chunk jj into the Gram columns
+                const int s = jj % kNS;
+                if (!wait_or_abort(&ctl->full[s], (uint32_t)(jj / kNS) & 1u, abortp)) return false;
                 tc_fence_after();
+                const uint8_t *stg = smem + s * kStage;
+                const uint32_t kb = smem_addr(stg + kOffK), qb = smem_addr(stg + kOffQ);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     const uint32_t off = (uint32_t)(ks >> 2) * kBox + (uint32_t)(ks & 3) * 32u;
@@ -186,9 +185,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ks > 0 ? 1u : 0u);
                 }
                 mma_commit(&ctl->gram_done);
-                // ---- O1^T = S0^T Q^T, once S0 is converted and the previous O1, O2 are read
-                if (!wait_or_abort(&ctl->gk_ready, par, abortp)) break;
-                if (!wait_or_abort(&ctl->xop_ready, par, abortp)) break;
+                return true;
+            };
+            bool ok = nc == 0 || gram(0);
+            for (int j = 0; j < nc && ok; ++j) {
+                const int s = j % kNS;
+                const uint32_t par = (uint32_t)j & 1u;
+                const uint8_t *stg = smem + s * kStage;
+                const uint32_t vb = smem_addr(stg + kOffV), qb = smem_addr(stg + kOffQ);
+                // Gq, K~ of this chunk and its S0 operand are in place (S rewritten as b_C S0)
+                if (!wait_or_abort(&ctl->gk_ready, par, abortp) || !wait_or_abort(&ctl->xop_ready, par, abortp)) break;
+                tc_fence_after();
+                // ---- S^T += V^T K~ (lo, then hi)
+                const uint32_t kt = smem_addr(smem + kKt);
+#pragma unroll
+                for (int hl = 1; hl >= 0; --hl)
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_f16(tmem + kTx, smem_desc_sw128(vb + (uint32_t)ks * 2048u, kBox, 1024),
+                                smem_desc_sw128(kt + (uint32_t)hl * 16384u + (uint32_t)ks * 2048u, kBox, 1024), id_x,
+                                1u);
+                mma_commit(&ctl->x_done);
+                // ---- the next chunk's Gram (its columns were read for this chunk's Gq)
+                if (j + 1 < nc && !gram(j + 1)) break;
+                // ---- O1^T = S0^T Q^T, O2^T = V^T Gq^T (lo, then hi), once the previous ones are read
                 if (j > 0 && !wait_or_abort(&ctl->o_free, par ^ 1u, abortp)) break;
                 tc_fence_after();
 #pragma unroll
@@ -199,17 +219,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_f16_ta(tmem + kTo1, tmem + kTxh + (uint32_t)hl * 64u + (uint32_t)ks * 8u,
                                    smem_desc_sw128(qb + off, 0, 1024), id_o1, (hl == 0 || ks > 0) ? 1u : 0u);
                     }
-                // ---- S^T += V^T K~ (lo, then hi)
-                const uint32_t kt = smem_addr(smem + kKt + (int)par * 32768);
-#pragma unroll
-                for (int hl = 1; hl >= 0; --hl)
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        mma_f16(tmem + kTx, smem_desc_sw128(vb + (uint32_t)ks * 2048u, kBox, 1024),
-                                smem_desc_sw128(kt + (uint32_t)hl * 16384u + (uint32_t)ks * 2048u, kBox, 1024), id_x,
-                                1u);
-                mma_commit(&ctl->x_done);
-                // ---- O2^T = V^T Gq^T (lo, then hi)
                 const uint32_t gq = smem_addr(smem + kGq + (int)par * 16384);
 #pragma unroll
                 for (int hl = 1; hl >= 0; --hl)
@@ -248,165 +257,191 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_st();
         }
 
-        bool alive = true;
-        for (int j = 0; j <= nc && alive; ++j) {
-            const uint32_t par = (uint32_t)j & 1u;
-            const int gsl = j % 3;   // gate slot of chunk j
-            if (j < nc) {
-                const int s = j % kNS;
-                const uint8_t *stg = smem + s * kStage;
-                const int nval = (int)min((int64_t)kC, t1 - t0 - (int64_t)j * kC);
-                // ---- gates of the chunk (warp 0 of the group): Lambda_t, b_t, beta_t
-                if (sw == 0) {
-                    float lg[2], pb[2];
+        // alpha, beta of one chunk (warp 0 of the group, two tokens a lane), loaded a chunk ahead
+        float ga[2] = {1.f, 1.f}, gb[2] = {0.f, 0.f};
+        auto gate_load = [&](int jj) {
+            if (jj >= nc) return;
 #pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        const int t = lane + 32 * q;
-                        const bool v = t < nval;
-                        const int64_t r = (row0 + (int64_t)j * kC + t) * a.H + h;
-                        lg[q] = v ? logf(a.alpha[r]) : 0.f;
-                        pb[q] = v ? (a.beta ? a.beta[r] : 1.f) : 0.f;
-                    }
-                    float inc[2];
-#pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        float x = lg[q];
-#pragma unroll
-                        for (int off = 1; off < 32; off <<= 1) {
-                            const float y = __shfl_up_sync(0xffffffffu, x, off);
-                            if (lane >= off) x += y;
-                        }
-                        inc[q] = x;
-                    }
-                    inc[1] += __shfl_sync(0xffffffffu, inc[0], 31);
-#pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        const int t = lane + 32 * q;
-                        ctl->lt[gsl][t] = inc[q];
-                        ctl->bt[gsl][t] = expf(inc[q]);
-                        ctl->beta[gsl][t] = pb[q];
-                    }
-                    lam += (double)__shfl_sync(0xffffffffu, inc[1], 31);   // lambda: chunk totals in double
-                }
-                bool ok = wait_or_abort(&ctl->full[s], (uint32_t)(j / kNS) & 1u, abortp) &&
-                          wait_or_abort(&ctl->gram_done, par, abortp);
-                if (!bar_and(2, kCW, ok)) {
-                    alive = false;
-                    break;
-                }
-                tc_fence_after();
-                const float LC = ctl->lt[gsl][kC - 1];
-                // ---- Gq[t][s] = [s <= t] exp(Lambda_t - Lambda_s) beta_s G[t][s] -> bf16 hi / lo
-                // (row t, s contiguous, 128-byte swizzle); lanes 0..63 of the Gram
-                if (quarter < 2) {
-                    const int t = m;
-                    uint32_t r[16];
-                    tmem_ld16(tmem + lane_off + kTg + (uint32_t)(cg * 16), r);
-                    const float ltt = ctl->lt[gsl][t];
-                    float f[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int sc = cg * 16 + i;
-                        f[i] = sc <= t ? __expf(ltt - ctl->lt[gsl][sc]) * ctl->beta[gsl][sc] : 0.f;
-                    }
-                    tmem_wait_ld();
-                    uint32_t hi[8], lo[8];
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        split_pair(f[2 * q] * __uint_as_float(r[2 * q]), f[2 * q + 1] * __uint_as_float(r[2 * q + 1]),
-                                   hi[q], lo[q]);
-                    uint8_t *gt = smem + kGq + (int)par * 16384 + t * 128;
-#pragma unroll
-                    for (int hc = 0; hc < 2; ++hc) {
-                        const int c = 2 * cg + hc;
-                        const int off = (c ^ (t & 7)) << 4;
-                        *reinterpret_cast<uint4 *>(gt + off) =
-                            make_uint4(hi[4 * hc], hi[4 * hc + 1], hi[4 * hc + 2], hi[4 * hc + 3]);
-                        *reinterpret_cast<uint4 *>(gt + 8192 + off) =
-                            make_uint4(lo[4 * hc], lo[4 * hc + 1], lo[4 * hc + 2], lo[4 * hc + 3]);
-                    }
-                }
-                // ---- K~_s = exp(LC - Lambda_s) beta_s k_s -> bf16 hi / lo (same swizzled layout as K)
-                {
-                    const int sidx = st >> 3;           // token
-                    const int g = st & 7;               // 16-channel group
-                    const int box = g >> 2;
-                    const float w = __expf(LC - ctl->lt[gsl][sidx]) * ctl->beta[gsl][sidx];
-                    uint8_t *kt = smem + kKt + (int)par * 32768;
-#pragma unroll
-                    for (int hc = 0; hc < 2; ++hc) {
-                        const int c = (g & 3) * 2 + hc;
-                        const int off = box * kBox + sidx * 128 + ((c ^ (sidx & 7)) << 4);
-                        const uint4 raw = *reinterpret_cast<const uint4 *>(stg + kOffK + off);
-                        const uint32_t in[4] = {raw.x, raw.y, raw.z, raw.w};
-                        uint32_t hv[4], lv[4];
-#pragma unroll
-                        for (int p = 0; p < 4; ++p)
-                            split_pair(__uint_as_float(in[p] << 16) * w, __uint_as_float(in[p] & 0xFFFF0000u) * w,
-                                       hv[p], lv[p]);
-                        *reinterpret_cast<uint4 *>(kt + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-                        *reinterpret_cast<uint4 *>(kt + 16384 + off) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
-                    }
-                }
-                fence_async_smem();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&ctl->gk_ready);
-                // ---- S0 operand (hi / lo) and S <- b_C S0, once the previous update is done
-                ok = j == 0 || wait_or_abort(&ctl->x_done, par ^ 1u, abortp);
-                if (!bar_and(2, kCW, ok)) {
-                    alive = false;
-                    break;
-                }
-                tc_fence_after();
-                const float bC = ctl->bt[gsl][kC - 1];
-#pragma unroll
-                for (int p = 0; p < 2; ++p) {
-                    uint32_t r[16], hi[8], lo[8];
-                    tmem_ld16(tx + (uint32_t)(p * 64), r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        split_pair(__uint_as_float(r[2 * q]), __uint_as_float(r[2 * q + 1]), hi[q], lo[q]);
-                    tmem_st8(txh + (uint32_t)(p * 32), hi);
-                    tmem_st8(txh + 64u + (uint32_t)(p * 32), lo);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(bC * __uint_as_float(r[i]));
-                    tmem_st16(tx + (uint32_t)(p * 64), r);
-                }
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&ctl->xop_ready);
+            for (int q = 0; q < 2; ++q) {
+                const int t = lane + 32 * q;
+                const bool v = (int64_t)jj * kC + t < t1 - t0;
+                const int64_t r = (row0 + (int64_t)jj * kC + t) * a.H + h;
+                ga[q] = v ? a.alpha[r] : 1.f;
+                gb[q] = v ? (a.beta ? a.beta[r] : 1.f) : 0.f;
             }
-            // ---- o_t of the previous chunk: b_t O1 + O2 -> bf16
-            if (j > 0) {
-                const uint32_t pp = par ^ 1u;
-                const int psl = (j + 2) % 3;   // gate slot of chunk j - 1
-                if (!bar_and(2, kCW, wait_or_abort(&ctl->o_done, pp, abortp))) {
-                    alive = false;
-                    break;
+        };
+        if (sw == 0) gate_load(0);
+        // gates, Gq and K~ of chunk jj (slot jj % 3, Gq tiles of parity jj & 1); false on a timeout
+        auto prep = [&](int jj) -> bool {
+            const int gsl = jj % 3;
+            const int s = jj % kNS;
+            const uint8_t *stg = smem + s * kStage;
+            const uint32_t par = (uint32_t)jj & 1u;
+            const int nval = (int)min((int64_t)kC, t1 - t0 - (int64_t)jj * kC);
+            if (sw == 0) {   // Lambda_t (inclusive log-space prefix), b_t, beta_t
+                float lg[2], pb[2];
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const bool v = lane + 32 * q < nval;
+                    lg[q] = v ? logf(ga[q]) : 0.f;
+                    pb[q] = v ? gb[q] : 0.f;
                 }
-                tc_fence_after();
-                uint32_t r1[16], r2[16];
-                tmem_ld16(tmem + lane_off + kTo1 + (uint32_t)(cg * 16), r1);
-                tmem_ld16(tmem + lane_off + kTo2 + (uint32_t)(cg * 16), r2);
+                gate_load(jj + 1);   // the next chunk's gates, in flight while this one is used
+                float inc[2];
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    float x = lg[q];
+#pragma unroll
+                    for (int off = 1; off < 32; off <<= 1) {
+                        const float y = __shfl_up_sync(0xffffffffu, x, off);
+                        if (lane >= off) x += y;
+                    }
+                    inc[q] = x;
+                }
+                inc[1] += __shfl_sync(0xffffffffu, inc[0], 31);
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int t = lane + 32 * q;
+                    ctl->lt[gsl][t] = inc[q];
+                    ctl->bt[gsl][t] = expf(inc[q]);
+                    ctl->beta[gsl][t] = pb[q];
+                }
+                lam += (double)__shfl_sync(0xffffffffu, inc[1], 31);   // lambda: chunk totals in double
+            }
+            const bool ok = wait_or_abort(&ctl->full[s], (uint32_t)(jj / kNS) & 1u, abortp) &&
+                            wait_or_abort(&ctl->gram_done, par, abortp);
+            if (!bar_and(2, kCW, ok)) return false;
+            tc_fence_after();
+            const float LC = ctl->lt[gsl][kC - 1];
+            // ---- Gq[t][s] = [s <= t] exp(Lambda_t - Lambda_s) beta_s G[t][s] -> bf16 hi / lo
+            // (row t, s contiguous, 128-byte swizzle); lanes 0..63 of the Gram
+            if (quarter < 2) {
+                const int t = m;
+                uint32_t r[16];
+                tmem_ld16(tmem + lane_off + kTg + (uint32_t)(cg * 16), r);
+                const float ltt = ctl->lt[gsl][t];
+                float f[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int sc = cg * 16 + i;
+                    f[i] = sc <= t ? __expf(ltt - ctl->lt[gsl][sc]) * ctl->beta[gsl][sc] : 0.f;
+                }
                 tmem_wait_ld();
+                uint32_t hi[8], lo[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    split_pair(f[2 * q] * __uint_as_float(r[2 * q]), f[2 * q + 1] * __uint_as_float(r[2 * q + 1]), hi[q],
+                               lo[q]);
+                uint8_t *gt = smem + kGq + (int)par * 16384 + t * 128;
+#pragma unroll
+                for (int hc = 0; hc < 2; ++hc) {
+                    const int c = 2 * cg + hc;
+                    const int off = (c ^ (t & 7)) << 4;
+                    *reinterpret_cast<uint4 *>(gt + off) =
+                        make_uint4(hi[4 * hc], hi[4 * hc + 1], hi[4 * hc + 2], hi[4 * hc + 3]);
+                    *reinterpret_cast<uint4 *>(gt + 8192 + off) =
+                        make_uint4(lo[4 * hc], lo[4 * hc + 1], lo[4 * hc + 2], lo[4 * hc + 3]);
+                }
+            }
+            // ---- K~_s = exp(LC - Lambda_s) beta_s k_s -> bf16 hi / lo (same swizzled layout as K),
+            // once the previous update has read the tiles
+            if (!bar_and(2, kCW, jj == 0 || wait_or_abort(&ctl->x_done, par ^ 1u, abortp))) return false;
+            {
+                const int sidx = st >> 3;           // token
+                const int g = st & 7;               // 16-channel group
+                const int box = g >> 2;
+                const float w = __expf(LC - ctl->lt[gsl][sidx]) * ctl->beta[gsl][sidx];
+                uint8_t *kt = smem + kKt;
+#pragma unroll
+                for (int hc = 0; hc < 2; ++hc) {
+                    const int c = (g & 3) * 2 + hc;
+                    const int off = box * kBox + sidx * 128 + ((c ^ (sidx & 7)) << 4);
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(stg + kOffK + off);
+                    const uint32_t in[4] = {raw.x, raw.y, raw.z, raw.w};
+                    uint32_t hv[4], lv[4];
+#pragma unroll
+                    for (int p = 0; p < 4; ++p)
+                        split_pair(__uint_as_float(in[p] << 16) * w, __uint_as_float(in[p] & 0xFFFF0000u) * w, hv[p],
+                                   lv[p]);
+                    *reinterpret_cast<uint4 *>(kt + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                    *reinterpret_cast<uint4 *>(kt + 16384 + off) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+                }
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->gk_ready);
+            return true;
+        };
+        // o_t of chunk jj (b_t O1 + O2 -> bf16); O1, O2 complete (o_done awaited)
+        auto out_o = [&](int jj, bool release) {
+            uint32_t r1[16], r2[16];
+            tmem_ld16(tmem + lane_off + kTo1 + (uint32_t)(cg * 16), r1);
+            tmem_ld16(tmem + lane_off + kTo2 + (uint32_t)(cg * 16), r2);
+            tmem_wait_ld();
+            if (release) {
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ctl->o_free);
-                uint32_t opk[8];
+            }
+            const int psl = jj % 3;
+            uint32_t opk[8];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int t = cg * 16 + 2 * q;
-                    const __nv_bfloat162 v2 = __floats2bfloat162_rn(
-                        fmaf(ctl->bt[psl][t], __uint_as_float(r1[2 * q]), __uint_as_float(r2[2 * q])),
-                        fmaf(ctl->bt[psl][t + 1], __uint_as_float(r1[2 * q + 1]), __uint_as_float(r2[2 * q + 1])));
-                    opk[q] = *reinterpret_cast<const uint32_t *>(&v2);
-                }
-                const int jp = j - 1;
-                store_o(a, h, cg, quarter, lane, row0 + (int64_t)jp * kC,
-                        (int)min((int64_t)kC, t1 - t0 - (int64_t)jp * kC), opk, ostg);
+            for (int q = 0; q < 8; ++q) {
+                const int t = cg * 16 + 2 * q;
+                const __nv_bfloat162 v2 = __floats2bfloat162_rn(
+                    fmaf(ctl->bt[psl][t], __uint_as_float(r1[2 * q]), __uint_as_float(r2[2 * q])),
+                    fmaf(ctl->bt[psl][t + 1], __uint_as_float(r1[2 * q + 1]), __uint_as_float(r2[2 * q + 1])));
+                opk[q] = *reinterpret_cast<const uint32_t *>(&v2);
+            }
+            store_o(a, h, cg, quarter, lane, row0 + (int64_t)jj * kC, (int)min((int64_t)kC, t1 - t0 - (int64_t)jj * kC),
+                    opk, ostg);
+        };
+
+        bool alive = nc == 0 || prep(0);
+        for (int j = 0; j < nc && alive; ++j) {
+            const uint32_t par = (uint32_t)j & 1u;
+            // ---- S0 operand (hi / lo) and S <- b_C S0: the previous update and the previous
+            // outputs' products (which read the S0 operand) are done
+            bool ok = j == 0 || (wait_or_abort(&ctl->x_done, par ^ 1u, abortp) &&
+                                 wait_or_abort(&ctl->o_done, par ^ 1u, abortp));
+            if (!bar_and(2, kCW, ok)) {
+                alive = false;
+                break;
+            }
+            tc_fence_after();
+            const float bC = ctl->bt[j % 3][kC - 1];
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+                uint32_t r[16], hi[8], lo[8];
+                tmem_ld16(tx + (uint32_t)(p * 64), r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    split_pair(__uint_as_float(r[2 * q]), __uint_as_float(r[2 * q + 1]), hi[q], lo[q]);
+                tmem_st8(txh + (uint32_t)(p * 32), hi);
+                tmem_st8(txh + 64u + (uint32_t)(p * 32), lo);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(bC * __uint_as_float(r[i]));
+                tmem_st16(tx + (uint32_t)(p * 64), r);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->xop_ready);
+            // ---- the previous chunk's outputs, then the next chunk's Gq and K~
+            if (j > 0) out_o(j - 1, true);
+            if (j + 1 < nc && !prep(j + 1)) {
+                alive = false;
+                break;
+            }
+        }
+        if (alive && nc > 0) {   // the last chunk's outputs
+            if (bar_and(2, kCW, wait_or_abort(&ctl->o_done, (uint32_t)(nc - 1) & 1u, abortp))) {
+                tc_fence_after();
+                out_o(nc - 1, false);
+            } else {
+                alive = false;
             }
         }
 
