@@ -165,6 +165,7 @@ int64_t hypic_segment_scan_workspace_bytes(int fam, int in_dtype, int n_layers, 
     a.o_out = with_o ? reinterpret_cast<void *>(16) : nullptr;   // only tested against NULL
     if (n_layers == 0 || n_seg == 0) return 0;
     if (hypic::scan_dense_ws_shape(a)) return hypic::scan_dense_ws_bytes(a);
+    if (hypic::scan_kda_tc_shape(a)) return hypic::scan_kda_tc_bytes(a);
     if (hypic::scan_sd_bal_shape(a)) return hypic::scan_sd_bal_bytes();
     return 0;
 }
@@ -188,6 +189,14 @@ int hypic_segment_scan_ws(int fam, int in_dtype, int n_layers, int n_seg, int64_
     if (hypic::scan_dense_ws_supported(a)) {
         a.ws = static_cast<float *>(workspace);
         return from_cuda(hypic::launch_scan_dense_ws(a, s));
+    }
+    if (hypic::scan_kda_tc_shape(a)) {
+        if (!workspace || workspace_bytes < hypic::scan_kda_tc_bytes(a)) return HYPIC_EINVAL;
+        if (!aligned(workspace, 256)) return HYPIC_EALIGN;
+        if (hypic::scan_kda_tc_supported(a)) {
+            a.ws = static_cast<float *>(workspace);
+            return from_cuda(hypic::launch_scan_kda_tc(a, s));
+        }
     }
     if (hypic::scan_sd_bal_shape(a) && hypic::scan_sd_tc_supported(a)) {
         if (!workspace || workspace_bytes < hypic::scan_sd_bal_bytes()) return HYPIC_EINVAL;

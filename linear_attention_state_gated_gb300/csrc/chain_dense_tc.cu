@@ -87,7 +87,7 @@ __device__ __forceinline__ int64_t step_entry(const ChainArgs &a, int64_t u, int
     const int64_t lhn = (int64_t)a.n_layers * a.H;
     const int r = (int)(u / lhn);
     const int64_t lh = u % lhn;
-    int p = a.seg_idx ? a.seg_idx[(int64_t)r * a.max_chain + c] : r;
+    int p = a.seg_idx ? a.seg_idx[(int64_t)r * a.max_chain + c] : (a.seg_first ? a.seg_first[r] + c : r);
     if (p < 0 || p >= a.P) {
         if (flag) flag_index_error(a.d_err);
         p = p < 0 ? 0 : a.P - 1;

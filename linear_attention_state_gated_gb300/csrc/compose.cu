@@ -185,7 +185,7 @@ __device__ __forceinline__ int clamp_len(const ChainArgs &a, int r) {
 }
 
 __device__ __forceinline__ int clamp_idx(const ChainArgs &a, int r, int j) {
-    int p = a.seg_idx[(int64_t)r * a.max_chain + j];
+    int p = a.seg_idx ? a.seg_idx[(int64_t)r * a.max_chain + j] : a.seg_first[r] + j;
     if (p < 0 || p >= a.P) {
         flag_index_error(a.d_err);
         p = p < 0 ? 0 : a.P - 1;

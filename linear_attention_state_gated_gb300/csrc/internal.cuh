@@ -24,6 +24,7 @@ struct ScanArgs {
     float *ws;        // caller-owned scratch of the two-pass dense scan (or NULL)
     int *d_err;
     const int *order = nullptr;   // two-pass dense: segments longest first (or NULL: as given)
+    const int *unit_mask = nullptr;   // token-by-token kernel: only units u with unit_mask[u] != 0 (or NULL: all)
 };
 
 struct ComposeArgs {
@@ -37,6 +38,8 @@ struct ComposeArgs {
 struct ChainArgs {
     int fam, R, n_layers, H, dk, dv, max_chain, P;
     const int32_t *chain_len, *seg_idx;
+    // without seg_idx: the entries of request r are seg_first[r], seg_first[r] + 1, ... (or NULL)
+    const int32_t *seg_first = nullptr;
     const float *pool_lam, *pool_M, *pool_S, *S_init;
     float *S_out;
     int *d_err;
@@ -77,6 +80,13 @@ bool scan_dense_ws_shape(const ScanArgs &a);       // sizes / options the two-pa
 bool scan_dense_ws_supported(const ScanArgs &a);   // ... and the runtime can encode its tensor maps
 int64_t scan_dense_ws_bytes(const ScanArgs &a);
 cudaError_t launch_scan_dense_ws(const ScanArgs &a, cudaStream_t s);
+// KDA-style gates on tcgen05 (bf16, 128 x 128, no o_t): each chunk's pair in parallel,
+// then the composed-prefix kernels over each segment's chunks.  Scratch-backed.
+constexpr int64_t kKdaMaxScratch = (int64_t)64 << 30;   // beyond this the token-by-token kernel
+bool scan_kda_tc_shape(const ScanArgs &a);
+bool scan_kda_tc_supported(const ScanArgs &a);
+int64_t scan_kda_tc_bytes(const ScanArgs &a);
+cudaError_t launch_scan_kda_tc(const ScanArgs &a, cudaStream_t s);
 int64_t static_scratch_bytes();            // size of the fixed scratch of hypic_segment_scan_static
 cudaError_t static_scratch(void **p);      // its address on the current device
 

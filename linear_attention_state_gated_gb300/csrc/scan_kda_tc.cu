@@ -1,0 +1,672 @@
+// scan_kda_tc.cu -- segment scan of the KDA-style family (a gate per key channel
+// inside the erasing update, T_t = diag(alpha_t)(I - beta_t k_t k_t^T)) on tcgen05
+// tensor cores, bf16 k / v, d_k = d_v = 128, no o_t.
+//
+// Two passes.  The pair of a concatenation is the composition of the pairs of its
+// parts, T(C1.C2) = T(C2) T(C1) and S(C1.C2|0) = T(C2) S(C1|0) + S(C2|0), so:
+//   1. every chunk of 64 tokens of every segment becomes a cached pair (lambda_c,
+//      M_c, S_c) with T_c = exp(lambda_c) M_c, all chunks in parallel
+//      (scan_kda_chunk_kernel, one CTA per (layer, chunk slot, head));
+//   2. each segment folds its chunks' pairs in order with the composed-prefix
+//      kernels (the state's chain from zero and the operator chain from I).
+//
+// The chunk's pair in closed form (WY / UT form of the per-channel gated delta
+// rule).  Inside a chunk, with Lam_t the inclusive prefix sum of log alpha over
+// tokens (per channel; Lam_{-1} = 0), Lp_t = Lam_{t-1}, L = Lam_63:
+//   Lc[t][s] = [s < t] beta_s sum_i k_ti k_si exp(Lp_t,i - Lp_s,i)
+//   Le[t][s] = [s < t] beta_s sum_i k_ti k_si exp(Lp_t,i - Lam_s,i)
+//   P        = (beta o Ct)^T (I + Lc)^-1,   Ct[s][i] = k_si exp(L_i - Lp_s,i)
+//   T_c      = diag(exp(L)) - P Ka,          Ka[t][j] = k_tj exp(Lp_t,j)
+//   S_c      = Q V,  Q = (beta o Et)^T - P Le,  Et[s][i] = k_si exp(L_i - Lam_s,i)
+// The Gram terms factor through a reference r = Lam_31 of the chunk,
+// exp(Lp_t - Lp_s) = exp(Lp_t - r) exp(r - Lp_s), so that Lc and Le are one
+// tensor-core product [Ck'; Ek'] Aq^T (Aq_t = k_t exp(Lp_t - r), Ck'_s = beta_s k_s
+// exp(r - Lp_s), Ek'_s = beta_s k_s exp(r - Lam_s)); every factor stays finite while
+// |Lam| <= 60 nats (times log2 e in the base-2 units used here).  A chunk beyond that
+// (a channel decaying by more than e^60 within 64 tokens) is marked and its pair is
+// formed token by token by the fp32 kernel instead.
+//
+// Products on tcgen05 with fp32 accumulation, every non-exact operand split into
+// bf16 hi + lo (three products, lo ones first; V is exact bf16: two):
+//   Gram^T [Ck'; Ek'] Aq^T (M = 128, N = 64, K = 128),  P (128 x 64, K = 64),
+//   P Ka (128 x 128) and P Le (128 x 64) (K = 64),  Q V (128 x 128, K = 64).
+// (I + Lc)^-1 is the blocked triangular inverse on CUDA cores.  Lanes of every
+// accumulator are key channels i (or tokens s for the Gram), so each thread of the
+// epilogue owns one row of T_c and S_c.
+#include "dense_common.cuh"
+#include "internal.cuh"
+#include "sm100.cuh"
+
+namespace hypic {
+namespace {
+
+using namespace sm100;
+using dense::kLd;
+using dense::split_pair;
+
+constexpr int kC = 64;
+constexpr int kD = 128;
+constexpr int kBox = kC * 128;                 // 64 channels x 64 tokens, bf16: 8 KB
+constexpr int kThreads = 256;
+constexpr float kMaxLog2 = 60.f * 1.4426950408889634f;   // |Lam| bound, base 2
+
+// shared memory, from the 1024-aligned base
+constexpr int kK = 0;                          // keys: two 64-channel boxes (token rows, 128-byte swizzle)
+constexpr int kV = 2 * kBox;                   // values, the same layout
+constexpr int kG = 4 * kBox;                   // 96 KB, reused phase by phase:
+constexpr int kGa = kG;                        //   Gram A [Ck'; Ek'] hi (per channel half 128 rows x 128 B), lo +32 KB
+constexpr int kGb = kG + 65536;                //   Gram B Aq hi (two boxes), lo +16 KB
+constexpr int kLe = kG;                        //   then Le^T (rows s, t along K) hi, lo +8 KB
+constexpr int kLw = kG + 16384;                //   fp32 Lc, then A = (I + Lc)^-1, then 3 x 256 temporaries
+constexpr int kAw = kLw + kC * kLd * 4;
+constexpr int kTw = kAw + kC * kLd * 4;
+constexpr int kAi = kG + 55296;                //   A (rows s, t along N) hi, lo +8 KB
+constexpr int kP = kG + 16384;                 //   then P (rows i, t along K) hi, lo +16 KB
+constexpr int kQ = kG + 49152;                 //   then Q (rows i, s along K) hi, lo +16 KB
+constexpr int kX = kG + 98304;                 // beta o Ct (token rows, two boxes) hi, lo +16 KB; then Ka
+constexpr int kLam = kX + 32768;               // Lam, base 2, fp32 [65][128]: row 0 zero, row t + 1 = Lam_t
+constexpr int kCtl = kLam + (kC + 1) * kD * 4;
+
+struct Ctl {
+    uint64_t full, mma, drain;
+    float beta[kC];
+    float red[kThreads / 32];
+    uint32_t tmem;
+};
+constexpr int kSmem = kCtl + (int)sizeof(Ctl) + 1024;
+static_assert(kSmem <= 232448, "fits in one SM's shared memory");
+static_assert(kTw + 3 * 256 * 4 <= kAi, "the inverse's temporaries end before the A tiles");
+static_assert(kAi + 16384 <= kX && kQ + 32768 <= kX, "phase tiles stay inside the reused region");
+static_assert(kAi % 1024 == 0 && kP % 1024 == 0 && kQ % 1024 == 0 && kX % 1024 == 0 && kLam % 16 == 0,
+              "operand tiles 1024-byte aligned");
+
+// TMEM columns (256 allocated)
+constexpr uint32_t kTG = 0;     // Gram^T (lanes s / 64 + s), then P Le (64), then Q V (128)
+constexpr uint32_t kTP = 64;    // P
+constexpr uint32_t kTT = 128;   // P Ka
+
+// byte offset of the 16-byte chunk c of row r in a 128-byte-swizzled tile
+__device__ __forceinline__ int swz(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// 8 fp32 values -> bf16 hi / lo 16-byte chunks at dst (lo at dst + lo_off)
+__device__ __forceinline__ void put8(uint8_t *dst, int lo_off, const float (&x)[8]) {
+    uint32_t hv[4], lv[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) split_pair(x[2 * p], x[2 * p + 1], hv[p], lv[p]);
+    *reinterpret_cast<uint4 *>(dst) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+    *reinterpret_cast<uint4 *>(dst + lo_off) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+}
+
+__device__ __forceinline__ void load8(const float *p, float (&x)[8]) {
+    const float4 a = *reinterpret_cast<const float4 *>(p), b = *reinterpret_cast<const float4 *>(p + 4);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
+// Output staging: row i of a 128 x 128 fp32 result (rows 0..63 over the dead Le / P
+// tiles, rows 64..127 over the dead Ka tiles and the first rows of Lam), 132 floats
+// apart so that a warp's 32 rows land in distinct banks; then coalesced 512-byte rows out.
+constexpr int kStg = 132;
+static_assert(kG + 64 * kStg * 4 <= kQ, "staging rows 0..63 end before the Q tiles");
+static_assert(kX + 64 * kStg * 4 <= kCtl, "staging rows 64..127 end before the control block");
+
+__device__ __forceinline__ float *stage_row(uint8_t *smem, int i) {
+    return reinterpret_cast<float *>(smem + (i < 64 ? kG : kX)) + (i & 63) * kStg;
+}
+
+__device__ __forceinline__ void copy_out(uint8_t *smem, float *dst, int tid) {
+#pragma unroll 4
+    for (int f = tid; f < kD * 32; f += kThreads) {
+        const int i = f >> 5, c4 = f & 31;
+        *reinterpret_cast<float4 *>(dst + i * kD + c4 * 4) = *reinterpret_cast<const float4 *>(stage_row(smem, i) + c4 * 4);
+    }
+}
+
+// One elected thread: three split products D (+)= A B over nk k-steps of 16,
+// lo ones first (A_lo B_hi, A_hi B_lo, A_hi B_hi).
+template <typename DescA, typename DescB>
+__device__ __forceinline__ void mma3(uint32_t d, uint32_t idesc, int nk, DescA da, DescB db, bool accumulate) {
+    const int order[3][2] = {{1, 0}, {0, 1}, {0, 0}};
+#pragma unroll
+    for (int p = 0; p < 3; ++p)
+        for (int ks = 0; ks < nk; ++ks)
+            mma_f16(d, da(order[p][0], ks), db(order[p][1], ks), idesc, (accumulate || p > 0 || ks > 0) ? 1u : 0u);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    scan_kda_chunk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                          const ScanArgs a, int64_t slots, float *pool_lam, float *pool_M, float *pool_S,
+                          int *steep) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_align1024(smem_raw);
+    Ctl *ctl = reinterpret_cast<Ctl *>(smem + kCtl);
+    float *lam = reinterpret_cast<float *>(smem + kLam);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h = (int)(blockIdx.x % (unsigned)a.H);
+    const int64_t slot = blockIdx.x / (unsigned)a.H;
+    const int l = blockIdx.y;
+    const int64_t u = ((int64_t)l * slots + slot) * a.H + h;   // pool row of this chunk
+
+    // slot -> (segment, chunk): the last segment s with s + floor(t0_s / 64) <= slot
+    int lo = 0, hi = a.n_seg - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((int64_t)mid + a.seg_offsets[mid] / kC <= slot) lo = mid;
+        else hi = mid - 1;
+    }
+    const int64_t t0 = a.seg_offsets[lo], t1 = a.seg_offsets[lo + 1];
+    const int64_t j = slot - (lo + t0 / kC);
+    if (!(t0 >= 0 && t0 <= t1 && t1 <= a.N) || j < 0 || j * kC >= t1 - t0) {   // no chunk here
+        if (tid == 0) steep[u] = 0;
+        return;
+    }
+    const int64_t c0 = t0 + j * kC;
+    const int nval = (int)min((int64_t)kC, t1 - c0);
+
+    if (tid == 0) {
+        mbar_init(&ctl->full, 1);
+        mbar_init(&ctl->mma, 1);
+        mbar_init(&ctl->drain, 1);
+        mbar_fence_init();
+        mbar_expect_tx(&ctl->full, (uint32_t)(4 * kBox + nval * kD * 4));
+        const int row = (int)((int64_t)l * a.N + c0);
+        tma_load_3d(smem + kK, &tm_k, &ctl->full, 0, h, row);
+        tma_load_3d(smem + kK + kBox, &tm_k, &ctl->full, 64, h, row);
+        tma_load_3d(smem + kV, &tm_v, &ctl->full, 0, h, row);
+        tma_load_3d(smem + kV + kBox, &tm_v, &ctl->full, 64, h, row);
+        // the gates of the chunk's tokens (512 contiguous bytes each) into rows 1..nval of Lam
+        const float *ap = a.alpha + (((int64_t)l * a.N + c0) * a.H + h) * kD;
+        for (int t = 0; t < nval; ++t)
+            bulk_load(smem + kLam + (t + 1) * kD * 4, ap + (int64_t)t * a.H * kD, kD * 4, &ctl->full);
+    }
+    if (warp == 0) tmem_alloc(&ctl->tmem, 256);
+    if (tid >= kD && tid < kD + kC) {
+        const int t = tid - kD;
+        ctl->beta[t] = t < nval ? (a.beta ? a.beta[((int64_t)l * a.N + c0 + t) * a.H + h] : 1.f) : 0.f;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem;
+    bool ok = __syncthreads_and(mbar_wait(&ctl->full, 0));   // the tiles land before any exit
+
+    // ---- gates: Lam (base 2), the prefix over tokens per channel; tokens past the
+    // segment's end get alpha = 1 and beta = 0 (their keys then act on nothing)
+    float mx = 0.f;
+    if (ok) {
+        float4 *g4 = reinterpret_cast<float4 *>(lam + kD);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int f = tid + kThreads * i;   // float4 index: token f / 32
+            const bool v = (f >> 5) < nval;
+            const float4 x = g4[f];
+            g4[f] = v ? make_float4(log2f(x.x), log2f(x.y), log2f(x.z), log2f(x.w)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        if (tid < kD) lam[tid] = 0.f;
+        __syncthreads();
+        const int ch = tid & (kD - 1), part = tid >> 7;   // tokens 32 part .. 32 part + 31
+        float acc = 0.f;
+#pragma unroll 8
+        for (int t = part * 32; t < part * 32 + 32; ++t) {
+            acc += lam[(t + 1) * kD + ch];
+            lam[(t + 1) * kD + ch] = acc;
+        }
+        __syncthreads();
+        const float base = part ? lam[32 * kD + ch] : 0.f;   // Lam_31 of the channel
+#pragma unroll 8
+        for (int t = part * 32; t < part * 32 + 32; ++t) {
+            const float x = lam[(t + 1) * kD + ch] + base;
+            if (part) lam[(t + 1) * kD + ch] = x;
+            mx = fmaxf(mx, fabsf(x));
+        }
+        if (!(mx <= kMaxLog2)) mx = INFINITY;   // a NaN gate counts as steep
+    }
+    const bool is_steep = __syncthreads_or(mx > kMaxLog2);
+    if (tid == 0) steep[u] = (is_steep || !ok) ? 1 : 0;
+    if (is_steep || !ok) {
+        if (!ok && tid == 0 && a.d_err) atomicExch(a.d_err, (int)HYPIC_ETIMEOUT);   // the tiles never came
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) {
+            tc_fence_after();
+            tmem_dealloc(tmem, 256);
+        }
+        return;
+    }
+
+    const uint8_t *kt = smem + kK;
+    // ---- the Gram operands: Aq, Ck', Ek' (bf16 hi / lo, 128-byte swizzle)
+#pragma unroll 1
+    for (int f = tid; f < kC * 16; f += kThreads) {
+        const int t = f >> 4, cc = f & 15, b = cc >> 3, c = cc & 7, ch = cc * 8;
+        const uint4 raw = *reinterpret_cast<const uint4 *>(kt + b * kBox + swz(t, c));
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+        float lp[8], lt[8], rf[8];
+        load8(lam + t * kD + ch, lp);
+        load8(lam + (t + 1) * kD + ch, lt);
+        load8(lam + 32 * kD + ch, rf);
+        const float bt = ctl->beta[t];
+        float aq[8], ck[8], ek[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float kv = (e & 1) ? bf_hi(w[e >> 1]) : bf_lo(w[e >> 1]);
+            aq[e] = kv * exp2f(lp[e] - rf[e]);
+            ck[e] = bt * kv * exp2f(rf[e] - lp[e]);
+            ek[e] = bt * kv * exp2f(rf[e] - lt[e]);
+        }
+        put8(smem + kGb + b * kBox + swz(t, c), 16384, aq);
+        put8(smem + kGa + b * 16384 + swz(t, c), 32768, ck);
+        put8(smem + kGa + b * 16384 + swz(kC + t, c), 32768, ek);
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    uint32_t mma_phase = 0;
+    if (tid == 0) {
+        tc_fence_after();
+        constexpr uint32_t id_g = idesc_bf16_f32(128, 64, false, false);
+        const uint32_t ga = smem_addr(smem + kGa), gb = smem_addr(smem + kGb);
+        mma3(tmem + kTG, id_g, 8,
+             [&](int hl, int ks) {
+                 return smem_desc_sw128(ga + (uint32_t)hl * 32768u + (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u,
+                                        0, 1024);
+             },
+             [&](int hl, int ks) {
+                 return smem_desc_sw128(gb + (uint32_t)hl * 16384u + (uint32_t)(ks >> 2) * kBox + (uint32_t)(ks & 3) * 32u,
+                                        0, 1024);
+             },
+             false);
+        mma_commit(&ctl->mma);
+    }
+    // ---- meanwhile beta o Ct (token rows s, channels along M of P's A operand)
+#pragma unroll 1
+    for (int f = tid; f < kC * 16; f += kThreads) {
+        const int t = f >> 4, cc = f & 15, b = cc >> 3, c = cc & 7, ch = cc * 8;
+        const uint4 raw = *reinterpret_cast<const uint4 *>(kt + b * kBox + swz(t, c));
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+        float lp[8], lc[8];
+        load8(lam + t * kD + ch, lp);
+        load8(lam + kC * kD + ch, lc);
+        const float bt = ctl->beta[t];
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float kv = (e & 1) ? bf_hi(w[e >> 1]) : bf_lo(w[e >> 1]);
+            x[e] = bt * kv * exp2f(lc[e] - lp[e]);
+        }
+        put8(smem + kX + b * kBox + swz(t, c), 16384, x);
+    }
+    ok = __syncthreads_and(mbar_wait(&ctl->mma, mma_phase));
+    mma_phase ^= 1u;
+    tc_fence_after();
+    const int q4 = warp & 3, half = warp >> 2;       // TMEM lane quarter, column half
+    const int m = q4 * 32 + lane;                    // accumulator row of this thread
+    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+    float *Lw = reinterpret_cast<float *>(smem + kLw);
+    float *Aw = reinterpret_cast<float *>(smem + kAw);
+    float *Tw = reinterpret_cast<float *>(smem + kTw);
+
+    if (ok) {
+        // ---- Lc (fp32, for the inverse) and Le^T (bf16 hi / lo) from the Gram, t > s only
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + kTG + (uint32_t)(half * 32), r);
+        tmem_wait_ld();
+        if (q4 < 2) {
+            const int s = m;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int t = half * 32 + i;
+                Lw[t * kLd + s] = t > s ? __uint_as_float(r[i]) : 0.f;
+            }
+        } else {
+            const int s = m - kC;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                float x[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int t = half * 32 + cc * 8 + e;
+                    x[e] = t > s ? __uint_as_float(r[cc * 8 + e]) : 0.f;
+                }
+                put8(smem + kLe + swz(s, half * 4 + cc), 8192, x);
+            }
+        }
+        __syncthreads();
+        dense::tri_inverse<kThreads, 1, true, true>(Lw, Aw, Tw, tid);
+        // ---- A -> bf16 hi / lo (rows s, t contiguous: MN-major B of P)
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int f = tid + kThreads * i;   // 0 .. 511
+            const int s = f >> 3, c = f & 7;
+            float x[8];
+            load8(Aw + s * kLd + c * 8, x);
+            put8(smem + kAi + swz(s, c), 8192, x);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t id_p = idesc_bf16_f32(128, 64, true, true);
+            const uint32_t xb = smem_addr(smem + kX), ab = smem_addr(smem + kAi);
+            mma3(tmem + kTP, id_p, 4,
+                 [&](int hl, int ks) {
+                     return smem_desc_sw128(xb + (uint32_t)hl * 16384u + (uint32_t)ks * 2048u, kBox, 1024);
+                 },
+                 [&](int hl, int ks) {
+                     return smem_desc_sw128(ab + (uint32_t)hl * 8192u + (uint32_t)ks * 2048u, kBox, 1024);
+                 },
+                 false);
+            mma_commit(&ctl->mma);
+        }
+        ok = __syncthreads_and(mbar_wait(&ctl->mma, mma_phase));
+        mma_phase ^= 1u;
+        tc_fence_after();
+    }
+    if (ok) {
+        // ---- P -> bf16 hi / lo (rows i, t along K); Ka over beta o Ct's tiles
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + kTP + (uint32_t)(half * 32), r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(r[cc * 8 + e]);
+            put8(smem + kP + swz(m, half * 4 + cc), 16384, x);
+        }
+#pragma unroll 1
+        for (int f = tid; f < kC * 16; f += kThreads) {
+            const int t = f >> 4, cc = f & 15, b = cc >> 3, c = cc & 7, ch = cc * 8;
+            const uint4 raw = *reinterpret_cast<const uint4 *>(kt + b * kBox + swz(t, c));
+            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+            float lp[8];
+            load8(lam + t * kD + ch, lp);
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float kv = (e & 1) ? bf_hi(w[e >> 1]) : bf_lo(w[e >> 1]);
+                x[e] = kv * exp2f(lp[e]);
+            }
+            put8(smem + kX + b * kBox + swz(t, c), 16384, x);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t id_t = idesc_bf16_f32(128, 128, false, true);
+            constexpr uint32_t id_l = idesc_bf16_f32(128, 64, false, false);
+            const uint32_t pb = smem_addr(smem + kP), xb = smem_addr(smem + kX), lb = smem_addr(smem + kLe);
+            auto pd = [&](int hl, int ks) {
+                return smem_desc_sw128(pb + (uint32_t)hl * 16384u + (uint32_t)ks * 32u, 0, 1024);
+            };
+            mma3(tmem + kTT, id_t, 4, pd,
+                 [&](int hl, int ks) {
+                     return smem_desc_sw128(xb + (uint32_t)hl * 16384u + (uint32_t)ks * 2048u, kBox, 1024);
+                 },
+                 false);
+            mma3(tmem + kTG, id_l, 4, pd,
+                 [&](int hl, int ks) {
+                     return smem_desc_sw128(lb + (uint32_t)hl * 8192u + (uint32_t)ks * 32u, 0, 1024);
+                 },
+                 false);
+            mma_commit(&ctl->mma);
+        }
+        ok = __syncthreads_and(mbar_wait(&ctl->mma, mma_phase));
+        mma_phase ^= 1u;
+        tc_fence_after();
+    }
+    const float ln2 = 0.6931471805599453f;
+    if (ok) {
+        // ---- Q[i][s] = beta_s k_si exp(L_i - Lam_s,i) - (P Le)[i][s] -> bf16 hi / lo
+        const int i = m;
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + kTG + (uint32_t)(half * 32), r);
+        const float lc = lam[kC * kD + i];
+        const uint8_t *kcol = kt + (i >> 6) * kBox + ((i & 7) << 1);
+        const int ci = (i & 63) >> 3;
+        tmem_wait_ld();
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int s = half * 32 + cc * 8 + e;
+                const uint16_t kb = *reinterpret_cast<const uint16_t *>(kcol + swz(s, ci));
+                const float kv = __uint_as_float((uint32_t)kb << 16);
+                x[e] = ctl->beta[s] * kv * exp2f(lc - lam[(s + 1) * kD + i]) - __uint_as_float(r[cc * 8 + e]);
+            }
+            put8(smem + kQ + swz(i, half * 4 + cc), 16384, x);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {   // S_c = Q V (V exact in bf16: Q_lo V, then Q_hi V)
+            tc_fence_after();
+            constexpr uint32_t id_z = idesc_bf16_f32(128, 128, false, true);
+            const uint32_t qb = smem_addr(smem + kQ), vb = smem_addr(smem + kV);
+#pragma unroll
+            for (int hl = 1; hl >= 0; --hl)
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_f16(tmem + kTG, smem_desc_sw128(qb + (uint32_t)hl * 16384u + (uint32_t)ks * 32u, 0, 1024),
+                            smem_desc_sw128(vb + (uint32_t)ks * 2048u, kBox, 1024), id_z,
+                            (hl == 0 || ks > 0) ? 1u : 0u);
+            mma_commit(&ctl->mma);
+        }
+        // ---- T_c = diag(exp(L)) - P Ka, scaled by a power of two to max |M_c| in [1, 2)
+        float tmx = 0.f;
+        const float di = exp2f(lc);
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            tmem_ld32(tmem + lane_off + kTT + (uint32_t)(half * 64 + p * 32), r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const int col = half * 64 + p * 32 + e;
+                tmx = fmaxf(tmx, fabsf((col == i ? di : 0.f) - __uint_as_float(r[e])));
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) tmx = fmaxf(tmx, __shfl_xor_sync(0xffffffffu, tmx, off));
+        if (lane == 0) ctl->red[warp] = tmx;
+        __syncthreads();
+        tmx = 0.f;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) tmx = fmaxf(tmx, ctl->red[w]);
+        const int ex = dense::exponent_of(tmx);
+        const float scl = ldexpf(1.f, -ex);
+        float *row = stage_row(smem, i) + half * 64;
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            tmem_ld32(tmem + lane_off + kTT + (uint32_t)(half * 64 + p * 32), r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+                float4 v;
+                float *vp = &v.x;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int col = half * 64 + p * 32 + e + q;
+                    vp[q] = ((col == i ? di : 0.f) - __uint_as_float(r[e + q])) * scl;
+                }
+                *reinterpret_cast<float4 *>(row + p * 32 + e) = v;
+            }
+        }
+        __syncthreads();
+        copy_out(smem, pool_M + u * (kD * kD), tid);
+        if (tid == 0) pool_lam[u] = (float)ex * ln2;
+        ok = __syncthreads_and(mbar_wait(&ctl->mma, mma_phase));   // S_c done; the staging tiles read
+        tc_fence_after();
+    }
+    if (ok) {
+        // ---- S_c
+        float *row = stage_row(smem, m) + half * 64;
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_off + kTG + (uint32_t)(half * 64 + p * 32), r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+                *reinterpret_cast<float4 *>(row + p * 32 + e) =
+                    make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]),
+                                __uint_as_float(r[e + 3]));
+        }
+        __syncthreads();
+        copy_out(smem, pool_S + u * (kD * kD), tid);
+    } else if (tid == 0) {   // a wait gave up: drain this thread's MMAs, then report
+        mma_commit(&ctl->drain);
+        mbar_wait(&ctl->drain, 0);
+        if (a.d_err) atomicExch(a.d_err, (int)HYPIC_ETIMEOUT);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 256);
+    }
+}
+
+// Per (layer, segment): the first pool row of its chunks and their count; per chunk
+// slot p (and p = slots): the first token of the chunk in that slot, or for a slot no
+// chunk uses, the end of the segment before it -- monotone, so that the chunks form
+// a segment list for the token-by-token kernel.
+__global__ void kda_index_kernel(const ScanArgs a, int64_t slots, int32_t *seg_first, int32_t *chain_len,
+                                 int64_t *voffs) {
+    const int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t R = (int64_t)a.n_layers * a.n_seg;
+    if (x < R) {
+        const int l = (int)(x / a.n_seg), seg = (int)(x % a.n_seg);
+        int64_t t0 = a.seg_offsets[seg], t1 = a.seg_offsets[seg + 1];
+        if (!(t0 >= 0 && t0 <= t1 && t1 <= a.N)) {
+            if (l == 0) flag_index_error(a.d_err);
+            t0 = t1 = 0;
+        }
+        seg_first[x] = (int32_t)((int64_t)l * slots + seg + t0 / kC);
+        chain_len[x] = (int32_t)((t1 - t0 + kC - 1) / kC);
+    }
+    if (x <= slots) {
+        int lo = 0, hi = a.n_seg - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if ((int64_t)mid + a.seg_offsets[mid] / kC <= x) lo = mid;
+            else hi = mid - 1;
+        }
+        const int64_t t0 = a.seg_offsets[lo], t1 = a.seg_offsets[lo + 1];
+        const int64_t j = x - (lo + t0 / kC);
+        voffs[x] = j < 0 ? t0 : (j * kC < t1 - t0 ? t0 + j * kC : t1);
+    }
+}
+
+struct KdaLayout {
+    int64_t slots, P;
+    int64_t M, S, lam, steep, voffs, first, len, total;   // byte offsets
+};
+
+int64_t up256(int64_t b) { return (b + 255) / 256 * 256; }
+
+KdaLayout kda_layout(const ScanArgs &a) {
+    KdaLayout t{};
+    t.slots = (int64_t)a.n_seg + a.N / kC;
+    t.P = (int64_t)a.n_layers * t.slots;
+    const int64_t rows = t.P * a.H;
+    const int64_t R = (int64_t)a.n_layers * a.n_seg;
+    int64_t o = 0;
+    t.M = o;      o += up256(rows * kD * kD * 4);
+    t.S = o;      o += up256(rows * kD * kD * 4);
+    t.lam = o;    o += up256(rows * 4);
+    t.steep = o;  o += up256(rows * 4);
+    t.voffs = o;  o += up256((t.slots + 1) * 8);
+    t.first = o;  o += up256(R * 4);
+    t.len = o;    o += up256(R * 4);
+    t.total = o;
+    return t;
+}
+
+}  // namespace
+
+bool scan_kda_tc_shape(const ScanArgs &a) {
+    if (!(a.fam == HYPIC_KDA && a.in_dtype == HYPIC_BF16 && a.dk == kD && a.dv == kD && a.o_out == nullptr &&
+          a.N > 0 && a.n_layers > 0 && a.n_seg > 0 && a.n_layers <= 65535))
+        return false;
+    const int64_t slots = (int64_t)a.n_seg + a.N / kC;
+    const int64_t rows = (int64_t)a.n_layers * slots * a.H;
+    return (int64_t)a.n_layers * a.N < ((int64_t)1 << 31) && slots * a.H < ((int64_t)1 << 31) &&
+           rows < ((int64_t)1 << 31) && (int64_t)a.n_layers * a.n_seg * a.H < ((int64_t)1 << 30) &&
+           kda_layout(a).total <= kKdaMaxScratch;
+}
+
+bool scan_kda_tc_supported(const ScanArgs &a) { return scan_kda_tc_shape(a) && tensor_map_encoder() != nullptr; }
+
+int64_t scan_kda_tc_bytes(const ScanArgs &a) { return kda_layout(a).total; }
+
+cudaError_t launch_scan_kda_tc(const ScanArgs &a, cudaStream_t s) {
+    const KdaLayout t = kda_layout(a);
+    uint8_t *ws = reinterpret_cast<uint8_t *>(a.ws);
+    float *pM = reinterpret_cast<float *>(ws + t.M), *pS = reinterpret_cast<float *>(ws + t.S);
+    float *plam = reinterpret_cast<float *>(ws + t.lam);
+    int *steep = reinterpret_cast<int *>(ws + t.steep);
+    int64_t *voffs = reinterpret_cast<int64_t *>(ws + t.voffs);
+    int32_t *first = reinterpret_cast<int32_t *>(ws + t.first), *clen = reinterpret_cast<int32_t *>(ws + t.len);
+    const int64_t R = (int64_t)a.n_layers * a.n_seg;
+
+    const int64_t nidx = R > t.slots + 1 ? R : t.slots + 1;
+    kda_index_kernel<<<(unsigned)((nidx + 255) / 256), 256, 0, s>>>(a, t.slots, first, clen, voffs);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    const uint64_t rows = (uint64_t)a.n_layers * (uint64_t)a.N;
+    CUtensorMap mk, mv;
+    if (!make_tensor_map_3d(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.k, kD, a.H, rows, 64, kC,
+                            CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map_3d(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.v, kD, a.H, rows, 64, kC,
+                            CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    e = cudaFuncSetAttribute(scan_kda_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    scan_kda_chunk_kernel<<<dim3((unsigned)(t.slots * a.H), (unsigned)a.n_layers), kThreads, kSmem, s>>>(
+        mk, mv, a, t.slots, plam, pM, pS, steep);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    // chunks too steep for the factored Gram: their pairs token by token (every other
+    // unit of this launch returns at once)
+    ScanArgs f = a;
+    f.n_seg = (int)t.slots;
+    f.seg_offsets = voffs;
+    f.lam_out = plam;
+    f.M_out = pM;
+    f.S_out = pS;
+    f.ws = nullptr;
+    f.unit_mask = steep;
+    e = launch_scan_recurrent(f, s);
+    if (e != cudaSuccess) return e;
+
+    // each segment: its chunks' pairs in order
+    ChainArgs c{};
+    c.fam = HYPIC_DENSE;   // (lambda, M) pairs
+    c.R = (int)R;
+    c.n_layers = 1;
+    c.H = a.H;
+    c.dk = kD;
+    c.dv = kD;
+    c.max_chain = (int)((a.N + kC - 1) / kC);
+    c.P = (int)t.P;
+    c.chain_len = clen;
+    c.seg_idx = nullptr;
+    c.seg_first = first;
+    c.pool_lam = plam;
+    c.pool_M = pM;
+    c.pool_S = pS;
+    c.S_init = nullptr;
+    c.S_out = a.S_out;
+    c.d_err = a.d_err;
+    return launch_compose_prefix(c, a.lam_out, a.M_out, s);
+}
+
+}  // namespace hypic

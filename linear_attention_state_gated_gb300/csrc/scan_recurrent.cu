@@ -81,6 +81,7 @@ __global__ void __launch_bounds__(256, 2) scan_recurrent_kernel(const ScanArgs a
     const int h = unit % a.H;
     const int seg = (unit / a.H) % a.n_seg;
     const int l = unit / (a.H * a.n_seg);
+    if (a.unit_mask && a.unit_mask[unit] == 0) return;   // the whole CTA: nothing to do here
 
     int64_t t0 = a.seg_offsets[seg], t1 = a.seg_offsets[seg + 1];
     if (!(t0 >= 0 && t0 <= t1 && t1 <= a.N)) {

@@ -94,7 +94,8 @@ def scan_ws(lib, fam=2, dtype=0, L=1, S=2, N=64, H=2, dk=128, dv=128, ws=0x40000
 def test_workspace_size_and_checks(lib):
     """The two-pass dense scan: one 49424-byte record (50192 with o_t) per
     (layer, head, chunk slot), n_seg + N / 64 slots, then the segments' order
-    (int32 each), both 256-byte aligned; the balanced
+    (int32 each), both 256-byte aligned; the chunked KDA scan: a pair per
+    (layer, chunk slot, head) and its index arrays; the balanced
     diagonal scan: a fixed 2 x 512 partial slots; other options take none."""
     ws = lib.hypic_segment_scan_workspace_bytes
     up = lambda b: (b + 255) // 256 * 256   # noqa: E731
@@ -106,7 +107,17 @@ def test_workspace_size_and_checks(lib):
     assert ws(2, 0, 1, 3, 200, 2, 128, 128, 0) == dense(1, 3, 200, 2, 49424)
     assert ws(2, 0, 1, 1, 2048, 2, 128, 128, 1) == dense(1, 1, 2048, 2, 50192)   # with o_t: Gq tiles and b_t too
     assert ws(2, 1, 1, 1, 2048, 2, 128, 128, 0) == 0     # fp32 inputs
-    assert ws(3, 0, 1, 1, 2048, 2, 128, 128, 0) == 0     # KDA: the token-by-token kernel
+    def kda(L, n_seg, N, H):   # per chunk slot: M_c, S_c (fp32), lambda, steep flag; slot starts; chains
+        slots = n_seg + N // 64
+        rows = L * slots * H
+        return (2 * up(rows * 128 * 128 * 4) + 2 * up(rows * 4) + up((slots + 1) * 8) + 2 * up(L * n_seg * 4))
+
+    assert ws(3, 0, 30, 1, 2048, 32, 128, 128, 0) == kda(30, 1, 2048, 32)   # KDA: chunk pairs, then chains
+    assert ws(3, 0, 2, 7, 592, 3, 128, 128, 0) == kda(2, 7, 592, 3)
+    assert ws(3, 0, 1, 1, 2048, 2, 128, 128, 1) == 0     # KDA with o_t: the token-by-token kernel
+    assert ws(3, 1, 1, 1, 2048, 2, 128, 128, 0) == 0     # ... fp32 inputs too
+    assert ws(3, 0, 1, 1, 2048, 2, 64, 64, 0) == 0
+    assert ws(3, 0, 30, 2000, 1 << 20, 32, 128, 128, 0) == 0   # above 64 GiB of pairs: token by token
     assert ws(2, 0, 1, 1, 2048, 2, 64, 64, 0) == 0
     sd = 2 * 512 * (128 + 128 * 128) * 4      # diag: two partial slots per CTA, up to 512 CTAs
     assert ws(1, 0, 1, 1, 2048, 2, 128, 128, 0) == sd

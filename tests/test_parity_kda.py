@@ -150,3 +150,51 @@ def test_kda_scan_full_size_sampled():
         assert rel_fro(S[l:l + 1, :, h:h + 1], ref["S"]).max() <= TOL_SCAN_BF16, (l, h)
         assert t_err(2, lam[l:l + 1, :, h:h + 1], ref["lam"], M[l:l + 1, :, h:h + 1], ref["M"]).max() \
             <= TOL_SCAN_BF16, (l, h)
+
+
+def test_kda_chunked_tensor_core_scan_ragged():
+    """The chunked tensor-core form (d = 128, bf16, no o_t): ragged segments with
+    an empty one, a one-token one and exact multiples of the chunk, against the oracle."""
+    lens = [70, 0, 129, 1, 200, 64, 128]
+    w = wl.kda_stack(lengths=lens, n_layers=2, H=3, d=128, seed=92)
+    ref = oracle.segment_scan(KDA, w["k"], w["v"], w["alpha"], w["seg_offsets"], beta=w["beta"])
+    got = gpu_scan(w)
+    err_s = rel_fro(to_host(got["S"]), ref["S"])
+    err_t = t_err(2, to_host(got["lam"]), ref["lam"], to_host(got["M"]), ref["M"])
+    print(f"chunked KDA scan: S error max {err_s.max():.3e}, T error max {err_t.max():.3e}")
+    assert err_s.max() <= TOL_SCAN_BF16 and err_t.max() <= TOL_SCAN_BF16
+    mx = np.abs(to_host(got["M"])).max(axis=(-2, -1))
+    assert np.all((mx >= 1) & (mx < 2))
+    assert np.all(to_host(got["S"])[:, 1] == 0) and np.all(to_host(got["lam"])[:, 1] == 0)
+    assert np.array_equal(to_host(got["M"])[0, 1, 0], np.eye(128))
+
+
+def test_kda_chunked_scan_steep_channels():
+    """Channels that decay by more than e^60 inside a chunk send that chunk's pair
+    to the token-by-token kernel; mixed with ordinary chunks the result still
+    matches the oracle."""
+    lens = [150, 300, 40]
+    w = wl.kda_stack(lengths=lens, n_layers=1, H=2, d=128, seed=93)
+    alpha = w["alpha"].copy()
+    # head 0: channels 0..7 forget fast (alpha = 0.05, ln = -3 a token) on tokens 100..229
+    alpha[:, 100:230, 0, :8] = np.float32(0.05)
+    w = dict(w, alpha=alpha)
+    ref = oracle.segment_scan(KDA, w["k"], w["v"], w["alpha"], w["seg_offsets"], beta=w["beta"])
+    got = gpu_scan(w)
+    assert rel_fro(to_host(got["S"]), ref["S"]).max() <= TOL_SCAN_BF16
+    assert t_err(2, to_host(got["lam"]), ref["lam"], to_host(got["M"]), ref["M"]).max() <= TOL_SCAN_BF16
+
+
+def test_kda_chunked_scan_uses_scratch_and_matches_token_kernel():
+    """The workspace form takes the chunked path (positive scratch); without a
+    workspace the token-by-token kernel runs; both agree within the scan tolerance."""
+    import torch
+    import linear_attention_state_gated_gb300 as hy
+    w = wl.kda_stack(lengths=[500, 260], n_layers=2, H=2, d=128, seed=94)
+    assert hy.segment_scan_workspace_bytes(KDA, torch.bfloat16, 2, 2, 760, 2, 128, 128) > 0
+    a = gpu_scan(w)
+    dev = lambda x: to_dev(x)   # noqa: E731
+    b = hy.segment_scan(KDA, dev(w["k"]).to(torch.bfloat16), dev(w["v"]).to(torch.bfloat16), dev(w["alpha"]),
+                        to_dev(w["seg_offsets"]), beta=dev(w["beta"]), workspace=None)
+    assert rel_fro(to_host(a["S"]), to_host(b["S"])).max() <= TOL_SCAN_BF16
+    assert t_err(2, to_host(a["lam"]), to_host(b["lam"]), to_host(a["M"]), to_host(b["M"])).max() <= TOL_SCAN_BF16
