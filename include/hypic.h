@@ -96,7 +96,8 @@ typedef enum { HYPIC_BF16 = 0, HYPIC_F32 = 1 } hypic_dtype;
  * An empty segment yields lambda = 0, M = I, S = 0.
  * Alignment: q, k, v, o_out, S_out, M_out, the diag / kda alpha and the diag
  * lambda must be 16-byte aligned; other pointers 4-byte (seg_offsets 8-byte).
- * The KDA family runs on the token-by-token fp32 kernel (CUDA cores).
+ * Without a workspace the KDA family runs on the token-by-token fp32 kernel
+ * (CUDA cores); hypic_segment_scan_ws takes it to the tensor cores.
  */
 int hypic_segment_scan(int fam, int in_dtype, int n_layers, int n_seg,
                        int64_t total_tokens, int n_heads, int d_k, int d_v,
@@ -118,7 +119,13 @@ int hypic_segment_scan(int fam, int in_dtype, int n_layers, int n_seg,
  *   the diagonal family without o_t and with n_seg <= 512: 2 x 512 partial
  *     states of 66048 bytes (67.6 MB), for a schedule that spreads all
  *     segments' chunks evenly over the GPU and then folds the pieces of
- *     segments split between CTAs with the composition rule.
+ *     segments split between CTAs with the composition rule;
+ *   the KDA family without o_t: per (layer, 64-token chunk slot, head) the
+ *     chunk's pair (M_c, S_c: 2 x 65536 bytes, lambda_c and a flag: 2 x 4
+ *     bytes), n_layers * (n_seg + total_tokens / 64) * n_heads of them, then
+ *     n_seg + total_tokens / 64 + 1 int64 chunk starts and 2 x n_layers * n_seg
+ *     int32 (each segment's first pair and count), each part rounded up to 256
+ *     bytes; above 64 GiB the token-by-token kernel is used and this is 0.
  */
 int64_t hypic_segment_scan_workspace_bytes(int fam, int in_dtype, int n_layers, int n_seg,
                                            int64_t total_tokens, int n_heads, int d_k, int d_v,
@@ -138,8 +145,12 @@ int64_t hypic_segment_scan_workspace_bytes(int fam, int in_dtype, int n_layers, 
  * chunks, then the ordered state pass (the chunked WY/UT form of the gated
  * delta rule; the pages give no chunked algorithm); the diagonal scan balances
  * its work over the GPU (results equal to hypic_segment_scan's up to rounding;
- * they depend on the batch's total work, not on a segment's position).  Other
- * cases run exactly as hypic_segment_scan.
+ * they depend on the batch's total work, not on a segment's position); the KDA
+ * scan forms every 64-token chunk's pair (T_c, S(c|0)) on the tensor cores in
+ * parallel (a chunk in which a channel decays by more than e^60 token by token)
+ * and composes each segment's chunk pairs in order, T(C1.C2) = T(C2) T(C1)
+ * (xix.ai/fr, paragraph on linear layers).  Other cases run exactly as
+ * hypic_segment_scan.
  */
 int hypic_segment_scan_ws(int fam, int in_dtype, int n_layers, int n_seg,
                           int64_t total_tokens, int n_heads, int d_k, int d_v,

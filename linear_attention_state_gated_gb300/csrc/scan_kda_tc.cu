@@ -47,43 +47,53 @@ using dense::split_pair;
 constexpr int kC = 64;
 constexpr int kD = 128;
 constexpr int kBox = kC * 128;                 // 64 channels x 64 tokens, bf16: 8 KB
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
+constexpr int kCG = kThreads / 128;            // warps per TMEM lane quarter (column groups)
+constexpr int kW64 = 64 / kCG;                 // columns of a 64-column accumulator per warp
+constexpr int kW128 = 128 / kCG;
+constexpr int kParts = kThreads / 128;         // token parts of the per-channel prefix
+static_assert(kW64 == 16 || kW64 == 32, "a warp reads 16 or 32 columns of a 64-column accumulator");
 constexpr float kMaxLog2 = 60.f * 1.4426950408889634f;   // |Lam| bound, base 2
 
 // shared memory, from the 1024-aligned base
-constexpr int kK = 0;                          // keys: two 64-channel boxes (token rows, 128-byte swizzle)
+constexpr int kK = 0;                          // keys (token rows, two 64-channel boxes, 128-byte swizzle);
+                                               // after the Gram: Le^T (rows s, t along K) hi, lo +8 KB
 constexpr int kV = 2 * kBox;                   // values, the same layout
-constexpr int kG = 4 * kBox;                   // 96 KB, reused phase by phase:
-constexpr int kGa = kG;                        //   Gram A [Ck'; Ek'] hi (per channel half 128 rows x 128 B), lo +32 KB
-constexpr int kGb = kG + 65536;                //   Gram B Aq hi (two boxes), lo +16 KB
-constexpr int kLe = kG;                        //   then Le^T (rows s, t along K) hi, lo +8 KB
-constexpr int kLw = kG + 16384;                //   fp32 Lc, then A = (I + Lc)^-1, then 3 x 256 temporaries
+constexpr int kG = 4 * kBox;                   // the Gram operands, kept until Q is built:
+constexpr int kGa = kG;                        //   [Ck'; Ek'] hi: channel half b is the 128-row tile at
+                                               //   kGa + 16384 b (rows 0..63 Ck', 64..127 Ek'); lo +32 KB
+constexpr int kGb = kG + 65536;                //   Aq hi (two boxes), lo +16 KB
+constexpr int kX = kG + 98304;                 // fp32 Lc, A = (I + Lc)^-1 and temporaries; then P hi, lo +16 KB
+constexpr int kLw = kX;
 constexpr int kAw = kLw + kC * kLd * 4;
 constexpr int kTw = kAw + kC * kLd * 4;
-constexpr int kAi = kG + 55296;                //   A (rows s, t along N) hi, lo +8 KB
-constexpr int kP = kG + 16384;                 //   then P (rows i, t along K) hi, lo +16 KB
-constexpr int kQ = kG + 49152;                 //   then Q (rows i, s along K) hi, lo +16 KB
-constexpr int kX = kG + 98304;                 // beta o Ct (token rows, two boxes) hi, lo +16 KB; then Ka
-constexpr int kLam = kX + 32768;               // Lam, base 2, fp32 [65][128]: row 0 zero, row t + 1 = Lam_t
+constexpr int kLam = kX + 32768;               // Lam, base 2, fp32 [65][128] (row 0 zero, row t + 1 = Lam_t)
+                                               // while the Gram operands are built; then A's tiles, then Q
+constexpr int kAi = kLam + 6144;               //   A (rows s, t along N) hi, lo +8 KB
+constexpr int kQ = kLam;                       //   Q (rows i, s along K) hi, lo +16 KB
 constexpr int kCtl = kLam + (kC + 1) * kD * 4;
+constexpr int kStM = kG;                       // M_c staged for the TMA store: four 16 KB boxes of 32 columns
+constexpr int kStS = kG + 65536;               // S_c staged likewise
 
 struct Ctl {
-    uint64_t full, mma, drain;
+    uint64_t full, mma, tdone, drain;
     float beta[kC];
+    float eLr[kD];     // exp(L - r) per channel
+    float er[kD];      // exp(r)
+    float eL[kD];      // exp(L)
     float red[kThreads / 32];
     uint32_t tmem;
 };
 constexpr int kSmem = kCtl + (int)sizeof(Ctl) + 1024;
 static_assert(kSmem <= 232448, "fits in one SM's shared memory");
-static_assert(kTw + 3 * 256 * 4 <= kAi, "the inverse's temporaries end before the A tiles");
-static_assert(kAi + 16384 <= kX && kQ + 32768 <= kX, "phase tiles stay inside the reused region");
-static_assert(kAi % 1024 == 0 && kP % 1024 == 0 && kQ % 1024 == 0 && kX % 1024 == 0 && kLam % 16 == 0,
-              "operand tiles 1024-byte aligned");
+static_assert(kTw + 3 * 256 * 4 <= kAi, "the inverse's temporaries end before A's tiles");
+static_assert(kAi + 16384 <= kCtl && kQ + 32768 <= kCtl && kStS + 65536 <= kLam, "tiles inside their regions");
+static_assert(kAi % 1024 == 0 && kQ % 1024 == 0 && kX % 1024 == 0 && kStS % 1024 == 0, "tiles 1024-byte aligned");
 
 // TMEM columns (256 allocated)
 constexpr uint32_t kTG = 0;     // Gram^T (lanes s / 64 + s), then P Le (64), then Q V (128)
-constexpr uint32_t kTP = 64;    // P
-constexpr uint32_t kTT = 128;   // P Ka
+constexpr uint32_t kTP = 64;    // Ck'^T A (P before its row scale)
+constexpr uint32_t kTT = 128;   // P Aq (P Ka before its column scale)
 
 // byte offset of the 16-byte chunk c of row r in a 128-byte-swizzled tile
 __device__ __forceinline__ int swz(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
@@ -105,40 +115,34 @@ __device__ __forceinline__ void load8(const float *p, float (&x)[8]) {
     x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
 }
 
-// Output staging: row i of a 128 x 128 fp32 result (rows 0..63 over the dead Le / P
-// tiles, rows 64..127 over the dead Ka tiles and the first rows of Lam), 132 floats
-// apart so that a warp's 32 rows land in distinct banks; then coalesced 512-byte rows out.
-constexpr int kStg = 132;
-static_assert(kG + 64 * kStg * 4 <= kQ, "staging rows 0..63 end before the Q tiles");
-static_assert(kX + 64 * kStg * 4 <= kCtl, "staging rows 64..127 end before the control block");
-
-__device__ __forceinline__ float *stage_row(uint8_t *smem, int i) {
-    return reinterpret_cast<float *>(smem + (i < 64 ? kG : kX)) + (i & 63) * kStg;
+// 4 values of row r, columns 4 c4 .. 4 c4 + 3 of a staged 128 x 128 fp32 result:
+// box c4 / 8 (32 columns), chunk c4 % 8 of the 128-byte-swizzled row
+__device__ __forceinline__ void stage4(uint8_t *st, int r, int c4, float4 v) {
+    *reinterpret_cast<float4 *>(st + (c4 >> 3) * 16384 + swz(r, c4 & 7)) = v;
 }
 
-__device__ __forceinline__ void copy_out(uint8_t *smem, float *dst, int tid) {
-#pragma unroll 4
-    for (int f = tid; f < kD * 32; f += kThreads) {
-        const int i = f >> 5, c4 = f & 31;
-        *reinterpret_cast<float4 *>(dst + i * kD + c4 * 4) = *reinterpret_cast<const float4 *>(stage_row(smem, i) + c4 * 4);
-    }
+// W (16 or 32) consecutive columns of the warp's 32 lanes
+template <int W> __device__ __forceinline__ void tmem_ldw(uint32_t taddr, uint32_t (&r)[W]) {
+    if constexpr (W == 32) tmem_ld32(taddr, r);
+    else tmem_ld16(taddr, r);
 }
 
 // One elected thread: three split products D (+)= A B over nk k-steps of 16,
 // lo ones first (A_lo B_hi, A_hi B_lo, A_hi B_hi).
 template <typename DescA, typename DescB>
-__device__ __forceinline__ void mma3(uint32_t d, uint32_t idesc, int nk, DescA da, DescB db, bool accumulate) {
+__device__ __forceinline__ void mma3(uint32_t d, uint32_t idesc, int nk, DescA da, DescB db) {
     const int order[3][2] = {{1, 0}, {0, 1}, {0, 0}};
 #pragma unroll
     for (int p = 0; p < 3; ++p)
         for (int ks = 0; ks < nk; ++ks)
-            mma_f16(d, da(order[p][0], ks), db(order[p][1], ks), idesc, (accumulate || p > 0 || ks > 0) ? 1u : 0u);
+            mma_f16(d, da(order[p][0], ks), db(order[p][1], ks), idesc, (p > 0 || ks > 0) ? 1u : 0u);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     scan_kda_chunk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                          const ScanArgs a, int64_t slots, float *pool_lam, float *pool_M, float *pool_S,
-                          int *steep) {
+                          const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_m,
+                          const __grid_constant__ CUtensorMap tm_s, const ScanArgs a, int64_t slots,
+                          float *pool_lam, int *steep) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_align1024(smem_raw);
     Ctl *ctl = reinterpret_cast<Ctl *>(smem + kCtl);
@@ -168,18 +172,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         mbar_init(&ctl->full, 1);
         mbar_init(&ctl->mma, 1);
+        mbar_init(&ctl->tdone, 1);
         mbar_init(&ctl->drain, 1);
         mbar_fence_init();
-        mbar_expect_tx(&ctl->full, (uint32_t)(4 * kBox + nval * kD * 4));
+        mbar_expect_tx(&ctl->full, (uint32_t)(4 * kBox + kC * kD * 4));
         const int row = (int)((int64_t)l * a.N + c0);
         tma_load_3d(smem + kK, &tm_k, &ctl->full, 0, h, row);
         tma_load_3d(smem + kK + kBox, &tm_k, &ctl->full, 64, h, row);
         tma_load_3d(smem + kV, &tm_v, &ctl->full, 0, h, row);
         tma_load_3d(smem + kV + kBox, &tm_v, &ctl->full, 64, h, row);
-        // the gates of the chunk's tokens (512 contiguous bytes each) into rows 1..nval of Lam
-        const float *ap = a.alpha + (((int64_t)l * a.N + c0) * a.H + h) * kD;
-        for (int t = 0; t < nval; ++t)
-            bulk_load(smem + kLam + (t + 1) * kD * 4, ap + (int64_t)t * a.H * kD, kD * 4, &ctl->full);
+        tma_load_3d(smem + kLam + kD * 4, &tm_a, &ctl->full, 0, h, row);   // alpha: rows 1..64 of Lam
     }
     if (warp == 0) tmem_alloc(&ctl->tmem, 256);
     if (tid >= kD && tid < kD + kC) {
@@ -198,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
         float4 *g4 = reinterpret_cast<float4 *>(lam + kD);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < kC * kD / 4 / kThreads; ++i) {
             const int f = tid + kThreads * i;   // float4 index: token f / 32
             const bool v = (f >> 5) < nval;
             const float4 x = g4[f];
@@ -206,17 +208,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (tid < kD) lam[tid] = 0.f;
         __syncthreads();
-        const int ch = tid & (kD - 1), part = tid >> 7;   // tokens 32 part .. 32 part + 31
+        constexpr int kTok = kC / kParts;                  // tokens of a part
+        const int ch = tid & (kD - 1), part = tid >> 7;   // tokens kTok part .. kTok part + kTok - 1
         float acc = 0.f;
 #pragma unroll 8
-        for (int t = part * 32; t < part * 32 + 32; ++t) {
+        for (int t = part * kTok; t < part * kTok + kTok; ++t) {
             acc += lam[(t + 1) * kD + ch];
             lam[(t + 1) * kD + ch] = acc;
         }
         __syncthreads();
-        const float base = part ? lam[32 * kD + ch] : 0.f;   // Lam_31 of the channel
+        float base = 0.f;   // the totals of the earlier parts
+        for (int q = 0; q < part; ++q) base += lam[(q + 1) * kTok * kD + ch];
+        __syncthreads();
 #pragma unroll 8
-        for (int t = part * 32; t < part * 32 + 32; ++t) {
+        for (int t = part * kTok; t < part * kTok + kTok; ++t) {
             const float x = lam[(t + 1) * kD + ch] + base;
             if (part) lam[(t + 1) * kD + ch] = x;
             mx = fmaxf(mx, fabsf(x));
@@ -235,18 +240,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return;
     }
+    if (tid < kD) {   // per-channel factors of the scales below (r = Lam_31, L = Lam_63)
+        const float r = lam[32 * kD + tid], L = lam[kC * kD + tid];
+        ctl->eLr[tid] = exp2f(L - r);
+        ctl->er[tid] = exp2f(r);
+        ctl->eL[tid] = exp2f(L);
+    }
 
+    // ---- the Gram operands (bf16 hi / lo, 128-byte swizzle): Aq_t = k_t e^(Lp_t - r),
+    // Ck'_s = beta_s k_s e^(r - Lp_s), Ek'_s = beta_s k_s e^(r - Lam_s).  They are kept:
+    // beta o Ct = Ck' diag(e^(L - r)), Ka = Aq diag(e^r), beta o Et = Ek' diag(e^(L - r)).
     const uint8_t *kt = smem + kK;
-    // ---- the Gram operands: Aq, Ck', Ek' (bf16 hi / lo, 128-byte swizzle)
 #pragma unroll 1
     for (int f = tid; f < kC * 16; f += kThreads) {
-        const int t = f >> 4, cc = f & 15, b = cc >> 3, c = cc & 7, ch = cc * 8;
+        const int t = f >> 4, cc = f & 15, b = cc >> 3, c = cc & 7, chn = cc * 8;
         const uint4 raw = *reinterpret_cast<const uint4 *>(kt + b * kBox + swz(t, c));
         const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
         float lp[8], lt[8], rf[8];
-        load8(lam + t * kD + ch, lp);
-        load8(lam + (t + 1) * kD + ch, lt);
-        load8(lam + 32 * kD + ch, rf);
+        load8(lam + t * kD + chn, lp);
+        load8(lam + (t + 1) * kD + chn, lt);
+        load8(lam + 32 * kD + chn, rf);
         const float bt = ctl->beta[t];
         float aq[8], ck[8], ek[8];
 #pragma unroll
@@ -264,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     uint32_t mma_phase = 0;
-    if (tid == 0) {
+    if (tid == 0) {   // Gram^T = [Ck'; Ek'] Aq^T (M = 128, N = 64, K = 128)
         tc_fence_after();
         constexpr uint32_t id_g = idesc_bf16_f32(128, 64, false, false);
         const uint32_t ga = smem_addr(smem + kGa), gb = smem_addr(smem + kGb);
@@ -276,32 +289,13 @@ __global__ void __launch_bounds__(kThreads, 1)
              [&](int hl, int ks) {
                  return smem_desc_sw128(gb + (uint32_t)hl * 16384u + (uint32_t)(ks >> 2) * kBox + (uint32_t)(ks & 3) * 32u,
                                         0, 1024);
-             },
-             false);
+             });
         mma_commit(&ctl->mma);
-    }
-    // ---- meanwhile beta o Ct (token rows s, channels along M of P's A operand)
-#pragma unroll 1
-    for (int f = tid; f < kC * 16; f += kThreads) {
-        const int t = f >> 4, cc = f & 15, b = cc >> 3, c = cc & 7, ch = cc * 8;
-        const uint4 raw = *reinterpret_cast<const uint4 *>(kt + b * kBox + swz(t, c));
-        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-        float lp[8], lc[8];
-        load8(lam + t * kD + ch, lp);
-        load8(lam + kC * kD + ch, lc);
-        const float bt = ctl->beta[t];
-        float x[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float kv = (e & 1) ? bf_hi(w[e >> 1]) : bf_lo(w[e >> 1]);
-            x[e] = bt * kv * exp2f(lc[e] - lp[e]);
-        }
-        put8(smem + kX + b * kBox + swz(t, c), 16384, x);
     }
     ok = __syncthreads_and(mbar_wait(&ctl->mma, mma_phase));
     mma_phase ^= 1u;
     tc_fence_after();
-    const int q4 = warp & 3, half = warp >> 2;       // TMEM lane quarter, column half
+    const int q4 = warp & 3, cg = warp >> 2;         // TMEM lane quarter, column group
     const int m = q4 * 32 + lane;                    // accumulator row of this thread
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     float *Lw = reinterpret_cast<float *>(smem + kLw);
@@ -309,36 +303,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *Tw = reinterpret_cast<float *>(smem + kTw);
 
     if (ok) {
-        // ---- Lc (fp32, for the inverse) and Le^T (bf16 hi / lo) from the Gram, t > s only
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_off + kTG + (uint32_t)(half * 32), r);
+        // ---- Lc (fp32, for the inverse) and Le^T (bf16 hi / lo, over the keys) from the
+        // Gram, t > s only
+        uint32_t r[kW64];
+        tmem_ldw<kW64>(tmem + lane_off + kTG + (uint32_t)(cg * kW64), r);
         tmem_wait_ld();
         if (q4 < 2) {
             const int s = m;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int t = half * 32 + i;
+            for (int i = 0; i < kW64; ++i) {
+                const int t = cg * kW64 + i;
                 Lw[t * kLd + s] = t > s ? __uint_as_float(r[i]) : 0.f;
             }
         } else {
             const int s = m - kC;
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
+            for (int cc = 0; cc < kW64 / 8; ++cc) {
                 float x[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const int t = half * 32 + cc * 8 + e;
+                    const int t = cg * kW64 + cc * 8 + e;
                     x[e] = t > s ? __uint_as_float(r[cc * 8 + e]) : 0.f;
                 }
-                put8(smem + kLe + swz(s, half * 4 + cc), 8192, x);
+                put8(smem + kK + swz(s, cg * (kW64 / 8) + cc), 8192, x);
             }
         }
         __syncthreads();
         dense::tri_inverse<kThreads, 1, true, true>(Lw, Aw, Tw, tid);
-        // ---- A -> bf16 hi / lo (rows s, t contiguous: MN-major B of P)
+        // ---- A -> bf16 hi / lo (rows s, t contiguous: the MN-major B of Ck'^T A)
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const int f = tid + kThreads * i;   // 0 .. 511
+        for (int i = 0; i < kC * 8 / kThreads; ++i) {
+            const int f = tid + kThreads * i;
             const int s = f >> 3, c = f & 7;
             float x[8];
             load8(Aw + s * kLd + c * 8, x);
@@ -347,18 +342,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        if (tid == 0) {
+        if (tid == 0) {   // Ck'^T A (M = 128 channels, N = 64, K = 64): Ck' read MN-major from the Gram tile
             tc_fence_after();
             constexpr uint32_t id_p = idesc_bf16_f32(128, 64, true, true);
-            const uint32_t xb = smem_addr(smem + kX), ab = smem_addr(smem + kAi);
+            const uint32_t ga = smem_addr(smem + kGa), ab = smem_addr(smem + kAi);
             mma3(tmem + kTP, id_p, 4,
                  [&](int hl, int ks) {
-                     return smem_desc_sw128(xb + (uint32_t)hl * 16384u + (uint32_t)ks * 2048u, kBox, 1024);
+                     return smem_desc_sw128(ga + (uint32_t)hl * 32768u + (uint32_t)ks * 2048u, 16384, 1024);
                  },
                  [&](int hl, int ks) {
-                     return smem_desc_sw128(ab + (uint32_t)hl * 8192u + (uint32_t)ks * 2048u, kBox, 1024);
-                 },
-                 false);
+                     return smem_desc_sw128(ab + (uint32_t)hl * 8192u + (uint32_t)ks * 2048u, 8192, 1024);
+                 });
             mma_commit(&ctl->mma);
         }
         ok = __syncthreads_and(mbar_wait(&ctl->mma, mma_phase));
@@ -366,54 +360,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
     }
     if (ok) {
-        // ---- P -> bf16 hi / lo (rows i, t along K); Ka over beta o Ct's tiles
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_off + kTP + (uint32_t)(half * 32), r);
+        // ---- P = diag(e^(L - r)) Ck'^T A -> bf16 hi / lo (rows i, t along K)
+        uint32_t r[kW64];
+        tmem_ldw<kW64>(tmem + lane_off + kTP + (uint32_t)(cg * kW64), r);
+        const float sc = ctl->eLr[m];
         tmem_wait_ld();
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < kW64 / 8; ++cc) {
             float x[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(r[cc * 8 + e]);
-            put8(smem + kP + swz(m, half * 4 + cc), 16384, x);
-        }
-#pragma unroll 1
-        for (int f = tid; f < kC * 16; f += kThreads) {
-            const int t = f >> 4, cc = f & 15, b = cc >> 3, c = cc & 7, ch = cc * 8;
-            const uint4 raw = *reinterpret_cast<const uint4 *>(kt + b * kBox + swz(t, c));
-            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-            float lp[8];
-            load8(lam + t * kD + ch, lp);
-            float x[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float kv = (e & 1) ? bf_hi(w[e >> 1]) : bf_lo(w[e >> 1]);
-                x[e] = kv * exp2f(lp[e]);
-            }
-            put8(smem + kX + b * kBox + swz(t, c), 16384, x);
+            for (int e = 0; e < 8; ++e) x[e] = sc * __uint_as_float(r[cc * 8 + e]);
+            put8(smem + kX + swz(m, cg * (kW64 / 8) + cc), 16384, x);
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        if (tid == 0) {
+        if (tid == 0) {   // P Le first (Q waits on it), then P Aq (the epilogue of T_c)
             tc_fence_after();
             constexpr uint32_t id_t = idesc_bf16_f32(128, 128, false, true);
             constexpr uint32_t id_l = idesc_bf16_f32(128, 64, false, false);
-            const uint32_t pb = smem_addr(smem + kP), xb = smem_addr(smem + kX), lb = smem_addr(smem + kLe);
+            const uint32_t pb = smem_addr(smem + kX), gb = smem_addr(smem + kGb), lb = smem_addr(smem + kK);
             auto pd = [&](int hl, int ks) {
                 return smem_desc_sw128(pb + (uint32_t)hl * 16384u + (uint32_t)ks * 32u, 0, 1024);
             };
-            mma3(tmem + kTT, id_t, 4, pd,
-                 [&](int hl, int ks) {
-                     return smem_desc_sw128(xb + (uint32_t)hl * 16384u + (uint32_t)ks * 2048u, kBox, 1024);
-                 },
-                 false);
-            mma3(tmem + kTG, id_l, 4, pd,
-                 [&](int hl, int ks) {
-                     return smem_desc_sw128(lb + (uint32_t)hl * 8192u + (uint32_t)ks * 32u, 0, 1024);
-                 },
-                 false);
+            mma3(tmem + kTG, id_l, 4, pd, [&](int hl, int ks) {
+                return smem_desc_sw128(lb + (uint32_t)hl * 8192u + (uint32_t)ks * 32u, 0, 1024);
+            });
             mma_commit(&ctl->mma);
+            mma3(tmem + kTT, id_t, 4, pd, [&](int hl, int ks) {
+                return smem_desc_sw128(gb + (uint32_t)hl * 16384u + (uint32_t)ks * 2048u, kBox, 1024);
+            });
+            mma_commit(&ctl->tdone);
         }
         ok = __syncthreads_and(mbar_wait(&ctl->mma, mma_phase));
         mma_phase ^= 1u;
@@ -421,25 +398,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const float ln2 = 0.6931471805599453f;
     if (ok) {
-        // ---- Q[i][s] = beta_s k_si exp(L_i - Lam_s,i) - (P Le)[i][s] -> bf16 hi / lo
+        // ---- Q[i][s] = e^(L_i - r_i) Ek'[s][i] - (P Le)[i][s] -> bf16 hi / lo (rows i, s along K)
         const int i = m;
         uint32_t r[32];
-        tmem_ld32(tmem + lane_off + kTG + (uint32_t)(half * 32), r);
-        const float lc = lam[kC * kD + i];
-        const uint8_t *kcol = kt + (i >> 6) * kBox + ((i & 7) << 1);
+        tmem_ldw<kW64>(tmem + lane_off + kTG + (uint32_t)(cg * kW64), *reinterpret_cast<uint32_t(*)[kW64]>(r));
+        const float sc = ctl->eLr[i];
+        const uint8_t *ecol = smem + kGa + (i >> 6) * 16384 + ((i & 7) << 1);   // Ek' rows 64 + s
         const int ci = (i & 63) >> 3;
         tmem_wait_ld();
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < kW64 / 8; ++cc) {
             float x[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                const int s = half * 32 + cc * 8 + e;
-                const uint16_t kb = *reinterpret_cast<const uint16_t *>(kcol + swz(s, ci));
-                const float kv = __uint_as_float((uint32_t)kb << 16);
-                x[e] = ctl->beta[s] * kv * exp2f(lc - lam[(s + 1) * kD + i]) - __uint_as_float(r[cc * 8 + e]);
+                const int s = cg * kW64 + cc * 8 + e;
+                const int off = swz(kC + s, ci);
+                const float ek = __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t *>(ecol + off) << 16) +
+                                 __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t *>(ecol + 32768 + off) << 16);
+                x[e] = sc * ek - __uint_as_float(r[cc * 8 + e]);
             }
-            put8(smem + kQ + swz(i, half * 4 + cc), 16384, x);
+            put8(smem + kQ + swz(i, cg * (kW64 / 8) + cc), 16384, x);
         }
         fence_async_smem();
         tc_fence_before();
@@ -457,72 +435,87 @@ __global__ void __launch_bounds__(kThreads, 1)
                             (hl == 0 || ks > 0) ? 1u : 0u);
             mma_commit(&ctl->mma);
         }
-        // ---- T_c = diag(exp(L)) - P Ka, scaled by a power of two to max |M_c| in [1, 2)
+        // ---- T_c = diag(e^L) - (P Aq) diag(e^r), scaled by a power of two to max |M_c| in [1, 2)
+        ok = __all_sync(0xffffffffu, mbar_wait(&ctl->tdone, 0));   // warp-uniform: TMEM loads are collective
+        tc_fence_after();
         float tmx = 0.f;
-        const float di = exp2f(lc);
+        const float di = ctl->eL[i];
+        if (ok) {
 #pragma unroll
-        for (int p = 0; p < 2; ++p) {
-            tmem_ld32(tmem + lane_off + kTT + (uint32_t)(half * 64 + p * 32), r);
-            tmem_wait_ld();
+            for (int p = 0; p < kW128 / 32; ++p) {
+                tmem_ld32(tmem + lane_off + kTT + (uint32_t)(cg * kW128 + p * 32), r);
+                tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const int col = half * 64 + p * 32 + e;
-                tmx = fmaxf(tmx, fabsf((col == i ? di : 0.f) - __uint_as_float(r[e])));
+                for (int e = 0; e < 32; ++e) {
+                    const int col = cg * kW128 + p * 32 + e;
+                    tmx = fmaxf(tmx, fabsf((col == i ? di : 0.f) - ctl->er[col] * __uint_as_float(r[e])));
+                }
             }
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) tmx = fmaxf(tmx, __shfl_xor_sync(0xffffffffu, tmx, off));
         if (lane == 0) ctl->red[warp] = tmx;
-        __syncthreads();
-        tmx = 0.f;
+        ok = __syncthreads_and(ok);
+        if (ok) {
+            tmx = 0.f;
 #pragma unroll
-        for (int w = 0; w < kThreads / 32; ++w) tmx = fmaxf(tmx, ctl->red[w]);
-        const int ex = dense::exponent_of(tmx);
-        const float scl = ldexpf(1.f, -ex);
-        float *row = stage_row(smem, i) + half * 64;
+            for (int w = 0; w < kThreads / 32; ++w) tmx = fmaxf(tmx, ctl->red[w]);
+            const int ex = dense::exponent_of(tmx);
+            const float scl = ldexpf(1.f, -ex);
 #pragma unroll
-        for (int p = 0; p < 2; ++p) {
-            tmem_ld32(tmem + lane_off + kTT + (uint32_t)(half * 64 + p * 32), r);
-            tmem_wait_ld();
+            for (int p = 0; p < kW128 / 32; ++p) {
+                tmem_ld32(tmem + lane_off + kTT + (uint32_t)(cg * kW128 + p * 32), r);
+                tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; e += 4) {
-                float4 v;
-                float *vp = &v.x;
+                for (int e = 0; e < 32; e += 4) {
+                    float4 v;
+                    float *vp = &v.x;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int col = half * 64 + p * 32 + e + q;
-                    vp[q] = ((col == i ? di : 0.f) - __uint_as_float(r[e + q])) * scl;
+                    for (int q = 0; q < 4; ++q) {
+                        const int col = cg * kW128 + p * 32 + e + q;
+                        vp[q] = ((col == i ? di : 0.f) - ctl->er[col] * __uint_as_float(r[e + q])) * scl;
+                    }
+                    stage4(smem + kStM, i, (cg * kW128 + p * 32 + e) >> 2, v);
                 }
-                *reinterpret_cast<float4 *>(row + p * 32 + e) = v;
+            }
+            fence_async_smem();
+            __syncthreads();
+            if (tid == 0) {
+#pragma unroll
+                for (int b = 0; b < 4; ++b) tma_store_3d(&tm_m, smem + kStM + b * 16384, 32 * b, 0, (int)(u * kD));
+                bulk_commit();
+                pool_lam[u] = (float)ex * ln2;
             }
         }
-        __syncthreads();
-        copy_out(smem, pool_M + u * (kD * kD), tid);
-        if (tid == 0) pool_lam[u] = (float)ex * ln2;
-        ok = __syncthreads_and(mbar_wait(&ctl->mma, mma_phase));   // S_c done; the staging tiles read
+        ok = __syncthreads_and(ok && mbar_wait(&ctl->mma, mma_phase));   // S_c is done
         tc_fence_after();
     }
     if (ok) {
         // ---- S_c
-        float *row = stage_row(smem, m) + half * 64;
 #pragma unroll
-        for (int p = 0; p < 2; ++p) {
+        for (int p = 0; p < kW128 / 32; ++p) {
             uint32_t r[32];
-            tmem_ld32(tmem + lane_off + kTG + (uint32_t)(half * 64 + p * 32), r);
+            tmem_ld32(tmem + lane_off + kTG + (uint32_t)(cg * kW128 + p * 32), r);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; e += 4)
-                *reinterpret_cast<float4 *>(row + p * 32 + e) =
-                    make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]),
-                                __uint_as_float(r[e + 3]));
+                stage4(smem + kStS, m, (cg * kW128 + p * 32 + e) >> 2,
+                       make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]),
+                                   __uint_as_float(r[e + 3])));
         }
+        fence_async_smem();
         __syncthreads();
-        copy_out(smem, pool_S + u * (kD * kD), tid);
+        if (tid == 0) {
+#pragma unroll
+            for (int b = 0; b < 4; ++b) tma_store_3d(&tm_s, smem + kStS + b * 16384, 32 * b, 0, (int)(u * kD));
+            bulk_commit();
+        }
     } else if (tid == 0) {   // a wait gave up: drain this thread's MMAs, then report
         mma_commit(&ctl->drain);
         mbar_wait(&ctl->drain, 0);
         if (a.d_err) atomicExch(a.d_err, (int)HYPIC_ETIMEOUT);
     }
+    if (tid == 0) bulk_wait_all();   // the staged tiles are read and the stores complete
 
     tc_fence_before();
     __syncthreads();
@@ -597,7 +590,7 @@ bool scan_kda_tc_shape(const ScanArgs &a) {
     const int64_t slots = (int64_t)a.n_seg + a.N / kC;
     const int64_t rows = (int64_t)a.n_layers * slots * a.H;
     return (int64_t)a.n_layers * a.N < ((int64_t)1 << 31) && slots * a.H < ((int64_t)1 << 31) &&
-           rows < ((int64_t)1 << 31) && (int64_t)a.n_layers * a.n_seg * a.H < ((int64_t)1 << 30) &&
+           rows * kD < ((int64_t)1 << 31) && (int64_t)a.n_layers * a.n_seg * a.H < ((int64_t)1 << 30) &&
            kda_layout(a).total <= kKdaMaxScratch;
 }
 
@@ -621,16 +614,23 @@ cudaError_t launch_scan_kda_tc(const ScanArgs &a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
 
     const uint64_t rows = (uint64_t)a.n_layers * (uint64_t)a.N;
-    CUtensorMap mk, mv;
+    const uint64_t prow = (uint64_t)t.P * a.H * kD;   // pool rows of 128 floats
+    CUtensorMap mk, mv, ma, mm, ms;
     if (!make_tensor_map_3d(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.k, kD, a.H, rows, 64, kC,
                             CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tensor_map_3d(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.v, kD, a.H, rows, 64, kC,
+                            CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map_3d(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.alpha, kD, a.H, rows, kD, kC,
+                            CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_tensor_map_3d(&mm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pM, kD, 1, prow, 32, kD,
+                            CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map_3d(&ms, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pS, kD, 1, prow, 32, kD,
                             CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     e = cudaFuncSetAttribute(scan_kda_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     scan_kda_chunk_kernel<<<dim3((unsigned)(t.slots * a.H), (unsigned)a.n_layers), kThreads, kSmem, s>>>(
-        mk, mv, a, t.slots, plam, pM, pS, steep);
+        mk, mv, ma, mm, ms, a, t.slots, plam, steep);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
