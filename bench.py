@@ -465,7 +465,7 @@ def run_kda(args, L):
     import torch
     import linear_attention_state_gated_gb300 as hy
     from linear_attention_state_gated_gb300 import workloads as wl
-    Lyr, H, d = 30, 32, 128
+    Lyr, H, d = args.kda_layers, 32, 128
     w = wl.kda_stack(seg_len=L, n_layers=Lyr, H=H, d=d)
     dev = torch.device("cuda")
     k = torch.from_numpy(w["k"]).to(torch.bfloat16).to(dev)
@@ -497,7 +497,7 @@ def run_kda(args, L):
     del k, v, a, b, offs, out, ws
     torch.cuda.empty_cache()
     return {"workload": f"KDA-style gates, {Lyr} layers x {H} heads x {d}, one segment of {L} tokens per layer",
-            "value": L / t, "unit": "tokens/s (all 30 layers)", "head_tokens_per_s": tok_heads / t,
+            "value": L / t, "unit": f"tokens/s (all {Lyr} layers)", "head_tokens_per_s": tok_heads / t,
             "ms": t * 1e3,
             "kernel": "chunk pairs on tcgen05 (scan_kda_chunk_kernel), then the composed-prefix chains",
             "roofline": {"bound": "tensor", "achieved": flops / t / 1e12, "peak": bf16, "unit": "TFLOP/s",
@@ -1013,6 +1013,8 @@ def main():
     ap.add_argument("--sd-lengths", default="512,2048",
                     help="scalar / diagonal rows at lengths other than the headline's")
     ap.add_argument("--kda-L", type=int, default=2048)
+    ap.add_argument("--kda-layers", type=int, default=30,
+                    help="layers of the KDA row (30: the dense stack's shape; fewer for a profiling capture)")
     ap.add_argument("--dense-form", choices=["two_pass", "single"], default="two_pass",
                     help="dense row: two passes over a workspace, or the single-pass kernel")
     ap.add_argument("--compose-n", type=int, default=1920,

@@ -144,6 +144,7 @@ int hypic_segment_scan(int fam, int in_dtype, int n_layers, int n_seg, int64_t t
     if (rc != HYPIC_OK || none) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     if (hypic::scan_sd_o_supported(a)) return from_cuda(hypic::launch_scan_sd_o(a, s));
+    if (hypic::scan_diag_o_supported(a)) return from_cuda(hypic::launch_scan_diag_o(a, s));
     if (hypic::scan_sd_tc_supported(a)) return from_cuda(hypic::launch_scan_sd_tc(a, s));
     if (hypic::scan_dense_tc_supported(a)) return from_cuda(hypic::launch_scan_dense_tc(a, s));
     return from_cuda(hypic::launch_scan_recurrent(a, s));
@@ -205,6 +206,7 @@ int hypic_segment_scan_ws(int fam, int in_dtype, int n_layers, int n_seg, int64_
         return from_cuda(hypic::launch_scan_sd_bal(a, s));
     }
     if (hypic::scan_sd_o_supported(a)) return from_cuda(hypic::launch_scan_sd_o(a, s));
+    if (hypic::scan_diag_o_supported(a)) return from_cuda(hypic::launch_scan_diag_o(a, s));
     if (hypic::scan_sd_tc_supported(a)) return from_cuda(hypic::launch_scan_sd_tc(a, s));
     if (hypic::scan_dense_tc_supported(a)) return from_cuda(hypic::launch_scan_dense_tc(a, s));
     return from_cuda(hypic::launch_scan_recurrent(a, s));

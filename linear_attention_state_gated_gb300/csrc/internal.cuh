@@ -72,6 +72,9 @@ cudaError_t launch_scan_sd_bal(const ScanArgs &a, cudaStream_t s);
 // Scalar gates with the per-token outputs o_t, chunks in order on tcgen05 (bf16, 128 x 128).
 bool scan_sd_o_supported(const ScanArgs &a);
 cudaError_t launch_scan_sd_o(const ScanArgs &a, cudaStream_t s);
+// Diagonal gates with o_t, chunks in order on tcgen05 (bf16, 128 x 128).
+bool scan_diag_o_supported(const ScanArgs &a);
+cudaError_t launch_scan_diag_o(const ScanArgs &a, cudaStream_t s);
 
 // Gated delta rule scan on tcgen05 tensor cores (bf16 inputs, d_k = d_v = 128, no o_t).
 bool scan_dense_tc_supported(const ScanArgs &a);

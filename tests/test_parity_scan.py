@@ -122,18 +122,48 @@ def test_scan_with_beta_and_mamba_like_gates():
         check(fam, got, ref, TOL_SCAN_BF16)
 
 
-def test_scalar_o_mamba_like_gates_and_beta():
-    """o_t on the scalar tensor-core path (chunks in order): per-token decays, some
-    strong, a write scale beta in [0, 2], segments across chunk edges and empty."""
+@pytest.mark.parametrize("fam", [SCALAR, DIAG], ids=["scalar", "diag"])
+def test_o_mamba_like_gates_and_beta(fam):
+    """o_t on the tensor-core paths (chunks in order): per-token decays (per channel
+    for the diagonal family), some strong, a write scale beta in [0, 2], segments
+    across chunk edges and empty."""
     g = np.random.default_rng(13)
     lens = [300, 77, 0, 640, 64, 1, 65]
-    w = wl.scalar_diag(SCALAR, lengths=lens, n_layers=2, H=4, d=128, seed=10, with_q=True)
+    w = wl.scalar_diag(fam, lengths=lens, n_layers=2, H=4, d=128, seed=10, with_q=True)
     w["alpha"] = np.exp(-g.exponential(0.5, size=w["alpha"].shape)).astype(np.float32)
     w["beta"] = g.uniform(0.0, 2.0, size=w["k"].shape[:3]).astype(np.float32)
     got = host(gpu_scan(w, want_o=True))
     ref = oracle_scan(w, want_o=True)
-    check(SCALAR, got, ref, TOL_SCAN_BF16, o_tol=TOL_O_BF16, seg_offsets=w["seg_offsets"])
+    e = check(fam, got, ref, TOL_SCAN_BF16, o_tol=TOL_O_BF16, seg_offsets=w["seg_offsets"])
+    print(f"family {fam} o_t path: S error {e[0]:.3e}, T error {e[1]:.3e}")
     assert np.all(got["S"][:, 2] == 0) and np.all(got["lam"][:, 2] == 0)
+
+
+def test_diag_o_steep_channels():
+    """Diagonal gates with o_t where some channels decay by more than e^60 inside a
+    chunk (those chunks take the exact Gram on CUDA cores and the end-of-chunk
+    references): still equal to the oracle."""
+    lens = [200, 130, 64]
+    w = wl.scalar_diag(DIAG, lengths=lens, n_layers=1, H=2, d=128, seed=11, with_q=True)
+    w["alpha"][:, 40:170, 0, :5] = np.float32(0.02)   # ln 0.02 = -3.9 a token
+    got = host(gpu_scan(w, want_o=True))
+    ref = oracle_scan(w, want_o=True)
+    check(DIAG, got, ref, TOL_SCAN_BF16, o_tol=TOL_O_BF16, seg_offsets=w["seg_offsets"])
+
+
+def test_diag_o_gla_full_size_sampled():
+    """GLA-style gates, 8 segments x 2048 tokens x 32 heads with o_t (the benchmark's
+    launch), sampled (segment, head) units against the straight recurrence."""
+    w = wl.scalar_diag(DIAG, seg_len=2048, n_seg=8, with_q=True)
+    got = host(gpu_scan(w, want_o=True))
+    rs = np.random.default_rng(2049)
+    for seg, h in [(0, 0), (7, 31)] + [tuple(x) for x in rs.integers([0, 0], [8, 32], size=(2, 2))]:
+        a, b = w["seg_offsets"][seg], w["seg_offsets"][seg + 1]
+        ref = oracle.sequential(DIAG, w["k"][:, a:b, h:h + 1], w["v"][:, a:b, h:h + 1],
+                                w["alpha"][:, a:b, h:h + 1], q=w["q"][:, a:b, h:h + 1], want_o=True)
+        sub = {"S": got["S"][:, seg, h:h + 1], "lam": got["lam"][:, seg, h:h + 1],
+               "o": got["o"][:, a:b, h:h + 1]}
+        check(DIAG, sub, ref, TOL_SCAN_BF16, o_tol=TOL_O_BF16, seg_offsets=[0, b - a])
 
 
 def test_scalar_o_retnet_full_size_sampled():
