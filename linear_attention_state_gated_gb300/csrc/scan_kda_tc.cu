@@ -5,8 +5,9 @@
 // Two passes.  The pair of a concatenation is the composition of the pairs of its
 // parts, T(C1.C2) = T(C2) T(C1) and S(C1.C2|0) = T(C2) S(C1|0) + S(C2|0), so:
 //   1. every chunk of 64 tokens of every segment becomes a cached pair (lambda_c,
-//      M_c, S_c) with T_c = exp(lambda_c) M_c, all chunks in parallel
-//      (scan_kda_chunk_kernel, one CTA per (layer, chunk slot, head));
+//      M_c, S_c) with T_c = exp(lambda_c) M_c, all chunks independently
+//      (scan_kda_chunk_kernel: one persistent CTA per SM walks the chunks, loading
+//      the next chunk's tiles while the current one's products and epilogues run);
 //   2. each segment folds its chunks' pairs in order with the composed-prefix
 //      kernels (the state's chain from zero and the operator chain from I).
 //
@@ -63,7 +64,8 @@ constexpr int kG = 4 * kBox;                   // the Gram operands, kept until 
 constexpr int kGa = kG;                        //   [Ck'; Ek'] hi: channel half b is the 128-row tile at
                                                //   kGa + 16384 b (rows 0..63 Ck', 64..127 Ek'); lo +32 KB
 constexpr int kGb = kG + 65536;                //   Aq hi (two boxes), lo +16 KB
-constexpr int kX = kG + 98304;                 // fp32 Lc, A = (I + Lc)^-1 and temporaries; then P hi, lo +16 KB
+constexpr int kX = kG + 98304;                 // the gates alpha (fp32 [64][128], TMA); then fp32 Lc, A =
+                                               // (I + Lc)^-1 and temporaries; then P hi, lo +16 KB
 constexpr int kLw = kX;
 constexpr int kAw = kLw + kC * kLd * 4;
 constexpr int kTw = kAw + kC * kLd * 4;
@@ -73,7 +75,9 @@ constexpr int kAi = kLam + 6144;               //   A (rows s, t along N) hi, lo
 constexpr int kQ = kLam;                       //   Q (rows i, s along K) hi, lo +16 KB
 constexpr int kCtl = kLam + (kC + 1) * kD * 4;
 constexpr int kStM = kG;                       // M_c staged for the TMA store: four 16 KB boxes of 32 columns
-constexpr int kStS = kG + 65536;               // S_c staged likewise
+// S_c staged likewise, boxes 0, 1 over Aq's tiles and 2, 3 over Q's (the next chunk's
+// gates arrive in kX meanwhile)
+__host__ __device__ constexpr int st_s_box(int b) { return b < 2 ? kGb + 16384 * b : kQ + 16384 * (b - 2); }
 
 struct Ctl {
     uint64_t full, mma, tdone, drain;
@@ -87,8 +91,8 @@ struct Ctl {
 constexpr int kSmem = kCtl + (int)sizeof(Ctl) + 1024;
 static_assert(kSmem <= 232448, "fits in one SM's shared memory");
 static_assert(kTw + 3 * 256 * 4 <= kAi, "the inverse's temporaries end before A's tiles");
-static_assert(kAi + 16384 <= kCtl && kQ + 32768 <= kCtl && kStS + 65536 <= kLam, "tiles inside their regions");
-static_assert(kAi % 1024 == 0 && kQ % 1024 == 0 && kX % 1024 == 0 && kStS % 1024 == 0, "tiles 1024-byte aligned");
+static_assert(kAi + 16384 <= kCtl && kQ + 32768 <= kCtl && kGb + 32768 <= kX, "tiles inside their regions");
+static_assert(kAi % 1024 == 0 && kQ % 1024 == 0 && kX % 1024 == 0 && kGb % 1024 == 0, "tiles 1024-byte aligned");
 
 // TMEM columns (256 allocated)
 constexpr uint32_t kTG = 0;     // Gram^T (lanes s / 64 + s), then P Le (64), then Q V (128)
@@ -117,8 +121,10 @@ __device__ __forceinline__ void load8(const float *p, float (&x)[8]) {
 
 // 4 values of row r, columns 4 c4 .. 4 c4 + 3 of a staged 128 x 128 fp32 result:
 // box c4 / 8 (32 columns), chunk c4 % 8 of the 128-byte-swizzled row
-__device__ __forceinline__ void stage4(uint8_t *st, int r, int c4, float4 v) {
-    *reinterpret_cast<float4 *>(st + (c4 >> 3) * 16384 + swz(r, c4 & 7)) = v;
+__device__ __forceinline__ int st_m_box(int b) { return kStM + 16384 * b; }
+template <bool S> __device__ __forceinline__ void stage4(uint8_t *smem, int r, int c4, float4 v) {
+    const int b = c4 >> 3;
+    *reinterpret_cast<float4 *>(smem + (S ? st_s_box(b) : st_m_box(b)) + swz(r, c4 & 7)) = v;
 }
 
 // W (16 or 32) consecutive columns of the warp's 32 lanes
@@ -138,6 +144,40 @@ __device__ __forceinline__ void mma3(uint32_t d, uint32_t idesc, int nk, DescA d
             mma_f16(d, da(order[p][0], ks), db(order[p][1], ks), idesc, (p > 0 || ks > 0) ? 1u : 0u);
 }
 
+// One chunk of the launch: its pool row u (= work index), first token and length.
+struct Item {
+    int64_t u, c0;
+    int l, h, nval;
+};
+
+// Work index w -> the chunk in slot w / H of its layer (false: no chunk uses the slot).
+// Slot of chunk j of segment s: s + floor(t0_s / 64) + j.
+__device__ __forceinline__ bool decode_item(const ScanArgs &a, int64_t slots, int64_t w, Item &it) {
+    const int64_t per_layer = slots * a.H;
+    const int l = (int)(w / per_layer);
+    const int64_t rem = w % per_layer;
+    const int64_t slot = rem / a.H;
+    int lo = 0, hi = a.n_seg - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((int64_t)mid + a.seg_offsets[mid] / kC <= slot) lo = mid;
+        else hi = mid - 1;
+    }
+    const int64_t t0 = a.seg_offsets[lo], t1 = a.seg_offsets[lo + 1];
+    const int64_t j = slot - (lo + t0 / kC);
+    if (!(t0 >= 0 && t0 <= t1 && t1 <= a.N) || j < 0 || j * kC >= t1 - t0) return false;
+    it.u = w;
+    it.l = l;
+    it.h = (int)(rem % a.H);
+    it.c0 = t0 + j * kC;
+    it.nval = (int)min((int64_t)kC, t1 - it.c0);
+    return true;
+}
+
+// Persistent: each CTA walks the chunks w = blockIdx.x, + gridDim.x, ...  While a
+// chunk's products and epilogues run, the next chunk's keys, gates and values are
+// loaded into the regions that fall free (keys after P Le, gates after P Aq, values
+// after Q V).
 __global__ void __launch_bounds__(kThreads, 1)
     scan_kda_chunk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                           const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_m,
@@ -148,184 +188,211 @@ __global__ void __launch_bounds__(kThreads, 1)
     Ctl *ctl = reinterpret_cast<Ctl *>(smem + kCtl);
     float *lam = reinterpret_cast<float *>(smem + kLam);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h = (int)(blockIdx.x % (unsigned)a.H);
-    const int64_t slot = blockIdx.x / (unsigned)a.H;
-    const int l = blockIdx.y;
-    const int64_t u = ((int64_t)l * slots + slot) * a.H + h;   // pool row of this chunk
+    const int64_t n_items = (int64_t)a.n_layers * slots * a.H;
 
-    // slot -> (segment, chunk): the last segment s with s + floor(t0_s / 64) <= slot
-    int lo = 0, hi = a.n_seg - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if ((int64_t)mid + a.seg_offsets[mid] / kC <= slot) lo = mid;
-        else hi = mid - 1;
-    }
-    const int64_t t0 = a.seg_offsets[lo], t1 = a.seg_offsets[lo + 1];
-    const int64_t j = slot - (lo + t0 / kC);
-    if (!(t0 >= 0 && t0 <= t1 && t1 <= a.N) || j < 0 || j * kC >= t1 - t0) {   // no chunk here
-        if (tid == 0) steep[u] = 0;
-        return;
-    }
-    const int64_t c0 = t0 + j * kC;
-    const int nval = (int)min((int64_t)kC, t1 - c0);
+    // the next chunk at or after w in this CTA's stride (slots without a chunk get flag 0)
+    auto find = [&](int64_t &w, Item &it) -> bool {
+        for (; w < n_items; w += gridDim.x) {
+            if (decode_item(a, slots, w, it)) return true;
+            if (tid == 0) steep[w] = 0;
+        }
+        return false;
+    };
+    auto row_of = [&](const Item &it) { return (int)((int64_t)it.l * a.N + it.c0); };
+    auto beta_of = [&](const Item &it, int t) {
+        return t < it.nval ? (a.beta ? a.beta[((int64_t)it.l * a.N + it.c0 + t) * a.H + it.h] : 1.f) : 0.f;
+    };
+    // (thread 0) the tiles of chunk it: keys, gates, values
+    auto load_k = [&](const Item &it) {
+        mbar_expect_tx(&ctl->full, (uint32_t)(4 * kBox + kC * kD * 4));
+        tma_load_3d(smem + kK, &tm_k, &ctl->full, 0, it.h, row_of(it));
+        tma_load_3d(smem + kK + kBox, &tm_k, &ctl->full, 64, it.h, row_of(it));
+    };
+    auto load_a = [&](const Item &it) { tma_load_3d(smem + kX, &tm_a, &ctl->full, 0, it.h, row_of(it)); };
+    auto load_v = [&](const Item &it) {
+        tma_load_3d(smem + kV, &tm_v, &ctl->full, 0, it.h, row_of(it));
+        tma_load_3d(smem + kV + kBox, &tm_v, &ctl->full, 64, it.h, row_of(it));
+    };
 
+    int64_t w = blockIdx.x;
+    Item cur;
+    bool have = find(w, cur);
     if (tid == 0) {
         mbar_init(&ctl->full, 1);
         mbar_init(&ctl->mma, 1);
         mbar_init(&ctl->tdone, 1);
         mbar_init(&ctl->drain, 1);
         mbar_fence_init();
-        mbar_expect_tx(&ctl->full, (uint32_t)(4 * kBox + kC * kD * 4));
-        const int row = (int)((int64_t)l * a.N + c0);
-        tma_load_3d(smem + kK, &tm_k, &ctl->full, 0, h, row);
-        tma_load_3d(smem + kK + kBox, &tm_k, &ctl->full, 64, h, row);
-        tma_load_3d(smem + kV, &tm_v, &ctl->full, 0, h, row);
-        tma_load_3d(smem + kV + kBox, &tm_v, &ctl->full, 64, h, row);
-        tma_load_3d(smem + kLam + kD * 4, &tm_a, &ctl->full, 0, h, row);   // alpha: rows 1..64 of Lam
+        if (have) {
+            load_k(cur);
+            load_a(cur);
+            load_v(cur);
+        }
     }
     if (warp == 0) tmem_alloc(&ctl->tmem, 256);
-    if (tid >= kD && tid < kD + kC) {
-        const int t = tid - kD;
-        ctl->beta[t] = t < nval ? (a.beta ? a.beta[((int64_t)l * a.N + c0 + t) * a.H + h] : 1.f) : 0.f;
-    }
+    if (have && tid >= kD && tid < kD + kC) ctl->beta[tid - kD] = beta_of(cur, tid - kD);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ctl->tmem;
-    bool ok = __syncthreads_and(mbar_wait(&ctl->full, 0));   // the tiles land before any exit
-
-    // ---- gates: Lam (base 2), the prefix over tokens per channel; tokens past the
-    // segment's end get alpha = 1 and beta = 0 (their keys then act on nothing)
-    float mx = 0.f;
-    if (ok) {
-        float4 *g4 = reinterpret_cast<float4 *>(lam + kD);
-#pragma unroll
-        for (int i = 0; i < kC * kD / 4 / kThreads; ++i) {
-            const int f = tid + kThreads * i;   // float4 index: token f / 32
-            const bool v = (f >> 5) < nval;
-            const float4 x = g4[f];
-            g4[f] = v ? make_float4(log2f(x.x), log2f(x.y), log2f(x.z), log2f(x.w)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        if (tid < kD) lam[tid] = 0.f;
-        __syncthreads();
-        constexpr int kTok = kC / kParts;                  // tokens of a part
-        const int ch = tid & (kD - 1), part = tid >> 7;   // tokens kTok part .. kTok part + kTok - 1
-        float acc = 0.f;
-#pragma unroll 8
-        for (int t = part * kTok; t < part * kTok + kTok; ++t) {
-            acc += lam[(t + 1) * kD + ch];
-            lam[(t + 1) * kD + ch] = acc;
-        }
-        __syncthreads();
-        float base = 0.f;   // the totals of the earlier parts
-        for (int q = 0; q < part; ++q) base += lam[(q + 1) * kTok * kD + ch];
-        __syncthreads();
-#pragma unroll 8
-        for (int t = part * kTok; t < part * kTok + kTok; ++t) {
-            const float x = lam[(t + 1) * kD + ch] + base;
-            if (part) lam[(t + 1) * kD + ch] = x;
-            mx = fmaxf(mx, fabsf(x));
-        }
-        if (!(mx <= kMaxLog2)) mx = INFINITY;   // a NaN gate counts as steep
-    }
-    const bool is_steep = __syncthreads_or(mx > kMaxLog2);
-    if (tid == 0) steep[u] = (is_steep || !ok) ? 1 : 0;
-    if (is_steep || !ok) {
-        if (!ok && tid == 0 && a.d_err) atomicExch(a.d_err, (int)HYPIC_ETIMEOUT);   // the tiles never came
-        tc_fence_before();
-        __syncthreads();
-        if (warp == 0) {
-            tc_fence_after();
-            tmem_dealloc(tmem, 256);
-        }
-        return;
-    }
-    if (tid < kD) {   // per-channel factors of the scales below (r = Lam_31, L = Lam_63)
-        const float r = lam[32 * kD + tid], L = lam[kC * kD + tid];
-        ctl->eLr[tid] = exp2f(L - r);
-        ctl->er[tid] = exp2f(r);
-        ctl->eL[tid] = exp2f(L);
-    }
-
-    // ---- the Gram operands (bf16 hi / lo, 128-byte swizzle): Aq_t = k_t e^(Lp_t - r),
-    // Ck'_s = beta_s k_s e^(r - Lp_s), Ek'_s = beta_s k_s e^(r - Lam_s).  They are kept:
-    // beta o Ct = Ck' diag(e^(L - r)), Ka = Aq diag(e^r), beta o Et = Ek' diag(e^(L - r)).
-    const uint8_t *kt = smem + kK;
-#pragma unroll 1
-    for (int f = tid; f < kC * 16; f += kThreads) {
-        const int t = f >> 4, cc = f & 15, b = cc >> 3, c = cc & 7, chn = cc * 8;
-        const uint4 raw = *reinterpret_cast<const uint4 *>(kt + b * kBox + swz(t, c));
-        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-        float lp[8], lt[8], rf[8];
-        load8(lam + t * kD + chn, lp);
-        load8(lam + (t + 1) * kD + chn, lt);
-        load8(lam + 32 * kD + chn, rf);
-        const float bt = ctl->beta[t];
-        float aq[8], ck[8], ek[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float kv = (e & 1) ? bf_hi(w[e >> 1]) : bf_lo(w[e >> 1]);
-            aq[e] = kv * exp2f(lp[e] - rf[e]);
-            ck[e] = bt * kv * exp2f(rf[e] - lp[e]);
-            ek[e] = bt * kv * exp2f(rf[e] - lt[e]);
-        }
-        put8(smem + kGb + b * kBox + swz(t, c), 16384, aq);
-        put8(smem + kGa + b * 16384 + swz(t, c), 32768, ck);
-        put8(smem + kGa + b * 16384 + swz(kC + t, c), 32768, ek);
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    uint32_t mma_phase = 0;
-    if (tid == 0) {   // Gram^T = [Ck'; Ek'] Aq^T (M = 128, N = 64, K = 128)
-        tc_fence_after();
-        constexpr uint32_t id_g = idesc_bf16_f32(128, 64, false, false);
-        const uint32_t ga = smem_addr(smem + kGa), gb = smem_addr(smem + kGb);
-        mma3(tmem + kTG, id_g, 8,
-             [&](int hl, int ks) {
-                 return smem_desc_sw128(ga + (uint32_t)hl * 32768u + (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u,
-                                        0, 1024);
-             },
-             [&](int hl, int ks) {
-                 return smem_desc_sw128(gb + (uint32_t)hl * 16384u + (uint32_t)(ks >> 2) * kBox + (uint32_t)(ks & 3) * 32u,
-                                        0, 1024);
-             });
-        mma_commit(&ctl->mma);
-    }
-    ok = __syncthreads_and(mbar_wait(&ctl->mma, mma_phase));
-    mma_phase ^= 1u;
-    tc_fence_after();
     const int q4 = warp & 3, cg = warp >> 2;         // TMEM lane quarter, column group
     const int m = q4 * 32 + lane;                    // accumulator row of this thread
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     float *Lw = reinterpret_cast<float *>(smem + kLw);
     float *Aw = reinterpret_cast<float *>(smem + kAw);
     float *Tw = reinterpret_cast<float *>(smem + kTw);
+    const float ln2 = 0.6931471805599453f;
+    uint32_t full_par = 0, t_par = 0, mma_phase = 0;
+    bool ok = true, pending = have;   // pending: loads in flight on `full`
 
-    if (ok) {
-        // ---- Lc (fp32, for the inverse) and Le^T (bf16 hi / lo, over the keys) from the
-        // Gram, t > s only
-        uint32_t r[kW64];
-        tmem_ldw<kW64>(tmem + lane_off + kTG + (uint32_t)(cg * kW64), r);
-        tmem_wait_ld();
-        if (q4 < 2) {
-            const int s = m;
+    while (have && ok) {
+        int64_t wn = w + gridDim.x;
+        Item nxt;
+        const bool have_n = find(wn, nxt);
+        float bnext = 0.f;   // the next chunk's beta (threads kD .. kD + 63)
+        // the previous chunk's TMA stores have read their staging tiles (Gram, Q and Lam regions)
+        if (tid == 0) bulk_wait_read_all();
+        ok = __syncthreads_and(mbar_wait(&ctl->full, full_par));   // this chunk's tiles
+        full_par ^= 1u;
+        pending = false;
+        if (!ok) break;
+        const int64_t u = cur.u;
+        const int nval = cur.nval;
+
+        // ---- gates: Lam (base 2), the prefix over tokens per channel; tokens past the
+        // segment's end get alpha = 1 and beta = 0 (their keys then act on nothing)
+        float mx = 0.f;
+        {
+            const float4 *a4 = reinterpret_cast<const float4 *>(smem + kX);
+            float4 *g4 = reinterpret_cast<float4 *>(lam + kD);
 #pragma unroll
-            for (int i = 0; i < kW64; ++i) {
-                const int t = cg * kW64 + i;
-                Lw[t * kLd + s] = t > s ? __uint_as_float(r[i]) : 0.f;
+            for (int i = 0; i < kC * kD / 4 / kThreads; ++i) {
+                const int f = tid + kThreads * i;   // float4 index: token f / 32
+                const bool v = (f >> 5) < nval;
+                const float4 x = a4[f];
+                g4[f] = v ? make_float4(log2f(x.x), log2f(x.y), log2f(x.z), log2f(x.w)) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
-        } else {
-            const int s = m - kC;
-#pragma unroll
-            for (int cc = 0; cc < kW64 / 8; ++cc) {
-                float x[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int t = cg * kW64 + cc * 8 + e;
-                    x[e] = t > s ? __uint_as_float(r[cc * 8 + e]) : 0.f;
+            if (tid < kD) lam[tid] = 0.f;
+            __syncthreads();
+            constexpr int kTok = kC / kParts;                  // tokens of a part
+            const int ch = tid & (kD - 1), part = tid >> 7;   // tokens kTok part .. kTok part + kTok - 1
+            float acc = 0.f;
+#pragma unroll 8
+            for (int t = part * kTok; t < part * kTok + kTok; ++t) {
+                acc += lam[(t + 1) * kD + ch];
+                lam[(t + 1) * kD + ch] = acc;
+            }
+            __syncthreads();
+            float base = 0.f;   // the totals of the earlier parts
+            for (int q = 0; q < part; ++q) base += lam[(q + 1) * kTok * kD + ch];
+            __syncthreads();
+#pragma unroll 8
+            for (int t = part * kTok; t < part * kTok + kTok; ++t) {
+                const float x = lam[(t + 1) * kD + ch] + base;
+                if (part) lam[(t + 1) * kD + ch] = x;
+                mx = fmaxf(mx, fabsf(x));
+            }
+            if (!(mx <= kMaxLog2)) mx = INFINITY;   // a NaN gate counts as steep
+        }
+        const bool is_steep = __syncthreads_or(mx > kMaxLog2);
+        if (tid == 0) steep[u] = is_steep ? 1 : 0;
+        if (is_steep) {   // its pair comes from the token-by-token kernel; nothing here is in use
+            if (have_n) {
+                if (tid == 0) {
+                    load_k(nxt);
+                    load_a(nxt);
+                    load_v(nxt);
                 }
-                put8(smem + kK + swz(s, cg * (kW64 / 8) + cc), 8192, x);
+                pending = true;
+                if (tid >= kD && tid < kD + kC) ctl->beta[tid - kD] = beta_of(nxt, tid - kD);
+            }
+            __syncthreads();
+            w = wn;
+            cur = nxt;
+            have = have_n;
+            continue;
+        }
+        if (tid < kD) {   // per-channel factors of the scales below (r = Lam_31, L = Lam_63)
+            const float r = lam[32 * kD + tid], L = lam[kC * kD + tid];
+            ctl->eLr[tid] = exp2f(L - r);
+            ctl->er[tid] = exp2f(r);
+            ctl->eL[tid] = exp2f(L);
+        }
+
+        // ---- the Gram operands (bf16 hi / lo, 128-byte swizzle): Aq_t = k_t e^(Lp_t - r),
+        // Ck'_s = beta_s k_s e^(r - Lp_s), Ek'_s = beta_s k_s e^(r - Lam_s).  They are kept:
+        // beta o Ct = Ck' diag(e^(L - r)), Ka = Aq diag(e^r), beta o Et = Ek' diag(e^(L - r)).
+        const uint8_t *kt = smem + kK;
+#pragma unroll 1
+        for (int f = tid; f < kC * 16; f += kThreads) {
+            const int t = f >> 4, cc = f & 15, b = cc >> 3, c = cc & 7, chn = cc * 8;
+            const uint4 raw = *reinterpret_cast<const uint4 *>(kt + b * kBox + swz(t, c));
+            const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+            float lp[8], lt[8], rf[8];
+            load8(lam + t * kD + chn, lp);
+            load8(lam + (t + 1) * kD + chn, lt);
+            load8(lam + 32 * kD + chn, rf);
+            const float bt = ctl->beta[t];
+            float aq[8], ck[8], ek[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float kv = (e & 1) ? bf_hi(wv[e >> 1]) : bf_lo(wv[e >> 1]);
+                aq[e] = kv * exp2f(lp[e] - rf[e]);
+                ck[e] = bt * kv * exp2f(rf[e] - lp[e]);
+                ek[e] = bt * kv * exp2f(rf[e] - lt[e]);
+            }
+            put8(smem + kGb + b * kBox + swz(t, c), 16384, aq);
+            put8(smem + kGa + b * 16384 + swz(t, c), 32768, ck);
+            put8(smem + kGa + b * 16384 + swz(kC + t, c), 32768, ek);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {   // Gram^T = [Ck'; Ek'] Aq^T (M = 128, N = 64, K = 128)
+            tc_fence_after();
+            constexpr uint32_t id_g = idesc_bf16_f32(128, 64, false, false);
+            const uint32_t ga = smem_addr(smem + kGa), gb = smem_addr(smem + kGb);
+            mma3(tmem + kTG, id_g, 8,
+                 [&](int hl, int ks) {
+                     return smem_desc_sw128(ga + (uint32_t)hl * 32768u + (uint32_t)(ks >> 2) * 16384u +
+                                                (uint32_t)(ks & 3) * 32u,
+                                            0, 1024);
+                 },
+                 [&](int hl, int ks) {
+                     return smem_desc_sw128(gb + (uint32_t)hl * 16384u + (uint32_t)(ks >> 2) * kBox +
+                                                (uint32_t)(ks & 3) * 32u,
+                                            0, 1024);
+                 });
+            mma_commit(&ctl->mma);
+        }
+        ok = __syncthreads_and(mbar_wait(&ctl->mma, mma_phase));
+        mma_phase ^= 1u;
+        tc_fence_after();
+        if (!ok) break;
+
+        {   // ---- Lc (fp32, for the inverse) and Le^T (bf16 hi / lo, over the keys), t > s only
+            uint32_t r[kW64];
+            tmem_ldw<kW64>(tmem + lane_off + kTG + (uint32_t)(cg * kW64), r);
+            tmem_wait_ld();
+            if (q4 < 2) {
+                const int s = m;
+#pragma unroll
+                for (int i = 0; i < kW64; ++i) {
+                    const int t = cg * kW64 + i;
+                    Lw[t * kLd + s] = t > s ? __uint_as_float(r[i]) : 0.f;
+                }
+            } else {
+                const int s = m - kC;
+#pragma unroll
+                for (int cc = 0; cc < kW64 / 8; ++cc) {
+                    float x[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int t = cg * kW64 + cc * 8 + e;
+                        x[e] = t > s ? __uint_as_float(r[cc * 8 + e]) : 0.f;
+                    }
+                    put8(smem + kK + swz(s, cg * (kW64 / 8) + cc), 8192, x);
+                }
             }
         }
         __syncthreads();
@@ -358,19 +425,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __syncthreads_and(mbar_wait(&ctl->mma, mma_phase));
         mma_phase ^= 1u;
         tc_fence_after();
-    }
-    if (ok) {
-        // ---- P = diag(e^(L - r)) Ck'^T A -> bf16 hi / lo (rows i, t along K)
-        uint32_t r[kW64];
-        tmem_ldw<kW64>(tmem + lane_off + kTP + (uint32_t)(cg * kW64), r);
-        const float sc = ctl->eLr[m];
-        tmem_wait_ld();
+        if (!ok) break;
+
+        {   // ---- P = diag(e^(L - r)) Ck'^T A -> bf16 hi / lo (rows i, t along K)
+            uint32_t r[kW64];
+            tmem_ldw<kW64>(tmem + lane_off + kTP + (uint32_t)(cg * kW64), r);
+            const float sc = ctl->eLr[m];
+            tmem_wait_ld();
 #pragma unroll
-        for (int cc = 0; cc < kW64 / 8; ++cc) {
-            float x[8];
+            for (int cc = 0; cc < kW64 / 8; ++cc) {
+                float x[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = sc * __uint_as_float(r[cc * 8 + e]);
-            put8(smem + kX + swz(m, cg * (kW64 / 8) + cc), 16384, x);
+                for (int e = 0; e < 8; ++e) x[e] = sc * __uint_as_float(r[cc * 8 + e]);
+                put8(smem + kX + swz(m, cg * (kW64 / 8) + cc), 16384, x);
+            }
         }
         fence_async_smem();
         tc_fence_before();
@@ -395,29 +463,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __syncthreads_and(mbar_wait(&ctl->mma, mma_phase));
         mma_phase ^= 1u;
         tc_fence_after();
-    }
-    const float ln2 = 0.6931471805599453f;
-    if (ok) {
-        // ---- Q[i][s] = e^(L_i - r_i) Ek'[s][i] - (P Le)[i][s] -> bf16 hi / lo (rows i, s along K)
+        if (!ok) break;
+        // the keys' region (Le^T) is free: the next chunk's keys; its beta in flight too
+        if (have_n) {
+            if (tid == 0) load_k(nxt);
+            pending = true;
+            if (tid >= kD && tid < kD + kC) bnext = beta_of(nxt, tid - kD);
+        }
+
         const int i = m;
         uint32_t r[32];
-        tmem_ldw<kW64>(tmem + lane_off + kTG + (uint32_t)(cg * kW64), *reinterpret_cast<uint32_t(*)[kW64]>(r));
-        const float sc = ctl->eLr[i];
-        const uint8_t *ecol = smem + kGa + (i >> 6) * 16384 + ((i & 7) << 1);   // Ek' rows 64 + s
-        const int ci = (i & 63) >> 3;
-        tmem_wait_ld();
+        {   // ---- Q[i][s] = e^(L_i - r_i) Ek'[s][i] - (P Le)[i][s] -> bf16 hi / lo (rows i, s along K)
+            tmem_ldw<kW64>(tmem + lane_off + kTG + (uint32_t)(cg * kW64), *reinterpret_cast<uint32_t(*)[kW64]>(r));
+            const float sc = ctl->eLr[i];
+            const uint8_t *ecol = smem + kGa + (i >> 6) * 16384 + ((i & 7) << 1);   // Ek' rows 64 + s
+            const int ci = (i & 63) >> 3;
+            tmem_wait_ld();
 #pragma unroll
-        for (int cc = 0; cc < kW64 / 8; ++cc) {
-            float x[8];
+            for (int cc = 0; cc < kW64 / 8; ++cc) {
+                float x[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int s = cg * kW64 + cc * 8 + e;
-                const int off = swz(kC + s, ci);
-                const float ek = __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t *>(ecol + off) << 16) +
-                                 __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t *>(ecol + 32768 + off) << 16);
-                x[e] = sc * ek - __uint_as_float(r[cc * 8 + e]);
+                for (int e = 0; e < 8; ++e) {
+                    const int s = cg * kW64 + cc * 8 + e;
+                    const int off = swz(kC + s, ci);
+                    const float ek =
+                        __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t *>(ecol + off) << 16) +
+                        __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t *>(ecol + 32768 + off) << 16);
+                    x[e] = sc * ek - __uint_as_float(r[cc * 8 + e]);
+                }
+                put8(smem + kQ + swz(i, cg * (kW64 / 8) + cc), 16384, x);
             }
-            put8(smem + kQ + swz(i, cg * (kW64 / 8) + cc), 16384, x);
         }
         fence_async_smem();
         tc_fence_before();
@@ -436,8 +511,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(&ctl->mma);
         }
         // ---- T_c = diag(e^L) - (P Aq) diag(e^r), scaled by a power of two to max |M_c| in [1, 2)
-        ok = __all_sync(0xffffffffu, mbar_wait(&ctl->tdone, 0));   // warp-uniform: TMEM loads are collective
+        ok = __all_sync(0xffffffffu, mbar_wait(&ctl->tdone, t_par));   // warp-uniform: TMEM loads are collective
+        t_par ^= 1u;
         tc_fence_after();
+        if (ok && have_n && tid == 0) load_a(nxt);   // P's tiles are read: the next chunk's gates
         float tmx = 0.f;
         const float di = ctl->eL[i];
         if (ok) {
@@ -456,10 +533,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int off = 16; off > 0; off >>= 1) tmx = fmaxf(tmx, __shfl_xor_sync(0xffffffffu, tmx, off));
         if (lane == 0) ctl->red[warp] = tmx;
         ok = __syncthreads_and(ok);
-        if (ok) {
+        if (!ok) break;
+        {
             tmx = 0.f;
 #pragma unroll
-            for (int w = 0; w < kThreads / 32; ++w) tmx = fmaxf(tmx, ctl->red[w]);
+            for (int wi = 0; wi < kThreads / 32; ++wi) tmx = fmaxf(tmx, ctl->red[wi]);
             const int ex = dense::exponent_of(tmx);
             const float scl = ldexpf(1.f, -ex);
 #pragma unroll
@@ -475,48 +553,55 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int col = cg * kW128 + p * 32 + e + q;
                         vp[q] = ((col == i ? di : 0.f) - ctl->er[col] * __uint_as_float(r[e + q])) * scl;
                     }
-                    stage4(smem + kStM, i, (cg * kW128 + p * 32 + e) >> 2, v);
+                    stage4<false>(smem, i, (cg * kW128 + p * 32 + e) >> 2, v);
                 }
             }
             fence_async_smem();
             __syncthreads();
             if (tid == 0) {
 #pragma unroll
-                for (int b = 0; b < 4; ++b) tma_store_3d(&tm_m, smem + kStM + b * 16384, 32 * b, 0, (int)(u * kD));
+                for (int b = 0; b < 4; ++b) tma_store_3d(&tm_m, smem + st_m_box(b), 32 * b, 0, (int)(u * kD));
                 bulk_commit();
                 pool_lam[u] = (float)ex * ln2;
             }
         }
-        ok = __syncthreads_and(ok && mbar_wait(&ctl->mma, mma_phase));   // S_c is done
+        ok = __syncthreads_and(mbar_wait(&ctl->mma, mma_phase));   // S_c is done
+        mma_phase ^= 1u;
         tc_fence_after();
-    }
-    if (ok) {
+        if (!ok) break;
+        if (have_n && tid == 0) load_v(nxt);   // the values are read: the next chunk's
         // ---- S_c
 #pragma unroll
         for (int p = 0; p < kW128 / 32; ++p) {
-            uint32_t r[32];
             tmem_ld32(tmem + lane_off + kTG + (uint32_t)(cg * kW128 + p * 32), r);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; e += 4)
-                stage4(smem + kStS, m, (cg * kW128 + p * 32 + e) >> 2,
+                stage4<true>(smem, m, (cg * kW128 + p * 32 + e) >> 2,
                        make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]),
                                    __uint_as_float(r[e + 3])));
         }
         fence_async_smem();
+        tc_fence_before();
         __syncthreads();
         if (tid == 0) {
 #pragma unroll
-            for (int b = 0; b < 4; ++b) tma_store_3d(&tm_s, smem + kStS + b * 16384, 32 * b, 0, (int)(u * kD));
+            for (int b = 0; b < 4; ++b) tma_store_3d(&tm_s, smem + st_s_box(b), 32 * b, 0, (int)(u * kD));
             bulk_commit();
         }
-    } else if (tid == 0) {   // a wait gave up: drain this thread's MMAs, then report
+        if (have_n && tid >= kD && tid < kD + kC) ctl->beta[tid - kD] = bnext;   // this chunk's beta is done
+        w = wn;
+        cur = nxt;
+        have = have_n;
+    }
+
+    if (!ok && tid == 0) {   // a wait gave up: drain this thread's MMAs and loads, then report
         mma_commit(&ctl->drain);
         mbar_wait(&ctl->drain, 0);
+        if (pending) mbar_wait(&ctl->full, full_par);
         if (a.d_err) atomicExch(a.d_err, (int)HYPIC_ETIMEOUT);
     }
     if (tid == 0) bulk_wait_all();   // the staged tiles are read and the stores complete
-
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -629,8 +714,13 @@ cudaError_t launch_scan_kda_tc(const ScanArgs &a, cudaStream_t s) {
         return cudaErrorInvalidValue;
     e = cudaFuncSetAttribute(scan_kda_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    scan_kda_chunk_kernel<<<dim3((unsigned)(t.slots * a.H), (unsigned)a.n_layers), kThreads, kSmem, s>>>(
-        mk, mv, ma, mm, ms, a, t.slots, plam, steep);
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        sms = 148;
+    const int64_t items = t.P * a.H;   // one CTA per SM walks the chunks
+    const unsigned grid = (unsigned)(items < sms ? items : sms);
+    scan_kda_chunk_kernel<<<grid, kThreads, kSmem, s>>>(mk, mv, ma, mm, ms, a, t.slots, plam, steep);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 

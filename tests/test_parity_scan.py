@@ -182,13 +182,15 @@ def test_scalar_o_retnet_full_size_sampled():
 
 
 @pytest.mark.parametrize("fam", [SCALAR, DIAG], ids=["scalar", "diag"])
-@pytest.mark.parametrize("L", [512, 8192])
+@pytest.mark.parametrize("L", [512, 2048, 8192])
 def test_scalar_diag_full_size_sampled(fam, L):
-    """32 heads, d=128, batch of 8 segments of L tokens (the benchmark's launch)."""
+    """32 heads, d=128, batch of 8 segments of L tokens (the benchmark's launch);
+    sampled units at the batch's ends, in interior segments and at random."""
     w = wl.scalar_diag(fam, seg_len=L, n_seg=8)
     got = host(gpu_scan(w))
     rs = np.random.default_rng(L + fam)
-    for seg, h in [(0, 0), (7, 31)] + [tuple(x) for x in rs.integers([0, 0], [8, 32], size=(2, 2))]:
+    picks = [(0, 0), (7, 31), (3, 15), (4, 16)] + [tuple(x) for x in rs.integers([1, 0], [7, 32], size=(2, 2))]
+    for seg, h in picks:
         a, b = w["seg_offsets"][seg], w["seg_offsets"][seg + 1]
         ref = oracle.sequential(fam, w["k"][:, a:b, h:h + 1], w["v"][:, a:b, h:h + 1],
                                 w["alpha"][:, a:b, h:h + 1])
