@@ -70,6 +70,16 @@ __device__ __forceinline__ void split3_pair(float x0, float x1, uint32_t &hi, ui
     lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
+// Two fp32 values -> two packed bf16 pairs with x = hi + lo (to ~2^-17 relative).
+__device__ __forceinline__ void split2_pair(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    float r0, r1;
+    upk2(sub2(pk2(x0, x1), bf16x2_to_f32x2(hi)), r0, r1);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(r0, r1);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
+}
+
 // Steps of unit u (a chain of request r; one step without a chain list), clamped.
 __device__ __forceinline__ int unit_steps(const ChainArgs &a, int64_t u, bool flag) {
     if (!a.chain_len) return 1;
@@ -96,8 +106,10 @@ __device__ __forceinline__ int64_t step_entry(const ChainArgs &a, int64_t u, int
 }
 
 // OP: operator mode (ChainArgs::op), a compile-time switch so that the state's
-// chain carries none of it
-template <bool OP>
+// chain carries none of it.  NS: bf16 parts per operand, 3 (hi / mid / lo, six
+// products: the fp32 compose) or 2 (hi / lo, three products, ~2^-17 per product:
+// ChainArgs::two_way, for chains inside a scan whose inputs are bf16)
+template <bool OP, int NS>
 __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: <= 96 registers per thread
     chain_dense_tc_kernel(const __grid_constant__ CUtensorMap tm_m, const __grid_constant__ CUtensorMap tm_s,
                           const __grid_constant__ CUtensorMap tm_i, const __grid_constant__ CUtensorMap tm_o,
@@ -199,7 +211,23 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: <= 96 registers pe
                     }
                     tc_fence_after();
                     const uint32_t abuf = tmem + kTa + (uint32_t)(g & 1) * 192u;
-                    if (OP) {
+                    if (NS == 2) {
+                        // hi / lo parts (at the mid positions): lo products first, then hi x hi
+#pragma unroll 4
+                        for (int ks = 0; ks < 8; ++ks) {
+                            const uint32_t off = (uint32_t)ks * 2048u;
+                            const uint64_t bh = smem_desc_sw128(b0 + off, 16384, 1024);
+                            const uint64_t bl = smem_desc_sw128(b0 + kBpart + off, 16384, 1024);
+                            const uint32_t ah = abuf + (uint32_t)ks * 8u, al = ah + 64u;
+                            mma_f16_ta(dcol, ah, bl, idesc, ks > 0);
+                            mma_f16_ta(dcol, al, bh, idesc, 1u);
+                        }
+#pragma unroll 4
+                        for (int ks = 0; ks < 8; ++ks) {
+                            const uint64_t bh = smem_desc_sw128(b0 + (uint32_t)ks * 2048u, 16384, 1024);
+                            mma_f16_ta(dcol, abuf + (uint32_t)ks * 8u, bh, idesc, 1u);
+                        }
+                    } else if (OP) {
                         // operator chains: smallest terms first.  The unit rounds each
                         // instruction's sum into the fp32 accumulator; nothing decays an
                         // operator chain's early error, so the 2^-16-level products (hl, mm,
@@ -285,13 +313,18 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: <= 96 registers pe
                 const int box = col >> 5, chunk = (col & 31) >> 2;
                 const float4 m4 =
                     *reinterpret_cast<const float4 *>(ms + box * 16384 + i * 128 + ((chunk ^ (i & 7)) << 4));
-                split3_pair(m4.x, m4.y, hi[2 * q], mid[2 * q], lo[2 * q]);
-                split3_pair(m4.z, m4.w, hi[2 * q + 1], mid[2 * q + 1], lo[2 * q + 1]);
+                if (NS == 3) {
+                    split3_pair(m4.x, m4.y, hi[2 * q], mid[2 * q], lo[2 * q]);
+                    split3_pair(m4.z, m4.w, hi[2 * q + 1], mid[2 * q + 1], lo[2 * q + 1]);
+                } else {   // hi / lo: the second part goes where mid goes
+                    split2_pair(m4.x, m4.y, hi[2 * q], mid[2 * q]);
+                    split2_pair(m4.z, m4.w, hi[2 * q + 1], mid[2 * q + 1]);
+                }
             }
             const uint32_t ab = tmem + lane_off + kTa + (uint32_t)(g & 1) * 192u + (uint32_t)(cq * 16);
             tmem_st16(ab, hi);
             tmem_st16(ab + 64u, mid);
-            tmem_st16(ab + 128u, lo);
+            if (NS == 3) tmem_st16(ab + 128u, lo);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -368,11 +401,14 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: <= 96 registers pe
                     const int off = (cq >> 1) * 16384 + i * 128 + ((chunk ^ (i & 7)) << 4);
                     uint32_t h[4], md[4], l[4];
 #pragma unroll
-                    for (int p = 0; p < 4; ++p)
-                        split3_pair(srow[8 * q + 2 * p], srow[8 * q + 2 * p + 1], h[p], md[p], l[p]);
+                    for (int p = 0; p < 4; ++p) {
+                        if (NS == 3) split3_pair(srow[8 * q + 2 * p], srow[8 * q + 2 * p + 1], h[p], md[p], l[p]);
+                        else split2_pair(srow[8 * q + 2 * p], srow[8 * q + 2 * p + 1], h[p], md[p]);
+                    }
                     *reinterpret_cast<uint4 *>(smem + off) = make_uint4(h[0], h[1], h[2], h[3]);
                     *reinterpret_cast<uint4 *>(smem + kBpart + off) = make_uint4(md[0], md[1], md[2], md[3]);
-                    *reinterpret_cast<uint4 *>(smem + 2 * kBpart + off) = make_uint4(l[0], l[1], l[2], l[3]);
+                    if (NS == 3)
+                        *reinterpret_cast<uint4 *>(smem + 2 * kBpart + off) = make_uint4(l[0], l[1], l[2], l[3]);
                 }
                 fence_async_smem();
                 __syncwarp();
@@ -507,7 +543,8 @@ cudaError_t launch_chain_dense_tc(const ChainArgs &a, cudaStream_t s) {
     if (a.S_init && !make_tensor_map_3d(&ti, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.S_init, 128, 1, urows, 32, 128,
                                         CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    auto kern = a.op ? chain_dense_tc_kernel<true> : chain_dense_tc_kernel<false>;
+    auto kern = a.two_way ? (a.op ? chain_dense_tc_kernel<true, 2> : chain_dense_tc_kernel<false, 2>)
+                          : (a.op ? chain_dense_tc_kernel<true, 3> : chain_dense_tc_kernel<false, 3>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;

@@ -47,6 +47,9 @@ struct ChainArgs {
     // rescaled by powers of two on the way; the exponent per unit goes to lam_out
     int op = 0;
     float *lam_out = nullptr;
+    // dense tensor-core chains: bf16 hi / lo operands (three products a step) instead of
+    // hi / mid / lo (six); for chains inside a scan of bf16 inputs (1e-3), not the fp32 compose
+    int two_way = 0;
 };
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (nullptr if unavailable).

@@ -756,6 +756,7 @@ cudaError_t launch_scan_kda_tc(const ScanArgs &a, cudaStream_t s) {
     c.S_init = nullptr;
     c.S_out = a.S_out;
     c.d_err = a.d_err;
+    c.two_way = 1;   // the chunk pairs carry ~1e-5 from bf16 inputs; two-way splits keep the chains at ~1e-5
     return launch_compose_prefix(c, a.lam_out, a.M_out, s);
 }
 
