@@ -121,11 +121,12 @@ int hypic_segment_scan(int fam, int in_dtype, int n_layers, int n_seg,
  *     segments' chunks evenly over the GPU and then folds the pieces of
  *     segments split between CTAs with the composition rule;
  *   the KDA family without o_t: per (layer, 64-token chunk slot, head) the
- *     chunk's pair (M_c, S_c: 2 x 65536 bytes, lambda_c and a flag: 2 x 4
- *     bytes), n_layers * (n_seg + total_tokens / 64) * n_heads of them, then
- *     n_seg + total_tokens / 64 + 1 int64 chunk starts and 2 x n_layers * n_seg
- *     int32 (each segment's first pair and count), each part rounded up to 256
- *     bytes; above 64 GiB the token-by-token kernel is used and this is 0.
+ *     chunk's pair (M_c, S_c: 2 x 65536 bytes, lambda_c: 4 bytes), n_layers *
+ *     (n_seg + total_tokens / 64) * n_heads of them, then as many int32 plus one
+ *     (the list of chunks formed token by token, with its count), n_seg +
+ *     total_tokens / 64 + 1 int64 chunk starts and 2 x n_layers * n_seg int32
+ *     (each segment's first pair and count), each part rounded up to 256 bytes;
+ *     above 64 GiB the token-by-token kernel is used and this is 0.
  */
 int64_t hypic_segment_scan_workspace_bytes(int fam, int in_dtype, int n_layers, int n_seg,
                                            int64_t total_tokens, int n_heads, int d_k, int d_v,

@@ -24,7 +24,8 @@ struct ScanArgs {
     float *ws;        // caller-owned scratch of the two-pass dense scan (or NULL)
     int *d_err;
     const int *order = nullptr;   // two-pass dense: segments longest first (or NULL: as given)
-    const int *unit_mask = nullptr;   // token-by-token kernel: only units u with unit_mask[u] != 0 (or NULL: all)
+    // token-by-token kernel: only the units unit_list[0 .. *unit_count) (device; or NULL: all)
+    const int *unit_list = nullptr, *unit_count = nullptr;
 };
 
 struct ComposeArgs {

@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     scan_kda_chunk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                           const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_m,
                           const __grid_constant__ CUtensorMap tm_s, const ScanArgs a, int64_t slots,
-                          float *pool_lam, int *steep) {
+                          float *pool_lam, int *steep_list) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_align1024(smem_raw);
     Ctl *ctl = reinterpret_cast<Ctl *>(smem + kCtl);
@@ -190,12 +190,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t n_items = (int64_t)a.n_layers * slots * a.H;
 
-    // the next chunk at or after w in this CTA's stride (slots without a chunk get flag 0)
+    // the next chunk at or after w in this CTA's stride
     auto find = [&](int64_t &w, Item &it) -> bool {
-        for (; w < n_items; w += gridDim.x) {
+        for (; w < n_items; w += gridDim.x)
             if (decode_item(a, slots, w, it)) return true;
-            if (tid == 0) steep[w] = 0;
-        }
         return false;
     };
     auto row_of = [&](const Item &it) { return (int)((int64_t)it.l * a.N + it.c0); };
@@ -295,8 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(mx <= kMaxLog2)) mx = INFINITY;   // a NaN gate counts as steep
         }
         const bool is_steep = __syncthreads_or(mx > kMaxLog2);
-        if (tid == 0) steep[u] = is_steep ? 1 : 0;
-        if (is_steep) {   // its pair comes from the token-by-token kernel; nothing here is in use
+        if (is_steep) {   // listed: its pair comes from the token-by-token kernel; nothing here is in use
+            if (tid == 0) steep_list[1 + atomicAdd(steep_list, 1)] = (int)u;
             if (have_n) {
                 if (tid == 0) {
                     load_k(nxt);
@@ -615,8 +613,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // chunk uses, the end of the segment before it -- monotone, so that the chunks form
 // a segment list for the token-by-token kernel.
 __global__ void kda_index_kernel(const ScanArgs a, int64_t slots, int32_t *seg_first, int32_t *chain_len,
-                                 int64_t *voffs) {
+                                 int64_t *voffs, int *steep_list) {
     const int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (x == 0) *steep_list = 0;   // the count of chunks listed for the token-by-token kernel
     const int64_t R = (int64_t)a.n_layers * a.n_seg;
     if (x < R) {
         const int l = (int)(x / a.n_seg), seg = (int)(x % a.n_seg);
@@ -658,7 +657,7 @@ KdaLayout kda_layout(const ScanArgs &a) {
     t.M = o;      o += up256(rows * kD * kD * 4);
     t.S = o;      o += up256(rows * kD * kD * 4);
     t.lam = o;    o += up256(rows * 4);
-    t.steep = o;  o += up256(rows * 4);
+    t.steep = o;  o += up256((rows + 1) * 4);   // count, then the listed pool rows
     t.voffs = o;  o += up256((t.slots + 1) * 8);
     t.first = o;  o += up256(R * 4);
     t.len = o;    o += up256(R * 4);
@@ -688,13 +687,13 @@ cudaError_t launch_scan_kda_tc(const ScanArgs &a, cudaStream_t s) {
     uint8_t *ws = reinterpret_cast<uint8_t *>(a.ws);
     float *pM = reinterpret_cast<float *>(ws + t.M), *pS = reinterpret_cast<float *>(ws + t.S);
     float *plam = reinterpret_cast<float *>(ws + t.lam);
-    int *steep = reinterpret_cast<int *>(ws + t.steep);
+    int *steep = reinterpret_cast<int *>(ws + t.steep);   // [0]: count, then pool rows
     int64_t *voffs = reinterpret_cast<int64_t *>(ws + t.voffs);
     int32_t *first = reinterpret_cast<int32_t *>(ws + t.first), *clen = reinterpret_cast<int32_t *>(ws + t.len);
     const int64_t R = (int64_t)a.n_layers * a.n_seg;
 
     const int64_t nidx = R > t.slots + 1 ? R : t.slots + 1;
-    kda_index_kernel<<<(unsigned)((nidx + 255) / 256), 256, 0, s>>>(a, t.slots, first, clen, voffs);
+    kda_index_kernel<<<(unsigned)((nidx + 255) / 256), 256, 0, s>>>(a, t.slots, first, clen, voffs, steep);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
@@ -724,8 +723,8 @@ cudaError_t launch_scan_kda_tc(const ScanArgs &a, cudaStream_t s) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
-    // chunks too steep for the factored Gram: their pairs token by token (every other
-    // unit of this launch returns at once)
+    // chunks too steep for the factored Gram (listed by the chunk kernel): their pairs
+    // token by token, a few CTAs walking the list
     ScanArgs f = a;
     f.n_seg = (int)t.slots;
     f.seg_offsets = voffs;
@@ -733,7 +732,8 @@ cudaError_t launch_scan_kda_tc(const ScanArgs &a, cudaStream_t s) {
     f.M_out = pM;
     f.S_out = pS;
     f.ws = nullptr;
-    f.unit_mask = steep;
+    f.unit_list = steep + 1;
+    f.unit_count = steep;
     e = launch_scan_recurrent(f, s);
     if (e != cudaSuccess) return e;
 

@@ -46,7 +46,8 @@ __device__ __forceinline__ void kahan_add(float &sum, float &comp, float v) {
     sum = t;
 }
 
-template <int FAM, int DK, typename TIn>
+// LIST: the units are a.unit_list[0 .. *a.unit_count), walked in a grid-stride loop
+template <int FAM, int DK, typename TIn, bool LIST = false>
 __global__ void __launch_bounds__(256, 2) scan_recurrent_kernel(const ScanArgs a) {
     constexpr int RPT = DK == 128 ? 64 : 32;   // rows per thread
     constexpr int G = DK / RPT;              // row groups
@@ -77,11 +78,16 @@ __global__ void __launch_bounds__(256, 2) scan_recurrent_kernel(const ScanArgs a
     float *redo = red + 2 * G * NCOL;                    // [G][DV]
     float *redm = redo + G * DV;                         // [32]
 
-    const int unit = kDense ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    // one unit per CTA (pair of CTAs with M), or with a unit list the listed units in a
+    // grid-stride loop
+    const int first = kDense ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int stride = kDense ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+    const int n_list = LIST ? *a.unit_count : 0;
+    for (int it = first; !LIST || it < n_list; it += stride) {
+    const int unit = LIST ? a.unit_list[it] : it;
     const int h = unit % a.H;
     const int seg = (unit / a.H) % a.n_seg;
     const int l = unit / (a.H * a.n_seg);
-    if (a.unit_mask && a.unit_mask[unit] == 0) return;   // the whole CTA: nothing to do here
 
     int64_t t0 = a.seg_offsets[seg], t1 = a.seg_offsets[seg + 1];
     if (!(t0 >= 0 && t0 <= t1 && t1 <= a.N)) {
@@ -251,6 +257,9 @@ __global__ void __launch_bounds__(256, 2) scan_recurrent_kernel(const ScanArgs a
         const double lam = (double)lam_sum + (double)lam_exp * 0.69314718055994530942;
         a.lam_out[u_out] = (float)lam;
     }
+    if (!LIST) break;
+    __syncthreads();   // the next listed unit reuses the shared tiles
+    }
 }
 
 template <int FAM, int DK, typename TIn>
@@ -265,11 +274,23 @@ cudaError_t launch_one(const ScanArgs &a, cudaStream_t s) {
                     (size_t)kTB * (FAM == HYPIC_DIAG || FAM == HYPIC_KDA ? DK : 1) + kTB + 2 * G * ncol + G * a.dv + 32;
     const size_t smem = floats * sizeof(float);
     auto kern = scan_recurrent_kernel<FAM, DK, TIn>;
+    // listed units: only the KDA scan's steep chunks (d = 128, bf16) use them
+    if (a.unit_list) {
+        if constexpr (FAM == HYPIC_KDA && DK == 128 && sizeof(TIn) == 2) kern = scan_recurrent_kernel<FAM, DK, TIn, true>;
+        else return cudaErrorInvalidValue;
+    }
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    const int64_t units = (int64_t)a.n_layers * a.n_seg * a.H;
+    int64_t units = (int64_t)a.n_layers * a.n_seg * a.H;
+    if (a.unit_list) {   // a few listed units at most: two CTAs (pairs with M) per SM walk them
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+            sms = 148;
+        units = units < 2 * sms ? units : 2 * sms;
+    }
     kern<<<(unsigned)(units * (kM ? 2 : 1)), nt, smem, s>>>(a);
     return cudaGetLastError();
 }

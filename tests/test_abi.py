@@ -107,10 +107,11 @@ def test_workspace_size_and_checks(lib):
     assert ws(2, 0, 1, 3, 200, 2, 128, 128, 0) == dense(1, 3, 200, 2, 49424)
     assert ws(2, 0, 1, 1, 2048, 2, 128, 128, 1) == dense(1, 1, 2048, 2, 50192)   # with o_t: Gq tiles and b_t too
     assert ws(2, 1, 1, 1, 2048, 2, 128, 128, 0) == 0     # fp32 inputs
-    def kda(L, n_seg, N, H):   # per chunk slot: M_c, S_c (fp32), lambda, steep flag; slot starts; chains
+    def kda(L, n_seg, N, H):   # per chunk slot: M_c, S_c (fp32), lambda; steep list; slot starts; chains
         slots = n_seg + N // 64
         rows = L * slots * H
-        return (2 * up(rows * 128 * 128 * 4) + 2 * up(rows * 4) + up((slots + 1) * 8) + 2 * up(L * n_seg * 4))
+        return (2 * up(rows * 128 * 128 * 4) + up(rows * 4) + up((rows + 1) * 4) + up((slots + 1) * 8)
+                + 2 * up(L * n_seg * 4))
 
     assert ws(3, 0, 30, 1, 2048, 32, 128, 128, 0) == kda(30, 1, 2048, 32)   # KDA: chunk pairs, then chains
     assert ws(3, 0, 2, 7, 592, 3, 128, 128, 0) == kda(2, 7, 592, 3)
