@@ -198,3 +198,25 @@ def test_kda_chunked_scan_uses_scratch_and_matches_token_kernel():
                         to_dev(w["seg_offsets"]), beta=dev(w["beta"]), workspace=None)
     assert rel_fro(to_host(a["S"]), to_host(b["S"])).max() <= TOL_SCAN_BF16
     assert t_err(2, to_host(a["lam"]), to_host(b["lam"]), to_host(a["M"]), to_host(b["M"])).max() <= TOL_SCAN_BF16
+
+
+@pytest.mark.parametrize("case", ["no_decay", "no_write", "all_steep"])
+def test_kda_chunked_scan_degenerate_gates(case):
+    """The tensor-core KDA scan at its degenerate gates: alpha = 1 (the delta rule
+    without decay), beta = 0 (pure per-channel decay: S = 0, T diagonal) and every
+    chunk too steep for the factored Gram (all pairs token by token)."""
+    lens = [130, 64, 1]
+    w = wl.kda_stack(lengths=lens, n_layers=1, H=2, d=128, seed=95)
+    if case == "no_decay":
+        w = dict(w, alpha=np.ones_like(w["alpha"]))
+    elif case == "no_write":
+        w = dict(w, beta=np.zeros_like(w["beta"]))
+    else:
+        w = dict(w, alpha=np.full_like(w["alpha"], np.float32(0.01)))
+    ref = oracle.segment_scan(KDA, w["k"], w["v"], w["alpha"], w["seg_offsets"], beta=w["beta"])
+    got = gpu_scan(w)
+    if case == "no_write":
+        assert np.all(to_host(got["S"]) == 0)
+    else:
+        assert rel_fro(to_host(got["S"]), ref["S"]).max() <= TOL_SCAN_BF16
+    assert t_err(2, to_host(got["lam"]), ref["lam"], to_host(got["M"]), ref["M"]).max() <= TOL_SCAN_BF16

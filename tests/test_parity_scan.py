@@ -151,6 +151,18 @@ def test_diag_o_steep_channels():
     check(DIAG, got, ref, TOL_SCAN_BF16, o_tol=TOL_O_BF16, seg_offsets=w["seg_offsets"])
 
 
+@pytest.mark.parametrize("case", ["no_decay", "all_steep"])
+def test_diag_o_degenerate_gates(case):
+    """Diagonal o_t path at alpha = 1 (plain linear attention) and with every chunk
+    too steep for the factored Gram (the exact CUDA-core Gram everywhere)."""
+    lens = [130, 64, 1, 0, 200]
+    w = wl.scalar_diag(DIAG, lengths=lens, n_layers=1, H=2, d=128, seed=12, with_q=True)
+    w["alpha"] = np.ones_like(w["alpha"]) if case == "no_decay" else np.full_like(w["alpha"], np.float32(0.02))
+    got = host(gpu_scan(w, want_o=True))
+    ref = oracle_scan(w, want_o=True)
+    check(DIAG, got, ref, TOL_SCAN_BF16, o_tol=TOL_O_BF16, seg_offsets=w["seg_offsets"])
+
+
 def test_diag_o_gla_full_size_sampled():
     """GLA-style gates, 8 segments x 2048 tokens x 32 heads with o_t (the benchmark's
     launch), sampled (segment, head) units against the straight recurrence."""
