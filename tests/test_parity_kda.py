@@ -220,3 +220,24 @@ def test_kda_chunked_scan_degenerate_gates(case):
     else:
         assert rel_fro(to_host(got["S"]), ref["S"]).max() <= TOL_SCAN_BF16
     assert t_err(2, to_host(got["lam"]), ref["lam"], to_host(got["M"]), ref["M"]).max() <= TOL_SCAN_BF16
+
+
+def test_kda_chunked_scan_bad_offsets_flag_error():
+    """A segment whose offsets leave [0, N]: reported through d_err (no fault) and
+    treated as empty (S = 0, T = I) on the tensor-core path; the others unchanged."""
+    import torch
+    import linear_attention_state_gated_gb300 as hy
+    lens = [100, 64, 70]
+    w = wl.kda_stack(lengths=lens, n_layers=1, H=2, d=128, seed=96)
+    ref = oracle.segment_scan(KDA, w["k"], w["v"], w["alpha"], w["seg_offsets"], beta=w["beta"])
+    offs = np.concatenate([w["seg_offsets"][:-1], [w["seg_offsets"][-1] + 5000]])
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bf = lambda x: to_dev(x).to(torch.bfloat16)   # noqa: E731
+    got = hy.segment_scan(KDA, bf(w["k"]), bf(w["v"]), to_dev(w["alpha"]), to_dev(offs), beta=to_dev(w["beta"]),
+                          d_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == -5
+    S, lam, M = to_host(got["S"]), to_host(got["lam"]), to_host(got["M"])
+    assert np.all(S[:, -1] == 0) and np.all(lam[:, -1] == 0)
+    assert np.array_equal(M[0, -1, 0], np.eye(128))
+    assert rel_fro(S[:, :2], ref["S"][:, :2]).max() <= TOL_SCAN_BF16
