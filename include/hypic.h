@@ -96,8 +96,11 @@ typedef enum { HYPIC_BF16 = 0, HYPIC_F32 = 1 } hypic_dtype;
  * An empty segment yields lambda = 0, M = I, S = 0.
  * Alignment: q, k, v, o_out, S_out, M_out, the diag / kda alpha and the diag
  * lambda must be 16-byte aligned; other pointers 4-byte (seg_offsets 8-byte).
- * Without a workspace the KDA family runs on the token-by-token fp32 kernel
- * (CUDA cores); hypic_segment_scan_ws takes it to the tensor cores.
+ * Kernels: with bf16 inputs and d_k = d_v = 128 every family runs on the tensor
+ * cores (scalar and diagonal with or without o_t, the gated delta rule with or
+ * without o_t); without a workspace the KDA family runs on the token-by-token
+ * fp32 kernel (CUDA cores), as do fp32 inputs, head sizes 32 / 64 and KDA with
+ * o_t; hypic_segment_scan_ws takes KDA without o_t to the tensor cores.
  */
 int hypic_segment_scan(int fam, int in_dtype, int n_layers, int n_seg,
                        int64_t total_tokens, int n_heads, int d_k, int d_v,
