@@ -241,3 +241,17 @@ def test_kda_chunked_scan_bad_offsets_flag_error():
     assert np.all(S[:, -1] == 0) and np.all(lam[:, -1] == 0)
     assert np.array_equal(M[0, -1, 0], np.eye(128))
     assert rel_fro(S[:, :2], ref["S"][:, :2]).max() <= TOL_SCAN_BF16
+
+
+def test_kda_chunked_scan_many_ragged_segments():
+    """Forty ragged segments (empty ones, one-token ones, chunk multiples) in one
+    call: every chunk slot mapping of the tensor-core path against the oracle."""
+    g = np.random.default_rng(97)
+    lens = [int(x) for x in g.integers(0, 300, size=40)]
+    lens[3], lens[7], lens[11], lens[20] = 0, 1, 64, 128
+    w = wl.kda_stack(lengths=lens, n_layers=2, H=2, d=128, seed=97)
+    ref = oracle.segment_scan(KDA, w["k"], w["v"], w["alpha"], w["seg_offsets"], beta=w["beta"])
+    got = gpu_scan(w)
+    assert rel_fro(to_host(got["S"]), ref["S"]).max() <= TOL_SCAN_BF16
+    assert t_err(2, to_host(got["lam"]), ref["lam"], to_host(got["M"]), ref["M"]).max() <= TOL_SCAN_BF16
+    assert np.all(to_host(got["S"])[:, 3] == 0)
