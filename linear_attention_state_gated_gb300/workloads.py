@@ -270,6 +270,51 @@ def long_mix_split(n_seg: int = 64, n_uncached: int = 16, seed: int = 4):
     return np.sort(g.permutation(n_seg)[:n_uncached]).astype(np.int64)
 
 
+def long_mix_layout(n_seg: int = 64, n_layers: int = 30, n_uncached: int = 16, seed: int = 4):
+    """Pool rows of the long-context mix with its layers as requests (one chain per
+    layer over all 64 segments in prompt order; n_layers = 1 in the chain call).
+
+    The uncached segments are scanned in one call that treats every (layer,
+    uncached segment) as a segment of one token array, so their pairs land at rows
+    l * n_uncached + u; cached segment c's pairs (one scan call each) at rows
+    n_layers * n_uncached + c * n_layers + l.  Returns (uncached, cached, rows) with
+    rows[l, s] the pool row of segment s at layer l (int32, the chains' seg_idx).
+    """
+    unc = [int(x) for x in long_mix_split(n_seg=n_seg, n_uncached=n_uncached, seed=seed)]
+    cached = [s for s in range(n_seg) if s not in unc]
+    rows = np.empty((n_layers, n_seg), np.int32)
+    for u, s in enumerate(unc):
+        rows[:, s] = np.arange(n_layers) * len(unc) + u
+    for c, s in enumerate(cached):
+        rows[:, s] = n_layers * len(unc) + c * n_layers + np.arange(n_layers)
+    return unc, cached, rows
+
+
+def long_mix_uncached_flat(unc, seg_len: int = 2048, n_layers: int = 30, H: int = 32, d: int = 128,
+                           seed: int = 4, device="cuda"):
+    """The uncached segments' inputs (same draws as ``long_mix_segment_device``) as
+    one token array for a single scan call: tokens ordered (layer, uncached segment,
+    token), shapes [1, n_layers * len(unc) * seg_len, H, d] (bf16 q, k, v) and
+    [1, ..., H] (fp32 alpha, beta); offsets of the n_layers * len(unc) segments."""
+    import torch
+    n = n_layers * len(unc) * seg_len
+    flat = {"k": torch.empty((1, n, H, d), dtype=torch.bfloat16, device=device),
+            "v": torch.empty((1, n, H, d), dtype=torch.bfloat16, device=device),
+            "q": torch.empty((1, n, H, d), dtype=torch.bfloat16, device=device),
+            "alpha": torch.empty((1, n, H), dtype=torch.float32, device=device),
+            "beta": torch.empty((1, n, H), dtype=torch.float32, device=device)}
+    for u, s in enumerate(unc):
+        w = long_mix_segment_device(s, seg_len=seg_len, n_layers=n_layers, H=H, d=d, seed=seed, with_q=True,
+                                    device=device)
+        for l in range(n_layers):
+            a = (l * len(unc) + u) * seg_len
+            for key in flat:
+                flat[key][0, a:a + seg_len] = w[key][l]
+        del w
+    offs = np.arange(n_layers * len(unc) + 1, dtype=np.int64) * seg_len
+    return flat, offs
+
+
 def _seed_key(*parts) -> int:
     x = 0
     for p in parts:

@@ -377,36 +377,41 @@ def test_bad_offsets_flag_error_without_fault():
 
 def test_long_mix_full_size_sampled():
     """131072-token prompt, 64 x 2048 segments (48 cached / 16 uncached), gated
-    delta rule, 30 layers x 32 heads (the benchmark's launches): the state folded
-    over all 64 pairs equals the straight recurrence over the prompt (sampled
-    layer and head, oracle), segment-boundary states equal the oracle's own
-    composition of its pairs, and o_t of an uncached segment equals the
-    oracle's isolated scan."""
+    delta rule, 30 layers x 32 heads, in the benchmark's launches (cached segments
+    one scan call each; the 16 uncached in one call over their (layer, segment)
+    units, with o_t; chains with the layers as requests): the state folded over
+    all 64 pairs equals the straight recurrence over the prompt (sampled layer and
+    head, oracle), segment-boundary states equal the oracle's own composition of
+    its pairs, and o_t of an uncached segment equals the oracle's isolated scan."""
     import torch
     import linear_attention_state_gated_gb300 as hy
     n_seg, L, Lyr, H, d = 64, 2048, 30, 32, 128
-    unc = [int(x) for x in wl.long_mix_split(n_seg=n_seg)]
+    unc, cached, rows = wl.long_mix_layout(n_seg=n_seg, n_layers=Lyr)
+    nu = len(unc)
     dev = torch.device("cuda")
-    offs = torch.tensor([0, L], dtype=torch.int64, device=dev)
-    pool_lam = torch.empty((n_seg, Lyr, H), dtype=torch.float32, device=dev)
-    pool_M = torch.empty((n_seg, Lyr, H, d, d), dtype=torch.float32, device=dev)
-    pool_S = torch.empty((n_seg, Lyr, H, d, d), dtype=torch.float32, device=dev)
-    o_first = None
-    for s in range(n_seg):
-        w = wl.long_mix_segment_device(s, seg_len=L, n_layers=Lyr, H=H, d=d, with_q=s in unc)
-        out = {"lam": pool_lam[s].view(Lyr, 1, H), "M": pool_M[s].view(Lyr, 1, H, d, d),
-               "S": pool_S[s].view(Lyr, 1, H, d, d)}
-        r = hy.segment_scan(2, w["k"], w["v"], w["alpha"], offs, beta=w["beta"], q=w.get("q"),
-                            want_o=s == unc[0], out=out)
-        if s == unc[0]:
-            o_first = r["o"]
+    P = Lyr * n_seg
+    pool_lam = torch.empty((P, 1, H), dtype=torch.float32, device=dev)
+    pool_M = torch.empty((P, 1, H, d, d), dtype=torch.float32, device=dev)
+    pool_S = torch.empty((P, 1, H, d, d), dtype=torch.float32, device=dev)
+    offs1 = torch.tensor([0, L], dtype=torch.int64, device=dev)
+    for c, s in enumerate(cached):
+        w = wl.long_mix_segment_device(s, seg_len=L, n_layers=Lyr, H=H, d=d, with_q=False)
+        r0 = Lyr * nu + c * Lyr
+        out = {"lam": pool_lam[r0:r0 + Lyr].view(Lyr, 1, H), "M": pool_M[r0:r0 + Lyr].view(Lyr, 1, H, d, d),
+               "S": pool_S[r0:r0 + Lyr].view(Lyr, 1, H, d, d)}
+        hy.segment_scan(2, w["k"], w["v"], w["alpha"], offs1, beta=w["beta"], out=out)
         del w
-    # prefix chains: request r folds segments 0..r
-    clen = torch.arange(1, n_seg + 1, dtype=torch.int32, device=dev)
-    idx = torch.arange(n_seg, dtype=torch.int32, device=dev)[None].repeat(n_seg, 1).contiguous()
+    flat, offs = wl.long_mix_uncached_flat(unc, seg_len=L, n_layers=Lyr, H=H, d=d)
+    out = {"lam": pool_lam[:Lyr * nu].view(1, Lyr * nu, H), "M": pool_M[:Lyr * nu].view(1, Lyr * nu, H, d, d),
+           "S": pool_S[:Lyr * nu].view(1, Lyr * nu, H, d, d)}
+    o = hy.segment_scan(2, flat["k"], flat["v"], flat["alpha"], to_dev(offs), beta=flat["beta"], q=flat["q"],
+                        want_o=True, out=out)["o"]
+    del flat
+    # prefix chains of the sampled layer: request r folds segments 0..r in prompt order
     l, h = 17, 5
-    S_pref = hy.compose_chain(2, clen, idx, pool_lam[:, l:l + 1].contiguous(),
-                              pool_S[:, l:l + 1].contiguous(), pool_M=pool_M[:, l:l + 1].contiguous())
+    clen = torch.arange(1, n_seg + 1, dtype=torch.int32, device=dev)
+    idx = torch.from_numpy(np.ascontiguousarray(np.repeat(rows[l][None], n_seg, axis=0))).to(dev)
+    S_pref = hy.compose_chain(2, clen, idx, pool_lam, pool_S, pool_M=pool_M)
     S_pref = to_host(S_pref[:, 0, h])
     # oracle: inputs of the sampled layer and head for every segment
     parts = [wl.long_mix_segment_device(s, seg_len=L, n_layers=Lyr, H=H, d=d, layers=[l], heads=[h])
@@ -423,9 +428,10 @@ def test_long_mix_full_size_sampled():
     for r in (0, 15, 31, 62):
         ref = oracle.compose_chain(DENSE, [r + 1], np.arange(n_seg, dtype=np.int32)[None], pl, pS, pool_M=pM)
         assert rel_fro(S_pref[r], ref[0, 0, 0]) <= TOL_SCAN_BF16, r
-    # o_t of the first uncached segment from its own zero start
+    # o_t of the first uncached segment from its own zero start (rows of (layer l, uncached 0))
     a0 = unc[0] * L
     iso = oracle.segment_scan(DENSE, cat["k"][:, a0:a0 + L], cat["v"][:, a0:a0 + L], cat["alpha"][:, a0:a0 + L],
                               [0, L], beta=cat["beta"][:, a0:a0 + L], q=cat["q"][:, a0:a0 + L], want_o=True)
-    go = to_host(o_first[l, :, h])
+    f0 = (l * nu + 0) * L
+    go = to_host(o[0, f0:f0 + L, h])
     assert rel_fro(go, iso["o"][0, :, 0], axes=(-2, -1)) <= TOL_O_BF16
