@@ -1169,6 +1169,19 @@ static_assert(PairSmem::Stage % 1024 == 0 && PairSmem::Tiles % 1024 == 0 && Pair
 static_assert((hypic::Rec<false>::GateFloats * 4) % 16 == 0, "gate copy in 16-byte units");
 
 // max over the 16 conversion warps (named barrier 2)
+// max over the 8 warps of one half's group (named barrier 2 + half)
+__device__ __forceinline__ float group_max(float mx, PairCtl *ctl, int x, int gw, int lane) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (lane == 0) ctl->redmax[x * 8 + gw] = mx;
+    bar_sync(2 + x, kState / 2);
+    mx = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) mx = fmaxf(mx, ctl->redmax[x * 8 + w]);
+    bar_sync(2 + x, kState / 2);
+    return mx;
+}
+
 __device__ __forceinline__ float pair_max(float mx, PairCtl *ctl, int sw, int lane) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
@@ -1440,23 +1453,30 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             }
         }
     } else {
-        // ------------------------------------------------------------ conversion warps
+        // ------------------------------------------------------------ conversion warps: warps
+        // 3..10 take the transition half, warps 11..18 the state half, each group its own
+        // pipeline (named barrier 2 + half) with two 16-column groups a thread, so that one
+        // half's conversions run while the other half's products do
         const int st = threadIdx.x - 96;            // 0..511
         const int sw = warp - 3;                    // 0..15
-        const int cg = sw >> 2;                     // row group of this warp (16 rows k per k half)
+        const int x = sw >> 3;                      // this group's half
+        const int gt = st & 255;                    // thread within the group
+        const int sub = (sw >> 2) & 1;              // column groups 2 sub and 2 sub + 1
         const int quarter = warp & 3;               // TMEM lanes this warp may touch
         const int m = quarter * 32 + lane;          // column of X = TMEM lane
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const int gbar = 2 + x;
         int lam_exp = 0;
         double lam_d = 0.0;
         float ls = 0.f;
 
-        {   // initial X^T: identity (transition) and zero (state)
+        {   // initial X^T of this half: identity (transition) or zero (state)
             uint32_t r[16];
 #pragma unroll
-            for (int x = 0; x < 2; ++x)
+            for (int c2 = 0; c2 < 2; ++c2)
 #pragma unroll
                 for (int p = 0; p < 2; ++p) {
+                    const int cg = sub * 2 + c2;
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
                         r[i] = __float_as_uint((x == 0 && p * 64 + cg * 16 + i == m) ? 1.f : 0.f);
@@ -1470,87 +1490,89 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             const int s = j % kNS;
             const uint32_t par = (uint32_t)j & 1u;
             const float *gates = ctl->gates[s];
-            HalfScale z[2];
+            // ---- X0 of this half: the chunk is in and the half's previous update is done
+            bool ok = wait_or_abort(&ctl->full[s], (uint32_t)(j / kNS) & 1u, abortp);
+            if (j > 0) ok = ok && wait_or_abort(&ctl->x_done[x], par ^ 1u, abortp);
+            if (!bar_and(gbar, kState / 2, ok)) {
+                alive = false;
+                break;
+            }
+            tc_fence_after();
+            const HalfScale z = pair_scale(x, j, gates, ls, lam_d, gt == 0);
+            float g = z.g;
+            if (x == 0 && z.renorm) {   // the transition's power-of-two renormalisation
+                float mx = 0.f;
 #pragma unroll
-            for (int x = 0; x < 2; ++x) {
-                // ---- X0 of this half: the chunk is in and the half's previous update is done
-                bool ok = wait_or_abort(&ctl->full[s], (uint32_t)(j / kNS) & 1u, abortp);
-                if (j > 0) ok = ok && wait_or_abort(&ctl->x_done[x], par ^ 1u, abortp);
-                if (!bar_and(2, kState, ok)) {
-                    alive = false;
-                    break;
-                }
-                tc_fence_after();
-                z[x] = pair_scale(x, j, gates, ls, lam_d, st == 0);
-                float g = z[x].g;
-                const uint32_t tx = tmem + lane_off + kPX(x) + (uint32_t)(cg * 16);
-                if (x == 0 && z[x].renorm) {   // the transition's power-of-two renormalisation
-                    float mx = 0.f;
+                for (int c2 = 0; c2 < 2; ++c2)
 #pragma unroll
                     for (int p = 0; p < 2; ++p) {
                         uint32_t r[16];
-                        tmem_ld16(tx + (uint32_t)(p * 64), r);
+                        tmem_ld16(tmem + lane_off + kPX(0) + (uint32_t)(p * 64 + (sub * 2 + c2) * 16), r);
                         tmem_wait_ld();
 #pragma unroll
                         for (int i = 0; i < 16; ++i) mx = fmaxf(mx, fabsf(__uint_as_float(r[i])));
                     }
-                    const int e = exponent_of(pair_max(mx, ctl, sw, lane));
-                    g = ldexpf(1.f, -e);
-                    lam_exp += e;
-                }
-                pair_x0(tx, tmem + lane_off + kPXh(x) + (uint32_t)(cg * 8), smem + SM::X0lo + x * 32768, m, cg,
-                        g * z[x].fP, g * z[x].wscale, z[x].renorm, ctl->xop_ready[x], lane);
+                const int e = exponent_of(group_max(mx, ctl, x, sw & 7, lane));
+                g = ldexpf(1.f, -e);
+                lam_exp += e;
             }
-            if (!alive) break;
 #pragma unroll
-            for (int x = 0; x < 2; ++x) {
-                // ---- Delta~ of this half, once its Delta products are done
-                if (!bar_and(2, kState, wait_or_abort(&ctl->d_done[x], par, abortp))) {
-                    alive = false;
-                    break;
-                }
-                tc_fence_after();
-                pair_dt(tmem + lane_off + kPD(x) + (uint32_t)(cg * 16), z[x].fD, gates + (R::Gw - R::G), cg, lane,
+            for (int c2 = 0; c2 < 2; ++c2) {
+                const int cg = sub * 2 + c2;
+                pair_x0(tmem + lane_off + kPX(x) + (uint32_t)(cg * 16), tmem + lane_off + kPXh(x) + (uint32_t)(cg * 8),
+                        smem + SM::X0lo + x * 32768, m, cg, g * z.fP, g * z.wscale, z.renorm, ctl->xop_ready[x], lane);
+            }
+            // ---- Delta~ of this half, once its Delta products are done
+            if (!bar_and(gbar, kState / 2, wait_or_abort(&ctl->d_done[x], par, abortp))) {
+                alive = false;
+                break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2) {
+                const int cg = sub * 2 + c2;
+                pair_dt(tmem + lane_off + kPD(x) + (uint32_t)(cg * 16), z.fD, gates + (R::Gw - R::G), cg, lane,
                         &ctl->dt_ready[x]);
             }
         }
 
-        // ------------------------------------------------------------ epilogue
+        // ------------------------------------------------------------ epilogue: this half
         bool ok = alive;
-        if (ok && nc > 0)
-            ok = wait_or_abort(&ctl->x_done[0], (uint32_t)(nc - 1) & 1u, abortp) &&
-                 wait_or_abort(&ctl->x_done[1], (uint32_t)(nc - 1) & 1u, abortp);
-        if (bar_and(2, kState, ok)) {
+        if (ok && nc > 0) ok = wait_or_abort(&ctl->x_done[x], (uint32_t)(nc - 1) & 1u, abortp);
+        if (bar_and(gbar, kState / 2, ok)) {
             tc_fence_after();
             const int64_t u_out = ((int64_t)l * a.n_seg + seg) * a.H + h;
+            uint32_t r[2][2][16];
 #pragma unroll
-            for (int x = 0; x < 2; ++x) {
-                const uint32_t tx = tmem + lane_off + kPX(x) + (uint32_t)(cg * 16);
-                uint32_t r[2][16];
-                tmem_ld16(tx, r[0]);
-                tmem_ld16(tx + 64u, r[1]);
-                tmem_wait_ld();
-                float scale;
-                if (x == 0) {
-                    float mx = 0.f;
+            for (int c2 = 0; c2 < 2; ++c2)
+#pragma unroll
+                for (int p = 0; p < 2; ++p)
+                    tmem_ld16(tmem + lane_off + kPX(x) + (uint32_t)(p * 64 + (sub * 2 + c2) * 16), r[c2][p]);
+            tmem_wait_ld();
+            float scale;
+            if (x == 0) {
+                float mx = 0.f;
+#pragma unroll
+                for (int c2 = 0; c2 < 2; ++c2)
 #pragma unroll
                     for (int p = 0; p < 2; ++p)
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) mx = fmaxf(mx, fabsf(__uint_as_float(r[p][i])));
-                    const int e = exponent_of(pair_max(mx, ctl, sw, lane));
-                    scale = ldexpf(1.f, -e);
-                    lam_exp += e;
-                    if (st == 0) a.lam_out[u_out] = (float)(lam_d + (double)lam_exp * 0.69314718055994530942);
-                } else {
-                    scale = expf(ls);
-                }
-                float *out = (x == 0 ? a.M_out : a.S_out) + u_out * kD * kD;
+                        for (int i = 0; i < 16; ++i) mx = fmaxf(mx, fabsf(__uint_as_float(r[c2][p][i])));
+                const int e = exponent_of(group_max(mx, ctl, x, sw & 7, lane));
+                scale = ldexpf(1.f, -e);
+                lam_exp += e;
+                if (gt == 0) a.lam_out[u_out] = (float)(lam_d + (double)lam_exp * 0.69314718055994530942);
+            } else {
+                scale = expf(ls);
+            }
+            float *out = (x == 0 ? a.M_out : a.S_out) + u_out * kD * kD;
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2)
 #pragma unroll
                 for (int p = 0; p < 2; ++p)
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
-                        out[(int64_t)(p * 64 + cg * 16 + i) * kD + m] = scale * __uint_as_float(r[p][i]);
-            }
+                        out[(int64_t)(p * 64 + (sub * 2 + c2) * 16 + i) * kD + m] = scale * __uint_as_float(r[c2][p][i]);
         } else {
             *abortp = 1;
         }
