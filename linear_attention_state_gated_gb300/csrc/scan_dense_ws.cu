@@ -1168,7 +1168,6 @@ static_assert(PairSmem::Stage % 1024 == 0 && PairSmem::Tiles % 1024 == 0 && Pair
               "operand tiles 1024-byte aligned");
 static_assert((hypic::Rec<false>::GateFloats * 4) % 16 == 0, "gate copy in 16-byte units");
 
-// max over the 16 conversion warps (named barrier 2)
 // max over the 8 warps of one half's group (named barrier 2 + half)
 __device__ __forceinline__ float group_max(float mx, PairCtl *ctl, int x, int gw, int lane) {
 #pragma unroll
@@ -1179,18 +1178,6 @@ __device__ __forceinline__ float group_max(float mx, PairCtl *ctl, int x, int gw
 #pragma unroll
     for (int w = 0; w < 8; ++w) mx = fmaxf(mx, ctl->redmax[x * 8 + w]);
     bar_sync(2 + x, kState / 2);
-    return mx;
-}
-
-__device__ __forceinline__ float pair_max(float mx, PairCtl *ctl, int sw, int lane) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    if (lane == 0) ctl->redmax[sw] = mx;
-    bar_sync(2, kState);
-    mx = 0.f;
-#pragma unroll
-    for (int w = 0; w < 16; ++w) mx = fmaxf(mx, ctl->redmax[w]);
-    bar_sync(2, kState);
     return mx;
 }
 
