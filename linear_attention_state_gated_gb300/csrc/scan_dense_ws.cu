@@ -1129,12 +1129,14 @@ __global__ void __maxnreg__(80)
 // conversions overlap the other half's tensor products.  -W^T comes ready from
 // the record (the preparation pass built it), so both halves read one copy.
 // Each half has its own X0 operand: hi in TMEM, lo in shared memory (TMEM holds
-// X, X0 hi and Delta of both halves: 2 x (128 + 64 + 64) columns).  Per chunk j
-// the conversion warps run
-//   X0_M(j) | X0_S(j) | Delta~_M(j) | Delta~_S(j)
-// while the two issuing threads (one per half) run, per chunk,
-//   [U^T ->] Delta^T = U^T - X0^T W^T (three-term split) | X^T += Delta~^T K.
-// 19 warps: 0 TMA, 1 issuer for M, 2 issuer for S, 3-18 conversions.
+// X, X0 hi and Delta of both halves: 2 x (128 + 64 + 64) columns).  Each half has
+// its own group of eight conversion warps, which per chunk j run
+//   X0(j) | Delta~(j)
+// while that half's issuing thread runs
+//   [U^T ->] Delta^T = U^T - X0^T W^T (three-term split) | X^T += Delta~^T K,
+// so the halves' pipelines advance independently on one tensor pipe.
+// 19 warps: 0 TMA, 1 issuer for M, 2 issuer for S, 3-10 conversions for M,
+// 11-18 conversions for S.
 
 constexpr int kPairThreads = 608;
 struct PairSmem {
