@@ -1155,7 +1155,7 @@ __device__ __forceinline__ uint32_t kPD(int x) { return (uint32_t)x * 256u + 192
 struct PairCtl {
     uint64_t full[kNS], empty[kNS];
     uint64_t xop_ready[2][2];   // [half][k half] the half's X0 operand is in place
-    uint64_t dt_ready[2];       // the half's Delta~ is in place
+    uint64_t dt_ready[2][4];    // [half][16-token block] the half's Delta~ block is in place
     uint64_t d_done[2];         // the half's Delta products are done
     uint64_t x_done[2];         // the half's update is done
     uint64_t drain[2];
@@ -1327,7 +1327,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         for (int x = 0; x < 2; ++x) {
             mbar_init(&ctl->xop_ready[x][0], kState / 32);
             mbar_init(&ctl->xop_ready[x][1], kState / 32);
-            mbar_init(&ctl->dt_ready[x], kState / 32);
+            for (int q = 0; q < 4; ++q) mbar_init(&ctl->dt_ready[x][q], 4);   // the 4 warps converting block q
             mbar_init(&ctl->d_done[x], 1);
             mbar_init(&ctl->x_done[x], 1);
             mbar_init(&ctl->drain[x], 1);
@@ -1423,16 +1423,19 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 }
                 if (!ok) break;
                 mma_commit(&ctl->d_done[x]);
-                // ---- X^T += Delta~^T K (K as the MN-major B operand: row t, channels contiguous)
-                if (!wait_or_abort(&ctl->dt_ready[x], par, abortp)) break;
-                tc_fence_after();
+                // ---- X^T += Delta~^T K (K as the MN-major B operand: row t, channels contiguous),
+                // each 16-token block as soon as its Delta~ is converted (lo, then hi)
                 const uint32_t kb = smem_addr(stg + SM::K);
+                for (int ks = 0; ks < 4 && ok; ++ks) {
+                    ok = wait_or_abort(&ctl->dt_ready[x][ks], par, abortp);
+                    if (!ok) break;
+                    tc_fence_after();
 #pragma unroll
-                for (int hl = 1; hl >= 0; --hl)
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
+                    for (int hl = 1; hl >= 0; --hl)
                         mma_f16_ta(tmem + kPX(x), dacc + (uint32_t)ks * 16u + (uint32_t)hl * 8u,
                                    smem_desc_sw128(kb + (uint32_t)ks * 2048u, kBox, 1024), id_x, 1u);
+                }
+                if (!ok) break;
                 mma_commit(&ctl->x_done[x]);
                 mma_commit(&ctl->empty[s]);
             }
@@ -1521,7 +1524,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             for (int c2 = 0; c2 < 2; ++c2) {
                 const int cg = sub * 2 + c2;
                 pair_dt(tmem + lane_off + kPD(x) + (uint32_t)(cg * 16), z.fD, gates + (R::Gw - R::G), cg, lane,
-                        &ctl->dt_ready[x]);
+                        &ctl->dt_ready[x][cg]);
             }
         }
 
