@@ -1183,33 +1183,35 @@ __device__ __forceinline__ float group_max(float mx, PairCtl *ctl, int x, int gw
     return mx;
 }
 
-// X0 operand of one half: this thread's 2 x 16 rows k of its column m of X, times
-// `mult`, split into bf16 hi (TMEM, A operand) and lo (shared memory, K-major
-// row m, 128-byte swizzle); X rewritten times `sc` when `rewrite`; each k half
-// announced as soon as it is in place
-__device__ __forceinline__ void pair_x0(uint32_t tx, uint32_t txh, uint8_t *lo_tile, int m, int cg, float mult,
+// X0 operand of one half: this thread's 32 rows k (two 16-row groups) of its column m
+// of X in each k half, times `mult`, split into bf16 hi (TMEM, A operand) and lo
+// (shared memory, K-major row m, 128-byte swizzle); X rewritten times `sc` when
+// `rewrite`; each k half announced as soon as it is in place.  One TMEM load per
+// k half (32 columns), so the first k half is ready after one load round trip.
+__device__ __forceinline__ void pair_x0(uint32_t tx, uint32_t txh, uint8_t *lo_tile, int m, int sub, float mult,
                                        float sc, bool rewrite, uint64_t *ready, int lane) {
     const uint64_t mult2 = pk2(mult, mult);
 #pragma unroll
     for (int p = 0; p < 2; ++p) {
-        uint32_t r[16], hi[8], lo[8];
-        tmem_ld16(tx + (uint32_t)(p * 64), r);
+        uint32_t r[32], hi[16], lo[16];
+        tmem_ld32(tx + (uint32_t)(p * 64 + sub * 32), r);
         tmem_wait_ld();
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
+        for (int q = 0; q < 16; ++q) {
             float x0, x1;
             upk2(mul2(mult2, pk2(__uint_as_float(r[2 * q]), __uint_as_float(r[2 * q + 1]))), x0, x1);
             split_pair(x0, x1, hi[q], lo[q]);
         }
-        tmem_st8(txh + (uint32_t)(p * 32), hi);
+        tmem_st16(txh + (uint32_t)(p * 32 + sub * 16), hi);
         uint8_t *row = lo_tile + p * 16384 + m * 128;
-        const int c0 = 2 * cg;   // this thread's two 16-byte groups of the row
-        *reinterpret_cast<uint4 *>(row + ((c0 ^ (m & 7)) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        *reinterpret_cast<uint4 *>(row + (((c0 + 1) ^ (m & 7)) << 4)) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+#pragma unroll
+        for (int g = 0; g < 4; ++g)   // this thread's four 16-byte groups of the row
+            *reinterpret_cast<uint4 *>(row + (((4 * sub + g) ^ (m & 7)) << 4)) =
+                make_uint4(lo[4 * g], lo[4 * g + 1], lo[4 * g + 2], lo[4 * g + 3]);
         if (rewrite) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(sc * __uint_as_float(r[i]));
-            tmem_st16(tx + (uint32_t)(p * 64), r);
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(sc * __uint_as_float(r[i]));
+            tmem_st32(tx + (uint32_t)(p * 64 + sub * 32), r);
         }
         tmem_wait_st();
         fence_async_smem();
@@ -1219,35 +1221,43 @@ __device__ __forceinline__ void pair_x0(uint32_t tx, uint32_t txh, uint8_t *lo_t
     }
 }
 
-// Delta~^T = fD Delta^T diag(b_C / b) in place (this thread's 16 tokens), bf16 hi / lo
-__device__ __forceinline__ void pair_dt(uint32_t tacc, float fD, const float *gw, int cg, int lane,
+// Delta~^T = fD Delta^T diag(b_C / b) in place, this thread's 32 tokens (16-token
+// blocks 2 sub and 2 sub + 1, one TMEM load), bf16 hi / lo; each block announced
+// as soon as it is in place
+__device__ __forceinline__ void pair_dt(uint32_t tacc, float fD, const float *gw, int sub, int lane,
                                         uint64_t *ready) {
-    uint32_t r[16], hi[8], lo[8];
-    tmem_ld16(tacc, r);
-    const float4 *g4 = reinterpret_cast<const float4 *>(gw + cg * 16);
-    float sc[16];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float4 gv = g4[i];
-        sc[4 * i] = fD * gv.x;
-        sc[4 * i + 1] = fD * gv.y;
-        sc[4 * i + 2] = fD * gv.z;
-        sc[4 * i + 3] = fD * gv.w;
-    }
+    uint32_t r[32];
+    tmem_ld32(tacc + (uint32_t)(sub * 32), r);
     tmem_wait_ld();
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        float x0, x1;
-        upk2(mul2(pk2(sc[2 * q], sc[2 * q + 1]), pk2(__uint_as_float(r[2 * q]), __uint_as_float(r[2 * q + 1]))), x0,
-             x1);
-        split_pair(x0, x1, hi[q], lo[q]);
+    for (int c2 = 0; c2 < 2; ++c2) {
+        const int cg = sub * 2 + c2;
+        const float4 *g4 = reinterpret_cast<const float4 *>(gw + cg * 16);
+        float sc[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float4 gv = g4[i];
+            sc[4 * i] = fD * gv.x;
+            sc[4 * i + 1] = fD * gv.y;
+            sc[4 * i + 2] = fD * gv.z;
+            sc[4 * i + 3] = fD * gv.w;
+        }
+        uint32_t hi[8], lo[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            float x0, x1;
+            upk2(mul2(pk2(sc[2 * q], sc[2 * q + 1]),
+                      pk2(__uint_as_float(r[c2 * 16 + 2 * q]), __uint_as_float(r[c2 * 16 + 2 * q + 1]))),
+                 x0, x1);
+            split_pair(x0, x1, hi[q], lo[q]);
+        }
+        tmem_st8(tacc + (uint32_t)(cg * 16), hi);
+        tmem_st8(tacc + (uint32_t)(cg * 16 + 8), lo);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ready[cg]);
     }
-    tmem_st8(tacc, hi);
-    tmem_st8(tacc + 8u, lo);
-    tmem_wait_st();
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(ready);
 }
 
 // Scale bookkeeping of one half for one chunk (as the two-CTA form).  Transition
@@ -1295,7 +1305,7 @@ __device__ __forceinline__ HalfScale pair_scale(int h, int j, const float *gates
 
 __global__ void __launch_bounds__(kPairThreads, 1)
     dense_pair_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                      const ScanArgs a, int64_t slots) {
+                      const ScanArgs a, int64_t slots, int n_pair) {
     using R = Rec<false>;
     using SM = PairSmem;
     extern __shared__ uint8_t smem_raw[];
@@ -1305,8 +1315,13 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // chains in the order of their segments, longest first (all layers and heads of
-    // a segment together), so that the last wave holds the shortest chains
-    const int unit = blockIdx.x;
+    // a segment together), so that the last wave holds the shortest chains.  CTAs
+    // [0, n_pair) run both halves of chain blockIdx.x; each CTA after them runs one
+    // half of one of the remaining chains (a last wave shorter than half the SMs is
+    // spread over twice as many SMs)
+    const bool split = (int)blockIdx.x >= n_pair;
+    const int unit = split ? n_pair + (((int)blockIdx.x - n_pair) >> 1) : (int)blockIdx.x;
+    const int only = split ? (((int)blockIdx.x - n_pair) & 1) : -1;   // the one half run here, or -1
     const int rank = unit / (a.H * a.n_layers);
     const int l = (unit / a.H) % a.n_layers;
     const int h = unit % a.H;
@@ -1322,11 +1337,11 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         if (bad) flag_index_error(a.d_err);
         for (int s = 0; s < kNS; ++s) {
             mbar_init(&ctl->full[s], 1);
-            mbar_init(&ctl->empty[s], 2);   // both issuers' updates read the stage last
+            mbar_init(&ctl->empty[s], split ? 1 : 2);   // the issuers' updates read the stage last
         }
         for (int x = 0; x < 2; ++x) {
-            mbar_init(&ctl->xop_ready[x][0], kState / 32);
-            mbar_init(&ctl->xop_ready[x][1], kState / 32);
+            mbar_init(&ctl->xop_ready[x][0], kState / 64);   // the half's 8 conversion warps
+            mbar_init(&ctl->xop_ready[x][1], kState / 64);
             for (int q = 0; q < 4; ++q) mbar_init(&ctl->dt_ready[x][q], 4);   // the 4 warps converting block q
             mbar_init(&ctl->d_done[x], 1);
             mbar_init(&ctl->x_done[x], 1);
@@ -1373,7 +1388,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     } else if (warp <= 2) {
         // ------------------------------------------------------------ MMA issuers: warp 1 the
         // transition half, warp 2 the state half
-        if (lane == 0) {
+        if (lane == 0 && (only < 0 || only == warp - 1)) {
             const int x = warp - 1;
             const uint32_t dacc = tmem + kPD(x);
             const uint32_t lo_t = smem_addr(smem + SM::X0lo + x * 32768);
@@ -1444,7 +1459,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 mbar_wait(&ctl->drain[x], 0);
             }
         }
-    } else {
+    } else if (only < 0 || ((warp - 3) >> 3) == only) {
         // ------------------------------------------------------------ conversion warps: warps
         // 3..10 take the transition half, warps 11..18 the state half, each group its own
         // pipeline (named barrier 2 + half) with two 16-column groups a thread, so that one
@@ -1495,37 +1510,26 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             if (x == 0 && z.renorm) {   // the transition's power-of-two renormalisation
                 float mx = 0.f;
 #pragma unroll
-                for (int c2 = 0; c2 < 2; ++c2)
+                for (int p = 0; p < 2; ++p) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + lane_off + kPX(0) + (uint32_t)(p * 64 + sub * 32), r);
+                    tmem_wait_ld();
 #pragma unroll
-                    for (int p = 0; p < 2; ++p) {
-                        uint32_t r[16];
-                        tmem_ld16(tmem + lane_off + kPX(0) + (uint32_t)(p * 64 + (sub * 2 + c2) * 16), r);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) mx = fmaxf(mx, fabsf(__uint_as_float(r[i])));
-                    }
+                    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fabsf(__uint_as_float(r[i])));
+                }
                 const int e = exponent_of(group_max(mx, ctl, x, sw & 7, lane));
                 g = ldexpf(1.f, -e);
                 lam_exp += e;
             }
-#pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2) {
-                const int cg = sub * 2 + c2;
-                pair_x0(tmem + lane_off + kPX(x) + (uint32_t)(cg * 16), tmem + lane_off + kPXh(x) + (uint32_t)(cg * 8),
-                        smem + SM::X0lo + x * 32768, m, cg, g * z.fP, g * z.wscale, z.renorm, ctl->xop_ready[x], lane);
-            }
+            pair_x0(tmem + lane_off + kPX(x), tmem + lane_off + kPXh(x), smem + SM::X0lo + x * 32768, m, sub,
+                    g * z.fP, g * z.wscale, z.renorm, ctl->xop_ready[x], lane);
             // ---- Delta~ of this half, once its Delta products are done
             if (!bar_and(gbar, kState / 2, wait_or_abort(&ctl->d_done[x], par, abortp))) {
                 alive = false;
                 break;
             }
             tc_fence_after();
-#pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2) {
-                const int cg = sub * 2 + c2;
-                pair_dt(tmem + lane_off + kPD(x) + (uint32_t)(cg * 16), z.fD, gates + (R::Gw - R::G), cg, lane,
-                        &ctl->dt_ready[x][cg]);
-            }
+            pair_dt(tmem + lane_off + kPD(x), z.fD, gates + (R::Gw - R::G), sub, lane, ctl->dt_ready[x]);
         }
 
         // ------------------------------------------------------------ epilogue: this half
@@ -1606,6 +1610,14 @@ __global__ void __launch_bounds__(1024) lpt_order_kernel(const int64_t *seg_offs
     }
 }
 
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        n = 148;
+    return n;
+}
+
 // bytes of the records (then the order array, 256-byte aligned)
 int64_t records_bytes(const ScanArgs &a) {
     const int64_t b = (int64_t)a.n_layers * a.H * n_slots(a.N, a.n_seg) * (a.o_out ? Rec<true>::Bytes : Rec<false>::Bytes);
@@ -1648,7 +1660,12 @@ cudaError_t launch_two_pass(const ScanArgs &a0, cudaStream_t s) {
     } else {
         e = cudaFuncSetAttribute(dense_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, pair_smem());
         if (e != cudaSuccess) return e;
-        dense_pair_kernel<<<(unsigned)units, kPairThreads, pair_smem(), s>>>(mk, mv, a, slots);
+        // one CTA per SM: a last wave of at most half the SMs runs its chains' halves
+        // on separate SMs (a lone half steps faster than an interleaved pair)
+        const int64_t sms = sm_count(), tail = units % sms;
+        const int64_t n_pair = (tail > 0 && 2 * tail <= sms) ? units - tail : units;
+        dense_pair_kernel<<<(unsigned)(2 * units - n_pair), kPairThreads, pair_smem(), s>>>(mk, mv, a, slots,
+                                                                                             (int)n_pair);
     }
     return cudaGetLastError();
 }
