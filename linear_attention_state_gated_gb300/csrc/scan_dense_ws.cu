@@ -1390,31 +1390,41 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         // transition half, warp 2 the state half
         if (lane == 0 && (only < 0 || only == warp - 1)) {
             const int x = warp - 1;
-            const uint32_t dacc = tmem + kPD(x);
-            const uint32_t lo_t = smem_addr(smem + SM::X0lo + x * 32768);
+            const uint32_t dacc = tmem + kPD(x), xh = tmem + kPXh(x);
+            const uint32_t acc0 = x == 1 ? 1u : 0u;   // the state half adds to U^T
+            // shared-memory descriptors, built once per stage: an operand offset of o bytes
+            // adds o >> 4 to the start-address field (no carry: addresses < 256 KB)
+            uint64_t d_wh[kNS], d_wl[kNS], d_k[kNS], d_v[kNS], d_a[kNS];
+#pragma unroll
+            for (int s = 0; s < kNS; ++s) {
+                const uint32_t tb = smem_addr(smem + s * SM::Stage + SM::Tiles);
+                d_wh[s] = smem_desc_sw128(tb + (uint32_t)R::Wt * 4u, 16384, 1024);
+                d_wl[s] = smem_desc_sw128(tb + (uint32_t)R::Wt * 4u + 16384u, 16384, 1024);
+                d_k[s] = smem_desc_sw128(smem_addr(smem + s * SM::Stage + SM::K), kBox, 1024);
+                d_v[s] = smem_desc_sw128(smem_addr(smem + s * SM::Stage + SM::V), kBox, 1024);
+                d_a[s] = smem_desc_sw128(tb + (uint32_t)R::Ab * 4u, 0, 1024);
+            }
+            const uint64_t d_lo = smem_desc_sw128(smem_addr(smem + SM::X0lo + x * 32768), 0, 1024);
             for (int j = 0; j < nc; ++j) {
                 const int s = j % kNS;
                 const uint32_t par = (uint32_t)j & 1u;
-                const uint8_t *stg = smem + s * SM::Stage;
+                const uint64_t wh = s ? d_wh[1] : d_wh[0], wl = s ? d_wl[1] : d_wl[0];
                 // the accumulator is free (the previous update has read Delta~), the chunk is in
                 if (j > 0 && !wait_or_abort(&ctl->x_done[x], par ^ 1u, abortp)) break;
                 if (!wait_or_abort(&ctl->full[s], (uint32_t)(j / kNS) & 1u, abortp)) break;
-                const uint32_t tb = smem_addr(stg + SM::Tiles);
                 // ---- U^T = V^T (A diag(beta))^T into the accumulator (state half), lo first
                 if (x == 1) {
                     tc_fence_after();
-                    const uint32_t vb = smem_addr(stg + SM::V), ab = tb + (uint32_t)R::Ab * 4u;
+                    const uint64_t vd = s ? d_v[1] : d_v[0], ad = s ? d_a[1] : d_a[0];
 #pragma unroll
                     for (int hl = 1; hl >= 0; --hl)
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks)
-                            mma_f16(dacc, smem_desc_sw128(vb + (uint32_t)ks * 2048u, kBox, 1024),
-                                    smem_desc_sw128(ab + (uint32_t)hl * 8192u + (uint32_t)ks * 32u, 0, 1024), id_wu,
+                            mma_f16(dacc, vd + (uint64_t)(ks * 128), ad + (uint64_t)(hl * 512 + ks * 2), id_wu,
                                     (hl == 0 || ks > 0) ? 1u : 0u);
                 }
                 // ---- Delta^T = U^T - X0^T W^T (three-term split), per k half: hi x lo and
                 // lo x hi first, then hi x hi (the accumulator rounds each instruction's sum)
-                const uint32_t wt = tb + (uint32_t)R::Wt * 4u;
                 bool ok = true;
                 for (int p = 0; p < 2 && ok; ++p) {
                     ok = wait_or_abort(&ctl->xop_ready[x][p], par, abortp);
@@ -1423,24 +1433,21 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 #pragma unroll
                     for (int kq = 0; kq < 4; ++kq) {
                         const int ks = p * 4 + kq;
-                        const uint64_t bh = smem_desc_sw128(wt + (uint32_t)ks * 2048u, 16384, 1024);
-                        const uint64_t bl = smem_desc_sw128(wt + 16384u + (uint32_t)ks * 2048u, 16384, 1024);
-                        mma_f16_ta(dacc, tmem + kPXh(x) + (uint32_t)ks * 8u, bl, id_d, (x == 1 || ks > 0) ? 1u : 0u);
-                        mma_f16(dacc, smem_desc_sw128(lo_t + (uint32_t)p * 16384u + (uint32_t)kq * 32u, 0, 1024), bh,
-                                id_d, 1u);
+                        mma_f16_ta(dacc, xh + (uint32_t)ks * 8u, wl + (uint64_t)(ks * 128), id_d,
+                                   (p > 0 || kq > 0) ? 1u : acc0);
+                        mma_f16(dacc, d_lo + (uint64_t)(p * 1024 + kq * 2), wh + (uint64_t)(ks * 128), id_d, 1u);
                     }
 #pragma unroll
                     for (int kq = 0; kq < 4; ++kq) {
                         const int ks = p * 4 + kq;
-                        mma_f16_ta(dacc, tmem + kPXh(x) + (uint32_t)ks * 8u,
-                                   smem_desc_sw128(wt + (uint32_t)ks * 2048u, 16384, 1024), id_d, 1u);
+                        mma_f16_ta(dacc, xh + (uint32_t)ks * 8u, wh + (uint64_t)(ks * 128), id_d, 1u);
                     }
                 }
                 if (!ok) break;
                 mma_commit(&ctl->d_done[x]);
                 // ---- X^T += Delta~^T K (K as the MN-major B operand: row t, channels contiguous),
                 // each 16-token block as soon as its Delta~ is converted (lo, then hi)
-                const uint32_t kb = smem_addr(stg + SM::K);
+                const uint64_t kd = s ? d_k[1] : d_k[0];
                 for (int ks = 0; ks < 4 && ok; ++ks) {
                     ok = wait_or_abort(&ctl->dt_ready[x][ks], par, abortp);
                     if (!ok) break;
@@ -1448,7 +1455,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 #pragma unroll
                     for (int hl = 1; hl >= 0; --hl)
                         mma_f16_ta(tmem + kPX(x), dacc + (uint32_t)ks * 16u + (uint32_t)hl * 8u,
-                                   smem_desc_sw128(kb + (uint32_t)ks * 2048u, kBox, 1024), id_x, 1u);
+                                   kd + (uint64_t)(ks * 128), id_x, 1u);
                 }
                 if (!ok) break;
                 mma_commit(&ctl->x_done[x]);
@@ -1497,15 +1504,16 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             const int s = j % kNS;
             const uint32_t par = (uint32_t)j & 1u;
             const float *gates = ctl->gates[s];
-            // ---- X0 of this half: the chunk is in and the half's previous update is done
+            // ---- the chunk's scales as soon as its gates are in (register work, kept off
+            // the wait for the previous update); then X0 of this half once that update is done
             bool ok = wait_or_abort(&ctl->full[s], (uint32_t)(j / kNS) & 1u, abortp);
+            const HalfScale z = pair_scale(x, j, gates, ls, lam_d, gt == 0);
             if (j > 0) ok = ok && wait_or_abort(&ctl->x_done[x], par ^ 1u, abortp);
             if (!bar_and(gbar, kState / 2, ok)) {
                 alive = false;
                 break;
             }
             tc_fence_after();
-            const HalfScale z = pair_scale(x, j, gates, ls, lam_d, gt == 0);
             float g = z.g;
             if (x == 0 && z.renorm) {   // the transition's power-of-two renormalisation
                 float mx = 0.f;
