@@ -275,8 +275,14 @@ __global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_cons
                 }
             }
         } else if (O) {
-            // ---- Gq[t][s] = [s <= t] exp(Lambda_t - Lambda_s) (q_t.k_s) -> bf16 hi / lo tiles
+            // ---- Gq -> bf16 hi / lo tiles: the state pass multiplies it with Delta~_s =
+            // fD (b_C / b_s) Delta_s, so Gq[t][s] = [s <= t] (b_t / b_C) (q_t.k_s) (the
+            // factor of s cancels); a chunk that decays below e^-40 keeps Delta_s itself
+            // there (Delta~ may underflow) and takes Gq[t][s] = [s <= t] (b_t / b_s) (q_t.k_s)
             uint8_t *gq = reinterpret_cast<uint8_t *>(rec + R::Gq);
+            const float lc = ctl->gl[kC - 1];    // log b_C
+            const bool steep = lc < -40.f;
+            const float rt = __expf(lt - lc);   // b_t / b_C
             for (int cb = 0; cb < 2; ++cb) {
                 uint32_t r[32];
                 tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(cb * 32), r);
@@ -294,8 +300,8 @@ __global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_cons
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
                             const int sc = c * 8 + 2 * p + e;
-                            x[e] = sc <= t ? __expf(lt - gs[cc * 8 + 2 * p + e]) * __uint_as_float(r[cc * 8 + 2 * p + e])
-                                           : 0.f;
+                            const float f = steep ? __expf(lt - gs[cc * 8 + 2 * p + e]) : rt;
+                            x[e] = sc <= t ? f * __uint_as_float(r[cc * 8 + 2 * p + e]) : 0.f;
                         }
                         split_pair(x[0], x[1], hv[p], lv[p]);
                     }
@@ -530,7 +536,7 @@ __device__ __forceinline__ float state_max(float mx, StateCtl *ctl, int sw, int 
 // o_t = b_t O1 + O2 for this thread's 16 tokens (column group cg) of one chunk, as
 // bf16 pairs (tokens 2q, 2q + 1 in opk[q]); then the warp arrives on `freed` (if
 // given): O1 and O2 have been read
-__device__ __forceinline__ void load_o(uint32_t to1, uint32_t to2, const float *b, int cg, int lane,
+__device__ __forceinline__ void load_o(uint32_t to1, uint32_t to2, const float *b, float o2s, int cg, int lane,
                                        uint32_t (&opk)[8], uint64_t *freed) {
     uint32_t r1[16], r2[16];
     tmem_ld16(to1, r1);
@@ -544,9 +550,9 @@ __device__ __forceinline__ void load_o(uint32_t to1, uint32_t to2, const float *
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
         const int t = cg * 16 + 2 * q;
-        const __nv_bfloat162 v = __floats2bfloat162_rn(fmaf(b[t], __uint_as_float(r1[2 * q]), __uint_as_float(r2[2 * q])),
-                                                       fmaf(b[t + 1], __uint_as_float(r1[2 * q + 1]),
-                                                            __uint_as_float(r2[2 * q + 1])));
+        const __nv_bfloat162 v =
+            __floats2bfloat162_rn(fmaf(b[t], __uint_as_float(r1[2 * q]), o2s * __uint_as_float(r2[2 * q])),
+                                  fmaf(b[t + 1], __uint_as_float(r1[2 * q + 1]), o2s * __uint_as_float(r2[2 * q + 1])));
         opk[q] = *reinterpret_cast<const uint32_t *>(&v);
     }
 }
@@ -781,6 +787,10 @@ __global__ void __maxnreg__(80)
         int lam_exp = 0;
         double lam_d = 0.0;
         float ls = 0.f;
+        // o_t: the previous chunk's O2 factor (1 / fD, or 1 where O2 took Delta itself) and
+        // whether its Delta sits in the X0 operand columns (a chunk below e^-40)
+        float o2s_prev = 1.f;
+        bool steep_prev = false;
 
         {   // initial X^T: identity (transition) or zero (state)
             uint32_t r[16];
@@ -830,17 +840,13 @@ __global__ void __maxnreg__(80)
                 }
             }
             if (j > 0) ok = ok && wait_or_abort(&ctl->x_done, (uint32_t)(j - 1) & 1u, abortp);
-            if (with_o && j > 0) ok = ok && wait_or_abort(&ctl->o2_done, (uint32_t)(j - 1) & 1u, abortp);
+            // the previous chunk's O2 products read Delta from the X0 operand columns
+            if (with_o && j > 0 && steep_prev) ok = ok && wait_or_abort(&ctl->o2_done, (uint32_t)(j - 1) & 1u, abortp);
             if (!bar_and(2, kState, ok)) {
                 *abortp = 1;
                 break;
             }
             tc_fence_after();
-            // ---- o_t of the previous chunk into registers (its O1, O2 are complete:
-            // o1_done was awaited in that chunk, o2_done at this one's start); the O1
-            // products of this chunk wait for o_free
-            uint32_t opk[8];
-            if (with_o && j > 0) load_o(to1, to2, ctl->bo, cg, lane, opk, &ctl->o_free);
             if (half == 0 && renorm) {   // the transition's power-of-two renormalisation
                 float mx = 0.f;
 #pragma unroll
@@ -881,12 +887,20 @@ __global__ void __maxnreg__(80)
                     if (lane == 0) mbar_arrive(&ctl->xop_ready[p]);
                 }
             }
-            // ---- and to memory while the Delta products run
-            if (with_o && j > 0) store_o(a, h, cg, quarter, lane, row0 + (int64_t)(j - 1) * kC, kC, opk, ostg);
+            // ---- o_t of the previous chunk (its O1 and O2 complete), to memory while the
+            // Delta products run; the O1 products of this chunk wait for o_free
+            bool ok_o = true;
+            if (with_o && j > 0) {
+                ok_o = wait_or_abort(&ctl->o2_done, (uint32_t)(j - 1) & 1u, abortp);
+                tc_fence_after();
+                uint32_t opk[8];
+                load_o(to1, to2, ctl->bo, o2s_prev, cg, lane, opk, &ctl->o_free);
+                store_o(a, h, cg, quarter, lane, row0 + (int64_t)(j - 1) * kC, kC, opk, ostg);
+            }
             // ---- Delta~^T = fD Delta^T diag(b_C / b) -> bf16 hi / lo in place
             // (with o_t also Delta^T itself, hi / lo, into the X0 operand columns, once
             // the O1 products have read X0 there)
-            if (!bar_and(2, kState, wait_or_abort(&ctl->d_done, (uint32_t)j & 1u, abortp) &&
+            if (!bar_and(2, kState, ok_o && wait_or_abort(&ctl->d_done, (uint32_t)j & 1u, abortp) &&
                                         (!with_o || wait_or_abort(&ctl->o1_done, (uint32_t)j & 1u, abortp)))) {
                 *abortp = 1;
                 break;
@@ -903,7 +917,7 @@ __global__ void __maxnreg__(80)
                     for (int q = 0; q < 16; ++q) r[q] = __float_as_uint(__uint_as_float(r[q]) + __uint_as_float(r2[q]));
                 }
                 tmem_wait_ld();
-                if (with_o) {
+                if (with_o && slow) {   // O2 takes Delta itself (Delta~ may underflow)
 #pragma unroll
                     for (int q = 0; q < 8; ++q)
                         split_pair(__uint_as_float(r[2 * q]), __uint_as_float(r[2 * q + 1]), hi[q], lo[q]);
@@ -924,6 +938,8 @@ __global__ void __maxnreg__(80)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->dt_ready);
+            o2s_prev = slow ? 1.f : 1.f / fD;
+            steep_prev = slow;
         }
 
         // ------------------------------------------------------------ epilogue
@@ -934,7 +950,7 @@ __global__ void __maxnreg__(80)
             tc_fence_after();
             if (with_o && nc > 0) {
                 uint32_t opk[8];
-                load_o(to1, to2, ctl->bo, cg, lane, opk, nullptr);
+                load_o(to1, to2, ctl->bo, o2s_prev, cg, lane, opk, nullptr);
                 store_o(a, h, cg, quarter, lane, row0 + (int64_t)(nc - 1) * kC,
                         (int)(t1 - t0 - (int64_t)(nc - 1) * kC), opk, ostg);
             }
@@ -1009,6 +1025,10 @@ __global__ void __maxnreg__(80)
                 const uint8_t *stg = smem + s * SM::Stage;
                 if (!wait_or_abort(&ctl->full[s], (uint32_t)(j / kNS) & 1u, abortp)) break;
                 const uint32_t qb = smem_addr(stg + SM::Q);
+                // O2 reads Delta~ from its accumulator, or Delta from the X0 operand columns
+                // on a chunk that decays below e^-40
+                const bool steep = reinterpret_cast<const float *>(stg + SM::Rec)[R::LC] < -40.f;
+                const uint32_t d2 = tmem + (steep ? kTxop : kTacc);
                 bool ok = true;
                 for (int p = 0; p < 2 && ok; ++p) {
                     ok = wait_or_abort(&ctl->xop_ready[p], par, abortp);
@@ -1037,7 +1057,7 @@ __global__ void __maxnreg__(80)
                 for (int ks = 0; ks < 4; ++ks) {
                     const uint64_t gh = smem_desc_sw128(gq + (uint32_t)ks * 32u, 0, 1024);
                     const uint64_t gl = smem_desc_sw128(gq + 8192u + (uint32_t)ks * 32u, 0, 1024);
-                    const uint32_t ah = tmem + kTxop + (uint32_t)ks * 16u;
+                    const uint32_t ah = d2 + (uint32_t)ks * 16u;
                     mma_f16_ta(tmem + kTo2, ah, gh, id_o, ks > 0);
                     mma_f16_ta(tmem + kTo2, ah, gl, id_o, 1u);
                     mma_f16_ta(tmem + kTo2, ah + 8u, gh, id_o, 1u);
@@ -1057,8 +1077,10 @@ __global__ void __maxnreg__(80)
             const uint32_t use = (uint32_t)(j / SM::NB);
             const uint32_t par = (uint32_t)j & 1u;
             const uint8_t *stg = smem + s * SM::Stage;
-            // the accumulator is free (the previous update has read Delta~), the chunk is in
+            // the accumulator is free (the previous update and, with o_t, the previous O2
+            // products have read Delta~), the chunk is in
             if (j > 0 && !wait_or_abort(&ctl->x_done, par ^ 1u, abortp)) break;
+            if (with_o && j > 0 && !wait_or_abort(&ctl->o2_done, par ^ 1u, abortp)) break;
             if (!wait_or_abort(&ctl->full[s], (uint32_t)(j / kNS) & 1u, abortp)) break;
             // ---- U^T = V^T (A diag(beta))^T into the accumulator (state half)
             if (half) {

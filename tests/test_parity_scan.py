@@ -266,8 +266,9 @@ def test_dense_long_segment_and_special_gates(form):
 @DENSE_FORMS
 def test_dense_o_long_and_special_gates(form):
     """o_t of the gated delta rule over several chunks (both forms): a long
-    segment with a ragged tail, alpha = beta = 1, and strong decay (chunks below
-    e^-40 alternating with mild ones)."""
+    segment with a ragged tail, alpha = beta = 1, strong decay (chunks below
+    e^-40 alternating with mild ones), and every chunk decaying by e^-38 (just
+    above that bound: the largest b_t / b_C the output products take)."""
     w = wl.dense_stack(lengths=[2048 + 17, 700], n_layers=1, H=2, d=128, seed=16, with_q=True)
     got = host(gpu_scan(w, want_o=True, workspace=form))
     check(DENSE, got, oracle_scan(w, want_o=True), TOL_SCAN_BF16, o_tol=TOL_O_BF16, seg_offsets=w["seg_offsets"])
@@ -282,6 +283,10 @@ def test_dense_o_long_and_special_gates(form):
     w2["alpha"][:, (t // 64) % 3 == 1] = 0.3
     got = host(gpu_scan(w2, want_o=True, workspace=form))
     check(DENSE, got, oracle_scan(w2, want_o=True), TOL_SCAN_BF16, o_tol=TOL_O_BF16, seg_offsets=w["seg_offsets"])
+    w3 = dict(w)
+    w3["alpha"] = np.full_like(w["alpha"], np.float32(0.55))   # 64 ln 0.55 = -38.3
+    got = host(gpu_scan(w3, want_o=True, workspace=form))
+    check(DENSE, got, oracle_scan(w3, want_o=True), TOL_SCAN_BF16, o_tol=TOL_O_BF16, seg_offsets=w["seg_offsets"])
 
 
 @pytest.mark.parametrize("fam", [SCALAR, DIAG, DENSE], ids=["scalar", "diag", "dense"])
