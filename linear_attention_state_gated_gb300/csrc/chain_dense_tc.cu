@@ -199,6 +199,11 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: <= 96 registers pe
             const uint32_t nh = warp == 1 ? 0u : 1u;
             const uint32_t b0 = smem_addr(smem) + nh * 16384u;   // the B atom of this column half
             const uint32_t dcol = tmem + kTd + nh * 64u;
+            // B descriptors of the three parts, built once: a k step of 16 rows (2048 bytes)
+            // adds 2048 >> 4 to the start-address field
+            const uint64_t dh0 = smem_desc_sw128(b0, 16384, 1024);
+            const uint64_t dm0 = smem_desc_sw128(b0 + kBpart, 16384, 1024);
+            const uint64_t dl0 = smem_desc_sw128(b0 + 2 * kBpart, 16384, 1024);
             int64_t g = 0;
             for (int64_t u = blockIdx.x; u < units && !*abortp; u += gridDim.x) {
                 const int n = unit_steps(a, u, false);
@@ -216,15 +221,15 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: <= 96 registers pe
 #pragma unroll 4
                         for (int ks = 0; ks < 8; ++ks) {
                             const uint32_t off = (uint32_t)ks * 2048u;
-                            const uint64_t bh = smem_desc_sw128(b0 + off, 16384, 1024);
-                            const uint64_t bl = smem_desc_sw128(b0 + kBpart + off, 16384, 1024);
+                            const uint64_t bh = dh0 + (uint64_t)(ks * 128);
+                            const uint64_t bl = dm0 + (uint64_t)(ks * 128);
                             const uint32_t ah = abuf + (uint32_t)ks * 8u, al = ah + 64u;
                             mma_f16_ta(dcol, ah, bl, idesc, ks > 0);
                             mma_f16_ta(dcol, al, bh, idesc, 1u);
                         }
 #pragma unroll 4
                         for (int ks = 0; ks < 8; ++ks) {
-                            const uint64_t bh = smem_desc_sw128(b0 + (uint32_t)ks * 2048u, 16384, 1024);
+                            const uint64_t bh = dh0 + (uint64_t)(ks * 128);
                             mma_f16_ta(dcol, abuf + (uint32_t)ks * 8u, bh, idesc, 1u);
                         }
                     } else if (OP) {
@@ -237,9 +242,9 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: <= 96 registers pe
 #pragma unroll 2
                         for (int ks = 0; ks < 8; ++ks) {   // K = 128 in steps of 16 (two 8-row groups of B)
                             const uint32_t off = (uint32_t)ks * 2048u;
-                            const uint64_t bh = smem_desc_sw128(b0 + off, 16384, 1024);
-                            const uint64_t bm = smem_desc_sw128(b0 + kBpart + off, 16384, 1024);
-                            const uint64_t bl = smem_desc_sw128(b0 + 2 * kBpart + off, 16384, 1024);
+                            const uint64_t bh = dh0 + (uint64_t)(ks * 128);
+                            const uint64_t bm = dm0 + (uint64_t)(ks * 128);
+                            const uint64_t bl = dl0 + (uint64_t)(ks * 128);
                             const uint32_t ah = abuf + (uint32_t)ks * 8u, am = ah + 64u, al = ah + 128u;
                             mma_f16_ta(dcol, ah, bl, idesc, ks > 0);
                             mma_f16_ta(dcol, am, bm, idesc, 1u);
@@ -248,15 +253,15 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: <= 96 registers pe
 #pragma unroll 2
                         for (int ks = 0; ks < 8; ++ks) {
                             const uint32_t off = (uint32_t)ks * 2048u;
-                            const uint64_t bh = smem_desc_sw128(b0 + off, 16384, 1024);
-                            const uint64_t bm = smem_desc_sw128(b0 + kBpart + off, 16384, 1024);
+                            const uint64_t bh = dh0 + (uint64_t)(ks * 128);
+                            const uint64_t bm = dm0 + (uint64_t)(ks * 128);
                             const uint32_t ah = abuf + (uint32_t)ks * 8u, am = ah + 64u;
                             mma_f16_ta(dcol, ah, bm, idesc, 1u);
                             mma_f16_ta(dcol, am, bh, idesc, 1u);
                         }
 #pragma unroll 4
                         for (int ks = 0; ks < 8; ++ks) {
-                            const uint64_t bh = smem_desc_sw128(b0 + (uint32_t)ks * 2048u, 16384, 1024);
+                            const uint64_t bh = dh0 + (uint64_t)(ks * 128);
                             mma_f16_ta(dcol, abuf + (uint32_t)ks * 8u, bh, idesc, 1u);
                         }
                     } else {
@@ -264,9 +269,9 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: <= 96 registers pe
 #pragma unroll 2
                         for (int ks = 0; ks < 8; ++ks) {
                             const uint32_t off = (uint32_t)ks * 2048u;
-                            const uint64_t bh = smem_desc_sw128(b0 + off, 16384, 1024);
-                            const uint64_t bm = smem_desc_sw128(b0 + kBpart + off, 16384, 1024);
-                            const uint64_t bl = smem_desc_sw128(b0 + 2 * kBpart + off, 16384, 1024);
+                            const uint64_t bh = dh0 + (uint64_t)(ks * 128);
+                            const uint64_t bm = dm0 + (uint64_t)(ks * 128);
+                            const uint64_t bl = dl0 + (uint64_t)(ks * 128);
                             const uint32_t ah = abuf + (uint32_t)ks * 8u, am = ah + 64u, al = ah + 128u;
                             mma_f16_ta(dcol, ah, bh, idesc, ks > 0);
                             mma_f16_ta(dcol, ah, bm, idesc, 1u);
