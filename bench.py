@@ -854,7 +854,7 @@ def run_long_mix(args):
     import torch
     import linear_attention_state_gated_gb300 as hy
     from linear_attention_state_gated_gb300 import workloads as wl
-    n_seg, L, Lyr, H, d = 64, 2048, 30, 32, 128
+    n_seg, L, Lyr, H, d = 64, 2048, args.mix_layers, 32, 128
     unc, cached, rows = wl.long_mix_layout(n_seg=n_seg, n_layers=Lyr)
     nu = len(unc)
     dev = torch.device("cuda")
@@ -916,10 +916,10 @@ def run_long_mix(args):
     hbm, _, _, src = peaks()
     chain_bytes = n_seg * Lyr * H * (2 * 4 * d * d + 4) + Lyr * H * 4 * d * d
     res = {"workload": "131072-token prompt, 64 x 2048-token segments (48 cached, 16 uncached), gated delta "
-                       "rule, 30 layers x 32 heads x 128",
+                       f"rule, {Lyr} layers x 32 heads x 128",
            "value": n_seg * L / t, "unit": "prompt tokens/s", "ms": t * 1e3,
            "scan_uncached_with_o_ms": t_scan * 1e3, "chain_ms": t_chain * 1e3,
-           "uncached_scan": "one call, 16 x 30 (layer, segment) units of 2048 tokens",
+           "uncached_scan": f"one call, 16 x {Lyr} (layer, segment) units of 2048 tokens",
            "composes_per_s": n_seg * Lyr / t_chain,
            "scan_state_only_one_segment_ms": t_state_only * 1e3,
            "chain_roofline": {"bound": "hbm", "achieved": chain_bytes / t_chain / 1e9, "peak": hbm,
@@ -1024,6 +1024,8 @@ def main():
                     help="compose row: items (64 requests x 30 layers by default)")
     ap.add_argument("--chain-layers", type=int, default=30,
                     help="RAG chain row: layers of the pool (30 by default)")
+    ap.add_argument("--mix-layers", type=int, default=30,
+                    help="layers of the long-mix row (fewer for a profiling capture; 30 in the benchmark)")
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
