@@ -161,8 +161,25 @@ __global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_cons
     const uint32_t tmem = ctl->tmem;
     bool ok = true;
 
-    // ---- gates (warp 0): Lambda, b_C / b, beta b, beta, log b_C, b_C (, b)
-    if (warp == 0) {
+    // ---- Gram [K; Q] K^T as soon as the keys are in (warp 0): lanes 0..63 K K^T,
+    // lanes 64..127 Q K^T (K K^T again without o_t); the gates meanwhile (warp 1)
+    if (warp == 0 && lane == 0) {
+        ok = mbar_wait(&ctl->full, 0);
+        if (ok) {
+            tc_fence_after();
+            constexpr uint32_t id_gram = idesc_bf16_f32(128, 64, false, false);
+            const uint32_t kb = smem_addr(smem + kPK);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t off = (uint32_t)(ks >> 2) * (2u * kBox) + (uint32_t)(ks & 3) * 32u;
+                const uint64_t d = smem_desc_sw128(kb + off, 0, 1024);
+                mma_f16(tmem, d, d, id_gram, ks > 0);
+            }
+        }
+        mma_commit(&ctl->mma);
+    }
+    // ---- gates (warp 1): Lambda, b_C / b, beta b, beta, log b_C, b_C (, b)
+    if (warp == 1) {
         float lg[2], pb[2], inc[2];
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
@@ -202,22 +219,6 @@ __global__ void __launch_bounds__(kPThreads) dense_prep_kernel(const __grid_cons
             rec[R::LC] = total;
             rec[R::BC] = expf(total);
             if (!O) rec[R::BC + 1] = rec[R::BC + 2] = 0.f;
-        }
-        // Gram [K; Q] K^T: lanes 0..63 K K^T, lanes 64..127 Q K^T (K K^T again without o_t)
-        if (lane == 0) {
-            ok = mbar_wait(&ctl->full, 0);
-            if (ok) {
-                tc_fence_after();
-                constexpr uint32_t id_gram = idesc_bf16_f32(128, 64, false, false);
-                const uint32_t kb = smem_addr(smem + kPK);
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t off = (uint32_t)(ks >> 2) * (2u * kBox) + (uint32_t)(ks & 3) * 32u;
-                    const uint64_t d = smem_desc_sw128(kb + off, 0, 1024);
-                    mma_f16(tmem, d, d, id_gram, ks > 0);
-                }
-            }
-            mma_commit(&ctl->mma);
         }
     }
     ok = __syncthreads_and(ok && mbar_wait(&ctl->mma, 0));
@@ -718,11 +719,12 @@ __global__ void __maxnreg__(80)
                 tc_fence_after();
                 const uint32_t kb = smem_addr(st + SM::K);
                 const uint32_t ab2 = smem_addr(st + SM::Rec);
+                const uint64_t dk0 = smem_desc_sw128(kb, kBox, 1024), da0 = smem_desc_sw128(ab2, 0, 1024);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
-                    const uint64_t ad = smem_desc_sw128(kb + (uint32_t)ks * 2048u, kBox, 1024);
-                    mma_f16(tmem + kTw, ad, smem_desc_sw128(ab2 + (uint32_t)ks * 32u, 0, 1024), id_wu, ks > 0);
-                    mma_f16(tmem + kTw, ad, smem_desc_sw128(ab2 + 8192u + (uint32_t)ks * 32u, 0, 1024), id_wu, 1u);
+                    const uint64_t ad = dk0 + (uint64_t)(ks * 128);
+                    mma_f16(tmem + kTw, ad, da0 + (uint64_t)(ks * 2), id_wu, ks > 0);
+                    mma_f16(tmem + kTw, ad, da0 + (uint64_t)(512 + ks * 2), id_wu, 1u);
                 }
                 mma_commit(&ctl->w_done);
             }
@@ -996,11 +998,12 @@ __global__ void __maxnreg__(80)
                 if (!wait_or_abort(&ctl->xop_ready[1], par, abortp)) break;
                 tc_fence_after();
                 const uint32_t wtile = smem_addr(smem + SM::Wt + b * 32768);
+            const uint64_t dwh = smem_desc_sw128(wtile, 16384, 1024);
 #pragma unroll
                 for (int kq = 0; kq < 4; ++kq) {
                     const int ks = 4 + kq;
-                    const uint64_t bh = smem_desc_sw128(wtile + (uint32_t)ks * 2048u, 16384, 1024);
-                    const uint64_t bl = smem_desc_sw128(wtile + 16384u + (uint32_t)ks * 2048u, 16384, 1024);
+                    const uint64_t bh = dwh + (uint64_t)(ks * 128);
+                    const uint64_t bl = dwh + (uint64_t)(1024 + ks * 128);
                     const uint32_t ah = tmem + kTxop + (uint32_t)ks * 8u, al = ah + 64u;
                     mma_f16_ta(tmem + kTacc2, ah, bh, id_d, kq > 0 ? 1u : 0u);
                     mma_f16_ta(tmem + kTacc2, ah, bl, id_d, 1u);
@@ -1025,6 +1028,7 @@ __global__ void __maxnreg__(80)
                 const uint8_t *stg = smem + s * SM::Stage;
                 if (!wait_or_abort(&ctl->full[s], (uint32_t)(j / kNS) & 1u, abortp)) break;
                 const uint32_t qb = smem_addr(stg + SM::Q);
+                const uint64_t dq0 = smem_desc_sw128(qb, 0, 1024);
                 // O2 reads Delta~ from its accumulator, or Delta from the X0 operand columns
                 // on a chunk that decays below e^-40
                 const bool steep = reinterpret_cast<const float *>(stg + SM::Rec)[R::LC] < -40.f;
@@ -1039,8 +1043,7 @@ __global__ void __maxnreg__(80)
 #pragma unroll
                     for (int kq = 0; kq < 4; ++kq) {
                         const int ks = p * 4 + kq;
-                        const uint64_t bq =
-                            smem_desc_sw128(qb + (uint32_t)(ks >> 2) * kBox + (uint32_t)(ks & 3) * 32u, 0, 1024);
+                        const uint64_t bq = dq0 + (uint64_t)((ks >> 2) * (kBox >> 4) + (ks & 3) * 2);
                         const uint32_t ah = tmem + kTxop + (uint32_t)ks * 8u;
                         mma_f16_ta(tmem + kTo1, ah, bq, id_o, ks > 0);
                         mma_f16_ta(tmem + kTo1, ah + 64u, bq, id_o, 1u);
@@ -1053,10 +1056,11 @@ __global__ void __maxnreg__(80)
                 if (!wait_or_abort(&ctl->gfull, par, abortp)) break;
                 tc_fence_after();
                 const uint32_t gq = smem_addr(smem + SM::Gqb);
+                const uint64_t dg0 = smem_desc_sw128(gq, 0, 1024);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
-                    const uint64_t gh = smem_desc_sw128(gq + (uint32_t)ks * 32u, 0, 1024);
-                    const uint64_t gl = smem_desc_sw128(gq + 8192u + (uint32_t)ks * 32u, 0, 1024);
+                    const uint64_t gh = dg0 + (uint64_t)(ks * 2);
+                    const uint64_t gl = dg0 + (uint64_t)(512 + ks * 2);
                     const uint32_t ah = d2 + (uint32_t)ks * 16u;
                     mma_f16_ta(tmem + kTo2, ah, gh, id_o, ks > 0);
                     mma_f16_ta(tmem + kTo2, ah, gl, id_o, 1u);
@@ -1086,16 +1090,18 @@ __global__ void __maxnreg__(80)
             if (half) {
                 tc_fence_after();
                 const uint32_t vb = smem_addr(stg + SM::V), ab = smem_addr(stg + SM::Rec + R::Ab * 4);
+                const uint64_t dv0 = smem_desc_sw128(vb, kBox, 1024), dab0 = smem_desc_sw128(ab, 0, 1024);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
-                    const uint64_t ad = smem_desc_sw128(vb + (uint32_t)ks * 2048u, kBox, 1024);
-                    mma_f16(tmem + kTacc, ad, smem_desc_sw128(ab + (uint32_t)ks * 32u, 0, 1024), id_wu, ks > 0);
-                    mma_f16(tmem + kTacc, ad, smem_desc_sw128(ab + 8192u + (uint32_t)ks * 32u, 0, 1024), id_wu, 1u);
+                    const uint64_t ad = dv0 + (uint64_t)(ks * 128);
+                    mma_f16(tmem + kTacc, ad, dab0 + (uint64_t)(ks * 2), id_wu, ks > 0);
+                    mma_f16(tmem + kTacc, ad, dab0 + (uint64_t)(512 + ks * 2), id_wu, 1u);
                 }
             }
             // ---- Delta^T = U^T - X0^T W^T (three-term split), per k half
             if (!wait_or_abort(&ctl->wop_ready[b], use & 1u, abortp)) break;
             const uint32_t wtile = smem_addr(smem + SM::Wt + b * 32768);
+            const uint64_t dwh = smem_desc_sw128(wtile, 16384, 1024);
             bool ok = true;
             for (int p = 0; p < (split_d ? 1 : 2) && ok; ++p) {   // split: the second half is warp 22's
                 ok = wait_or_abort(&ctl->xop_ready[p], par, abortp);
@@ -1104,8 +1110,8 @@ __global__ void __maxnreg__(80)
 #pragma unroll
                 for (int kq = 0; kq < 4; ++kq) {
                     const int ks = p * 4 + kq;
-                    const uint64_t bh = smem_desc_sw128(wtile + (uint32_t)ks * 2048u, 16384, 1024);
-                    const uint64_t bl = smem_desc_sw128(wtile + 16384u + (uint32_t)ks * 2048u, 16384, 1024);
+                    const uint64_t bh = dwh + (uint64_t)(ks * 128);
+                    const uint64_t bl = dwh + (uint64_t)(1024 + ks * 128);
                     const uint32_t ah = tmem + kTxop + (uint32_t)ks * 8u, al = ah + 64u;
                     mma_f16_ta(tmem + kTacc, ah, bh, id_d, (half || ks > 0) ? 1u : 0u);
                     mma_f16_ta(tmem + kTacc, ah, bl, id_d, 1u);
@@ -1119,9 +1125,10 @@ __global__ void __maxnreg__(80)
             if (!wait_or_abort(&ctl->dt_ready, par, abortp)) break;
             tc_fence_after();
             const uint32_t kb = smem_addr(stg + SM::K);
+            const uint64_t dkb = smem_desc_sw128(kb, kBox, 1024);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t bd = smem_desc_sw128(kb + (uint32_t)ks * 2048u, kBox, 1024);
+                const uint64_t bd = dkb + (uint64_t)(ks * 128);
                 const uint32_t ah = tmem + kTacc + (uint32_t)ks * 16u;
                 mma_f16_ta(tmem + kTx, ah, bd, id_x, 1u);
                 mma_f16_ta(tmem + kTx, ah + 8u, bd, id_x, 1u);

@@ -200,6 +200,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t id_o2 = idesc_bf16_f32(128, 64, true, false);    // V^T (MN-major) x Gq (K-major)
             const uint32_t aq = smem_addr(smem + kAq), bk = smem_addr(smem + kBk), gq = smem_addr(smem + kGq);
             const int order[3][2] = {{1, 0}, {0, 1}, {0, 0}};   // lo products first
+            // descriptors built once; an operand offset of o bytes adds o >> 4
+            const uint64_t daq = smem_desc_sw128(aq, 0, 1024), dbk = smem_desc_sw128(bk, 0, 1024),
+                           dbkx = smem_desc_sw128(bk, kBox, 1024), dgq = smem_desc_sw128(gq, 0, 1024);
             for (int j = 0; j < nc; ++j) {
                 const int s = j % kNS;
                 const uint32_t par = (uint32_t)j & 1u;
@@ -211,8 +214,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int ks = 0; ks < 8; ++ks) {
                             const uint32_t off = (uint32_t)(ks >> 2) * kBox + (uint32_t)(ks & 3) * 32u;
-                            mma_f16(tmem + kTg, smem_desc_sw128(aq + (uint32_t)order[p][0] * 16384u + off, 0, 1024),
-                                    smem_desc_sw128(bk + (uint32_t)order[p][1] * 16384u + off, 0, 1024), id_g,
+                            mma_f16(tmem + kTg, daq + (uint64_t)((order[p][0] * 16384 + (int)off) >> 4),
+                                    dbk + (uint64_t)((order[p][1] * 16384 + (int)off) >> 4), id_g,
                                     (p > 0 || ks > 0) ? 1u : 0u);
                         }
                 }
@@ -223,13 +226,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 tc_fence_after();
                 const uint32_t vb = smem_addr(smem + s * kStage + kOffV);
+                const uint64_t dv = smem_desc_sw128(vb, kBox, 1024);
                 // ---- X^T += V^T Bk (lo, then hi)
 #pragma unroll
                 for (int hl = 1; hl >= 0; --hl)
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_f16(tmem + kTx, smem_desc_sw128(vb + (uint32_t)ks * 2048u, kBox, 1024),
-                                smem_desc_sw128(bk + (uint32_t)hl * 16384u + (uint32_t)ks * 2048u, kBox, 1024), id_x, 1u);
+                        mma_f16(tmem + kTx, dv + (uint64_t)(ks * 128), dbkx + (uint64_t)(hl * 1024 + ks * 128), id_x, 1u);
                 // ---- O1^T = (S0 op)^T Aq^T, both split
 #pragma unroll
                 for (int p = 0; p < 3; ++p)
@@ -237,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int ks = 0; ks < 8; ++ks) {
                         const uint32_t off = (uint32_t)(ks >> 2) * kBox + (uint32_t)(ks & 3) * 32u;
                         mma_f16_ta(tmem + kTo1, tmem + kTxh + (uint32_t)order[p][0] * 64u + (uint32_t)ks * 8u,
-                                   smem_desc_sw128(aq + (uint32_t)order[p][1] * 16384u + off, 0, 1024), id_o1,
+                                   daq + (uint64_t)((order[p][1] * 16384 + (int)off) >> 4), id_o1,
                                    (p > 0 || ks > 0) ? 1u : 0u);
                     }
                 // ---- O2^T = V^T Gq^T (lo, then hi)
@@ -245,8 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int hl = 1; hl >= 0; --hl)
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_f16(tmem + kTo2, smem_desc_sw128(vb + (uint32_t)ks * 2048u, kBox, 1024),
-                                smem_desc_sw128(gq + (uint32_t)hl * 8192u + (uint32_t)ks * 32u, 0, 1024), id_o2,
+                        mma_f16(tmem + kTo2, dv + (uint64_t)(ks * 128), dgq + (uint64_t)(hl * 512 + ks * 2), id_o2,
                                 (hl == 0 || ks > 0) ? 1u : 0u);
                 mma_commit(&ctl->o_done);
                 mma_commit(&ctl->empty[s]);

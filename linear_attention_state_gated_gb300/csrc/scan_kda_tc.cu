@@ -350,16 +350,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             constexpr uint32_t id_g = idesc_bf16_f32(128, 64, false, false);
             const uint32_t ga = smem_addr(smem + kGa), gb = smem_addr(smem + kGb);
+            const uint64_t dga = smem_desc_sw128(ga, 0, 1024), dgb = smem_desc_sw128(gb, 0, 1024);
             mma3(tmem + kTG, id_g, 8,
                  [&](int hl, int ks) {
-                     return smem_desc_sw128(ga + (uint32_t)hl * 32768u + (uint32_t)(ks >> 2) * 16384u +
-                                                (uint32_t)(ks & 3) * 32u,
-                                            0, 1024);
+                     return dga + (uint64_t)(hl * 2048 + (ks >> 2) * 1024 + (ks & 3) * 2);
                  },
                  [&](int hl, int ks) {
-                     return smem_desc_sw128(gb + (uint32_t)hl * 16384u + (uint32_t)(ks >> 2) * kBox +
-                                                (uint32_t)(ks & 3) * 32u,
-                                            0, 1024);
+                     return dgb + (uint64_t)(hl * 1024 + (ks >> 2) * (kBox >> 4) + (ks & 3) * 2);
                  });
             mma_commit(&ctl->mma);
         }
@@ -411,13 +408,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             constexpr uint32_t id_p = idesc_bf16_f32(128, 64, true, true);
             const uint32_t ga = smem_addr(smem + kGa), ab = smem_addr(smem + kAi);
+            const uint64_t dga = smem_desc_sw128(ga, 16384, 1024), dab = smem_desc_sw128(ab, 8192, 1024);
             mma3(tmem + kTP, id_p, 4,
-                 [&](int hl, int ks) {
-                     return smem_desc_sw128(ga + (uint32_t)hl * 32768u + (uint32_t)ks * 2048u, 16384, 1024);
-                 },
-                 [&](int hl, int ks) {
-                     return smem_desc_sw128(ab + (uint32_t)hl * 8192u + (uint32_t)ks * 2048u, 8192, 1024);
-                 });
+                 [&](int hl, int ks) { return dga + (uint64_t)(hl * 2048 + ks * 128); },
+                 [&](int hl, int ks) { return dab + (uint64_t)(hl * 512 + ks * 128); });
             mma_commit(&ctl->mma);
         }
         ok = __syncthreads_and(mbar_wait(&ctl->mma, mma_phase));
@@ -446,16 +440,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t id_t = idesc_bf16_f32(128, 128, false, true);
             constexpr uint32_t id_l = idesc_bf16_f32(128, 64, false, false);
             const uint32_t pb = smem_addr(smem + kX), gb = smem_addr(smem + kGb), lb = smem_addr(smem + kK);
-            auto pd = [&](int hl, int ks) {
-                return smem_desc_sw128(pb + (uint32_t)hl * 16384u + (uint32_t)ks * 32u, 0, 1024);
-            };
-            mma3(tmem + kTG, id_l, 4, pd, [&](int hl, int ks) {
-                return smem_desc_sw128(lb + (uint32_t)hl * 8192u + (uint32_t)ks * 32u, 0, 1024);
-            });
+            const uint64_t dpb = smem_desc_sw128(pb, 0, 1024), dlb = smem_desc_sw128(lb, 0, 1024),
+                           dgb = smem_desc_sw128(gb, kBox, 1024);
+            auto pd = [&](int hl, int ks) { return dpb + (uint64_t)(hl * 1024 + ks * 2); };
+            mma3(tmem + kTG, id_l, 4, pd, [&](int hl, int ks) { return dlb + (uint64_t)(hl * 512 + ks * 2); });
             mma_commit(&ctl->mma);
-            mma3(tmem + kTT, id_t, 4, pd, [&](int hl, int ks) {
-                return smem_desc_sw128(gb + (uint32_t)hl * 16384u + (uint32_t)ks * 2048u, kBox, 1024);
-            });
+            mma3(tmem + kTT, id_t, 4, pd, [&](int hl, int ks) { return dgb + (uint64_t)(hl * 1024 + ks * 128); });
             mma_commit(&ctl->tdone);
         }
         ok = __syncthreads_and(mbar_wait(&ctl->mma, mma_phase));
@@ -499,12 +489,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             constexpr uint32_t id_z = idesc_bf16_f32(128, 128, false, true);
             const uint32_t qb = smem_addr(smem + kQ), vb = smem_addr(smem + kV);
+            const uint64_t dqb = smem_desc_sw128(qb, 0, 1024), dvb = smem_desc_sw128(vb, kBox, 1024);
 #pragma unroll
             for (int hl = 1; hl >= 0; --hl)
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_f16(tmem + kTG, smem_desc_sw128(qb + (uint32_t)hl * 16384u + (uint32_t)ks * 32u, 0, 1024),
-                            smem_desc_sw128(vb + (uint32_t)ks * 2048u, kBox, 1024), id_z,
+                    mma_f16(tmem + kTG, dqb + (uint64_t)(hl * 1024 + ks * 2), dvb + (uint64_t)(ks * 128), id_z,
                             (hl == 0 || ks > 0) ? 1u : 0u);
             mma_commit(&ctl->mma);
         }

@@ -178,11 +178,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint8_t *stg = smem + s * kStage;
                 const uint32_t kb = smem_addr(stg + kOffK), qb = smem_addr(stg + kOffQ);
+                const uint64_t dq = smem_desc_sw128(qb, 0, 1024), dk = smem_desc_sw128(kb, 0, 1024);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t off = (uint32_t)(ks >> 2) * kBox + (uint32_t)(ks & 3) * 32u;
-                    mma_f16(tmem + kTg, smem_desc_sw128(qb + off, 0, 1024), smem_desc_sw128(kb + off, 0, 1024), id_g,
-                            ks > 0 ? 1u : 0u);
+                    const uint64_t o = (uint64_t)((ks >> 2) * (kBox >> 4) + (ks & 3) * 2);
+                    mma_f16(tmem + kTg, dq + o, dk + o, id_g, ks > 0 ? 1u : 0u);
                 }
                 mma_commit(&ctl->gram_done);
                 return true;
@@ -198,12 +198,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 // ---- S^T += V^T K~ (lo, then hi)
                 const uint32_t kt = smem_addr(smem + kKt);
+                const uint64_t dv = smem_desc_sw128(vb, kBox, 1024), dkt = smem_desc_sw128(kt, kBox, 1024),
+                               dq = smem_desc_sw128(qb, 0, 1024);
 #pragma unroll
                 for (int hl = 1; hl >= 0; --hl)
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_f16(tmem + kTx, smem_desc_sw128(vb + (uint32_t)ks * 2048u, kBox, 1024),
-                                smem_desc_sw128(kt + (uint32_t)hl * 16384u + (uint32_t)ks * 2048u, kBox, 1024), id_x,
+                        mma_f16(tmem + kTx, dv + (uint64_t)(ks * 128), dkt + (uint64_t)(hl * 1024 + ks * 128), id_x,
                                 1u);
                 mma_commit(&ctl->x_done);
                 // ---- the next chunk's Gram (its columns were read for this chunk's Gq)
@@ -217,15 +218,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int ks = 0; ks < 8; ++ks) {
                         const uint32_t off = (uint32_t)(ks >> 2) * kBox + (uint32_t)(ks & 3) * 32u;
                         mma_f16_ta(tmem + kTo1, tmem + kTxh + (uint32_t)hl * 64u + (uint32_t)ks * 8u,
-                                   smem_desc_sw128(qb + off, 0, 1024), id_o1, (hl == 0 || ks > 0) ? 1u : 0u);
+                                   dq + (uint64_t)(off >> 4), id_o1, (hl == 0 || ks > 0) ? 1u : 0u);
                     }
-                const uint32_t gq = smem_addr(smem + kGq + (int)par * 16384);
+                const uint64_t dg = smem_desc_sw128(smem_addr(smem + kGq + (int)par * 16384), 0, 1024);
 #pragma unroll
                 for (int hl = 1; hl >= 0; --hl)
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_f16(tmem + kTo2, smem_desc_sw128(vb + (uint32_t)ks * 2048u, kBox, 1024),
-                                smem_desc_sw128(gq + (uint32_t)hl * 8192u + (uint32_t)ks * 32u, 0, 1024), id_o2,
+                        mma_f16(tmem + kTo2, dv + (uint64_t)(ks * 128), dg + (uint64_t)(hl * 512 + ks * 2), id_o2,
                                 (hl == 0 || ks > 0) ? 1u : 0u);
                 mma_commit(&ctl->o_done);
                 mma_commit(&ctl->empty[s]);
