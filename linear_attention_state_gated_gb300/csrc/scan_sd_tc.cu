@@ -310,14 +310,13 @@ __global__ void __launch_bounds__(SdCfg<FAM, C, NS, TW>::THREADS, 2)
                     const uint32_t kb = smem_addr(smem + s * Cfg::STAGE);
                     const uint32_t vb = kb + Cfg::TILE;
                     const uint32_t lb = smem_addr(smem + Cfg::LO + (c & 1) * Cfg::TILE);
-                    // descriptors built once; 16 tokens (two 8-row groups, 2048 bytes) add 2048 >> 4
-                    const uint64_t dk = smem_desc_sw128(kb, Cfg::BOX, 1024), dv = smem_desc_sw128(vb, Cfg::BOX, 1024),
-                                   dl = smem_desc_sw128(lb, Cfg::BOX, 1024);
 #pragma unroll
                     for (int ks = 0; ks < C / 16; ++ks) {
-                        const uint64_t o = (uint64_t)(ks * 128);
-                        mma_f16(tmem, dk + o, dv + o, idesc, (j != p.jb || ks != 0) ? 1u : 0u);
-                        mma_f16(tmem, dl + o, dv + o, idesc, 1u);
+                        const uint32_t off = (uint32_t)ks * 2048u;   // 16 tokens = two 8-row groups
+                        const uint64_t bd = smem_desc_sw128(vb + off, Cfg::BOX, 1024);
+                        mma_f16(tmem, smem_desc_sw128(kb + off, Cfg::BOX, 1024), bd, idesc,
+                                (j != p.jb || ks != 0) ? 1u : 0u);
+                        mma_f16(tmem, smem_desc_sw128(lb + off, Cfg::BOX, 1024), bd, idesc, 1u);
                     }
                     mma_commit(&ctl->empty[s]);
                     mma_commit(&ctl->lofree[c & 1]);
