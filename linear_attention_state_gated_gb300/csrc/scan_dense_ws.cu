@@ -1165,7 +1165,9 @@ __global__ void __maxnreg__(80)
 //   [U^T ->] Delta^T = U^T - X0^T W^T (three-term split) | X^T += Delta~^T K,
 // so the halves' pipelines advance independently on one tensor pipe.
 // 19 warps: 0 TMA, 1 issuer for M, 2 issuer for S, 3-10 conversions for M,
-// 11-18 conversions for S.
+// 11-18 conversions for S.  A launch whose last wave would fill at most half the
+// SMs runs that wave's chains as single halves, one CTA each (the other half's
+// issuer and conversion warps stay idle), so the wave spreads over twice the SMs.
 
 constexpr int kPairThreads = 608;
 struct PairSmem {
